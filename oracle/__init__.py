@@ -1,0 +1,207 @@
+"""CPU oracle for the QLoRA NF4 + LoRA linear layer -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU baseline / reference
+arm may import this package.  The CUDA library never calls it and shares no code with it.
+
+The arithmetic lives in ``nf4_oracle.c`` (plain C loops, fp64 contractions); this module
+only marshals numpy arrays through ctypes.  Every function cites the passage of the QLoRA
+pages it follows in the C file's header (readings R1-R8).
+
+Pinning status: levels, quantize, double quantization, dequantize and the LoRA
+forward/backward are pinned by the not-gpu tests in ``tests/test_oracle_pins.py``
+(structural invariants, brute force on small inputs, closed forms, numpy matmul special
+cases and finite differences).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        i64, f64, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        L.nf4o_levels.argtypes = [vp, vp]
+        L.nf4o_levels.restype = None
+        L.nf4o_bf16_rne.argtypes = [ctypes.c_float]
+        L.nf4o_bf16_rne.restype = ctypes.c_uint16
+        L.nf4o_num_blocks.argtypes = [i64]
+        L.nf4o_num_blocks.restype = i64
+        L.nf4o_num_groups.argtypes = [i64]
+        L.nf4o_num_groups.restype = i64
+        L.nf4o_absmax_mean.argtypes = [vp, i64]
+        L.nf4o_absmax_mean.restype = ctypes.c_float
+        L.nf4o_block_absmax.argtypes = [vp, i64, vp]
+        L.nf4o_block_absmax.restype = None
+        L.nf4o_quantize.argtypes = [vp, i64, vp, vp, vp, vp, vp]
+        L.nf4o_quantize.restype = None
+        L.nf4o_dequantize.argtypes = [vp, vp, vp, ctypes.c_float, i64, vp]
+        L.nf4o_dequantize.restype = None
+        L.nf4o_lora_u_rows.argtypes = [vp, vp, i64, i64, vp, i64, vp]
+        L.nf4o_lora_u_rows.restype = None
+        L.nf4o_lora_fwd_rows.argtypes = [vp, vp, vp, vp, i64, i64, i64, f64, vp, i64, vp, vp]
+        L.nf4o_lora_fwd_rows.restype = None
+        L.nf4o_lora_v_rows.argtypes = [vp, vp, i64, i64, vp, i64, vp]
+        L.nf4o_lora_v_rows.restype = None
+        L.nf4o_lora_dx_rows.argtypes = [vp, vp, vp, vp, i64, i64, i64, f64, vp, i64, vp, vp]
+        L.nf4o_lora_dx_rows.restype = None
+        L.nf4o_lora_dadb.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f64, vp, vp]
+        L.nf4o_lora_dadb.restype = None
+        L.nf4o_num_threads.argtypes = []
+        L.nf4o_num_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, "bf16 inputs are passed as raw uint16 bits"
+    return a
+
+
+def num_threads() -> int:
+    return int(lib().nf4o_num_threads())
+
+
+def levels() -> tuple[np.ndarray, np.ndarray]:
+    """(L[16], T[15]) fp32: NF4 levels and decision thresholds (readings R1, R2)."""
+    L = np.zeros(16, np.float32)
+    T = np.zeros(15, np.float32)
+    lib().nf4o_levels(_p(L), _p(T))
+    return L, T
+
+
+def bf16_rne(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bits, round to nearest even, one element at a time through C."""
+    x = np.ascontiguousarray(x, np.float32).ravel()
+    f = lib().nf4o_bf16_rne
+    return np.array([f(float(v)) for v in x], np.uint16)
+
+
+def num_blocks(numel: int) -> int:
+    return int(lib().nf4o_num_blocks(numel))
+
+
+def num_groups(numel: int) -> int:
+    return int(lib().nf4o_num_groups(numel))
+
+
+def block_absmax(W: np.ndarray) -> np.ndarray:
+    W = np.ascontiguousarray(W, np.float32).ravel()
+    out = np.zeros(num_blocks(W.size), np.float32)
+    lib().nf4o_block_absmax(_p(W), W.size, _p(out))
+    return out
+
+
+def absmax_mean(absmax: np.ndarray) -> np.float32:
+    a = np.ascontiguousarray(absmax, np.float32)
+    return np.float32(lib().nf4o_absmax_mean(_p(a), a.size))
+
+
+def quantize(W: np.ndarray) -> dict:
+    """NF4 + double quantization of a fp32 tensor (flat order).  Returns a dict with
+    codes (uint8), qscale (int8), steps (fp32), mean (fp32 scalar), absmax (fp32)."""
+    W = np.ascontiguousarray(W, np.float32).ravel()
+    n = W.size
+    nb, ng = num_blocks(n), num_groups(n)
+    codes = np.zeros((n + 1) // 2, np.uint8)
+    qscale = np.zeros(nb, np.int8)
+    steps = np.zeros(ng, np.float32)
+    mean = np.zeros(1, np.float32)
+    absmax = np.zeros(nb, np.float32)
+    lib().nf4o_quantize(_p(W), n, _p(codes), _p(qscale), _p(steps), _p(mean), _p(absmax))
+    return {"codes": codes, "qscale": qscale, "steps": steps, "mean": mean[0],
+            "absmax": absmax, "numel": n}
+
+
+def dequantize(q: dict) -> np.ndarray:
+    """bf16 bits (uint16) of the dequantized weights, flat order (reading R7)."""
+    n = int(q["numel"])
+    out = np.zeros(n, np.uint16)
+    codes = np.ascontiguousarray(q["codes"], np.uint8)
+    qscale = np.ascontiguousarray(q["qscale"], np.int8)
+    steps = np.ascontiguousarray(q["steps"], np.float32)
+    lib().nf4o_dequantize(_p(codes), _p(qscale), _p(steps), float(q["mean"]), n, _p(out))
+    return out
+
+
+def _rows(rows, M):
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    return np.ascontiguousarray(rows, np.int64)
+
+
+def lora_u(X, A, rows=None):
+    """U[i] = X[rows[i]] A^T in fp64.  X [M,K], A [r,K] bf16 bits."""
+    X, A = _u16(X), _u16(A)
+    M, K = X.shape
+    r = A.shape[0]
+    rows = _rows(rows, M)
+    U = np.zeros((rows.size, r), np.float64)
+    lib().nf4o_lora_u_rows(_p(X), _p(A), K, r, _p(rows), rows.size, _p(U))
+    return U
+
+
+def lora_fwd(X, Wd, A, B, scale, rows=None):
+    """(Y, U) for the selected rows, fp64 (reading R8).  Wd [N,K] bf16 bits."""
+    X, Wd, A, B = _u16(X), _u16(Wd), _u16(A), _u16(B)
+    M, K = X.shape
+    N = Wd.shape[0]
+    r = A.shape[0]
+    rows = _rows(rows, M)
+    Y = np.zeros((rows.size, N), np.float64)
+    U = np.zeros((rows.size, r), np.float64)
+    lib().nf4o_lora_fwd_rows(_p(X), _p(Wd), _p(A), _p(B), N, K, r, float(scale),
+                             _p(rows), rows.size, _p(Y), _p(U))
+    return Y, U
+
+
+def lora_v(dY, B, rows=None):
+    dY, B = _u16(dY), _u16(B)
+    M, N = dY.shape
+    r = B.shape[1]
+    rows = _rows(rows, M)
+    V = np.zeros((rows.size, r), np.float64)
+    lib().nf4o_lora_v_rows(_p(dY), _p(B), N, r, _p(rows), rows.size, _p(V))
+    return V
+
+
+def lora_dx(dY, Wd, A, B, scale, rows=None):
+    """(dX, V) for the selected rows, fp64 (reading R8)."""
+    dY, Wd, A, B = _u16(dY), _u16(Wd), _u16(A), _u16(B)
+    M, N = dY.shape
+    K = Wd.shape[1]
+    r = A.shape[0]
+    rows = _rows(rows, M)
+    dX = np.zeros((rows.size, K), np.float64)
+    V = np.zeros((rows.size, r), np.float64)
+    lib().nf4o_lora_dx_rows(_p(dY), _p(Wd), _p(A), _p(B), N, K, r, float(scale),
+                            _p(rows), rows.size, _p(dX), _p(V))
+    return dX, V
+
+
+def lora_dadb(dY, X, A, B, scale):
+    """(dA [r,K], dB [N,r]) over all rows, fp64 (reading R8)."""
+    dY, X, A, B = _u16(dY), _u16(X), _u16(A), _u16(B)
+    M, N = dY.shape
+    K = X.shape[1]
+    r = A.shape[0]
+    dA = np.zeros((r, K), np.float64)
+    dB = np.zeros((N, r), np.float64)
+    lib().nf4o_lora_dadb(_p(dY), _p(X), _p(A), _p(B), M, N, K, r, float(scale),
+                         _p(dA), _p(dB))
+    return dA, dB

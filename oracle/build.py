@@ -1,0 +1,31 @@
+"""Compile the CPU oracle (plain C, OpenMP) into oracle/libnf4_oracle.so.
+
+Test infrastructure only: the test suite, the smoke check and the benchmark's CPU
+baseline load the result.  Run as ``python oracle/build.py``.
+"""
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "nf4_oracle.c")
+LIB = os.path.join(HERE, "libnf4_oracle.so")
+
+# -ffp-contract=off: every fp32 multiply/add is one IEEE operation (no fused contraction),
+# which the oracle's fp32 steps (normalisation, double quantization, dequantization) rely on.
+CFLAGS = ["-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+          "-fPIC", "-shared", "-Wall", "-Wextra"]
+
+
+def build(force: bool = False) -> str:
+    if (not force and os.path.exists(LIB)
+            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
+        return LIB
+    tmp = LIB + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, SRC, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv))

@@ -1,0 +1,393 @@
+"""Pins for the CPU oracle: checks against what the QLoRA pages and the mathematics fix,
+never against the oracle itself.  CPU only (not marked gpu).
+
+Pages cited: infivelines.com "QLoRA" (mechanism paragraphs), junaidshaukat.com
+"QLoRA -- the democratization event" (recipe), aicurriculum "QLoRA -- Module 12.4"
+(Design Details: NF4), addaly.com "QLoRA on one card" (What each setting is doing),
+digipro.cn "QLoRA: Fine-Tuning a 7B Model on a 16GB GPU".
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special as sp
+import torch
+
+import oracle
+from bit_nf4_quantized_37_b300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            key, val, tol, src = [p.strip() for p in line.split("|", 3)]
+            out[key] = (float(val), float(tol), src)
+    return out
+
+
+def _exact_nearest(x: np.ndarray, L: np.ndarray) -> np.ndarray:
+    """Brute force: index of the nearest level in exact fp64 arithmetic, ties -> lower."""
+    d = np.abs(x.astype(np.float64)[:, None] - L.astype(np.float64)[None, :])
+    return np.argmin(d, axis=1)  # argmin returns the first (lower) index on ties
+
+
+def _unpack(codes: np.ndarray, numel: int) -> np.ndarray:
+    c = np.stack([codes >> 4, codes & 0xF], axis=1).reshape(-1)
+    return c[:numel].astype(np.int64)
+
+
+# ---------------------------------------------------------------- levels (NF4 data type)
+
+def test_levels_structure():
+    """16 levels (4 bits), ascending, 0 exact, block absmax maps to -1 / +1."""
+    L, T = oracle.levels()
+    assert L.shape == (16,) and L.dtype == np.float32
+    assert np.all(np.diff(L) > 0)
+    assert L[0] == -1.0 and L[15] == 1.0 and L[7] == 0.0
+    assert (L > 0).sum() == 8 and (L < 0).sum() == 7
+
+
+def test_levels_sit_at_equally_spaced_normal_probabilities():
+    """infivelines 'QLoRA': NF4 places its 16 levels at quantiles of a normal
+    distribution.  Mapped back through the normal CDF (scipy ndtr, not the oracle's
+    quantile routine), the positive levels sit at equally spaced probabilities and so do
+    the negative ones."""
+    L, _ = oracle.levels()
+    delta = 0.5 * ((1 - 1 / 32) + (1 - 1 / 30))
+    zmax = sp.ndtri(delta)
+    p_pos = sp.ndtr(L[8:].astype(np.float64) * zmax)       # ascending
+    p_neg = sp.ndtr(-L[:7].astype(np.float64) * zmax)      # -L ascending magnitude reversed
+    dp = np.diff(p_pos)
+    assert np.allclose(dp, (delta - 0.5) / 8, rtol=2e-6, atol=0)
+    dn = np.diff(p_neg[::-1])
+    assert np.allclose(dn, (delta - 0.5) / 7, rtol=2e-6, atol=0)
+    # the construction through scipy's own quantile gives the same fp32 table
+    pos = sp.ndtri(np.linspace(delta, 0.5, 9)[:-1])
+    neg = -sp.ndtri(np.linspace(delta, 0.5, 8)[:-1])
+    v = np.sort(np.concatenate([pos, neg, [0.0]]))
+    assert np.array_equal((v / np.abs(v).max()).astype(np.float32), L)
+
+
+def test_nf4_levels_used_about_equally_and_beat_int4():
+    """infivelines 'QLoRA': each NF4 level is about equally likely on normal weights;
+    aicurriculum 'Design Details' and addaly 'What each setting is doing': NF4 keeps more
+    information than plain 4-bit integers.  Compare with a uniform 16-level grid."""
+    W = wl.weight((512, 1024), seed=7, sigma=0.02)
+    q = oracle.quantize(W)
+    c = _unpack(q["codes"], W.size)
+    h = np.bincount(c, minlength=16) / c.size
+    inner = h[1:15]
+    ent = -(h * np.log2(h)).sum()
+    L, _ = oracle.levels()
+    a = q["absmax"][:, None]
+    Wb = W.reshape(-1, 64)
+    nf4 = L[c].reshape(-1, 64) * a
+    grid = np.linspace(-1, 1, 16)
+    gi = np.abs((Wb / a)[..., None] - grid).argmin(-1)
+    hi = np.bincount(gi.ravel(), minlength=16) / gi.size
+    ent_int4 = -(hi * np.log2(hi)).sum()
+    assert inner.max() / inner.min() < 3.0
+    assert ent > 3.85 and ent > ent_int4 + 0.2
+    rmse_nf4 = np.sqrt(((nf4 - Wb) ** 2).mean())
+    rmse_int4 = np.sqrt(((grid[gi] * a - Wb) ** 2).mean())
+    assert rmse_nf4 < 0.95 * rmse_int4
+
+
+def test_thresholds_round_midpoints_down():
+    L, T = oracle.levels()
+    for i in range(15):
+        m = (Fraction(float(L[i])) + Fraction(float(L[i + 1]))) / 2
+        assert Fraction(float(T[i])) <= m
+        assert Fraction(float(np.nextafter(T[i], np.float32(2)))) > m
+
+
+# ---------------------------------------------------------------- quantize (blockwise absmax)
+
+def _blocks_with_unit_absmax(x: np.ndarray) -> np.ndarray:
+    """Blocks of 64 whose first entry is 1.0, so w / absmax == w exactly."""
+    n = len(x)
+    nb = -(-n // 63)
+    W = np.zeros((nb, 64), np.float32)
+    W[:, 0] = 1.0
+    flat = np.zeros(nb * 63, np.float32)
+    flat[:n] = x
+    W[:, 1:] = flat.reshape(nb, 63)
+    return W, n
+
+
+def _codes_of_unit_blocks(x):
+    W, n = _blocks_with_unit_absmax(x)
+    q = oracle.quantize(W)
+    c = _unpack(q["codes"], W.size).reshape(-1, 64)
+    assert np.all(c[:, 0] == 15)
+    return c[:, 1:].reshape(-1)[:n]
+
+
+def test_nearest_level_brute_force_around_every_midpoint():
+    """Every fp32 value within 3000 ulps of each midpoint, plus random values, gets the
+    exactly nearest level (ties to the lower index)."""
+    L, T = oracle.levels()
+    xs = []
+    for t in T:
+        base = np.float32(t).view(np.int32)
+        ints = base + np.arange(-3000, 3001, dtype=np.int64)  # both sides of the midpoint
+        xs.append(ints.astype(np.int32).view(np.float32))
+    g = wl.rng(11)
+    xs.append(g.uniform(-1, 1, size=200_000).astype(np.float32))
+    x = np.concatenate(xs)
+    x = x[(x >= -1) & (x <= 1)]
+    got = _codes_of_unit_blocks(x)
+    want = _exact_nearest(x, L)
+    assert np.array_equal(got, want)
+
+
+def test_exact_midpoint_ties_go_down():
+    L, T = oracle.levels()
+    ties = []
+    for i in range(15):
+        m = (np.float64(L[i]) + np.float64(L[i + 1])) / 2
+        if np.float64(np.float32(m)) == m:
+            ties.append((i, np.float32(m)))
+    for i, m in ties:
+        assert _codes_of_unit_blocks(np.array([m], np.float32))[0] == i
+
+
+def test_quantize_brute_force_small_ragged():
+    """Random weights with a ragged last block and odd length: codes equal the brute-force
+    nearest level of the fp32 quotient w / absmax (numpy's IEEE fp32 division)."""
+    L, _ = oracle.levels()
+    for n in (1, 63, 64, 65, 1001, 64 * 300 + 37):
+        W = wl.weight((n,), seed=100 + n, sigma=0.02)
+        q = oracle.quantize(W)
+        nb = -(-n // 64)
+        pad = np.zeros(nb * 64, np.float32)
+        pad[:n] = W
+        a = np.abs(pad.reshape(nb, 64)).max(1)
+        assert np.array_equal(q["absmax"], a)
+        x = (pad.reshape(nb, 64) / a[:, None]).astype(np.float32).reshape(-1)[:n]
+        want = _exact_nearest(x, L)
+        assert np.array_equal(_unpack(q["codes"], n), want)
+        if n % 2:
+            assert q["codes"][-1] & 0xF == 0
+
+
+def test_absmax_element_and_zero_block():
+    W = wl.weight((64 * 8,), seed=5, sigma=1.0).reshape(8, 64)
+    W[3] = 0.0
+    W[5, 17] = -abs(W[5]).max() * 2
+    q = oracle.quantize(W)
+    c = _unpack(q["codes"], W.size).reshape(8, 64)
+    for b in range(8):
+        if b == 3:
+            assert np.all(c[b] == 7)  # 0 is a level: an all-zero block is all code 7
+            continue
+        j = np.argmax(np.abs(W[b]))
+        assert c[b, j] == (15 if W[b, j] > 0 else 0)
+
+
+def test_requantize_is_idempotent():
+    """Quantizing the level-times-absmax reconstruction returns the same codes."""
+    L, _ = oracle.levels()
+    W = wl.weight((64 * 500,), seed=9, sigma=0.02)
+    q = oracle.quantize(W)
+    c = _unpack(q["codes"], W.size)
+    rec = (L[c].reshape(-1, 64) * q["absmax"][:, None]).astype(np.float32).reshape(-1)
+    q2 = oracle.quantize(rec)
+    assert np.array_equal(q2["codes"], q["codes"])
+
+
+# ---------------------------------------------------------------- double quantization
+
+def test_mean_equals_exact_rational_mean():
+    for n_blocks in (1, 7, 256, 1000, 5000):
+        a = np.abs(wl.weight((n_blocks,), seed=n_blocks, sigma=0.05)) + np.float32(1e-3)
+        exact = sum(Fraction(float(v)) for v in a) / n_blocks
+        mu = oracle.absmax_mean(a.astype(np.float32))
+        # the mean is rounded twice (fp64 then fp32); it must be one of the two fp32
+        # neighbours of the exact value and the nearest one unless exact is a near-tie
+        lo = np.float32(float(exact))
+        cands = {lo, np.nextafter(lo, np.float32(-1)), np.nextafter(lo, np.float32(1))}
+        assert mu in cands
+        assert abs(Fraction(float(mu)) - exact) <= abs(Fraction(float(np.float32(float(exact)))) - exact) + Fraction(1, 2**60)
+
+
+def test_double_quant_constant_group_has_zero_step():
+    W = np.zeros((256, 64), np.float32)
+    W[:, 5] = 0.125  # every block absmax == 0.125
+    q = oracle.quantize(W)
+    assert q["mean"] == np.float32(0.125)
+    assert q["steps"][0] == 0.0 and np.all(q["qscale"] == 0)
+
+
+def test_double_quant_two_value_group():
+    W = np.zeros((256, 64), np.float32)
+    W[:128, 0] = 0.25
+    W[128:, 0] = 0.75
+    q = oracle.quantize(W)
+    assert q["mean"] == np.float32(0.5)
+    assert q["steps"][0] == np.float32(np.float32(0.25) / np.float32(127))
+    assert np.all(q["qscale"][:128] == -127) and np.all(q["qscale"][128:] == 127)
+
+
+def test_double_quant_error_bound_and_range():
+    """|ahat - a| <= step/2 (plus fp32 rounding); codes in [-127, 127]; the block with the
+    largest |a - mu| in each group gets |q| = 127."""
+    W = wl.weight((64 * 256 * 5 + 64 * 3 + 11,), seed=21, sigma=0.02, outlier_frac=0.001)
+    q = oracle.quantize(W)
+    a, qs, st, mu = q["absmax"], q["qscale"].astype(np.int64), q["steps"], q["mean"]
+    g = np.arange(a.size) // 256
+    # q * step is exact in fp64 (8-bit times 24-bit significands)
+    ahat = (qs.astype(np.float64) * st[g].astype(np.float64) + np.float64(mu)).astype(np.float32)
+    err = np.abs(ahat.astype(np.float64) - a.astype(np.float64))
+    tol = st[g].astype(np.float64) * (0.5 + 1e-5) + 4 * np.spacing(np.abs(a)).astype(np.float64)
+    assert np.all(err <= tol)
+    assert qs.min() >= -127 and qs.max() <= 127
+    for gi in range(st.size):
+        sel = g == gi
+        d = np.abs(a[sel].astype(np.float64) - np.float64(mu))
+        assert np.abs(qs[sel][np.argmax(d)]) == 127
+
+
+# ---------------------------------------------------------------- dequantize
+
+def test_bf16_rne_matches_torch_conversion():
+    g = wl.rng(3)
+    x = np.concatenate([g.standard_normal(20000).astype(np.float32),
+                        np.array([0.0, -0.0, 1.0, -1.0, 3.4e38, 1e-40, -1e-40], np.float32),
+                        (np.arange(1, 3000, dtype=np.uint32) * 0x8000 + 0x3F800000).view(np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.bf16_rne(x), want)
+
+
+def test_dequant_error_bound_and_values():
+    """Dequantized weights stay within half the largest level gap times the block scale,
+    plus the second-level and bf16 rounding errors (infivelines: each block of 64 weights
+    carries its own scale, quantized again in blocks of 256)."""
+    L, _ = oracle.levels()
+    W = wl.weight((300, 512), seed=31, sigma=0.02, outlier_frac=0.001)
+    q = oracle.quantize(W)
+    wd = wl.bf16_bits_to_f32(oracle.dequantize(q)).astype(np.float64)
+    n = W.size
+    b = np.arange(n) // 64
+    g = b // 256
+    a = q["absmax"][b].astype(np.float64)
+    ahat = (q["qscale"][b].astype(np.float64) * q["steps"][g] + np.float64(q["mean"]))
+    gap = np.diff(L.astype(np.float64)).max() / 2
+    bound = gap * a + np.abs(ahat - a) + np.abs(wd) * 2.0 ** -8 + 1e-12
+    assert np.all(np.abs(wd - W.reshape(-1).astype(np.float64)) <= bound)
+    # level times recovered scale, rounded to bf16 by torch (a library conversion)
+    c = _unpack(q["codes"], n)
+    ahat32 = np.array([np.float32(np.float64(qq) * np.float64(s) + np.float64(q["mean"]))
+                       for qq, s in zip(q["qscale"][b[::997]], q["steps"][g[::997]])], np.float32)
+    prod = (L[c[::997]] * ahat32).astype(np.float32)
+    want = torch.from_numpy(prod).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.dequantize(q)[::997], want)
+
+
+# ---------------------------------------------------------------- storage accounting
+
+def test_storage_matches_the_pages():
+    gold = _golden("storage_accounting.txt")
+    numel = 4096 * 11008
+    q = oracle.quantize(np.zeros(64 * 256 * 2, np.float32))  # shapes only
+    assert q["codes"].size == 64 * 256 and q["qscale"].size == 512 and q["steps"].size == 2
+    nb, ng = -(-numel // 64), -(-numel // (64 * 256))
+    meta_bits = (8 * nb + 32 * ng) / numel
+    v, tol, _ = gold["metadata_bits_per_weight"]
+    assert abs(meta_bits - v) <= tol * v
+    assert meta_bits == pytest.approx(8 / 64 + 32 / (64 * 256), rel=1e-12)
+    assert gold["storage_shrink_vs_16bit"][0] == 16 / 4
+    for size, k16, k4 in ((7e9, "base_7b_16bit_gb", "base_7b_4bit_gb"),
+                          (70e9, "base_70b_16bit_gb", "base_70b_4bit_gb")):
+        assert 2 * size / 1e9 == gold[k16][0]
+        assert 0.5 * size / 1e9 == gold[k4][0]
+    saving = (32 / 64 - meta_bits) * 7e9 / 8 / 1e9  # fp32 absmax per block vs double quant
+    assert gold["double_quant_saving_7b_gb_min"][0] < saving < gold["double_quant_saving_7b_gb_max"][0]
+
+
+# ---------------------------------------------------------------- LoRA forward / backward
+
+def _f(bits):
+    return wl.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+@pytest.fixture(scope="module")
+def small():
+    p = wl.config1()
+    W = p.W()
+    q = oracle.quantize(W)
+    Wd = oracle.dequantize(q).reshape(p.N, p.K)
+    return p, Wd, p.X(), p.A(), p.B(), p.dY()
+
+
+def test_forward_matches_numpy_matmul(small):
+    p, Wd, X, A, B, dY = small
+    Y, U = oracle.lora_fwd(X, Wd, A, B, p.scale)
+    Uref = _f(X) @ _f(A).T
+    Yref = _f(X) @ _f(Wd).T + p.scale * (Uref @ _f(B).T)
+    assert np.allclose(U, Uref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(Y, Yref, rtol=1e-12, atol=1e-12)
+    rows = np.array([3, 0, 15], np.int64)
+    Ys, _ = oracle.lora_fwd(X, Wd, A, B, p.scale, rows)
+    assert np.array_equal(Ys, Y[rows])
+
+
+def test_zero_b_reduces_to_base_matmul(small):
+    p, Wd, X, A, B, dY = small
+    B0 = np.zeros_like(B)
+    Y, _ = oracle.lora_fwd(X, Wd, A, B0, p.scale)
+    assert np.allclose(Y, _f(X) @ _f(Wd).T, rtol=1e-12, atol=1e-12)
+    dA, dB = oracle.lora_dadb(dY, X, A, B0, p.scale)
+    assert np.all(dA == 0.0)
+    A0 = np.zeros_like(A)
+    dA, dB = oracle.lora_dadb(dY, X, A0, B, p.scale)
+    assert np.all(dB == 0.0)
+
+
+def test_backward_is_adjoint_of_forward(small):
+    """<dY, Y> pairs with the gradients: Y is linear in X, in A and in B separately, so
+    <dY, dY/dX-direction> identities pin every transpose and index of the backward."""
+    p, Wd, X, A, B, dY = small
+    s = p.scale
+    g = _f(dY)
+    Y, _ = oracle.lora_fwd(X, Wd, A, B, s)
+    dX, V = oracle.lora_dx(dY, Wd, A, B, s)
+    dA, dB = oracle.lora_dadb(dY, X, A, B, s)
+    lhs = (g * Y).sum()
+    assert lhs == pytest.approx((dX * _f(X)).sum(), rel=1e-10)
+    Y_noA, _ = oracle.lora_fwd(X, Wd, np.zeros_like(A), B, s)
+    lora = (g * (Y - Y_noA)).sum()
+    assert lora == pytest.approx((dA * _f(A)).sum(), rel=1e-9)
+    assert lora == pytest.approx((dB * _f(B)).sum(), rel=1e-9)
+    assert np.allclose(V, g @ _f(B), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dX, g @ _f(Wd) + s * (g @ _f(B)) @ _f(A), rtol=1e-12, atol=1e-12)
+
+
+def test_backward_finite_difference(small):
+    """Central differences of L = <dY, Y> in fp64 along random directions."""
+    p, Wd, X, A, B, dY = small
+    s = p.scale
+    g = _f(dY)
+    Xf, Af, Bf, Wf = _f(X), _f(A), _f(B), _f(Wd)
+
+    def loss(Xv, Av, Bv):
+        return (g * (Xv @ Wf.T + s * (Xv @ Av.T) @ Bv.T)).sum()
+
+    dX, _ = oracle.lora_dx(dY, Wd, A, B, s)
+    dA, dB = oracle.lora_dadb(dY, X, A, B, s)
+    r = wl.rng(77)
+    for grad, which in ((dX, 0), (dA, 1), (dB, 2)):
+        D = r.standard_normal(grad.shape)
+        h = 1e-3
+        args_p = [Xf, Af, Bf]
+        args_m = [Xf, Af, Bf]
+        args_p[which] = args_p[which] + h * D
+        args_m[which] = args_m[which] - h * D
+        fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert fd == pytest.approx((grad * D).sum(), rel=1e-6)
