@@ -1,0 +1,32 @@
+"""QLoRA NF4 + LoRA linear layer on B300 (sm_103a): thin Python binding of the C ABI.
+
+The entry points have the names of the C ABI in ``include/qlora_nf4.h``:
+``nf4_quantize``, ``nf4_dequantize``, ``qlora_linear_fwd``, ``qlora_linear_bwd`` (plus the
+size/utility calls).  This module only marshals torch tensors (device memory and the
+current stream) into raw pointers; every step of the computation runs in the CUDA library
+``libqlora_nf4.so``.  There is no CPU fallback: without the library or a compute-capability
+10.3 GPU the calls raise.
+"""
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    NF4Tensor,
+    QLoRAError,
+    device_status,
+    level_table,
+    lib,
+    nf4_dequantize,
+    nf4_quantize,
+    nf4_quantize_workspace_bytes,
+    nf4_storage_bytes,
+    qlora_linear_bwd,
+    qlora_linear_fwd,
+    qlora_workspace_bytes,
+    status_str,
+)
+
+__all__ = [
+    "NF4Tensor", "QLoRAError", "device_status", "level_table", "lib", "nf4_dequantize",
+    "nf4_quantize", "nf4_quantize_workspace_bytes", "nf4_storage_bytes", "qlora_linear_bwd",
+    "qlora_linear_fwd", "qlora_workspace_bytes", "status_str",
+]

@@ -1,0 +1,249 @@
+"""ctypes binding of libqlora_nf4.so (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqlora_nf4.so")
+
+NF4_BLOCKSIZE = 64
+NF4_DQ_BLOCK = 256
+
+_STATUS = {0: "QLORA_OK", -1: "QLORA_ERR_INVALID_ARG", -2: "QLORA_ERR_UNSUPPORTED",
+           -3: "QLORA_ERR_MISALIGNED", -4: "QLORA_ERR_WORKSPACE", -5: "QLORA_ERR_CUDA",
+           -6: "QLORA_ERR_DEVICE_TIMEOUT", -7: "QLORA_ERR_NO_DEVICE"}
+
+# Every symbol include/qlora_nf4.h declares.
+EXPORTS = ["nf4_storage_bytes", "nf4_quantize_workspace_bytes", "nf4_quantize",
+           "nf4_dequantize", "qlora_workspace_bytes", "qlora_linear_fwd", "qlora_linear_bwd",
+           "nf4_level_table", "qlora_device_status", "qlora_status_str", "qlora_version"]
+
+
+class QLoRAError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        self.status = status
+        super().__init__(f"{call} failed: {_STATUS.get(status, status)} "
+                         f"({status_str(status) if _lib is not None else ''})")
+
+
+class _NF4Struct(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scale_codes", ctypes.c_void_p),
+                ("scale_steps", ctypes.c_void_p), ("scale_mean", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("blocksize", ctypes.c_int32), ("dq_block", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m bit_nf4_quantized_37_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, u64p = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        sp = ctypes.POINTER(_NF4Struct)
+        sig = {
+            "nf4_storage_bytes": [i64, i64, i32, i32, u64p, u64p],
+            "nf4_quantize_workspace_bytes": [i64, u64p],
+            "nf4_quantize": [vp, sp, vp, ctypes.c_uint64, vp],
+            "nf4_dequantize": [sp, vp, vp],
+            "qlora_workspace_bytes": [i64, i64, i64, i32, u64p],
+            "qlora_linear_fwd": [vp, i64, sp, vp, vp, i32, ctypes.c_float, vp, vp, vp,
+                                 ctypes.c_uint64, vp],
+            "qlora_linear_bwd": [vp, vp, i64, sp, vp, vp, i32, ctypes.c_float, vp, vp, vp, vp,
+                                 vp, ctypes.c_uint64, vp],
+            "nf4_level_table": [vp, vp],
+            "qlora_device_status": [vp, vp],
+            "qlora_status_str": [ctypes.c_int],
+            "qlora_version": [],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_char_p if name == "qlora_status_str" else ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().qlora_status_str(int(status)).decode()
+
+
+def _check(call: str, status: int):
+    if status != 0:
+        raise QLoRAError(call, status)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream() -> int:
+    return int(torch.cuda.current_stream().cuda_stream)
+
+
+def _u64() -> ctypes.c_uint64:
+    return ctypes.c_uint64(0)
+
+
+# ------------------------------------------------------------------------- NF4 tensor
+@dataclass
+class NF4Tensor:
+    """Blockwise NF4 weights with double-quantized scales (device tensors)."""
+    codes: torch.Tensor        # uint8 [ceil(numel/2)]
+    scale_codes: torch.Tensor  # int8  [ceil(numel/64)]
+    scale_steps: torch.Tensor  # fp32  [ceil(numel/16384)]
+    scale_mean: torch.Tensor   # fp32  [1]
+    rows: int
+    cols: int
+
+    @property
+    def numel(self) -> int:
+        return self.rows * self.cols
+
+    def c_struct(self) -> _NF4Struct:
+        return _NF4Struct(_ptr(self.codes), _ptr(self.scale_codes), _ptr(self.scale_steps),
+                          _ptr(self.scale_mean), self.rows, self.cols, NF4_BLOCKSIZE,
+                          NF4_DQ_BLOCK)
+
+    def storage_bytes(self) -> int:
+        return nf4_storage_bytes(self.rows, self.cols)[1]
+
+    @staticmethod
+    def empty(rows: int, cols: int, device) -> "NF4Tensor":
+        sizes, _ = nf4_storage_bytes(rows, cols)
+        return NF4Tensor(torch.empty(sizes[0], dtype=torch.uint8, device=device),
+                         torch.empty(sizes[1], dtype=torch.int8, device=device),
+                         torch.empty(sizes[2] // 4, dtype=torch.float32, device=device),
+                         torch.empty(1, dtype=torch.float32, device=device), rows, cols)
+
+
+def nf4_storage_bytes(rows: int, cols: int) -> tuple[list[int], int]:
+    sizes = (ctypes.c_uint64 * 4)()
+    total = _u64()
+    _check("nf4_storage_bytes", lib().nf4_storage_bytes(rows, cols, NF4_BLOCKSIZE, NF4_DQ_BLOCK,
+                                                         sizes, ctypes.byref(total)))
+    return [int(s) for s in sizes], int(total.value)
+
+
+def nf4_quantize_workspace_bytes(numel: int) -> int:
+    out = _u64()
+    _check("nf4_quantize_workspace_bytes", lib().nf4_quantize_workspace_bytes(numel, ctypes.byref(out)))
+    return int(out.value)
+
+
+def qlora_workspace_bytes(M: int, N: int, K: int, r: int) -> int:
+    out = _u64()
+    _check("qlora_workspace_bytes", lib().qlora_workspace_bytes(M, N, K, r, ctypes.byref(out)))
+    return int(out.value)
+
+
+def level_table():
+    L = (ctypes.c_float * 16)()
+    T = (ctypes.c_float * 15)()
+    _check("nf4_level_table", lib().nf4_level_table(L, T))
+    return list(L), list(T)
+
+
+# Workspaces are caller-owned device memory; the binding keeps one growing buffer per device.
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _req(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def nf4_quantize(W: torch.Tensor, out: NF4Tensor | None = None,
+                 workspace: torch.Tensor | None = None) -> NF4Tensor:
+    """Quantize fp32 weights [rows, cols] (CUDA) to NF4 with double-quantized scales."""
+    _req(W, torch.float32, "W")
+    rows, cols = (W.shape[0], W.shape[1]) if W.dim() == 2 else (1, W.numel())
+    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device)
+    nb = nf4_quantize_workspace_bytes(rows * cols)
+    ws = workspace if workspace is not None else _workspace(nb, W.device)
+    s = q.c_struct()
+    _check("nf4_quantize", lib().nf4_quantize(_ptr(W), ctypes.byref(s), _ptr(ws),
+                                              ws.numel() * ws.element_size(), _stream()))
+    return q
+
+
+def nf4_dequantize(q: NF4Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """bf16 [rows, cols] dequantization of an NF4Tensor."""
+    o = out if out is not None else torch.empty(q.rows, q.cols, dtype=torch.bfloat16,
+                                                device=q.codes.device)
+    s = q.c_struct()
+    _check("nf4_dequantize", lib().nf4_dequantize(ctypes.byref(s), _ptr(o), _stream()))
+    return o
+
+
+def qlora_linear_fwd(X: torch.Tensor, q: NF4Tensor, A: torch.Tensor, B: torch.Tensor,
+                     scale: float, save_u: bool = True, out: torch.Tensor | None = None):
+    """Y = X W'^T + scale (X A^T) B^T.  Returns (Y bf16 [M, N], U fp32 [M, r] or None)."""
+    for t, n in ((X, "X"), (A, "A"), (B, "B")):
+        _req(t, torch.bfloat16, n)
+    M, K = X.shape
+    r = A.shape[0]
+    N = q.rows
+    Y = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=X.device)
+    U = torch.empty(M, r, dtype=torch.float32, device=X.device) if save_u else None
+    nb = qlora_workspace_bytes(M, N, K, r)
+    ws = _workspace(nb, X.device)
+    s = q.c_struct()
+    _check("qlora_linear_fwd", lib().qlora_linear_fwd(
+        _ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(Y), _ptr(U),
+        _ptr(ws), ws.numel(), _stream()))
+    return Y, U
+
+
+def qlora_linear_bwd(dY: torch.Tensor, X: torch.Tensor, q: NF4Tensor, A: torch.Tensor,
+                     B: torch.Tensor, scale: float, U: torch.Tensor | None = None,
+                     need_dx: bool = True):
+    """Returns (dX bf16 [M, K] or None, dA fp32 [r, K], dB fp32 [N, r]); the base is frozen."""
+    for t, n in ((dY, "dY"), (X, "X"), (A, "A"), (B, "B")):
+        _req(t, torch.bfloat16, n)
+    if U is not None:
+        _req(U, torch.float32, "U")
+    M, K = X.shape
+    r = A.shape[0]
+    N = q.rows
+    dX = torch.empty(M, K, dtype=torch.bfloat16, device=X.device) if need_dx else None
+    dA = torch.empty(r, K, dtype=torch.float32, device=X.device)
+    dB = torch.empty(N, r, dtype=torch.float32, device=X.device)
+    nb = qlora_workspace_bytes(M, N, K, r)
+    ws = _workspace(nb, X.device)
+    s = q.c_struct()
+    _check("qlora_linear_bwd", lib().qlora_linear_bwd(
+        _ptr(dY), _ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(U),
+        _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), ws.numel(), _stream()))
+    return dX, dA, dB
+
+
+def device_status() -> int:
+    """Synchronizes the current stream; returns the kernels' bounded-wait error word."""
+    out = ctypes.c_int32(0)
+    st = lib().qlora_device_status(ctypes.byref(out), _stream())
+    if st not in (0, -6):
+        raise QLoRAError("qlora_device_status", st)
+    return int(out.value)

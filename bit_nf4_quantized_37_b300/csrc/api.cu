@@ -1,0 +1,175 @@
+// api.cu -- the C ABI (include/qlora_nf4.h): host-side validation, then launches.
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+#include "linear.h"
+#include "nf4_device.cuh"
+
+using namespace qlora;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QLORA_ERR_NO_DEVICE;
+  static thread_local int cached_dev = -1, cached_ok = 0;
+  if (dev != cached_dev) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return QLORA_ERR_NO_DEVICE;
+    cached_dev = dev;
+    cached_ok = (major == 10 && minor == 3);
+  }
+  return cached_ok ? QLORA_OK : QLORA_ERR_NO_DEVICE;
+}
+
+int check_tensor(const nf4_tensor* q) {
+  if (!q) return QLORA_ERR_INVALID_ARG;
+  if (q->rows < 1 || q->cols < 1) return QLORA_ERR_INVALID_ARG;
+  if (q->blocksize != NF4_BLOCKSIZE || q->dq_block != NF4_DQ_BLOCK) return QLORA_ERR_UNSUPPORTED;
+  if (!q->codes || !q->scale_codes || !q->scale_steps || !q->scale_mean)
+    return QLORA_ERR_INVALID_ARG;
+  if (!aligned16(q->codes) || !aligned16(q->scale_codes) || !aligned16(q->scale_steps) ||
+      !aligned16(q->scale_mean))
+    return QLORA_ERR_MISALIGNED;
+  return QLORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qlora_version(void) { return 10000; }
+
+const char* qlora_status_str(int status) {
+  switch (status) {
+    case QLORA_OK: return "ok";
+    case QLORA_ERR_INVALID_ARG: return "invalid argument";
+    case QLORA_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case QLORA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case QLORA_ERR_WORKSPACE: return "workspace too small";
+    case QLORA_ERR_CUDA: return "CUDA runtime or launch error";
+    case QLORA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    case QLORA_ERR_NO_DEVICE: return "current device is not compute capability 10.3";
+    default: return "unknown status";
+  }
+}
+
+int nf4_level_table(float levels[16], float thresholds[15]) {
+  static const float L[16] = QLORA_NF4_LEVELS;
+  static const float T[15] = QLORA_NF4_THRESHOLDS;
+  if (levels) std::memcpy(levels, L, sizeof(L));
+  if (thresholds) std::memcpy(thresholds, T, sizeof(T));
+  return QLORA_OK;
+}
+
+int nf4_storage_bytes(int64_t rows, int64_t cols, int32_t blocksize, int32_t dq_block,
+                      uint64_t sizes[4], uint64_t* total) {
+  if (rows < 1 || cols < 1) return QLORA_ERR_INVALID_ARG;
+  if (blocksize != NF4_BLOCKSIZE || dq_block != NF4_DQ_BLOCK) return QLORA_ERR_UNSUPPORTED;
+  const uint64_t numel = (uint64_t)rows * (uint64_t)cols;
+  const uint64_t nb = (numel + NF4_BLOCKSIZE - 1) / NF4_BLOCKSIZE;
+  const uint64_t ng = (nb + NF4_DQ_BLOCK - 1) / NF4_DQ_BLOCK;
+  const uint64_t s[4] = {(numel + 1) / 2, nb, ng * 4, 4};
+  if (sizes) std::memcpy(sizes, s, sizeof(s));
+  if (total) *total = s[0] + s[1] + s[2] + s[3];
+  return QLORA_OK;
+}
+
+int nf4_quantize_workspace_bytes(int64_t numel, uint64_t* out) {
+  if (numel < 1 || !out) return QLORA_ERR_INVALID_ARG;
+  *out = quantize_workspace_bytes(numel);
+  return QLORA_OK;
+}
+
+int nf4_quantize(const float* W, const nf4_tensor* out, void* workspace,
+                 uint64_t workspace_bytes, void* stream) {
+  int st = check_tensor(out);
+  if (st) return st;
+  if (!W || !workspace) return QLORA_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(workspace)) return QLORA_ERR_MISALIGNED;
+  const int64_t numel = out->rows * out->cols;
+  if (workspace_bytes < quantize_workspace_bytes(numel)) return QLORA_ERR_WORKSPACE;
+  if ((st = check_device())) return st;
+  return launch_quantize(W, numel, *out, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int nf4_dequantize(const nf4_tensor* q, uint16_t* W_out, void* stream) {
+  int st = check_tensor(q);
+  if (st) return st;
+  if (!W_out) return QLORA_ERR_INVALID_ARG;
+  if (!aligned16(W_out)) return QLORA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+  return launch_dequantize(*q, q->rows * q->cols, W_out, static_cast<cudaStream_t>(stream));
+}
+
+int qlora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r, uint64_t* out) {
+  if (M < 1 || N < 1 || K < 1 || r < 1 || !out) return QLORA_ERR_INVALID_ARG;
+  if (r > kMaxRank) return QLORA_ERR_UNSUPPORTED;
+  *out = linear_workspace_bytes(M, N, K, r);
+  return QLORA_OK;
+}
+
+int qlora_linear_fwd(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const uint16_t* A,
+                     const uint16_t* B, int32_t r, float scale, uint16_t* Y, float* U_save,
+                     void* ws, uint64_t ws_bytes, void* stream) {
+  int st = check_tensor(Wq);
+  if (st) return st;
+  if (!X || !A || !B || !Y || !ws || M < 1 || r < 1) return QLORA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return QLORA_ERR_INVALID_ARG;
+  if (r > kMaxRank) return QLORA_ERR_UNSUPPORTED;
+  const int64_t N = Wq->rows, K = Wq->cols;
+  if (N % 64 != 0 || K % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(Y) || !aligned16(ws) ||
+      (U_save && !aligned16(U_save)))
+    return QLORA_ERR_MISALIGNED;
+  if (ws_bytes < linear_workspace_bytes(M, N, K, r)) return QLORA_ERR_WORKSPACE;
+  if ((st = check_device())) return st;
+  LinearArgs a{};
+  a.M = M; a.N = N; a.K = K; a.r = r; a.scale = scale;
+  a.X = X; a.A = A; a.B = B; a.Y = Y; a.U = U_save; a.q = *Wq;
+  a.ws = ws; a.ws_bytes = ws_bytes;
+  return linear_forward(a, static_cast<cudaStream_t>(stream));
+}
+
+int qlora_linear_bwd(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                     const uint16_t* A, const uint16_t* B, int32_t r, float scale,
+                     const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,
+                     uint64_t ws_bytes, void* stream) {
+  int st = check_tensor(Wq);
+  if (st) return st;
+  if (!dY || !X || !A || !B || !dA || !dB || !ws || M < 1 || r < 1) return QLORA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return QLORA_ERR_INVALID_ARG;
+  if (r > kMaxRank) return QLORA_ERR_UNSUPPORTED;
+  const int64_t N = Wq->rows, K = Wq->cols;
+  if (N % 64 != 0 || K % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (!aligned16(dY) || !aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(dA) ||
+      !aligned16(dB) || !aligned16(ws) || (dX && !aligned16(dX)) ||
+      (U_saved && !aligned16(U_saved)))
+    return QLORA_ERR_MISALIGNED;
+  if (ws_bytes < linear_workspace_bytes(M, N, K, r)) return QLORA_ERR_WORKSPACE;
+  if ((st = check_device())) return st;
+  LinearArgs a{};
+  a.M = M; a.N = N; a.K = K; a.r = r; a.scale = scale;
+  a.X = X; a.A = A; a.B = B; a.dY = dY; a.dX = dX; a.dA = dA; a.dB = dB;
+  a.U_in = U_saved; a.q = *Wq; a.ws = ws; a.ws_bytes = ws_bytes;
+  return linear_backward(a, static_cast<cudaStream_t>(stream));
+}
+
+int qlora_device_status(int32_t* out, void* stream) {
+  if (!out) return QLORA_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return QLORA_ERR_CUDA;
+  if ((st = read_and_clear_gemm_error(&v))) return st;
+  *out = v;
+  return v ? QLORA_ERR_DEVICE_TIMEOUT : QLORA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// launch.h -- host-side declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qlora_nf4.h"
+
+namespace qlora {
+
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms();
+
+// Reads and clears the fused GEMMs' device error word (umma_gemm.cu).
+int read_and_clear_gemm_error(int* out);
+
+// Quantize / dequantize (nf4_codec.cu).
+uint64_t quantize_workspace_bytes(int64_t numel);
+int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws,
+                    cudaStream_t stream);
+int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, cudaStream_t stream);
+
+// 2-D tiled tensor map over a row-major matrix (tensormap.cu).  `inner` is the contiguous
+// extent in elements, `outer` the row count, `row_bytes` the row pitch; the box is
+// box_inner x box_outer elements.  Returns false when the driver rejects the map.
+enum class MapSwizzle { None, B32, B64, B128 };
+bool make_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                        int elem_bytes, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_outer, MapSwizzle sw);
+
+}  // namespace qlora

@@ -1,0 +1,75 @@
+// linear.h -- the LoRA-wrapped NF4 linear layer: argument bundle, workspace layout, and the
+// forward / backward orchestration entry points (linear.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qlora_nf4.h"
+
+namespace qlora {
+
+constexpr int kMaxRank = 128;
+constexpr int64_t kSkinnyMaxM = 16;  // M at or below this takes the decode kernel
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+struct LinearArgs {
+  int64_t M, N, K;
+  int r;
+  float scale;
+  nf4_tensor q;
+  const uint16_t* X;
+  const uint16_t* A;
+  const uint16_t* B;
+  uint16_t* Y;
+  float* U;             // forward: optional fp32 U output
+  const float* U_in;    // backward: optional saved U
+  const uint16_t* dY;
+  uint16_t* dX;
+  float* dA;
+  float* dB;
+  void* ws;
+  uint64_t ws_bytes;
+};
+
+// Workspace regions (byte offsets, each 1024-aligned), for rank padded to rp = 64*ceil(r/64).
+struct WorkspaceLayout {
+  int64_t rp;
+  uint64_t sU;      // bf16 [M, rp]   scale * U, zero columns past r
+  uint64_t sV;      // bf16 [M, rp]   scale * V
+  uint64_t Ut;      // bf16 [rp, Mp]  U transposed (Mp = M rounded up to 64)
+  uint64_t Vt;      // bf16 [rp, Mp]  V transposed
+  uint64_t Bp;      // bf16 [N, rp]   B zero-padded
+  uint64_t Bt;      // bf16 [rp, N]   B transposed, zero rows past r
+  uint64_t Ap;      // bf16 [rp, K]   A zero-padded rows
+  uint64_t part;    // fp32 split-contraction partial sums (side products and decode path)
+  uint64_t part_bytes;
+  uint64_t total;
+};
+
+WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r);
+uint64_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int r);
+
+int linear_forward(const LinearArgs& a, cudaStream_t stream);
+int linear_backward(const LinearArgs& a, cudaStream_t stream);
+
+// ---- kernels behind the orchestration (umma_gemm.cu, lora_side.cu, skinny.cu)
+// Fused tcgen05 GEMMs.  Forward: Y = [X | sU] [W' | Bp]^T.  Input gradient:
+// dX = [dY | sV] [W' ; Ap].  W' is dequantized inside the kernel.
+int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+// Decode path (M <= 16): Y = X W'^T + sU Bp^T with the weights streamed once.
+int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+// Rank-r side products on the tensor cores (mma.sync), split over the contraction.
+int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+int launch_lora_db(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+int launch_lora_da(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+int launch_pad_adapters(const LinearArgs& a, const WorkspaceLayout& L, bool need_bt,
+                        cudaStream_t stream);
+int launch_u_from_saved(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+uint64_t side_partial_bytes(int64_t M, int64_t N, int64_t K, int r);
+uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K);
+
+}  // namespace qlora

@@ -1,0 +1,381 @@
+// umma_gemm.cu -- the fused NF4 + LoRA GEMMs on the 5th-generation tensor cores.
+//
+// infivelines.com "QLoRA": the base is dequantized to bf16 one block at a time inside the
+// matrix multiply; addaly.com "QLoRA on one card": dequantized on the fly for each matrix
+// multiply.  Here that "inside" is literal: warps expand the packed 4-bit codes of each
+// 64-wide k-slice straight into the shared-memory operand tile of tcgen05.mma, so W' never
+// exists in HBM.  The rank-r LoRA term rides in the same TMEM accumulator as extra
+// contraction stages in front of the NF4 stages:
+//   forward          Y  = [X  | sU] . [W' | Bp]^T      (contract over K, then over r)
+//   input gradient   dX = [dY | sV] . [W' ; Ap]        (contract over N, then over r)
+//
+// CTA tile 128 x 256 (UMMA M x N), k-slice 64, 4-stage ring.  Warp roles (384 threads):
+//   warp 0      TMA producer: X/dY tiles, and for the LoRA stages both operands
+//   warp 1      TMEM owner + single-thread UMMA issuer
+//   warps 4-11  NF4 producers (one 64-weight block per thread per stage: codes and block
+//               scale from global memory two stages ahead, byte-permute dequantization into
+//               the swizzled operand layout), then the epilogue (TMEM -> bf16 -> TMA store)
+// Every wait is bounded; on a time-out the CTA records the site and unwinds.
+#include "common.cuh"
+#include "launch.h"
+#include "linear.h"
+#include "nf4_device.cuh"
+
+namespace qlora {
+
+// Device error word of the fused GEMMs (bounded waits that gave up).
+__device__ int g_gemm_error = 0;
+
+int read_and_clear_gemm_error(int* out) {
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(int)) != cudaSuccess) return QLORA_ERR_CUDA;
+  if (v && cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(int)) != cudaSuccess) return QLORA_ERR_CUDA;
+  *out = v;
+  return QLORA_OK;
+}
+
+namespace fused {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 384;
+constexpr int DEQ_WARP0 = 4;
+constexpr int NUM_DEQ_WARPS = 8;
+constexpr int TMEM_COLS = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+
+struct Params {
+  int64_t M;      // output rows (tokens)
+  int64_t Nout;   // output columns
+  int64_t Kc;     // NF4 contraction length (forward: K, input gradient: N)
+  int64_t Kw;     // columns of W (K)
+  int64_t Nw;     // rows of W (N)
+  int n_lora;     // LoRA stages in front of the NF4 stages
+  int lora_last_k16;
+  const uint8_t* codes;
+  const int8_t* qs;
+  const float* steps;
+  const float* mean;
+};
+
+// One thread's share of an NF4 stage: 64 codes (32 bytes) and the block's scale code/step.
+struct Slice {
+  uint4 c0, c1;
+  float step;
+  int q;
+  bool valid;
+};
+
+__device__ __forceinline__ void load_slice(Slice& s, const Params& p, int64_t row, int64_t kcol) {
+  s.valid = (row < p.Nw) && (kcol < p.Kw);
+  if (s.valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.codes + row * (p.Kw / 2) + kcol / 2);
+    s.c0 = __ldg(src);
+    s.c1 = __ldg(src + 1);
+    const int64_t b = row * (p.Kw / 64) + kcol / 64;
+    s.q = __ldg(p.qs + b);
+    s.step = __ldg(p.steps + (b >> 8));
+  }
+}
+
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_src, int32_t x,
+                                             int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int kMode>  // 0: forward (W tile K-major), 1: input gradient (W tile MN-major)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fused_nf4_lora_gemm(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmA2,
+                        const __grid_constant__ CUtensorMap tmB2,
+                        const __grid_constant__ CUtensorMap tmOut, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t bready_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t n0 = (int64_t)blockIdx.x * BN;  // output-column tile
+  const int64_t m0 = (int64_t)blockIdx.y * BM;  // token tile
+  const int n_main = static_cast<int>(p.Kc / BK);
+  const int total = p.n_lora + n_main;
+  volatile int* abort_p = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&bready_bar[i], NUM_DEQ_WARPS);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(&acc_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc<1>(&tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one_sync()) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+      for (int s = 0; s < total; ++s) {
+        const int slot = s % STAGES, round = s / STAGES;
+        if (round > 0 && !mbar_wait(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) break;
+        uint8_t* a_dst = smem + slot * STAGE_BYTES;
+        uint8_t* b_dst = a_dst + A_BYTES;
+        if (s < p.n_lora) {
+          mbar_arrive_expect_tx(&full_bar[slot], A_BYTES + B_BYTES);
+          tma_load_2d(a_dst, &tmA2, &full_bar[slot], s * BK, (int32_t)m0);
+          if (kMode == 0) {
+            tma_load_2d(b_dst, &tmB2, &full_bar[slot], s * BK, (int32_t)n0);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              tma_load_2d(b_dst + i * 8192, &tmB2, &full_bar[slot], (int32_t)(n0 + 64 * i), s * BK);
+          }
+        } else {
+          mbar_arrive_expect_tx(&full_bar[slot], A_BYTES);
+          tma_load_2d(a_dst, &tmA, &full_bar[slot], (s - p.n_lora) * BK, (int32_t)m0);
+        }
+      }
+      // never leave with a load in flight: the last issued stages must have landed
+      for (int s = total - STAGES < 0 ? 0 : total - STAGES; s < total; ++s)
+        mbar_wait(&full_bar[s % STAGES], (s / STAGES) & 1, kWaitTmaFull, abort_p, &g_gemm_error);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (elect_one_sync()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, kMode);
+      bool ok = true;
+      for (int s = 0; s < total && ok; ++s) {
+        const int slot = s % STAGES, round = s / STAGES;
+        ok = mbar_wait(&full_bar[slot], round & 1, kWaitTmaFull, abort_p, &g_gemm_error) &&
+             mbar_wait(&bready_bar[slot], round & 1, kWaitBReady, abort_p, &g_gemm_error);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(smem + slot * STAGE_BYTES);
+        const uint32_t b_addr = a_addr + A_BYTES;
+        const int ksteps = (s < p.n_lora && s == p.n_lora - 1) ? p.lora_last_k16 : 4;
+        for (int kk = 0; kk < ksteps; ++kk) {
+          const uint64_t adesc = smem_desc(a_addr + kk * 32, 16, 1024, Swizzle::B128);
+          const uint64_t bdesc = (kMode == 0)
+                                     ? smem_desc(b_addr + kk * 32, 16, 1024, Swizzle::B128)
+                                     : smem_desc(b_addr + kk * 2048, 8192, 1024, Swizzle::B128);
+          umma_bf16_ss<1>(tmem, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&empty_bar[slot]);
+      }
+      if (ok) umma_commit(&acc_bar);
+    }
+    __syncwarp();
+  } else if (warp >= DEQ_WARP0) {
+    // ------------------------------------------------------------ NF4 producers
+    const int dt = threadIdx.x - DEQ_WARP0 * 32;  // 0..255
+    const float mu = __ldg(p.mean);
+    int64_t row_base, kcol;
+    uint32_t dst_off, swz;
+    if (kMode == 0) {
+      row_base = n0 + dt;  // one W row per thread, k-slice of the stage
+      kcol = 0;
+      dst_off = dt * 128;
+      swz = dt & 7;
+    } else {
+      const int nl = (dt & 7) + 8 * ((dt >> 3) & 7);  // W row within the stage's 64
+      const int blk = dt >> 6;                         // which 64 of the tile's 256 columns
+      row_base = nl;
+      kcol = n0 + blk * 64;
+      dst_off = blk * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
+      swz = nl & 7;
+    }
+    auto slice_coords = [&](int kc, int64_t& row, int64_t& col) {
+      if (kMode == 0) { row = row_base; col = (int64_t)kc * BK; }
+      else { row = (int64_t)kc * BK + row_base; col = kcol; }
+    };
+    Slice pf0, pf1;  // slices two stages ahead (even / odd NF4 stage)
+    {
+      int64_t row, col;
+      if (n_main > 0) { slice_coords(0, row, col); load_slice(pf0, p, row, col); }
+      if (n_main > 1) { slice_coords(1, row, col); load_slice(pf1, p, row, col); }
+    }
+    bool ok = true;
+    for (int s = 0; s < total; ++s) {
+      const int slot = s % STAGES, round = s / STAGES;
+      if (s >= p.n_lora) {
+        if (round > 0 && !mbar_wait(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) {
+          ok = false;
+          break;
+        }
+        const int kc = s - p.n_lora;
+        const bool odd = kc & 1;
+        const Slice cur = odd ? pf1 : pf0;
+        if (kc + 2 < n_main) {
+          int64_t row, col;
+          slice_coords(kc + 2, row, col);
+          if (odd) load_slice(pf1, p, row, col);
+          else load_slice(pf0, p, row, col);
+        }
+        uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
+        if (cur.valid) {
+          const Nf4ByteTable tab = nf4_make_table(__fmaf_rn((float)cur.q, cur.step, mu));
+          const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
+                                     cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[4];
+            nf4_dequant8(tab, words[c], o);
+            *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bready_bar[slot]);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok && mbar_wait(&acc_bar, 0, kWaitAccFull, abort_p, &g_gemm_error)) {
+      tc_fence_after();
+      const int lg = warp & 3;                     // TMEM lanes 32*lg .. 32*lg+31
+      const int ch = (warp - DEQ_WARP0) >> 2;      // column half
+      uint8_t* buf0 = smem + (warp - DEQ_WARP0) * 4096;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int col = ch * 128 + c * 32;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(lg * 32) << 16) + col, v);
+        tmem_ld_wait();
+        uint8_t* buf = buf0 + (c & 1) * 2048;
+        if (c >= 2) {
+          if (lane == 0) bulk_wait_read1();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t phys = j ^ ((lane >> 1) & 3);  // 64-byte swizzle
+          *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) = make_uint4(
+              pack_bf16(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+              pack_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+              pack_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+              pack_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && n0 + col < p.Nout && m0 + lg * 32 < p.M) {
+          tma_store_2d(&tmOut, buf, (int32_t)(n0 + col), (int32_t)(m0 + lg * 32));
+        }
+        if (lane == 0) bulk_commit();
+      }
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<1>(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace fused
+
+namespace {
+
+bool map_bf16(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t pitch_elems,
+              uint32_t box_inner, uint32_t box_outer, MapSwizzle sw) {
+  return make_tensor_map_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)inner,
+                            (uint64_t)outer, (uint64_t)pitch_elems * 2, box_inner, box_outer, sw);
+}
+
+template <int kMode>
+int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+  using namespace fused;
+  static bool attr_set = false;  // per process; the attribute is per function
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fused_nf4_lora_gemm<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return QLORA_ERR_CUDA;
+    attr_set = true;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  const int64_t rp = L.rp;
+  CUtensorMap tA, tA2, tB2, tOut;
+  bool ok;
+  Params p{};
+  p.M = a.M;
+  p.Kw = a.K;
+  p.Nw = a.N;
+  p.codes = a.q.codes;
+  p.qs = a.q.scale_codes;
+  p.steps = a.q.scale_steps;
+  p.mean = a.q.scale_mean;
+  p.n_lora = static_cast<int>(rp / 64);
+  p.lora_last_k16 = static_cast<int>((a.r - 64 * (p.n_lora - 1) + 15) / 16);
+  if (kMode == 0) {
+    p.Nout = a.N;
+    p.Kc = a.K;
+    ok = map_bf16(&tA, a.X, a.K, a.M, a.K, 64, BM, MapSwizzle::B128) &&
+         map_bf16(&tA2, ws + L.sU, rp, a.M, rp, 64, BM, MapSwizzle::B128) &&
+         map_bf16(&tB2, ws + L.Bp, rp, a.N, rp, 64, BN, MapSwizzle::B128) &&
+         map_bf16(&tOut, a.Y, a.N, a.M, a.N, 32, 32, MapSwizzle::B64);
+  } else {
+    p.Nout = a.K;
+    p.Kc = a.N;
+    ok = map_bf16(&tA, a.dY, a.N, a.M, a.N, 64, BM, MapSwizzle::B128) &&
+         map_bf16(&tA2, ws + L.sV, rp, a.M, rp, 64, BM, MapSwizzle::B128) &&
+         map_bf16(&tB2, ws + L.Ap, a.K, rp, a.K, 64, 64, MapSwizzle::B128) &&
+         map_bf16(&tOut, a.dX, a.K, a.M, a.K, 32, 32, MapSwizzle::B64);
+  }
+  if (!ok) return QLORA_ERR_CUDA;
+  dim3 grid((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM));
+  fused_nf4_lora_gemm<kMode><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tA, tA2, tB2, tOut, p);
+  return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+  return launch_fused<0>(a, L, stream);
+}
+
+int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+  return launch_fused<1>(a, L, stream);
+}
+
+}  // namespace qlora

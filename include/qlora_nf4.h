@@ -1,0 +1,173 @@
+/*
+ * qlora_nf4.h -- C ABI of the B300 (sm_103a) QLoRA NF4 + LoRA linear-layer library.
+ *
+ * The method (QLoRA tutorial pages):
+ *   - infivelines.com "QLoRA", mechanism paragraphs: the frozen base is stored in 4 bits
+ *     as NormalFloat4 (16 levels at normal quantiles), each block of 64 weights carries
+ *     its own scale, the block scales are quantized again in blocks of 256 (about 0.127
+ *     bits per weight), the base is dequantized to bf16 one block at a time inside the
+ *     matrix multiply, and gradients flow through the frozen base into the adapters.
+ *   - junaidshaukat.com "QLoRA -- the democratization event", recipe items 1-4: 4-bit NF4
+ *     frozen base, 16-bit LoRA adapters, on-the-fly dequantization, double quantization.
+ *   - addaly.com "QLoRA on one card", "What each setting is doing": weights stored in
+ *     4 bits, dequantized to bfloat16 for each matrix multiply.
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller allocates and owns every buffer (device memory unless stated);
+ *     the library never allocates or frees memory.
+ *   - Asynchrony: device work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and the call returns without synchronizing.
+ *   - Validation: all arguments are checked on the host before any launch; on a negative
+ *     status nothing has been enqueued.
+ *   - bf16 buffers are passed as uint16_t (raw bfloat16 bits), row-major.
+ *   - Inputs must be finite; NaN/Inf inputs give unspecified (but memory-safe) results.
+ *   - Layout: W is [N, K] row-major (out x in, the PyTorch Linear layout), X is [M, K],
+ *     Y is [M, N], A is [r, K], B is [N, r], s = scale = alpha / r.
+ */
+#ifndef QLORA_NF4_H
+#define QLORA_NF4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  0 is success; every failure is negative. */
+#define QLORA_OK 0
+#define QLORA_ERR_INVALID_ARG (-1)    /* null pointer, non-positive size, bad scale      */
+#define QLORA_ERR_UNSUPPORTED (-2)    /* blocksize != 64, dq_block != 256, r > 128, or a
+                                         GEMM shape the kernels do not cover            */
+#define QLORA_ERR_MISALIGNED (-3)     /* a pointer is not 16-byte aligned                */
+#define QLORA_ERR_WORKSPACE (-4)      /* workspace smaller than the *_workspace_bytes size */
+#define QLORA_ERR_CUDA (-5)           /* a CUDA runtime call or kernel launch failed     */
+#define QLORA_ERR_DEVICE_TIMEOUT (-6) /* a kernel gave up a bounded wait (see
+                                         qlora_device_status)                            */
+#define QLORA_ERR_NO_DEVICE (-7)      /* current device is not a compute-capability 10.3
+                                         GPU                                             */
+
+#define NF4_BLOCKSIZE 64  /* weights per first-level block (one absmax scale each)   */
+#define NF4_DQ_BLOCK 256  /* first-level scales per second-level (double-quant) group */
+
+/*
+ * A blockwise NF4 tensor with double-quantized scales: views into caller-owned device
+ * memory.  numel = rows * cols, flattened row-major; block b covers flat elements
+ * [64 b, 64 b + 64); group g covers blocks [256 g, 256 g + 256).
+ *   codes        [ceil(numel / 2)] uint8: two 4-bit level indices per byte, the even flat
+ *                element in the high nibble (an odd numel leaves the last low nibble 0).
+ *   scale_codes  [ceil(numel / 64)] int8 in [-127, 127]: second-level code of each block's
+ *                absmax, relative to scale_mean.
+ *   scale_steps  [ceil(numel / 16384)] fp32: second-level step of each group.
+ *   scale_mean   [1] fp32 on the device: the per-tensor mean of the block absmax values.
+ * The recovered block scale is fmaf(scale_codes[b], scale_steps[b / 256], scale_mean[0]),
+ * and weight e dequantizes to bf16_rne(level[code_e] * scale) (one fp32 multiply).
+ * All four pointers must be 16-byte aligned.
+ */
+typedef struct nf4_tensor {
+  uint8_t* codes;
+  int8_t* scale_codes;
+  float* scale_steps;
+  float* scale_mean;
+  int64_t rows; /* N */
+  int64_t cols; /* K */
+  int32_t blocksize; /* must be NF4_BLOCKSIZE */
+  int32_t dq_block;  /* must be NF4_DQ_BLOCK  */
+} nf4_tensor;
+
+/*
+ * Sizes in bytes of the four nf4_tensor buffers for a rows x cols tensor:
+ * sizes[0] codes, sizes[1] scale_codes, sizes[2] scale_steps, sizes[3] scale_mean; *total
+ * is their sum (4.127 bits per weight: infivelines.com "QLoRA", the 0.127 bits/weight
+ * figure for scales per 64 quantized again per 256).  Either output may be NULL.
+ * Host only.  Returns QLORA_ERR_INVALID_ARG for rows or cols < 1,
+ * QLORA_ERR_UNSUPPORTED for another blocksize or dq_block.
+ */
+int nf4_storage_bytes(int64_t rows, int64_t cols, int32_t blocksize, int32_t dq_block,
+                      uint64_t sizes[4], uint64_t* total);
+
+/* Device workspace nf4_quantize needs for numel weights (host only). */
+int nf4_quantize_workspace_bytes(int64_t numel, uint64_t* out);
+
+/*
+ * Quantize fp32 weights W [rows*cols] (device) to NF4 with double-quantized scales into
+ * the caller's nf4_tensor `out` (infivelines.com "QLoRA": NF4 levels, blocks of 64,
+ * scales quantized again in blocks of 256; digipro.cn "QLoRA: Fine-Tuning a 7B Model on a
+ * 16GB GPU": the weights are quantized as they are loaded).
+ * Per block: absmax a, x = w / a (IEEE fp32 division; a = 0 gives x = 0), code = index of
+ * the nearest of the 16 levels (ties to the lower index).  Then mean = fp64 pairwise sum of
+ * all a / count (rounded to fp32); per group step = max |a - mean| / 127 and
+ * scale_code = clamp(rint((a - mean) / step), -127, 127) (0 when step = 0).
+ * `workspace` (device, >= nf4_quantize_workspace_bytes) is scratch that the call
+ * overwrites.  W, out buffers and workspace must be 16-byte aligned.  Any numel >= 1.
+ */
+int nf4_quantize(const float* W, const nf4_tensor* out, void* workspace,
+                 uint64_t workspace_bytes, void* stream);
+
+/*
+ * Dequantize an nf4_tensor to bf16 W_out [rows*cols] (device), bit-exactly the rule in
+ * the nf4_tensor comment (addaly.com "QLoRA on one card": 4-bit storage dequantized to
+ * bfloat16).  W_out 16-byte aligned.  Any numel >= 1.
+ */
+int nf4_dequantize(const nf4_tensor* q, uint16_t* W_out, void* stream);
+
+/* Device workspace (bytes) qlora_linear_fwd / qlora_linear_bwd need for these sizes. */
+int qlora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r, uint64_t* out);
+
+/*
+ * LoRA-wrapped NF4 linear layer, forward (junaidshaukat.com recipe items 2-3; infivelines
+ * "QLoRA": dequantized to bf16 one block at a time inside the matrix multiply):
+ *     U = X A^T (fp32),   Y = bf16( X W'^T + scale * U B^T )
+ * where W' is the bf16 dequantization of Wq.  X [M, K], A [r, K], B [N, r], Y [M, N] are
+ * bf16 device buffers; U_save, if not NULL, receives U as fp32 [M, r] for the backward.
+ * M >= 1; N = Wq->rows and K = Wq->cols must be multiples of 64; 1 <= r <= 128.
+ * M <= 16 runs the decode (GEMV-shaped) kernel, larger M the tensor-core GEMM.
+ * The product accumulates in fp32; the LoRA term enters the accumulator as bf16(scale*U).
+ * ws: device scratch of at least qlora_workspace_bytes(M, N, K, r).
+ */
+int qlora_linear_fwd(const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                     const uint16_t* A, const uint16_t* B, int32_t r, float scale,
+                     uint16_t* Y, float* U_save, void* ws, uint64_t ws_bytes, void* stream);
+
+/*
+ * Backward of qlora_linear_fwd with the base frozen (junaidshaukat.com recipe item 3 and
+ * infivelines "QLoRA": gradients flow back through the quantized weights without updating
+ * them -- there is no dW):
+ *     V  = dY B (fp32 [M, r])
+ *     dX = bf16( dY W' + scale * V A )      [M, K]  (skipped when dX is NULL)
+ *     dA = scale * V^T X                     [r, K]  fp32
+ *     dB = scale * dY^T U                    [N, r]  fp32
+ * U_saved is the fp32 U from the forward, or NULL to recompute it from X and A.
+ * dY [M, N], X [M, K] bf16.  Shapes and ws as for the forward.  The NF4 buffers are only
+ * read.
+ */
+int qlora_linear_bwd(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                     const uint16_t* A, const uint16_t* B, int32_t r, float scale,
+                     const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,
+                     uint64_t ws_bytes, void* stream);
+
+/*
+ * The fp32 constants the kernels use (host only): levels[16], the NF4 levels in ascending
+ * order, and thresholds[15], the midpoints of adjacent levels rounded toward -inf
+ * (code = number of thresholds strictly below x).  Either pointer may be NULL.
+ */
+int nf4_level_table(float levels[16], float thresholds[15]);
+
+/*
+ * Reads and clears the device error word that kernels set when a bounded wait on an
+ * mbarrier gives up (instead of hanging).  Synchronizes `stream`.  *out = 0 when clean,
+ * else a nonzero code naming the wait.  Returns QLORA_ERR_DEVICE_TIMEOUT if it was set.
+ */
+int qlora_device_status(int32_t* out, void* stream);
+
+/* Human-readable text for a status code (static storage, host only). */
+const char* qlora_status_str(int status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int qlora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLORA_NF4_H */

@@ -3,6 +3,7 @@
 Test infrastructure only: the test suite, the smoke check and the benchmark's CPU
 baseline load the result.  Run as ``python oracle/build.py``.
 """
+import hashlib
 import os
 import subprocess
 import sys
@@ -17,13 +18,24 @@ CFLAGS = ["-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
           "-fPIC", "-shared", "-Wall", "-Wextra"]
 
 
+STAMP = LIB + ".stamp"
+
+
+def _digest() -> str:
+    with open(SRC, "rb") as f:
+        return hashlib.sha256(" ".join(CFLAGS).encode() + f.read()).hexdigest()
+
+
 def build(force: bool = False) -> str:
-    if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
-        return LIB
+    if not force and os.path.exists(LIB) and os.path.exists(STAMP):
+        with open(STAMP) as f:
+            if f.read().strip() == _digest():
+                return LIB
     tmp = LIB + f".tmp{os.getpid()}"
     subprocess.run(["gcc", *CFLAGS, SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(_digest())
     return LIB
 
 

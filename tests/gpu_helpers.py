@@ -1,0 +1,56 @@
+"""Helpers for the GPU parity tests: moving seeded inputs to the device and comparing the
+CUDA path against the CPU oracle."""
+import numpy as np
+import torch
+
+import oracle
+import bit_nf4_quantized_37_b300 as qn
+from bit_nf4_quantized_37_b300 import workloads as wl
+
+TOL = 5e-3  # relative Frobenius bound for Y, dX, dA, dB against the fp64 oracle
+
+
+def bf16_dev(bits: np.ndarray) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16).cuda()
+
+
+def bits_host(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def f32_host(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return wl.bf16_bits_to_f32(bits_host(t)).astype(np.float64)
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def rel_fro(got: np.ndarray, ref: np.ndarray) -> float:
+    d = np.linalg.norm((got - ref).ravel())
+    n = np.linalg.norm(ref.ravel())
+    return float(d / n) if n > 0 else float(d)
+
+
+def upload_oracle_tensor(q: dict, rows: int, cols: int) -> qn.NF4Tensor:
+    dev = "cuda"
+    return qn.NF4Tensor(torch.from_numpy(q["codes"]).to(dev),
+                        torch.from_numpy(q["qscale"]).to(dev),
+                        torch.from_numpy(q["steps"]).to(dev),
+                        torch.tensor([q["mean"]], dtype=torch.float32, device=dev), rows, cols)
+
+
+class Problem:
+    """A LinearProblem with its oracle quantization and device copies."""
+
+    def __init__(self, p: wl.LinearProblem, quantize_on_gpu: bool = True):
+        self.p = p
+        W = p.W()
+        self.qo = oracle.quantize(W)
+        self.Wd = oracle.dequantize(self.qo).reshape(p.N, p.K)
+        if quantize_on_gpu:
+            self.qd = qn.nf4_quantize(torch.from_numpy(W).cuda())
+        else:
+            self.qd = upload_oracle_tensor(self.qo, p.N, p.K)
+        self.X, self.A, self.B, self.dY = p.X(), p.A(), p.B(), p.dY()
+        self.Xd, self.Ad, self.Bd, self.dYd = (bf16_dev(self.X), bf16_dev(self.A),
+                                               bf16_dev(self.B), bf16_dev(self.dY))

@@ -1,0 +1,228 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: packed codes, second-level scale codes, steps, mean, dequantized bf16 weights.
+Relative Frobenius error <= 5e-3 against the fp64 oracle: Y, U, dX, dA, dB.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import bit_nf4_quantized_37_b300 as qn
+from bit_nf4_quantized_37_b300 import workloads as wl
+from gpu_helpers import (TOL, Problem, bf16_dev, bits_host, f32_host, rel_fro,
+                         upload_oracle_tensor)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_nf4_quantized_37_b300 import build
+    build.build()
+    qn.lib()
+    yield
+    assert qn.device_status() == 0
+
+
+def _quant_parity(W: np.ndarray):
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda())
+    o = oracle.quantize(W)
+    assert np.array_equal(q.codes.cpu().numpy(), o["codes"])
+    assert np.array_equal(q.scale_codes.cpu().numpy(), o["qscale"])
+    assert np.array_equal(q.scale_steps.cpu().numpy().view(np.uint32), o["steps"].view(np.uint32))
+    assert q.scale_mean.cpu().numpy()[0].view(np.uint32) == np.float32(o["mean"]).view(np.uint32)
+    return q, o
+
+
+# ------------------------------------------------------------------ quantize / dequantize
+@pytest.mark.parametrize("n", [1, 2, 63, 64, 65, 127, 1001, 64 * 256, 64 * 256 + 1,
+                               64 * 300 + 37, 64 * 256 * 5 + 3, 1 << 20])
+def test_quantize_bit_exact_ragged(n):
+    W = wl.weight((1, n), seed=500 + n, sigma=0.02, outlier_frac=0.001 if n > 5000 else 0.0)
+    _quant_parity(W)
+
+
+def test_quantize_special_blocks():
+    W = wl.weight((64 * 512,), seed=3, sigma=0.02).reshape(512, 64)
+    W[5] = 0.0                      # all-zero block
+    W[9] = 0.125                    # constant block
+    W[11, 3] = 1e-30                # tiny absmax
+    W[12, :] = -W[12, :]
+    W[200:456] = W[200]             # a whole group of identical blocks
+    _quant_parity(W.reshape(1, -1))
+
+
+def test_quantize_config_tensors_bit_exact():
+    _quant_parity(wl.config1().W())
+    _quant_parity(wl.config2().W())
+    _quant_parity(wl.config3()[2].W())
+
+
+def test_quantize_decode_tensor_bit_exact():
+    _quant_parity(wl.config4(1).W())
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (1, 17), (3, 333), (256, 256), (64, 64 * 256 + 64),
+                                       (4096, 4096)])
+def test_dequantize_bit_exact(rows, cols):
+    W = wl.weight((rows, cols), seed=rows * 7 + cols, sigma=0.02, outlier_frac=0.001)
+    o = oracle.quantize(W)
+    want = oracle.dequantize(o)
+    # from the oracle's own encoding (independent of the GPU quantizer)
+    qd = upload_oracle_tensor(o, rows, cols)
+    got = bits_host(qn.nf4_dequantize(qd)).reshape(-1)
+    assert np.array_equal(got, want)
+    # and round trip through the GPU quantizer
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda())
+    assert np.array_equal(bits_host(qn.nf4_dequantize(q)).reshape(-1), want)
+
+
+def test_dequantize_decode_tensor_bit_exact():
+    p = wl.config4(1)
+    W = p.W()
+    o = oracle.quantize(W)
+    want = oracle.dequantize(o)
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda())
+    got = bits_host(qn.nf4_dequantize(q)).reshape(-1)
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------------ forward / backward
+def _check_fwd(pb: Problem, rows=None):
+    p = pb.p
+    Y, U = qn.qlora_linear_fwd(pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale)
+    Yo, Uo = oracle.lora_fwd(pb.X, pb.Wd, pb.A, pb.B, p.scale, rows)
+    Yg = f32_host(Y)
+    Ug = f32_host(U)
+    if rows is not None:
+        Yg, Ug = Yg[rows], Ug[rows]
+    ey, eu = rel_fro(Yg, Yo), rel_fro(Ug, Uo)
+    assert ey <= TOL, ey
+    assert eu <= TOL, eu
+    return Y, U
+
+
+def _check_bwd(pb: Problem, U, rows=None):
+    p = pb.p
+    dX, dA, dB = qn.qlora_linear_bwd(pb.dYd, pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale, U)
+    dXo, _ = oracle.lora_dx(pb.dY, pb.Wd, pb.A, pb.B, p.scale, rows)
+    dAo, dBo = oracle.lora_dadb(pb.dY, pb.X, pb.A, pb.B, p.scale)
+    dXg = f32_host(dX)
+    if rows is not None:
+        dXg = dXg[rows]
+    ex = rel_fro(dXg, dXo)
+    assert ex <= TOL, ex
+    if np.linalg.norm(dAo) > 0:
+        ea = rel_fro(f32_host(dA), dAo)
+        assert ea <= TOL, ea
+    else:
+        assert np.all(f32_host(dA) == 0)
+    eb = rel_fro(f32_host(dB), dBo)
+    assert eb <= TOL, eb
+    return dX, dA, dB
+
+
+SMALL = [
+    # name, M, N, K, r, alpha
+    ("cfg1", 16, 256, 256, 8, 16.0),
+    ("ragged", 200, 320, 448, 16, 32.0),
+    ("rank40", 130, 512, 256, 40, 16.0),
+    ("rank72", 129, 256, 320, 72, 16.0),
+    ("rank128", 300, 384, 512, 128, 64.0),
+    ("tokens17", 17, 640, 192, 16, 32.0),
+    ("tokens1", 1, 576, 320, 8, 16.0),
+    ("tokens5", 5, 256, 1024, 64, 16.0),
+    ("multi_tile", 520, 1024, 1088, 16, 32.0),
+]
+
+
+@pytest.mark.parametrize("name,M,N,K,r,alpha", SMALL)
+def test_fwd_bwd_small(name, M, N, K, r, alpha):
+    p = wl.LinearProblem(name, M, N, K, r, alpha, 0.02, 0.001, config=90 + len(name))
+    pb = Problem(p)
+    Y, U = _check_fwd(pb)
+    _check_bwd(pb, U)
+    _check_bwd(pb, None)  # U recomputed in the backward
+
+
+def test_zero_b_equals_base_matmul():
+    pb = Problem(wl.config1(b_zero=True))
+    p = pb.p
+    Y, U = qn.qlora_linear_fwd(pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale)
+    base = wl.bf16_bits_to_f32(pb.X).astype(np.float64) @ wl.bf16_bits_to_f32(pb.Wd).astype(np.float64).T
+    assert rel_fro(f32_host(Y), base) <= TOL
+    dX, dA, dB = qn.qlora_linear_bwd(pb.dYd, pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale, U)
+    assert np.all(dA.cpu().numpy() == 0.0)
+    # same with the fused GEMM path (M > 16)
+    p2 = wl.LinearProblem("bzero-fused", 96, 256, 256, 8, 16.0, config=1, b_zero=True)
+    pb2 = Problem(p2)
+    Y2, _ = qn.qlora_linear_fwd(pb2.Xd, pb2.qd, pb2.Ad, pb2.Bd, p2.scale)
+    base2 = wl.bf16_bits_to_f32(pb2.X).astype(np.float64) @ wl.bf16_bits_to_f32(pb2.Wd).astype(np.float64).T
+    assert rel_fro(f32_host(Y2), base2) <= TOL
+
+
+def test_base_is_frozen_and_results_reproducible():
+    p = wl.LinearProblem("repro", 300, 512, 512, 16, 32.0, config=77)
+    pb = Problem(p)
+    before = [t.clone() for t in (pb.qd.codes, pb.qd.scale_codes, pb.qd.scale_steps, pb.qd.scale_mean)]
+    Y1, U1 = qn.qlora_linear_fwd(pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale)
+    g1 = qn.qlora_linear_bwd(pb.dYd, pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale, U1)
+    Y2, U2 = qn.qlora_linear_fwd(pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale)
+    g2 = qn.qlora_linear_bwd(pb.dYd, pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale, U2)
+    after = (pb.qd.codes, pb.qd.scale_codes, pb.qd.scale_steps, pb.qd.scale_mean)
+    for b, a in zip(before, after):
+        assert torch.equal(b, a)
+    assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+    assert torch.equal(U1, U2)
+    for x, y in zip(g1, g2):
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y)
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _sample_rows(M, n=24, seed=0):
+    r = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, M - 1], r.choice(M, size=min(n, M), replace=False)]))
+    return rows.astype(np.int64)
+
+
+def test_config2_attention_projection():
+    pb = Problem(wl.config2())
+    rows = _sample_rows(pb.p.M)
+    Y, U = _check_fwd(pb, rows)
+    _check_bwd(pb, U, rows)
+
+
+@pytest.mark.parametrize("which", [0, 2])
+def test_config3_mlp_projection(which):
+    pb = Problem(wl.config3()[which])
+    rows = _sample_rows(pb.p.M, 16, which)
+    Y, U = _check_fwd(pb, rows)
+    _check_bwd(pb, U, rows)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_config4_decode(M):
+    pb = Problem(wl.config4(M))
+    _check_fwd(pb)
+
+
+def test_config5_layer_sampled():
+    for p in wl.config5(layer=0)[::3]:
+        pb = Problem(p)
+        rows = _sample_rows(p.M, 12, 5)
+        Y, U = _check_fwd(pb, rows)
+        _check_bwd(pb, U, rows)
+
+
+# ------------------------------------------------------------------ error paths
+def test_bad_arguments_raise():
+    pb = Problem(wl.config1())
+    with pytest.raises(ValueError):
+        qn.qlora_linear_fwd(pb.Xd.float(), pb.qd, pb.Ad, pb.Bd, 2.0)
+    bad = qn.NF4Tensor(pb.qd.codes, pb.qd.scale_codes, pb.qd.scale_steps, pb.qd.scale_mean, 250, 256)
+    with pytest.raises(qn.QLoRAError):
+        qn.qlora_linear_fwd(pb.Xd[:, :256], bad, pb.Ad, pb.Bd, 2.0)

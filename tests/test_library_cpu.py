@@ -1,0 +1,89 @@
+"""CPU-side checks of the C-ABI library: it loads, exports every declared symbol, its
+constant tables equal the oracle's construction, and host-side validation answers without
+touching a GPU.  No compute calls (there is no GPU here)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import bit_nf4_quantized_37_b300 as qn
+from bit_nf4_quantized_37_b300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qlora_nf4.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_0-9]+)\s*\(", src, re.M)
+    return sorted(set(n for n in names if n.startswith(("nf4_", "qlora_"))))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_nf4_quantized_37_b300 import build
+    build.build()
+    return qn.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 11
+    assert sorted(declared) == sorted(_binding.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_level_table_equals_oracle_construction(lib):
+    L, T = qn.level_table()
+    Lo, To = oracle.levels()
+    assert np.array_equal(np.array(L, np.float32), Lo)
+    assert np.array_equal(np.array(T, np.float32), To)
+
+
+def test_storage_bytes_formula(lib):
+    for rows, cols in ((1, 1), (3, 5), (256, 256), (4096, 11008), (28672, 8192), (7, 64 * 256 + 3)):
+        sizes, total = qn.nf4_storage_bytes(rows, cols)
+        n = rows * cols
+        nb = -(-n // 64)
+        ng = -(-nb // 256)
+        assert sizes == [(n + 1) // 2, nb, 4 * ng, 4]
+        assert total == sum(sizes)
+    # 4.127 bits per weight on a large tensor (infivelines.com "QLoRA": ~0.127 bits/weight)
+    _, total = qn.nf4_storage_bytes(4096, 11008)
+    assert abs(total * 8 / (4096 * 11008) - 4.127) < 0.001
+
+
+def test_host_validation_without_device(lib):
+    u64 = ctypes.c_uint64(0)
+    assert lib.nf4_storage_bytes(0, 5, 64, 256, None, ctypes.byref(u64)) == -1
+    assert lib.nf4_storage_bytes(5, 5, 32, 256, None, ctypes.byref(u64)) == -2
+    assert lib.nf4_storage_bytes(5, 5, 64, 128, None, ctypes.byref(u64)) == -2
+    assert lib.qlora_workspace_bytes(16, 256, 256, 129, ctypes.byref(u64)) == -2
+    assert lib.qlora_workspace_bytes(16, 256, 256, 8, ctypes.byref(u64)) == 0 and u64.value > 0
+    S = _binding._NF4Struct
+    good = S(16, 32, 48, 64, 256, 256, 64, 256)
+    assert lib.nf4_dequantize(ctypes.byref(S(16, 32, 48, 64, 256, 256, 32, 256)), 16, None) == -2
+    assert lib.nf4_dequantize(ctypes.byref(S(17, 32, 48, 64, 256, 256, 64, 256)), 16, None) == -3
+    assert lib.nf4_dequantize(ctypes.byref(S(0, 32, 48, 64, 256, 256, 64, 256)), 16, None) == -1
+    assert lib.nf4_dequantize(ctypes.byref(good), 24, None) == -3
+    # fused path needs N, K multiples of 64
+    bad_shape = S(16, 32, 48, 64, 250, 256, 64, 256)
+    assert lib.qlora_linear_fwd(16, 16, ctypes.byref(bad_shape), 16, 16, 8, ctypes.c_float(2.0),
+                                16, None, 16, 1 << 30, None) == -2
+    # well-formed arguments reach the device check, which fails cleanly on a CPU-only host
+    st = lib.nf4_dequantize(ctypes.byref(good), 16, None)
+    assert st in (-7, 0)
+    assert lib.qlora_status_str(-4).decode() == "workspace too small"
+
+
+def test_workspace_grows_with_problem(lib):
+    a = qn.qlora_workspace_bytes(16, 256, 256, 8)
+    b = qn.qlora_workspace_bytes(4096, 4096, 4096, 16)
+    c = qn.qlora_workspace_bytes(4096, 4096, 4096, 128)
+    assert 0 < a < b < c
+    assert qn.nf4_quantize_workspace_bytes(28672 * 8192) >= 28672 * 8192 // 64 * 4
