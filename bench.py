@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Benchmark of the NF4 + LoRA linear layer on B300.
+
+Headline: forward + backward (to dX, dA, dB) TFLOP/s of the 7B-attention-shaped projection
+(W 4096 x 4096 as NF4 with double-quantized scales, X 4096 tokens x 4096 bf16, LoRA r=16,
+alpha=32), inputs resident in HBM, L2 flushed between steps, per-step CUDA events.
+Alongside: the dominant kernel's roofline (live CUDA-event timing through the library's
+profiling hook), an end-to-end number through the public API with host buffers, the HBM-bound
+kernels (dequantize, quantize, decode M = 1/4/16) in GB/s, SM clocks sampled during the
+timed region, and the CPU oracle timed on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica (the layer needs no exchange
+for a fixed batch); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+METRIC = "NF4+LoRA linear fwd+bwd TFLOP/s and dequant GB/s on 1 B300, % of roofline"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_records():
+    """ncu DRAM bytes per launch committed under profiles/, keyed by kernel, valid only
+    while the kernel's source file is unchanged (sha256 of the file)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    for line in open(path):
+        if not line.strip() or line.startswith("#"):
+            continue
+        name, src, sha, nbytes, workload = line.split(None, 4)
+        fp = os.path.join(ROOT, src)
+        if os.path.exists(fp) and hashlib.sha256(open(fp, "rb").read()).hexdigest() == sha:
+            out[(name, workload.strip())] = float(nbytes)
+    return out
+
+
+# ------------------------------------------------------------------ clocks sampler
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+def bf16_dev(bits, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def oracle_sample(p, X, Wd, A, B, dY, target_s: float = 12.0):
+    """The oracle (fp64 CPU loops) on a bounded sample of the workload: Y and dX for a
+    subset of token rows plus U, V, dA, dB over all rows.  Returns (TFLOP/s, desc, cores)."""
+    import oracle
+    M, N, K, r = p.M, p.N, p.K, p.r
+
+    def run(nrows):
+        rows = np.linspace(0, M - 1, nrows).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.lora_fwd(X, Wd, A, B, p.scale, rows)
+        oracle.lora_dx(dY, Wd, A, B, p.scale, rows)
+        t1 = time.perf_counter()
+        return t1 - t0
+
+    t_rows = run(8) / 8
+    t0 = time.perf_counter()
+    oracle.lora_dadb(dY, X, A, B, p.scale)
+    t_full = time.perf_counter() - t0
+    nrows = int(max(8, min(M, (target_s - t_full) / max(t_rows, 1e-9))))
+    t_rows_total = run(nrows)
+    flops = (2.0 * nrows * (N * K + r * K + r * N) * 2          # Y rows (with U), dX rows (with V)
+             + 2.0 * (M * K * r + M * N * r + r * K * M + N * r * M))  # U, V, dA, dB over all M
+    secs = t_rows_total + t_full
+    desc = (f"oracle fp64 loops: Y and dX for {nrows} of {M} token rows, U/V/dA/dB over all "
+            f"{M} rows ({flops / 1e9:.1f} GFLOP in {secs:.1f} s)")
+    return flops / secs / 1e12, desc, oracle.num_threads(), secs
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from bit_nf4_quantized_37_b300 import workloads as wl
+    import oracle
+    p = wl.config2()
+    W = p.W()
+    q = oracle.quantize(W)
+    Wd = oracle.dequantize(q).reshape(p.N, p.K)
+    X, A, B, dY = p.X(), p.A(), p.B(), p.dY()
+    vals = []
+    descs = []
+    cores = oracle.num_threads()
+    per_step_s = max(3.0, 60.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        v, d, cores, secs = oracle_sample(p, X, Wd, A, B, dY, target_s=per_step_s)
+        if i >= args.warmup:
+            vals.append(v)
+            descs.append(d)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(p),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": descs[-1]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(p):
+    return {"workload": f"7B attention projection: W {p.N}x{p.K} NF4 (block 64, double-quant 256),"
+                        f" X {p.M}x{p.K} bf16, LoRA r={p.r} alpha={p.alpha:g}, fwd + bwd (dX, dA, dB)",
+            "M": p.M, "N": p.N, "K": p.K, "r": p.r, "alpha": p.alpha,
+            "l2": "flushed between timed steps (256 MiB write)",
+            "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    world, rank, local = dist_setup(args)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import bit_nf4_quantized_37_b300 as qn
+    from bit_nf4_quantized_37_b300 import build, workloads as wl
+    build.build()
+    qn.lib()
+    peaks, peak_src = load_peaks()
+    traffic = traffic_records()
+
+    p = wl.config2()
+    W = p.W()
+    Xh, Ah, Bh, dYh = p.X(), p.A(), p.B(), p.dY()
+    q = qn.nf4_quantize(torch.from_numpy(W).to(dev))
+    X, A, B, dY = (bf16_dev(t, dev) for t in (Xh, Ah, Bh, dYh))
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = p.scale
+
+    def step():
+        Y, U = qn.qlora_linear_fwd(X, q, A, B, s)
+        dX, dA, dB = qn.qlora_linear_bwd(dY, X, q, A, B, s, U)
+        return Y, dX, dA, dB
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    qn.profile_start()
+    for i in range(args.steps):
+        flush_buf.zero_()
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    prof = qn.profile_stop()
+    clk = clocks.stop() if clocks else None
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    flops_step = p.fwd_bwd_flops()
+    value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
+    launches = sum(v[0] for v in prof.values())
+
+    # dominant kernel and its roofline (algorithmic FLOPs per launch / mean launch time)
+    dom = max(prof.items(), key=lambda kv: kv[1][1])
+    dom_name, (dom_n, dom_ms) = dom
+    per_launch_flops = {
+        "fused_fwd_gemm": 2.0 * p.M * p.N * p.K + 2.0 * p.M * p.N * p.r,
+        "fused_dx_gemm": 2.0 * p.M * p.N * p.K + 2.0 * p.M * p.K * p.r,
+    }
+    rl = None
+    if dom_name in per_launch_flops:
+        ach = per_launch_flops[dom_name] / (dom_ms / dom_n / 1e3) / 1e12
+        tr = traffic.get((dom_name, "config2"))
+        rl = {"bound": "tensor", "kernel": dom_name, "achieved": ach, "peak": peaks["bf16_tflops"],
+              "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": tr,
+              "peak_source": f"{peak_src} bf16 burst",
+              "mean_launch_ms": dom_ms / dom_n}
+    kernels = {k: {"launches": n, "ms_per_launch": ms / n, "share": ms / sum(v[1] for v in prof.values())}
+               for k, (n, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1])}
+    other = {}
+    for k in ("fused_fwd_gemm", "fused_dx_gemm"):
+        if k in prof:
+            n, ms = prof[k]
+            a = per_launch_flops[k] / (ms / n / 1e3) / 1e12
+            other[k] = {"achieved_tflops": a, "frac_of_bf16_burst": a / peaks["bf16_tflops"],
+                        "frac_of_bf16_sustained": a / peaks["bf16_tflops_sustained"]}
+
+    # end to end through the public API with host buffers (pinned), copies inside the region
+    Xp = torch.from_numpy(Xh.view(np.int16)).view(torch.bfloat16).pin_memory()
+    dYp = torch.from_numpy(dYh.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Yp = torch.empty(p.M, p.N, dtype=torch.bfloat16).pin_memory()
+    dXp = torch.empty(p.M, p.K, dtype=torch.bfloat16).pin_memory()
+    dAp = torch.empty(p.r, p.K, dtype=torch.float32).pin_memory()
+    dBp = torch.empty(p.N, p.r, dtype=torch.float32).pin_memory()
+    Xd = torch.empty_like(X)
+    dYd = torch.empty_like(dY)
+
+    def e2e_step():
+        Xd.copy_(Xp, non_blocking=True)
+        dYd.copy_(dYp, non_blocking=True)
+        Y, U = qn.qlora_linear_fwd(Xd, q, A, B, s)
+        dX, dA, dB = qn.qlora_linear_bwd(dYd, Xd, q, A, B, s, U)
+        Yp.copy_(Y, non_blocking=True)
+        dXp.copy_(dX, non_blocking=True)
+        dAp.copy_(dA, non_blocking=True)
+        dBp.copy_(dB, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_val = flops_step * args.steps * world / (e2e_ms / 1e3) / 1e12
+    h2d = Xp.numel() * 2 + dYp.numel() * 2
+    d2h = Yp.numel() * 2 + dXp.numel() * 2 + dAp.numel() * 4 + dBp.numel() * 4
+
+    secondary = {} if args.no_secondary else measure_secondary(qn, wl, dev, peaks, traffic,
+                                                               flush_buf)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normal weights / activations, random-init adapters)",
+        "config": config_block(p),
+        "roofline": rl,
+        "gemm_rooflines": other,
+        "kernels": kernels,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "secondary": secondary,
+    }
+    if rank == 0 and not args.no_cpu:
+        import oracle
+        Wd = oracle.dequantize(oracle.quantize(W)).reshape(p.N, p.K)
+        v, desc, cores, _ = oracle_sample(p, Xh, Wd, Ah, Bh, dYh)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_secondary(qn, wl, dev, peaks, traffic, flush_buf, reps: int = 10):
+    """HBM-bound paths on the decode-shaped 28672 x 8192 weight: dequantize, quantize and the
+    M = 1 / 4 / 16 decode forward, each in GB/s of algorithmic bytes against the HBM peak."""
+    import torch
+    out = {}
+    p4 = wl.config4(1)
+    W = torch.from_numpy(p4.W()).to(dev)
+    numel = W.numel()
+    q = qn.nf4_quantize(W)
+    meta = q.storage_bytes()
+    Wd = torch.empty(p4.N, p4.K, dtype=torch.bfloat16, device=dev)
+
+    def timed(fn, names):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        qn.profile_start()
+        for _ in range(reps):
+            flush_buf.zero_()
+            fn()
+        torch.cuda.synchronize()
+        prof = qn.profile_stop()
+        ms = sum(prof[n][1] for n in names if n in prof) / reps
+        return ms, prof
+
+    hbm = peaks["hbm_gbs"]
+    ms, _ = timed(lambda: qn.nf4_dequantize(q, Wd), ["nf4_dequant"])
+    nbytes = meta + 2 * numel
+    out["dequantize_28672x8192"] = {"GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm,
+                                    "ms": ms, "bytes": nbytes,
+                                    "traffic": traffic.get(("nf4_dequant", "config4"))}
+    qq = qn.NF4Tensor.empty(p4.N, p4.K, dev)
+    ms, prof = timed(lambda: qn.nf4_quantize(W, qq),
+                     ["nf4_quant_blocks", "nf4_absmax_mean", "nf4_double_quant"])
+    nbytes = 4 * numel + meta
+    out["quantize_28672x8192"] = {"GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm,
+                                  "ms": ms, "bytes": nbytes,
+                                  "kernels_ms": {k: v[1] / reps for k, v in prof.items()}}
+    del W
+    for M in (1, 4, 16):
+        p = wl.config4(M)
+        X = bf16_dev(p.X(), dev)
+        A = bf16_dev(p.A(), dev)
+        B = bf16_dev(p.B(), dev)
+        Y = torch.empty(M, p.N, dtype=torch.bfloat16, device=dev)
+        fn = lambda: qn.qlora_linear_fwd(X, q, A, B, p.scale, save_u=False, out=Y)  # noqa: E731
+        ms_all, prof = timed(fn, ["pad_adapters", "side_u", "finalize_rows", "decode_gemv",
+                                  "decode_finalize"])
+        ms_gemv = prof["decode_gemv"][1] / reps
+        nbytes = meta + 2 * M * p.K + 2 * M * p.N + 2 * p.r * (p.K + p.N)
+        out[f"decode_fwd_M{M}"] = {
+            "GB/s": nbytes / ms_all / 1e6, "frac_hbm": nbytes / ms_all / 1e6 / hbm,
+            "ms": ms_all, "bytes": nbytes,
+            "gemv_kernel_GB/s": meta / ms_gemv / 1e6,
+            "gemv_kernel_frac_hbm": meta / ms_gemv / 1e6 / hbm,
+            "kernels_ms": {k: v[1] / reps for k, v in prof.items()}}
+    return out
+
+
+if __name__ == "__main__":
+    main()

@@ -20,7 +20,8 @@ _STATUS = {0: "QLORA_OK", -1: "QLORA_ERR_INVALID_ARG", -2: "QLORA_ERR_UNSUPPORTE
 # Every symbol include/qlora_nf4.h declares.
 EXPORTS = ["nf4_storage_bytes", "nf4_quantize_workspace_bytes", "nf4_quantize",
            "nf4_dequantize", "qlora_workspace_bytes", "qlora_linear_fwd", "qlora_linear_bwd",
-           "nf4_level_table", "qlora_device_status", "qlora_status_str", "qlora_version"]
+           "nf4_level_table", "qlora_device_status", "qlora_status_str", "qlora_version",
+           "qlora_profile_start", "qlora_profile_stop"]
 
 
 class QLoRAError(RuntimeError):
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
             "qlora_device_status": [vp, vp],
             "qlora_status_str": [ctypes.c_int],
             "qlora_version": [],
+            "qlora_profile_start": [],
+            "qlora_profile_stop": [vp, i32, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -238,6 +241,26 @@ def qlora_linear_bwd(dY: torch.Tensor, X: torch.Tensor, q: NF4Tensor, A: torch.T
         _ptr(dY), _ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(U),
         _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), ws.numel(), _stream()))
     return dX, dA, dB
+
+
+class _KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int32),
+                ("total_ms", ctypes.c_double)]
+
+
+def profile_start() -> None:
+    """Bracket every library kernel launch with CUDA events until profile_stop()."""
+    _check("qlora_profile_start", lib().qlora_profile_start())
+
+
+def profile_stop() -> dict:
+    """{kernel name: (launches, summed device ms)} since profile_start (synchronizes)."""
+    cap = 64
+    buf = (_KernelTime * cap)()
+    n = ctypes.c_int32(0)
+    _check("qlora_profile_stop", lib().qlora_profile_stop(buf, cap, ctypes.byref(n)))
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+            for i in range(min(n.value, cap))}
 
 
 def device_status() -> int:

@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "linear.h"
+#include "profile.h"
 
 namespace qlora {
 namespace side {
@@ -231,8 +232,10 @@ int64_t pick_chunk(int64_t rows, int64_t C) {
 }
 
 template <bool kCol>
-int run_side(const uint16_t* P, int64_t R, int64_t C, int64_t ldp, const uint16_t* Q, int64_t ldq,
-             int NJ, float* part, int64_t chunk, cudaStream_t stream) {
+int run_side(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t ldp,
+             const uint16_t* Q, int64_t ldq, int NJ, float* part, int64_t chunk,
+             cudaStream_t stream) {
+  ProfileScope ps(name, stream);
   const int64_t c_pad = (C + side::TC - 1) / side::TC * side::TC;
   dim3 grid((unsigned)((R + side::TR - 1) / side::TR), (unsigned)((c_pad + chunk - 1) / chunk));
   const int smem = 2 * (side::TR * side::TC + NJ * side::TC) * 2;
@@ -284,6 +287,7 @@ uint64_t side_partial_bytes(int64_t M, int64_t N, int64_t K, int r) {
 int launch_pad_adapters(const LinearArgs& a, const WorkspaceLayout& L, bool need_bt,
                         cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  ProfileScope ps("pad_adapters", stream);
   side::pad_adapters<<<grid_for(a.N * L.rp + L.rp * a.K), 256, 0, stream>>>(
       a.A, a.B, a.N, a.K, a.r, L.rp, reinterpret_cast<uint16_t*>(ws + L.Bp),
       need_bt ? reinterpret_cast<uint16_t*>(ws + L.Bt) : nullptr,
@@ -297,10 +301,11 @@ int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t st
   const int NJ = pick_nj(a.r);
   float* part = reinterpret_cast<float*>(ws + L.part);
   const int64_t chunk = pick_chunk(a.M, a.K);
-  int st = run_side<false>(a.X, a.M, a.K, a.K, reinterpret_cast<const uint16_t*>(ws + L.Ap), a.K,
+  int st = run_side<false>("side_u", a.X, a.M, a.K, a.K, reinterpret_cast<const uint16_t*>(ws + L.Ap), a.K,
                            NJ, part, chunk, stream);
   if (st) return st;
   const int64_t Mp = round_up(a.M, 64);
+  ProfileScope ps("finalize_rows", stream);
   side::finalize_rows<<<grid_for(Mp * L.rp), 256, 0, stream>>>(
       part, splits_of(a.K, chunk), a.M, NJ, a.r, L.rp, Mp, a.U, a.r,
       reinterpret_cast<uint16_t*>(ws + L.sU), a.scale, nullptr, 0.f);
@@ -323,6 +328,7 @@ int launch_u_from_saved(const LinearArgs& a, const WorkspaceLayout& L, cudaStrea
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   const int64_t Mp = round_up(a.M, 64);
   if (a.U_in) {
+    ProfileScope ps("ut_from_saved", stream);
     ut_from_saved<<<grid_for(L.rp * Mp), 256, 0, stream>>>(a.U_in, a.M, a.r, L.rp, Mp,
                                                            reinterpret_cast<uint16_t*>(ws + L.Ut));
     return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
@@ -331,9 +337,10 @@ int launch_u_from_saved(const LinearArgs& a, const WorkspaceLayout& L, cudaStrea
   const int NJ = pick_nj(a.r);
   float* part = reinterpret_cast<float*>(ws + L.part);
   const int64_t chunk = pick_chunk(a.M, a.K);
-  int st = run_side<false>(a.X, a.M, a.K, a.K, reinterpret_cast<const uint16_t*>(ws + L.Ap), a.K,
-                           NJ, part, chunk, stream);
+  int st = run_side<false>("side_u", a.X, a.M, a.K, a.K, reinterpret_cast<const uint16_t*>(ws + L.Ap),
+                           a.K, NJ, part, chunk, stream);
   if (st) return st;
+  ProfileScope ps("finalize_rows", stream);
   side::finalize_rows<<<grid_for(Mp * L.rp), 256, 0, stream>>>(
       part, splits_of(a.K, chunk), a.M, NJ, a.r, L.rp, Mp, nullptr, 0, nullptr, 0.f,
       reinterpret_cast<uint16_t*>(ws + L.Ut), 1.0f);
@@ -346,10 +353,11 @@ int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t st
   const int NJ = pick_nj(a.r);
   float* part = reinterpret_cast<float*>(ws + L.part);
   const int64_t chunk = pick_chunk(a.M, a.N);
-  int st = run_side<false>(a.dY, a.M, a.N, a.N, reinterpret_cast<const uint16_t*>(ws + L.Bt), a.N,
-                           NJ, part, chunk, stream);
+  int st = run_side<false>("side_v", a.dY, a.M, a.N, a.N, reinterpret_cast<const uint16_t*>(ws + L.Bt),
+                           a.N, NJ, part, chunk, stream);
   if (st) return st;
   const int64_t Mp = round_up(a.M, 64);
+  ProfileScope ps("finalize_rows", stream);
   side::finalize_rows<<<grid_for(Mp * L.rp), 256, 0, stream>>>(
       part, splits_of(a.N, chunk), a.M, NJ, a.r, L.rp, Mp, nullptr, 0,
       reinterpret_cast<uint16_t*>(ws + L.sV), a.scale, reinterpret_cast<uint16_t*>(ws + L.Vt),
@@ -364,9 +372,10 @@ int launch_lora_db(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t s
   float* part = reinterpret_cast<float*>(ws + L.part);
   const int64_t chunk = pick_chunk(a.N, a.M);
   const int64_t Mp = round_up(a.M, 64);
-  int st = run_side<true>(a.dY, a.N, a.M, a.N, reinterpret_cast<const uint16_t*>(ws + L.Ut), Mp, NJ,
-                          part, chunk, stream);
+  int st = run_side<true>("side_db", a.dY, a.N, a.M, a.N, reinterpret_cast<const uint16_t*>(ws + L.Ut),
+                          Mp, NJ, part, chunk, stream);
   if (st) return st;
+  ProfileScope ps("finalize_grad", stream);
   side::finalize_grad<<<grid_for(a.N * a.r), 256, 0, stream>>>(part, splits_of(a.M, chunk), a.N, NJ,
                                                                a.r, a.scale, a.dB, a.r, 1);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
@@ -379,9 +388,10 @@ int launch_lora_da(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t s
   float* part = reinterpret_cast<float*>(ws + L.part);
   const int64_t chunk = pick_chunk(a.K, a.M);
   const int64_t Mp = round_up(a.M, 64);
-  int st = run_side<true>(a.X, a.K, a.M, a.K, reinterpret_cast<const uint16_t*>(ws + L.Vt), Mp, NJ,
-                          part, chunk, stream);
+  int st = run_side<true>("side_da", a.X, a.K, a.M, a.K, reinterpret_cast<const uint16_t*>(ws + L.Vt),
+                          Mp, NJ, part, chunk, stream);
   if (st) return st;
+  ProfileScope ps("finalize_grad", stream);
   side::finalize_grad<<<grid_for(a.K * a.r), 256, 0, stream>>>(part, splits_of(a.M, chunk), a.K, NJ,
                                                                a.r, 1.0f, a.dA, 1, a.K);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;

@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "nf4_device.cuh"
 #include "launch.h"
+#include "profile.h"
 
 namespace qlora {
 
@@ -223,13 +224,22 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   const int64_t ng = (nb + kGroup - 1) / kGroup;
   float* absmax = reinterpret_cast<float*>(ws);
   double* gsum = reinterpret_cast<double*>(reinterpret_cast<char*>(ws) + ng * kGroup * 4);
-  nf4_quant_blocks<<<(unsigned)ng, kQuantThreads, 0, stream>>>(W, numel, q.codes, absmax, gsum);
+  {
+    ProfileScope ps("nf4_quant_blocks", stream);
+    nf4_quant_blocks<<<(unsigned)ng, kQuantThreads, 0, stream>>>(W, numel, q.codes, absmax, gsum);
+  }
   int64_t p2 = 1;
   while (p2 < ng) p2 *= 2;
   const int64_t run = p2 > 1024 ? p2 / 1024 : 1;
-  nf4_absmax_mean<<<1, 1024, 0, stream>>>(gsum, ng, nb, run, q.scale_mean);
-  nf4_double_quant<<<(unsigned)ng, kGroup, 0, stream>>>(absmax, nb, q.scale_mean, q.scale_codes,
-                                                        q.scale_steps);
+  {
+    ProfileScope ps("nf4_absmax_mean", stream);
+    nf4_absmax_mean<<<1, 1024, 0, stream>>>(gsum, ng, nb, run, q.scale_mean);
+  }
+  {
+    ProfileScope ps("nf4_double_quant", stream);
+    nf4_double_quant<<<(unsigned)ng, kGroup, 0, stream>>>(absmax, nb, q.scale_mean, q.scale_codes,
+                                                          q.scale_steps);
+  }
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
@@ -239,6 +249,7 @@ int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, cudaStr
   int64_t blocks = (npieces + threads - 1) / threads;
   const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
+  ProfileScope ps("nf4_dequant", stream);
   nf4_dequant_kernel<<<(unsigned)blocks, threads, 0, stream>>>(q.codes, q.scale_codes,
                                                                q.scale_steps, q.scale_mean,
                                                                numel, out);

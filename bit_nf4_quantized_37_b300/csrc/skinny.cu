@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "linear.h"
+#include "profile.h"
 #include "nf4_device.cuh"
 
 namespace qlora {
@@ -200,9 +201,13 @@ int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_
                            smem) != cudaSuccess)
     return QLORA_ERR_CUDA;
   dim3 grid((unsigned)((a.N + skinny::ROWS_PER_CTA - 1) / skinny::ROWS_PER_CTA), (unsigned)S);
+  {
+  ProfileScope ps("decode_gemv", stream);
   skinny::nf4_decode_gemv<<<grid, skinny::THREADS, smem, stream>>>(
       a.X, a.M, a.N, a.K, a.q.codes, a.q.scale_codes, a.q.scale_steps, a.q.scale_mean, ks, part);
+  }
   if (cudaGetLastError() != cudaSuccess) return QLORA_ERR_CUDA;
+  ProfileScope ps("decode_finalize", stream);
   const int fsmem = static_cast<int>(a.M * a.r * 4);
   skinny::decode_finalize<<<(unsigned)((a.N + 255) / 256), 256, fsmem, stream>>>(
       part, (int)S, a.M, a.N, reinterpret_cast<const uint16_t*>(ws + L.sU),

@@ -19,6 +19,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "linear.h"
+#include "profile.h"
 #include "nf4_device.cuh"
 
 namespace qlora {
@@ -364,6 +365,7 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   }
   if (!ok) return QLORA_ERR_CUDA;
   dim3 grid((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM));
+  ProfileScope ps(kMode == 0 ? "fused_fwd_gemm" : "fused_dx_gemm", stream);
   fused_nf4_lora_gemm<kMode><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tA, tA2, tB2, tOut, p);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }

@@ -160,6 +160,23 @@ int nf4_level_table(float levels[16], float thresholds[15]);
  */
 int qlora_device_status(int32_t* out, void* stream);
 
+/*
+ * Opt-in per-kernel device timing (host only; a measurement aid, not thread-safe).
+ * qlora_profile_start: from now on every kernel the library launches is bracketed by CUDA
+ * events recorded on the launch's own stream.  qlora_profile_stop: waits for those events,
+ * writes one entry per kernel name (launch count, summed device milliseconds) into
+ * out[0 .. capacity), sets *count to the number of distinct kernels and turns timing off.
+ * Profiling creates CUDA events (driver objects) but never device memory.
+ */
+typedef struct qlora_kernel_time {
+  char name[48];
+  int32_t launches;
+  double total_ms;
+} qlora_kernel_time;
+
+int qlora_profile_start(void);
+int qlora_profile_stop(qlora_kernel_time* out, int32_t capacity, int32_t* count);
+
 /* Human-readable text for a status code (static storage, host only). */
 const char* qlora_status_str(int status);
 
