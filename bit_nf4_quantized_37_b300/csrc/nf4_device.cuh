@@ -77,13 +77,14 @@ __device__ __forceinline__ Nf4ByteTable nf4_make_table(float scale) {
 // the high nibble and 2j+1 in the low nibble) -> eight bf16 in element order, as four u32
 // (element 2k in the low half of out[k]).
 __device__ __forceinline__ void nf4_dequant8(const Nf4ByteTable& t, uint32_t q, uint32_t (&out)[4]) {
-  const uint32_t q4 = q << 4;
+  const uint32_t q4 = q * 16u;  // a multiply (IMAD, FMA pipe) keeps the shift off the ALU pipe
   // byte masks from bit 3 of each index, via prmt's sign-replicate mode; nibble order of a
   // half-word is [e1, e0, e3, e2] (low nibble of byte 0 first)
   const uint32_t m_lo = prmt(q4, q, 0xD9C8u);
   const uint32_t m_hi = prmt(q4, q, 0xFBEAu);
-  const uint32_t s_lo = q & 0x7777u;
-  const uint32_t s_hi = (q >> 16) & 0x7777u;
+  const uint32_t s_all = q & 0x77777777u;
+  const uint32_t s_lo = s_all;                    // prmt reads only the low 16 selector bits
+  const uint32_t s_hi = __umulhi(s_all, 0x10000u);  // s_all >> 16 as IMAD.HI (FMA pipe)
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const uint32_t s = h ? s_hi : s_lo;

@@ -38,18 +38,27 @@ int read_and_clear_gemm_error(int* out) {
 
 namespace fused {
 
-constexpr int BM = 128;
+constexpr int UM = 128;  // rows of one UMMA (cta_group::1)
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 384;
 constexpr int DEQ_WARP0 = 4;
 constexpr int NUM_DEQ_WARPS = 8;
-constexpr int TMEM_COLS = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+
+// kAcc TMEM accumulators of 128 x 256 per CTA share every dequantized W tile: the CTA tile
+// is (128 kAcc) x 256, so each dequantized weight feeds 256 kAcc FLOPs.  The byte-permute
+// dequantizer runs on the integer (ALU) pipe, which a 128-row tile saturates before the
+// tensor pipe; two accumulators halve the ALU work per FLOP.
+template <int kAcc>
+struct Tile {
+  static constexpr int BM = UM * kAcc;
+  static constexpr int STAGES = kAcc == 1 ? 4 : 3;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 256 * kAcc;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+};
 
 struct Params {
   int64_t M;      // output rows (tokens)
@@ -104,12 +113,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int kMode>  // 0: forward (W tile K-major), 1: input gradient (W tile MN-major)
+template <int kMode, int kAcc>  // kMode 0: forward (W tile K-major), 1: input gradient (MN-major)
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fused_nf4_lora_gemm(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB2,
                         const __grid_constant__ CUtensorMap tmOut, const Params p) {
+  using T = Tile<kAcc>;
+  constexpr int BM = T::BM, STAGES = T::STAGES, A_BYTES = T::A_BYTES;
+  constexpr int STAGE_BYTES = T::STAGE_BYTES, TMEM_COLS = T::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t bready_bar[STAGES];
@@ -177,7 +189,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
     if (elect_one_sync()) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, kMode);
+      constexpr uint32_t idesc = idesc_bf16_f32(UM, BN, 0, kMode);
       bool ok = true;
       for (int s = 0; s < total && ok; ++s) {
         const int slot = s % STAGES, round = s / STAGES;
@@ -189,11 +201,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t b_addr = a_addr + A_BYTES;
         const int ksteps = (s < p.n_lora && s == p.n_lora - 1) ? p.lora_last_k16 : 4;
         for (int kk = 0; kk < ksteps; ++kk) {
-          const uint64_t adesc = smem_desc(a_addr + kk * 32, 16, 1024, Swizzle::B128);
           const uint64_t bdesc = (kMode == 0)
                                      ? smem_desc(b_addr + kk * 32, 16, 1024, Swizzle::B128)
                                      : smem_desc(b_addr + kk * 2048, 8192, 1024, Swizzle::B128);
-          umma_bf16_ss<1>(tmem, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int acc = 0; acc < kAcc; ++acc) {
+            // accumulator acc: A rows 128 acc .. 128 acc + 127 (16 KB apart), TMEM columns 256 acc
+            const uint64_t adesc =
+                smem_desc(a_addr + acc * (UM * BK * 2) + kk * 32, 16, 1024, Swizzle::B128);
+            umma_bf16_ss<1>(tmem + acc * 256, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         umma_commit(&empty_bar[slot]);
       }
@@ -272,13 +289,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok && mbar_wait(&acc_bar, 0, kWaitAccFull, abort_p, &g_gemm_error)) {
       tc_fence_after();
       const int lg = warp & 3;                     // TMEM lanes 32*lg .. 32*lg+31
-      const int ch = (warp - DEQ_WARP0) >> 2;      // column half
+      const int half = (warp - DEQ_WARP0) >> 2;    // kAcc 1: column half; kAcc 2: accumulator
+      constexpr int NCHUNK = kAcc == 1 ? 4 : 8;    // 32-column chunks per warp
+      const int col0 = kAcc == 1 ? half * 128 : 0;
+      const uint32_t tbase = tmem + (kAcc == 1 ? 0u : static_cast<uint32_t>(half * 256));
+      const int64_t row0 = m0 + (kAcc == 1 ? 0 : half * UM) + lg * 32;
       uint8_t* buf0 = smem + (warp - DEQ_WARP0) * 4096;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        const int col = ch * 128 + c * 32;
+      for (int c = 0; c < NCHUNK; ++c) {
+        const int col = col0 + c * 32;
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(lg * 32) << 16) + col, v);
+        tmem_ld_32x32b_x32(tbase + (static_cast<uint32_t>(lg * 32) << 16) + col, v);
         tmem_ld_wait();
         uint8_t* buf = buf0 + (c & 1) * 2048;
         if (c >= 2) {
@@ -296,8 +317,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && n0 + col < p.Nout && m0 + lg * 32 < p.M) {
-          tma_store_2d(&tmOut, buf, (int32_t)(n0 + col), (int32_t)(m0 + lg * 32));
+        if (lane == 0 && n0 + col < p.Nout && row0 < p.M) {
+          tma_store_2d(&tmOut, buf, (int32_t)(n0 + col), (int32_t)row0);
         }
         if (lane == 0) bulk_commit();
       }
@@ -324,13 +345,14 @@ bool map_bf16(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
                             (uint64_t)outer, (uint64_t)pitch_elems * 2, box_inner, box_outer, sw);
 }
 
-template <int kMode>
+template <int kMode, int kAcc>
 int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
   using namespace fused;
+  constexpr int BM = Tile<kAcc>::BM, SMEM_BYTES = Tile<kAcc>::SMEM_BYTES;
   static bool attr_set = false;  // per process; the attribute is per function
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fused_nf4_lora_gemm<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(fused_nf4_lora_gemm<kMode, kAcc>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
       return QLORA_ERR_CUDA;
     attr_set = true;
   }
@@ -366,18 +388,24 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   if (!ok) return QLORA_ERR_CUDA;
   dim3 grid((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM));
   ProfileScope ps(kMode == 0 ? "fused_fwd_gemm" : "fused_dx_gemm", stream);
-  fused_nf4_lora_gemm<kMode><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tA, tA2, tB2, tOut, p);
+  fused_nf4_lora_gemm<kMode, kAcc><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tA, tA2, tB2, tOut, p);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
 }  // namespace
 
+// Two accumulators per CTA when the 256 x 256 tiles still give every SM work, else one.
+static bool use_two_acc(int64_t M, int64_t Nout) {
+  const int64_t tiles = ((M + 255) / 256) * ((Nout + 255) / 256);
+  return tiles >= num_sms();
+}
+
 int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  return launch_fused<0>(a, L, stream);
+  return use_two_acc(a.M, a.N) ? launch_fused<0, 2>(a, L, stream) : launch_fused<0, 1>(a, L, stream);
 }
 
 int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  return launch_fused<1>(a, L, stream);
+  return use_two_acc(a.M, a.K) ? launch_fused<1, 2>(a, L, stream) : launch_fused<1, 1>(a, L, stream);
 }
 
 }  // namespace qlora

@@ -148,6 +148,16 @@ def test_fwd_bwd_small(name, M, N, K, r, alpha):
     _check_bwd(pb, None)  # U recomputed in the backward
 
 
+@pytest.mark.parametrize("M,N,K,r", [(2000, 4800, 320, 24),    # forward takes 256-row tiles
+                                     (2000, 320, 4800, 40)])   # input gradient takes them
+def test_two_accumulator_tiles_ragged(M, N, K, r):
+    p = wl.LinearProblem(f"twoacc-{M}-{N}-{K}", M, N, K, r, 2.0 * r, 0.02, 0.001, config=60 + r)
+    pb = Problem(p)
+    rows = _sample_rows(M, 20, r)
+    Y, U = _check_fwd(pb, rows)
+    _check_bwd(pb, U, rows)
+
+
 def test_zero_b_equals_base_matmul():
     pb = Problem(wl.config1(b_zero=True))
     p = pb.p
