@@ -15,13 +15,14 @@ NF4_DQ_BLOCK = 256
 
 _STATUS = {0: "QLORA_OK", -1: "QLORA_ERR_INVALID_ARG", -2: "QLORA_ERR_UNSUPPORTED",
            -3: "QLORA_ERR_MISALIGNED", -4: "QLORA_ERR_WORKSPACE", -5: "QLORA_ERR_CUDA",
-           -6: "QLORA_ERR_DEVICE_TIMEOUT", -7: "QLORA_ERR_NO_DEVICE"}
+           -6: "QLORA_ERR_DEVICE_TIMEOUT", -7: "QLORA_ERR_NO_DEVICE", -8: "QLORA_ERR_TOO_LARGE"}
+NF4_NOALLOC_MAX_NUMEL = 1 << 26
 
 # Every symbol include/qlora_nf4.h declares.
 EXPORTS = ["nf4_storage_bytes", "nf4_quantize_workspace_bytes", "nf4_quantize",
            "nf4_dequantize", "qlora_workspace_bytes", "qlora_linear_fwd", "qlora_linear_bwd",
            "nf4_level_table", "qlora_device_status", "qlora_status_str", "qlora_version",
-           "qlora_profile_start", "qlora_profile_stop"]
+           "qlora_profile_start", "qlora_profile_stop", "nf4_quantize_noalloc"]
 
 
 class QLoRAError(RuntimeError):
@@ -67,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "qlora_version": [],
             "qlora_profile_start": [],
             "qlora_profile_stop": [vp, i32, vp],
+            "nf4_quantize_noalloc": [vp, sp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -190,6 +192,16 @@ def nf4_quantize(W: torch.Tensor, out: NF4Tensor | None = None,
     _check("nf4_quantize", lib().nf4_quantize(_ptr(W), ctypes.byref(s), _ptr(ws),
                                               ws.numel() * ws.element_size(), _stream()))
     return q
+
+
+def nf4_quantize_noalloc(W: torch.Tensor, out: NF4Tensor) -> NF4Tensor:
+    """nf4_quantize for callers that must not allocate device memory: the output buffers
+    are the caller's and the scratch is the library's fixed device array (up to
+    NF4_NOALLOC_MAX_NUMEL weights).  Calls overlapping on the GPU race on that array."""
+    _req(W, torch.float32, "W")
+    s = out.c_struct()
+    _check("nf4_quantize_noalloc", lib().nf4_quantize_noalloc(_ptr(W), ctypes.byref(s), _stream()))
+    return out
 
 
 def nf4_dequantize(q: NF4Tensor, out: torch.Tensor | None = None) -> torch.Tensor:

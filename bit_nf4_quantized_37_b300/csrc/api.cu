@@ -55,6 +55,7 @@ const char* qlora_status_str(int status) {
     case QLORA_ERR_CUDA: return "CUDA runtime or launch error";
     case QLORA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
     case QLORA_ERR_NO_DEVICE: return "current device is not compute capability 10.3";
+    case QLORA_ERR_TOO_LARGE: return "tensor exceeds the fixed scratch of the no-allocation call";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,83 @@
+// noalloc.cu -- nf4_quantize_noalloc: the NF4 quantizer with its scratch in a fixed
+// library-owned device array instead of a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they quantize: a plugin
+// running inside a host application that owns every device allocation through its own
+// pool, or a service that reserves all of its memory at start-up and must never call
+// cudaMalloc (with its implicit synchronization and its chance of failing) on the request
+// path.  They pass only W and the output buffers; the absmax values and group sums the
+// quantizer needs between its passes live in g_noalloc_quant_scratch below.
+//
+// The array is a file-scope __device__ variable, so every GPU that loads the library holds
+// it (about 4.2 MB) until the process exits.  Host code cannot hand the symbol itself to a
+// kernel (on the host it is only a stand-in), so the first call on each device looks up
+// its device address with cudaGetSymbolAddress while that device is current and caches it.
+// Every call shares the array and it keeps the last call's contents; the quantizer writes
+// every scratch entry it later reads, so nothing needs clearing between calls.  Calls that
+// overlap on the GPU (for instance on two streams) race on the array.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace qlora {
+namespace {
+
+constexpr int64_t kNoallocMaxNumel = NF4_NOALLOC_MAX_NUMEL;
+// absmax fp32 for whole groups of 256 blocks, one fp64 sum per group, 256 bytes of slack:
+// the same layout the workspace of nf4_quantize uses
+constexpr uint64_t kNoallocScratchBytes =
+    ((kNoallocMaxNumel + 64 * 256 - 1) / (64 * 256)) * (256 * 4 + 8) + 256;
+
+__device__ __align__(256) unsigned char g_noalloc_quant_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once per device).
+int scratch_for_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QLORA_ERR_NO_DEVICE;
+  if (dev < 0 || dev >= kMaxDevices) return QLORA_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_quant_scratch) != cudaSuccess || !p)
+      return QLORA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return QLORA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace qlora
+
+using namespace qlora;
+
+extern "C" int nf4_quantize_noalloc(const float* W, const nf4_tensor* out, void* stream) {
+  if (!out || !W) return QLORA_ERR_INVALID_ARG;
+  if (out->rows < 1 || out->cols < 1) return QLORA_ERR_INVALID_ARG;
+  if (out->blocksize != NF4_BLOCKSIZE || out->dq_block != NF4_DQ_BLOCK) return QLORA_ERR_UNSUPPORTED;
+  if (!out->codes || !out->scale_codes || !out->scale_steps || !out->scale_mean)
+    return QLORA_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(out->codes) || !aligned16(out->scale_codes) ||
+      !aligned16(out->scale_steps) || !aligned16(out->scale_mean))
+    return QLORA_ERR_MISALIGNED;
+  if (out->rows > kNoallocMaxNumel / out->cols) return QLORA_ERR_TOO_LARGE;
+  const int64_t numel = out->rows * out->cols;
+  if (quantize_workspace_bytes(numel) > kNoallocScratchBytes) return QLORA_ERR_TOO_LARGE;
+  int major = 0, minor = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      major != 10 || minor != 3)
+    return QLORA_ERR_NO_DEVICE;
+  void* scratch = nullptr;
+  const int st = scratch_for_current_device(&scratch);
+  if (st) return st;
+  return launch_quantize(W, numel, *out, scratch, static_cast<cudaStream_t>(stream));
+}

@@ -46,6 +46,8 @@ extern "C" {
                                          qlora_device_status)                            */
 #define QLORA_ERR_NO_DEVICE (-7)      /* current device is not a compute-capability 10.3
                                          GPU                                             */
+#define QLORA_ERR_TOO_LARGE (-8)      /* tensor larger than nf4_quantize_noalloc's fixed
+                                         scratch allows (NF4_NOALLOC_MAX_NUMEL)          */
 
 #define NF4_BLOCKSIZE 64  /* weights per first-level block (one absmax scale each)   */
 #define NF4_DQ_BLOCK 256  /* first-level scales per second-level (double-quant) group */
@@ -103,6 +105,23 @@ int nf4_quantize_workspace_bytes(int64_t numel, uint64_t* out);
  */
 int nf4_quantize(const float* W, const nf4_tensor* out, void* workspace,
                  uint64_t workspace_bytes, void* stream);
+
+/*
+ * nf4_quantize without a workspace argument, for callers that must not allocate device
+ * memory when they quantize: a plugin inside a host application that owns every device
+ * allocation, or a service that reserves its memory at start-up and keeps cudaMalloc (and
+ * its implicit synchronization) off the request path.  The QLoRA pages have no counterpart
+ * to this call; it computes exactly what nf4_quantize computes (bit-identical outputs).
+ * Its scratch is a file-scope device array of the library sized for NF4_NOALLOC_MAX_NUMEL
+ * weights (about 4.2 MB, held by every GPU that loads the library until exit); the call
+ * itself allocates nothing.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current, so make that first call before any
+ * stream capture.  All calls share the array: calls that overlap on the GPU (for example on
+ * two streams) race and must be ordered by the caller.  rows * cols above
+ * NF4_NOALLOC_MAX_NUMEL returns QLORA_ERR_TOO_LARGE with nothing enqueued.
+ */
+#define NF4_NOALLOC_MAX_NUMEL 67108864LL /* 2^26 weights, e.g. one 8192 x 8192 matrix */
+int nf4_quantize_noalloc(const float* W, const nf4_tensor* out, void* stream);
 
 /*
  * Dequantize an nf4_tensor to bf16 W_out [rows*cols] (device), bit-exactly the rule in
