@@ -15,7 +15,6 @@ namespace qlora {
 WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r) {
   WorkspaceLayout L{};
   L.rp = round_up(r, 64);
-  const int64_t Mp = round_up(M, 64);
   uint64_t off = 0;
   auto take = [&](uint64_t bytes) {
     const uint64_t at = off;
@@ -24,13 +23,12 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r) {
   };
   L.sU = take((uint64_t)M * L.rp * 2);
   L.sV = take((uint64_t)M * L.rp * 2);
-  L.Ut = take((uint64_t)L.rp * Mp * 2);
-  L.Vt = take((uint64_t)L.rp * Mp * 2);
-  L.Bp = take((uint64_t)N * L.rp * 2);
-  L.Bt = take((uint64_t)L.rp * N * 2);
-  L.Ap = take((uint64_t)L.rp * K * 2);
+  L.U32 = take((uint64_t)M * r * 4);
+  L.Bp = take(r % 8 ? (uint64_t)N * L.rp * 2 : 0);
   L.part_bytes = std::max(side_partial_bytes(M, N, K, r), skinny_partial_bytes(M, N, K));
   L.part = take(L.part_bytes);
+  L.ntickets = side_ticket_count(M, N, K);
+  L.tickets = take(L.ntickets * 4);
   L.total = off;
   return L;
 }
@@ -39,22 +37,35 @@ uint64_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int r) {
   return workspace_layout(M, N, K, r).total;
 }
 
+static int clear_tickets(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+  return cudaMemsetAsync(static_cast<uint8_t*>(a.ws) + L.tickets, 0, L.ntickets * 4, stream) ==
+                 cudaSuccess
+             ? QLORA_OK
+             : QLORA_ERR_CUDA;
+}
+
 int linear_forward(const LinearArgs& a, cudaStream_t stream) {
   const WorkspaceLayout L = workspace_layout(a.M, a.N, a.K, a.r);
-  int st = launch_pad_adapters(a, L, false, stream);
+  int st = clear_tickets(a, L, stream);
   if (st) return st;
-  if ((st = launch_lora_u(a, L, stream))) return st;
+  if ((st = launch_lora_u(a, L, a.U, stream))) return st;
   if (a.M <= kSkinnyMaxM) return launch_skinny_fwd(a, L, stream);
+  if (a.r % 8 && (st = launch_pad_b(a, L, stream))) return st;
   return launch_fused_fwd(a, L, stream);
 }
 
 int linear_backward(const LinearArgs& a, cudaStream_t stream) {
   const WorkspaceLayout L = workspace_layout(a.M, a.N, a.K, a.r);
-  int st = launch_pad_adapters(a, L, true, stream);
+  int st = clear_tickets(a, L, stream);
   if (st) return st;
-  if ((st = launch_u_from_saved(a, L, stream))) return st;
+  const float* u32 = a.U_in;
+  if (!u32) {
+    float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + L.U32);
+    if ((st = launch_lora_u(a, L, w, stream))) return st;
+    u32 = w;
+  }
   if ((st = launch_lora_v(a, L, stream))) return st;
-  if ((st = launch_lora_db(a, L, stream))) return st;
+  if ((st = launch_lora_db(a, L, u32, stream))) return st;
   if (a.dX && (st = launch_fused_dx(a, L, stream))) return st;
   return launch_lora_da(a, L, stream);
 }

@@ -36,15 +36,14 @@ struct LinearArgs {
 // Workspace regions (byte offsets, each 1024-aligned), for rank padded to rp = 64*ceil(r/64).
 struct WorkspaceLayout {
   int64_t rp;
-  uint64_t sU;      // bf16 [M, rp]   scale * U, zero columns past r
-  uint64_t sV;      // bf16 [M, rp]   scale * V
-  uint64_t Ut;      // bf16 [rp, Mp]  U transposed (Mp = M rounded up to 64)
-  uint64_t Vt;      // bf16 [rp, Mp]  V transposed
-  uint64_t Bp;      // bf16 [N, rp]   B zero-padded
-  uint64_t Bt;      // bf16 [rp, N]   B transposed, zero rows past r
-  uint64_t Ap;      // bf16 [rp, K]   A zero-padded rows
-  uint64_t part;    // fp32 split-contraction partial sums (side products and decode path)
+  uint64_t sU;       // bf16 [M, rp]  scale * U, zero columns past r
+  uint64_t sV;       // bf16 [M, rp]  scale * V
+  uint64_t U32;      // fp32 [M, r]   U recomputed by the backward when none is saved
+  uint64_t Bp;       // bf16 [N, rp]  B zero-padded (only for r not a multiple of 8)
+  uint64_t part;     // fp32 split-contraction partial sums (side products, decode path)
   uint64_t part_bytes;
+  uint64_t tickets;  // int [ntickets] arrival counters of the split reductions
+  uint64_t ntickets;
   uint64_t total;
 };
 
@@ -61,15 +60,16 @@ int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t
 int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 // Decode path (M <= 16): Y = X W'^T + sU Bp^T with the weights streamed once.
 int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
-// Rank-r side products on the tensor cores (mma.sync), split over the contraction.
-int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+// Rank-r side products on the tensor cores (mma.sync), split over the contraction, with the
+// split reduction done by the last CTA of each row tile (lora_side.cu).
+int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cudaStream_t stream);
 int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
-int launch_lora_db(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+int launch_lora_db(const LinearArgs& a, const WorkspaceLayout& L, const float* u32,
+                   cudaStream_t stream);
 int launch_lora_da(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
-int launch_pad_adapters(const LinearArgs& a, const WorkspaceLayout& L, bool need_bt,
-                        cudaStream_t stream);
-int launch_u_from_saved(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+int launch_pad_b(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 uint64_t side_partial_bytes(int64_t M, int64_t N, int64_t K, int r);
+uint64_t side_ticket_count(int64_t M, int64_t N, int64_t K);
 uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K);
 
 }  // namespace qlora

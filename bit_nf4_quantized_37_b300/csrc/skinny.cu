@@ -141,11 +141,11 @@ __global__ void __launch_bounds__(THREADS) nf4_decode_gemv(
   }
 }
 
-// Y[m][n] = bf16( sum_s part[s][m][n] + sum_j sU[m][j] Bp[n][j] ), splits in order.
+// Y[m][n] = bf16( sum_s part[s][m][n] + sum_j sU[m][j] B[n][j] ), splits in order.
 __global__ void __launch_bounds__(256) decode_finalize(const float* __restrict__ part, int S,
                                                       int64_t M, int64_t N,
                                                       const uint16_t* __restrict__ sU,
-                                                      const uint16_t* __restrict__ Bp, int r,
+                                                      const uint16_t* __restrict__ B, int r,
                                                       int64_t rp, uint16_t* __restrict__ Y) {
   extern __shared__ float su[];  // [M][r]
   for (int i = threadIdx.x; i < M * r; i += blockDim.x) {
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(256) decode_finalize(const float* __restrict__
     for (int s = 0; s < S; ++s) v += part[((int64_t)s * M + m) * N + n];
     float l = 0.f;
     for (int j = 0; j < r; ++j)
-      l = fmaf(su[m * r + j], __bfloat162float(__ushort_as_bfloat16(Bp[n * rp + j])), l);
+      l = fmaf(su[m * r + j], __bfloat162float(__ushort_as_bfloat16(B[n * r + j])), l);
     Y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v + l));
   }
 }
@@ -211,7 +211,7 @@ int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_
   const int fsmem = static_cast<int>(a.M * a.r * 4);
   skinny::decode_finalize<<<(unsigned)((a.N + 255) / 256), 256, fsmem, stream>>>(
       part, (int)S, a.M, a.N, reinterpret_cast<const uint16_t*>(ws + L.sU),
-      reinterpret_cast<const uint16_t*>(ws + L.Bp), a.r, L.rp, a.Y);
+      a.B, a.r, L.rp, a.Y);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 

@@ -6,8 +6,8 @@
 // 64-wide k-slice straight into the shared-memory operand tile of tcgen05.mma, so W' never
 // exists in HBM.  The rank-r LoRA term rides in the same TMEM accumulator as extra
 // contraction stages in front of the NF4 stages:
-//   forward          Y  = [X  | sU] . [W' | Bp]^T      (contract over K, then over r)
-//   input gradient   dX = [dY | sV] . [W' ; Ap]        (contract over N, then over r)
+//   forward          Y  = [X  | sU] . [W' | B]^T       (contract over K, then over r)
+//   input gradient   dX = [dY | sV] . [W' ; A]         (contract over N, then over r)
 //
 // CTA tile 128 x 256 (UMMA M x N), k-slice 64, 4-stage ring.  Warp roles (384 threads):
 //   warp 0      TMA producer: X/dY tiles, and for the LoRA stages both operands
@@ -375,14 +375,16 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
     p.Kc = a.K;
     ok = map_bf16(&tA, a.X, a.K, a.M, a.K, 64, BM, MapSwizzle::B128) &&
          map_bf16(&tA2, ws + L.sU, rp, a.M, rp, 64, BM, MapSwizzle::B128) &&
-         map_bf16(&tB2, ws + L.Bp, rp, a.N, rp, 64, BN, MapSwizzle::B128) &&
+         (a.r % 8 == 0  // B [N, r] itself; TMA fills the columns past r with zeros
+              ? map_bf16(&tB2, a.B, a.r, a.N, a.r, 64, BN, MapSwizzle::B128)
+              : map_bf16(&tB2, ws + L.Bp, rp, a.N, rp, 64, BN, MapSwizzle::B128)) &&
          map_bf16(&tOut, a.Y, a.N, a.M, a.N, 32, 32, MapSwizzle::B64);
   } else {
     p.Nout = a.K;
     p.Kc = a.N;
     ok = map_bf16(&tA, a.dY, a.N, a.M, a.N, 64, BM, MapSwizzle::B128) &&
          map_bf16(&tA2, ws + L.sV, rp, a.M, rp, 64, BM, MapSwizzle::B128) &&
-         map_bf16(&tB2, ws + L.Ap, a.K, rp, a.K, 64, 64, MapSwizzle::B128) &&
+         map_bf16(&tB2, a.A, a.K, a.r, a.K, 64, 64, MapSwizzle::B128) &&  // rows past r: zeros
          map_bf16(&tOut, a.dX, a.K, a.M, a.K, 32, 32, MapSwizzle::B64);
   }
   if (!ok) return QLORA_ERR_CUDA;

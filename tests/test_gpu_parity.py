@@ -136,6 +136,9 @@ SMALL = [
     ("tokens1", 1, 576, 320, 8, 16.0),
     ("tokens5", 5, 256, 1024, 64, 16.0),
     ("multi_tile", 520, 1024, 1088, 16, 32.0),
+    ("rank12", 150, 256, 320, 12, 24.0),     # rank not a multiple of 8: padded B path
+    ("rank3", 40, 192, 128, 3, 6.0),
+    ("tokens9_rank13", 9, 320, 256, 13, 26.0),
 ]
 
 
