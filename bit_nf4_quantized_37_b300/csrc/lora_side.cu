@@ -83,6 +83,104 @@ struct Epi {
   float scale_op;
 };
 
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Stage Q(c, j), c in [c_begin, c_begin + clen), into sQ[c][j] (pitch NJ + 8).  Three vector
+// layouts of the source: bf16 contiguous along c (A[j][k]), bf16 contiguous along j (B[n][j],
+// sV[m][j]) and fp32 contiguous along j (U[m][j]); anything else element by element.
+template <int NJ>
+__device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int64_t C,
+                                        int64_t c_begin, int clen, int tid) {
+  constexpr int QP = NJ + 8;
+  constexpr int BATCH = 8;
+  const uint16_t* b16 = static_cast<const uint16_t*>(qs.ptr);
+  const float* f32 = static_cast<const float*>(qs.ptr);
+  if (!qs.fp32 && qs.ldc == 1 && (qs.ldj % 8) == 0 && (c_begin % 8) == 0) {
+    // A[j][c]: 8 consecutive c per load, scattered into 8 rows of sQ
+    const int per_j = clen / 8, n = NJ * per_j;
+    for (int base = tid; base < n; base += BATCH * THREADS) {
+      uint4 v[BATCH];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int idx = base + u * THREADS;
+        const int j = idx / per_j, c8 = idx % per_j;
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (idx < n && j < r && c_begin + 8 * c8 < C)
+          v[u] = __ldg(reinterpret_cast<const uint4*>(b16 + (int64_t)j * qs.ldj + c_begin + 8 * c8));
+      }
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int idx = base + u * THREADS;
+        if (idx >= n) break;
+        const int j = idx / per_j, c8 = idx % per_j;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          sQ[(8 * c8 + e) * QP + j] = static_cast<uint16_t>(w[e >> 1] >> (16 * (e & 1)));
+      }
+    }
+  } else if (!qs.fp32 && qs.ldj == 1 && (qs.ldc % 8) == 0 && (r % 8) == 0) {
+    // src[c][j]: one 16-byte row piece of 8 j per load
+    constexpr int J8 = NJ / 8;
+    const int n = clen * J8;
+    for (int base = tid; base < n; base += BATCH * THREADS) {
+      uint4 v[BATCH];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int idx = base + u * THREADS;
+        const int c = idx / J8, j8 = idx % J8;
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (idx < n && 8 * j8 < r && c_begin + c < C)
+          v[u] = __ldg(reinterpret_cast<const uint4*>(b16 + (c_begin + c) * qs.ldc + 8 * j8));
+      }
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int idx = base + u * THREADS;
+        if (idx >= n) break;
+        const int c = idx / J8, j8 = idx % J8;
+        *reinterpret_cast<uint4*>(sQ + c * QP + 8 * j8) = v[u];
+      }
+    }
+  } else if (qs.fp32 && qs.ldj == 1 && (qs.ldc % 4) == 0 && (r % 4) == 0) {
+    // fp32 src[c][j]: 4 j per load, converted to bf16
+    constexpr int J4 = NJ / 4;
+    const int n = clen * J4;
+    for (int base = tid; base < n; base += BATCH * THREADS) {
+      float4 v[BATCH];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int idx = base + u * THREADS;
+        const int c = idx / J4, j4 = idx % J4;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (idx < n && 4 * j4 < r && c_begin + c < C)
+          v[u] = __ldg(reinterpret_cast<const float4*>(f32 + (c_begin + c) * qs.ldc + 4 * j4));
+      }
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int idx = base + u * THREADS;
+        if (idx >= n) break;
+        const int c = idx / J4, j4 = idx % J4;
+        *reinterpret_cast<uint2*>(sQ + c * QP + 4 * j4) =
+            make_uint2(pack2_bf16(v[u].x, v[u].y), pack2_bf16(v[u].z, v[u].w));
+      }
+    }
+  } else {
+    for (int i = tid; i < clen * NJ; i += THREADS) {
+      const int c = i / NJ, j = i % NJ;
+      const int64_t gc = c_begin + c;
+      float v = 0.f;
+      if (j < r && gc < C) {
+        const int64_t off = gc * qs.ldc + (int64_t)j * qs.ldj;
+        v = qs.fp32 ? __ldg(f32 + off) : __bfloat162float(__ushort_as_bfloat16(__ldg(b16 + off)));
+      }
+      sQ[c * QP + j] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+  }
+}
+
 template <bool kPCol, int NJ>
 __global__ void __launch_bounds__(THREADS, 1)
     side_gemm(const uint16_t* __restrict__ P, int64_t R, int64_t C, int64_t ldp, QSrc qs, int r,
@@ -123,20 +221,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (st < nst) load_P(st);
     cp_async_commit();
   }
-  // rank-r operand for the whole contraction range, as [c][j] bf16
-  const int clen = static_cast<int>(c_end - c_begin);
-  const bool c_fast = qs.ldc == 1;  // walk the source's contiguous index across threads
-  for (int i = tid; i < clen * NJ; i += THREADS) {
-    const int c = c_fast ? i % clen : i / NJ, j = c_fast ? i / clen : i % NJ;
-    const int64_t gc = c_begin + c;
-    float v = 0.f;
-    if (j < r && gc < C) {
-      const int64_t off = gc * qs.ldc + (int64_t)j * qs.ldj;
-      v = qs.fp32 ? __ldg(static_cast<const float*>(qs.ptr) + off)
-                  : __bfloat162float(__ushort_as_bfloat16(__ldg(static_cast<const uint16_t*>(qs.ptr) + off)));
-    }
-    sQ[c * QP + j] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  }
+  // rank-r operand for the whole contraction range, as [c][j] bf16 (zero past the rank),
+  // loaded with 16-byte vectors in batches of 8 per thread so the loads overlap
+  stage_q<NJ>(sQ, qs, r, C, c_begin, static_cast<int>(c_end - c_begin), tid);
 
   float acc[NJ / 8][4];
 #pragma unroll
@@ -190,19 +277,45 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (!s_last) return;
   __threadfence();
 
-  // last CTA of this row tile: fixed-order sum over the splits, then the outputs
-  const int cols = epi.op ? (epi.op_cols > NJ ? epi.op_cols : NJ) : NJ;
-  for (int i = tid; i < TR * cols; i += THREADS) {
-    const int lr = i / cols, j = i % cols;
+  // last CTA of this row tile: fixed-order sum over the splits (float4 pieces, the S loads of
+  // a piece in flight together), then the outputs
+  constexpr int V4 = NJ / 4;
+  for (int i = tid; i < TR * V4; i += THREADS) {
+    const int lr = i / V4, j0 = (i % V4) * 4;
     const int64_t row = r0 + lr;
     if (row >= R) continue;
-    float v = 0.f;
-    if (j < NJ)
-      for (int s = 0; s < S; ++s) v += __ldcg(part + ((int64_t)s * R + row) * NJ + j);
-    if (j >= r) v = 0.f;
-    if (epi.out32 && j < r) epi.out32[row * epi.ld_row + j * epi.ld_j] = v * epi.scale32;
-    if (epi.op && j < epi.op_cols)
-      epi.op[row * epi.ld_op + j] = __bfloat16_as_ushort(__float2bfloat16_rn(v * epi.scale_op));
+    const float4* src = reinterpret_cast<const float4*>(part + row * NJ + j0);
+    const int64_t sstride = R * NJ / 4;  // float4 stride between splits
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 4 <= S; s += 4) {
+      const float4 a0 = __ldcg(src + (s + 0) * sstride), a1 = __ldcg(src + (s + 1) * sstride);
+      const float4 a2 = __ldcg(src + (s + 2) * sstride), a3 = __ldcg(src + (s + 3) * sstride);
+      v.x += a0.x; v.y += a0.y; v.z += a0.z; v.w += a0.w;
+      v.x += a1.x; v.y += a1.y; v.z += a1.z; v.w += a1.w;
+      v.x += a2.x; v.y += a2.y; v.z += a2.z; v.w += a2.w;
+      v.x += a3.x; v.y += a3.y; v.z += a3.z; v.w += a3.w;
+    }
+    for (; s < S; ++s) {
+      const float4 a = __ldcg(src + s * sstride);
+      v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+    }
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j0 + e;
+      const float x = j < r ? vv[e] : 0.f;
+      if (epi.out32 && j < r) epi.out32[row * epi.ld_row + j * epi.ld_j] = x * epi.scale32;
+      if (epi.op && j < epi.op_cols)
+        epi.op[row * epi.ld_op + j] = __bfloat16_as_ushort(__float2bfloat16_rn(x * epi.scale_op));
+    }
+  }
+  if (epi.op && epi.op_cols > NJ) {  // zero columns of the operand copy past NJ
+    const int extra = epi.op_cols - NJ;
+    for (int i = tid; i < TR * extra; i += THREADS) {
+      const int64_t row = r0 + i / extra;
+      if (row < R) epi.op[row * epi.ld_op + NJ + i % extra] = 0;
+    }
   }
   if (tid == 0) tickets[blockIdx.x] = 0;  // ready for the next launch
 }
