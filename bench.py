@@ -162,6 +162,7 @@ def oracle_sample(p, X, Wd, A, B, dY, target_s: float = 12.0):
         t1 = time.perf_counter()
         return t1 - t0
 
+    run(2)  # thread-pool start-up outside the calibration
     t_rows = run(8) / 8
     t0 = time.perf_counter()
     oracle.lora_dadb(dY, X, A, B, p.scale)
@@ -230,6 +231,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="no CUDA graph for the timed step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -264,6 +266,30 @@ def main():
         step()
     torch.cuda.synchronize()
 
+    # The timed step is one CUDA-graph replay of forward + backward (the library's launches
+    # captured once; per-kernel CUDA events are captured with them, so the profile below is
+    # the device time of each kernel in the last timed replay).  --eager times the calls
+    # as issued from Python instead.
+    graph = None
+    if not args.eager:
+        qn.profile_start()  # fill the event pool before capture
+        step()
+        torch.cuda.synchronize()
+        qn.profile_stop()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        qn.profile_start()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+
     clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
     if clocks:
         clocks.start()
@@ -271,11 +297,15 @@ def main():
           for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
-    qn.profile_start()
+    if graph is None:
+        qn.profile_start()
     for i in range(args.steps):
         flush_buf.zero_()
         ev[i][0].record()
-        step()
+        if graph is None:
+            step()
+        else:
+            graph.replay()
         ev[i][1].record()
     torch.cuda.synchronize()
     barrier(world)
@@ -285,7 +315,7 @@ def main():
     total_ms = max_over_ranks(sum(step_ms), world)
     flops_step = p.fwd_bwd_flops()
     value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
-    launches = sum(v[0] for v in prof.values())
+    launches = sum(v[0] for v in prof.values()) * (args.steps if graph is not None else 1)
 
     # dominant kernel and its roofline (algorithmic FLOPs per launch / mean launch time)
     dom = max(prof.items(), key=lambda kv: kv[1][1])
@@ -362,6 +392,7 @@ def main():
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
+        "timed_step": "eager calls" if graph is None else "CUDA graph replay of fwd + bwd",
         "clocks": clk,
         "secondary": secondary,
     }

@@ -377,8 +377,14 @@ int run_side(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t 
   switch (NJ) {
 #define QLORA_SIDE_CASE(nj)                                                                       \
   case nj:                                                                                        \
-    cudaFuncSetAttribute(side::side_gemm<kCol, nj>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
-                         smem);                                                                   \
+    {                                                                                             \
+      static bool attr = false; /* once per instantiation: the largest configuration */          \
+      if (!attr)                                                                                  \
+        attr = cudaFuncSetAttribute(side::side_gemm<kCol, nj>,                                     \
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,                  \
+                                    side::STAGES * side::P_STAGE_BYTES + side::Q_SMEM_MAX + 1024) \
+               == cudaSuccess;                                                                    \
+    }                                                                                             \
     side::side_gemm<kCol, nj><<<grid, side::THREADS, smem, stream>>>(P, R, C, ldp, qs, r, part,     \
                                                                      tickets, sp.chunk, sp.S, epi); \
     break;

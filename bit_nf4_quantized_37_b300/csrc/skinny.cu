@@ -197,9 +197,13 @@ int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_
   const int64_t S = (a.K + ks - 1) / ks;
   float* part = reinterpret_cast<float*>(ws + L.part);
   const int smem = static_cast<int>(16 * ks * 2);
-  if (cudaFuncSetAttribute(skinny::nf4_decode_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem) != cudaSuccess)
-    return QLORA_ERR_CUDA;
+  static bool attr = false;  // once: the largest X tile (2048 columns of 16 tokens)
+  if (!attr) {
+    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             16 * 2048 * 2) != cudaSuccess)
+      return QLORA_ERR_CUDA;
+    attr = true;
+  }
   dim3 grid((unsigned)((a.N + skinny::ROWS_PER_CTA - 1) / skinny::ROWS_PER_CTA), (unsigned)S);
   {
   ProfileScope ps("decode_gemv", stream);
