@@ -41,7 +41,8 @@ ProfileScope::ProfileScope(const char* name, cudaStream_t stream) : name_(name),
   if (!g_on) return;
   std::lock_guard<std::mutex> lk(g_mu);
   start_ = take_event();
-  if (start_) cudaEventRecord(start_, stream_);
+  // external: inside a stream capture this becomes a real event-record node of the graph
+  if (start_) cudaEventRecordWithFlags(start_, stream_, cudaEventRecordExternal);
 }
 
 ProfileScope::~ProfileScope() {
@@ -49,7 +50,7 @@ ProfileScope::~ProfileScope() {
   std::lock_guard<std::mutex> lk(g_mu);
   cudaEvent_t stop = take_event();
   if (!stop) return;
-  cudaEventRecord(stop, stream_);
+  cudaEventRecordWithFlags(stop, stream_, cudaEventRecordExternal);
   g_recs.push_back({name_, start_, stop});
 }
 
