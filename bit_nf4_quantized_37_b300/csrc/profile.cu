@@ -22,6 +22,17 @@ bool g_on = false;
 std::vector<Rec> g_recs;
 std::vector<cudaEvent_t> g_pool;
 
+// Inside a stream capture an event record must be "external" to become a real event-record
+// node of the graph (a plain record only marks a capture dependency); outside a capture
+// the plain record is the valid form.
+void record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 cudaEvent_t take_event() {
   if (!g_pool.empty()) {
     cudaEvent_t e = g_pool.back();
@@ -41,8 +52,7 @@ ProfileScope::ProfileScope(const char* name, cudaStream_t stream) : name_(name),
   if (!g_on) return;
   std::lock_guard<std::mutex> lk(g_mu);
   start_ = take_event();
-  // external: inside a stream capture this becomes a real event-record node of the graph
-  if (start_) cudaEventRecordWithFlags(start_, stream_, cudaEventRecordExternal);
+  if (start_) record(start_, stream_);
 }
 
 ProfileScope::~ProfileScope() {
@@ -50,7 +60,7 @@ ProfileScope::~ProfileScope() {
   std::lock_guard<std::mutex> lk(g_mu);
   cudaEvent_t stop = take_event();
   if (!stop) return;
-  cudaEventRecordWithFlags(stop, stream_, cudaEventRecordExternal);
+  record(stop, stream_);
   g_recs.push_back({name_, start_, stop});
 }
 
