@@ -20,25 +20,28 @@
 #include "profile.h"
 
 namespace qlora {
+
+// Device error word of the side kernels (bounded waits that gave up).
+__device__ int g_side_error = 0;
+
+int read_and_clear_side_error(int* out) {
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_side_error, sizeof(int)) != cudaSuccess) return QLORA_ERR_CUDA;
+  if (v && cudaMemcpyToSymbol(g_side_error, &zero, sizeof(int)) != cudaSuccess) return QLORA_ERR_CUDA;
+  *out = v;
+  return QLORA_OK;
+}
+
 namespace side {
 
 constexpr int THREADS = 256;  // 8 warps x 16 rows
 constexpr int TR = 128;       // rows per CTA
 constexpr int TC = 64;        // contraction per stage
-constexpr int STAGES = 6;
+constexpr int STAGES = 8;
 constexpr int P_STAGE_BYTES = TR * TC * 2;
-constexpr int Q_SMEM_MAX = 72 * 1024;
+constexpr int Q_SMEM_MAX = 64 * 1024;
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
-  const int n = valid ? 16 : 0;  // src-size 0 zero-fills the 16 bytes
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -106,7 +109,7 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
 #pragma unroll
       for (int u = 0; u < BATCH; ++u) {
         const int idx = base + u * THREADS;
-        const int j = idx / per_j, c8 = idx % per_j;
+        const int c8 = idx / NJ, j = idx % NJ;  // consecutive threads: consecutive j (smem)
         v[u] = make_uint4(0, 0, 0, 0);
         if (idx < n && j < r && c_begin + 8 * c8 < C)
           v[u] = __ldg(reinterpret_cast<const uint4*>(b16 + (int64_t)j * qs.ldj + c_begin + 8 * c8));
@@ -115,7 +118,7 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
       for (int u = 0; u < BATCH; ++u) {
         const int idx = base + u * THREADS;
         if (idx >= n) break;
-        const int j = idx / per_j, c8 = idx % per_j;
+        const int c8 = idx / NJ, j = idx % NJ;
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -183,13 +186,19 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
 
 template <bool kPCol, int NJ>
 __global__ void __launch_bounds__(THREADS, 1)
-    side_gemm(const uint16_t* __restrict__ P, int64_t R, int64_t C, int64_t ldp, QSrc qs, int r,
+    side_gemm(const __grid_constant__ CUtensorMap tmP, int64_t R, int64_t C, QSrc qs, int r,
               float* __restrict__ part, int* __restrict__ tickets, int64_t chunk, int S, Epi epi) {
   constexpr int QP = NJ + 8;  // Q row pitch in elements (+16 bytes: conflict-free ldmatrix)
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  // TMA writes 128-byte-swizzled tiles: stage buffers start on 1024-byte boundaries
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint16_t* sP = reinterpret_cast<uint16_t*>(smem);
   uint16_t* sQ = reinterpret_cast<uint16_t*>(smem + STAGES * P_STAGE_BYTES);
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ int s_last;
+  __shared__ int abort_flag;
+  volatile int* abort_p = &abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t r0 = (int64_t)blockIdx.x * TR;
   const int64_t c_pad = (C + TC - 1) / TC * TC;
@@ -197,29 +206,32 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int64_t c_end = (c_begin + chunk < c_pad) ? c_begin + chunk : c_pad;
   const int nst = c_end > c_begin ? static_cast<int>((c_end - c_begin) / TC) : 0;
 
-  auto load_P = [&](int st) {
-    uint16_t* d = sP + (st % STAGES) * (TR * TC);
-    const int64_t c0 = c_begin + (int64_t)st * TC;
-#pragma unroll
-    for (int i = tid; i < TR * TC / 8; i += THREADS) {
-      if (!kPCol) {  // [128 rows][64 c], chunk ^ (row & 7)
-        const int row = i >> 3, ch = i & 7;
-        const int64_t gr = r0 + row;
-        const bool v = gr < R;
-        cp_async16(d + row * TC + ((ch ^ (row & 7)) << 3), P + (v ? gr : 0) * ldp + c0 + ch * 8, v);
-      } else {  // [64 c][128 rows], chunk ^ (c & 7)
-        const int c = i >> 4, ch = i & 15;
-        const int64_t gc = c0 + c;
-        const bool v = gc < C && r0 + ch * 8 < R;
-        cp_async16(d + c * TR + ((ch ^ (c & 7)) << 3), P + (v ? gc * ldp + r0 + ch * 8 : 0), v);
-      }
+  if (tid == 0) {
+    for (int i = 0; i < STAGES; ++i) mbar_init(&full_bar[i], 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // One thread streams P with TMA: K-major tiles are one [64 c x 128 rows] box (row r at
+  // r*128 bytes, 16-byte chunk ^ (r & 7)); column-wise tiles are two [64 rows x 64 c] boxes
+  // (c at c*128 bytes within each half).  Out-of-range rows / columns arrive as zeros.
+  auto issue = [&](int st) {
+    const int slot = st % STAGES;
+    uint16_t* d = sP + slot * (TR * TC);
+    const int32_t c0 = static_cast<int32_t>(c_begin + (int64_t)st * TC);
+    mbar_arrive_expect_tx(&full_bar[slot], P_STAGE_BYTES);
+    if (!kPCol) {
+      tma_load_2d(d, &tmP, &full_bar[slot], c0, static_cast<int32_t>(r0));
+    } else {
+      tma_load_2d(d, &tmP, &full_bar[slot], static_cast<int32_t>(r0), c0);
+      tma_load_2d(d + TR * TC / 2, &tmP, &full_bar[slot], static_cast<int32_t>(r0 + 64), c0);
     }
   };
-
-#pragma unroll
-  for (int st = 0; st < STAGES - 1; ++st) {
-    if (st < nst) load_P(st);
-    cp_async_commit();
+  int issued = 0;
+  if (tid == 0) {
+    tma_prefetch_desc(&tmP);
+    for (; issued < STAGES - 1 && issued < nst; ++issued) issue(issued);
   }
   // rank-r operand for the whole contraction range, as [c][j] bf16 (zero past the rank),
   // loaded with 16-byte vectors in batches of 8 per thread so the loads overlap
@@ -229,11 +241,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
   for (int t = 0; t < NJ / 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 
+  bool ok = true;
   for (int st = 0; st < nst; ++st) {
-    cp_async_wait<STAGES - 2>();
-    __syncthreads();
-    if (st + STAGES - 1 < nst) load_P(st + STAGES - 1);
-    cp_async_commit();
+    ok = mbar_wait(&full_bar[st % STAGES], (st / STAGES) & 1, kWaitTmaFull, abort_p, &g_side_error);
+    __syncthreads();  // every warp is past stage st - 1: its buffer can be refilled
+    if (!ok || *abort_p) {
+      ok = false;
+      break;
+    }
+    if (tid == 0 && st + STAGES - 1 < nst) {
+      fence_proxy_async_smem();  // the generic-proxy reads of that buffer precede the refill
+      issue(st + STAGES - 1);
+      ++issued;
+    }
     const uint16_t* tP = sP + (st % STAGES) * (TR * TC);
 #pragma unroll
     for (int kk = 0; kk < TC / 16; ++kk) {
@@ -244,7 +264,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       } else {
         const int i = lane >> 3;
         const int c = kk * 16 + (lane & 7) + 8 * (i >> 1);
-        ldsm_x4_t(smem_u32(tP + c * TR + (((warp * 2 + (i & 1)) ^ (c & 7)) << 3)), a);
+        const int chunk16 = warp * 2 + (i & 1);  // 8-row group of the 128 rows
+        ldsm_x4_t(smem_u32(tP + (chunk16 >> 3) * (TR * TC / 2) + c * 64 +
+                           (((chunk16 & 7) ^ (c & 7)) << 3)), a);
       }
       const int qc = st * TC + kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
@@ -255,7 +277,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   }
-  cp_async_wait<0>();
+  if (!ok) {
+    // give up without a result (the row tile's ticket never completes), but never leave a
+    // copy in flight into this CTA's shared memory
+    if (tid == 0)
+      for (int st = issued - (STAGES - 1) < 0 ? 0 : issued - (STAGES - 1); st < issued; ++st)
+        mbar_drain(&full_bar[st % STAGES], (st / STAGES) & 1);
+    __syncthreads();
+    return;
+  }
 
   // this CTA's partial sums
   const int g = lane >> 2, q = lane & 3;
@@ -371,7 +401,16 @@ int run_side(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t 
   const Split sp = pick_split(R, C, NJ);
   float* part = reinterpret_cast<float*>(ws + L.part);
   int* tickets = reinterpret_cast<int*>(ws + L.tickets);
-  const int smem = side::STAGES * side::P_STAGE_BYTES + (int)sp.chunk * (NJ + 8) * 2;
+  CUtensorMap tm;
+  // K-major: P is [R rows][C] and a box is 64 c x 128 rows; column-wise: P is [C][R] and a
+  // box is 64 rows x 64 c
+  const bool mapped =
+      kCol ? make_tensor_map_2d(&tm, P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)R,
+                                (uint64_t)C, (uint64_t)ldp * 2, 64, 64, MapSwizzle::B128)
+           : make_tensor_map_2d(&tm, P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)C,
+                                (uint64_t)R, (uint64_t)ldp * 2, 64, side::TR, MapSwizzle::B128);
+  if (!mapped) return QLORA_ERR_CUDA;
+  const int smem = side::STAGES * side::P_STAGE_BYTES + (int)sp.chunk * (NJ + 8) * 2 + 1024;
   dim3 grid(sp.row_tiles, (unsigned)sp.S);
   ProfileScope ps(name, stream);
   switch (NJ) {
@@ -385,7 +424,7 @@ int run_side(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t 
                                     side::STAGES * side::P_STAGE_BYTES + side::Q_SMEM_MAX + 1024) \
                == cudaSuccess;                                                                    \
     }                                                                                             \
-    side::side_gemm<kCol, nj><<<grid, side::THREADS, smem, stream>>>(P, R, C, ldp, qs, r, part,     \
+    side::side_gemm<kCol, nj><<<grid, side::THREADS, smem, stream>>>(tm, R, C, qs, r, part,         \
                                                                      tickets, sp.chunk, sp.S, epi); \
     break;
     QLORA_SIDE_CASE(16)
