@@ -3,10 +3,11 @@
 // scale per 64 weights, scales quantized again in blocks of 256; digipro.cn "QLoRA:
 // Fine-Tuning a 7B Model on a 16GB GPU": quantized on the fly during load).
 //
-// Three launches quantize a tensor, all HBM-bound, no host synchronization:
-//   nf4_quant_blocks   reads W once: per-64 absmax (half-warp shuffle max), the nearest
-//                      level of w/absmax, 4-bit packing; writes the codes, the absmax values
-//                      and, per group of 256 blocks, the fp64 pairwise sum of its absmax.
+// Three launches quantize a tensor, no host synchronization:
+//   nf4_quant_blocks   reads W once: per-64 absmax, the nearest level of w/absmax (exactly as
+//                      with an IEEE division, see below), 4-bit packing; writes the codes, the
+//                      absmax values and, per group of 256 blocks, the fp64 pairwise sum of
+//                      its absmax.
 //   nf4_absmax_mean    one CTA: the pairwise sum over the group sums -> mean (fp32).
 //   nf4_double_quant   one CTA per group: step = max|a - mean| / 127, int8 codes.
 // Dequantization is one launch (nf4_dequant_kernel) built on the byte-permute table
@@ -24,65 +25,129 @@ constexpr int64_t kGroupElems = (int64_t)kBlock * kGroup;  // 16384 weights
 constexpr int kQuantThreads = 256;
 
 // -------------------------------------------------------------------- pass 1
-// One CTA per group of 256 blocks (16384 weights).  A half-warp covers one block with one
-// float4 per lane; each warp walks 32 of the group's blocks, 4 pairs per iteration so that
-// four 512-byte loads are in flight per warp.
+// One CTA per group of 256 blocks (16384 weights).
+//
+// Full groups: four lanes per 64-block, 16 weights per lane (four float4 loads), so a block's
+// absmax is 15 max operations and two shuffles.  The exact quotient x = RN(w / a) is never
+// needed away from a threshold: y = RN(w * RN(1/a)) is within 3 * 2^-24 * |x| of x, so
+// whenever y is more than 2^-20 from every threshold, y and x fall between the same two
+// thresholds and the level follows from y.  The level comes from a shared-memory table over
+// cells of y (sign, binade, top 4 mantissa bits for |y| in [2^-5, 1]): each cell holds at most
+// one threshold T, the level is c_lo + (y > T), and |y - T| < 2^-20 sends that weight to the
+// exact division (thresholds lie >= 2.3e-4 inside their cells, so a threshold between x and y
+// is always the one in y's cell).  |y| < 2^-5 is level 7 outright.
+// The last, partial group takes the element-by-element path with the exact division.
+constexpr int kCells = 81;                 // |y| cells: 5 binades x 16, plus [1, 1.0625)
+constexpr uint32_t kCellBase = 0x3D000000u;  // bits of 2^-5
+constexpr float kGuard = 0x1p-20f;
+
+__device__ __forceinline__ uint32_t code_exact(float w, float a) {
+  return a == 0.0f ? nf4_code(0.0f) : nf4_code(__fdiv_rn(w, a));
+}
+
+// cell table entry: (threshold inside the cell or +inf, lowest level of the cell)
+__device__ void build_cells(float2* tab) {
+  constexpr float T[15] = QLORA_NF4_THRESHOLDS;
+  for (int i = threadIdx.x; i < 2 * kCells; i += blockDim.x) {
+    const int neg = i / kCells, idx = i % kCells;
+    const float lo = __uint_as_float(kCellBase + (static_cast<uint32_t>(idx) << 19));
+    const float hi = __uint_as_float(kCellBase + (static_cast<uint32_t>(idx + 1) << 19));
+    int c_lo = 0;
+    float thr = __int_as_float(0x7f800000);  // +inf: no threshold in the cell
+    for (int t = 0; t < 15; ++t) {
+      if (!neg) {  // y in [lo, hi)
+        if (T[t] < lo) ++c_lo;
+        else if (T[t] < hi) thr = T[t];
+      } else {     // y in (-hi, -lo]
+        if (T[t] <= -hi) ++c_lo;
+        else if (T[t] <= -lo) thr = T[t];
+      }
+    }
+    tab[i] = make_float2(thr, __int_as_float(c_lo));
+  }
+}
+
+__device__ __forceinline__ uint32_t code_fast(float w, float y, float a, const float2* tab) {
+  const uint32_t u = __float_as_uint(y);
+  const uint32_t m = u & 0x7FFFFFFFu;
+  if (m < kCellBase) return 7u;
+  const float2 e = tab[(u >> 31) * kCells + ((m - kCellBase) >> 19)];
+  if (fabsf(y - e.x) < kGuard) return code_exact(w, a);
+  return static_cast<uint32_t>(__float_as_int(e.y)) + (y > e.x ? 1u : 0u);
+}
+
 __global__ void __launch_bounds__(kQuantThreads) nf4_quant_blocks(
     const float* __restrict__ W, int64_t numel, uint8_t* __restrict__ codes,
     float* __restrict__ absmax, double* __restrict__ group_sum) {
   __shared__ float s_abs[kGroup];
+  __shared__ float2 s_cells[2 * kCells];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int half = lane >> 4, hl = lane & 15;
   const int64_t g = blockIdx.x;
   const int64_t nblocks = (numel + kBlock - 1) / kBlock;
+  const bool full = (g + 1) * kGroupElems <= numel;
 
+  if (full) {
+    build_cells(s_cells);
+    __syncthreads();
+    const int ql = lane & 3, bw = lane >> 2;  // quarter of the block, block within the warp
 #pragma unroll 1
-  for (int it = 0; it < 4; ++it) {
-    float4 v[4];
-    int64_t e0[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int local_block = warp * 32 + it * 8 + u * 2 + half;
+    for (int it = 0; it < 4; ++it) {
+      const int local_block = warp * 32 + it * 8 + bw;
       const int64_t b = g * kGroup + local_block;
-      e0[u] = b * kBlock + hl * 4;
-      if (e0[u] + 3 < numel) {
-        v[u] = __ldg(reinterpret_cast<const float4*>(W + e0[u]));
-      } else {
-        v[u].x = e0[u] + 0 < numel ? W[e0[u] + 0] : 0.0f;
-        v[u].y = e0[u] + 1 < numel ? W[e0[u] + 1] : 0.0f;
-        v[u].z = e0[u] + 2 < numel ? W[e0[u] + 2] : 0.0f;
-        v[u].w = e0[u] + 3 < numel ? W[e0[u] + 3] : 0.0f;
-      }
-    }
+      const float4* src = reinterpret_cast<const float4*>(W + b * kBlock + ql * 16);
+      float w[16];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float m = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+      for (int v = 0; v < 4; ++v) {
+        const float4 f = __ldg(src + v);
+        w[4 * v + 0] = f.x; w[4 * v + 1] = f.y; w[4 * v + 2] = f.z; w[4 * v + 3] = f.w;
+      }
+      float m = fabsf(w[0]);
+#pragma unroll
+      for (int i = 1; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      if (ql == 0) {
+        s_abs[local_block] = m;
+        absmax[b] = m;
+      }
+      uint32_t c[16];
+      if (m >= 0x1p-100f) {  // the reciprocal of a normal-range absmax is finite and exact to RN
+        const float rcp = __frcp_rn(m);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) c[i] = code_fast(w[i], __fmul_rn(w[i], rcp), m, s_cells);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) c[i] = code_exact(w[i], m);
+      }
+      uint32_t lo = 0, hi = 0;  // byte j = (c[2j] << 4) | c[2j+1], little endian
+#pragma unroll
+      for (int j = 0; j < 4; ++j) lo |= ((c[2 * j] << 4) | c[2 * j + 1]) << (8 * j);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) hi |= ((c[8 + 2 * j] << 4) | c[8 + 2 * j + 1]) << (8 * j);
+      *reinterpret_cast<uint2*>(codes + b * (kBlock / 2) + ql * 8) = make_uint2(lo, hi);
+    }
+  } else {
+    // partial last group: half a warp per block, one float4 per lane, exact division
+    const int half = lane >> 4, hl = lane & 15;
+#pragma unroll 1
+    for (int it = 0; it < 16; ++it) {
+      const int local_block = warp * 32 + it * 2 + half;
+      const int64_t b = g * kGroup + local_block;
+      const int64_t e = b * kBlock + hl * 4;
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = e + i < numel ? W[e + i] : 0.0f;
+      float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
       for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      const int local_block = warp * 32 + it * 8 + u * 2 + half;
-      const int64_t b = g * kGroup + local_block;
       if (hl == 0) {
         s_abs[local_block] = m;  // blocks past the end hold 0 (all their inputs read as 0)
         if (b < nblocks) absmax[b] = m;
       }
-      uint32_t c0, c1, c2, c3;
-      if (m == 0.0f) {
-        c0 = c1 = c2 = c3 = nf4_code(0.0f);
-      } else {
-        c0 = nf4_code(__fdiv_rn(v[u].x, m));
-        c1 = nf4_code(__fdiv_rn(v[u].y, m));
-        c2 = nf4_code(__fdiv_rn(v[u].z, m));
-        c3 = nf4_code(__fdiv_rn(v[u].w, m));
-      }
-      // even element in the high nibble
-      const uint32_t byte0 = (c0 << 4) | c1, byte1 = (c2 << 4) | c3;
-      const int64_t e = e0[u];
-      if (e + 3 < numel) {
-        *reinterpret_cast<uint16_t*>(codes + e / 2) = static_cast<uint16_t>(byte0 | (byte1 << 8));
-      } else {
-        if (e < numel) codes[e / 2] = static_cast<uint8_t>(e + 1 < numel ? byte0 : (c0 << 4));
-        if (e + 2 < numel) codes[e / 2 + 1] = static_cast<uint8_t>(e + 3 < numel ? byte1 : (c2 << 4));
-      }
+      const uint32_t c0 = code_exact(v[0], m), c1 = code_exact(v[1], m);
+      const uint32_t c2 = code_exact(v[2], m), c3 = code_exact(v[3], m);
+      if (e < numel) codes[e / 2] = static_cast<uint8_t>(e + 1 < numel ? ((c0 << 4) | c1) : (c0 << 4));
+      if (e + 2 < numel) codes[e / 2 + 1] = static_cast<uint8_t>(e + 3 < numel ? ((c2 << 4) | c3) : (c2 << 4));
     }
   }
   __syncthreads();
@@ -90,11 +155,11 @@ __global__ void __launch_bounds__(kQuantThreads) nf4_quant_blocks(
     // Perfect binary tree over the 256 absmax values in block order: each lane sums 8
     // neighbours pairwise, then the xor butterfly combines lanes (x+y == y+x in IEEE).
     const float* a = s_abs + lane * 8;
-    double s = (((double)a[0] + (double)a[1]) + ((double)a[2] + (double)a[3])) +
-               (((double)a[4] + (double)a[5]) + ((double)a[6] + (double)a[7]));
+    double sum = (((double)a[0] + (double)a[1]) + ((double)a[2] + (double)a[3])) +
+                 (((double)a[4] + (double)a[5]) + ((double)a[6] + (double)a[7]));
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) group_sum[g] = s;
+    for (int o = 1; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) group_sum[g] = sum;
   }
 }
 

@@ -55,6 +55,23 @@ def test_quantize_special_blocks():
     _quant_parity(W.reshape(1, -1))
 
 
+def test_quantize_near_thresholds():
+    """Weights planted within a few ulps of level boundaries (w ~ T_i * absmax): the
+    quotient w / absmax lands next to a threshold, where the quantizer must take its exact
+    division path to stay bit-exact."""
+    L, T = oracle.levels()
+    g = wl.rng(44)
+    nb = 64 * 256 * 4  # whole groups of 256 blocks
+    a = g.uniform(0.005, 1.5, size=nb).astype(np.float32)
+    i = g.integers(0, 15, size=(nb, 64))
+    base = (T[i].astype(np.float32) * a[:, None]).astype(np.float32)
+    k = g.integers(-3, 4, size=(nb, 64)).astype(np.int32)
+    W = (base.view(np.int32) + k).view(np.float32)
+    W[:, 0] = np.where(g.integers(0, 2, size=nb) == 1, a, -a)  # absmax element
+    W = np.clip(W, -a[:, None], a[:, None]).astype(np.float32)
+    _quant_parity(W.reshape(1, -1))
+
+
 def test_quantize_config_tensors_bit_exact():
     _quant_parity(wl.config1().W())
     _quant_parity(wl.config2().W())
