@@ -90,17 +90,24 @@ __global__ void __launch_bounds__(kQuantThreads) nf4_quant_blocks(
     build_cells(s_cells);
     __syncthreads();
     const int ql = lane & 3, bw = lane >> 2;  // quarter of the block, block within the warp
+    auto load16 = [&](int it, float4 (&f)[4]) {
+      const int64_t b = g * kGroup + warp * 32 + it * 8 + bw;
+      const float4* src = reinterpret_cast<const float4*>(W + b * kBlock + ql * 16);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) f[v] = __ldg(src + v);
+    };
+    float4 nxt[4];
+    load16(0, nxt);
 #pragma unroll 1
     for (int it = 0; it < 4; ++it) {
       const int local_block = warp * 32 + it * 8 + bw;
       const int64_t b = g * kGroup + local_block;
-      const float4* src = reinterpret_cast<const float4*>(W + b * kBlock + ql * 16);
       float w[16];
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        const float4 f = __ldg(src + v);
-        w[4 * v + 0] = f.x; w[4 * v + 1] = f.y; w[4 * v + 2] = f.z; w[4 * v + 3] = f.w;
+        w[4 * v + 0] = nxt[v].x; w[4 * v + 1] = nxt[v].y; w[4 * v + 2] = nxt[v].z; w[4 * v + 3] = nxt[v].w;
       }
+      if (it + 1 < 4) load16(it + 1, nxt);  // next block's loads in flight during this one
       float m = fabsf(w[0]);
 #pragma unroll
       for (int i = 1; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
@@ -165,28 +172,49 @@ __global__ void __launch_bounds__(kQuantThreads) nf4_quant_blocks(
 
 // -------------------------------------------------------------------- pass 2
 // One CTA of 1024 threads: the pairwise tree over the group sums (zero-padded to a power of
-// two) -> mean = (float)(total / nblocks).  Each thread first folds a run of `run` leaves
-// (a power of two) with a binary-counter stack, which is exactly the pairwise tree of the
-// run; the runs then combine through warp butterflies and a final warp.
+// two) -> mean = (float)(total / nblocks).  Each thread folds a run of kRun consecutive
+// leaves (a power of two) with a register tree -- exactly the pairwise tree of the run -- and
+// the runs combine through warp butterflies and a final warp.
+template <int kRun>
+__device__ __forceinline__ double fold_run(const double* __restrict__ leaf, int64_t lo, int64_t n) {
+  double v[kRun];
+#pragma unroll
+  for (int i = 0; i < kRun; ++i) v[i] = (lo + i < n) ? leaf[lo + i] : 0.0;
+#pragma unroll
+  for (int w = 1; w < kRun; w <<= 1)
+#pragma unroll
+    for (int i = 0; i < kRun; i += 2 * w) v[i] = v[i] + v[i + w];
+  return v[0];
+}
+
 __global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict__ group_sum,
                                                         int64_t ngroups, int64_t nblocks,
                                                         int64_t run, float* __restrict__ mean) {
   __shared__ double s_warp[32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  double stack[32];
-  int depth = 0;
   const int64_t lo = (int64_t)t * run;
-  for (int64_t i = 0; i < run; ++i) {
-    double v = (lo + i < ngroups) ? group_sum[lo + i] : 0.0;
-    // merge equal-sized subtrees, like incrementing a binary counter
-    int64_t k = i + 1;
-    while ((k & 1) == 0) {
-      v = stack[--depth] + v;
-      k >>= 1;
+  double s;
+  switch (run) {
+    case 1: s = fold_run<1>(group_sum, lo, ngroups); break;
+    case 2: s = fold_run<2>(group_sum, lo, ngroups); break;
+    case 4: s = fold_run<4>(group_sum, lo, ngroups); break;
+    case 8: s = fold_run<8>(group_sum, lo, ngroups); break;
+    case 16: s = fold_run<16>(group_sum, lo, ngroups); break;
+    default: {  // very large tensors: binary-counter fold of the run, still the pairwise tree
+      double stack[48];
+      int depth = 0;
+      for (int64_t i = 0; i < run; ++i) {
+        double v = (lo + i < ngroups) ? group_sum[lo + i] : 0.0;
+        int64_t k = i + 1;
+        while ((k & 1) == 0) {
+          v = stack[--depth] + v;
+          k >>= 1;
+        }
+        stack[depth++] = v;
+      }
+      s = stack[0];
     }
-    stack[depth++] = v;
   }
-  double s = stack[0];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   if (lane == 0) s_warp[warp] = s;
@@ -200,33 +228,52 @@ __global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict
 }
 
 // -------------------------------------------------------------------- pass 3
-__global__ void __launch_bounds__(kGroup) nf4_double_quant(const float* __restrict__ absmax,
-                                                           int64_t nblocks,
-                                                           const float* __restrict__ mean,
-                                                           int8_t* __restrict__ scale_codes,
-                                                           float* __restrict__ steps) {
-  __shared__ float s_max[kGroup / 32];
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int64_t b = (int64_t)blockIdx.x * kGroup + t;
-  const float mu = mean[0];
-  const float d = (b < nblocks) ? __fsub_rn(absmax[b], mu) : 0.0f;
-  float m = fabsf(d);
+// A warp per group of 256 blocks (8 per lane), 8 groups per CTA.
+__global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict__ absmax,
+                                                        int64_t nblocks, int64_t ngroups,
+                                                        const float* __restrict__ mean,
+                                                        int8_t* __restrict__ scale_codes,
+                                                        float* __restrict__ steps) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t g = (int64_t)blockIdx.x * 8 + warp;
+  if (g >= ngroups) return;
+  const float mu = __ldg(mean);
+  const int64_t b0 = g * kGroup + lane * 8;
+  float d[8];
+  if (b0 + 8 <= nblocks) {
+    const float4* src = reinterpret_cast<const float4*>(absmax + b0);
+    const float4 x = __ldg(src), y = __ldg(src + 1);
+    const float a[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = __fsub_rn(a[i], mu);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = (b0 + i < nblocks) ? __fsub_rn(absmax[b0 + i], mu) : 0.0f;
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(d[i]));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) s_max[warp] = m;
-  __syncthreads();
-  float s2 = s_max[0];
+  const float step = __fdiv_rn(m, 127.0f);
+  if (lane == 0) steps[g] = step;
+  uint32_t q[8];
 #pragma unroll
-  for (int i = 1; i < kGroup / 32; ++i) s2 = fmaxf(s2, s_max[i]);
-  const float step = __fdiv_rn(s2, 127.0f);
-  if (t == 0) steps[blockIdx.x] = step;
-  if (b < nblocks) {
-    int q = 0;
+  for (int i = 0; i < 8; ++i) {
+    int v = 0;
     if (step > 0.0f) {
-      q = __float2int_rn(__fdiv_rn(d, step));  // round half to even
-      q = q > 127 ? 127 : (q < -127 ? -127 : q);
+      v = __float2int_rn(__fdiv_rn(d[i], step));  // round half to even
+      v = v > 127 ? 127 : (v < -127 ? -127 : v);
     }
-    scale_codes[b] = static_cast<int8_t>(q);
+    q[i] = static_cast<uint32_t>(v) & 0xFFu;
+  }
+  if (b0 + 8 <= nblocks) {
+    *reinterpret_cast<uint2*>(scale_codes + b0) =
+        make_uint2(q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24),
+                   q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24));
+  } else {
+    for (int i = 0; i < 8; ++i)
+      if (b0 + i < nblocks) scale_codes[b0 + i] = static_cast<int8_t>(q[i]);
   }
 }
 
@@ -302,8 +349,8 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   }
   {
     ProfileScope ps("nf4_double_quant", stream);
-    nf4_double_quant<<<(unsigned)ng, kGroup, 0, stream>>>(absmax, nb, q.scale_mean, q.scale_codes,
-                                                          q.scale_steps);
+    nf4_double_quant<<<(unsigned)((ng + 7) / 8), 256, 0, stream>>>(absmax, nb, ng, q.scale_mean,
+                                                                 q.scale_codes, q.scale_steps);
   }
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
