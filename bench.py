@@ -455,8 +455,7 @@ def measure_secondary(qn, wl, dev, peaks, traffic, flush_buf, reps: int = 10):
         B = bf16_dev(p.B(), dev)
         Y = torch.empty(M, p.N, dtype=torch.bfloat16, device=dev)
         fn = lambda: qn.qlora_linear_fwd(X, q, A, B, p.scale, save_u=False, out=Y)  # noqa: E731
-        ms_all, prof = timed(fn, ["pad_adapters", "side_u", "finalize_rows", "decode_gemv",
-                                  "decode_finalize"])
+        ms_all, prof = timed(fn, ["decode_u", "decode_gemv"])
         ms_gemv = prof["decode_gemv"][1] / reps
         nbytes = meta + 2 * M * p.K + 2 * M * p.N + 2 * p.r * (p.K + p.N)
         out[f"decode_fwd_M{M}"] = {

@@ -169,9 +169,11 @@ int qlora_device_status(int32_t* out, void* stream) {
   int v = 0;
   if (cudaStreamSynchronize(s) != cudaSuccess) return QLORA_ERR_CUDA;
   if ((st = read_and_clear_gemm_error(&v))) return st;
-  int w = 0;
+  int w = 0, d = 0;
   if ((st = read_and_clear_side_error(&w))) return st;
+  if ((st = read_and_clear_decode_error(&d))) return st;
   if (!v) v = w;
+  if (!v) v = d;
   *out = v;
   return v ? QLORA_ERR_DEVICE_TIMEOUT : QLORA_OK;
 }

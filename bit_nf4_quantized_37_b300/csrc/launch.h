@@ -16,6 +16,8 @@ int num_sms();
 int read_and_clear_gemm_error(int* out);
 // Reads and clears the side kernels' device error word (lora_side.cu).
 int read_and_clear_side_error(int* out);
+// Reads and clears the decode kernel's device error word (skinny.cu).
+int read_and_clear_decode_error(int* out);
 
 // Quantize / dequantize (nf4_codec.cu).
 uint64_t quantize_workspace_bytes(int64_t numel);

@@ -48,8 +48,8 @@ int linear_forward(const LinearArgs& a, cudaStream_t stream) {
   const WorkspaceLayout L = workspace_layout(a.M, a.N, a.K, a.r);
   int st = clear_tickets(a, L, stream);
   if (st) return st;
-  if ((st = launch_lora_u(a, L, a.U, stream))) return st;
   if (a.M <= kSkinnyMaxM) return launch_skinny_fwd(a, L, stream);
+  if ((st = launch_lora_u(a, L, a.U, stream))) return st;
   if (a.r % 8 && (st = launch_pad_b(a, L, stream))) return st;
   return launch_fused_fwd(a, L, stream);
 }
