@@ -335,6 +335,253 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ============================================================================ CTA pairs
+// The same GEMMs on CTA pairs (cta_group::2).  A pair owns a 512 x 256 output tile: each CTA
+// holds 256 rows of X/dY (two 128-row slabs) and half of the dequantized W tile (128 W rows
+// for the forward, 128 output columns for the input gradient), the leader issues UMMAs of
+// M = 256 (128 rows from each CTA) x N = 256 (128 columns from each CTA's W half) into two
+// TMEM accumulators per CTA.  Each SM now dequantizes 8192 weights per stage for 4 x 128 x 256
+// x 64 multiply-adds: twice the tensor work per integer-pipe instruction of the single-CTA
+// 256 x 256 tile, and a quarter of its W tile in shared memory.
+//   full_bar   (leader) TMA bytes of both CTAs            waited by the leader's UMMA thread
+//   bready_bar (leader) 4 dequant warps of each CTA       waited by the leader's UMMA thread
+//   empty_bar  (each)   multicast tcgen05.commit          waited by each CTA's producers
+//   acc_bar    (each)   multicast tcgen05.commit          waited by each CTA's epilogue
+// Two dequant groups of 4 warps take alternate stages (one 64-weight block per thread each).
+namespace pairk {
+constexpr int BM_CTA = 256;
+constexpr int BN_CTA = 128;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM_CTA * BK * 2;   // 32 KB
+constexpr int B_BYTES = BN_CTA * BK * 2;   // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr int GROUP_WARPS = 4;
+constexpr int TMEM_COLS = 512;
+}  // namespace pairk
+
+template <int kMode>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    fused_pair_gemm(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmA2,
+                    const __grid_constant__ CUtensorMap tmB2,
+                    const __grid_constant__ CUtensorMap tmOut, const Params p) {
+  using pairk::BM_CTA; using pairk::BN_CTA; using pairk::STAGES; using pairk::A_BYTES;
+  using pairk::STAGE_BYTES; using pairk::GROUP_WARPS; using pairk::TMEM_COLS;
+  constexpr int B_BYTES = pairk::B_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t bready_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();           // 0: leader, 1: peer
+  const int64_t m0 = (int64_t)(blockIdx.x >> 1) * 512 + rank * BM_CTA;  // this CTA's A rows
+  const int64_t n0 = (int64_t)blockIdx.y * BN;                          // pair's columns
+  const int64_t nb0 = n0 + rank * BN_CTA;                               // this CTA's W half
+  const int n_main = static_cast<int>(p.Kc / BK);
+  const int total = p.n_lora + n_main;
+  volatile int* abort_p = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&bready_bar[i], 2 * GROUP_WARPS);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(&acc_bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc<2>(&tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the leader's barriers exist before the peer signals them
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (elect_one_sync()) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+      for (int s = 0; s < total; ++s) {
+        const int slot = s % STAGES, round = s / STAGES;
+        if (round > 0 &&
+            !mbar_wait<true>(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
+          break;
+        const uint32_t full_lead = mapa_shared(smem_u32(&full_bar[slot]), 0);
+        uint8_t* a_dst = smem + slot * STAGE_BYTES;
+        uint8_t* b_dst = a_dst + A_BYTES;
+        if (s < p.n_lora) {
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[slot], 2 * (A_BYTES + B_BYTES));
+          tma_load_2d_pair(a_dst, &tmA2, full_lead, s * BK, (int32_t)m0);
+          if (kMode == 0) {
+            tma_load_2d_pair(b_dst, &tmB2, full_lead, s * BK, (int32_t)nb0);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              tma_load_2d_pair(b_dst + i * 8192, &tmB2, full_lead, (int32_t)(nb0 + 64 * i), s * BK);
+          }
+        } else {
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[slot], 2 * A_BYTES);
+          tma_load_2d_pair(a_dst, &tmA, full_lead, (s - p.n_lora) * BK, (int32_t)m0);
+        }
+      }
+      // the leader's full barriers count both CTAs' copies: the leader drains them
+      if (rank == 0)
+        for (int s = total - STAGES < 0 ? 0 : total - STAGES; s < total; ++s)
+          mbar_drain(&full_bar[s % STAGES], (s / STAGES) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer (leader)
+    if (rank == 0 && elect_one_sync()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * UM, BN, 0, kMode);
+      bool ok = true;
+      for (int s = 0; s < total && ok; ++s) {
+        const int slot = s % STAGES, round = s / STAGES;
+        ok = mbar_wait<true>(&full_bar[slot], round & 1, kWaitTmaFull, abort_p, &g_gemm_error) &&
+             mbar_wait<true>(&bready_bar[slot], round & 1, kWaitBReady, abort_p, &g_gemm_error);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(smem + slot * STAGE_BYTES);
+        const uint32_t b_addr = a_addr + A_BYTES;
+        const int ksteps = (s < p.n_lora && s == p.n_lora - 1) ? p.lora_last_k16 : 4;
+        for (int kk = 0; kk < ksteps; ++kk) {
+          const uint64_t bdesc = (kMode == 0)
+                                     ? smem_desc(b_addr + kk * 32, 16, 1024, Swizzle::B128)
+                                     : smem_desc(b_addr + kk * 2048, 8192, 1024, Swizzle::B128);
+#pragma unroll
+          for (int acc = 0; acc < 2; ++acc) {
+            const uint64_t adesc =
+                smem_desc(a_addr + acc * (UM * BK * 2) + kk * 32, 16, 1024, Swizzle::B128);
+            umma_bf16_ss<2>(tmem + acc * 256, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit_pair(&empty_bar[slot], 0x3);
+      }
+      if (ok) umma_commit_pair(&acc_bar, 0x3);
+    }
+    __syncwarp();
+  } else if (warp >= DEQ_WARP0) {
+    // ------------------------------------------------------------ NF4 producers (both CTAs)
+    const int group = (warp - DEQ_WARP0) / GROUP_WARPS;           // owns stages s % 2 == group
+    const int t = ((warp - DEQ_WARP0) % GROUP_WARPS) * 32 + lane;  // 0..127
+    const float mu = __ldg(p.mean);
+    int64_t row_base, kcol;
+    uint32_t dst_off, swz;
+    if (kMode == 0) {
+      row_base = nb0 + t;  // one W row per thread, k-slice of the stage
+      kcol = 0;
+      dst_off = t * 128;
+      swz = t & 7;
+    } else {
+      const int nl = (t & 7) + 8 * ((t >> 3) & 7);  // W row within the stage's 64
+      const int blk = t >> 6;                        // which 64 of this CTA's 128 columns
+      row_base = nl;
+      kcol = nb0 + blk * 64;
+      dst_off = blk * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
+      swz = nl & 7;
+    }
+    auto slice_at = [&](int s, Slice& sl) {
+      const int kc = s - p.n_lora;
+      if (kMode == 0) load_slice(sl, p, row_base, (int64_t)kc * BK);
+      else load_slice(sl, p, (int64_t)kc * BK + row_base, kcol);
+    };
+    int s = group;
+    Slice cur;
+    cur.valid = false;
+    if (s >= p.n_lora && s < total) slice_at(s, cur);
+    bool ok = true;
+    for (; s < total; s += 2) {
+      const int slot = s % STAGES, round = s / STAGES;
+      if (s >= p.n_lora) {
+        Slice nxt;
+        nxt.valid = false;
+        if (s + 2 < total && s + 2 >= p.n_lora) slice_at(s + 2, nxt);  // in flight meanwhile
+        if (round > 0 &&
+            !mbar_wait<true>(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
+        if (cur.valid) {
+          const Nf4ByteTable tab = nf4_make_table(__fmaf_rn((float)cur.q, cur.step, mu));
+          const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
+                                     cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[4];
+            nf4_dequant8(tab, words[c], o);
+            *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+        cur = nxt;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bready_bar[slot]), 0));
+    }
+
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    if (ok && mbar_wait<true>(&acc_bar, 0, kWaitAccFull, abort_p, &g_gemm_error)) {
+      tc_fence_after();
+      const int lg = warp & 3;                           // TMEM lanes 32*lg .. 32*lg+31
+      const int acc = (warp - DEQ_WARP0) >> 2;           // accumulator (128-row slab)
+      const uint32_t tbase = tmem + static_cast<uint32_t>(acc * 256);
+      const int64_t row0 = m0 + acc * UM + lg * 32;
+      uint8_t* buf0 = smem + (warp - DEQ_WARP0) * 4096;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        const int col = c * 32;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tbase + (static_cast<uint32_t>(lg * 32) << 16) + col, v);
+        tmem_ld_wait();
+        uint8_t* buf = buf0 + (c & 1) * 2048;
+        if (c >= 2) {
+          if (lane == 0) bulk_wait_read1();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t phys = j ^ ((lane >> 1) & 3);  // 64-byte swizzle
+          *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) = make_uint4(
+              pack_bf16(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+              pack_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+              pack_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+              pack_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && n0 + col < p.Nout && row0 < p.M)
+          tma_store_2d(&tmOut, buf, (int32_t)(n0 + col), (int32_t)row0);
+        if (lane == 0) bulk_commit();
+      }
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its pair may still touch its barriers or smem
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<2>(tmem, TMEM_COLS);
+  }
+}
+
 }  // namespace fused
 
 namespace {
@@ -345,15 +592,20 @@ bool map_bf16(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
                             (uint64_t)outer, (uint64_t)pitch_elems * 2, box_inner, box_outer, sw);
 }
 
-template <int kMode, int kAcc>
+template <int kMode, int kAcc, bool kPair>
 int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
   using namespace fused;
-  constexpr int BM = Tile<kAcc>::BM, SMEM_BYTES = Tile<kAcc>::SMEM_BYTES;
+  constexpr int BM = kPair ? pairk::BM_CTA : Tile<kAcc>::BM;
+  constexpr int SMEM_BYTES = kPair ? pairk::SMEM_BYTES : Tile<kAcc>::SMEM_BYTES;
+  constexpr int BNB = kPair ? pairk::BN_CTA : BN;  // W-tile box of one CTA (forward)
   static bool attr_set = false;  // per process; the attribute is per function
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fused_nf4_lora_gemm<kMode, kAcc>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
-      return QLORA_ERR_CUDA;
+    const cudaError_t e =
+        kPair ? cudaFuncSetAttribute(fused_pair_gemm<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES)
+              : cudaFuncSetAttribute(fused_nf4_lora_gemm<kMode, kAcc>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return QLORA_ERR_CUDA;
     attr_set = true;
   }
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
@@ -376,8 +628,8 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
     ok = map_bf16(&tA, a.X, a.K, a.M, a.K, 64, BM, MapSwizzle::B128) &&
          map_bf16(&tA2, ws + L.sU, rp, a.M, rp, 64, BM, MapSwizzle::B128) &&
          (a.r % 8 == 0  // B [N, r] itself; TMA fills the columns past r with zeros
-              ? map_bf16(&tB2, a.B, a.r, a.N, a.r, 64, BN, MapSwizzle::B128)
-              : map_bf16(&tB2, ws + L.Bp, rp, a.N, rp, 64, BN, MapSwizzle::B128)) &&
+              ? map_bf16(&tB2, a.B, a.r, a.N, a.r, 64, BNB, MapSwizzle::B128)
+              : map_bf16(&tB2, ws + L.Bp, rp, a.N, rp, 64, BNB, MapSwizzle::B128)) &&
          map_bf16(&tOut, a.Y, a.N, a.M, a.N, 32, 32, MapSwizzle::B64);
   } else {
     p.Nout = a.K;
@@ -388,26 +640,42 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
          map_bf16(&tOut, a.dX, a.K, a.M, a.K, 32, 32, MapSwizzle::B64);
   }
   if (!ok) return QLORA_ERR_CUDA;
-  dim3 grid((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM));
   ProfileScope ps(kMode == 0 ? "fused_fwd_gemm" : "fused_dx_gemm", stream);
-  fused_nf4_lora_gemm<kMode, kAcc><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tA, tA2, tB2, tOut, p);
+  if (kPair) {
+    dim3 grid((unsigned)(2 * ((a.M + 511) / 512)), (unsigned)((p.Nout + BN - 1) / BN));
+    fused_pair_gemm<kMode><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tA, tA2, tB2, tOut, p);
+  } else {
+    dim3 grid((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM));
+    fused_nf4_lora_gemm<kMode, kAcc><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tA, tA2, tB2, tOut, p);
+  }
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
 }  // namespace
 
-// Two accumulators per CTA when the 256 x 256 tiles still give every SM work, else one.
-static bool use_two_acc(int64_t M, int64_t Nout) {
+// Tile choice: CTA pairs with 512 x 256 tiles when at least half the SMs get a pair tile,
+// single CTAs with 256 x 256 tiles when those fill the SMs, else 128 x 256 tiles.
+static int tile_choice(int64_t M, int64_t Nout) {
+  const int64_t pair_tiles = ((M + 511) / 512) * ((Nout + 255) / 256);
+  if (pair_tiles * 4 >= num_sms()) return 2;
   const int64_t tiles = ((M + 255) / 256) * ((Nout + 255) / 256);
-  return tiles >= num_sms();
+  return tiles >= num_sms() ? 1 : 0;
 }
 
 int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  return use_two_acc(a.M, a.N) ? launch_fused<0, 2>(a, L, stream) : launch_fused<0, 1>(a, L, stream);
+  switch (tile_choice(a.M, a.N)) {
+    case 2: return launch_fused<0, 2, true>(a, L, stream);
+    case 1: return launch_fused<0, 2, false>(a, L, stream);
+    default: return launch_fused<0, 1, false>(a, L, stream);
+  }
 }
 
 int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  return use_two_acc(a.M, a.K) ? launch_fused<1, 2>(a, L, stream) : launch_fused<1, 1>(a, L, stream);
+  switch (tile_choice(a.M, a.K)) {
+    case 2: return launch_fused<1, 2, true>(a, L, stream);
+    case 1: return launch_fused<1, 2, false>(a, L, stream);
+    default: return launch_fused<1, 1, false>(a, L, stream);
+  }
 }
 
 }  // namespace qlora
