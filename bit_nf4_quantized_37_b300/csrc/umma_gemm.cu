@@ -502,10 +502,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (; s < total; s += 2) {
       const int slot = s % STAGES, round = s / STAGES;
+      Slice nxt;  // the group's next stage (also after a LoRA stage), in flight meanwhile
+      nxt.valid = false;
+      if (s + 2 < total && s + 2 >= p.n_lora) slice_at(s + 2, nxt);
       if (s >= p.n_lora) {
-        Slice nxt;
-        nxt.valid = false;
-        if (s + 2 < total && s + 2 >= p.n_lora) slice_at(s + 2, nxt);  // in flight meanwhile
         if (round > 0 &&
             !mbar_wait<true>(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) {
           ok = false;
@@ -528,8 +528,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(0, 0, 0, 0);
         }
         asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-        cur = nxt;
       }
+      cur = nxt;
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bready_bar[slot]), 0));
     }
