@@ -527,7 +527,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(0, 0, 0, 0);
         }
-        asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+        // this CTA's generic-proxy writes, ordered before the tensor core's (async-proxy)
+        // reads; the leader sees them through the release/acquire of the cluster arrive below
+        fence_proxy_async_smem();
       }
       cur = nxt;
       __syncwarp();
