@@ -5,8 +5,8 @@
 //   dB   = s dY^T U     [N, r]  backward     rows n, contraction over M (dY read by columns)
 //   dA^T = X^T sV       [K, r]  backward     rows k, contraction over M (X read by columns)
 // Each is tall and skinny: one big operand P read once from HBM, one rank-r operand Q that
-// fits in shared memory.  One kernel serves all four: P streams through a 6-stage cp.async
-// ring of 128 x 64 tiles into the warp-level tensor cores (mma.sync m16n8k16, bf16 in, fp32
+// fits in shared memory.  One kernel serves all four: P streams through a 4-stage TMA
+// ring of 128 x 64 tiles (two CTAs per SM) into the warp-level tensor cores (mma.sync m16n8k16, bf16 in, fp32
 // accumulate; ldmatrix.trans reads the column-wise P), Q is staged once per CTA for its whole
 // contraction range (converted to bf16 on the way, zero past the rank), and the contraction
 // is split over blockIdx.y.  The CTA that finishes a row tile last (atomic ticket) adds the
@@ -38,9 +38,9 @@ namespace side {
 constexpr int THREADS = 256;  // 8 warps x 16 rows
 constexpr int TR = 128;       // rows per CTA
 constexpr int TC = 64;        // contraction per stage
-constexpr int STAGES = 8;
+constexpr int STAGES = 4;
 constexpr int P_STAGE_BYTES = TR * TC * 2;
-constexpr int Q_SMEM_MAX = 64 * 1024;
+constexpr int Q_SMEM_MAX = 40 * 1024;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -185,7 +185,7 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
 }
 
 template <bool kPCol, int NJ>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     side_gemm(const __grid_constant__ CUtensorMap tmP, int64_t R, int64_t C, QSrc qs, int r,
               float* __restrict__ part, int* __restrict__ tickets, int64_t chunk, int S, Epi epi) {
   constexpr int QP = NJ + 8;  // Q row pitch in elements (+16 bytes: conflict-free ldmatrix)
@@ -380,7 +380,7 @@ Split pick_split(int64_t R, int64_t C, int NJ) {
   Split sp;
   sp.row_tiles = (unsigned)((R + side::TR - 1) / side::TR);
   const int64_t c_tiles = (C + side::TC - 1) / side::TC;
-  int64_t want = num_sms() / (int64_t)sp.row_tiles;
+  int64_t want = 2LL * num_sms() / (int64_t)sp.row_tiles;  // two CTAs per SM
   if (want < 1) want = 1;
   if (want > c_tiles) want = c_tiles;
   int64_t per = (c_tiles + want - 1) / want;
