@@ -25,7 +25,7 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r) {
   L.sV = take((uint64_t)M * L.rp * 2);
   L.U32 = take((uint64_t)M * r * 4);
   L.Bp = take(r % 8 ? (uint64_t)N * L.rp * 2 : 0);
-  L.part_bytes = std::max(side_partial_bytes(M, N, K, r), skinny_partial_bytes(M, N, K));
+  L.part_bytes = std::max(side_partial_bytes(M, N, K, r), skinny_partial_bytes(M, N, K, r));
   L.part = take(L.part_bytes);
   L.ntickets = side_ticket_count(M, N, K);
   L.tickets = take(L.ntickets * 4);

@@ -70,6 +70,6 @@ int launch_lora_da(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t s
 int launch_pad_b(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 uint64_t side_partial_bytes(int64_t M, int64_t N, int64_t K, int r);
 uint64_t side_ticket_count(int64_t M, int64_t N, int64_t K);
-uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K);
+uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K, int r);
 
 }  // namespace qlora

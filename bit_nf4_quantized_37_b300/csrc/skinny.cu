@@ -2,19 +2,32 @@
 // "QLoRA -- the democratization event": serve the 4-bit base plus a separate adapter;
 // addaly.com "QLoRA on one card": keep the adapter separate and load it over the base).
 // With so few tokens the layer is a stream over the packed weights: every weight byte is
-// read once, dequantized in registers and consumed by the warp-level tensor cores with the
-// tokens padded to 16 (mma.sync m16n8k16: tokens are the MMA rows, 8 weight rows the MMA
-// columns).  Nothing of W' is written anywhere.
+// read once from HBM and nothing of W' is written anywhere.
 //
-// nf4_decode_gemv: a CTA owns 128 weight rows and a k range.  One thread streams the packed
-// codes with TMA ([128 rows x 256 k] per stage, 128-byte swizzle, 4 stages in flight); every
-// warp dequantizes two 8-row groups: lane (g, q) = (lane/4, lane%4) owns weight row g of each
-// group and, per 256-wide stage, the 64-block q of that row -- one byte table per block and
-// lane.  Inside an MMA the 16 contraction slots of lane class q map to the physical k of its
-// own block (the contraction order is free as long as the X fragment uses the same map), so
-// X comes from shared memory as 16-byte loads.  The k ranges of a row block are summed, in
-// a fixed order, by the CTA that finishes last (atomic ticket), which also adds the LoRA
-// term s U B^T and writes Y.
+// Arithmetic.  A weight is level[c] * a (a = the block's dequantized absmax), so a row's
+// dot product with a token is  sum_b a_b * sum_{k in b} level[c_k] x_k.  The kernel forms
+// the inner sums on the warp-level tensor cores from bf16(level[c]) and x (mma.sync
+// m16n8k16, fp32 accumulate; weight rows are the MMA rows, tokens the MMA columns) and
+// applies a_b to each 64-wide partial in fp32.  This is W' x up to the bf16 rounding of W'
+// (the weight enters with its level rounded instead of its product with a), which is far
+// inside the GEMM tolerance.  With the scale outside, the code -> operand step is one fixed
+// table: byte v of the code stream (elements 2j, 2j+1 in its high and low nibble) maps to
+// the bf16 pair (level[v >> 4], level[v & 15]), which is exactly one 32-bit MMA operand
+// register.  The table sits in shared memory with one copy per lane (32 KB), so the
+// lookups of a warp never collide on a bank: a byte costs one byte-extract, one multiply-
+// add for the address and one shared load, instead of the ~10 integer-pipe operations of a
+// per-block byte-permute table.
+//
+// Work split.  The packed codes are walked as stages of [128 rows x 256 k] (16 KB, one TMA
+// box, 128-byte swizzle) together with the tokens' [M x 256] slice (four 64-wide boxes).
+// The stages of all row blocks, k-fastest, are cut into one contiguous run per CTA (one CTA
+// per SM, a deep TMA ring): every SM streams the same number of bytes.  A row block whose
+// stages fall to several CTAs ("pieces") is summed, in CTA order, by the CTA whose piece
+// completes it (atomic stage count); the piece that starts a row block adds the LoRA term
+// s U B^T (B rows by TMA, U from the small-M U kernel) on the tensor cores as well.
+// Inside a stage, warp w dequantizes 64-block (w & 3) of four 16-row groups; the 16
+// contraction slots of an MMA map to k = 16 q + 4 i + {0..3} of the block for lane class q
+// and MMA i (the contraction order is free as long as the token operand uses the same map).
 #include "common.cuh"
 #include "launch.h"
 #include "linear.h"
@@ -37,345 +50,676 @@ int read_and_clear_decode_error(int* out) {
 
 namespace skinny {
 
-constexpr int THREADS = 256;
-constexpr int R = 2;                                 // 8-row groups per warp
-constexpr int ROWS = 8 * R * (THREADS / 32);         // 128 weight rows per CTA
-constexpr int KSTEP = 256;                           // k per stage
-constexpr int STAGE_BYTES = ROWS * KSTEP / 2;        // 16 KB of packed codes
-constexpr int STAGES = 4;
-constexpr int KS_MAX = 1024;                         // k range per CTA (X tile <= 32 KB)
-constexpr int X_BYTES = 16 * KS_MAX * 2;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + X_BYTES + 1024;
+__constant__ float c_levels[16] = QLORA_NF4_LEVELS;
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+constexpr int THREADS = 512;                     // 16 consumer warps
+constexpr int PRODUCERS = 128;                   // one producer warpgroup (one thread per row)
+constexpr int ROWS = 128;                        // weight rows per stage (8 groups of 16)
+constexpr int KSTEP = 256;                       // k per stage (4 blocks of 64)
+constexpr int CODE_BYTES = ROWS * KSTEP / 2;     // 16 KB
+// Byte table: entry v at v * 256 bytes, lane l's copy of it at + 4 l (the upper half of each
+// entry row is unused), so one byte_perm forms the address from the code word and 4 l.
+constexpr int TABLE_BYTES = 256 * 256;
+constexpr int LORA_BOX_BYTES = ROWS * 128;       // B rows [128 x 64 j] bf16, swizzled
+constexpr int LORA_BYTES = 2 * LORA_BOX_BYTES;   // rank up to 128
+constexpr int SU_PITCH = 128 + 8;                // bf16 per token row of the staged sU
+constexpr int SU_BYTES = 16 * SU_PITCH * 2;
+constexpr int SCALE_AHEAD = 4;                   // stages between a scale load and its use
+
+// NT token octets (M <= 8 NT).
+template <int NT>
+struct Cfg {
+  static constexpr int XSLOT = NT * 8 * 128;              // [8 NT tokens x 64 k] bf16
+  static constexpr int STAGE_BYTES = CODE_BYTES + 4 * XSLOT;
+  static constexpr int STAGES = NT == 1 ? 6 : 5;
+  static constexpr int ACC = 2 * NT * 4;                  // accumulators per lane
+  static constexpr int RED_BYTES = (THREADS / 32) * 32 * ACC * 4;
+  // the B-row tile of the LoRA term and the cross-warp reduction share one region: the
+  // tile is consumed before the reduction writes it
+  static constexpr int LR_BYTES = LORA_BYTES > RED_BYTES ? LORA_BYTES : RED_BYTES;
+  static constexpr int SMEM_BYTES = TABLE_BYTES + 1024 + STAGES * STAGE_BYTES + LR_BYTES + SU_BYTES;
+};
+static_assert(Cfg<1>::SMEM_BYTES <= 227 * 1024 - 256, "decode kernel shared memory");
+static_assert(Cfg<2>::SMEM_BYTES <= 227 * 1024 - 256, "decode kernel shared memory");
+
+// Row order inside a 16-row group: MMA row g (and g + 8) is weight row perm8(g) (and + 8),
+// so the four rows a half-warp reads from one swizzled code tile hit eight distinct 16-byte
+// bank groups.
+__device__ __forceinline__ int perm8(int g) { return 2 * (g & 3) + (g >> 2); }
+__device__ __forceinline__ int inv_perm8(int p) { return (p >> 1) + 4 * (p & 1); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
       " {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-
-// 16-byte chunk position of logical chunk `ch` of token row `row` in the X tile: xor by the
-// 64-element window and the row so the 8 lanes of a quarter warp hit 8 distinct bank groups.
-__device__ __forceinline__ int xchunk(int row, int ch) {
-  return ch ^ ((2 * ((ch >> 3) & 3) + row) & 7);
+// Same with a zero accumulator input.
+__device__ __forceinline__ void mma_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
 struct Params {
-  const uint16_t* X;
   int64_t M, N, K;
+  int64_t KB;   // 64-blocks per weight row
+  int64_t KST;  // stages per row block
+  int64_t T;    // stages in all
   const int8_t* qs;
   const float* steps;
   const float* mean;
-  int64_t KS;       // k range per CTA (multiple of 256)
-  int S;            // k ranges per row block
-  float* part;      // [S][M][N]
-  int* tickets;     // [row blocks]
+  int qs_words;        // scale codes of a row's stage are one aligned 32-bit word
+  float* part;         // [CTAs][2][16][128] fp32 pieces of split row blocks
+  int* tickets;        // [row blocks] stages summed so far
   const uint16_t* sU;  // [M][rp] bf16, scale * U
   int64_t rp;
-  const uint16_t* B;   // [N][r]
   int r;
   uint16_t* Y;
 };
 
-__global__ void __launch_bounds__(THREADS, 2)
-    nf4_decode_gemv(const __grid_constant__ CUtensorMap tmCodes, const Params p) {
+// First stage of CTA c, and the CTA that owns stage s, for T stages over G CTAs.
+__device__ __forceinline__ int64_t stage_begin(int64_t T, int64_t G, int64_t c) { return T * c / G; }
+__device__ __forceinline__ int64_t owner_of(int64_t T, int64_t G, int64_t s) {
+  return ((s + 1) * G + T - 1) / T - 1;
+}
+
+__device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_s64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_s128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float2 ld_sf2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+
+// Consumer-warp barrier (the producer warp never joins it).
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+}
+
+// Shared byte offset of stage-scale entry e (0..511) of ring slot sl: the scale tables live
+// in the unused upper halves of the byte-table rows (128 bytes = 32 entries per row).
+__device__ __forceinline__ uint32_t scale_slot_off(int sl, int e) {
+  return static_cast<uint32_t>(((sl * 16 + (e >> 5)) * 256) + 128 + (e & 31) * 4);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
+    nf4_decode_gemv(const __grid_constant__ CUtensorMap tmCodes,
+                    const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using C = Cfg<NT>;
+  constexpr int STAGES = C::STAGES;
+  static_assert(STAGES * 16 <= 256, "scale tables fit the byte-table holes");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sC = smem;                                               // STAGES x [128 rows][128 B]
-  uint4* xs = reinterpret_cast<uint4*>(smem + STAGES * STAGE_BYTES);  // [16][KS / 8] chunks
+  // the byte table first, at the start of the dynamic window (4-byte alignment is all it
+  // needs); the TMA regions after it on a 1024-byte boundary
+  uint8_t* sTab = smem_raw;
+  uint8_t* smem = smem_raw + TABLE_BYTES;
+  smem += (1024u - (smem_u32(smem) & 1023u)) & 1023u;
+  uint8_t* sStage = smem;
+  uint8_t* sLora = sStage + STAGES * C::STAGE_BYTES;
+  float* sRed = reinterpret_cast<float*>(sLora);  // shares the region (see Cfg)
+  uint16_t* sUs = reinterpret_cast<uint16_t*>(sLora + C::LR_BYTES);
   __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t lora_bar;
   __shared__ int abort_flag, s_last;
   volatile int* abort_p = &abort_flag;
+
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, q = lane & 3;
-  const int64_t n0 = (int64_t)blockIdx.x * ROWS;
-  const int64_t k_begin = (int64_t)blockIdx.y * p.KS;
-  const int64_t k_end = (k_begin + p.KS < p.K) ? k_begin + p.KS : p.K;
-  const int nst = static_cast<int>((k_end - k_begin + KSTEP - 1) / KSTEP);
-  const int cpr = static_cast<int>(p.KS / 8);  // X chunks per token row
+  const int64_t G = gridDim.x;
+  const int64_t s_begin = stage_begin(p.T, G, blockIdx.x);
+  const int64_t s_end = stage_begin(p.T, G, blockIdx.x + 1);
+  if (s_begin >= s_end) return;
+  const int64_t rb_first = s_begin / p.KST;
+  const int nst = static_cast<int>(s_end - s_begin);
 
   if (tid == 0) {
-    for (int i = 0; i < STAGES; ++i) mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_bar[i], PRODUCERS / 32);
+      mbar_init(&empty_bar[i], THREADS / 32);
+    }
+    mbar_init(&lora_bar, 1);
     abort_flag = 0;
     fence_barrier_init();
   }
-  __syncthreads();
-  auto issue = [&](int st) {
-    const int slot = st % STAGES;
-    mbar_arrive_expect_tx(&full_bar[slot], STAGE_BYTES);
-    tma_load_2d(sC + slot * STAGE_BYTES, &tmCodes, &full_bar[slot],
-                static_cast<int32_t>((k_begin + (int64_t)st * KSTEP) / 2), static_cast<int32_t>(n0));
-  };
-  if (tid == 0) {
-    tma_prefetch_desc(&tmCodes);
-    for (int st = 0; st < STAGES && st < nst; ++st) issue(st);
+  // fixed byte table (lower half of each row), and the scaled U rows (zero past M and past
+  // the rank padding)
+  for (int i = tid; i < 256 * 32; i += THREADS + PRODUCERS) {
+    const int v = i >> 5;  // uniform across a warp: broadcast constant reads
+    *reinterpret_cast<uint32_t*>(sTab + v * 256 + (i & 31) * 4) =
+        pack_bf16x2(c_levels[v >> 4], c_levels[v & 15]);
   }
-  // the tokens' k range (rows >= M and k >= K are zero)
-  for (int i = tid; i < 16 * cpr; i += THREADS) {
-    const int row = i / cpr, ch = i % cpr;
-    const int64_t k = k_begin + (int64_t)ch * 8;
+  for (int i = tid; i < 16 * (SU_PITCH / 8); i += THREADS + PRODUCERS) {
+    const int t = i / (SU_PITCH / 8), c8 = i % (SU_PITCH / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < p.M && k < k_end) v = __ldg(reinterpret_cast<const uint4*>(p.X + row * p.K + k));
-    xs[row * cpr + xchunk(row, ch)] = v;
+    if (t < p.M && 8 * c8 < p.rp) v = __ldg(reinterpret_cast<const uint4*>(p.sU + t * p.rp + 8 * c8));
+    *reinterpret_cast<uint4*>(sUs + t * SU_PITCH + 8 * c8) = v;
   }
   __syncthreads();
 
-  const float mu = __ldg(p.mean);
-  const int64_t KB = p.K / 64;
-  int lrow[R];
-  int64_t wrow[R];
+  if (warp >= THREADS / 32) {
+    // ============================================================ producer warpgroup
+    // Per stage, thread R of the four producer warps writes the four block scales of weight
+    // row R into the stage's slot table, and lane 0 of the first producer warp issues the
+    // TMA of codes and token slice; the full barrier of a slot counts all four warps.
+    // A row's four scale codes of a stage are one aligned 32-bit word when the 64-blocks
+    // per row are a multiple of 4: that word and its dq step are loaded SCALE_AHEAD stages
+    // early into rotating register sets; otherwise each code is read when needed.
+    const int R = tid - THREADS;
+    const int pw_idx = warp - THREADS / 32;
+    const float mu = __ldg(p.mean);
+    const bool word_path = p.qs_words != 0;
+    const uint32_t tab_s = smem_u32(sTab);
+    const uint32_t x_bytes = 4u * 128u * static_cast<uint32_t>(p.M);
+    const int e0 = 16 * (R >> 4) + 2 * inv_perm8(R & 7) + ((R >> 3) & 1);
+    uint32_t pw[SCALE_AHEAD];
+    float pst[SCALE_AHEAD];
+    int64_t f_n = rb_first * ROWS + R, f_ks = s_begin % p.KST;  // next stage to fetch
+    auto fetch = [&](uint32_t& w, float& st) {
+      w = 0u;
+      st = 0.f;
+      if (f_n < p.N) {
+        const int64_t idx = f_n * p.KB + f_ks * 4;
+        w = __ldg(reinterpret_cast<const uint32_t*>(p.qs + idx));
+        st = __ldg(p.steps + (idx >> 8));
+      }
+      if (++f_ks == p.KST) f_ks = 0, f_n += ROWS;
+    };
+    auto fetch_set = [&](int set) {
+      switch (set) {
+        case 0: fetch(pw[0], pst[0]); break;
+        case 1: fetch(pw[1], pst[1]); break;
+        case 2: fetch(pw[2], pst[2]); break;
+        default: fetch(pw[3], pst[3]); break;
+      }
+    };
+    auto write_set = [&](int slot, int64_t n, int64_t ks, uint32_t w, float st) {
 #pragma unroll
-  for (int rg = 0; rg < R; ++rg) {
-    lrow[rg] = warp * (8 * R) + rg * 8 + g;
-    wrow[rg] = n0 + lrow[rg];
+      for (int b = 0; b < 4; ++b) {
+        const int64_t kb = ks * 4 + b;
+        float v = 0.f;
+        if (n < p.N && kb < p.KB) {
+          if (word_path) {
+            v = __fmaf_rn(static_cast<float>(static_cast<int8_t>((w >> (8 * b)) & 0xFFu)), st, mu);
+          } else {
+            const int64_t idx = n * p.KB + kb;
+            v = __fmaf_rn(static_cast<float>(__ldg(p.qs + idx)), __ldg(p.steps + (idx >> 8)), mu);
+          }
+        }
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(tab_s + scale_slot_off(slot, b * 128 + e0)), "f"(v));
+      }
+    };
+    if (word_path)
+      for (int d = 0; d < SCALE_AHEAD && d < nst; ++d) fetch_set(d);
+    int64_t rb = rb_first, ks = s_begin % p.KST;
+    int slot = 0, issued = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < nst; ++i) {
+      if (i >= STAGES &&
+          !mbar_wait(&empty_bar[slot], phase ^ 1u, kWaitEmpty, abort_p, &g_decode_error))
+        break;
+      const int set = i & (SCALE_AHEAD - 1);
+      const int64_t n = rb * ROWS + R;
+      switch (set) {
+        case 0: write_set(slot, n, ks, pw[0], pst[0]); break;
+        case 1: write_set(slot, n, ks, pw[1], pst[1]); break;
+        case 2: write_set(slot, n, ks, pw[2], pst[2]); break;
+        default: write_set(slot, n, ks, pw[3], pst[3]); break;
+      }
+      if (word_path && i + SCALE_AHEAD < nst) fetch_set(set);
+      __syncwarp();
+      if (lane == 0) {
+        if (pw_idx == 0) {
+          uint8_t* d = sStage + slot * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full_bar[slot], CODE_BYTES + x_bytes);
+          tma_load_2d(d, &tmCodes, &full_bar[slot], static_cast<int32_t>(ks * (KSTEP / 2)),
+                      static_cast<int32_t>(rb * ROWS));
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            tma_load_2d(d + CODE_BYTES + x * C::XSLOT, &tmX, &full_bar[slot],
+                        static_cast<int32_t>(ks * KSTEP + 64 * x), 0);
+        } else {
+          mbar_arrive(&full_bar[slot]);
+        }
+      }
+      issued = i + 1;
+      if (++ks == p.KST) ks = 0, ++rb;
+      if (++slot == STAGES) slot = 0, phase ^= 1u;
+    }
+    __syncthreads();  // with the consumers: everything issued has been consumed or aborted
+    if (pw_idx == 0 && lane == 0 && *abort_p) {
+      // never release shared memory with a copy still landing in it: only the last STAGES
+      // issues can still be in flight (the first producer warp issued them all)
+      for (int k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
+        mbar_drain(&full_bar[k % STAGES], static_cast<uint32_t>((k / STAGES) & 1));
+    }
+    return;
   }
-  auto scale_of = [&](int rg, int st) -> float {
-    const int64_t kq = k_begin + (int64_t)st * KSTEP + 64 * q;
-    if (wrow[rg] >= p.N || kq >= k_end) return 0.f;  // zero table -> zero weights
-    const int64_t b = wrow[rg] * KB + kq / 64;
-    return __fmaf_rn((float)__ldg(p.qs + b), __ldg(p.steps + (b >> 8)), mu);
-  };
-  float sc_next[R];
-#pragma unroll
-  for (int rg = 0; rg < R; ++rg) sc_next[rg] = scale_of(rg, 0);
 
-  float acc[R][4];
+  // ============================================================ consumer warps
+  const int g = lane >> 2, q = lane & 3;
+  const int blk = warp & 3;         // the 64-block of each stage this warp dequantizes
+  const int gi0 = (warp >> 2) * 2;  // its first 16-row group (two per warp)
+  const int lora_boxes = static_cast<int>(p.rp / 64);
+  auto issue_lora = [&](int64_t rb) {
+    mbar_arrive_expect_tx(&lora_bar, static_cast<uint32_t>(lora_boxes * LORA_BOX_BYTES));
+    for (int i = 0; i < lora_boxes; ++i)
+      tma_load_2d(sLora + i * LORA_BOX_BYTES, &tmB, &lora_bar, 64 * i, static_cast<int32_t>(rb * ROWS));
+  };
+  if (tid == 0 && s_begin % p.KST == 0) issue_lora(rb_first);
+  bool lora_pending = s_begin % p.KST == 0;  // a B-row tile is in flight, not yet used
+
+  const uint32_t tab_s = smem_u32(sTab);
+  const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
+  auto lut = [&](uint32_t word, uint32_t j) -> uint32_t {
+    // byte j of the code word at bits 8..15, 4 * lane at bits 0..7: the entry's address
+    return ld_s32(tab_s + __byte_perm(word, lane4, 0x5504u | (j << 4)));
+  };
+
+  float acc[2][NT][4];
 #pragma unroll
-  for (int rg = 0; rg < R; ++rg) acc[rg][0] = acc[rg][1] = acc[rg][2] = acc[rg][3] = 0.f;
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int o = 0; o < NT; ++o) acc[j][o][0] = acc[j][o][1] = acc[j][o][2] = acc[j][o][3] = 0.f;
+
+  // ---------------------------------------------------------------- piece flush
+  // Adds the LoRA term if the piece starts its row block, sums the four block-warps of each
+  // row in a fixed order, and writes Y -- or the piece's partial sums, the last of which
+  // sums all pieces of the row block in CTA order.
+  uint32_t lora_phase = 0;
+  const int nchunks = (p.r + 15) / 16;
+  auto flush = [&](int64_t rb, int64_t ks_first, int64_t ks_last) -> bool {
+    if (ks_first == 0) {
+      if (blk == 0 && mbar_wait(&lora_bar, lora_phase, kWaitLora, abort_p, &g_decode_error)) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int gi = gi0 + j;
+          const int mat = lane >> 3, rr = lane & 7;
+          const int R = 16 * gi + perm8(rr) + 8 * (mat & 1);
+          for (int c = 0; c < nchunks; ++c) {
+            const int jc8 = 2 * c + (mat >> 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(smem_u32(sLora + (jc8 >> 3) * LORA_BOX_BYTES + R * 128 +
+                             (((jc8 & 7) ^ (R & 7)) << 4)),
+                    a0, a1, a2, a3);
+#pragma unroll
+            for (int o = 0; o < NT; ++o) {
+              const uint16_t* ur = sUs + (g + 8 * o) * SU_PITCH + 16 * c + 2 * q;
+              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(ur);
+              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(ur + 8);
+              mma_16816(acc[j][o], a0, a1, a2, a3, b0, b1);
+            }
+          }
+        }
+      }
+      consumers_sync();  // the B-row tile is read before the reduction overwrites it
+    }
+    // every warp's accumulators to shared memory, lane-contiguous
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int o = 0; o < NT; ++o)
+#pragma unroll
+        for (int d = 0; d < 4; ++d)
+          sRed[(warp * C::ACC + (j * NT + o) * 4 + d) * 32 + lane] = acc[j][o][d];
+    consumers_sync();
+    if (*abort_p) return false;  // uniform after the barrier; the B-row tile stays pending
+    if (ks_first == 0) {
+      lora_phase ^= 1u;
+      lora_pending = false;
+    }
+    const bool whole = ks_first == 0 && ks_last == p.KST - 1;
+    const int R = tid & (ROWS - 1);
+    const int64_t n = rb * ROWS + R;
+    const int gi = R >> 4, h = (R >> 3) & 1, gg = inv_perm8(R & 7);
+    const int wb = 4 * (gi >> 1), jj = gi & 1;
+    const int64_t slot = rb == rb_first ? 0 : 1;
+    float* mine = p.part + (static_cast<int64_t>(blockIdx.x) * 2 + slot) * 16 * ROWS;
+    for (int t = tid >> 7; t < p.M; t += THREADS / ROWS) {
+      const int o = t >> 3, qq = (t & 7) >> 1, d = 2 * h + (t & 1);
+      const int idx = ((jj * NT + o) * 4 + d) * 32 + 4 * gg + qq;
+      float v = sRed[(wb + 0) * C::ACC * 32 + idx];
+      v += sRed[(wb + 1) * C::ACC * 32 + idx];
+      v += sRed[(wb + 2) * C::ACC * 32 + idx];
+      v += sRed[(wb + 3) * C::ACC * 32 + idx];
+      if (whole) {
+        if (n < p.N) p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      } else {
+        __stcg(mine + t * ROWS + R, v);
+      }
+    }
+    if (!whole) {
+      __threadfence();
+      consumers_sync();
+      if (tid == 0) {
+        const int add = static_cast<int>(ks_last - ks_first + 1);
+        s_last = atomicAdd(&p.tickets[rb], add) + add == p.KST;
+      }
+      consumers_sync();
+      if (s_last) {
+        __threadfence();
+        const int64_t c_lo = owner_of(p.T, G, rb * p.KST);
+        const int64_t c_hi = owner_of(p.T, G, rb * p.KST + p.KST - 1);
+        for (int t = tid >> 7; t < p.M; t += THREADS / ROWS) {
+          float v = 0.f;
+          for (int64_t c = c_lo; c <= c_hi; ++c) {
+            const int64_t sl = rb == stage_begin(p.T, G, c) / p.KST ? 0 : 1;
+            v += __ldcg(p.part + (c * 2 + sl) * 16 * ROWS + t * ROWS + R);
+          }
+          if (n < p.N) p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        }
+        if (tid == 0) p.tickets[rb] = 0;  // ready for the next launch
+      }
+    }
+    consumers_sync();  // the shared region is free again
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int o = 0; o < NT; ++o) acc[j][o][0] = acc[j][o][1] = acc[j][o][2] = acc[j][o][3] = 0.f;
+    return true;
+  };
+
+  // ---------------------------------------------------------------- main loop
+  // per-lane constant shared-memory offsets: code words of rows R0, R0 + 8 of both groups,
+  // the token fragments, and the scale pairs
+  uint32_t code_off[2], scale_e[2];
+  {
+    const int chunk = 2 * blk + (q >> 1);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int gi = gi0 + j;
+      const int R0 = 16 * gi + perm8(g);  // MMA rows g, g + 8 -> weight rows R0, R0 + 8
+      code_off[j] = R0 * 128 + ((chunk ^ (R0 & 7)) << 4) + (q & 1) * 8;
+      scale_e[j] = ((blk * 8 + gi) * 8 + g) * 2;
+    }
+  }
+  uint32_t x_off[NT][2];
+#pragma unroll
+  for (int o = 0; o < NT; ++o) {
+    const int t = g + 8 * o;
+    x_off[o][0] = CODE_BYTES + blk * C::XSLOT + t * 128 + (((2 * q) ^ g) << 4);
+    x_off[o][1] = CODE_BYTES + blk * C::XSLOT + t * 128 + (((2 * q + 1) ^ g) << 4);
+  }
+  const uint32_t stage_s = smem_u32(sStage);
 
   bool ok = true;
-  for (int st = 0; st < nst; ++st) {
-    float sc[R];
-#pragma unroll
-    for (int rg = 0; rg < R; ++rg) sc[rg] = sc_next[rg];
-    if (st + 1 < nst) {
-#pragma unroll
-      for (int rg = 0; rg < R; ++rg) sc_next[rg] = scale_of(rg, st + 1);
-    }
-    if (!mbar_wait(&full_bar[st % STAGES], (st / STAGES) & 1, kWaitTmaFull, abort_p,
-                   &g_decode_error)) {
-      ok = false;
-      break;
-    }
-    const uint8_t* cs = sC + (st % STAGES) * STAGE_BYTES;
-    Nf4ByteTable tab[R];
-    uint4 cw[R][2];
-#pragma unroll
-    for (int rg = 0; rg < R; ++rg) {
-      tab[rg] = nf4_make_table(sc[rg]);
-      const int row = lrow[rg];
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        cw[rg][h] = *reinterpret_cast<const uint4*>(cs + row * 128 + (((2 * q + h) ^ (row & 7)) << 4));
-    }
-    const int chunk0 = static_cast<int>((int64_t)st * KSTEP / 8) + 8 * q;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 xa = xs[g * cpr + xchunk(g, chunk0 + c)];
-      const uint4 xb = xs[(g + 8) * cpr + xchunk(g + 8, chunk0 + c)];
-#pragma unroll
-      for (int rg = 0; rg < R; ++rg) {
-        const uint4& v = cw[rg][c >> 2];
-        const uint32_t word = (c & 3) == 0 ? v.x : (c & 3) == 1 ? v.y : (c & 3) == 2 ? v.z : v.w;
-        uint32_t w[4];
-        nf4_dequant8(tab[rg], word, w);
-        mma_bf16_16816(acc[rg], xa.x, xb.x, xa.y, xb.y, w[0], w[1]);
-        mma_bf16_16816(acc[rg], xa.z, xb.z, xa.w, xb.w, w[2], w[3]);
+  int64_t rb = rb_first, ks = s_begin % p.KST, ks_first = ks;
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int64_t s = s_begin; s < s_end; ++s) {
+    if (ks == 0 && s != s_begin) {
+      ks_first = 0;
+      if (tid == 0) {
+        fence_proxy_async_smem();  // the last flush's accesses to the region precede the refill
+        issue_lora(rb);
       }
+      lora_pending = true;
     }
-    __syncthreads();  // every warp is done with this stage's buffer
-    if (tid == 0 && st + STAGES < nst) {
-      fence_proxy_async_smem();
-      issue(st + STAGES);
-    }
-  }
-  if (!ok) {
-    __syncthreads();
-    if (tid == 0)  // never release shared memory with a copy still landing in it
-      for (int st = 0; st < nst && st < STAGES; ++st) mbar_drain(&full_bar[st], 0);
-    return;
-  }
-
-  // acc[rg]: [0] token g / row 2q, [1] token g / row 2q+1, [2] token g+8 / 2q, [3] token g+8 / 2q+1
-  float* mine = p.part + (int64_t)blockIdx.y * p.M * p.N;
+    const bool got = mbar_wait(&full_bar[slot], phase, kWaitTmaFull, abort_p, &g_decode_error);
+    if (got) {
+      const uint32_t cs = stage_s + slot * C::STAGE_BYTES;
+      uint32_t xf[NT][8];
 #pragma unroll
-  for (int rg = 0; rg < R; ++rg) {
-    const int64_t n = n0 + warp * (8 * R) + rg * 8 + 2 * q;
-    if (n < p.N) {
-      if (g < p.M) __stcg(reinterpret_cast<float2*>(mine + g * p.N + n), make_float2(acc[rg][0], acc[rg][1]));
-      if (g + 8 < p.M)
-        __stcg(reinterpret_cast<float2*>(mine + (g + 8) * p.N + n), make_float2(acc[rg][2], acc[rg][3]));
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&p.tickets[blockIdx.x], 1) == p.S - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // Last CTA of this row block: sum the k ranges in order, add s U B^T, write Y (bf16).
-  // B rows and sU are staged in the (now idle) code buffers.
-  const int r = p.r;
-  const int bp = r + 1;  // odd pitch in floats: conflict-free row reads
-  float* sB = reinterpret_cast<float*>(sC);                // [128][r + 1]
-  float* sUf = sB + ROWS * bp;                             // [M][r]
-  for (int i = tid; i < ROWS * r; i += THREADS) {
-    const int rr = i / r, j = i % r;
-    const int64_t n = n0 + rr;
-    sB[rr * bp + j] = n < p.N ? __bfloat162float(__ushort_as_bfloat16(p.B[n * r + j])) : 0.f;
-  }
-  for (int i = tid; i < p.M * r; i += THREADS) {
-    const int m = i / r, j = i % r;
-    sUf[i] = __bfloat162float(__ushort_as_bfloat16(p.sU[m * p.rp + j]));
-  }
-  __syncthreads();
-  const int nl = tid % ROWS, half = tid / ROWS;  // 2 threads per row, tokens split in halves
-  const int64_t n = n0 + nl;
-  if (n < p.N) {
-    for (int m = half; m < p.M; m += 2) {
-      float v = 0.f;
-      const float* src = p.part + m * p.N + n;
-      int s = 0;
-      for (; s + 4 <= p.S; s += 4) {
-        const float a0 = __ldcg(src + (int64_t)(s + 0) * p.M * p.N);
-        const float a1 = __ldcg(src + (int64_t)(s + 1) * p.M * p.N);
-        const float a2 = __ldcg(src + (int64_t)(s + 2) * p.M * p.N);
-        const float a3 = __ldcg(src + (int64_t)(s + 3) * p.M * p.N);
-        v += a0; v += a1; v += a2; v += a3;
+      for (int o = 0; o < NT; ++o) {
+        const uint4 lo = ld_s128(cs + x_off[o][0]);
+        const uint4 hi = ld_s128(cs + x_off[o][1]);
+        xf[o][0] = lo.x; xf[o][1] = lo.y; xf[o][2] = lo.z; xf[o][3] = lo.w;
+        xf[o][4] = hi.x; xf[o][5] = hi.y; xf[o][6] = hi.z; xf[o][7] = hi.w;
       }
-      for (; s < p.S; ++s) v += __ldcg(src + (int64_t)s * p.M * p.N);
-      float l = 0.f;
-      for (int j = 0; j < r; ++j) l = fmaf(sUf[m * r + j], sB[nl * bp + j], l);
-      p.Y[m * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v + l));
-    }
-  }
-  if (tid == 0) p.tickets[blockIdx.x] = 0;  // ready for the next launch
-}
-
-// U = X A^T for a few tokens: one CTA per adapter row j (and zero columns r .. rp-1 of sU).
-__global__ void __launch_bounds__(256) small_u(const uint16_t* __restrict__ X, int64_t M, int64_t K,
-                                               const uint16_t* __restrict__ A, int r, int64_t rp,
-                                               float scale, uint16_t* __restrict__ sU,
-                                               float* __restrict__ U_out) {
-  __shared__ float red[8][16];
-  const int j = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (j >= r) {
-    for (int m = tid; m < M; m += blockDim.x) sU[m * rp + j] = 0;
-    return;
-  }
-  float acc[16];
 #pragma unroll
-  for (int m = 0; m < 16; ++m) acc[m] = 0.f;
-  for (int64_t k = (int64_t)tid * 8; k < K; k += (int64_t)blockDim.x * 8) {
-    const uint4 av = __ldg(reinterpret_cast<const uint4*>(A + (int64_t)j * K + k));
-    const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-    float af[8];
+      for (int j = 0; j < 2; ++j) {
+        const uint2 c0 = ld_s64(cs + code_off[j]);
+        const uint2 c1 = ld_s64(cs + code_off[j] + 8 * 128);
+        const float2 sc = ld_sf2(tab_s + scale_slot_off(slot, scale_e[j]));
+        float d[NT][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      af[2 * e] = __uint_as_float(aw[e] << 16);
-      af[2 * e + 1] = __uint_as_float(aw[e] & 0xFFFF0000u);
-    }
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t w0 = m < 2 ? c0.x : c0.y, w1 = m < 2 ? c1.x : c1.y;
+          const uint32_t by = (m & 1) * 2;
+          const uint32_t a0 = lut(w0, by), a2 = lut(w0, by + 1);
+          const uint32_t a1 = lut(w1, by), a3 = lut(w1, by + 1);
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      if (m < M) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(X + (int64_t)m * K + k));
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+          for (int o = 0; o < NT; ++o) {
+            if (m == 0)
+              mma_16816_z(d[o], a0, a1, a2, a3, xf[o][0], xf[o][1]);
+            else
+              mma_16816(d[o], a0, a1, a2, a3, xf[o][2 * m], xf[o][2 * m + 1]);
+          }
+        }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[m] = fmaf(__uint_as_float(xw[e] << 16), af[2 * e], acc[m]);
-          acc[m] = fmaf(__uint_as_float(xw[e] & 0xFFFF0000u), af[2 * e + 1], acc[m]);
+        for (int o = 0; o < NT; ++o) {
+          acc[j][o][0] = __fmaf_rn(sc.x, d[o][0], acc[j][o][0]);
+          acc[j][o][1] = __fmaf_rn(sc.x, d[o][1], acc[j][o][1]);
+          acc[j][o][2] = __fmaf_rn(sc.y, d[o][2], acc[j][o][2]);
+          acc[j][o][3] = __fmaf_rn(sc.y, d[o][3], acc[j][o][3]);
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[slot]);  // this warp is done with the slot
+    if (++slot == STAGES) slot = 0, phase ^= 1u;
+    if (ks == p.KST - 1 || s == s_end - 1) {
+      if (!flush(rb, ks_first, ks)) ok = false;
+      if (!ok) break;  // uniform: decided after a consumer barrier
+    }
+    if (++ks == p.KST) ks = 0, ++rb;
   }
+  (void)ok;
+  __syncthreads();  // with the producer warp
+  if (tid == 0 && lora_pending && *abort_p) mbar_drain(&lora_bar, lora_phase);
+}
+
+// U = X A^T for M <= 16 tokens.  The contraction over K is cut into 256-wide chunks, one
+// CTA each: the chunk of X (tokens padded to 16) and of A (rows padded to rp) is staged in
+// shared memory with 16-byte loads, warp w forms the [16 x 8] tile of adapter rows
+// 8 w (+ 64) on the tensor cores, and the CTA that finishes last sums the chunks in chunk
+// order and writes sU = bf16(scale U) (zero past the rank) and, when asked, U in fp32.
+constexpr int U_KC = 256;
+constexpr int U_PITCH = U_KC + 8;  // bf16 per staged row (+16 bytes: conflict-free ldmatrix)
+
+inline int small_u_smem(int64_t rp) { return static_cast<int>((16 + rp) * U_PITCH * 2); }
+
+__global__ void __launch_bounds__(256) small_u(const uint16_t* __restrict__ X, int64_t M,
+                                               int64_t K, const uint16_t* __restrict__ A, int r,
+                                               int64_t rp, float scale, uint16_t* __restrict__ sU,
+                                               float* __restrict__ U_out, float* __restrict__ part,
+                                               int* __restrict__ ticket) {
+  extern __shared__ __align__(16) uint16_t su_smem[];
+  uint16_t* sX = su_smem;               // [16][U_PITCH]
+  uint16_t* sA = su_smem + 16 * U_PITCH;  // [rp][U_PITCH]
+  __shared__ int s_last;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t k0 = static_cast<int64_t>(blockIdx.x) * U_KC;
+  const int S = gridDim.x;
+  constexpr int C8 = U_KC / 8;  // 16-byte pieces per staged row
+  // stage X (rows >= M zero) and A (rows >= r zero); columns past K zero
+  {
+    const int n = (16 + static_cast<int>(rp)) * C8;
+    for (int base = tid; base < n; base += 4 * 256) {
+      uint4 v[4];
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * 256;
+        const int row = i / C8, c8 = i % C8;
+        const int64_t k = k0 + 8 * c8;
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (i < n && k < K) {
+          if (row < 16) {
+            if (row < M) v[u] = __ldg(reinterpret_cast<const uint4*>(X + row * K + k));
+          } else if (row - 16 < r) {
+            v[u] = __ldg(reinterpret_cast<const uint4*>(A + (row - 16) * K + k));
+          }
+        }
+      }
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int m = 0; m < 16; ++m) red[warp][m] = acc[m];
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * 256;
+        if (i < n) *reinterpret_cast<uint4*>(su_smem + (i / C8) * U_PITCH + 8 * (i % C8)) = v[u];
+      }
+    }
   }
   __syncthreads();
-  if (tid < M) {
-    float u = 0.f;
-    for (int w = 0; w < 8; ++w) u += red[w][tid];
-    sU[tid * rp + j] = __bfloat16_as_ushort(__float2bfloat16_rn(u * scale));
-    if (U_out) U_out[tid * r + j] = u;
+  const int g = lane >> 2, q = lane & 3;
+  float* mine = part + static_cast<int64_t>(blockIdx.x) * 16 * rp;
+  for (int oc = warp; oc < rp / 8; oc += 8) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int kk = 0; kk < U_KC / 16; ++kk) {
+      uint32_t a0, a1, a2, a3, b0, b1;
+      // A operand: tokens x k (rows lane & 15, k half lane >> 4); B operand: k x adapter rows
+      ldsm_x4(smem_u32(sX + (lane & 15) * U_PITCH + 16 * kk + 8 * (lane >> 4)), a0, a1, a2, a3);
+      {
+        const int rr = lane & 7, half = (lane >> 3) & 1;
+        uint32_t t0, t1, t2, t3;
+        ldsm_x4(smem_u32(sA + (8 * oc + rr) * U_PITCH + 16 * kk + 8 * half), t0, t1, t2, t3);
+        b0 = t0;
+        b1 = t1;
+      }
+      mma_16816(d, a0, a1, a2, a3, b0, b1);
+    }
+    // d: [0] token g / row 8 oc + 2q, [1] token g / + 1, [2] token g + 8 / 2q, [3] token g + 8
+    *reinterpret_cast<float2*>(mine + g * rp + 8 * oc + 2 * q) = make_float2(d[0], d[1]);
+    *reinterpret_cast<float2*>(mine + (g + 8) * rp + 8 * oc + 2 * q) = make_float2(d[2], d[3]);
   }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(ticket, 1) == S - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int rpi = static_cast<int>(rp);
+  for (int i = tid; i < static_cast<int>(M) * rpi; i += 256) {
+    const int t = i / rpi, j = i % rpi;
+    float u = 0.f;
+    for (int c = 0; c < S; ++c) u += __ldcg(part + (c * 16 + t) * rpi + j);
+    sU[t * rp + j] = j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(u * scale)) : 0;
+    if (U_out && j < r) U_out[t * r + j] = u;
+  }
+  if (tid == 0) *ticket = 0;  // ready for the next launch
 }
 
 }  // namespace skinny
 
 namespace {
 
-int64_t skinny_ks(int64_t N, int64_t K) {
-  // k range per CTA: a multiple of 256, at most 1024, small enough for ~2 CTAs per SM
-  const int64_t row_blocks = (N + skinny::ROWS - 1) / skinny::ROWS;
-  int64_t want = (2LL * num_sms() + row_blocks - 1) / row_blocks;
-  if (want < 1) want = 1;
-  int64_t ks = (K + want - 1) / want;
-  ks = (ks + skinny::KSTEP - 1) / skinny::KSTEP * skinny::KSTEP;
-  if (ks > skinny::KS_MAX) ks = skinny::KS_MAX;
-  if (ks < skinny::KSTEP) ks = skinny::KSTEP;
-  return ks;
+int64_t skinny_stages(int64_t N, int64_t K) {
+  return ((N + skinny::ROWS - 1) / skinny::ROWS) * ((K + skinny::KSTEP - 1) / skinny::KSTEP);
+}
+
+int64_t skinny_ctas(int64_t N, int64_t K) {
+  const int64_t T = skinny_stages(N, K);
+  return T < num_sms() ? T : num_sms();
+}
+
+template <int NT>
+int run_decode(const CUtensorMap& tmC, const CUtensorMap& tmX, const CUtensorMap& tmB,
+               const skinny::Params& p, unsigned ctas, cudaStream_t stream) {
+  using C = skinny::Cfg<NT>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+      return QLORA_ERR_CUDA;
+    attr = true;
+  }
+  skinny::nf4_decode_gemv<NT><<<ctas, skinny::THREADS + skinny::PRODUCERS, C::SMEM_BYTES, stream>>>(tmC, tmX, tmB, p);
+  return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
 }  // namespace
 
-uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K) {
+uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K, int r) {
   if (M > kSkinnyMaxM) return 0;
-  const int64_t ks = skinny_ks(N, K);
-  const int64_t S = (K + ks - 1) / ks;
-  return (uint64_t)S * M * N * 4;
+  const uint64_t gemv = (uint64_t)skinny_ctas(N, K) * 2 * 16 * skinny::ROWS * 4;
+  const uint64_t u = (uint64_t)((K + skinny::U_KC - 1) / skinny::U_KC) * 16 * round_up(r, 64) * 4;
+  return gemv > u ? gemv : u;
 }
 
 int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   uint16_t* sU = reinterpret_cast<uint16_t*>(ws + L.sU);
   {
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(skinny::small_u, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               skinny::small_u_smem(2 * 64)) != cudaSuccess)
+        return QLORA_ERR_CUDA;
+      attr = true;
+    }
     ProfileScope ps("decode_u", stream);
-    skinny::small_u<<<(unsigned)L.rp, 256, 0, stream>>>(a.X, a.M, a.K, a.A, a.r, L.rp, a.scale, sU,
-                                                        a.U);
+    const unsigned chunks = (unsigned)((a.K + skinny::U_KC - 1) / skinny::U_KC);
+    skinny::small_u<<<chunks, 256, skinny::small_u_smem(L.rp), stream>>>(
+        a.X, a.M, a.K, a.A, a.r, L.rp, a.scale, sU, a.U, reinterpret_cast<float*>(ws + L.part),
+        reinterpret_cast<int*>(ws + L.tickets));
     if (cudaGetLastError() != cudaSuccess) return QLORA_ERR_CUDA;
   }
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             skinny::SMEM_BYTES) != cudaSuccess)
-      return QLORA_ERR_CUDA;
-    attr = true;
-  }
-  CUtensorMap tm;
-  if (!make_tensor_map_2d(&tm, a.q.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)(a.K / 2),
-                          (uint64_t)a.N, (uint64_t)(a.K / 2), 128, skinny::ROWS, MapSwizzle::B128))
-    return QLORA_ERR_CUDA;
+  int st = QLORA_OK;
+  if (a.r % 8 && (st = launch_pad_b(a, L, stream))) return st;
+  CUtensorMap tmC, tmX, tmB;
+  const bool mapped =
+      make_tensor_map_2d(&tmC, a.q.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)(a.K / 2),
+                         (uint64_t)a.N, (uint64_t)(a.K / 2), 128, skinny::ROWS, MapSwizzle::B128) &&
+      make_tensor_map_2d(&tmX, a.X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.K,
+                         (uint64_t)a.M, (uint64_t)a.K * 2, 64, (uint32_t)a.M, MapSwizzle::B128) &&
+      (a.r % 8 == 0  // B [N, r] itself; TMA fills the columns past r with zeros
+           ? make_tensor_map_2d(&tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.r,
+                                (uint64_t)a.N, (uint64_t)a.r * 2, 64, skinny::ROWS, MapSwizzle::B128)
+           : make_tensor_map_2d(&tmB, ws + L.Bp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                (uint64_t)L.rp, (uint64_t)a.N, (uint64_t)L.rp * 2, 64, skinny::ROWS,
+                                MapSwizzle::B128));
+  if (!mapped) return QLORA_ERR_CUDA;
   skinny::Params p{};
-  p.X = a.X;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
+  p.KB = a.K / 64;
+  p.KST = (a.K + skinny::KSTEP - 1) / skinny::KSTEP;
+  p.T = skinny_stages(a.N, a.K);
   p.qs = a.q.scale_codes;
   p.steps = a.q.scale_steps;
   p.mean = a.q.scale_mean;
-  p.KS = skinny_ks(a.N, a.K);
-  p.S = (int)((a.K + p.KS - 1) / p.KS);
+  p.qs_words = (p.KB % 4 == 0 && reinterpret_cast<uintptr_t>(a.q.scale_codes) % 4 == 0) ? 1 : 0;
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.tickets = reinterpret_cast<int*>(ws + L.tickets);
   p.sU = sU;
   p.rp = L.rp;
-  p.B = a.B;
   p.r = a.r;
   p.Y = a.Y;
-  dim3 grid((unsigned)((a.N + skinny::ROWS - 1) / skinny::ROWS), (unsigned)p.S);
+  const unsigned ctas = (unsigned)skinny_ctas(a.N, a.K);
   ProfileScope ps("decode_gemv", stream);
-  skinny::nf4_decode_gemv<<<grid, skinny::THREADS, skinny::SMEM_BYTES, stream>>>(tm, p);
-  return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+  return a.M > 8 ? run_decode<2>(tmC, tmX, tmB, p, ctas, stream)
+                 : run_decode<1>(tmC, tmX, tmB, p, ctas, stream);
 }
 
 }  // namespace qlora
