@@ -1,10 +1,16 @@
-// linear.cu -- orchestration of the LoRA-wrapped NF4 linear layer on one stream.
+// linear.cu -- orchestration of the LoRA-wrapped NF4 linear layer.
 //
 // forward   pad adapters -> U = X A^T (sU = bf16(s U)) -> fused GEMM (M > 16) or the decode
 //           kernel (M <= 16)
-// backward  pad adapters -> U^T (saved or recomputed) -> V = dY B (sV, sV^T)
-//           -> dB = s dY^T U -> fused input-gradient GEMM -> dA = (X^T sV)^T
+// backward  U (saved or recomputed) -> V = dY B (sV) -> fused input-gradient GEMM, with
+//           dB = s dY^T U and dA = (X^T sV)^T on a side stream meanwhile
 // The NF4 buffers are only read (junaidshaukat.com recipe item 3: the base never moves).
+//
+// The input-gradient GEMM leaves SMs idle in its last wave; the two rank-r side products
+// of the backward do not depend on it, so they run on a low-priority side stream forked
+// from the caller's stream (the GEMM is launched first, at the greatest priority) and the
+// caller's stream waits for both before the call returns.  Fork and join are event-based,
+// so the pattern is also captured into CUDA graphs.
 #include <algorithm>
 
 #include "launch.h"
@@ -54,6 +60,42 @@ int linear_forward(const LinearArgs& a, cudaStream_t stream) {
   return launch_fused_fwd(a, L, stream);
 }
 
+namespace {
+
+// Side stream and fork / join events of the calling host thread on the current device.
+struct SideContext {
+  int device = -1;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  int prio_hi = 0;
+  ~SideContext() {
+    if (side) cudaStreamDestroy(side);
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+  }
+};
+
+SideContext* side_context() {
+  thread_local SideContext ctx[8];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8) return nullptr;
+  SideContext& c = ctx[dev];
+  if (c.device == dev) return &c;
+  int least = 0, greatest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, least) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  c.prio_hi = greatest;
+  c.device = dev;
+  return &c;
+}
+
+}  // namespace
+
 int linear_backward(const LinearArgs& a, cudaStream_t stream) {
   const WorkspaceLayout L = workspace_layout(a.M, a.N, a.K, a.r);
   int st = clear_tickets(a, L, stream);
@@ -65,9 +107,23 @@ int linear_backward(const LinearArgs& a, cudaStream_t stream) {
     u32 = w;
   }
   if ((st = launch_lora_v(a, L, stream))) return st;
-  if ((st = launch_lora_db(a, L, u32, stream))) return st;
-  if (a.dX && (st = launch_fused_dx(a, L, stream))) return st;
-  return launch_lora_da(a, L, stream);
+  SideContext* sc = a.dX ? side_context() : nullptr;
+  if (!sc) {
+    if ((st = launch_lora_db(a, L, u32, stream))) return st;
+    if (a.dX && (st = launch_fused_dx(a, L, stream))) return st;
+    return launch_lora_da(a, L, stream);
+  }
+  // fork: the GEMM first (greatest priority) on the caller's stream, then dB and dA on the
+  // side stream; they share the split-reduction workspace only with each other
+  if (cudaEventRecord(sc->fork, stream) != cudaSuccess) return QLORA_ERR_CUDA;
+  LinearArgs hi = a;
+  hi.gemm_priority = sc->prio_hi;
+  if ((st = launch_fused_dx(hi, L, stream))) return st;
+  if (cudaStreamWaitEvent(sc->side, sc->fork, 0) != cudaSuccess) return QLORA_ERR_CUDA;
+  if ((st = launch_lora_db(a, L, u32, sc->side))) return st;
+  if ((st = launch_lora_da(a, L, sc->side))) return st;
+  if (cudaEventRecord(sc->join, sc->side) != cudaSuccess) return QLORA_ERR_CUDA;
+  return cudaStreamWaitEvent(stream, sc->join, 0) == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
 }  // namespace qlora

@@ -31,6 +31,7 @@ struct LinearArgs {
   float* dB;
   void* ws;
   uint64_t ws_bytes;
+  int gemm_priority;    // launch priority of the fused GEMM (0: the stream's own)
 };
 
 // Workspace regions (byte offsets, each 1024-aligned), for rank padded to rp = 64*ceil(r/64).

@@ -307,37 +307,62 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (!s_last) return;
   __threadfence();
 
-  // last CTA of this row tile: fixed-order sum over the splits (float4 pieces, the S loads of
-  // a piece in flight together), then the outputs
+  // last CTA of this row tile: fixed-order sum over the splits, then the outputs.  Each
+  // thread owns PER float4 pieces; 16 partial loads are in flight per batch.
   constexpr int V4 = NJ / 4;
-  for (int i = tid; i < TR * V4; i += THREADS) {
-    const int lr = i / V4, j0 = (i % V4) * 4;
-    const int64_t row = r0 + lr;
-    if (row >= R) continue;
-    const float4* src = reinterpret_cast<const float4*>(part + row * NJ + j0);
-    const int64_t sstride = R * NJ / 4;  // float4 stride between splits
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int PER = TR * V4 / THREADS;
+  constexpr int PB = PER < 2 ? PER : 2;  // pieces per pass
+  constexpr int SB = 16 / PB;            // splits per batch
+  const int64_t sstride = R * NJ / 4;    // float4 stride between splits
+#pragma unroll 1
+  for (int p0 = 0; p0 < PER; p0 += PB) {
+    const float4* src[PB];
+    bool live[PB];
+    float4 v[PB];
+#pragma unroll
+    for (int b = 0; b < PB; ++b) {
+      const int i = tid + (p0 + b) * THREADS;
+      const int64_t row = r0 + i / V4;
+      live[b] = row < R;
+      src[b] = reinterpret_cast<const float4*>(part + (live[b] ? row : r0) * NJ + (i % V4) * 4);
+      v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     int s = 0;
-    for (; s + 4 <= S; s += 4) {
-      const float4 a0 = __ldcg(src + (s + 0) * sstride), a1 = __ldcg(src + (s + 1) * sstride);
-      const float4 a2 = __ldcg(src + (s + 2) * sstride), a3 = __ldcg(src + (s + 3) * sstride);
-      v.x += a0.x; v.y += a0.y; v.z += a0.z; v.w += a0.w;
-      v.x += a1.x; v.y += a1.y; v.z += a1.z; v.w += a1.w;
-      v.x += a2.x; v.y += a2.y; v.z += a2.z; v.w += a2.w;
-      v.x += a3.x; v.y += a3.y; v.z += a3.z; v.w += a3.w;
+    for (; s + SB <= S; s += SB) {
+      float4 a[PB][SB];
+#pragma unroll
+      for (int b = 0; b < PB; ++b)
+#pragma unroll
+        for (int u = 0; u < SB; ++u) a[b][u] = __ldcg(src[b] + (s + u) * sstride);
+#pragma unroll
+      for (int b = 0; b < PB; ++b)
+#pragma unroll
+        for (int u = 0; u < SB; ++u) {
+          v[b].x += a[b][u].x; v[b].y += a[b][u].y; v[b].z += a[b][u].z; v[b].w += a[b][u].w;
+        }
     }
     for (; s < S; ++s) {
-      const float4 a = __ldcg(src + s * sstride);
-      v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
-    }
-    const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = j0 + e;
-      const float x = j < r ? vv[e] : 0.f;
-      if (epi.out32 && j < r) epi.out32[row * epi.ld_row + j * epi.ld_j] = x * epi.scale32;
-      if (epi.op && j < epi.op_cols)
-        epi.op[row * epi.ld_op + j] = __bfloat16_as_ushort(__float2bfloat16_rn(x * epi.scale_op));
+      for (int b = 0; b < PB; ++b) {
+        const float4 a = __ldcg(src[b] + s * sstride);
+        v[b].x += a.x; v[b].y += a.y; v[b].z += a.z; v[b].w += a.w;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < PB; ++b) {
+      if (!live[b]) continue;
+      const int i = tid + (p0 + b) * THREADS;
+      const int64_t row = r0 + i / V4;
+      const int j0 = (i % V4) * 4;
+      const float vv[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j0 + e;
+        const float x = j < r ? vv[e] : 0.f;
+        if (epi.out32 && j < r) epi.out32[row * epi.ld_row + j * epi.ld_j] = x * epi.scale32;
+        if (epi.op && j < epi.op_cols)
+          epi.op[row * epi.ld_op + j] = __bfloat16_as_ushort(__float2bfloat16_rn(x * epi.scale_op));
+      }
     }
   }
   if (epi.op && epi.op_cols > NJ) {  // zero columns of the operand copy past NJ

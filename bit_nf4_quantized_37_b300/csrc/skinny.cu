@@ -621,8 +621,18 @@ __global__ void __launch_bounds__(256) small_u(const uint16_t* __restrict__ X, i
   const int rpi = static_cast<int>(rp);
   for (int i = tid; i < static_cast<int>(M) * rpi; i += 256) {
     const int t = i / rpi, j = i % rpi;
+    const float* src = part + t * rpi + j;
+    const int cs = 16 * rpi;  // stride between chunks
     float u = 0.f;
-    for (int c = 0; c < S; ++c) u += __ldcg(part + (c * 16 + t) * rpi + j);
+    int c = 0;
+    for (; c + 16 <= S; c += 16) {  // 16 loads in flight, summed in chunk order
+      float a[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) a[k] = __ldcg(src + (c + k) * cs);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) u += a[k];
+    }
+    for (; c < S; ++c) u += __ldcg(src + c * cs);
     sU[t * rp + j] = j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(u * scale)) : 0;
     if (U_out && j < r) U_out[t * r + j] = u;
   }

@@ -643,14 +643,24 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   }
   if (!ok) return QLORA_ERR_CUDA;
   ProfileScope ps(kMode == 0 ? "fused_fwd_gemm" : "fused_dx_gemm", stream);
-  if (kPair) {
-    dim3 grid((unsigned)(2 * ((a.M + 511) / 512)), (unsigned)((p.Nout + BN - 1) / BN));
-    fused_pair_gemm<kMode><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tA, tA2, tB2, tOut, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributePriority;
+  attr[0].val.priority = a.gemm_priority;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.gemm_priority ? 1 : 0;
+  cudaError_t e;
+  if (kPair) {  // the CTA pair is the kernel's compile-time cluster shape
+    cfg.gridDim = dim3((unsigned)(2 * ((a.M + 511) / 512)), (unsigned)((p.Nout + BN - 1) / BN));
+    e = cudaLaunchKernelEx(&cfg, fused_pair_gemm<kMode>, tA, tA2, tB2, tOut, p);
   } else {
-    dim3 grid((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM));
-    fused_nf4_lora_gemm<kMode, kAcc><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tA, tA2, tB2, tOut, p);
+    cfg.gridDim = dim3((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM));
+    e = cudaLaunchKernelEx(&cfg, fused_nf4_lora_gemm<kMode, kAcc>, tA, tA2, tB2, tOut, p);
   }
-  return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
 }  // namespace
