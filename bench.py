@@ -163,12 +163,19 @@ def oracle_sample(p, X, Wd, A, B, dY, target_s: float = 12.0):
         return t1 - t0
 
     run(2)  # thread-pool start-up outside the calibration
-    t_rows = run(8) / 8
+    t_rows = run(64) / 64
     t0 = time.perf_counter()
     oracle.lora_dadb(dY, X, A, B, p.scale)
     t_full = time.perf_counter() - t0
-    nrows = int(max(8, min(M, (target_s - t_full) / max(t_rows, 1e-9))))
+
+    def rows_for(per_row):
+        return int(max(8, min(M, (target_s - t_full) / max(per_row, 1e-9))))
+
+    nrows = rows_for(t_rows)
     t_rows_total = run(nrows)
+    if t_rows_total + t_full < 0.6 * target_s and nrows < M:  # calibration ran slow: re-size once
+        nrows = rows_for(t_rows_total / nrows)
+        t_rows_total = run(nrows)
     flops = (2.0 * nrows * (N * K + r * K + r * N) * 2          # Y rows (with U), dX rows (with V)
              + 2.0 * (M * K * r + M * N * r + r * K * M + N * r * M))  # U, V, dA, dB over all M
     secs = t_rows_total + t_full

@@ -37,8 +37,8 @@ struct LinearArgs {
 // Workspace regions (byte offsets, each 1024-aligned), for rank padded to rp = 64*ceil(r/64).
 struct WorkspaceLayout {
   int64_t rp;
-  uint64_t sU;       // bf16 [M, rp]  scale * U, zero columns past r
-  uint64_t sV;       // bf16 [M, rp]  scale * V
+  uint64_t sU;       // bf16 [M, rp]  scale * U (columns past r: read as TMA zero fill)
+  uint64_t sV;       // bf16 [M, rp]  scale * V (the same)
   uint64_t U32;      // fp32 [M, r]   U recomputed by the backward when none is saved
   uint64_t Bp;       // bf16 [N, rp]  B zero-padded (only for r not a multiple of 8)
   uint64_t part;     // fp32 split-contraction partial sums (side products, decode path)

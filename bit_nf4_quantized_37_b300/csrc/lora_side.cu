@@ -510,7 +510,7 @@ int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cud
   e.ld_j = 1;
   e.op = reinterpret_cast<uint16_t*>(ws + L.sU);
   e.ld_op = L.rp;
-  e.op_cols = (int)L.rp;
+  e.op_cols = a.r;  // readers see the columns past r as zeros (TMA fill)
   e.scale_op = a.scale;
   return run_side<false>("side_u", a.X, a.M, a.K, a.K, qs, a.r, e, a, L, stream);
 }
@@ -522,7 +522,7 @@ int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t st
   side::Epi e = no_epi();
   e.op = reinterpret_cast<uint16_t*>(ws + L.sV);
   e.ld_op = L.rp;
-  e.op_cols = (int)L.rp;
+  e.op_cols = a.r;  // readers see the columns past r as zeros (TMA fill)
   e.scale_op = a.scale;
   return run_side<false>("side_v", a.dY, a.M, a.N, a.N, qs, a.r, e, a, L, stream);
 }

@@ -628,7 +628,7 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
     p.Nout = a.N;
     p.Kc = a.K;
     ok = map_bf16(&tA, a.X, a.K, a.M, a.K, 64, BM, MapSwizzle::B128) &&
-         map_bf16(&tA2, ws + L.sU, rp, a.M, rp, 64, BM, MapSwizzle::B128) &&
+         map_bf16(&tA2, ws + L.sU, a.r, a.M, rp, 64, BM, MapSwizzle::B128) &&  // zeros past r
          (a.r % 8 == 0  // B [N, r] itself; TMA fills the columns past r with zeros
               ? map_bf16(&tB2, a.B, a.r, a.N, a.r, 64, BNB, MapSwizzle::B128)
               : map_bf16(&tB2, ws + L.Bp, rp, a.N, rp, 64, BNB, MapSwizzle::B128)) &&
@@ -637,7 +637,7 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
     p.Nout = a.K;
     p.Kc = a.N;
     ok = map_bf16(&tA, a.dY, a.N, a.M, a.N, 64, BM, MapSwizzle::B128) &&
-         map_bf16(&tA2, ws + L.sV, rp, a.M, rp, 64, BM, MapSwizzle::B128) &&
+         map_bf16(&tA2, ws + L.sV, a.r, a.M, rp, 64, BM, MapSwizzle::B128) &&  // zeros past r
          map_bf16(&tB2, a.A, a.K, a.r, a.K, 64, 64, MapSwizzle::B128) &&  // rows past r: zeros
          map_bf16(&tOut, a.dX, a.K, a.M, a.K, 32, 32, MapSwizzle::B64);
   }
