@@ -255,14 +255,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         const int kc = s - p.n_lora;
-        const bool odd = kc & 1;
-        const Slice cur = odd ? pf1 : pf0;
-        if (kc + 2 < n_main) {
-          int64_t row, col;
-          slice_coords(kc + 2, row, col);
-          if (odd) load_slice(pf1, p, row, col);
-          else load_slice(pf0, p, row, col);
-        }
+        const Slice cur = (kc & 1) ? pf1 : pf0;  // loaded two stages ago
         uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
         if (cur.valid) {
           const Nf4ByteTable tab = nf4_make_table(__fmaf_rn((float)cur.q, cur.step, mu));
@@ -283,6 +276,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bready_bar[slot]);
+      // the slice two stages ahead goes into the register set just consumed; its loads are
+      // issued after the (release) arrive above, which therefore never waits for them
+      if (s >= p.n_lora) {
+        const int kc = s - p.n_lora;
+        if (kc + 2 < n_main) {
+          int64_t row, col;
+          slice_coords(kc + 2, row, col);
+          if (kc & 1) load_slice(pf1, p, row, col);
+          else load_slice(pf0, p, row, col);
+        }
+      }
     }
 
     // ------------------------------------------------------------ epilogue
@@ -344,7 +348,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // x 64 multiply-adds: twice the tensor work per integer-pipe instruction of the single-CTA
 // 256 x 256 tile, and a quarter of its W tile in shared memory.
 //   full_bar   (leader) TMA bytes of both CTAs            waited by the leader's UMMA thread
-//   bready_bar (leader) 4 dequant warps of each CTA       waited by the leader's UMMA thread
+//   bready_bar (leader) the leader's 4 dequant warps + one peer relay lane, waited by the
+//                       leader's UMMA thread
+//   pready_bar (peer)   the peer's 4 dequant warps        waited by the peer's relay lane
+// The dequant warps signal at CTA scope only; one lane of the peer per ring slot forwards
+// each stage to the leader with a single cluster-scope release (measured: a cluster-scope
+// release costs ~0.6 us, more than the dequantization of a stage; one per warp and stage
+// made the dequant warps the bottleneck, one thread for all stages made it the relay).
 //   empty_bar  (each)   multicast tcgen05.commit          waited by each CTA's producers
 //   acc_bar    (each)   multicast tcgen05.commit          waited by each CTA's epilogue
 // Two dequant groups of 4 warps take alternate stages (one 64-weight block per thread each).
@@ -372,6 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t bready_bar[STAGES];
+  __shared__ __align__(8) uint64_t pready_bar[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
   __shared__ __align__(8) uint64_t acc_bar;
   __shared__ uint32_t tmem_slot;
@@ -391,7 +402,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full_bar[i], 1);
-      mbar_init(&bready_bar[i], 2 * GROUP_WARPS);
+      mbar_init(&bready_bar[i], GROUP_WARPS + 1);
+      mbar_init(&pready_bar[i], GROUP_WARPS);
       mbar_init(&empty_bar[i], 1);
     }
     mbar_init(&acc_bar, 1);
@@ -470,6 +482,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (ok) umma_commit_pair(&acc_bar, 0x3);
     }
     __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ relay (peer)
+    // each stage's dequantized half of the peer, forwarded to the leader's bready barrier;
+    // one lane per ring slot, so the (slow) cluster-scope releases of consecutive stages
+    // are in flight together
+    if (rank == 1 && lane < STAGES) {
+      const uint32_t bready_lead = mapa_shared(smem_u32(&bready_bar[lane]), 0);
+      for (int s = lane; s < total; s += STAGES) {
+        if (!mbar_wait(&pready_bar[lane], (s / STAGES) & 1, kWaitBReady, abort_p, &g_gemm_error))
+          break;
+        mbar_arrive_cluster(bready_lead);
+      }
+    }
+    __syncwarp();
   } else if (warp >= DEQ_WARP0) {
     // ------------------------------------------------------------ NF4 producers (both CTAs)
     const int group = (warp - DEQ_WARP0) / GROUP_WARPS;           // owns stages s % 2 == group
@@ -495,45 +521,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (kMode == 0) load_slice(sl, p, row_base, (int64_t)kc * BK);
       else load_slice(sl, p, (int64_t)kc * BK + row_base, kcol);
     };
-    int s = group;
-    Slice cur;
-    cur.valid = false;
-    if (s >= p.n_lora && s < total) slice_at(s, cur);
-    bool ok = true;
-    for (; s < total; s += 2) {
+    // Each stage is dequantized into registers before its ring slot is free (while the group
+    // waits for it), so a freed slot only takes the stores, the proxy fence and the signal.
+    // The group's slices alternate between two register sets; a set is refilled right after
+    // the stage it held was dequantized, one group iteration before it is needed again.
+    uint4 rv[8];
+    auto dequant = [&](const Slice& cur) {
+      if (cur.valid) {
+        const Nf4ByteTable tab = nf4_make_table(__fmaf_rn((float)cur.q, cur.step, mu));
+        const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
+                                   cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[4];
+          nf4_dequant8(tab, words[c], o);
+          rv[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) rv[c] = make_uint4(0, 0, 0, 0);
+      }
+    };
+    auto put = [&](int s) -> bool {
       const int slot = s % STAGES, round = s / STAGES;
-      Slice nxt;  // the group's next stage (also after a LoRA stage), in flight meanwhile
-      nxt.valid = false;
-      if (s + 2 < total && s + 2 >= p.n_lora) slice_at(s + 2, nxt);
       if (s >= p.n_lora) {
         if (round > 0 &&
-            !mbar_wait<true>(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) {
-          ok = false;
-          break;
-        }
+            !mbar_wait<true>(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
+          return false;
         uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
-        if (cur.valid) {
-          const Nf4ByteTable tab = nf4_make_table(__fmaf_rn((float)cur.q, cur.step, mu));
-          const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
-                                     cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t o[4];
-            nf4_dequant8(tab, words[c], o);
-            *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(0, 0, 0, 0);
-        }
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = rv[c];
         // this CTA's generic-proxy writes, ordered before the tensor core's (async-proxy)
-        // reads; the leader sees them through the release/acquire of the cluster arrive below
+        // reads; the leader sees them through the barriers below
         fence_proxy_async_smem();
       }
-      cur = nxt;
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bready_bar[slot]), 0));
+      if (lane == 0) mbar_arrive(rank == 0 ? &bready_bar[slot] : &pready_bar[slot]);
+      return true;
+    };
+    auto refill = [&](int s, Slice& sl) {
+      sl.valid = false;
+      if (s < total && s >= p.n_lora) slice_at(s, sl);
+    };
+    Slice sa, sb;
+    refill(group, sa);
+    refill(group + 2, sb);
+    if (group >= p.n_lora) dequant(sa);
+    bool ok = true;
+    for (int s = group; s < total && ok; s += 4) {
+      if (!(ok = put(s))) break;
+      refill(s + 4, sa);
+      if (s + 2 >= total) break;
+      if (s + 2 >= p.n_lora) dequant(sb);
+      if (!(ok = put(s + 2))) break;
+      refill(s + 6, sb);
+      if (s + 4 < total && s + 4 >= p.n_lora) dequant(sa);
     }
 
     // ------------------------------------------------------------ epilogue (both CTAs)
