@@ -274,10 +274,12 @@ def main():
     torch.cuda.synchronize()
 
     # The timed step is one CUDA-graph replay of forward + backward (the library's launches
-    # captured once; per-kernel CUDA events are captured with them, so the profile below is
-    # the device time of each kernel in the last timed replay).  --eager times the calls
-    # as issued from Python instead.
-    graph = None
+    # captured once).  Per-kernel device times come from a second graph of the same step
+    # captured with the library's per-kernel CUDA events, replayed for the same number of
+    # steps right after the timed ones (event nodes between kernels would cut the
+    # programmatic-launch overlap of the timed graph).  --eager times the calls as issued
+    # from Python instead, with the events in the same calls.
+    graph = graph_prof = None
     if not args.eager:
         qn.profile_start()  # fill the event pool before capture
         step()
@@ -290,11 +292,15 @@ def main():
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
-        qn.profile_start()
         with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            step()
+        graph_prof = torch.cuda.CUDAGraph()
+        qn.profile_start()  # its records (the captured event nodes) stay live until the end
+        with torch.cuda.graph(graph_prof, capture_error_mode="thread_local"):
             step()
         for _ in range(args.warmup):
             graph.replay()
+            graph_prof.replay()
         torch.cuda.synchronize()
 
     clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
@@ -316,12 +322,18 @@ def main():
         ev[i][1].record()
     torch.cuda.synchronize()
     barrier(world)
+    if graph is not None:  # the per-kernel profile: same steps, same flushes
+        for i in range(args.steps):
+            flush_buf.zero_()
+            graph_prof.replay()
+        torch.cuda.synchronize()
     prof = qn.profile_stop()
     clk = clocks.stop() if clocks else None
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(sum(step_ms), world)
     flops_step = p.fwd_bwd_flops()
     value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
+    # launches recorded per captured step (graph) or over all steps (eager)
     launches = sum(v[0] for v in prof.values()) * (args.steps if graph is not None else 1)
 
     # dominant kernel and its roofline (algorithmic FLOPs per launch / mean launch time)

@@ -136,6 +136,18 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// ------------------------------------------------------------------ dependent launch
+// A kernel launched with programmatic stream serialization may start before the kernel in
+// front of it in the stream has finished; grid_dependency_wait() returns once that kernel
+// has completed and its memory writes are visible.  launch_dependents() lets the next such
+// kernel be scheduled as soon as every CTA of this one has issued it (a no-op otherwise).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     abort_flag = 0;
     fence_barrier_init();
   }
+  launch_dependents();  // the fused GEMM that reads this output may be scheduled meanwhile
   __syncthreads();
 
   // One thread streams P with TMA: K-major tiles are one [64 c x 128 rows] box (row r at

@@ -5,7 +5,8 @@
 // multiply.  Here that "inside" is literal: warps expand the packed 4-bit codes of each
 // 64-wide k-slice straight into the shared-memory operand tile of tcgen05.mma, so W' never
 // exists in HBM.  The rank-r LoRA term rides in the same TMEM accumulator as extra
-// contraction stages in front of the NF4 stages:
+// contraction stages after the NF4 stages (so the GEMM can start, as a programmatic
+// dependent launch, while the kernel producing sU / sV is still finishing):
 //   forward          Y  = [X  | sU] . [W' | B]^T       (contract over K, then over r)
 //   input gradient   dX = [dY | sV] . [W' ; A]         (contract over N, then over r)
 //
@@ -66,7 +67,7 @@ struct Params {
   int64_t Kc;     // NF4 contraction length (forward: K, input gradient: N)
   int64_t Kw;     // columns of W (K)
   int64_t Nw;     // rows of W (N)
-  int n_lora;     // LoRA stages in front of the NF4 stages
+  int n_lora;     // LoRA stages after the NF4 stages
   int lora_last_k16;
   const uint8_t* codes;
   const int8_t* qs;
@@ -166,19 +167,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (round > 0 && !mbar_wait(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) break;
         uint8_t* a_dst = smem + slot * STAGE_BYTES;
         uint8_t* b_dst = a_dst + A_BYTES;
-        if (s < p.n_lora) {
+        if (s >= n_main) {
+          const int li = s - n_main;
+          if (li == 0) grid_dependency_wait();  // sU / sV (and Bp) come from the kernel before
           mbar_arrive_expect_tx(&full_bar[slot], A_BYTES + B_BYTES);
-          tma_load_2d(a_dst, &tmA2, &full_bar[slot], s * BK, (int32_t)m0);
+          tma_load_2d(a_dst, &tmA2, &full_bar[slot], li * BK, (int32_t)m0);
           if (kMode == 0) {
-            tma_load_2d(b_dst, &tmB2, &full_bar[slot], s * BK, (int32_t)n0);
+            tma_load_2d(b_dst, &tmB2, &full_bar[slot], li * BK, (int32_t)n0);
           } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              tma_load_2d(b_dst + i * 8192, &tmB2, &full_bar[slot], (int32_t)(n0 + 64 * i), s * BK);
+              tma_load_2d(b_dst + i * 8192, &tmB2, &full_bar[slot], (int32_t)(n0 + 64 * i), li * BK);
           }
         } else {
           mbar_arrive_expect_tx(&full_bar[slot], A_BYTES);
-          tma_load_2d(a_dst, &tmA, &full_bar[slot], (s - p.n_lora) * BK, (int32_t)m0);
+          tma_load_2d(a_dst, &tmA, &full_bar[slot], s * BK, (int32_t)m0);
         }
       }
       // never leave with a load in flight: the last issued stages must have landed
@@ -193,13 +196,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int s = 0; s < total && ok; ++s) {
         const int slot = s % STAGES, round = s / STAGES;
+        // the LoRA stages (the last ones) come entirely by TMA: no dequantized tile to wait for
         ok = mbar_wait(&full_bar[slot], round & 1, kWaitTmaFull, abort_p, &g_gemm_error) &&
-             mbar_wait(&bready_bar[slot], round & 1, kWaitBReady, abort_p, &g_gemm_error);
+             (s >= n_main ||
+              mbar_wait(&bready_bar[slot], round & 1, kWaitBReady, abort_p, &g_gemm_error));
         if (!ok) break;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(smem + slot * STAGE_BYTES);
         const uint32_t b_addr = a_addr + A_BYTES;
-        const int ksteps = (s < p.n_lora && s == p.n_lora - 1) ? p.lora_last_k16 : 4;
+        const int ksteps = (s >= n_main && s == total - 1) ? p.lora_last_k16 : 4;
         for (int kk = 0; kk < ksteps; ++kk) {
           const uint64_t bdesc = (kMode == 0)
                                      ? smem_desc(b_addr + kk * 32, 16, 1024, Swizzle::B128)
@@ -247,14 +252,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (n_main > 1) { slice_coords(1, row, col); load_slice(pf1, p, row, col); }
     }
     bool ok = true;
-    for (int s = 0; s < total; ++s) {
+    for (int s = 0; s < n_main; ++s) {  // the NF4 stages (the LoRA stages after them need nothing)
       const int slot = s % STAGES, round = s / STAGES;
-      if (s >= p.n_lora) {
+      {
         if (round > 0 && !mbar_wait(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) {
           ok = false;
           break;
         }
-        const int kc = s - p.n_lora;
+        const int kc = s;
         const Slice cur = (kc & 1) ? pf1 : pf0;  // loaded two stages ago
         uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
         if (cur.valid) {
@@ -278,8 +283,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(&bready_bar[slot]);
       // the slice two stages ahead goes into the register set just consumed; its loads are
       // issued after the (release) arrive above, which therefore never waits for them
-      if (s >= p.n_lora) {
-        const int kc = s - p.n_lora;
+      {
+        const int kc = s;
         if (kc + 2 < n_main) {
           int64_t row, col;
           slice_coords(kc + 2, row, col);
@@ -431,19 +436,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t full_lead = mapa_shared(smem_u32(&full_bar[slot]), 0);
         uint8_t* a_dst = smem + slot * STAGE_BYTES;
         uint8_t* b_dst = a_dst + A_BYTES;
-        if (s < p.n_lora) {
+        if (s >= n_main) {
+          const int li = s - n_main;
+          if (li == 0) grid_dependency_wait();  // sU / sV (and Bp) come from the kernel before
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[slot], 2 * (A_BYTES + B_BYTES));
-          tma_load_2d_pair(a_dst, &tmA2, full_lead, s * BK, (int32_t)m0);
+          tma_load_2d_pair(a_dst, &tmA2, full_lead, li * BK, (int32_t)m0);
           if (kMode == 0) {
-            tma_load_2d_pair(b_dst, &tmB2, full_lead, s * BK, (int32_t)nb0);
+            tma_load_2d_pair(b_dst, &tmB2, full_lead, li * BK, (int32_t)nb0);
           } else {
 #pragma unroll
             for (int i = 0; i < 2; ++i)
-              tma_load_2d_pair(b_dst + i * 8192, &tmB2, full_lead, (int32_t)(nb0 + 64 * i), s * BK);
+              tma_load_2d_pair(b_dst + i * 8192, &tmB2, full_lead, (int32_t)(nb0 + 64 * i), li * BK);
           }
         } else {
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[slot], 2 * A_BYTES);
-          tma_load_2d_pair(a_dst, &tmA, full_lead, (s - p.n_lora) * BK, (int32_t)m0);
+          tma_load_2d_pair(a_dst, &tmA, full_lead, s * BK, (int32_t)m0);
         }
       }
       // the leader's full barriers count both CTAs' copies: the leader drains them
@@ -459,13 +466,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int s = 0; s < total && ok; ++s) {
         const int slot = s % STAGES, round = s / STAGES;
+        // the LoRA stages (the last ones) come entirely by TMA: no dequantized tile to wait for
         ok = mbar_wait<true>(&full_bar[slot], round & 1, kWaitTmaFull, abort_p, &g_gemm_error) &&
-             mbar_wait<true>(&bready_bar[slot], round & 1, kWaitBReady, abort_p, &g_gemm_error);
+             (s >= n_main ||
+              mbar_wait<true>(&bready_bar[slot], round & 1, kWaitBReady, abort_p, &g_gemm_error));
         if (!ok) break;
         tc_fence_after();
         const uint32_t a_addr = smem_u32(smem + slot * STAGE_BYTES);
         const uint32_t b_addr = a_addr + A_BYTES;
-        const int ksteps = (s < p.n_lora && s == p.n_lora - 1) ? p.lora_last_k16 : 4;
+        const int ksteps = (s >= n_main && s == total - 1) ? p.lora_last_k16 : 4;
         for (int kk = 0; kk < ksteps; ++kk) {
           const uint64_t bdesc = (kMode == 0)
                                      ? smem_desc(b_addr + kk * 32, 16, 1024, Swizzle::B128)
@@ -489,7 +498,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // are in flight together
     if (rank == 1 && lane < STAGES) {
       const uint32_t bready_lead = mapa_shared(smem_u32(&bready_bar[lane]), 0);
-      for (int s = lane; s < total; s += STAGES) {
+      for (int s = lane; s < n_main; s += STAGES) {
         if (!mbar_wait(&pready_bar[lane], (s / STAGES) & 1, kWaitBReady, abort_p, &g_gemm_error))
           break;
         mbar_arrive_cluster(bready_lead);
@@ -517,7 +526,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       swz = nl & 7;
     }
     auto slice_at = [&](int s, Slice& sl) {
-      const int kc = s - p.n_lora;
+      const int kc = s;
       if (kMode == 0) load_slice(sl, p, row_base, (int64_t)kc * BK);
       else load_slice(sl, p, (int64_t)kc * BK + row_base, kcol);
     };
@@ -542,9 +551,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < 8; ++c) rv[c] = make_uint4(0, 0, 0, 0);
       }
     };
-    auto put = [&](int s) -> bool {
+    auto put = [&](int s) -> bool {  // NF4 stages only
       const int slot = s % STAGES, round = s / STAGES;
-      if (s >= p.n_lora) {
+      {
         if (round > 0 &&
             !mbar_wait<true>(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
           return false;
@@ -561,21 +570,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     };
     auto refill = [&](int s, Slice& sl) {
       sl.valid = false;
-      if (s < total && s >= p.n_lora) slice_at(s, sl);
+      if (s < n_main) slice_at(s, sl);
     };
     Slice sa, sb;
     refill(group, sa);
     refill(group + 2, sb);
-    if (group >= p.n_lora) dequant(sa);
+    if (group < n_main) dequant(sa);
     bool ok = true;
-    for (int s = group; s < total && ok; s += 4) {
+    for (int s = group; s < n_main && ok; s += 4) {
       if (!(ok = put(s))) break;
       refill(s + 4, sa);
-      if (s + 2 >= total) break;
-      if (s + 2 >= p.n_lora) dequant(sb);
+      if (s + 2 >= n_main) break;
+      if (s + 2 < n_main) dequant(sb);
       if (!(ok = put(s + 2))) break;
       refill(s + 6, sb);
-      if (s + 4 < total && s + 4 >= p.n_lora) dequant(sa);
+      if (s + 4 < n_main) dequant(sa);
     }
 
     // ------------------------------------------------------------ epilogue (both CTAs)
@@ -689,11 +698,16 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributePriority;
-  attr[0].val.priority = a.gemm_priority;
+  // programmatic dependent launch: the GEMM may start while the kernel before it (the
+  // rank-r product it reads in its last stages) finishes; its TMA thread waits for that
+  // kernel before the first LoRA-stage load
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributePriority;
+  attr[1].val.priority = a.gemm_priority;
   cfg.attrs = attr;
-  cfg.numAttrs = a.gemm_priority ? 1 : 0;
+  cfg.numAttrs = a.gemm_priority ? 2 : 1;
   cudaError_t e;
   if (kPair) {  // the CTA pair is the kernel's compile-time cluster shape
     cfg.gridDim = dim3((unsigned)(2 * ((a.M + 511) / 512)), (unsigned)((p.Nout + BN - 1) / BN));
