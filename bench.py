@@ -482,6 +482,7 @@ def measure_secondary(qn, wl, dev, peaks, traffic, flush_buf, reps: int = 10):
             "ms": ms_all, "bytes": nbytes,
             "gemv_kernel_GB/s": meta / ms_gemv / 1e6,
             "gemv_kernel_frac_hbm": meta / ms_gemv / 1e6 / hbm,
+            "gemv_traffic": traffic.get(("decode_gemv", "config4")) if M == 1 else None,
             "kernels_ms": {k: v[1] / reps for k, v in prof.items()}}
     return out
 
