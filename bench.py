@@ -440,17 +440,46 @@ def measure_secondary(qn, wl, dev, peaks, traffic, flush_buf, reps: int = 10):
     meta = q.storage_bytes()
     Wd = torch.empty(p4.N, p4.K, dtype=torch.bfloat16, device=dev)
 
+    def capture(body):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            body()
+        return graph
+
+    def replay_ms(graph):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        graph.replay()  # warm
+        torch.cuda.synchronize()
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
     def timed(fn, names):
+        # Whole-call device time: reps x (L2 flush + call) as one CUDA graph, minus the same
+        # graph of flushes alone (no event nodes between the library's launches, so its
+        # programmatic-launch overlaps stay).  Per-kernel times: a third graph of the same
+        # sequence with the library's per-kernel events.
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
+
+        def calls():
+            for _ in range(reps):
+                flush_buf.zero_()
+                fn()
+
+        def flushes():
+            for _ in range(reps):
+                flush_buf.zero_()
+
+        ms = (replay_ms(capture(calls)) - replay_ms(capture(flushes))) / reps
         qn.profile_start()
-        for _ in range(reps):
-            flush_buf.zero_()
-            fn()
+        g_prof = capture(calls)
+        g_prof.replay()
         torch.cuda.synchronize()
         prof = qn.profile_stop()
-        ms = sum(prof[n][1] for n in names if n in prof) / reps
         return ms, prof
 
     hbm = peaks["hbm_gbs"]

@@ -25,148 +25,179 @@ constexpr int64_t kGroupElems = (int64_t)kBlock * kGroup;  // 16384 weights
 constexpr int kQuantThreads = 256;
 
 // -------------------------------------------------------------------- pass 1
-// One CTA per group of 256 blocks (16384 weights).
+// Persistent CTAs, each taking groups of 256 blocks (16384 weights) in a grid-stride loop.
 //
-// Full groups: four lanes per 64-block, 16 weights per lane (four float4 loads), so a block's
-// absmax is 15 max operations and two shuffles.  The exact quotient x = RN(w / a) is never
-// needed away from a threshold: y = RN(w * RN(1/a)) is within 3 * 2^-24 * |x| of x, so
-// whenever y is more than 2^-20 from every threshold, y and x fall between the same two
-// thresholds and the level follows from y.  The level comes from a shared-memory table over
-// cells of y (sign, binade, top 4 mantissa bits for |y| in [2^-5, 1]): each cell holds at most
-// one threshold T, the level is c_lo + (y > T), and |y - T| < 2^-20 sends that weight to the
-// exact division (thresholds lie >= 2.3e-4 inside their cells, so a threshold between x and y
-// is always the one in y's cell).  |y| < 2^-5 is level 7 outright.
+// Full groups: four lanes per 64-block, 16 weights per lane (four float4 loads, the next
+// group's first loads in flight across the group boundary), so a block's absmax is 15 max
+// operations and two shuffles.  The exact quotient x = RN(w / a) is never needed away from a
+// threshold: y = RN(w * RN(1/a)) is within 3 * 2^-24 * |x| of x, so whenever y is more than
+// 2^-20 from every threshold, y and x fall between the same two thresholds and the level
+// follows from y.  The level comes from a shared-memory table over cells of y (sign; cell 0
+// for |y| < 2^-5, then binade and top 4 mantissa bits for |y| in [2^-5, 1.0625)): each cell
+// holds at most one threshold T, the level is c_lo + (y > T), and |y - T| < 2^-20 (or a
+// non-finite y) sends the lane's 16 weights to the exact division (thresholds lie
+// >= 2.3e-4 inside their cells, so a threshold between x and y is always the one in y's
+// cell).  The table is built once per CTA, one interleaved copy per lane (entry i of copy l
+// at word pair 32 i + l), so the 8-byte lookups of a half-warp never collide on a bank.
 // The last, partial group takes the element-by-element path with the exact division.
-constexpr int kCells = 81;                 // |y| cells: 5 binades x 16, plus [1, 1.0625)
+constexpr int kCells = 82;                  // per sign: [0, 2^-5), then 5 binades x 16, [1, 1.0625)
+constexpr int kCopies = 32;                 // one table copy per lane
 constexpr uint32_t kCellBase = 0x3D000000u;  // bits of 2^-5
 constexpr float kGuard = 0x1p-20f;
+constexpr int kCellBytes = 2 * kCells * kCopies * 8;  // 41 KB of dynamic shared memory
 
 __device__ __forceinline__ uint32_t code_exact(float w, float a) {
   return a == 0.0f ? nf4_code(0.0f) : nf4_code(__fdiv_rn(w, a));
 }
 
-// cell table entry: (threshold inside the cell or +inf, lowest level of the cell)
+// cell table entry: (threshold inside the cell or +inf, lowest level of the cell), entry i of
+// copy c at tab[i * kCopies + c]
 __device__ void build_cells(float2* tab) {
   constexpr float T[15] = QLORA_NF4_THRESHOLDS;
   for (int i = threadIdx.x; i < 2 * kCells; i += blockDim.x) {
     const int neg = i / kCells, idx = i % kCells;
-    const float lo = __uint_as_float(kCellBase + (static_cast<uint32_t>(idx) << 19));
-    const float hi = __uint_as_float(kCellBase + (static_cast<uint32_t>(idx + 1) << 19));
-    int c_lo = 0;
+    int c_lo = 7;                            // |y| < 2^-5: level 7 (every threshold is farther)
     float thr = __int_as_float(0x7f800000);  // +inf: no threshold in the cell
-    for (int t = 0; t < 15; ++t) {
-      if (!neg) {  // y in [lo, hi)
-        if (T[t] < lo) ++c_lo;
-        else if (T[t] < hi) thr = T[t];
-      } else {     // y in (-hi, -lo]
-        if (T[t] <= -hi) ++c_lo;
-        else if (T[t] <= -lo) thr = T[t];
+    if (idx > 0) {
+      const float lo = __uint_as_float(kCellBase + (static_cast<uint32_t>(idx - 1) << 19));
+      const float hi = __uint_as_float(kCellBase + (static_cast<uint32_t>(idx) << 19));
+      c_lo = 0;
+      for (int t = 0; t < 15; ++t) {
+        if (!neg) {  // y in [lo, hi)
+          if (T[t] < lo) ++c_lo;
+          else if (T[t] < hi) thr = T[t];
+        } else {     // y in (-hi, -lo]
+          if (T[t] <= -hi) ++c_lo;
+          else if (T[t] <= -lo) thr = T[t];
+        }
       }
     }
-    tab[i] = make_float2(thr, __int_as_float(c_lo));
+    const float2 e = make_float2(thr, __int_as_float(c_lo));
+#pragma unroll
+    for (int c = 0; c < kCopies; ++c) tab[i * kCopies + c] = e;
   }
 }
 
-__device__ __forceinline__ uint32_t code_fast(float w, float y, float a, const float2* tab) {
+// Level of y = RN(w * RN(1/a)) from the cell table (tab points at this lane's copy); sets
+// `near` when the exact division must decide.
+__device__ __forceinline__ uint32_t code_fast(float y, const float2* tab, bool& near) {
   const uint32_t u = __float_as_uint(y);
-  const uint32_t m = u & 0x7FFFFFFFu;
-  if (m < kCellBase) return 7u;
-  const float2 e = tab[(u >> 31) * kCells + ((m - kCellBase) >> 19)];
-  if (fabsf(y - e.x) < kGuard) return code_exact(w, a);
+  uint32_t m = u & 0x7FFFFFFFu;
+  m = m < kCellBase - (1u << 19) ? kCellBase - (1u << 19) : m;  // tiny |y| -> cell 0
+  uint32_t cell = (m >> 19) - ((kCellBase >> 19) - 1u);
+  cell = cell < kCells - 1 ? cell : kCells - 1;                 // non-finite y stays in range
+  const float2 e = tab[((u >> 31) * kCells + cell) * kCopies];
+  near |= !(fabsf(y - e.x) >= kGuard);  // also true for a NaN y
   return static_cast<uint32_t>(__float_as_int(e.y)) + (y > e.x ? 1u : 0u);
 }
 
-__global__ void __launch_bounds__(kQuantThreads) nf4_quant_blocks(
+__global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
     const float* __restrict__ W, int64_t numel, uint8_t* __restrict__ codes,
     float* __restrict__ absmax, double* __restrict__ group_sum) {
-  __shared__ float s_abs[kGroup];
-  __shared__ float2 s_cells[2 * kCells];
+  __shared__ float s_abs[2][kGroup];  // per group, double-buffered across groups
+  extern __shared__ float2 s_cells[];  // 2 * kCells * kCopies entries
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t g = blockIdx.x;
   const int64_t nblocks = (numel + kBlock - 1) / kBlock;
-  const bool full = (g + 1) * kGroupElems <= numel;
-
-  if (full) {
-    build_cells(s_cells);
-    __syncthreads();
-    const int ql = lane & 3, bw = lane >> 2;  // quarter of the block, block within the warp
-    auto load16 = [&](int it, float4 (&f)[4]) {
-      const int64_t b = g * kGroup + warp * 32 + it * 8 + bw;
-      const float4* src = reinterpret_cast<const float4*>(W + b * kBlock + ql * 16);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) f[v] = __ldg(src + v);
-    };
-    float4 nxt[4];
-    load16(0, nxt);
-#pragma unroll 1
-    for (int it = 0; it < 4; ++it) {
-      const int local_block = warp * 32 + it * 8 + bw;
-      const int64_t b = g * kGroup + local_block;
-      float w[16];
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        w[4 * v + 0] = nxt[v].x; w[4 * v + 1] = nxt[v].y; w[4 * v + 2] = nxt[v].z; w[4 * v + 3] = nxt[v].w;
-      }
-      if (it + 1 < 4) load16(it + 1, nxt);  // next block's loads in flight during this one
-      float m = fabsf(w[0]);
-#pragma unroll
-      for (int i = 1; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      if (ql == 0) {
-        s_abs[local_block] = m;
-        absmax[b] = m;
-      }
-      uint32_t c[16];
-      if (m >= 0x1p-100f) {  // the reciprocal of a normal-range absmax is finite and exact to RN
-        const float rcp = __frcp_rn(m);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) c[i] = code_fast(w[i], __fmul_rn(w[i], rcp), m, s_cells);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) c[i] = code_exact(w[i], m);
-      }
-      uint32_t lo = 0, hi = 0;  // byte j = (c[2j] << 4) | c[2j+1], little endian
-#pragma unroll
-      for (int j = 0; j < 4; ++j) lo |= ((c[2 * j] << 4) | c[2 * j + 1]) << (8 * j);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) hi |= ((c[8 + 2 * j] << 4) | c[8 + 2 * j + 1]) << (8 * j);
-      *reinterpret_cast<uint2*>(codes + b * (kBlock / 2) + ql * 8) = make_uint2(lo, hi);
-    }
-  } else {
-    // partial last group: half a warp per block, one float4 per lane, exact division
-    const int half = lane >> 4, hl = lane & 15;
-#pragma unroll 1
-    for (int it = 0; it < 16; ++it) {
-      const int local_block = warp * 32 + it * 2 + half;
-      const int64_t b = g * kGroup + local_block;
-      const int64_t e = b * kBlock + hl * 4;
-      float v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = e + i < numel ? W[e + i] : 0.0f;
-      float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (hl == 0) {
-        s_abs[local_block] = m;  // blocks past the end hold 0 (all their inputs read as 0)
-        if (b < nblocks) absmax[b] = m;
-      }
-      const uint32_t c0 = code_exact(v[0], m), c1 = code_exact(v[1], m);
-      const uint32_t c2 = code_exact(v[2], m), c3 = code_exact(v[3], m);
-      if (e < numel) codes[e / 2] = static_cast<uint8_t>(e + 1 < numel ? ((c0 << 4) | c1) : (c0 << 4));
-      if (e + 2 < numel) codes[e / 2 + 1] = static_cast<uint8_t>(e + 3 < numel ? ((c2 << 4) | c3) : (c2 << 4));
-    }
-  }
+  const int64_t ngroups = (nblocks + kGroup - 1) / kGroup;
+  const int64_t nfull = numel / kGroupElems;  // groups with all 16384 weights present
+  launch_dependents();  // pass 2 may be scheduled meanwhile (it waits for this grid)
+  build_cells(s_cells);
   __syncthreads();
-  if (warp == 0) {
-    // Perfect binary tree over the 256 absmax values in block order: each lane sums 8
-    // neighbours pairwise, then the xor butterfly combines lanes (x+y == y+x in IEEE).
-    const float* a = s_abs + lane * 8;
-    double sum = (((double)a[0] + (double)a[1]) + ((double)a[2] + (double)a[3])) +
-                 (((double)a[4] + (double)a[5]) + ((double)a[6] + (double)a[7]));
+  const float2* tab = s_cells + lane;
+  const int ql = lane & 3, bw = lane >> 2;  // quarter of the block, block within the warp
+  auto load16 = [&](int64_t g, int it, float4 (&f)[4]) {
+    const int64_t b = g * kGroup + warp * 32 + it * 8 + bw;
+    const float4* src = reinterpret_cast<const float4*>(W + b * kBlock + ql * 16);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) group_sum[g] = sum;
+    for (int v = 0; v < 4; ++v) f[v] = __ldg(src + v);
+  };
+  float4 nxt[4];
+  if (blockIdx.x < nfull) load16(blockIdx.x, 0, nxt);
+
+  int buf = 0;
+#pragma unroll 1
+  for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x, buf ^= 1) {
+    float* sab = s_abs[buf];
+    if (g < nfull) {
+#pragma unroll 1
+      for (int it = 0; it < 4; ++it) {
+        const int local_block = warp * 32 + it * 8 + bw;
+        const int64_t b = g * kGroup + local_block;
+        float w[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          w[4 * v + 0] = nxt[v].x; w[4 * v + 1] = nxt[v].y; w[4 * v + 2] = nxt[v].z; w[4 * v + 3] = nxt[v].w;
+        }
+        // the next block's loads in flight during this one (across the group boundary too)
+        if (it + 1 < 4) load16(g, it + 1, nxt);
+        else if (g + gridDim.x < nfull) load16(g + gridDim.x, 0, nxt);
+        float m = fabsf(w[0]);
+#pragma unroll
+        for (int i = 1; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if (ql == 0) {
+          sab[local_block] = m;
+          absmax[b] = m;
+        }
+        uint32_t c[16];
+        bool near = !(m >= 0x1p-100f);  // tiny or NaN absmax: its reciprocal is not usable
+        if (!near) {
+          const float rcp = __frcp_rn(m);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) c[i] = code_fast(__fmul_rn(w[i], rcp), tab, near);
+        }
+        if (near) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) c[i] = code_exact(w[i], m);
+        }
+        // byte j = (c[2j] << 4) | c[2j+1], little endian: the nibbles from the top are
+        // c6 c7 c4 c5 c2 c3 c0 c1, accumulated as a multiply-add chain (multiply-add pipe)
+        uint32_t lo = c[6], hi = c[14];
+#pragma unroll
+        for (int t = 1; t < 8; ++t) {
+          const int e = 6 - 2 * (t >> 1) + (t & 1);  // 7, 4, 5, 2, 3, 0, 1
+          lo = lo * 16u + c[e];
+          hi = hi * 16u + c[8 + e];
+        }
+        *reinterpret_cast<uint2*>(codes + b * (kBlock / 2) + ql * 8) = make_uint2(lo, hi);
+      }
+    } else {
+      // partial last group: half a warp per block, one float4 per lane, exact division
+      const int half = lane >> 4, hl = lane & 15;
+#pragma unroll 1
+      for (int it = 0; it < 16; ++it) {
+        const int local_block = warp * 32 + it * 2 + half;
+        const int64_t b = g * kGroup + local_block;
+        const int64_t e = b * kBlock + hl * 4;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = e + i < numel ? W[e + i] : 0.0f;
+        float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (hl == 0) {
+          sab[local_block] = m;  // blocks past the end hold 0 (all their inputs read as 0)
+          if (b < nblocks) absmax[b] = m;
+        }
+        const uint32_t c0 = code_exact(v[0], m), c1 = code_exact(v[1], m);
+        const uint32_t c2 = code_exact(v[2], m), c3 = code_exact(v[3], m);
+        if (e < numel) codes[e / 2] = static_cast<uint8_t>(e + 1 < numel ? ((c0 << 4) | c1) : (c0 << 4));
+        if (e + 2 < numel) codes[e / 2 + 1] = static_cast<uint8_t>(e + 3 < numel ? ((c2 << 4) | c3) : (c2 << 4));
+      }
+    }
+    __syncthreads();  // the group's absmax values are all in sab
+    if (warp == 0) {
+      // Perfect binary tree over the 256 absmax values in block order: each lane sums 8
+      // neighbours pairwise, then the xor butterfly combines lanes (x+y == y+x in IEEE).
+      // The other warps go on with the next group, which writes the other buffer.
+      const float* a = sab + lane * 8;
+      double sum = (((double)a[0] + (double)a[1]) + ((double)a[2] + (double)a[3])) +
+                   (((double)a[4] + (double)a[5]) + ((double)a[6] + (double)a[7]));
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane == 0) group_sum[g] = sum;
+    }
   }
 }
 
@@ -192,6 +223,8 @@ __global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict
                                                         int64_t run, float* __restrict__ mean) {
   __shared__ double s_warp[32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  launch_dependents();     // pass 3 may be scheduled meanwhile (it waits for this grid)
+  grid_dependency_wait();  // the group sums of pass 1
   const int64_t lo = (int64_t)t * run;
   double s;
   switch (run) {
@@ -236,6 +269,7 @@ __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict_
                                                         float* __restrict__ steps) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t g = (int64_t)blockIdx.x * 8 + warp;
+  grid_dependency_wait();  // the mean of pass 2 (and with it the absmax of pass 1)
   if (g >= ngroups) return;
   const float mu = __ldg(mean);
   const int64_t b0 = g * kGroup + lane * 8;
@@ -338,19 +372,47 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   double* gsum = reinterpret_cast<double*>(reinterpret_cast<char*>(ws) + ng * kGroup * 4);
   {
     ProfileScope ps("nf4_quant_blocks", stream);
-    nf4_quant_blocks<<<(unsigned)ng, kQuantThreads, 0, stream>>>(W, numel, q.codes, absmax, gsum);
+    // persistent: as many CTAs as are resident at once, or fewer groups
+    static int per_sm = 0;
+    if (per_sm <= 0 &&
+        (cudaFuncSetAttribute(nf4_quant_blocks, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kCellBytes) != cudaSuccess ||
+         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nf4_quant_blocks, kQuantThreads,
+                                                       kCellBytes) != cudaSuccess))
+      return QLORA_ERR_CUDA;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t resident = (int64_t)per_sm * num_sms();
+    const int64_t ctas = ng < resident ? ng : resident;
+    nf4_quant_blocks<<<(unsigned)ctas, kQuantThreads, kCellBytes, stream>>>(W, numel, q.codes, absmax, gsum);
   }
   int64_t p2 = 1;
   while (p2 < ng) p2 *= 2;
   const int64_t run = p2 > 1024 ? p2 / 1024 : 1;
+  // passes 2 and 3 are programmatic dependents: launched while the pass before finishes,
+  // they wait for it (griddepcontrol.wait) before reading its output
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
   {
     ProfileScope ps("nf4_absmax_mean", stream);
-    nf4_absmax_mean<<<1, 1024, 0, stream>>>(gsum, ng, nb, run, q.scale_mean);
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1024);
+    if (cudaLaunchKernelEx(&cfg, nf4_absmax_mean, static_cast<const double*>(gsum), ng, nb, run,
+                           q.scale_mean) != cudaSuccess)
+      return QLORA_ERR_CUDA;
   }
   {
     ProfileScope ps("nf4_double_quant", stream);
-    nf4_double_quant<<<(unsigned)((ng + 7) / 8), 256, 0, stream>>>(absmax, nb, ng, q.scale_mean,
-                                                                 q.scale_codes, q.scale_steps);
+    cfg.gridDim = dim3((unsigned)((ng + 7) / 8));
+    cfg.blockDim = dim3(256);
+    if (cudaLaunchKernelEx(&cfg, nf4_double_quant, static_cast<const float*>(absmax), nb, ng,
+                           static_cast<const float*>(q.scale_mean), q.scale_codes,
+                           q.scale_steps) != cudaSuccess)
+      return QLORA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }

@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
 
   if (tid == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full_bar[i], PRODUCERS / 32);
+      mbar_init(&full_bar[i], PRODUCERS / 32 + 1);  // the TMA issuer + the scale writers
       mbar_init(&empty_bar[i], THREADS / 32);
     }
     mbar_init(&lora_bar, 1);
@@ -230,9 +230,10 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
 
   if (warp >= THREADS / 32) {
     // ============================================================ producer warpgroup
-    // Per stage, thread R of the four producer warps writes the four block scales of weight
-    // row R into the stage's slot table, and lane 0 of the first producer warp issues the
-    // TMA of codes and token slice; the full barrier of a slot counts all four warps.
+    // Per stage, lane 0 of the first producer warp issues the TMA of codes and token slice
+    // (one arrival with the transaction bytes) as soon as the slot is free, and thread R of
+    // the four producer warps writes the four block scales of weight row R into the stage's
+    // slot table (one arrival per warp): the full barrier counts 1 + 4 arrivals.
     // A row's four scale codes of a stage are one aligned 32-bit word when the 64-blocks
     // per row are a multiple of 4: that word and its dq step are loaded SCALE_AHEAD stages
     // early into rotating register sets; otherwise each code is read when needed.
@@ -289,6 +290,16 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       if (i >= STAGES &&
           !mbar_wait(&empty_bar[slot], phase ^ 1u, kWaitEmpty, abort_p, &g_decode_error))
         break;
+      if (pw_idx == 0 && lane == 0) {
+        uint8_t* d = sStage + slot * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full_bar[slot], CODE_BYTES + x_bytes);
+        tma_load_2d(d, &tmCodes, &full_bar[slot], static_cast<int32_t>(ks * (KSTEP / 2)),
+                    static_cast<int32_t>(rb * ROWS));
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          tma_load_2d(d + CODE_BYTES + x * C::XSLOT, &tmX, &full_bar[slot],
+                      static_cast<int32_t>(ks * KSTEP + 64 * x), 0);
+      }
       const int set = i & (SCALE_AHEAD - 1);
       const int64_t n = rb * ROWS + R;
       switch (set) {
@@ -299,20 +310,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       }
       if (word_path && i + SCALE_AHEAD < nst) fetch_set(set);
       __syncwarp();
-      if (lane == 0) {
-        if (pw_idx == 0) {
-          uint8_t* d = sStage + slot * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full_bar[slot], CODE_BYTES + x_bytes);
-          tma_load_2d(d, &tmCodes, &full_bar[slot], static_cast<int32_t>(ks * (KSTEP / 2)),
-                      static_cast<int32_t>(rb * ROWS));
-#pragma unroll
-          for (int x = 0; x < 4; ++x)
-            tma_load_2d(d + CODE_BYTES + x * C::XSLOT, &tmX, &full_bar[slot],
-                        static_cast<int32_t>(ks * KSTEP + 64 * x), 0);
-        } else {
-          mbar_arrive(&full_bar[slot]);
-        }
-      }
+      if (lane == 0) mbar_arrive(&full_bar[slot]);  // this warp's scales are written
       issued = i + 1;
       if (++ks == p.KST) ks = 0, ++rb;
       if (++slot == STAGES) slot = 0, phase ^= 1u;
