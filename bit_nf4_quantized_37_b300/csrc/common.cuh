@@ -23,6 +23,7 @@ enum WaitSite : int {
   kWaitAccFull = 4,
   kWaitLora = 5,
   kWaitPeer = 6,
+  kWaitLayout = 7,  // not a wait: the shared window does not fit a kernel's fixed layout
 };
 
 // ~2 s of wall time, far beyond any legitimate wait in these kernels (< 10 ms each).
@@ -92,6 +93,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same with a suspend-time hint: a thread whose phase has not completed may be suspended
+// (not spinning, so it takes no issue slots) until the phase completes or about
+// kSuspendHintNs have passed.
+constexpr uint32_t kSuspendHintNs = 1000000u;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -107,14 +124,17 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // Bounded wait for the phase with the given parity.  On time-out records `site` in the
 // device error word, raises the CTA's abort flag and returns false.  Once the abort flag is
 // up every later wait returns false at once so the CTA can unwind.
-template <bool kCluster = false>
+// kSleep: retries pass the suspend-time hint (the waiting warp yields its issue slots).
+template <bool kCluster = false, bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int site,
                                           volatile int* abort_flag, int* err_word) {
   const uint32_t a = smem_u32(bar);
   if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+    if (kCluster ? mbar_try_wait_cluster(a, parity)
+                 : (kSleep ? mbar_try_wait_sleep(a, parity) : mbar_try_wait(a, parity)))
+      return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {

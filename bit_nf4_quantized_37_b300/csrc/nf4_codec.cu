@@ -8,8 +8,10 @@
 //                      with an IEEE division, see below), 4-bit packing; writes the codes, the
 //                      absmax values and, per group of 256 blocks, the fp64 pairwise sum of
 //                      its absmax.
-//   nf4_absmax_mean    one CTA: the pairwise sum over the group sums -> mean (fp32).
-//   nf4_double_quant   one CTA per group: step = max|a - mean| / 127, int8 codes.
+//   nf4_absmax_mean    up to 32 CTAs: aligned subtrees of the pairwise sum over the group
+//                      sums.
+//   nf4_double_quant   a warp per group: mean (fp32) from the subtree sums, then
+//                      step = max|a - mean| / 127, int8 codes.
 // Dequantization is one launch (nf4_dequant_kernel) built on the byte-permute table
 // dequantizer shared with the GEMM producers.
 #include "common.cuh"
@@ -34,10 +36,10 @@ constexpr int kQuantThreads = 256;
 // 2^-20 from every threshold, y and x fall between the same two thresholds and the level
 // follows from y.  The level comes from a shared-memory table over cells of y (sign; cell 0
 // for |y| < 2^-5, then binade and top 4 mantissa bits for |y| in [2^-5, 1.0625)): each cell
-// holds at most one threshold T, the level is c_lo + (y > T), and |y - T| < 2^-20 (or a
-// non-finite y) sends the lane's 16 weights to the exact division (thresholds lie
-// >= 2.3e-4 inside their cells, so a threshold between x and y is always the one in y's
-// cell).  The table is built once per CTA, one interleaved copy per lane (entry i of copy l
+// holds at most one threshold T, the level is c_lo + (y > T), and |y - T| < 2^-20 sends the
+// lane's 16 weights to the exact division (thresholds lie >= 2.3e-4 inside their cells, so
+// a threshold between x and y is always the one in y's cell); so does an absmax without a
+// finite reciprocal, which leaves every y of the fast path finite and inside the table.  The table is built once per CTA, one interleaved copy per lane (entry i of copy l
 // at word pair 32 i + l), so the 8-byte lookups of a half-warp never collide on a bank.
 // The last, partial group takes the element-by-element path with the exact division.
 constexpr int kCells = 82;                  // per sign: [0, 2^-5), then 5 binades x 16, [1, 1.0625)
@@ -78,17 +80,23 @@ __device__ void build_cells(float2* tab) {
   }
 }
 
-// Level of y = RN(w * RN(1/a)) from the cell table (tab points at this lane's copy); sets
-// `near` when the exact division must decide.
-__device__ __forceinline__ uint32_t code_fast(float y, const float2* tab, bool& near) {
-  const uint32_t u = __float_as_uint(y);
-  uint32_t m = u & 0x7FFFFFFFu;
-  m = m < kCellBase - (1u << 19) ? kCellBase - (1u << 19) : m;  // tiny |y| -> cell 0
-  uint32_t cell = (m >> 19) - ((kCellBase >> 19) - 1u);
-  cell = cell < kCells - 1 ? cell : kCells - 1;                 // non-finite y stays in range
-  const float2 e = tab[((u >> 31) * kCells + cell) * kCopies];
-  near |= !(fabsf(y - e.x) >= kGuard);  // also true for a NaN y
-  return static_cast<uint32_t>(__float_as_int(e.y)) + (y > e.x ? 1u : 0u);
+// Level of a finite y = RN(w * RN(1/a)), |y| <= 1 + 2^-23, from the cell table.  tab_b is
+// the shared-window address of this lane's copy of entry 0, less the bias of the cell
+// index, so the entry address is two multiply-adds of the sign bit and of the top bits of
+// max(|y|, bottom of cell 1).  dmin collects |T - y|, which decides whether the exact
+// division is needed.  The level is c_lo + (y > T), and y > T exactly when T - y is
+// negative (T = +inf for a cell without threshold gives +inf).
+constexpr uint32_t kCellBias = (kCellBase >> 19) - 1u;       // top bits of cell 0
+constexpr uint32_t kEntryBytes = kCopies * 8;                // one entry, all copies
+__device__ __forceinline__ uint32_t code_fast(float y, uint32_t tab_b, float& dmin) {
+  const float ay = fmaxf(fabsf(y), __uint_as_float(kCellBase - (1u << 19)));  // tiny -> cell 0
+  const uint32_t addr = tab_b + (__float_as_uint(y) >> 31) * (kCells * kEntryBytes) +
+                        (__float_as_uint(ay) >> 19) * kEntryBytes;
+  float t, lo;
+  asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(t), "=f"(lo) : "r"(addr));
+  const float nd = t - y;
+  dmin = fminf(dmin, fabsf(nd));
+  return __float_as_uint(lo) + (__float_as_uint(nd) >> 31);
 }
 
 __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
@@ -103,7 +111,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
   launch_dependents();  // pass 2 may be scheduled meanwhile (it waits for this grid)
   build_cells(s_cells);
   __syncthreads();
-  const float2* tab = s_cells + lane;
+  const uint32_t tab_b = smem_u32(s_cells) + static_cast<uint32_t>(lane) * 8u - kCellBias * kEntryBytes;
   const int ql = lane & 3, bw = lane >> 2;  // quarter of the block, block within the warp
   auto load16 = [&](int64_t g, int it, float4 (&f)[4]) {
     const int64_t b = g * kGroup + warp * 32 + it * 8 + bw;
@@ -141,11 +149,14 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
           absmax[b] = m;
         }
         uint32_t c[16];
-        bool near = !(m >= 0x1p-100f);  // tiny or NaN absmax: its reciprocal is not usable
+        // a tiny, infinite or NaN absmax has no usable reciprocal: exact division
+        bool near = !(m >= 0x1p-100f && m <= 0x1.fffffep127f);
         if (!near) {
           const float rcp = __frcp_rn(m);
+          float dmin = __int_as_float(0x7f800000);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) c[i] = code_fast(__fmul_rn(w[i], rcp), tab, near);
+          for (int i = 0; i < 16; ++i) c[i] = code_fast(__fmul_rn(w[i], rcp), tab_b, dmin);
+          near = !(dmin >= kGuard);
         }
         if (near) {
 #pragma unroll
@@ -202,10 +213,12 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
 }
 
 // -------------------------------------------------------------------- pass 2
-// One CTA of 1024 threads: the pairwise tree over the group sums (zero-padded to a power of
-// two) -> mean = (float)(total / nblocks).  Each thread folds a run of kRun consecutive
-// leaves (a power of two) with a register tree -- exactly the pairwise tree of the run -- and
-// the runs combine through warp butterflies and a final warp.
+// The pairwise tree over the group sums, zero-padded to a power of two P, is cut into
+// nparts <= 32 aligned subtrees of P / nparts leaves, one CTA of 1024 threads each; pass 3
+// combines the subtree sums (the top levels of the same tree) and forms
+// mean = (float)(total / nblocks).  Each thread folds a run of kRun consecutive leaves (a
+// power of two) with a register tree -- exactly the pairwise tree of the run -- and the runs
+// combine through warp butterflies and a final warp.
 template <int kRun>
 __device__ __forceinline__ double fold_run(const double* __restrict__ leaf, int64_t lo, int64_t n) {
   double v[kRun];
@@ -219,13 +232,13 @@ __device__ __forceinline__ double fold_run(const double* __restrict__ leaf, int6
 }
 
 __global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict__ group_sum,
-                                                        int64_t ngroups, int64_t nblocks,
-                                                        int64_t run, float* __restrict__ mean) {
+                                                        int64_t ngroups, int64_t run,
+                                                        double* __restrict__ part) {
   __shared__ double s_warp[32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   launch_dependents();     // pass 3 may be scheduled meanwhile (it waits for this grid)
   grid_dependency_wait();  // the group sums of pass 1
-  const int64_t lo = (int64_t)t * run;
+  const int64_t lo = ((int64_t)blockIdx.x * 1024 + t) * run;
   double s;
   switch (run) {
     case 1: s = fold_run<1>(group_sum, lo, ngroups); break;
@@ -256,34 +269,55 @@ __global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict
     double w = s_warp[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-    if (lane == 0) mean[0] = (float)(w / (double)nblocks);
+    if (lane == 0) part[blockIdx.x] = w;
   }
 }
 
 // -------------------------------------------------------------------- pass 3
-// A warp per group of 256 blocks (8 per lane), 8 groups per CTA.
+// A warp per group of 256 blocks (8 per lane), 8 groups per CTA.  Every CTA first combines
+// the nparts subtree sums of pass 2 (a butterfly over lanes < nparts: the top levels of the
+// pairwise tree) into the mean; CTA 0 stores it.
 __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict__ absmax,
                                                         int64_t nblocks, int64_t ngroups,
-                                                        const float* __restrict__ mean,
+                                                        const double* __restrict__ part,
+                                                        int nparts, float* __restrict__ mean,
                                                         int8_t* __restrict__ scale_codes,
                                                         float* __restrict__ steps) {
+  __shared__ float s_mu;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t g = (int64_t)blockIdx.x * 8 + warp;
-  grid_dependency_wait();  // the mean of pass 2 (and with it the absmax of pass 1)
-  if (g >= ngroups) return;
-  const float mu = __ldg(mean);
+  grid_dependency_wait();  // the subtree sums of pass 2 (and with them the absmax of pass 1)
+  // the group's absmax values first, so their loads overlap the mean's fp64 arithmetic
   const int64_t b0 = g * kGroup + lane * 8;
-  float d[8];
-  if (b0 + 8 <= nblocks) {
-    const float4* src = reinterpret_cast<const float4*>(absmax + b0);
-    const float4 x = __ldg(src), y = __ldg(src + 1);
-    const float a[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+  const bool whole = b0 + 8 <= nblocks;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (g < ngroups) {
+    if (whole) {
+      const float4* src = reinterpret_cast<const float4*>(absmax + b0);
+      const float4 x = __ldg(src), y = __ldg(src + 1);
+      a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
+      a[4] = y.x; a[5] = y.y; a[6] = y.z; a[7] = y.w;
+    } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = __fsub_rn(a[i], mu);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = (b0 + i < nblocks) ? __fsub_rn(absmax[b0 + i], mu) : 0.0f;
+      for (int i = 0; i < 8; ++i)
+        if (b0 + i < nblocks) a[i] = absmax[b0 + i];
+    }
   }
+  if (warp == 0) {
+    double v = lane < nparts ? part[lane] : 0.0;
+    for (int o = 1; o < nparts; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) {
+      const float mu = (float)(v / (double)nblocks);
+      s_mu = mu;
+      if (blockIdx.x == 0) mean[0] = mu;
+    }
+  }
+  __syncthreads();
+  if (g >= ngroups) return;
+  const float mu = s_mu;
+  float d[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d[i] = (whole || b0 + i < nblocks) ? __fsub_rn(a[i], mu) : 0.0f;
   float m = 0.0f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(d[i]));
@@ -301,7 +335,7 @@ __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict_
     }
     q[i] = static_cast<uint32_t>(v) & 0xFFu;
   }
-  if (b0 + 8 <= nblocks) {
+  if (whole) {
     *reinterpret_cast<uint2*>(scale_codes + b0) =
         make_uint2(q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24),
                    q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24));
@@ -360,7 +394,8 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
 uint64_t quantize_workspace_bytes(int64_t numel) {
   const int64_t nb = (numel + kBlock - 1) / kBlock;
   const int64_t ng = (nb + kGroup - 1) / kGroup;
-  // absmax fp32 [ngroups * 256] (padded to whole groups), then group sums fp64 [ngroups]
+  // absmax fp32 [ngroups * 256] (padded to whole groups), group sums fp64 [ngroups], then the
+  // mean's subtree sums fp64 [<= 32] in the 256-byte tail
   return (uint64_t)ng * kGroup * 4 + (uint64_t)ng * 8 + 256;
 }
 
@@ -385,9 +420,11 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     const int64_t ctas = ng < resident ? ng : resident;
     nf4_quant_blocks<<<(unsigned)ctas, kQuantThreads, kCellBytes, stream>>>(W, numel, q.codes, absmax, gsum);
   }
+  double* part = gsum + ng;
   int64_t p2 = 1;
   while (p2 < ng) p2 *= 2;
-  const int64_t run = p2 > 1024 ? p2 / 1024 : 1;
+  const int nparts = p2 > 1024 ? static_cast<int>(p2 / 1024 < 32 ? p2 / 1024 : 32) : 1;
+  const int64_t run = p2 > 1024 * nparts ? p2 / (1024 * nparts) : 1;
   // passes 2 and 3 are programmatic dependents: launched while the pass before finishes,
   // they wait for it (griddepcontrol.wait) before reading its output
   cudaLaunchAttribute pdl[1];
@@ -399,10 +436,10 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   cfg.numAttrs = 1;
   {
     ProfileScope ps("nf4_absmax_mean", stream);
-    cfg.gridDim = dim3(1);
+    cfg.gridDim = dim3(nparts);
     cfg.blockDim = dim3(1024);
-    if (cudaLaunchKernelEx(&cfg, nf4_absmax_mean, static_cast<const double*>(gsum), ng, nb, run,
-                           q.scale_mean) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, nf4_absmax_mean, static_cast<const double*>(gsum), ng, run,
+                           part) != cudaSuccess)
       return QLORA_ERR_CUDA;
   }
   {
@@ -410,8 +447,8 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     cfg.gridDim = dim3((unsigned)((ng + 7) / 8));
     cfg.blockDim = dim3(256);
     if (cudaLaunchKernelEx(&cfg, nf4_double_quant, static_cast<const float*>(absmax), nb, ng,
-                           static_cast<const float*>(q.scale_mean), q.scale_codes,
-                           q.scale_steps) != cudaSuccess)
+                           static_cast<const double*>(part), nparts, q.scale_mean,
+                           q.scale_codes, q.scale_steps) != cudaSuccess)
       return QLORA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;

@@ -50,8 +50,6 @@ int read_and_clear_decode_error(int* out) {
 
 namespace skinny {
 
-__constant__ float c_levels[16] = QLORA_NF4_LEVELS;
-
 constexpr int THREADS = 512;                     // 16 consumer warps
 constexpr int PRODUCERS = 128;                   // one producer warpgroup (one thread per row)
 constexpr int ROWS = 128;                        // weight rows per stage (8 groups of 16)
@@ -65,6 +63,13 @@ constexpr int LORA_BYTES = 2 * LORA_BOX_BYTES;   // rank up to 128
 constexpr int SU_PITCH = 128 + 8;                // bf16 per token row of the staged sU
 constexpr int SU_BYTES = 16 * SU_PITCH * 2;
 constexpr int SCALE_AHEAD = 4;                   // stages between a scale load and its use
+// Fixed shared-window layout.  The byte table sits at a 64 KB boundary, so the window
+// address of entry v, lane l's copy, is (0x02 << 16) | (v << 8) | 4 l: one byte_perm of the
+// code word and a per-lane constant forms it, with no add.  The TMA ring and the staged sU
+// lie below the table, the LoRA B-row tile (shared with the reduction) above it.
+constexpr uint32_t kStageBase = 0x800;
+constexpr uint32_t kTableBase = 0x20000;
+constexpr uint32_t kLoraBase = kTableBase + TABLE_BYTES;
 
 // NT token octets (M <= 8 NT).
 template <int NT>
@@ -77,10 +82,13 @@ struct Cfg {
   // the B-row tile of the LoRA term and the cross-warp reduction share one region: the
   // tile is consumed before the reduction writes it
   static constexpr int LR_BYTES = LORA_BYTES > RED_BYTES ? LORA_BYTES : RED_BYTES;
-  static constexpr int SMEM_BYTES = TABLE_BYTES + 1024 + STAGES * STAGE_BYTES + LR_BYTES + SU_BYTES;
+  static constexpr uint32_t SU_BASE = kStageBase + STAGES * STAGE_BYTES;
+  static constexpr uint32_t SMEM_END = kLoraBase + LR_BYTES;  // end of the used window
 };
-static_assert(Cfg<1>::SMEM_BYTES <= 227 * 1024 - 256, "decode kernel shared memory");
-static_assert(Cfg<2>::SMEM_BYTES <= 227 * 1024 - 256, "decode kernel shared memory");
+static_assert(Cfg<1>::SU_BASE + SU_BYTES <= kTableBase, "decode ring below the byte table");
+static_assert(Cfg<2>::SU_BASE + SU_BYTES <= kTableBase, "decode ring below the byte table");
+static_assert(Cfg<1>::SMEM_END <= 228 * 1024 && Cfg<2>::SMEM_END <= 228 * 1024,
+              "decode kernel shared window");
 
 // Row order inside a 16-row group: MMA row g (and g + 8) is weight row perm8(g) (and + 8),
 // so the four rows a half-warp reads from one swizzled code tile hit eight distinct 16-byte
@@ -130,6 +138,7 @@ struct Params {
   int64_t rp;
   int r;
   uint16_t* Y;
+  float levels[16];  // the NF4 levels (parameter space: no cold constant-cache miss)
 };
 
 // First stage of CTA c, and the CTA that owns stage s, for T stages over G CTAs.
@@ -181,15 +190,6 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   constexpr int STAGES = C::STAGES;
   static_assert(STAGES * 16 <= 256, "scale tables fit the byte-table holes");
   extern __shared__ uint8_t smem_raw[];
-  // the byte table first, at the start of the dynamic window (4-byte alignment is all it
-  // needs); the TMA regions after it on a 1024-byte boundary
-  uint8_t* sTab = smem_raw;
-  uint8_t* smem = smem_raw + TABLE_BYTES;
-  smem += (1024u - (smem_u32(smem) & 1023u)) & 1023u;
-  uint8_t* sStage = smem;
-  uint8_t* sLora = sStage + STAGES * C::STAGE_BYTES;
-  float* sRed = reinterpret_cast<float*>(sLora);  // shares the region (see Cfg)
-  uint16_t* sUs = reinterpret_cast<uint16_t*>(sLora + C::LR_BYTES);
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
   __shared__ __align__(8) uint64_t lora_bar;
@@ -203,6 +203,35 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   if (s_begin >= s_end) return;
   const int64_t rb_first = s_begin / p.KST;
   const int nst = static_cast<int>(s_end - s_begin);
+  {
+    // the fixed layout needs the dynamic window to start at or below the ring and reach
+    // past the LoRA region (uniform over the CTA: nothing has been initialised yet)
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const uint32_t base = smem_u32(smem_raw);
+    if (base > kStageBase || base + dyn < C::SMEM_END) {
+      if (tid == 0) atomicExch(&g_decode_error, kWaitLayout);
+      return;
+    }
+  }
+  uint8_t* const sWin = smem_raw - smem_u32(smem_raw);  // generic pointer of window offset 0
+  uint8_t* sStage = sWin + kStageBase;
+  uint8_t* sLora = sWin + kLoraBase;
+  float* sRed = reinterpret_cast<float*>(sLora);  // shares the region (see Cfg)
+  uint16_t* sUs = reinterpret_cast<uint16_t*>(sWin + C::SU_BASE);
+  uint8_t* sTab = sWin + kTableBase;
+  const uint32_t x_bytes = 4u * 128u * static_cast<uint32_t>(p.M);
+  auto issue_stage = [&](int slot, int64_t rb, int64_t ks) {
+    uint8_t* d = sStage + slot * C::STAGE_BYTES;
+    mbar_arrive_expect_tx(&full_bar[slot], CODE_BYTES + x_bytes);
+    tma_load_2d(d, &tmCodes, &full_bar[slot], static_cast<int32_t>(ks * (KSTEP / 2)),
+                static_cast<int32_t>(rb * ROWS));
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+      tma_load_2d(d + CODE_BYTES + x * C::XSLOT, &tmX, &full_bar[slot],
+                  static_cast<int32_t>(ks * KSTEP + 64 * x), 0);
+  };
+  const int pre = nst < STAGES ? nst : STAGES;  // stages issued before the table is built
 
   if (tid == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -213,19 +242,29 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     abort_flag = 0;
     fence_barrier_init();
   }
-  // fixed byte table (lower half of each row), and the scaled U rows (zero past M and past
-  // the rank padding)
-  for (int i = tid; i < 256 * 32; i += THREADS + PRODUCERS) {
-    const int v = i >> 5;  // uniform across a warp: broadcast constant reads
-    *reinterpret_cast<uint32_t*>(sTab + v * 256 + (i & 31) * 4) =
-        pack_bf16x2(c_levels[v >> 4], c_levels[v & 15]);
+  __syncthreads();
+  if (tid == THREADS) {  // lane 0 of the first producer warp: fill the ring right away
+    int64_t rb = rb_first, ks = s_begin % p.KST;
+    for (int i = 0; i < pre; ++i) {
+      issue_stage(i, rb, ks);
+      if (++ks == p.KST) ks = 0, ++rb;
+    }
   }
-  for (int i = tid; i < 16 * (SU_PITCH / 8); i += THREADS + PRODUCERS) {
-    const int t = i / (SU_PITCH / 8), c8 = i % (SU_PITCH / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (t < p.M && 8 * c8 < p.rp) v = __ldg(reinterpret_cast<const uint4*>(p.sU + t * p.rp + 8 * c8));
-    *reinterpret_cast<uint4*>(sUs + t * SU_PITCH + 8 * c8) = v;
+  // the scaled U rows (zero past M and past the rank padding): loads first, so they are in
+  // flight while the byte table (lower half of each row) is built
+  static_assert(16 * (SU_PITCH / 8) <= THREADS + PRODUCERS, "one sU piece per thread");
+  uint4 su_v = make_uint4(0, 0, 0, 0);
+  {
+    const int t = tid / (SU_PITCH / 8), c8 = tid % (SU_PITCH / 8);
+    if (t < p.M && 8 * c8 < p.rp) su_v = __ldg(reinterpret_cast<const uint4*>(p.sU + t * p.rp + 8 * c8));
   }
+  for (int i = tid; i < 256 * 8; i += THREADS + PRODUCERS) {
+    const int v = i >> 3;  // 8 threads per entry: 16 bytes (4 lane copies) each
+    const uint32_t e = pack_bf16x2(p.levels[v >> 4], p.levels[v & 15]);
+    *reinterpret_cast<uint4*>(sTab + v * 256 + (i & 7) * 16) = make_uint4(e, e, e, e);
+  }
+  if (tid < 16 * (SU_PITCH / 8))
+    *reinterpret_cast<uint4*>(sUs + (tid / (SU_PITCH / 8)) * SU_PITCH + 8 * (tid % (SU_PITCH / 8))) = su_v;
   __syncthreads();
 
   if (warp >= THREADS / 32) {
@@ -241,8 +280,6 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     const int pw_idx = warp - THREADS / 32;
     const float mu = __ldg(p.mean);
     const bool word_path = p.qs_words != 0;
-    const uint32_t tab_s = smem_u32(sTab);
-    const uint32_t x_bytes = 4u * 128u * static_cast<uint32_t>(p.M);
     const int e0 = 16 * (R >> 4) + 2 * inv_perm8(R & 7) + ((R >> 3) & 1);
     uint32_t pw[SCALE_AHEAD];
     float pst[SCALE_AHEAD];
@@ -278,7 +315,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
             v = __fmaf_rn(static_cast<float>(__ldg(p.qs + idx)), __ldg(p.steps + (idx >> 8)), mu);
           }
         }
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(tab_s + scale_slot_off(slot, b * 128 + e0)), "f"(v));
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(kTableBase + scale_slot_off(slot, b * 128 + e0)), "f"(v));
       }
     };
     if (word_path)
@@ -288,18 +325,9 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     uint32_t phase = 0;
     for (int i = 0; i < nst; ++i) {
       if (i >= STAGES &&
-          !mbar_wait(&empty_bar[slot], phase ^ 1u, kWaitEmpty, abort_p, &g_decode_error))
+          !mbar_wait<false, true>(&empty_bar[slot], phase ^ 1u, kWaitEmpty, abort_p, &g_decode_error))
         break;
-      if (pw_idx == 0 && lane == 0) {
-        uint8_t* d = sStage + slot * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full_bar[slot], CODE_BYTES + x_bytes);
-        tma_load_2d(d, &tmCodes, &full_bar[slot], static_cast<int32_t>(ks * (KSTEP / 2)),
-                    static_cast<int32_t>(rb * ROWS));
-#pragma unroll
-        for (int x = 0; x < 4; ++x)
-          tma_load_2d(d + CODE_BYTES + x * C::XSLOT, &tmX, &full_bar[slot],
-                      static_cast<int32_t>(ks * KSTEP + 64 * x), 0);
-      }
+      if (pw_idx == 0 && lane == 0 && i >= pre) issue_stage(slot, rb, ks);
       const int set = i & (SCALE_AHEAD - 1);
       const int64_t n = rb * ROWS + R;
       switch (set) {
@@ -338,11 +366,11 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   if (tid == 0 && s_begin % p.KST == 0) issue_lora(rb_first);
   bool lora_pending = s_begin % p.KST == 0;  // a B-row tile is in flight, not yet used
 
-  const uint32_t tab_s = smem_u32(sTab);
-  const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
+  const uint32_t lane_addr = kTableBase | (static_cast<uint32_t>(lane) * 4u);
   auto lut = [&](uint32_t word, uint32_t j) -> uint32_t {
-    // byte j of the code word at bits 8..15, 4 * lane at bits 0..7: the entry's address
-    return ld_s32(tab_s + __byte_perm(word, lane4, 0x5504u | (j << 4)));
+    // byte j of the code word at bits 8..15; 4 * lane at bits 0..7 and the table's 64 KB
+    // page at bits 16..31 from lane_addr: the entry's window address
+    return ld_s32(__byte_perm(word, lane_addr, 0x7604u | (j << 4)));
   };
 
   float acc[2][NT][4];
@@ -463,13 +491,15 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     }
   }
   uint32_t x_off[NT][2];
+  bool x_live[NT];
 #pragma unroll
   for (int o = 0; o < NT; ++o) {
     const int t = g + 8 * o;
+    x_live[o] = t < p.M;
     x_off[o][0] = CODE_BYTES + blk * C::XSLOT + t * 128 + (((2 * q) ^ g) << 4);
     x_off[o][1] = CODE_BYTES + blk * C::XSLOT + t * 128 + (((2 * q + 1) ^ g) << 4);
   }
-  const uint32_t stage_s = smem_u32(sStage);
+  const uint32_t stage_s = kStageBase;
 
   bool ok = true;
   int64_t rb = rb_first, ks = s_begin % p.KST, ks_first = ks;
@@ -484,14 +514,18 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       }
       lora_pending = true;
     }
-    const bool got = mbar_wait(&full_bar[slot], phase, kWaitTmaFull, abort_p, &g_decode_error);
+    const bool got =
+        mbar_wait<false, true>(&full_bar[slot], phase, kWaitTmaFull, abort_p, &g_decode_error);
     if (got) {
       const uint32_t cs = stage_s + slot * C::STAGE_BYTES;
       uint32_t xf[NT][8];
 #pragma unroll
       for (int o = 0; o < NT; ++o) {
-        const uint4 lo = ld_s128(cs + x_off[o][0]);
-        const uint4 hi = ld_s128(cs + x_off[o][1]);
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (x_live[o]) {  // token rows past M hold no TMA data: zero operands, no loads
+          lo = ld_s128(cs + x_off[o][0]);
+          hi = ld_s128(cs + x_off[o][1]);
+        }
         xf[o][0] = lo.x; xf[o][1] = lo.y; xf[o][2] = lo.z; xf[o][3] = lo.w;
         xf[o][4] = hi.x; xf[o][5] = hi.y; xf[o][6] = hi.z; xf[o][7] = hi.w;
       }
@@ -499,7 +533,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       for (int j = 0; j < 2; ++j) {
         const uint2 c0 = ld_s64(cs + code_off[j]);
         const uint2 c1 = ld_s64(cs + code_off[j] + 8 * 128);
-        const float2 sc = ld_sf2(tab_s + scale_slot_off(slot, scale_e[j]));
+        const float2 sc = ld_sf2(kTableBase + scale_slot_off(slot, scale_e[j]));
         float d[NT][4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -654,14 +688,28 @@ template <int NT>
 int run_decode(const CUtensorMap& tmC, const CUtensorMap& tmX, const CUtensorMap& tmB,
                const skinny::Params& p, unsigned ctas, cudaStream_t stream) {
   using C = skinny::Cfg<NT>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
+  // The kernel places its regions at fixed window offsets; it takes the whole opt-in
+  // dynamic window, which starts after the reserved and static shared memory.
+  static int dyn = 0;
+  if (!dyn) {
+    int dev = 0, optin = 0, reserved = 0;
+    cudaFuncAttributes fa{};
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, skinny::nf4_decode_gemv<NT>) != cudaSuccess)
       return QLORA_ERR_CUDA;
-    attr = true;
+    const int base = reserved + static_cast<int>(fa.sharedSizeBytes);
+    const int size = optin - static_cast<int>(fa.sharedSizeBytes);
+    if (base > static_cast<int>(skinny::kStageBase) ||
+        base + size < static_cast<int>(C::SMEM_END))
+      return QLORA_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             size) != cudaSuccess)
+      return QLORA_ERR_CUDA;
+    dyn = size;
   }
-  skinny::nf4_decode_gemv<NT><<<ctas, skinny::THREADS + skinny::PRODUCERS, C::SMEM_BYTES, stream>>>(tmC, tmX, tmB, p);
+  skinny::nf4_decode_gemv<NT><<<ctas, skinny::THREADS + skinny::PRODUCERS, dyn, stream>>>(tmC, tmX, tmB, p);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
@@ -724,6 +772,10 @@ int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_
   p.rp = L.rp;
   p.r = a.r;
   p.Y = a.Y;
+  {
+    constexpr float L[16] = QLORA_NF4_LEVELS;
+    for (int i = 0; i < 16; ++i) p.levels[i] = L[i];
+  }
   const unsigned ctas = (unsigned)skinny_ctas(a.N, a.K);
   ProfileScope ps("decode_gemv", stream);
   return a.M > 8 ? run_decode<2>(tmC, tmX, tmB, p, ctas, stream)

@@ -175,7 +175,9 @@ int nf4_level_table(float levels[16], float thresholds[15]);
 /*
  * Reads and clears the device error word that kernels set when a bounded wait on an
  * mbarrier gives up (instead of hanging).  Synchronizes `stream`.  *out = 0 when clean,
- * else a nonzero code naming the wait.  Returns QLORA_ERR_DEVICE_TIMEOUT if it was set.
+ * else a nonzero code naming the wait (1..6), or 7 when the decode kernel found a shared
+ * window that its fixed layout does not fit and returned without work.  Returns
+ * QLORA_ERR_DEVICE_TIMEOUT if it was set.
  */
 int qlora_device_status(int32_t* out, void* stream);
 
