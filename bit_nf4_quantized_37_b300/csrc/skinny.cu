@@ -502,11 +502,14 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   const uint32_t stage_s = kStageBase;
 
   bool ok = true;
-  int64_t rb = rb_first, ks = s_begin % p.KST, ks_first = ks;
+  // 32-bit bookkeeping in the loop: stage counts per CTA and per row block are small
+  const int KST = static_cast<int>(p.KST);
+  int64_t rb = rb_first;
+  int ks = static_cast<int>(s_begin % p.KST), ks_first = ks;
   int slot = 0;
   uint32_t phase = 0;
-  for (int64_t s = s_begin; s < s_end; ++s) {
-    if (ks == 0 && s != s_begin) {
+  for (int i = 0; i < nst; ++i) {
+    if (ks == 0 && i != 0) {
       ks_first = 0;
       if (tid == 0) {
         fence_proxy_async_smem();  // the last flush's accesses to the region precede the refill
@@ -561,11 +564,11 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[slot]);  // this warp is done with the slot
     if (++slot == STAGES) slot = 0, phase ^= 1u;
-    if (ks == p.KST - 1 || s == s_end - 1) {
+    if (ks == KST - 1 || i == nst - 1) {
       if (!flush(rb, ks_first, ks)) ok = false;
       if (!ok) break;  // uniform: decided after a consumer barrier
     }
-    if (++ks == p.KST) ks = 0, ++rb;
+    if (++ks == KST) ks = 0, ++rb;
   }
   (void)ok;
   __syncthreads();  // with the producer warp
