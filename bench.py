@@ -415,6 +415,8 @@ def main():
 
     secondary = {} if args.no_secondary else measure_secondary(qn, wl, dev, peaks, traffic,
                                                                l2_flush)
+    if not args.no_secondary:
+        secondary.update(measure_merge_and_error(qn, wl, p, q, A, B, dev, peaks, l2_flush))
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -443,6 +445,74 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def graph_timed_ms(fn, l2_flush, reps: int = 10) -> float:
+    """Device time of one call: reps x (L2 flush + call) as one CUDA graph minus the same
+    graph of flushes alone."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            body()
+        return g
+
+    def replay_ms(g):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g.replay()
+        torch.cuda.synchronize()
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    def calls():
+        for _ in range(reps):
+            l2_flush()
+            fn()
+
+    def flushes():
+        for _ in range(reps):
+            l2_flush()
+
+    return (replay_ms(capture(calls)) - replay_ms(capture(flushes))) / reps
+
+
+def measure_merge_and_error(qn, wl, p, q, A, B, dev, peaks, l2_flush):
+    """Adapter merge W' + s B A (bf16 out) on the 4096^2 layer, the loss of requantizing the
+    merged weights, and the NF4-vs-INT4 squared errors on normal and Student-t(3) weights."""
+    import torch
+    hbm = peaks["hbm_gbs"]
+    out = {}
+    Wm = torch.empty(p.N, p.K, dtype=torch.bfloat16, device=dev)
+    ms = graph_timed_ms(lambda: qn.nf4_merge_lora(q, A, B, p.scale, out=Wm), l2_flush)
+    nbytes = q.storage_bytes() + 2 * p.r * (p.N + p.K) + 2 * p.N * p.K
+    _, m32 = qn.nf4_merge_lora(q, A, B, p.scale, bf16=False, f32=True)
+    base = qn.nf4_dequantize(q).float()
+    requant = qn.nf4_dequantize(qn.nf4_quantize(m32)).float()
+    delta = torch.linalg.vector_norm(m32 - base).item()
+    loss = torch.linalg.vector_norm(requant - m32).item()
+    out["merge_4096x4096_r16"] = {"GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm,
+                                  "ms": ms, "bytes": nbytes,
+                                  "requant_error_over_adapter_update": loss / delta}
+    for kind in ("normal", "student_t3"):
+        if kind == "normal":
+            W = torch.from_numpy(p.W()).to(dev)
+        else:
+            W = torch.from_numpy(wl.student_t_weight((p.N, p.K), seed=43, df=3.0,
+                                                     sigma=0.02)).to(dev)
+        st = qn.nf4_int4_error_stats(W).cpu().tolist()
+        ms = graph_timed_ms(lambda: qn.nf4_int4_error_stats(W), l2_flush)
+        out[f"nf4_vs_int4_{kind}_4096x4096"] = {
+            "nf4_rel_mse": st[1] / st[0], "int4_rel_mse": st[2] / st[0],
+            "nf4_over_int4": st[1] / st[2], "ms": ms,
+            "GB/s": 4 * W.numel() / ms / 1e6}
+    return out
 
 
 def measure_secondary(qn, wl, dev, peaks, traffic, l2_flush, reps: int = 10):

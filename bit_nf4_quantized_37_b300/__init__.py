@@ -16,6 +16,8 @@ from ._binding import (  # noqa: F401
     level_table,
     lib,
     nf4_dequantize,
+    nf4_int4_error_stats,
+    nf4_merge_lora,
     nf4_quantize,
     nf4_quantize_noalloc,
     nf4_quantize_workspace_bytes,
@@ -30,6 +32,7 @@ from ._binding import (  # noqa: F401
 
 __all__ = [
     "NF4Tensor", "QLoRAError", "device_status", "level_table", "lib", "nf4_dequantize",
+    "nf4_int4_error_stats", "nf4_merge_lora",
     "nf4_quantize", "nf4_quantize_noalloc", "nf4_quantize_workspace_bytes", "nf4_storage_bytes", "profile_start",
     "profile_stop", "qlora_linear_bwd",
     "qlora_linear_fwd", "qlora_workspace_bytes", "status_str",

@@ -22,7 +22,8 @@ NF4_NOALLOC_MAX_NUMEL = 1 << 26
 EXPORTS = ["nf4_storage_bytes", "nf4_quantize_workspace_bytes", "nf4_quantize",
            "nf4_dequantize", "qlora_workspace_bytes", "qlora_linear_fwd", "qlora_linear_bwd",
            "nf4_level_table", "qlora_device_status", "qlora_status_str", "qlora_version",
-           "qlora_profile_start", "qlora_profile_stop", "nf4_quantize_noalloc"]
+           "qlora_profile_start", "qlora_profile_stop", "nf4_quantize_noalloc",
+           "nf4_merge_lora", "nf4_int4_error_workspace_bytes", "nf4_int4_error_stats"]
 
 
 class QLoRAError(RuntimeError):
@@ -69,6 +70,9 @@ def lib() -> ctypes.CDLL:
             "qlora_profile_start": [],
             "qlora_profile_stop": [vp, i32, vp],
             "nf4_quantize_noalloc": [vp, sp, vp],
+            "nf4_merge_lora": [sp, vp, vp, i32, ctypes.c_float, vp, vp, vp],
+            "nf4_int4_error_workspace_bytes": [u64p],
+            "nf4_int4_error_stats": [vp, i64, vp, vp, ctypes.c_uint64, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -253,6 +257,37 @@ def qlora_linear_bwd(dY: torch.Tensor, X: torch.Tensor, q: NF4Tensor, A: torch.T
         _ptr(dY), _ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(U),
         _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), ws.numel(), _stream()))
     return dX, dA, dB
+
+
+def nf4_merge_lora(q: NF4Tensor, A: torch.Tensor, B: torch.Tensor, scale: float,
+                   bf16: bool = True, f32: bool = False,
+                   out: torch.Tensor | None = None, out_f32: torch.Tensor | None = None):
+    """W_merged = bf16(W' + scale B A) for the NF4 base q, A [r, K], B [N, r] bf16.
+    Returns (bf16 [N, K] or None, the same values as fp32 [N, K] or None)."""
+    for t, n in ((A, "A"), (B, "B")):
+        _req(t, torch.bfloat16, n)
+    r = A.shape[0]
+    dev = q.codes.device
+    o16 = out if out is not None else (
+        torch.empty(q.rows, q.cols, dtype=torch.bfloat16, device=dev) if bf16 else None)
+    o32 = out_f32 if out_f32 is not None else (
+        torch.empty(q.rows, q.cols, dtype=torch.float32, device=dev) if f32 else None)
+    s = q.c_struct()
+    _check("nf4_merge_lora", lib().nf4_merge_lora(ctypes.byref(s), _ptr(A), _ptr(B), r,
+                                                  float(scale), _ptr(o16), _ptr(o32), _stream()))
+    return o16, o32
+
+
+def nf4_int4_error_stats(W: torch.Tensor) -> torch.Tensor:
+    """fp64 [3] on the device: sum w^2, NF4 and INT4 (absmax, 64-blocks) squared errors."""
+    _req(W, torch.float32, "W")
+    n = _u64()
+    _check("nf4_int4_error_workspace_bytes", lib().nf4_int4_error_workspace_bytes(ctypes.byref(n)))
+    ws = _workspace(n.value, W.device)
+    out = torch.empty(3, dtype=torch.float64, device=W.device)
+    _check("nf4_int4_error_stats", lib().nf4_int4_error_stats(
+        _ptr(W), W.numel(), _ptr(out), _ptr(ws), ws.numel(), _stream()))
+    return out
 
 
 class _KernelTime(ctypes.Structure):

@@ -108,6 +108,41 @@ int nf4_dequantize(const nf4_tensor* q, uint16_t* W_out, void* stream) {
   return launch_dequantize(*q, q->rows * q->cols, W_out, static_cast<cudaStream_t>(stream));
 }
 
+int nf4_merge_lora(const nf4_tensor* Wq, const uint16_t* A, const uint16_t* B, int32_t r,
+                   float scale, uint16_t* W_merged, float* W_merged_f32, void* stream) {
+  int st = check_tensor(Wq);
+  if (st) return st;
+  if (!A || !B || (!W_merged && !W_merged_f32) || r < 1) return QLORA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return QLORA_ERR_INVALID_ARG;
+  if (r > kMaxRank || Wq->cols % 8 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || (W_merged && !aligned16(W_merged)) ||
+      (W_merged_f32 && !aligned16(W_merged_f32)))
+    return QLORA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+  return launch_merge(*Wq, A, B, r, scale, W_merged, W_merged_f32,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int nf4_int4_error_workspace_bytes(uint64_t* out) {
+  if (!out) return QLORA_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st) return st;
+  *out = static_cast<uint64_t>(error_stats_parts()) * 3 * sizeof(double);
+  return QLORA_OK;
+}
+
+int nf4_int4_error_stats(const float* W, int64_t numel, double* out, void* workspace,
+                         uint64_t workspace_bytes, void* stream) {
+  if (!W || !out || !workspace || numel < 1) return QLORA_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return QLORA_ERR_MISALIGNED;
+  int st = check_device();
+  if (st) return st;
+  if (workspace_bytes < static_cast<uint64_t>(error_stats_parts()) * 3 * sizeof(double))
+    return QLORA_ERR_WORKSPACE;
+  return launch_error_stats(W, numel, out, workspace, static_cast<cudaStream_t>(stream));
+}
+
 int qlora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r, uint64_t* out) {
   if (M < 1 || N < 1 || K < 1 || r < 1 || !out) return QLORA_ERR_INVALID_ARG;
   if (r > kMaxRank) return QLORA_ERR_UNSUPPORTED;

@@ -25,6 +25,12 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
                     cudaStream_t stream);
 int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, cudaStream_t stream);
 
+// Adapter merge and NF4-vs-INT4 error statistics (merge.cu).
+int launch_merge(const nf4_tensor& q, const uint16_t* A, const uint16_t* B, int r, float scale,
+                 uint16_t* out16, float* out32, cudaStream_t stream);
+int error_stats_parts();
+int launch_error_stats(const float* W, int64_t numel, double* out, void* ws, cudaStream_t stream);
+
 // 2-D tiled tensor map over a row-major matrix (tensormap.cu).  `inner` is the contiguous
 // extent in elements, `outer` the row count, `row_bytes` the row pitch; the box is
 // box_inner x box_outer elements.  Returns false when the driver rejects the map.

@@ -43,6 +43,12 @@ def weight(shape, seed: int, sigma: float, outlier_frac: float = 0.0) -> np.ndar
     return w
 
 
+def student_t_weight(shape, seed: int, df: float, sigma: float) -> np.ndarray:
+    """fp32 heavy-tailed weights: Student-t(df) samples scaled by sigma."""
+    g = rng(seed)
+    return (g.standard_t(df, size=shape) * sigma).astype(np.float32)
+
+
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16)
     return t.view(torch.int16).numpy().view(np.uint16)

@@ -166,6 +166,36 @@ int qlora_linear_bwd(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4
                      uint64_t ws_bytes, void* stream);
 
 /*
+ * Fold a LoRA adapter into the NF4 base (junaidshaukat.com "QLoRA -- the democratization
+ * event", the deployment-subtlety paragraph: dequantize, merge, maybe requantize;
+ * infivelines.com "QLoRA": merging into a 4-bit base and saving loses precision twice;
+ * addaly.com "QLoRA on one card", "Merging a QLoRA adapter, and the subtlety"):
+ *     W_merged[n, k] = bf16( W'[n, k] + scale * sum_j B[n, j] A[j, k] )
+ * with W' the bf16 dequantization of Wq (as nf4_dequantize), the rank-r sum in fp32 in
+ * ascending j, then one fp32 multiply by scale, one fp32 add and one round to bf16.
+ * A [r, K], B [N, r] bf16; W_merged [N, K] bf16 and W_merged_f32 [N, K] fp32 (the same values,
+ * ready for nf4_quantize to requantize) are each optional but not both NULL.  N = Wq->rows,
+ * K = Wq->cols with K % 8 == 0; 1 <= r <= 128.  All pointers 16-byte aligned.
+ */
+int nf4_merge_lora(const nf4_tensor* Wq, const uint16_t* A, const uint16_t* B, int32_t r,
+                   float scale, uint16_t* W_merged, float* W_merged_f32, void* stream);
+
+/*
+ * NF4 against INT4 on the same weights (aicurriculum.codextroop.com "QLoRA -- Module 12.4",
+ * "Design Details That Matter": NF4 is often better than naive INT4; addaly.com "QLoRA on one
+ * card", "What each setting is doing"): for fp32 W [numel] (device), per block of 64 with its
+ * absmax a (no second-level quantization), out[0] = sum w^2, out[1] = sum (w - level[c] a)^2
+ * with c the nearest NF4 level of RN(w / a), out[2] = sum (w - q RN(a / 7))^2 with
+ * q = clamp(rint(RN(7 RN(w / a))), -7, 7) (symmetric absmax INT4).  Each thread sums its 16
+ * weights in fp32, the rest is summed in fp64; out is 3 doubles of device memory.
+ * workspace: device scratch of nf4_int4_error_workspace_bytes (current device).  W and
+ * workspace 16-byte aligned; any numel >= 1.
+ */
+int nf4_int4_error_workspace_bytes(uint64_t* out);
+int nf4_int4_error_stats(const float* W, int64_t numel, double* out, void* workspace,
+                         uint64_t workspace_bytes, void* stream);
+
+/*
  * The fp32 constants the kernels use (host only): levels[16], the NF4 levels in ascending
  * order, and thresholds[15], the midpoints of adjacent levels rounded toward -inf
  * (code = number of thresholds strictly below x).  Either pointer may be NULL.

@@ -56,6 +56,12 @@ def lib() -> ctypes.CDLL:
         L.nf4o_lora_dx_rows.restype = None
         L.nf4o_lora_dadb.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f64, vp, vp]
         L.nf4o_lora_dadb.restype = None
+        L.nf4o_bf16_rne_double.argtypes = [f64]
+        L.nf4o_bf16_rne_double.restype = ctypes.c_uint16
+        L.nf4o_merge.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i64, i64, i64, f64, vp]
+        L.nf4o_merge.restype = None
+        L.nf4o_int4_error.argtypes = [vp, i64, vp]
+        L.nf4o_int4_error.restype = None
         L.nf4o_num_threads.argtypes = []
         L.nf4o_num_threads.restype = ctypes.c_int
         _lib = L
@@ -205,3 +211,33 @@ def lora_dadb(dY, X, A, B, scale):
     lib().nf4o_lora_dadb(_p(dY), _p(X), _p(A), _p(B), M, N, K, r, float(scale),
                          _p(dA), _p(dB))
     return dA, dB
+
+
+def bf16_rne_double(x) -> np.ndarray:
+    """fp64 -> bf16 bits, one rounding (ties to even), element by element through C."""
+    x = np.ascontiguousarray(x, np.float64).ravel()
+    f = lib().nf4o_bf16_rne_double
+    return np.array([f(float(v)) for v in x], np.uint16)
+
+
+def merge(q: dict, A, B, scale) -> np.ndarray:
+    """bf16 bits [N, K] of bf16(W' + scale B A) from the fp64 bracket (reading R11).
+    q is an oracle quantize() dict of an N x K tensor, A [r, K] and B [N, r] bf16 bits."""
+    A, B = _u16(A), _u16(B)
+    r, K = A.shape
+    N = B.shape[0]
+    assert int(q["numel"]) == N * K
+    out = np.zeros((N, K), np.uint16)
+    lib().nf4o_merge(_p(np.ascontiguousarray(q["codes"], np.uint8)),
+                     _p(np.ascontiguousarray(q["qscale"], np.int8)),
+                     _p(np.ascontiguousarray(q["steps"], np.float32)), float(q["mean"]),
+                     _p(A), _p(B), N, K, r, float(scale), _p(out))
+    return out
+
+
+def int4_error(W: np.ndarray) -> np.ndarray:
+    """[sum w^2, sum NF4 squared error, sum INT4 squared error] in fp64 (reading R12)."""
+    W = np.ascontiguousarray(W, np.float32).ravel()
+    out = np.zeros(3, np.float64)
+    lib().nf4o_int4_error(_p(W), W.size, _p(out))
+    return out

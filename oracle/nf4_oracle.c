@@ -347,6 +347,86 @@ void nf4o_lora_dadb(const uint16_t* dY, const uint16_t* X, const uint16_t* A,
   free(V);
 }
 
+/* ------------------------------------------------------------------ merge (R11) */
+/* [junaidshaukat] deployment-subtlety paragraph (dequantize, merge, maybe requantize);
+ * [infivelines] step-five paragraph (a merge into the 4-bit base loses precision twice);
+ * [addaly] "Merging a QLoRA adapter, and the subtlety".
+ * R11: W_merged = bf16_rne(W' + s * sum_j B[n][j] A[j][k]) with W' the R7 dequantization and
+ * the bracket evaluated in fp64 (every bf16 x bf16 product is exact; the sum of r <= 128 of
+ * them is exact for the magnitudes of adapters), rounded once from fp64 to bf16. */
+
+/* Round a double to the nearest bf16 (ties to even) from the definition: 8 significant bits
+ * for |x| >= 2^-126, a fixed quantum of 2^-133 below that. */
+uint16_t nf4o_bf16_rne_double(double x) {
+  if (x == 0.0) return signbit(x) ? 0x8000u : 0u;
+  int e;
+  frexp(fabs(x), &e);                 /* |x| = m 2^e, m in [0.5, 1) */
+  int qexp = e - 8;
+  if (qexp < -133) qexp = -133;
+  double k = nearbyint(ldexp(fabs(x), -qexp));  /* round half to even */
+  float v = (float)ldexp(k, qexp);              /* exact: at most 9 significant bits */
+  if (x < 0) v = -v;
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  return (uint16_t)(u >> 16);
+}
+
+void nf4o_merge(const uint8_t* codes, const int8_t* qscale, const float* steps, float mean,
+                const uint16_t* A, const uint16_t* B, int64_t N, int64_t K, int64_t r,
+                double scale, uint16_t* out) {
+  float L[16], T[15];
+  nf4o_levels(L, T);
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k) {
+      int64_t e = n * K + k, b = e / NF4O_BLOCK;
+      float ahat = fmaf((float)qscale[b], steps[b / NF4O_GROUP], mean);
+      uint8_t byte = codes[e / 2];
+      int c = (e & 1) ? (byte & 0xF) : (byte >> 4);
+      double wd = bf16_to_double(nf4o_bf16_rne(L[c] * ahat));
+      double delta = 0.0;
+      for (int64_t j = 0; j < r; ++j) delta += bf16_to_double(B[n * r + j]) * bf16_to_double(A[j * K + k]);
+      out[e] = nf4o_bf16_rne_double(wd + scale * delta);
+    }
+}
+
+/* ------------------------------------------------------------------ NF4 vs INT4 (R12) */
+/* aicurriculum.codextroop.com "QLoRA -- Module 12.4", "Design Details That Matter" (NF4 is
+ * often better than naive INT4); [addaly] "What each setting is doing".
+ * R12: per block of 64 with its true absmax a (no second level): NF4 reconstruction
+ * L[c] a with c = R2 code of x = R3 quotient; INT4 reconstruction q RN(a/7) with
+ * q = clamp(rint(RN(7 x)), -7, 7) (symmetric absmax INT4, 15 levels).  out[0] = sum w^2,
+ * out[1] = sum (w - nf4)^2, out[2] = sum (w - int4)^2, all in fp64. */
+void nf4o_int4_error(const float* W, int64_t numel, double out[3]) {
+  float L[16], T[15];
+  nf4o_levels(L, T);
+  double s0 = 0.0, s1 = 0.0, s2 = 0.0;
+  int64_t nb = nf4o_num_blocks(numel);
+  for (int64_t b = 0; b < nb; ++b) {
+    int64_t lo = b * NF4O_BLOCK, hi = lo + NF4O_BLOCK < numel ? lo + NF4O_BLOCK : numel;
+    float a = 0.0f;
+    for (int64_t e = lo; e < hi; ++e) a = fabsf(W[e]) > a ? fabsf(W[e]) : a;
+    float a7 = a / 7.0f;
+    for (int64_t e = lo; e < hi; ++e) {
+      float w = W[e];
+      float x = a > 0.0f ? w / a : 0.0f;
+      int c = nearest_code(x, T);
+      float t = 7.0f * x;
+      float q = nearbyintf(t);
+      if (q > 7.0f) q = 7.0f;
+      if (q < -7.0f) q = -7.0f;
+      double en = (double)w - (double)L[c] * (double)a;
+      double ei = (double)w - (double)q * (double)a7;
+      s0 += (double)w * (double)w;
+      s1 += en * en;
+      s2 += ei * ei;
+    }
+  }
+  out[0] = s0;
+  out[1] = s1;
+  out[2] = s2;
+}
+
 /* Threads OpenMP will use (reported with CPU timings). */
 #ifdef _OPENMP
 #include <omp.h>

@@ -256,3 +256,84 @@ def test_bad_arguments_raise():
     bad = qn.NF4Tensor(pb.qd.codes, pb.qd.scale_codes, pb.qd.scale_steps, pb.qd.scale_mean, 250, 256)
     with pytest.raises(qn.QLoRAError):
         qn.qlora_linear_fwd(pb.Xd[:, :256], bad, pb.Ad, pb.Bd, 2.0)
+
+
+# ------------------------------------------------------------------ merge / requantize
+def _ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in bf16 steps between two arrays of bf16 bits (sign-magnitude order)."""
+    def key(h):
+        h = h.astype(np.int64)
+        return np.where(h & 0x8000, -(h & 0x7FFF), h & 0x7FFF)
+    return np.abs(key(a) - key(b))
+
+
+@pytest.mark.parametrize("cfg", ["config1", "config2"])
+def test_merge_matches_oracle(cfg):
+    """bf16(W' + s B A): the device's fp32 bracket against the oracle's fp64 one, each rounded
+    once to bf16.  Bound from the fp32 arithmetic: r sequential multiply-adds, one multiply and
+    one add leave at most (r + 2) 2^-24 (|W'| + s sum_j |B A|) before the final rounding, so the
+    two results differ by at most that plus one bf16 step of the result; more than one step
+    only where W' and s B A nearly cancel.  Differences of any size are rare (~2^-16)."""
+    p = getattr(wl, cfg)()
+    W = p.W()
+    qo = oracle.quantize(W)
+    qd = qn.nf4_quantize(torch.from_numpy(W).cuda())
+    A, B = p.A(), p.B()
+    m16, m32 = qn.nf4_merge_lora(qd, bf16_dev(A), bf16_dev(B), p.scale, f32=True)
+    got = bits_host(m16)
+    want = oracle.merge(qo, A, B, p.scale)
+    d = _ulp_diff(got, want)
+    assert (d > 0).mean() <= 1e-3
+    gv = wl.bf16_bits_to_f32(got).astype(np.float64)
+    wv = wl.bf16_bits_to_f32(want).astype(np.float64)
+    wd = wl.bf16_bits_to_f32(oracle.dequantize(qo)).astype(np.float64).reshape(p.N, p.K)
+    mag = np.abs(wd) + p.scale * (np.abs(wl.bf16_bits_to_f32(B).astype(np.float64)) @
+                                  np.abs(wl.bf16_bits_to_f32(A).astype(np.float64)))
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(wv), 2.0 ** -126))) - 7)
+    bound = (p.r + 2) * 2.0 ** -24 * mag + step
+    assert np.all(np.abs(gv - wv) <= bound)
+    assert np.array_equal(m32.cpu().numpy(), wl.bf16_bits_to_f32(got))
+
+
+def test_merge_zero_adapter_is_dequantize():
+    p = wl.config1()
+    qd = qn.nf4_quantize(torch.from_numpy(p.W()).cuda())
+    B = np.zeros((p.N, p.r), np.uint16)
+    m16, _ = qn.nf4_merge_lora(qd, bf16_dev(p.A()), bf16_dev(B), p.scale)
+    assert np.array_equal(bits_host(m16), bits_host(qn.nf4_dequantize(qd)))
+
+
+def test_requantized_merge_bit_exact_and_loses_the_adapter():
+    """Requantizing the merged weights (the pages' dequantize -> merge -> requantize path) is
+    bit-exact with the oracle's quantization of the same merged values; its reconstruction
+    error is of the size of the adapter update, so most of that update is lost."""
+    p = wl.config2()
+    qd = qn.nf4_quantize(torch.from_numpy(p.W()).cuda())
+    _, m32 = qn.nf4_merge_lora(qd, bf16_dev(p.A()), bf16_dev(p.B()), p.scale, bf16=False, f32=True)
+    q2 = qn.nf4_quantize(m32)
+    o2 = oracle.quantize(m32.cpu().numpy())
+    assert np.array_equal(q2.codes.cpu().numpy(), o2["codes"])
+    assert np.array_equal(q2.scale_codes.cpu().numpy(), o2["qscale"])
+    base = f32_host(qn.nf4_dequantize(qd))
+    merged = m32.cpu().numpy().astype(np.float64)
+    requant = f32_host(qn.nf4_dequantize(q2))
+    delta = np.linalg.norm(merged - base)
+    loss = np.linalg.norm(requant - merged)
+    assert delta > 0 and loss > 0.5 * delta
+
+
+# ------------------------------------------------------------------ NF4 vs INT4 error
+@pytest.mark.parametrize("kind,n", [("normal", 4096 * 4096), ("student_t", 1 << 20),
+                                    ("normal", 1001), ("normal", 64 * 3 + 5)])
+def test_int4_error_stats_match_oracle(kind, n):
+    if kind == "normal":
+        W = wl.weight((n,), seed=41, sigma=0.02)
+    else:
+        W = wl.student_t_weight((n,), seed=42, df=3.0, sigma=0.02)
+    got = qn.nf4_int4_error_stats(torch.from_numpy(W).cuda()).cpu().numpy()
+    want = oracle.int4_error(W)
+    assert got[0] == pytest.approx(want[0], rel=1e-6)
+    assert got[1] == pytest.approx(want[1], rel=1e-5)
+    assert got[2] == pytest.approx(want[2], rel=1e-5)
+    if kind == "normal" and n >= 4096:
+        assert got[1] < 0.9 * got[2]

@@ -391,3 +391,104 @@ def test_backward_finite_difference(small):
         args_m[which] = args_m[which] - h * D
         fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
         assert fd == pytest.approx((grad * D).sum(), rel=1e-6)
+
+
+# ---------------------------------------------------------------- merge (reading R11)
+
+def _bf16_nearest_exact(x: Fraction) -> int:
+    """Brute force: bits of the bf16 nearest to the rational x, ties to the even pattern."""
+    if x == 0:
+        return 0
+    sign = 0x8000 if x < 0 else 0
+    ax = -x if x < 0 else x
+    # bracket ax between consecutive positive bf16 values by bisection on the bit pattern
+    lo, hi = 0, 0x7F80  # +0 .. +inf
+    val = lambda b: Fraction(float(wl.bf16_bits_to_f32(np.array([b], np.uint16))[0]))
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if val(mid) <= ax:
+            lo = mid
+        else:
+            hi = mid
+    dl, dh = ax - val(lo), val(hi) - ax
+    b = lo if dl < dh or (dl == dh and lo % 2 == 0) else hi
+    return sign | b
+
+
+def test_bf16_rne_double_against_exact_rounding():
+    g = wl.rng(11)
+    xs = list(g.standard_normal(300) * 10.0 ** g.integers(-30, 30, 300))
+    xs += [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 3e-39, 2.0 ** -133,
+           1.5 * 2.0 ** -133, 1.0 + 2.0 ** -8 + 2.0 ** -40]
+    want = np.array([_bf16_nearest_exact(Fraction(float(x))) for x in xs], np.uint16)
+    assert np.array_equal(oracle.bf16_rne_double(xs), want)
+
+
+def test_merge_with_zero_adapter_is_the_dequantization():
+    W = wl.weight((64, 128), seed=21, sigma=0.02)
+    q = oracle.quantize(W)
+    A = wl.bf16_normal((8, 128), seed=22, sigma=0.01)
+    B = np.zeros((64, 8), np.uint16)
+    got = oracle.merge(q, A, B, 2.0)
+    assert np.array_equal(got.ravel(), oracle.dequantize(q))
+
+
+def test_merge_brute_force_small():
+    """Every element from exact rational arithmetic rounded once (R11)."""
+    N, K, r, s = 6, 64, 3, 0.75
+    W = wl.weight((N, K), seed=23, sigma=0.02)
+    q = oracle.quantize(W)
+    Wd = wl.bf16_bits_to_f32(oracle.dequantize(q)).reshape(N, K)
+    A = wl.bf16_normal((r, K), seed=24, sigma=0.01)
+    B = wl.bf16_normal((N, r), seed=25, sigma=0.01)
+    Af, Bf = wl.bf16_bits_to_f32(A), wl.bf16_bits_to_f32(B)
+    want = np.zeros((N, K), np.uint16)
+    for n in range(N):
+        for k in range(K):
+            d = sum(Fraction(float(Bf[n, j])) * Fraction(float(Af[j, k])) for j in range(r))
+            want[n, k] = _bf16_nearest_exact(Fraction(float(Wd[n, k])) + Fraction(s) * d)
+    assert np.array_equal(oracle.merge(q, A, B, s), want)
+
+
+# ---------------------------------------------------------------- NF4 vs INT4 (reading R12)
+
+def test_int4_error_zero_on_each_grid_and_sum_of_squares():
+    L, _ = oracle.levels()
+    g = wl.rng(31)
+    a = np.float32(0.5)
+    # every block holds the absmax and otherwise NF4 levels times it: NF4 error is exactly 0
+    c = g.integers(0, 16, size=(64, 64))
+    c[:, 0] = 15
+    Wn = (L[c] * a).astype(np.float32).ravel()
+    s = oracle.int4_error(Wn)
+    assert s[1] == 0.0 and s[2] > 0.0
+    assert s[0] == pytest.approx(float(np.sum(Wn.astype(np.float64) ** 2)), rel=1e-12)
+    # absmax 7 * 2^-6 and multiples of 2^-6: exactly on the INT4 grid
+    qv = g.integers(-7, 8, size=(64, 64)).astype(np.float32)
+    qv[:, 0] = 7
+    Wi = (qv * np.float32(2.0 ** -6)).ravel()
+    assert oracle.int4_error(Wi)[2] == 0.0
+
+
+def test_int4_error_brute_force_small():
+    """Exact nearest level (fp64 argmin, ties down) and plain rint for INT4."""
+    W = wl.weight((16, 64), seed=32, sigma=0.02)
+    L, _ = oracle.levels()
+    Wb = W.reshape(-1, 64)
+    a = np.abs(Wb).max(axis=1, keepdims=True)
+    x = (Wb / a).astype(np.float32)
+    c = _exact_nearest(x.ravel(), L).reshape(x.shape)
+    en = Wb.astype(np.float64) - L[c].astype(np.float64) * a.astype(np.float64)
+    qv = np.clip(np.rint((np.float32(7.0) * x).astype(np.float32)), -7, 7)
+    ei = Wb.astype(np.float64) - qv.astype(np.float64) * (a / np.float32(7.0)).astype(np.float32).astype(np.float64)
+    got = oracle.int4_error(W)
+    assert got[1] == pytest.approx(float((en ** 2).sum()), rel=1e-12)
+    assert got[2] == pytest.approx(float((ei ** 2).sum()), rel=1e-12)
+
+
+def test_nf4_beats_int4_on_normal_weights():
+    """aicurriculum 'Design Details That Matter': NF4 (normal quantiles) is often better
+    than naive INT4; on normally distributed weights its squared error is clearly lower."""
+    W = wl.weight((256, 1024), seed=33, sigma=0.02)
+    s = oracle.int4_error(W)
+    assert s[1] < 0.9 * s[2]
