@@ -600,6 +600,23 @@ def measure_secondary(qn, wl, dev, peaks, traffic, l2_flush, reps: int = 10):
             "gemv_kernel_frac_hbm": meta / ms_gemv / 1e6 / hbm,
             "gemv_traffic": traffic.get(("decode_gemv", "config4")) if M == 1 else None,
             "kernels_ms": {k: v[1] / reps for k, v in prof.items()}}
+    # per-token adapters: 16 tokens over 4 adapters (r = 64) on the same base
+    p = wl.config4(16)
+    nad = 4
+    X = bf16_dev(p.X(), dev)
+    A_all = torch.stack([bf16_dev(wl.bf16_normal((p.r, p.K), seed=4100 + i, sigma=0.01), dev)
+                         for i in range(nad)])
+    B_all = torch.stack([bf16_dev(wl.bf16_normal((p.N, p.r), seed=4200 + i, sigma=0.01), dev)
+                         for i in range(nad)])
+    idx = torch.arange(16, dtype=torch.int32, device=dev) % nad
+    scales = torch.full((nad,), p.scale, dtype=torch.float32, device=dev)
+    Y = torch.empty(16, p.N, dtype=torch.bfloat16, device=dev)
+    fn = lambda: qn.qlora_linear_fwd_multi(X, q, A_all, B_all, idx, scales, out=Y)  # noqa: E731
+    ms_all, prof = timed(fn, ["multi_u", "multi_z", "decode_gemv"])
+    nbytes = meta + 2 * 16 * p.K + 2 * 16 * p.N + nad * 2 * p.r * (p.K + p.N)
+    out["decode_fwd_M16_4adapters"] = {
+        "GB/s": nbytes / ms_all / 1e6, "frac_hbm": nbytes / ms_all / 1e6 / hbm, "ms": ms_all,
+        "bytes": nbytes, "kernels_ms": {k: v[1] / reps for k, v in prof.items()}}
     return out
 
 

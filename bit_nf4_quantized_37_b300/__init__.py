@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     profile_stop,
     qlora_linear_bwd,
     qlora_linear_fwd,
+    qlora_linear_fwd_multi,
     qlora_workspace_bytes,
     status_str,
 )
@@ -35,5 +36,5 @@ __all__ = [
     "nf4_int4_error_stats", "nf4_merge_lora",
     "nf4_quantize", "nf4_quantize_noalloc", "nf4_quantize_workspace_bytes", "nf4_storage_bytes", "profile_start",
     "profile_stop", "qlora_linear_bwd",
-    "qlora_linear_fwd", "qlora_workspace_bytes", "status_str",
+    "qlora_linear_fwd", "qlora_linear_fwd_multi", "qlora_workspace_bytes", "status_str",
 ]

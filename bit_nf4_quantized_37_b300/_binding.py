@@ -23,7 +23,8 @@ EXPORTS = ["nf4_storage_bytes", "nf4_quantize_workspace_bytes", "nf4_quantize",
            "nf4_dequantize", "qlora_workspace_bytes", "qlora_linear_fwd", "qlora_linear_bwd",
            "nf4_level_table", "qlora_device_status", "qlora_status_str", "qlora_version",
            "qlora_profile_start", "qlora_profile_stop", "nf4_quantize_noalloc",
-           "nf4_merge_lora", "nf4_int4_error_workspace_bytes", "nf4_int4_error_stats"]
+           "nf4_merge_lora", "nf4_int4_error_workspace_bytes", "nf4_int4_error_stats",
+           "qlora_linear_fwd_multi"]
 
 
 class QLoRAError(RuntimeError):
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
             "qlora_profile_stop": [vp, i32, vp],
             "nf4_quantize_noalloc": [vp, sp, vp],
             "nf4_merge_lora": [sp, vp, vp, i32, ctypes.c_float, vp, vp, vp],
+            "qlora_linear_fwd_multi": [vp, i64, sp, vp, vp, i32, i32, vp, vp, vp, vp,
+                                       ctypes.c_uint64, vp],
             "nf4_int4_error_workspace_bytes": [u64p],
             "nf4_int4_error_stats": [vp, i64, vp, vp, ctypes.c_uint64, vp],
         }
@@ -234,6 +237,28 @@ def qlora_linear_fwd(X: torch.Tensor, q: NF4Tensor, A: torch.Tensor, B: torch.Te
         _ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(Y), _ptr(U),
         _ptr(ws), ws.numel(), _stream()))
     return Y, U
+
+
+def qlora_linear_fwd_multi(X: torch.Tensor, q: NF4Tensor, A_all: torch.Tensor,
+                           B_all: torch.Tensor, adapter_idx: torch.Tensor, scales: torch.Tensor,
+                           out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y_t = X_t W'^T + s_a (X_t A_a^T) B_a^T with a = adapter_idx[t], for M <= 16 tokens.
+    A_all [n, r, K], B_all [n, N, r] bf16; adapter_idx int32 [M]; scales fp32 [n]."""
+    for t, n in ((X, "X"), (A_all, "A_all"), (B_all, "B_all")):
+        _req(t, torch.bfloat16, n)
+    _req(adapter_idx, torch.int32, "adapter_idx")
+    _req(scales, torch.float32, "scales")
+    M, K = X.shape
+    n_ad, r, _ = A_all.shape
+    N = q.rows
+    Y = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=X.device)
+    nb = qlora_workspace_bytes(M, N, K, r)
+    ws = _workspace(nb, X.device)
+    s = q.c_struct()
+    _check("qlora_linear_fwd_multi", lib().qlora_linear_fwd_multi(
+        _ptr(X), M, ctypes.byref(s), _ptr(A_all), _ptr(B_all), r, n_ad, _ptr(adapter_idx),
+        _ptr(scales), _ptr(Y), _ptr(ws), ws.numel(), _stream()))
+    return Y
 
 
 def qlora_linear_bwd(dY: torch.Tensor, X: torch.Tensor, q: NF4Tensor, A: torch.Tensor,

@@ -172,6 +172,32 @@ int qlora_linear_fwd(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const u
   return linear_forward(a, static_cast<cudaStream_t>(stream));
 }
 
+int qlora_linear_fwd_multi(const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                           const uint16_t* A_all, const uint16_t* B_all, int32_t r,
+                           int32_t n_adapters, const int32_t* adapter_idx, const float* scales,
+                           uint16_t* Y, void* ws, uint64_t ws_bytes, void* stream) {
+  int st = check_tensor(Wq);
+  if (st) return st;
+  if (!X || !A_all || !B_all || !adapter_idx || !scales || !Y || !ws || M < 1 || r < 1 ||
+      n_adapters < 1)
+    return QLORA_ERR_INVALID_ARG;
+  if (r > kMaxRank || M > kSkinnyMaxM) return QLORA_ERR_UNSUPPORTED;
+  const int64_t N = Wq->rows, K = Wq->cols;
+  if (N % 64 != 0 || K % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (!aligned16(X) || !aligned16(A_all) || !aligned16(B_all) || !aligned16(Y) ||
+      !aligned16(ws) || (reinterpret_cast<uintptr_t>(adapter_idx) & 3u) ||
+      (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return QLORA_ERR_MISALIGNED;
+  if (ws_bytes < linear_workspace_bytes(M, N, K, r)) return QLORA_ERR_WORKSPACE;
+  if ((st = check_device())) return st;
+  LinearArgs a{};
+  a.M = M; a.N = N; a.K = K; a.r = r; a.scale = 1.0f;
+  a.X = X; a.A = A_all; a.B = B_all; a.Y = Y; a.q = *Wq;
+  a.ws = ws; a.ws_bytes = ws_bytes;
+  a.adapter_idx = adapter_idx; a.n_adapters = n_adapters; a.scales = scales;
+  return linear_forward(a, static_cast<cudaStream_t>(stream));
+}
+
 int qlora_linear_bwd(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
                      const uint16_t* A, const uint16_t* B, int32_t r, float scale,
                      const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,

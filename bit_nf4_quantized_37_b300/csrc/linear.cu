@@ -33,8 +33,10 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r) {
   L.Bp = take(r % 8 ? (uint64_t)N * L.rp * 2 : 0);
   L.part_bytes = std::max(side_partial_bytes(M, N, K, r), skinny_partial_bytes(M, N, K, r));
   L.part = take(L.part_bytes);
-  L.ntickets = side_ticket_count(M, N, K);
+  // the split reductions' counters; at least one per token for the per-token adapter path
+  L.ntickets = std::max<uint64_t>(side_ticket_count(M, N, K), (uint64_t)kSkinnyMaxM);
   L.tickets = take(L.ntickets * 4);
+  L.Z = take(M <= kSkinnyMaxM ? (uint64_t)M * N * 4 : 0);
   L.total = off;
   return L;
 }
@@ -54,6 +56,7 @@ int linear_forward(const LinearArgs& a, cudaStream_t stream) {
   const WorkspaceLayout L = workspace_layout(a.M, a.N, a.K, a.r);
   int st = clear_tickets(a, L, stream);
   if (st) return st;
+  if (a.adapter_idx) return launch_multi_fwd(a, L, stream);  // M <= 16, checked by the caller
   if (a.M <= kSkinnyMaxM) return launch_skinny_fwd(a, L, stream);
   if ((st = launch_lora_u(a, L, a.U, stream))) return st;
   if (a.r % 8 && (st = launch_pad_b(a, L, stream))) return st;

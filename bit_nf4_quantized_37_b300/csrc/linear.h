@@ -32,6 +32,12 @@ struct LinearArgs {
   void* ws;
   uint64_t ws_bytes;
   int gemm_priority;    // launch priority of the fused GEMM (0: the stream's own)
+  // per-token adapters (decode path only): A = [n_adapters, r, K], B = [n_adapters, N, r],
+  // token t uses adapter adapter_idx[t] with scale scales[adapter_idx[t]] (both on the
+  // device); an index outside [0, n_adapters) means no adapter for that token
+  const int32_t* adapter_idx;
+  int n_adapters;
+  const float* scales;
 };
 
 // Workspace regions (byte offsets, each 1024-aligned), for rank padded to rp = 64*ceil(r/64).
@@ -45,6 +51,7 @@ struct WorkspaceLayout {
   uint64_t part_bytes;
   uint64_t tickets;  // int [ntickets] arrival counters of the split reductions
   uint64_t ntickets;
+  uint64_t Z;        // fp32 [M, N] per-token LoRA term (decode path, per-token adapters)
   uint64_t total;
 };
 
@@ -61,6 +68,14 @@ int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t
 int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 // Decode path (M <= 16): Y = X W'^T + sU Bp^T with the weights streamed once.
 int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+// Its two parts: sU = bf16(scale X A^T) (small_u), and the GEMV, which forms the LoRA term
+// from sU and B on the tensor cores, or adds a precomputed fp32 term Z when Z is not null.
+int launch_skinny_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const float* Z,
+                       cudaStream_t stream);
+// Decode path with per-token adapters (multi.cu): U_t = X_t A_{a(t)}^T, then
+// Z_t = s_{a(t)} U_t B_{a(t)}^T, then the GEMV adding Z.
+int launch_multi_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 // Rank-r side products on the tensor cores (mma.sync), split over the contraction, with the
 // split reduction done by the last CTA of each row tile (lora_side.cu).
 int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cudaStream_t stream);

@@ -138,6 +138,9 @@ struct Params {
   int64_t rp;
   int r;
   uint16_t* Y;
+  // [M][N] fp32 LoRA term computed outside (per-token adapters); when set, the kernel adds it
+  // before the final rounding instead of forming s U B^T on the tensor cores
+  const float* Z;
   float levels[16];  // the NF4 levels (parameter space: no cold constant-cache miss)
 };
 
@@ -256,7 +259,8 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   uint4 su_v = make_uint4(0, 0, 0, 0);
   {
     const int t = tid / (SU_PITCH / 8), c8 = tid % (SU_PITCH / 8);
-    if (t < p.M && 8 * c8 < p.rp) su_v = __ldg(reinterpret_cast<const uint4*>(p.sU + t * p.rp + 8 * c8));
+    if (p.sU && t < p.M && 8 * c8 < p.rp)
+      su_v = __ldg(reinterpret_cast<const uint4*>(p.sU + t * p.rp + 8 * c8));
   }
   for (int i = tid; i < 256 * 8; i += THREADS + PRODUCERS) {
     const int v = i >> 3;  // 8 threads per entry: 16 bytes (4 lane copies) each
@@ -363,8 +367,9 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     for (int i = 0; i < lora_boxes; ++i)
       tma_load_2d(sLora + i * LORA_BOX_BYTES, &tmB, &lora_bar, 64 * i, static_cast<int32_t>(rb * ROWS));
   };
-  if (tid == 0 && s_begin % p.KST == 0) issue_lora(rb_first);
-  bool lora_pending = s_begin % p.KST == 0;  // a B-row tile is in flight, not yet used
+  const bool own_lora = p.Z == nullptr;  // uniform: the LoRA term on the tensor cores here
+  if (tid == 0 && own_lora && s_begin % p.KST == 0) issue_lora(rb_first);
+  bool lora_pending = own_lora && s_begin % p.KST == 0;  // a B-row tile in flight, not yet used
 
   const uint32_t lane_addr = kTableBase | (static_cast<uint32_t>(lane) * 4u);
   auto lut = [&](uint32_t word, uint32_t j) -> uint32_t {
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   uint32_t lora_phase = 0;
   const int nchunks = (p.r + 15) / 16;
   auto flush = [&](int64_t rb, int64_t ks_first, int64_t ks_last) -> bool {
-    if (ks_first == 0) {
+    if (ks_first == 0 && own_lora) {
       if (blk == 0 && mbar_wait(&lora_bar, lora_phase, kWaitLora, abort_p, &g_decode_error)) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
           sRed[(warp * C::ACC + (j * NT + o) * 4 + d) * 32 + lane] = acc[j][o][d];
     consumers_sync();
     if (*abort_p) return false;  // uniform after the barrier; the B-row tile stays pending
-    if (ks_first == 0) {
+    if (ks_first == 0 && own_lora) {
       lora_phase ^= 1u;
       lora_pending = false;
     }
@@ -440,7 +445,10 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       v += sRed[(wb + 2) * C::ACC * 32 + idx];
       v += sRed[(wb + 3) * C::ACC * 32 + idx];
       if (whole) {
-        if (n < p.N) p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        if (n < p.N) {
+          if (p.Z) v += __ldg(p.Z + t * p.N + n);
+          p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        }
       } else {
         __stcg(mine + t * ROWS + R, v);
       }
@@ -463,7 +471,10 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
             const int64_t sl = rb == stage_begin(p.T, G, c) / p.KST ? 0 : 1;
             v += __ldcg(p.part + (c * 2 + sl) * 16 * ROWS + t * ROWS + R);
           }
-          if (n < p.N) p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+          if (n < p.N) {
+            if (p.Z) v += __ldg(p.Z + t * p.N + n);
+            p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+          }
         }
         if (tid == 0) p.tickets[rb] = 0;  // ready for the next launch
       }
@@ -511,11 +522,13 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   for (int i = 0; i < nst; ++i) {
     if (ks == 0 && i != 0) {
       ks_first = 0;
-      if (tid == 0) {
-        fence_proxy_async_smem();  // the last flush's accesses to the region precede the refill
-        issue_lora(rb);
+      if (own_lora) {
+        if (tid == 0) {
+          fence_proxy_async_smem();  // the last flush's accesses to the region precede the refill
+          issue_lora(rb);
+        }
+        lora_pending = true;
       }
-      lora_pending = true;
     }
     const bool got =
         mbar_wait<false, true>(&full_bar[slot], phase, kWaitTmaFull, abort_p, &g_decode_error);
@@ -725,33 +738,35 @@ uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K, int r) {
   return gemv > u ? gemv : u;
 }
 
-int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+int launch_skinny_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   uint16_t* sU = reinterpret_cast<uint16_t*>(ws + L.sU);
-  {
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(skinny::small_u, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               skinny::small_u_smem(2 * 64)) != cudaSuccess)
-        return QLORA_ERR_CUDA;
-      attr = true;
-    }
-    ProfileScope ps("decode_u", stream);
-    const unsigned chunks = (unsigned)((a.K + skinny::U_KC - 1) / skinny::U_KC);
-    skinny::small_u<<<chunks, 256, skinny::small_u_smem(L.rp), stream>>>(
-        a.X, a.M, a.K, a.A, a.r, L.rp, a.scale, sU, a.U, reinterpret_cast<float*>(ws + L.part),
-        reinterpret_cast<int*>(ws + L.tickets));
-    if (cudaGetLastError() != cudaSuccess) return QLORA_ERR_CUDA;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(skinny::small_u, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             skinny::small_u_smem(2 * 64)) != cudaSuccess)
+      return QLORA_ERR_CUDA;
+    attr = true;
   }
-  int st = QLORA_OK;
-  if (a.r % 8 && (st = launch_pad_b(a, L, stream))) return st;
+  ProfileScope ps("decode_u", stream);
+  const unsigned chunks = (unsigned)((a.K + skinny::U_KC - 1) / skinny::U_KC);
+  skinny::small_u<<<chunks, 256, skinny::small_u_smem(L.rp), stream>>>(
+      a.X, a.M, a.K, a.A, a.r, L.rp, a.scale, sU, a.U, reinterpret_cast<float*>(ws + L.part),
+      reinterpret_cast<int*>(ws + L.tickets));
+  return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+}
+
+int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const float* Z,
+                       cudaStream_t stream) {
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  const bool own_lora = Z == nullptr;
   CUtensorMap tmC, tmX, tmB;
   const bool mapped =
       make_tensor_map_2d(&tmC, a.q.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)(a.K / 2),
                          (uint64_t)a.N, (uint64_t)(a.K / 2), 128, skinny::ROWS, MapSwizzle::B128) &&
       make_tensor_map_2d(&tmX, a.X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.K,
                          (uint64_t)a.M, (uint64_t)a.K * 2, 64, (uint32_t)a.M, MapSwizzle::B128) &&
-      (a.r % 8 == 0  // B [N, r] itself; TMA fills the columns past r with zeros
+      (!own_lora || a.r % 8 == 0  // B [N, r] itself; TMA fills the columns past r with zeros
            ? make_tensor_map_2d(&tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)a.r,
                                 (uint64_t)a.N, (uint64_t)a.r * 2, 64, skinny::ROWS, MapSwizzle::B128)
            : make_tensor_map_2d(&tmB, ws + L.Bp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
@@ -771,18 +786,26 @@ int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_
   p.qs_words = (p.KB % 4 == 0 && reinterpret_cast<uintptr_t>(a.q.scale_codes) % 4 == 0) ? 1 : 0;
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.tickets = reinterpret_cast<int*>(ws + L.tickets);
-  p.sU = sU;
+  p.sU = own_lora ? reinterpret_cast<const uint16_t*>(ws + L.sU) : nullptr;
   p.rp = L.rp;
   p.r = a.r;
   p.Y = a.Y;
+  p.Z = Z;
   {
-    constexpr float L[16] = QLORA_NF4_LEVELS;
-    for (int i = 0; i < 16; ++i) p.levels[i] = L[i];
+    constexpr float Lv[16] = QLORA_NF4_LEVELS;
+    for (int i = 0; i < 16; ++i) p.levels[i] = Lv[i];
   }
   const unsigned ctas = (unsigned)skinny_ctas(a.N, a.K);
   ProfileScope ps("decode_gemv", stream);
   return a.M > 8 ? run_decode<2>(tmC, tmX, tmB, p, ctas, stream)
                  : run_decode<1>(tmC, tmX, tmB, p, ctas, stream);
+}
+
+int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+  int st = launch_skinny_u(a, L, stream);
+  if (st) return st;
+  if (a.r % 8 && (st = launch_pad_b(a, L, stream))) return st;
+  return launch_decode_gemv(a, L, nullptr, stream);
 }
 
 }  // namespace qlora

@@ -149,6 +149,23 @@ int qlora_linear_fwd(const uint16_t* X, int64_t M, const nf4_tensor* Wq,
                      uint16_t* Y, float* U_save, void* ws, uint64_t ws_bytes, void* stream);
 
 /*
+ * qlora_linear_fwd for M <= 16 tokens that each choose their own adapter over one shared NF4
+ * base (addaly.com "QLoRA on one card", "Merging a QLoRA adapter, and the subtlety": keep the
+ * adapter separate and load it over the base, which also lets you swap adapters):
+ *     Y_t = bf16( X_t W'^T + s_a (X_t A_a^T) B_a^T ),  a = adapter_idx[t]
+ * A_all [n_adapters, r, K] and B_all [n_adapters, N, r] bf16; adapter_idx [M] int32 and
+ * scales [n_adapters] fp32 are device buffers (4-byte aligned).  A token whose index is
+ * outside [0, n_adapters) gets the base product only.  U_t is formed in fp32 (fixed-order
+ * split over K), the adapter term s_a U_t B_a^T in fp32 and added to the fp32 base product
+ * before the one rounding to bf16.  Shapes as for qlora_linear_fwd; M > 16 returns
+ * QLORA_ERR_UNSUPPORTED.  ws: qlora_workspace_bytes(M, N, K, r).
+ */
+int qlora_linear_fwd_multi(const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                           const uint16_t* A_all, const uint16_t* B_all, int32_t r,
+                           int32_t n_adapters, const int32_t* adapter_idx, const float* scales,
+                           uint16_t* Y, void* ws, uint64_t ws_bytes, void* stream);
+
+/*
  * Backward of qlora_linear_fwd with the base frozen (junaidshaukat.com recipe item 3 and
  * infivelines "QLoRA": gradients flow back through the quantized weights without updating
  * them -- there is no dW):

@@ -337,3 +337,40 @@ def test_int4_error_stats_match_oracle(kind, n):
     assert got[2] == pytest.approx(want[2], rel=1e-5)
     if kind == "normal" and n >= 4096:
         assert got[1] < 0.9 * got[2]
+
+
+# ------------------------------------------------------------------ per-token adapters
+def _multi_case(N, K, M, r, nad, seed):
+    W = wl.weight((N, K), seed=seed, sigma=0.015)
+    qo = oracle.quantize(W)
+    Wd = oracle.dequantize(qo).reshape(N, K)
+    qd = qn.nf4_quantize(torch.from_numpy(W).cuda())
+    A = [wl.bf16_normal((r, K), seed=seed + 10 + i, sigma=0.01) for i in range(nad)]
+    B = [wl.bf16_normal((N, r), seed=seed + 20 + i, sigma=0.01) for i in range(nad)]
+    scales = np.array([0.25, 0.5, 2.0, 1.0][:nad], np.float32)
+    X = wl.bf16_normal((M, K), seed=seed + 30)
+    idx = np.array([(t % (nad + 1)) - 1 for t in range(M)], np.int32)  # -1: no adapter
+    Y = qn.qlora_linear_fwd_multi(bf16_dev(X), qd, bf16_dev(np.stack(A)), bf16_dev(np.stack(B)),
+                                  torch.from_numpy(idx).cuda(), torch.from_numpy(scales).cuda())
+    ref = np.zeros((M, N))
+    zeroB = np.zeros((N, r), np.uint16)
+    for t in range(M):
+        a = int(idx[t])
+        if 0 <= a < nad:
+            ref[t] = oracle.lora_fwd(X[t:t + 1], Wd, A[a], B[a], float(scales[a]))[0][0]
+        else:
+            ref[t] = oracle.lora_fwd(X[t:t + 1], Wd, A[0], zeroB, 1.0)[0][0]
+    return f32_host(Y), ref
+
+
+@pytest.mark.parametrize("M,r", [(1, 16), (5, 64), (16, 64), (16, 24), (9, 128)])
+def test_multi_adapter_decode(M, r):
+    got, ref = _multi_case(2048, 4096, M, r, 3, seed=51)
+    assert rel_fro(got, ref) <= TOL
+    for t in range(M):  # every token against its own adapter, not only the whole batch
+        assert rel_fro(got[t], ref[t]) <= TOL
+
+
+def test_multi_adapter_decode_full_size():
+    got, ref = _multi_case(28672, 8192, 4, 64, 3, seed=52)
+    assert rel_fro(got, ref) <= TOL
