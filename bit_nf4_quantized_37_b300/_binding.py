@@ -12,6 +12,7 @@ LIB_PATH = os.path.join(_HERE, "libqlora_nf4.so")
 
 NF4_BLOCKSIZE = 64
 NF4_DQ_BLOCK = 256
+NF4_NO_DQ = 0
 
 _STATUS = {0: "QLORA_OK", -1: "QLORA_ERR_INVALID_ARG", -2: "QLORA_ERR_UNSUPPORTED",
            -3: "QLORA_ERR_MISALIGNED", -4: "QLORA_ERR_WORKSPACE", -5: "QLORA_ERR_CUDA",
@@ -116,32 +117,36 @@ class NF4Tensor:
     scale_mean: torch.Tensor   # fp32  [1]
     rows: int
     cols: int
+    dq_block: int = NF4_DQ_BLOCK  # NF4_NO_DQ: scale_steps holds the fp32 block absmax
 
     @property
     def numel(self) -> int:
         return self.rows * self.cols
 
     def c_struct(self) -> _NF4Struct:
-        return _NF4Struct(_ptr(self.codes), _ptr(self.scale_codes), _ptr(self.scale_steps),
-                          _ptr(self.scale_mean), self.rows, self.cols, NF4_BLOCKSIZE,
-                          NF4_DQ_BLOCK)
+        def p(t):
+            return _ptr(t) if t is not None and t.numel() > 0 else 0
+        return _NF4Struct(p(self.codes), p(self.scale_codes), p(self.scale_steps),
+                          p(self.scale_mean), self.rows, self.cols, NF4_BLOCKSIZE, self.dq_block)
 
     def storage_bytes(self) -> int:
-        return nf4_storage_bytes(self.rows, self.cols)[1]
+        return nf4_storage_bytes(self.rows, self.cols, self.dq_block)[1]
 
     @staticmethod
-    def empty(rows: int, cols: int, device) -> "NF4Tensor":
-        sizes, _ = nf4_storage_bytes(rows, cols)
+    def empty(rows: int, cols: int, device, double_quant: bool = True) -> "NF4Tensor":
+        dq = NF4_DQ_BLOCK if double_quant else NF4_NO_DQ
+        sizes, _ = nf4_storage_bytes(rows, cols, dq)
         return NF4Tensor(torch.empty(sizes[0], dtype=torch.uint8, device=device),
                          torch.empty(sizes[1], dtype=torch.int8, device=device),
                          torch.empty(sizes[2] // 4, dtype=torch.float32, device=device),
-                         torch.empty(1, dtype=torch.float32, device=device), rows, cols)
+                         torch.empty(sizes[3] // 4, dtype=torch.float32, device=device), rows, cols,
+                         dq)
 
 
-def nf4_storage_bytes(rows: int, cols: int) -> tuple[list[int], int]:
+def nf4_storage_bytes(rows: int, cols: int, dq_block: int = 256) -> tuple[list[int], int]:
     sizes = (ctypes.c_uint64 * 4)()
     total = _u64()
-    _check("nf4_storage_bytes", lib().nf4_storage_bytes(rows, cols, NF4_BLOCKSIZE, NF4_DQ_BLOCK,
+    _check("nf4_storage_bytes", lib().nf4_storage_bytes(rows, cols, NF4_BLOCKSIZE, dq_block,
                                                          sizes, ctypes.byref(total)))
     return [int(s) for s in sizes], int(total.value)
 
@@ -188,11 +193,12 @@ def _req(t: torch.Tensor, dtype, name: str):
 
 
 def nf4_quantize(W: torch.Tensor, out: NF4Tensor | None = None,
-                 workspace: torch.Tensor | None = None) -> NF4Tensor:
-    """Quantize fp32 weights [rows, cols] (CUDA) to NF4 with double-quantized scales."""
+                 workspace: torch.Tensor | None = None, double_quant: bool = True) -> NF4Tensor:
+    """Quantize fp32 weights [rows, cols] (CUDA) to NF4 with double-quantized scales, or with
+    fp32 block absmax scales when double_quant is False (or `out` is of that variant)."""
     _req(W, torch.float32, "W")
     rows, cols = (W.shape[0], W.shape[1]) if W.dim() == 2 else (1, W.numel())
-    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device)
+    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, double_quant)
     nb = nf4_quantize_workspace_bytes(rows * cols)
     ws = workspace if workspace is not None else _workspace(nb, W.device)
     s = q.c_struct()

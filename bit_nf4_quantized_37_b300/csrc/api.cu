@@ -30,11 +30,13 @@ int check_device() {
 int check_tensor(const nf4_tensor* q) {
   if (!q) return QLORA_ERR_INVALID_ARG;
   if (q->rows < 1 || q->cols < 1) return QLORA_ERR_INVALID_ARG;
-  if (q->blocksize != NF4_BLOCKSIZE || q->dq_block != NF4_DQ_BLOCK) return QLORA_ERR_UNSUPPORTED;
-  if (!q->codes || !q->scale_codes || !q->scale_steps || !q->scale_mean)
+  if (q->blocksize != NF4_BLOCKSIZE || (q->dq_block != NF4_DQ_BLOCK && q->dq_block != NF4_NO_DQ))
+    return QLORA_ERR_UNSUPPORTED;
+  const bool dq = q->dq_block != NF4_NO_DQ;
+  if (!q->codes || !q->scale_steps || (dq && (!q->scale_codes || !q->scale_mean)))
     return QLORA_ERR_INVALID_ARG;
-  if (!aligned16(q->codes) || !aligned16(q->scale_codes) || !aligned16(q->scale_steps) ||
-      !aligned16(q->scale_mean))
+  if (!aligned16(q->codes) || !aligned16(q->scale_steps) ||
+      (dq && (!aligned16(q->scale_codes) || !aligned16(q->scale_mean))))
     return QLORA_ERR_MISALIGNED;
   return QLORA_OK;
 }
@@ -71,11 +73,13 @@ int nf4_level_table(float levels[16], float thresholds[15]) {
 int nf4_storage_bytes(int64_t rows, int64_t cols, int32_t blocksize, int32_t dq_block,
                       uint64_t sizes[4], uint64_t* total) {
   if (rows < 1 || cols < 1) return QLORA_ERR_INVALID_ARG;
-  if (blocksize != NF4_BLOCKSIZE || dq_block != NF4_DQ_BLOCK) return QLORA_ERR_UNSUPPORTED;
+  if (blocksize != NF4_BLOCKSIZE || (dq_block != NF4_DQ_BLOCK && dq_block != NF4_NO_DQ))
+    return QLORA_ERR_UNSUPPORTED;
   const uint64_t numel = (uint64_t)rows * (uint64_t)cols;
   const uint64_t nb = (numel + NF4_BLOCKSIZE - 1) / NF4_BLOCKSIZE;
   const uint64_t ng = (nb + NF4_DQ_BLOCK - 1) / NF4_DQ_BLOCK;
-  const uint64_t s[4] = {(numel + 1) / 2, nb, ng * 4, 4};
+  const bool dq = dq_block != NF4_NO_DQ;
+  const uint64_t s[4] = {(numel + 1) / 2, dq ? nb : 0, dq ? ng * 4 : nb * 4, dq ? 4u : 0u};
   if (sizes) std::memcpy(sizes, s, sizeof(s));
   if (total) *total = s[0] + s[1] + s[2] + s[3];
   return QLORA_OK;

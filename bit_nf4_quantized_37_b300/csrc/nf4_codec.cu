@@ -347,19 +347,23 @@ __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict_
 
 // -------------------------------------------------------------------- dequantize
 // Grid-stride over 16-weight pieces: 8 code bytes in, 32 bytes of bf16 out per thread; the
-// four threads of a 64-block each build the block's byte table.
+// four threads of a 64-block each build the block's byte table.  Without double
+// quantization (dq = 0) `steps` holds the fp32 absmax of every block, and the block scale is
+// fmaf(1, absmax, 0) = absmax through the same arithmetic.
 __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restrict__ codes,
                                                           const int8_t* __restrict__ scale_codes,
                                                           const float* __restrict__ steps,
                                                           const float* __restrict__ mean,
-                                                          int64_t numel, uint16_t* __restrict__ out) {
-  const float mu = __ldg(mean);
+                                                          int64_t numel, int dq,
+                                                          uint16_t* __restrict__ out) {
+  const float mu = dq ? __ldg(mean) : 0.0f;
   const int64_t npieces = (numel + 15) / 16;
   for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < npieces;
        p += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e0 = p * 16;
     const int64_t b = e0 / kBlock;
-    const float scale = __fmaf_rn((float)__ldg(scale_codes + b), __ldg(steps + b / kGroup), mu);
+    const float scale = dq ? __fmaf_rn((float)__ldg(scale_codes + b), __ldg(steps + b / kGroup), mu)
+                           : __ldg(steps + b);
     const Nf4ByteTable tab = nf4_make_table(scale);
     uint32_t q[2];
     if (e0 + 16 <= numel) {
@@ -403,7 +407,9 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
                     cudaStream_t stream) {
   const int64_t nb = (numel + kBlock - 1) / kBlock;
   const int64_t ng = (nb + kGroup - 1) / kGroup;
-  float* absmax = reinterpret_cast<float*>(ws);
+  const bool dq = q.dq_block != 0;
+  // without double quantization pass 1 writes the block absmax straight into the tensor
+  float* absmax = dq ? reinterpret_cast<float*>(ws) : q.scale_steps;
   double* gsum = reinterpret_cast<double*>(reinterpret_cast<char*>(ws) + ng * kGroup * 4);
   {
     ProfileScope ps("nf4_quant_blocks", stream);
@@ -420,6 +426,7 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     const int64_t ctas = ng < resident ? ng : resident;
     nf4_quant_blocks<<<(unsigned)ctas, kQuantThreads, kCellBytes, stream>>>(W, numel, q.codes, absmax, gsum);
   }
+  if (!dq) return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
   double* part = gsum + ng;
   int64_t p2 = 1;
   while (p2 < ng) p2 *= 2;
@@ -463,7 +470,8 @@ int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, cudaStr
   ProfileScope ps("nf4_dequant", stream);
   nf4_dequant_kernel<<<(unsigned)blocks, threads, 0, stream>>>(q.codes, q.scale_codes,
                                                                q.scale_steps, q.scale_mean,
-                                                               numel, out);
+                                                               numel, q.dq_block != 0 ? 1 : 0,
+                                                               out);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 

@@ -61,11 +61,14 @@ using namespace qlora;
 extern "C" int nf4_quantize_noalloc(const float* W, const nf4_tensor* out, void* stream) {
   if (!out || !W) return QLORA_ERR_INVALID_ARG;
   if (out->rows < 1 || out->cols < 1) return QLORA_ERR_INVALID_ARG;
-  if (out->blocksize != NF4_BLOCKSIZE || out->dq_block != NF4_DQ_BLOCK) return QLORA_ERR_UNSUPPORTED;
-  if (!out->codes || !out->scale_codes || !out->scale_steps || !out->scale_mean)
+  if (out->blocksize != NF4_BLOCKSIZE ||
+      (out->dq_block != NF4_DQ_BLOCK && out->dq_block != NF4_NO_DQ))
+    return QLORA_ERR_UNSUPPORTED;
+  const bool dq = out->dq_block != NF4_NO_DQ;
+  if (!out->codes || !out->scale_steps || (dq && (!out->scale_codes || !out->scale_mean)))
     return QLORA_ERR_INVALID_ARG;
-  if (!aligned16(W) || !aligned16(out->codes) || !aligned16(out->scale_codes) ||
-      !aligned16(out->scale_steps) || !aligned16(out->scale_mean))
+  if (!aligned16(W) || !aligned16(out->codes) || !aligned16(out->scale_steps) ||
+      (dq && (!aligned16(out->scale_codes) || !aligned16(out->scale_mean))))
     return QLORA_ERR_MISALIGNED;
   if (out->rows > kNoallocMaxNumel / out->cols) return QLORA_ERR_TOO_LARGE;
   const int64_t numel = out->rows * out->cols;

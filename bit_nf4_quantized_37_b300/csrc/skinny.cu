@@ -129,8 +129,9 @@ struct Params {
   int64_t KST;  // stages per row block
   int64_t T;    // stages in all
   const int8_t* qs;
-  const float* steps;
+  const float* steps;  // group steps, or without double quantization the block absmax
   const float* mean;
+  int dq;              // 1: double-quantized scales
   int qs_words;        // scale codes of a row's stage are one aligned 32-bit word
   float* part;         // [CTAs][2][16][128] fp32 pieces of split row blocks
   int* tickets;        // [row blocks] stages summed so far
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     // early into rotating register sets; otherwise each code is read when needed.
     const int R = tid - THREADS;
     const int pw_idx = warp - THREADS / 32;
-    const float mu = __ldg(p.mean);
+    const float mu = p.dq ? __ldg(p.mean) : 0.0f;
     const bool word_path = p.qs_words != 0;
     const int e0 = 16 * (R >> 4) + 2 * inv_perm8(R & 7) + ((R >> 3) & 1);
     uint32_t pw[SCALE_AHEAD];
@@ -316,7 +317,8 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
             v = __fmaf_rn(static_cast<float>(static_cast<int8_t>((w >> (8 * b)) & 0xFFu)), st, mu);
           } else {
             const int64_t idx = n * p.KB + kb;
-            v = __fmaf_rn(static_cast<float>(__ldg(p.qs + idx)), __ldg(p.steps + (idx >> 8)), mu);
+            v = p.dq ? __fmaf_rn(static_cast<float>(__ldg(p.qs + idx)), __ldg(p.steps + (idx >> 8)), mu)
+                     : __ldg(p.steps + idx);
           }
         }
         asm volatile("st.shared.f32 [%0], %1;" ::"r"(kTableBase + scale_slot_off(slot, b * 128 + e0)), "f"(v));
@@ -783,7 +785,8 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
   p.qs = a.q.scale_codes;
   p.steps = a.q.scale_steps;
   p.mean = a.q.scale_mean;
-  p.qs_words = (p.KB % 4 == 0 && reinterpret_cast<uintptr_t>(a.q.scale_codes) % 4 == 0) ? 1 : 0;
+  p.dq = a.q.dq_block != 0 ? 1 : 0;
+  p.qs_words = (p.dq && p.KB % 4 == 0 && reinterpret_cast<uintptr_t>(a.q.scale_codes) % 4 == 0) ? 1 : 0;
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.tickets = reinterpret_cast<int*>(ws + L.tickets);
   p.sU = own_lora ? reinterpret_cast<const uint16_t*>(ws + L.sU) : nullptr;

@@ -73,6 +73,7 @@ struct Params {
   const int8_t* qs;
   const float* steps;
   const float* mean;
+  int dq;         // 1: double-quantized scales; 0: steps holds the fp32 absmax per block
 };
 
 // One thread's share of an NF4 stage: 64 codes (32 bytes) and the block's scale code/step.
@@ -90,8 +91,13 @@ __device__ __forceinline__ void load_slice(Slice& s, const Params& p, int64_t ro
     s.c0 = __ldg(src);
     s.c1 = __ldg(src + 1);
     const int64_t b = row * (p.Kw / 64) + kcol / 64;
-    s.q = __ldg(p.qs + b);
-    s.step = __ldg(p.steps + (b >> 8));
+    if (p.dq) {
+      s.q = __ldg(p.qs + b);
+      s.step = __ldg(p.steps + (b >> 8));
+    } else {  // fmaf(1, absmax, 0) = absmax in the shared scale arithmetic
+      s.q = 1;
+      s.step = __ldg(p.steps + b);
+    }
   }
 }
 
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= DEQ_WARP0) {
     // ------------------------------------------------------------ NF4 producers
     const int dt = threadIdx.x - DEQ_WARP0 * 32;  // 0..255
-    const float mu = __ldg(p.mean);
+    const float mu = p.dq ? __ldg(p.mean) : 0.0f;
     int64_t row_base, kcol;
     uint32_t dst_off, swz;
     if (kMode == 0) {
@@ -509,7 +515,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ NF4 producers (both CTAs)
     const int group = (warp - DEQ_WARP0) / GROUP_WARPS;           // owns stages s % 2 == group
     const int t = ((warp - DEQ_WARP0) % GROUP_WARPS) * 32 + lane;  // 0..127
-    const float mu = __ldg(p.mean);
+    const float mu = p.dq ? __ldg(p.mean) : 0.0f;
     int64_t row_base, kcol;
     uint32_t dst_off, swz;
     if (kMode == 0) {
@@ -673,6 +679,7 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   p.qs = a.q.scale_codes;
   p.steps = a.q.scale_steps;
   p.mean = a.q.scale_mean;
+  p.dq = a.q.dq_block != 0 ? 1 : 0;
   p.n_lora = static_cast<int>(rp / 64);
   p.lora_last_k16 = static_cast<int>((a.r - 64 * (p.n_lora - 1) + 15) / 16);
   if (kMode == 0) {

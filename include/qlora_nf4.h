@@ -37,7 +37,7 @@ extern "C" {
 /* Status codes.  0 is success; every failure is negative. */
 #define QLORA_OK 0
 #define QLORA_ERR_INVALID_ARG (-1)    /* null pointer, non-positive size, bad scale      */
-#define QLORA_ERR_UNSUPPORTED (-2)    /* blocksize != 64, dq_block != 256, r > 128, or a
+#define QLORA_ERR_UNSUPPORTED (-2)    /* blocksize != 64, dq_block not 256 or 0, r > 128, or a
                                          GEMM shape the kernels do not cover            */
 #define QLORA_ERR_MISALIGNED (-3)     /* a pointer is not 16-byte aligned                */
 #define QLORA_ERR_WORKSPACE (-4)      /* workspace smaller than the *_workspace_bytes size */
@@ -51,6 +51,7 @@ extern "C" {
 
 #define NF4_BLOCKSIZE 64  /* weights per first-level block (one absmax scale each)   */
 #define NF4_DQ_BLOCK 256  /* first-level scales per second-level (double-quant) group */
+#define NF4_NO_DQ 0       /* dq_block value of the variant without double quantization */
 
 /*
  * A blockwise NF4 tensor with double-quantized scales: views into caller-owned device
@@ -65,6 +66,12 @@ extern "C" {
  * The recovered block scale is fmaf(scale_codes[b], scale_steps[b / 256], scale_mean[0]),
  * and weight e dequantizes to bf16_rne(level[code_e] * scale) (one fp32 multiply).
  * All four pointers must be 16-byte aligned.
+ * Variant without double quantization (dq_block = NF4_NO_DQ; junaidshaukat.com recipe item 4
+ * and addaly.com "What each setting is doing" present double quantization as a separate,
+ * optional saving; infivelines.com "QLoRA": without it the block scales cost 32/64 = 0.5 bits
+ * per weight): scale_steps holds the fp32 absmax of every block [ceil(numel / 64)], the block
+ * scale is that absmax, and scale_codes and scale_mean are unused (may be NULL).  Every call
+ * taking an nf4_tensor accepts either variant.
  */
 typedef struct nf4_tensor {
   uint8_t* codes;
@@ -79,11 +86,12 @@ typedef struct nf4_tensor {
 
 /*
  * Sizes in bytes of the four nf4_tensor buffers for a rows x cols tensor:
- * sizes[0] codes, sizes[1] scale_codes, sizes[2] scale_steps, sizes[3] scale_mean; *total
+ * sizes[0] codes, sizes[1] scale_codes, sizes[2] scale_steps, sizes[3] scale_mean (with
+ * dq_block = NF4_NO_DQ: codes, 0, 4 * ceil(numel / 64), 0); *total
  * is their sum (4.127 bits per weight: infivelines.com "QLoRA", the 0.127 bits/weight
  * figure for scales per 64 quantized again per 256).  Either output may be NULL.
  * Host only.  Returns QLORA_ERR_INVALID_ARG for rows or cols < 1,
- * QLORA_ERR_UNSUPPORTED for another blocksize or dq_block.
+ * QLORA_ERR_UNSUPPORTED for another blocksize, or a dq_block other than 256 and 0.
  */
 int nf4_storage_bytes(int64_t rows, int64_t cols, int32_t blocksize, int32_t dq_block,
                       uint64_t sizes[4], uint64_t* total);
@@ -99,7 +107,8 @@ int nf4_quantize_workspace_bytes(int64_t numel, uint64_t* out);
  * Per block: absmax a, x = w / a (IEEE fp32 division; a = 0 gives x = 0), code = index of
  * the nearest of the 16 levels (ties to the lower index).  Then mean = fp64 pairwise sum of
  * all a / count (rounded to fp32); per group step = max |a - mean| / 127 and
- * scale_code = clamp(rint((a - mean) / step), -127, 127) (0 when step = 0).
+ * scale_code = clamp(rint((a - mean) / step), -127, 127) (0 when step = 0).  With
+ * out->dq_block = NF4_NO_DQ the block absmax values are stored as they are (no second level).
  * `workspace` (device, >= nf4_quantize_workspace_bytes) is scratch that the call
  * overwrites.  W, out buffers and workspace must be 16-byte aligned.  Any numel >= 1.
  */

@@ -58,7 +58,9 @@ def lib() -> ctypes.CDLL:
         L.nf4o_lora_dadb.restype = None
         L.nf4o_bf16_rne_double.argtypes = [f64]
         L.nf4o_bf16_rne_double.restype = ctypes.c_uint16
-        L.nf4o_merge.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i64, i64, i64, f64, vp]
+        L.nf4o_merge.argtypes = [vp, vp, vp, i64, i64, i64, f64, vp]
+        L.nf4o_dequantize_nodq.argtypes = [vp, vp, i64, vp]
+        L.nf4o_dequantize_nodq.restype = None
         L.nf4o_merge.restype = None
         L.nf4o_int4_error.argtypes = [vp, i64, vp]
         L.nf4o_int4_error.restype = None
@@ -220,18 +222,25 @@ def bf16_rne_double(x) -> np.ndarray:
     return np.array([f(float(v)) for v in x], np.uint16)
 
 
-def merge(q: dict, A, B, scale) -> np.ndarray:
+def dequantize_nodq(q: dict) -> np.ndarray:
+    """bf16 bits of the variant without double quantization: L[c] times the block's fp32
+    absmax, one rounding (reading R14).  q is an oracle quantize() dict."""
+    n = int(q["numel"])
+    out = np.zeros(n, np.uint16)
+    lib().nf4o_dequantize_nodq(_p(np.ascontiguousarray(q["codes"], np.uint8)),
+                               _p(np.ascontiguousarray(q["absmax"], np.float32)), n, _p(out))
+    return out
+
+
+def merge(Wd, A, B, scale) -> np.ndarray:
     """bf16 bits [N, K] of bf16(W' + scale B A) from the fp64 bracket (reading R11).
-    q is an oracle quantize() dict of an N x K tensor, A [r, K] and B [N, r] bf16 bits."""
-    A, B = _u16(A), _u16(B)
+    Wd: the dequantized base as bf16 bits [N, K]; A [r, K] and B [N, r] bf16 bits."""
+    Wd, A, B = _u16(Wd), _u16(A), _u16(B)
     r, K = A.shape
     N = B.shape[0]
-    assert int(q["numel"]) == N * K
+    Wd = Wd.reshape(N, K)
     out = np.zeros((N, K), np.uint16)
-    lib().nf4o_merge(_p(np.ascontiguousarray(q["codes"], np.uint8)),
-                     _p(np.ascontiguousarray(q["qscale"], np.int8)),
-                     _p(np.ascontiguousarray(q["steps"], np.float32)), float(q["mean"]),
-                     _p(A), _p(B), N, K, r, float(scale), _p(out))
+    lib().nf4o_merge(_p(Wd), _p(A), _p(B), N, K, r, float(scale), _p(out))
     return out
 
 

@@ -228,6 +228,19 @@ void nf4o_dequantize(const uint8_t* codes, const int8_t* qscale, const float* st
   }
 }
 
+/* Dequantize the variant without double quantization (R14): the block scale is the stored
+ * fp32 absmax itself. */
+void nf4o_dequantize_nodq(const uint8_t* codes, const float* absmax, int64_t numel,
+                          uint16_t* out) {
+  float L[16], T[15];
+  nf4o_levels(L, T);
+  for (int64_t e = 0; e < numel; ++e) {
+    uint8_t byte = codes[e / 2];
+    int c = (e & 1) ? (byte & 0xF) : (byte >> 4);
+    out[e] = nf4o_bf16_rne(L[c] * absmax[e / NF4O_BLOCK]);
+  }
+}
+
 /* ------------------------------------------------------------------ LoRA linear (R8) */
 /* Shapes: X [M,K], Wd [N,K] (dequantized bf16), A [r,K], B [N,r], dY [M,N]; all bf16 bits.
  * Row subsets let the tests check sampled rows of full-size problems one by one. */
@@ -371,19 +384,15 @@ uint16_t nf4o_bf16_rne_double(double x) {
   return (uint16_t)(u >> 16);
 }
 
-void nf4o_merge(const uint8_t* codes, const int8_t* qscale, const float* steps, float mean,
-                const uint16_t* A, const uint16_t* B, int64_t N, int64_t K, int64_t r,
-                double scale, uint16_t* out) {
-  float L[16], T[15];
-  nf4o_levels(L, T);
+/* Wd: the dequantized base (bf16 bits [N][K], from nf4o_dequantize or its no-double-quant
+ * variant). */
+void nf4o_merge(const uint16_t* Wd, const uint16_t* A, const uint16_t* B, int64_t N, int64_t K,
+                int64_t r, double scale, uint16_t* out) {
 #pragma omp parallel for schedule(static)
   for (int64_t n = 0; n < N; ++n)
     for (int64_t k = 0; k < K; ++k) {
-      int64_t e = n * K + k, b = e / NF4O_BLOCK;
-      float ahat = fmaf((float)qscale[b], steps[b / NF4O_GROUP], mean);
-      uint8_t byte = codes[e / 2];
-      int c = (e & 1) ? (byte & 0xF) : (byte >> 4);
-      double wd = bf16_to_double(nf4o_bf16_rne(L[c] * ahat));
+      int64_t e = n * K + k;
+      double wd = bf16_to_double(Wd[e]);
       double delta = 0.0;
       for (int64_t j = 0; j < r; ++j) delta += bf16_to_double(B[n * r + j]) * bf16_to_double(A[j * K + k]);
       out[e] = nf4o_bf16_rne_double(wd + scale * delta);

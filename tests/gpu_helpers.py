@@ -42,13 +42,17 @@ def upload_oracle_tensor(q: dict, rows: int, cols: int) -> qn.NF4Tensor:
 class Problem:
     """A LinearProblem with its oracle quantization and device copies."""
 
-    def __init__(self, p: wl.LinearProblem, quantize_on_gpu: bool = True):
+    def __init__(self, p: wl.LinearProblem, quantize_on_gpu: bool = True,
+                 double_quant: bool = True):
         self.p = p
         W = p.W()
         self.qo = oracle.quantize(W)
-        self.Wd = oracle.dequantize(self.qo).reshape(p.N, p.K)
-        if quantize_on_gpu:
-            self.qd = qn.nf4_quantize(torch.from_numpy(W).cuda())
+        if double_quant:
+            self.Wd = oracle.dequantize(self.qo).reshape(p.N, p.K)
+        else:
+            self.Wd = oracle.dequantize_nodq(self.qo).reshape(p.N, p.K)
+        if quantize_on_gpu or not double_quant:
+            self.qd = qn.nf4_quantize(torch.from_numpy(W).cuda(), double_quant=double_quant)
         else:
             self.qd = upload_oracle_tensor(self.qo, p.N, p.K)
         self.X, self.A, self.B, self.dY = p.X(), p.A(), p.B(), p.dY()

@@ -281,7 +281,7 @@ def test_merge_matches_oracle(cfg):
     A, B = p.A(), p.B()
     m16, m32 = qn.nf4_merge_lora(qd, bf16_dev(A), bf16_dev(B), p.scale, f32=True)
     got = bits_host(m16)
-    want = oracle.merge(qo, A, B, p.scale)
+    want = oracle.merge(oracle.dequantize(qo).reshape(p.N, p.K), A, B, p.scale)
     d = _ulp_diff(got, want)
     assert (d > 0).mean() <= 1e-3
     gv = wl.bf16_bits_to_f32(got).astype(np.float64)
@@ -374,3 +374,59 @@ def test_multi_adapter_decode(M, r):
 def test_multi_adapter_decode_full_size():
     got, ref = _multi_case(28672, 8192, 4, 64, 3, seed=52)
     assert rel_fro(got, ref) <= TOL
+
+
+# ------------------------------------------------------------------ no double quantization
+@pytest.mark.parametrize("n", [1, 63, 65, 1001, 64 * 256 + 1, 1 << 20])
+def test_quantize_nodq_bit_exact(n):
+    W = wl.weight((n,), seed=80 + n % 7, sigma=0.02)
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda(), double_quant=False)
+    o = oracle.quantize(W)
+    assert q.dq_block == 0 and q.scale_codes.numel() == 0 and q.scale_mean.numel() == 0
+    assert np.array_equal(q.codes.cpu().numpy(), o["codes"])
+    assert np.array_equal(q.scale_steps.cpu().numpy().view(np.uint32), o["absmax"].view(np.uint32))
+    got = bits_host(qn.nf4_dequantize(q)).reshape(-1)
+    assert np.array_equal(got, oracle.dequantize_nodq(o))
+
+
+def test_dequantize_nodq_decode_tensor_bit_exact():
+    W = wl.config4(1).W()
+    o = oracle.quantize(W)
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda(), double_quant=False)
+    assert np.array_equal(bits_host(qn.nf4_dequantize(q)).reshape(-1), oracle.dequantize_nodq(o))
+
+
+@pytest.mark.parametrize("name,M,N,K,r,alpha", [s for s in SMALL if s[0] in
+                                                ("cfg1", "ragged", "rank72", "tokens5",
+                                                 "multi_tile", "rank12")])
+def test_fwd_bwd_nodq(name, M, N, K, r, alpha):
+    p = wl.LinearProblem(name, M, N, K, r, alpha, 0.02, 0.001, config=90 + len(name))
+    pb = Problem(p, double_quant=False)
+    Y, U = _check_fwd(pb)
+    _check_bwd(pb, U)
+
+
+def test_config2_nodq():
+    pb = Problem(wl.config2(), double_quant=False)
+    rows = _sample_rows(pb.p.M)
+    Y, U = _check_fwd(pb, rows)
+    _check_bwd(pb, U, rows)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_config4_decode_nodq(M):
+    pb = Problem(wl.config4(M), double_quant=False)
+    _check_fwd(pb)
+
+
+def test_merge_and_noalloc_nodq():
+    p = wl.config1()
+    W = p.W()
+    o = oracle.quantize(W)
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda(), double_quant=False)
+    m16, _ = qn.nf4_merge_lora(q, bf16_dev(p.A()), bf16_dev(p.B()), p.scale)
+    want = oracle.merge(oracle.dequantize_nodq(o).reshape(p.N, p.K), p.A(), p.B(), p.scale)
+    assert (_ulp_diff(bits_host(m16), want) > 0).mean() <= 1e-3
+    q2 = qn.nf4_quantize_noalloc(torch.from_numpy(W).cuda(),
+                                 qn.NF4Tensor.empty(p.N, p.K, "cuda", double_quant=False))
+    assert torch.equal(q2.codes, q.codes) and torch.equal(q2.scale_steps, q.scale_steps)

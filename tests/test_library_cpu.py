@@ -56,6 +56,10 @@ def test_storage_bytes_formula(lib):
     # 4.127 bits per weight on a large tensor (infivelines.com "QLoRA": ~0.127 bits/weight)
     _, total = qn.nf4_storage_bytes(4096, 11008)
     assert abs(total * 8 / (4096 * 11008) - 4.127) < 0.001
+    # without double quantization: fp32 absmax per 64 weights, 0.5 bits/weight of scales
+    sizes, total = qn.nf4_storage_bytes(4096, 11008, 0)
+    n = 4096 * 11008
+    assert sizes == [n // 2, 0, 4 * (n // 64), 0] and total * 8 / n == 4.5
 
 
 def test_host_validation_without_device(lib):

@@ -429,7 +429,7 @@ def test_merge_with_zero_adapter_is_the_dequantization():
     q = oracle.quantize(W)
     A = wl.bf16_normal((8, 128), seed=22, sigma=0.01)
     B = np.zeros((64, 8), np.uint16)
-    got = oracle.merge(q, A, B, 2.0)
+    got = oracle.merge(oracle.dequantize(q).reshape(64, 128), A, B, 2.0)
     assert np.array_equal(got.ravel(), oracle.dequantize(q))
 
 
@@ -447,7 +447,7 @@ def test_merge_brute_force_small():
         for k in range(K):
             d = sum(Fraction(float(Bf[n, j])) * Fraction(float(Af[j, k])) for j in range(r))
             want[n, k] = _bf16_nearest_exact(Fraction(float(Wd[n, k])) + Fraction(s) * d)
-    assert np.array_equal(oracle.merge(q, A, B, s), want)
+    assert np.array_equal(oracle.merge(oracle.dequantize(q).reshape(N, K), A, B, s), want)
 
 
 # ---------------------------------------------------------------- NF4 vs INT4 (reading R12)
@@ -492,3 +492,18 @@ def test_nf4_beats_int4_on_normal_weights():
     W = wl.weight((256, 1024), seed=33, sigma=0.02)
     s = oracle.int4_error(W)
     assert s[1] < 0.9 * s[2]
+
+
+# ---------------------------------------------------------------- no double quantization (R14)
+
+def test_dequantize_nodq_is_level_times_true_absmax():
+    """Without the second level the block scale is the stored absmax: every weight
+    dequantizes to bf16(L[c] * absmax) (numpy fp32 product, torch's bf16 rounding)."""
+    W = wl.weight((1, 64 * 40 + 13), seed=91, sigma=0.02).ravel()
+    q = oracle.quantize(W)
+    L, _ = oracle.levels()
+    c = _unpack(q["codes"], W.size)
+    a = np.repeat(q["absmax"], 64)[:W.size]
+    want = wl.to_bf16_bits((L[c] * a).astype(np.float32))
+    assert np.array_equal(oracle.dequantize_nodq(q), want)
+    assert np.array_equal(q["absmax"], np.abs(np.pad(W, (0, (-W.size) % 64))).reshape(-1, 64).max(1))
