@@ -39,7 +39,8 @@ class _NF4Struct(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scale_codes", ctypes.c_void_p),
                 ("scale_steps", ctypes.c_void_p), ("scale_mean", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
-                ("blocksize", ctypes.c_int32), ("dq_block", ctypes.c_int32)]
+                ("blocksize", ctypes.c_int32), ("dq_block", ctypes.c_int32),
+                ("dq_type", ctypes.c_int32)]
 
 
 _lib = None
@@ -118,6 +119,7 @@ class NF4Tensor:
     rows: int
     cols: int
     dq_block: int = NF4_DQ_BLOCK  # NF4_NO_DQ: scale_steps holds the fp32 block absmax
+    dq_type: int = 0              # 1: second-level codes are E4M3 8-bit floats (else int8)
 
     @property
     def numel(self) -> int:
@@ -127,20 +129,22 @@ class NF4Tensor:
         def p(t):
             return _ptr(t) if t is not None and t.numel() > 0 else 0
         return _NF4Struct(p(self.codes), p(self.scale_codes), p(self.scale_steps),
-                          p(self.scale_mean), self.rows, self.cols, NF4_BLOCKSIZE, self.dq_block)
+                          p(self.scale_mean), self.rows, self.cols, NF4_BLOCKSIZE, self.dq_block,
+                          self.dq_type)
 
     def storage_bytes(self) -> int:
         return nf4_storage_bytes(self.rows, self.cols, self.dq_block)[1]
 
     @staticmethod
-    def empty(rows: int, cols: int, device, double_quant: bool = True) -> "NF4Tensor":
+    def empty(rows: int, cols: int, device, double_quant: bool = True,
+              fp8_second_level: bool = False) -> "NF4Tensor":
         dq = NF4_DQ_BLOCK if double_quant else NF4_NO_DQ
         sizes, _ = nf4_storage_bytes(rows, cols, dq)
         return NF4Tensor(torch.empty(sizes[0], dtype=torch.uint8, device=device),
                          torch.empty(sizes[1], dtype=torch.int8, device=device),
                          torch.empty(sizes[2] // 4, dtype=torch.float32, device=device),
                          torch.empty(sizes[3] // 4, dtype=torch.float32, device=device), rows, cols,
-                         dq)
+                         dq, 1 if (fp8_second_level and double_quant) else 0)
 
 
 def nf4_storage_bytes(rows: int, cols: int, dq_block: int = 256) -> tuple[list[int], int]:
@@ -193,12 +197,15 @@ def _req(t: torch.Tensor, dtype, name: str):
 
 
 def nf4_quantize(W: torch.Tensor, out: NF4Tensor | None = None,
-                 workspace: torch.Tensor | None = None, double_quant: bool = True) -> NF4Tensor:
-    """Quantize fp32 weights [rows, cols] (CUDA) to NF4 with double-quantized scales, or with
-    fp32 block absmax scales when double_quant is False (or `out` is of that variant)."""
+                 workspace: torch.Tensor | None = None, double_quant: bool = True,
+                 fp8_second_level: bool = False) -> NF4Tensor:
+    """Quantize fp32 weights [rows, cols] (CUDA) to NF4 with double-quantized scales (int8, or
+    E4M3 with fp8_second_level), or with fp32 block absmax scales when double_quant is False
+    (an `out` tensor brings its own variant)."""
     _req(W, torch.float32, "W")
     rows, cols = (W.shape[0], W.shape[1]) if W.dim() == 2 else (1, W.numel())
-    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, double_quant)
+    q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, double_quant,
+                                                    fp8_second_level)
     nb = nf4_quantize_workspace_bytes(rows * cols)
     ws = workspace if workspace is not None else _workspace(nb, W.device)
     s = q.c_struct()

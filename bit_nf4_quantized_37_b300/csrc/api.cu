@@ -30,7 +30,8 @@ int check_device() {
 int check_tensor(const nf4_tensor* q) {
   if (!q) return QLORA_ERR_INVALID_ARG;
   if (q->rows < 1 || q->cols < 1) return QLORA_ERR_INVALID_ARG;
-  if (q->blocksize != NF4_BLOCKSIZE || (q->dq_block != NF4_DQ_BLOCK && q->dq_block != NF4_NO_DQ))
+  if (q->blocksize != NF4_BLOCKSIZE || (q->dq_block != NF4_DQ_BLOCK && q->dq_block != NF4_NO_DQ) ||
+      (q->dq_type != NF4_DQ_INT8 && q->dq_type != NF4_DQ_FP8))
     return QLORA_ERR_UNSUPPORTED;
   const bool dq = q->dq_block != NF4_NO_DQ;
   if (!q->codes || !q->scale_steps || (dq && (!q->scale_codes || !q->scale_mean)))

@@ -45,7 +45,7 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as
 __global__ void __launch_bounds__(THREADS) nf4_merge_kernel(
     const uint8_t* __restrict__ codes, const int8_t* __restrict__ qs,
     const float* __restrict__ steps, const float* __restrict__ mean,
-    int dq, const uint16_t* __restrict__ A, const uint16_t* __restrict__ B, int64_t N, int64_t K,
+    int dq, int fp8, const uint16_t* __restrict__ A, const uint16_t* __restrict__ B, int64_t N, int64_t K,
     int r, float scale, uint16_t* __restrict__ out16, float* __restrict__ out32) {
   extern __shared__ float msm[];
   float* sA = msm;               // [r][COLS]
@@ -110,8 +110,10 @@ __global__ void __launch_bounds__(THREADS) nf4_merge_kernel(
     const int64_t e = n * K + kk;
     const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(codes + e / 2));
     const int64_t blk = e / 64;
-    const float a_hat = dq ? __fmaf_rn(static_cast<float>(__ldg(qs + blk)), __ldg(steps + (blk >> 8)), mu)
-                           : __ldg(steps + blk);
+    const float a_hat =
+        dq ? __fmaf_rn(nf4_second_level(static_cast<uint8_t>(__ldg(qs + blk)), fp8),
+                       __ldg(steps + (blk >> 8)), mu)
+           : __ldg(steps + blk);
     uint32_t wd[4];
     nf4_dequant8(nf4_make_table(a_hat), word, wd);
     uint32_t o16[4];
@@ -222,8 +224,8 @@ int launch_merge(const nf4_tensor& q, const uint16_t* A, const uint16_t* B, int 
                   (unsigned)((q.rows + merge::ROWS - 1) / merge::ROWS));
   ProfileScope ps("nf4_merge", stream);
   merge::nf4_merge_kernel<<<grid, merge::THREADS, smem, stream>>>(
-      q.codes, q.scale_codes, q.scale_steps, q.scale_mean, q.dq_block != 0 ? 1 : 0, A, B, q.rows,
-      q.cols, r, scale, out16, out32);
+      q.codes, q.scale_codes, q.scale_steps, q.scale_mean, q.dq_block != 0 ? 1 : 0,
+      q.dq_type == NF4_DQ_FP8 ? 1 : 0, A, B, q.rows, q.cols, r, scale, out16, out32);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 

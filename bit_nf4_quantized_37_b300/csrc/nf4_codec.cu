@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict_
                                                         int64_t nblocks, int64_t ngroups,
                                                         const double* __restrict__ part,
                                                         int nparts, float* __restrict__ mean,
-                                                        int8_t* __restrict__ scale_codes,
+                                                        int fp8, int8_t* __restrict__ scale_codes,
                                                         float* __restrict__ steps) {
   __shared__ float s_mu;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -323,17 +323,24 @@ __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict_
   for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(d[i]));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  const float step = __fdiv_rn(m, 127.0f);
+  // int8: 127 steps each side; fp8: the E4M3 range, 448 at the largest |a - mean|
+  const float step = __fdiv_rn(m, fp8 ? 448.0f : 127.0f);
   if (lane == 0) steps[g] = step;
   uint32_t q[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    int v = 0;
-    if (step > 0.0f) {
-      v = __float2int_rn(__fdiv_rn(d[i], step));  // round half to even
-      v = v > 127 ? 127 : (v < -127 ? -127 : v);
+    if (fp8) {  // nearest E4M3 value, ties to even, saturating at 448 (code 0 when step = 0)
+      q[i] = step > 0.0f
+                 ? static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(d[i], step), __NV_SATFINITE, __NV_E4M3))
+                 : 0u;
+    } else {
+      int v = 0;
+      if (step > 0.0f) {
+        v = __float2int_rn(__fdiv_rn(d[i], step));  // round half to even
+        v = v > 127 ? 127 : (v < -127 ? -127 : v);
+      }
+      q[i] = static_cast<uint32_t>(v) & 0xFFu;
     }
-    q[i] = static_cast<uint32_t>(v) & 0xFFu;
   }
   if (whole) {
     *reinterpret_cast<uint2*>(scale_codes + b0) =
@@ -354,7 +361,7 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
                                                           const int8_t* __restrict__ scale_codes,
                                                           const float* __restrict__ steps,
                                                           const float* __restrict__ mean,
-                                                          int64_t numel, int dq,
+                                                          int64_t numel, int dq, int fp8,
                                                           uint16_t* __restrict__ out) {
   const float mu = dq ? __ldg(mean) : 0.0f;
   const int64_t npieces = (numel + 15) / 16;
@@ -362,8 +369,10 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
        p += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e0 = p * 16;
     const int64_t b = e0 / kBlock;
-    const float scale = dq ? __fmaf_rn((float)__ldg(scale_codes + b), __ldg(steps + b / kGroup), mu)
-                           : __ldg(steps + b);
+    const float scale =
+        dq ? __fmaf_rn(nf4_second_level(static_cast<uint8_t>(__ldg(scale_codes + b)), fp8),
+                       __ldg(steps + b / kGroup), mu)
+           : __ldg(steps + b);
     const Nf4ByteTable tab = nf4_make_table(scale);
     uint32_t q[2];
     if (e0 + 16 <= numel) {
@@ -455,7 +464,7 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     cfg.blockDim = dim3(256);
     if (cudaLaunchKernelEx(&cfg, nf4_double_quant, static_cast<const float*>(absmax), nb, ng,
                            static_cast<const double*>(part), nparts, q.scale_mean,
-                           q.scale_codes, q.scale_steps) != cudaSuccess)
+                           q.dq_type == NF4_DQ_FP8 ? 1 : 0, q.scale_codes, q.scale_steps) != cudaSuccess)
       return QLORA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
@@ -471,7 +480,7 @@ int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, cudaStr
   nf4_dequant_kernel<<<(unsigned)blocks, threads, 0, stream>>>(q.codes, q.scale_codes,
                                                                q.scale_steps, q.scale_mean,
                                                                numel, q.dq_block != 0 ? 1 : 0,
-                                                               out);
+                                                               q.dq_type == NF4_DQ_FP8 ? 1 : 0, out);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 

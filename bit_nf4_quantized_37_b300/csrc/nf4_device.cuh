@@ -5,6 +5,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace qlora {
@@ -35,6 +37,16 @@ __device__ __forceinline__ uint32_t nf4_code(float x) {
                       : (b2 ? (b1 ? T[6] : T[4]) : (b1 ? T[2] : T[0]));
   const bool b0 = x > t0;
   return (b3 ? 8u : 0u) | (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u);
+}
+
+// Value of a second-level scale code (the low byte of `byte`): an int8 step count, or with
+// fp8 an E4M3 number (widened exactly through half precision).
+__device__ __forceinline__ float nf4_second_level(uint32_t byte, int fp8) {
+  if (fp8) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte & 0xFFu), __NV_E4M3);
+    return __half2float(__half(h));
+  }
+  return static_cast<float>(static_cast<int8_t>(byte & 0xFFu));
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

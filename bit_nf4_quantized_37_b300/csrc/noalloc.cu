@@ -62,7 +62,8 @@ extern "C" int nf4_quantize_noalloc(const float* W, const nf4_tensor* out, void*
   if (!out || !W) return QLORA_ERR_INVALID_ARG;
   if (out->rows < 1 || out->cols < 1) return QLORA_ERR_INVALID_ARG;
   if (out->blocksize != NF4_BLOCKSIZE ||
-      (out->dq_block != NF4_DQ_BLOCK && out->dq_block != NF4_NO_DQ))
+      (out->dq_block != NF4_DQ_BLOCK && out->dq_block != NF4_NO_DQ) ||
+      (out->dq_type != NF4_DQ_INT8 && out->dq_type != NF4_DQ_FP8))
     return QLORA_ERR_UNSUPPORTED;
   const bool dq = out->dq_block != NF4_NO_DQ;
   if (!out->codes || !out->scale_steps || (dq && (!out->scale_codes || !out->scale_mean)))

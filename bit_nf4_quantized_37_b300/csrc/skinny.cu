@@ -132,6 +132,7 @@ struct Params {
   const float* steps;  // group steps, or without double quantization the block absmax
   const float* mean;
   int dq;              // 1: double-quantized scales
+  int fp8;             // second-level codes are E4M3 (else int8)
   int qs_words;        // scale codes of a row's stage are one aligned 32-bit word
   float* part;         // [CTAs][2][16][128] fp32 pieces of split row blocks
   int* tickets;        // [row blocks] stages summed so far
@@ -314,10 +315,11 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
         float v = 0.f;
         if (n < p.N && kb < p.KB) {
           if (word_path) {
-            v = __fmaf_rn(static_cast<float>(static_cast<int8_t>((w >> (8 * b)) & 0xFFu)), st, mu);
+            v = __fmaf_rn(nf4_second_level(w >> (8 * b), p.fp8), st, mu);
           } else {
             const int64_t idx = n * p.KB + kb;
-            v = p.dq ? __fmaf_rn(static_cast<float>(__ldg(p.qs + idx)), __ldg(p.steps + (idx >> 8)), mu)
+            v = p.dq ? __fmaf_rn(nf4_second_level(static_cast<uint8_t>(__ldg(p.qs + idx)), p.fp8),
+                                 __ldg(p.steps + (idx >> 8)), mu)
                      : __ldg(p.steps + idx);
           }
         }
@@ -786,6 +788,7 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
   p.steps = a.q.scale_steps;
   p.mean = a.q.scale_mean;
   p.dq = a.q.dq_block != 0 ? 1 : 0;
+  p.fp8 = a.q.dq_type == NF4_DQ_FP8 ? 1 : 0;
   p.qs_words = (p.dq && p.KB % 4 == 0 && reinterpret_cast<uintptr_t>(a.q.scale_codes) % 4 == 0) ? 1 : 0;
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.tickets = reinterpret_cast<int*>(ws + L.tickets);

@@ -74,13 +74,14 @@ struct Params {
   const float* steps;
   const float* mean;
   int dq;         // 1: double-quantized scales; 0: steps holds the fp32 absmax per block
+  int fp8;        // second-level codes are E4M3 (else int8)
 };
 
 // One thread's share of an NF4 stage: 64 codes (32 bytes) and the block's scale code/step.
 struct Slice {
   uint4 c0, c1;
   float step;
-  int q;
+  float q;  // value of the block's second-level code
   bool valid;
 };
 
@@ -92,10 +93,10 @@ __device__ __forceinline__ void load_slice(Slice& s, const Params& p, int64_t ro
     s.c1 = __ldg(src + 1);
     const int64_t b = row * (p.Kw / 64) + kcol / 64;
     if (p.dq) {
-      s.q = __ldg(p.qs + b);
+      s.q = nf4_second_level(static_cast<uint8_t>(__ldg(p.qs + b)), p.fp8);
       s.step = __ldg(p.steps + (b >> 8));
     } else {  // fmaf(1, absmax, 0) = absmax in the shared scale arithmetic
-      s.q = 1;
+      s.q = 1.0f;
       s.step = __ldg(p.steps + b);
     }
   }
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Slice cur = (kc & 1) ? pf1 : pf0;  // loaded two stages ago
         uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
         if (cur.valid) {
-          const Nf4ByteTable tab = nf4_make_table(__fmaf_rn((float)cur.q, cur.step, mu));
+          const Nf4ByteTable tab = nf4_make_table(__fmaf_rn(cur.q, cur.step, mu));
           const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
                                      cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
 #pragma unroll
@@ -543,7 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint4 rv[8];
     auto dequant = [&](const Slice& cur) {
       if (cur.valid) {
-        const Nf4ByteTable tab = nf4_make_table(__fmaf_rn((float)cur.q, cur.step, mu));
+        const Nf4ByteTable tab = nf4_make_table(__fmaf_rn(cur.q, cur.step, mu));
         const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
                                    cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
 #pragma unroll
@@ -680,6 +681,7 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   p.steps = a.q.scale_steps;
   p.mean = a.q.scale_mean;
   p.dq = a.q.dq_block != 0 ? 1 : 0;
+  p.fp8 = a.q.dq_type == NF4_DQ_FP8 ? 1 : 0;
   p.n_lora = static_cast<int>(rp / 64);
   p.lora_last_k16 = static_cast<int>((a.r - 64 * (p.n_lora - 1) + 15) / 16);
   if (kMode == 0) {

@@ -52,6 +52,8 @@ extern "C" {
 #define NF4_BLOCKSIZE 64  /* weights per first-level block (one absmax scale each)   */
 #define NF4_DQ_BLOCK 256  /* first-level scales per second-level (double-quant) group */
 #define NF4_NO_DQ 0       /* dq_block value of the variant without double quantization */
+#define NF4_DQ_INT8 0     /* dq_type: second-level codes are int8 steps around the mean  */
+#define NF4_DQ_FP8 1      /* dq_type: second-level codes are 8-bit floats (E4M3)          */
 
 /*
  * A blockwise NF4 tensor with double-quantized scales: views into caller-owned device
@@ -70,8 +72,13 @@ extern "C" {
  * and addaly.com "What each setting is doing" present double quantization as a separate,
  * optional saving; infivelines.com "QLoRA": without it the block scales cost 32/64 = 0.5 bits
  * per weight): scale_steps holds the fp32 absmax of every block [ceil(numel / 64)], the block
- * scale is that absmax, and scale_codes and scale_mean are unused (may be NULL).  Every call
- * taking an nf4_tensor accepts either variant.
+ * scale is that absmax, and scale_codes and scale_mean are unused (may be NULL).
+ * Variant with an 8-bit-float second level (dq_type = NF4_DQ_FP8; the QLoRA paper, which the
+ * pages cite, quantizes the constants to 8-bit floats in blocks of 256): scale_codes holds
+ * E4M3 bytes (sign, 4 exponent bits of bias 7, 3 mantissa bits, largest finite 448), the
+ * group step is max |a - mean| / 448 and the block scale is
+ * fmaf(e4m3_value(scale_codes[b]), scale_steps[b / 256], scale_mean[0]).
+ * Every call taking an nf4_tensor accepts each variant.
  */
 typedef struct nf4_tensor {
   uint8_t* codes;
@@ -81,7 +88,8 @@ typedef struct nf4_tensor {
   int64_t rows; /* N */
   int64_t cols; /* K */
   int32_t blocksize; /* must be NF4_BLOCKSIZE */
-  int32_t dq_block;  /* must be NF4_DQ_BLOCK  */
+  int32_t dq_block;  /* NF4_DQ_BLOCK, or NF4_NO_DQ */
+  int32_t dq_type;   /* NF4_DQ_INT8 or NF4_DQ_FP8 (with dq_block = NF4_DQ_BLOCK) */
 } nf4_tensor;
 
 /*
@@ -108,7 +116,9 @@ int nf4_quantize_workspace_bytes(int64_t numel, uint64_t* out);
  * the nearest of the 16 levels (ties to the lower index).  Then mean = fp64 pairwise sum of
  * all a / count (rounded to fp32); per group step = max |a - mean| / 127 and
  * scale_code = clamp(rint((a - mean) / step), -127, 127) (0 when step = 0).  With
- * out->dq_block = NF4_NO_DQ the block absmax values are stored as they are (no second level).
+ * out->dq_block = NF4_NO_DQ the block absmax values are stored as they are (no second level);
+ * with out->dq_type = NF4_DQ_FP8, step = max |a - mean| / 448 and the code is
+ * (a - mean) / step rounded to the nearest E4M3 value (ties to even, saturating at 448).
  * `workspace` (device, >= nf4_quantize_workspace_bytes) is scratch that the call
  * overwrites.  W, out buffers and workspace must be 16-byte aligned.  Any numel >= 1.
  */

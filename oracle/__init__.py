@@ -42,9 +42,13 @@ def lib() -> ctypes.CDLL:
         L.nf4o_absmax_mean.restype = ctypes.c_float
         L.nf4o_block_absmax.argtypes = [vp, i64, vp]
         L.nf4o_block_absmax.restype = None
-        L.nf4o_quantize.argtypes = [vp, i64, vp, vp, vp, vp, vp]
+        L.nf4o_quantize.argtypes = [vp, i64, vp, vp, vp, vp, vp, ctypes.c_int]
         L.nf4o_quantize.restype = None
-        L.nf4o_dequantize.argtypes = [vp, vp, vp, ctypes.c_float, i64, vp]
+        L.nf4o_dequantize.argtypes = [vp, vp, vp, ctypes.c_float, i64, vp, ctypes.c_int]
+        L.nf4o_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.nf4o_e4m3_decode.restype = f64
+        L.nf4o_e4m3_encode.argtypes = [ctypes.c_float]
+        L.nf4o_e4m3_encode.restype = ctypes.c_uint8
         L.nf4o_dequantize.restype = None
         L.nf4o_lora_u_rows.argtypes = [vp, vp, i64, i64, vp, i64, vp]
         L.nf4o_lora_u_rows.restype = None
@@ -120,9 +124,10 @@ def absmax_mean(absmax: np.ndarray) -> np.float32:
     return np.float32(lib().nf4o_absmax_mean(_p(a), a.size))
 
 
-def quantize(W: np.ndarray) -> dict:
+def quantize(W: np.ndarray, fp8: bool = False) -> dict:
     """NF4 + double quantization of a fp32 tensor (flat order).  Returns a dict with
-    codes (uint8), qscale (int8), steps (fp32), mean (fp32 scalar), absmax (fp32)."""
+    codes (uint8), qscale (int8; E4M3 bytes when fp8, reading R15), steps (fp32), mean (fp32
+    scalar), absmax (fp32)."""
     W = np.ascontiguousarray(W, np.float32).ravel()
     n = W.size
     nb, ng = num_blocks(n), num_groups(n)
@@ -131,9 +136,10 @@ def quantize(W: np.ndarray) -> dict:
     steps = np.zeros(ng, np.float32)
     mean = np.zeros(1, np.float32)
     absmax = np.zeros(nb, np.float32)
-    lib().nf4o_quantize(_p(W), n, _p(codes), _p(qscale), _p(steps), _p(mean), _p(absmax))
+    lib().nf4o_quantize(_p(W), n, _p(codes), _p(qscale), _p(steps), _p(mean), _p(absmax),
+                        1 if fp8 else 0)
     return {"codes": codes, "qscale": qscale, "steps": steps, "mean": mean[0],
-            "absmax": absmax, "numel": n}
+            "absmax": absmax, "numel": n, "fp8": bool(fp8)}
 
 
 def dequantize(q: dict) -> np.ndarray:
@@ -143,8 +149,19 @@ def dequantize(q: dict) -> np.ndarray:
     codes = np.ascontiguousarray(q["codes"], np.uint8)
     qscale = np.ascontiguousarray(q["qscale"], np.int8)
     steps = np.ascontiguousarray(q["steps"], np.float32)
-    lib().nf4o_dequantize(_p(codes), _p(qscale), _p(steps), float(q["mean"]), n, _p(out))
+    lib().nf4o_dequantize(_p(codes), _p(qscale), _p(steps), float(q["mean"]), n, _p(out),
+                          1 if q.get("fp8") else 0)
     return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    f = lib().nf4o_e4m3_decode
+    return np.array([f(int(c) & 0xFF) for c in np.ravel(codes)], np.float64)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    f = lib().nf4o_e4m3_encode
+    return np.array([f(float(v)) for v in np.ravel(np.asarray(x, np.float32))], np.uint8)
 
 
 def _rows(rows, M):

@@ -158,14 +158,44 @@ void nf4o_block_absmax(const float* W, int64_t numel, float* absmax) {
   }
 }
 
+/* ------------------------------------------------------------------ E4M3 (R15) */
+/* The OCP 8-bit float E4M3: sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent
+ * field 0 holds the subnormals m 2^-9; no infinities, S.1111.111 is NaN, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448. */
+double nf4o_e4m3_decode(uint8_t v) {
+  int e = (v >> 3) & 0xF, m = v & 7;
+  if (e == 15 && m == 7) return NAN;
+  double mag = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+  return (v & 0x80) ? -mag : mag;
+}
+
+/* Nearest E4M3 value to x by exhaustive search over the 127 finite magnitudes, ties to the
+ * even code; magnitudes past 448 saturate to 448 (the "satfinite" rule). */
+uint8_t nf4o_e4m3_encode(float x) {
+  double ax = fabs((double)x);
+  int best = 0;
+  double bd = ax;  /* distance to code 0 (+0) */
+  for (int c = 1; c <= 0x7E; ++c) {
+    double d = fabs(nf4o_e4m3_decode((uint8_t)c) - ax);
+    if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
+      bd = d;
+      best = c;
+    }
+  }
+  if (ax > 448.0) best = 0x7E;
+  return (uint8_t)(best | (signbit(x) ? 0x80 : 0));
+}
+
 /* Full NF4 + double quantization of a flat fp32 tensor.
  *   codes  [ceil(numel/2)]  packed 4-bit codes (R4)
  *   qscale [nblocks]        int8 second-level codes of the block absmax (R5)
  *   steps  [ngroups]        fp32 second-level step per group of 256 blocks
  *   mean   [1]              fp32 per-tensor mean of the absmax values (R6)
- *   absmax_out [nblocks]    optional: the true fp32 block absmax values */
+ *   absmax_out [nblocks]    optional: the true fp32 block absmax values
+ * fp8 != 0: the second level uses E4M3 codes (R15): step = max |a - mu| / 448 and
+ * code = nearest E4M3 value of (a - mu) / step, ties to even, saturating at 448. */
 void nf4o_quantize(const float* W, int64_t numel, uint8_t* codes, int8_t* qscale,
-                   float* steps, float* mean, float* absmax_out) {
+                   float* steps, float* mean, float* absmax_out, int fp8) {
   float L[16], T[15];
   nf4o_levels(L, T);
   int64_t nb = nf4o_num_blocks(numel), ng = nf4o_num_groups(numel);
@@ -190,9 +220,13 @@ void nf4o_quantize(const float* W, int64_t numel, uint8_t* codes, int8_t* qscale
       float d = fabsf(a[b] - mu);
       if (d > s2) s2 = d;
     }
-    float step = s2 / 127.0f;
+    float step = s2 / (fp8 ? 448.0f : 127.0f);
     steps[g] = step;
     for (int64_t b = b0; b < b1; ++b) {
+      if (fp8) {
+        qscale[b] = (int8_t)(step > 0.0f ? nf4o_e4m3_encode((a[b] - mu) / step) : 0);
+        continue;
+      }
       int q = 0;
       if (step > 0.0f) {
         float t = (a[b] - mu) / step;
@@ -215,12 +249,13 @@ float nf4o_block_scale(const int8_t* qscale, const float* steps, float mean, int
 
 /* Dequantize to bf16 (raw bits), R7. */
 void nf4o_dequantize(const uint8_t* codes, const int8_t* qscale, const float* steps,
-                     float mean, int64_t numel, uint16_t* out) {
+                     float mean, int64_t numel, uint16_t* out, int fp8) {
   float L[16], T[15];
   nf4o_levels(L, T);
   for (int64_t e = 0; e < numel; ++e) {
     int64_t b = e / NF4O_BLOCK;
-    float ahat = fmaf((float)qscale[b], steps[b / NF4O_GROUP], mean);
+    float qv = fp8 ? (float)nf4o_e4m3_decode((uint8_t)qscale[b]) : (float)qscale[b];
+    float ahat = fmaf(qv, steps[b / NF4O_GROUP], mean);
     uint8_t byte = codes[e / 2];
     int c = (e & 1) ? (byte & 0xF) : (byte >> 4);
     float p = L[c] * ahat;

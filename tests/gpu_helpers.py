@@ -43,16 +43,17 @@ class Problem:
     """A LinearProblem with its oracle quantization and device copies."""
 
     def __init__(self, p: wl.LinearProblem, quantize_on_gpu: bool = True,
-                 double_quant: bool = True):
+                 double_quant: bool = True, fp8_second_level: bool = False):
         self.p = p
         W = p.W()
-        self.qo = oracle.quantize(W)
+        self.qo = oracle.quantize(W, fp8=fp8_second_level)
         if double_quant:
             self.Wd = oracle.dequantize(self.qo).reshape(p.N, p.K)
         else:
             self.Wd = oracle.dequantize_nodq(self.qo).reshape(p.N, p.K)
-        if quantize_on_gpu or not double_quant:
-            self.qd = qn.nf4_quantize(torch.from_numpy(W).cuda(), double_quant=double_quant)
+        if quantize_on_gpu or not double_quant or fp8_second_level:
+            self.qd = qn.nf4_quantize(torch.from_numpy(W).cuda(), double_quant=double_quant,
+                                      fp8_second_level=fp8_second_level)
         else:
             self.qd = upload_oracle_tensor(self.qo, p.N, p.K)
         self.X, self.A, self.B, self.dY = p.X(), p.A(), p.B(), p.dY()

@@ -430,3 +430,47 @@ def test_merge_and_noalloc_nodq():
     q2 = qn.nf4_quantize_noalloc(torch.from_numpy(W).cuda(),
                                  qn.NF4Tensor.empty(p.N, p.K, "cuda", double_quant=False))
     assert torch.equal(q2.codes, q.codes) and torch.equal(q2.scale_steps, q.scale_steps)
+
+
+# ------------------------------------------------------------------ fp8 second level
+@pytest.mark.parametrize("n", [1, 65, 1001, 64 * 256 + 1, 64 * 300 + 37, 1 << 20])
+def test_quantize_fp8_second_level_bit_exact(n):
+    W = wl.weight((n,), seed=85 + n % 5, sigma=0.02)
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda(), fp8_second_level=True)
+    o = oracle.quantize(W, fp8=True)
+    assert q.dq_type == 1
+    assert np.array_equal(q.codes.cpu().numpy(), o["codes"])
+    assert np.array_equal(q.scale_codes.cpu().numpy(), o["qscale"])
+    assert np.array_equal(q.scale_steps.cpu().numpy().view(np.uint32), o["steps"].view(np.uint32))
+    assert q.scale_mean.cpu().numpy()[0].view(np.uint32) == np.float32(o["mean"]).view(np.uint32)
+    assert np.array_equal(bits_host(qn.nf4_dequantize(q)).reshape(-1), oracle.dequantize(o))
+
+
+def test_quantize_fp8_second_level_decode_tensor_bit_exact():
+    W = wl.config4(1).W()
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda(), fp8_second_level=True)
+    o = oracle.quantize(W, fp8=True)
+    assert np.array_equal(q.scale_codes.cpu().numpy(), o["qscale"])
+    assert np.array_equal(bits_host(qn.nf4_dequantize(q)).reshape(-1), oracle.dequantize(o))
+
+
+@pytest.mark.parametrize("name,M,N,K,r,alpha", [s for s in SMALL if s[0] in
+                                                ("cfg1", "ragged", "tokens5", "multi_tile")])
+def test_fwd_bwd_fp8_second_level(name, M, N, K, r, alpha):
+    p = wl.LinearProblem(name, M, N, K, r, alpha, 0.02, 0.001, config=90 + len(name))
+    pb = Problem(p, fp8_second_level=True)
+    Y, U = _check_fwd(pb)
+    _check_bwd(pb, U)
+
+
+def test_config2_fp8_second_level():
+    pb = Problem(wl.config2(), fp8_second_level=True)
+    rows = _sample_rows(pb.p.M)
+    Y, U = _check_fwd(pb, rows)
+    _check_bwd(pb, U, rows)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_config4_decode_fp8_second_level(M):
+    pb = Problem(wl.config4(M), fp8_second_level=True)
+    _check_fwd(pb)

@@ -507,3 +507,38 @@ def test_dequantize_nodq_is_level_times_true_absmax():
     want = wl.to_bf16_bits((L[c] * a).astype(np.float32))
     assert np.array_equal(oracle.dequantize_nodq(q), want)
     assert np.array_equal(q["absmax"], np.abs(np.pad(W, (0, (-W.size) % 64))).reshape(-1, 64).max(1))
+
+
+# ---------------------------------------------------------------- fp8 second level (R15)
+
+def test_e4m3_codec_matches_torch_and_the_format():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_decode(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    fin = ~np.isnan(want)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.array_equal(got[fin], want[fin])
+    assert got[0x7E] == 448.0 and got[0x38] == 1.0 and got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9
+    g = wl.rng(61)
+    x = np.concatenate([g.standard_normal(3000) * 10.0 ** g.integers(-3, 3, 3000),
+                        got[fin][::3] + 1e-9, (got[1:0x7E] + got[2:0x7F]) / 2]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    want_enc = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), want_enc)
+    assert list(oracle.e4m3_encode(np.array([500.0, -1e9, 449.0], np.float32))) == [0x7E, 0xFE, 0x7E]
+
+
+def test_fp8_second_level_error_bound_and_extremes():
+    """Every block scale is recovered within half an E4M3 step of its distance from the
+    mean (relative 2^-4), and the largest |a - mean| of a group maps to +-448."""
+    W = wl.weight((64 * 256 * 3 + 640,), seed=62, sigma=0.02)
+    q = oracle.quantize(W, fp8=True)
+    a = q["absmax"].astype(np.float64)
+    qv = oracle.e4m3_decode(q["qscale"].view(np.uint8))
+    step = np.repeat(q["steps"].astype(np.float64), 256)[:a.size]
+    ahat = qv * step + np.float64(q["mean"])
+    d = np.abs(a - np.float64(q["mean"]))
+    assert np.all(np.abs(ahat - a) <= d * 2.0 ** -4 + step * 2.0 ** -9 + 1e-12)
+    for gidx in range(q["steps"].size):
+        seg = slice(256 * gidx, min(256 * gidx + 256, a.size))
+        assert np.max(np.abs(qv[seg])) == 448.0
