@@ -9,8 +9,8 @@
 // swizzled against bank conflicts) and [32 x r] slice of B in shared memory as fp32, a thread
 // forms the rank-r product of eight consecutive columns of one row with fp32 multiply-adds
 // (each bf16 x bf16 product is exact in fp32), dequantizes the same eight codes exactly as
-// nf4_dequantize does, adds RN(s * delta) in fp32 and rounds once to bf16.  The fp32 copy (the same values) feeds nf4_quantize for the
-// requantized artifact.
+// nf4_dequantize does, adds RN(s * delta) in fp32 and rounds once to bf16.  The fp32 copy
+// (the same values) feeds nf4_quantize for the requantized artifact.
 //
 // Error statistics (aicurriculum.codextroop.com "QLoRA -- Module 12.4", "Design Details That
 // Matter": NF4 places levels at normal quantiles and is often better than naive INT4;
@@ -45,8 +45,8 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as
 __global__ void __launch_bounds__(THREADS) nf4_merge_kernel(
     const uint8_t* __restrict__ codes, const int8_t* __restrict__ qs,
     const float* __restrict__ steps, const float* __restrict__ mean,
-    int dq, int fp8, const uint16_t* __restrict__ A, const uint16_t* __restrict__ B, int64_t N, int64_t K,
-    int r, float scale, uint16_t* __restrict__ out16, float* __restrict__ out32) {
+    int dq, int fp8, const uint16_t* __restrict__ A, const uint16_t* __restrict__ B, int64_t N,
+    int64_t K, int r, float scale, uint16_t* __restrict__ out16, float* __restrict__ out32) {
   extern __shared__ float msm[];
   float* sA = msm;               // [r][COLS]
   float* sB = msm + r * COLS;    // [ROWS][r + 1]

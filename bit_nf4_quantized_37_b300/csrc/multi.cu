@@ -5,7 +5,7 @@
 // event", deployment-subtlety paragraph: serve the 4-bit base plus a separate adapter).
 //   U_t = X_t A_{a(t)}^T              multi_u: split over K in 256-wide chunks, the chunks of
 //                                     a token summed in chunk order by its last CTA
-//   Z_t = s_{a(t)} U_t B_{a(t)}^T     multi_z: fp32, one thread per output column
+//   Z_t = s_{a(t)} U_t B_{a(t)}^T     multi_z: fp32, one thread per (token, output column)
 //   Y_t = bf16( X_t W'^T + Z_t )      the decode GEMV (skinny.cu), adding Z before rounding
 // Tokens whose index is outside [0, n_adapters) get no adapter term.
 #include "common.cuh"
@@ -70,40 +70,38 @@ __global__ void __launch_bounds__(256) multi_u(const uint16_t* __restrict__ X, i
   if (tid == 0) tickets[t] = 0;  // ready for the next launch
 }
 
-__global__ void __launch_bounds__(128) multi_z(const float* __restrict__ U, int M, int64_t N,
+__global__ void __launch_bounds__(128) multi_z(const float* __restrict__ U, int64_t N,
                                                const uint16_t* __restrict__ B_all, int r,
                                                int n_adapters, const int32_t* __restrict__ idx,
                                                const float* __restrict__ scales,
                                                float* __restrict__ Z) {
-  extern __shared__ float su[];  // [M][r]
-  for (int i = threadIdx.x; i < M * r; i += 128) su[i] = U[i];
+  extern __shared__ float su[];  // U row of this CTA's token [r]
+  const int t = blockIdx.y;
+  for (int j = threadIdx.x; j < r; j += 128) su[j] = U[t * r + j];
   __syncthreads();
   const int64_t n = static_cast<int64_t>(blockIdx.x) * 128 + threadIdx.x;
   if (n >= N) return;
-  for (int t = 0; t < M; ++t) {
-    const int a = __ldg(idx + t);
-    float z = 0.0f;
-    if (a >= 0 && a < n_adapters) {
-      const uint16_t* Brow = B_all + (static_cast<int64_t>(a) * N + n) * r;
-      const float* ut = su + t * r;
-      float acc = 0.0f;  // ascending j
-      if ((r & 7) == 0) {
-        for (int j8 = 0; j8 < r; j8 += 8) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(Brow + j8));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const int a = __ldg(idx + t);
+  float z = 0.0f;
+  if (a >= 0 && a < n_adapters) {
+    const uint16_t* Brow = B_all + (static_cast<int64_t>(a) * N + n) * r;
+    float acc = 0.0f;  // ascending j
+    if ((r & 7) == 0) {
+      for (int j8 = 0; j8 < r; j8 += 8) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(Brow + j8));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc = __fmaf_rn(ut[j8 + 2 * e], bf16f(w[e] & 0xFFFFu), acc);
-            acc = __fmaf_rn(ut[j8 + 2 * e + 1], bf16f(w[e] >> 16), acc);
-          }
+        for (int e = 0; e < 4; ++e) {
+          acc = __fmaf_rn(su[j8 + 2 * e], bf16f(w[e] & 0xFFFFu), acc);
+          acc = __fmaf_rn(su[j8 + 2 * e + 1], bf16f(w[e] >> 16), acc);
         }
-      } else {
-        for (int j = 0; j < r; ++j) acc = __fmaf_rn(ut[j], bf16f(__ldg(Brow + j)), acc);
       }
-      z = __fmul_rn(__ldg(scales + a), acc);
+    } else {
+      for (int j = 0; j < r; ++j) acc = __fmaf_rn(su[j], bf16f(__ldg(Brow + j)), acc);
     }
-    Z[t * N + n] = z;
+    z = __fmul_rn(__ldg(scales + a), acc);
   }
+  Z[t * N + n] = z;
 }
 
 }  // namespace multi
@@ -122,8 +120,8 @@ int launch_multi_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t
   }
   {
     ProfileScope ps("multi_z", stream);
-    multi::multi_z<<<(unsigned)((a.N + 127) / 128), 128, (size_t)a.M * a.r * 4, stream>>>(
-        U, (int)a.M, a.N, a.B, a.r, a.n_adapters, a.adapter_idx, a.scales, Z);
+    multi::multi_z<<<dim3((unsigned)((a.N + 127) / 128), (unsigned)a.M), 128, (size_t)a.r * 4,
+                     stream>>>(U, a.N, a.B, a.r, a.n_adapters, a.adapter_idx, a.scales, Z);
     if (cudaGetLastError() != cudaSuccess) return QLORA_ERR_CUDA;
   }
   return launch_decode_gemv(a, L, Z, stream);

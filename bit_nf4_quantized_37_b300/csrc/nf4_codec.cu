@@ -39,8 +39,9 @@ constexpr int kQuantThreads = 256;
 // holds at most one threshold T, the level is c_lo + (y > T), and |y - T| < 2^-20 sends the
 // lane's 16 weights to the exact division (thresholds lie >= 2.3e-4 inside their cells, so
 // a threshold between x and y is always the one in y's cell); so does an absmax without a
-// finite reciprocal, which leaves every y of the fast path finite and inside the table.  The table is built once per CTA, one interleaved copy per lane (entry i of copy l
-// at word pair 32 i + l), so the 8-byte lookups of a half-warp never collide on a bank.
+// finite reciprocal, which leaves every y of the fast path finite and inside the table.  The
+// table is built once per CTA, one interleaved copy per lane (entry i of copy l at word pair
+// 32 i + l), so the 8-byte lookups of a half-warp never collide on a bank.
 // The last, partial group takes the element-by-element path with the exact division.
 constexpr int kCells = 82;                  // per sign: [0, 2^-5), then 5 binades x 16, [1, 1.0625)
 constexpr int kCopies = 32;                 // one table copy per lane

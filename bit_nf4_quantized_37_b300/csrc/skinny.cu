@@ -131,8 +131,6 @@ struct Params {
   const int8_t* qs;
   const float* steps;  // group steps, or without double quantization the block absmax
   const float* mean;
-  int dq;              // 1: double-quantized scales
-  int fp8;             // second-level codes are E4M3 (else int8)
   int qs_words;        // scale codes of a row's stage are one aligned 32-bit word
   float* part;         // [CTAs][2][16][128] fp32 pieces of split row blocks
   int* tickets;        // [row blocks] stages summed so far
@@ -186,13 +184,20 @@ __device__ __forceinline__ uint32_t scale_slot_off(int sl, int e) {
   return static_cast<uint32_t>(((sl * 16 + (e >> 5)) * 256) + 128 + (e & 31) * 4);
 }
 
-template <int NT>
+// Scale formats, a compile-time parameter so the producers' per-stage scale writes carry no
+// format test: the int8 or E4M3 second level, or the fp32 block absmax (no double quant).
+enum ScaleFormat : int { kScaleInt8 = 0, kScaleFp8 = 1, kScaleAbsmax = 2 };
+
+// OWN_LORA: the LoRA term from sU and B on the tensor cores (else the fp32 term p.Z is added)
+template <int NT, int SCALE, bool OWN_LORA>
 __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     nf4_decode_gemv(const __grid_constant__ CUtensorMap tmCodes,
                     const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmB, const Params p) {
   using C = Cfg<NT>;
   constexpr int STAGES = C::STAGES;
+  constexpr bool kDq = SCALE != kScaleAbsmax;
+  constexpr int kFp8 = SCALE == kScaleFp8 ? 1 : 0;
   static_assert(STAGES * 16 <= 256, "scale tables fit the byte-table holes");
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     // early into rotating register sets; otherwise each code is read when needed.
     const int R = tid - THREADS;
     const int pw_idx = warp - THREADS / 32;
-    const float mu = p.dq ? __ldg(p.mean) : 0.0f;
+    const float mu = kDq ? __ldg(p.mean) : 0.0f;
     const bool word_path = p.qs_words != 0;
     const int e0 = 16 * (R >> 4) + 2 * inv_perm8(R & 7) + ((R >> 3) & 1);
     uint32_t pw[SCALE_AHEAD];
@@ -315,12 +320,12 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
         float v = 0.f;
         if (n < p.N && kb < p.KB) {
           if (word_path) {
-            v = __fmaf_rn(nf4_second_level(w >> (8 * b), p.fp8), st, mu);
+            v = __fmaf_rn(nf4_second_level(w >> (8 * b), kFp8), st, mu);
           } else {
             const int64_t idx = n * p.KB + kb;
-            v = p.dq ? __fmaf_rn(nf4_second_level(static_cast<uint8_t>(__ldg(p.qs + idx)), p.fp8),
-                                 __ldg(p.steps + (idx >> 8)), mu)
-                     : __ldg(p.steps + idx);
+            v = kDq ? __fmaf_rn(nf4_second_level(static_cast<uint8_t>(__ldg(p.qs + idx)), kFp8),
+                                __ldg(p.steps + (idx >> 8)), mu)
+                    : __ldg(p.steps + idx);
           }
         }
         asm volatile("st.shared.f32 [%0], %1;" ::"r"(kTableBase + scale_slot_off(slot, b * 128 + e0)), "f"(v));
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     for (int i = 0; i < lora_boxes; ++i)
       tma_load_2d(sLora + i * LORA_BOX_BYTES, &tmB, &lora_bar, 64 * i, static_cast<int32_t>(rb * ROWS));
   };
-  const bool own_lora = p.Z == nullptr;  // uniform: the LoRA term on the tensor cores here
+  constexpr bool own_lora = OWN_LORA;
   if (tid == 0 && own_lora && s_begin % p.KST == 0) issue_lora(rb_first);
   bool lora_pending = own_lora && s_begin % p.KST == 0;  // a B-row tile in flight, not yet used
 
@@ -450,7 +455,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       v += sRed[(wb + 3) * C::ACC * 32 + idx];
       if (whole) {
         if (n < p.N) {
-          if (p.Z) v += __ldg(p.Z + t * p.N + n);
+          if constexpr (!OWN_LORA) v += __ldg(p.Z + t * p.N + n);
           p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
         }
       } else {
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
             v += __ldcg(p.part + (c * 2 + sl) * 16 * ROWS + t * ROWS + R);
           }
           if (n < p.N) {
-            if (p.Z) v += __ldg(p.Z + t * p.N + n);
+            if constexpr (!OWN_LORA) v += __ldg(p.Z + t * p.N + n);
             p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
           }
         }
@@ -704,7 +709,7 @@ int64_t skinny_ctas(int64_t N, int64_t K) {
   return T < num_sms() ? T : num_sms();
 }
 
-template <int NT>
+template <int NT, int SCALE, bool OWN_LORA>
 int run_decode(const CUtensorMap& tmC, const CUtensorMap& tmX, const CUtensorMap& tmB,
                const skinny::Params& p, unsigned ctas, cudaStream_t stream) {
   using C = skinny::Cfg<NT>;
@@ -717,19 +722,19 @@ int run_decode(const CUtensorMap& tmC, const CUtensorMap& tmX, const CUtensorMap
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, skinny::nf4_decode_gemv<NT>) != cudaSuccess)
+        cudaFuncGetAttributes(&fa, skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA>) != cudaSuccess)
       return QLORA_ERR_CUDA;
     const int base = reserved + static_cast<int>(fa.sharedSizeBytes);
     const int size = optin - static_cast<int>(fa.sharedSizeBytes);
     if (base > static_cast<int>(skinny::kStageBase) ||
         base + size < static_cast<int>(C::SMEM_END))
       return QLORA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              size) != cudaSuccess)
       return QLORA_ERR_CUDA;
     dyn = size;
   }
-  skinny::nf4_decode_gemv<NT><<<ctas, skinny::THREADS + skinny::PRODUCERS, dyn, stream>>>(tmC, tmX, tmB, p);
+  skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA><<<ctas, skinny::THREADS + skinny::PRODUCERS, dyn, stream>>>(tmC, tmX, tmB, p);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
@@ -787,9 +792,7 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
   p.qs = a.q.scale_codes;
   p.steps = a.q.scale_steps;
   p.mean = a.q.scale_mean;
-  p.dq = a.q.dq_block != 0 ? 1 : 0;
-  p.fp8 = a.q.dq_type == NF4_DQ_FP8 ? 1 : 0;
-  p.qs_words = (p.dq && p.KB % 4 == 0 && reinterpret_cast<uintptr_t>(a.q.scale_codes) % 4 == 0) ? 1 : 0;
+  p.qs_words = (a.q.dq_block != 0 && p.KB % 4 == 0 && reinterpret_cast<uintptr_t>(a.q.scale_codes) % 4 == 0) ? 1 : 0;
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.tickets = reinterpret_cast<int*>(ws + L.tickets);
   p.sU = own_lora ? reinterpret_cast<const uint16_t*>(ws + L.sU) : nullptr;
@@ -803,8 +806,25 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
   }
   const unsigned ctas = (unsigned)skinny_ctas(a.N, a.K);
   ProfileScope ps("decode_gemv", stream);
-  return a.M > 8 ? run_decode<2>(tmC, tmX, tmB, p, ctas, stream)
-                 : run_decode<1>(tmC, tmX, tmB, p, ctas, stream);
+  const int fmt = a.q.dq_block == 0 ? skinny::kScaleAbsmax
+                  : a.q.dq_type == NF4_DQ_FP8 ? skinny::kScaleFp8 : skinny::kScaleInt8;
+  if (!own_lora)  // per-token adapters: the int8 / fp8 / absmax formats without the LoRA MMA
+    switch (fmt + 3 * (a.M > 8 ? 1 : 0)) {
+      case 0: return run_decode<1, skinny::kScaleInt8, false>(tmC, tmX, tmB, p, ctas, stream);
+      case 1: return run_decode<1, skinny::kScaleFp8, false>(tmC, tmX, tmB, p, ctas, stream);
+      case 2: return run_decode<1, skinny::kScaleAbsmax, false>(tmC, tmX, tmB, p, ctas, stream);
+      case 3: return run_decode<2, skinny::kScaleInt8, false>(tmC, tmX, tmB, p, ctas, stream);
+      case 4: return run_decode<2, skinny::kScaleFp8, false>(tmC, tmX, tmB, p, ctas, stream);
+      default: return run_decode<2, skinny::kScaleAbsmax, false>(tmC, tmX, tmB, p, ctas, stream);
+    }
+  switch (fmt + 3 * (a.M > 8 ? 1 : 0)) {
+    case 0: return run_decode<1, skinny::kScaleInt8, true>(tmC, tmX, tmB, p, ctas, stream);
+    case 1: return run_decode<1, skinny::kScaleFp8, true>(tmC, tmX, tmB, p, ctas, stream);
+    case 2: return run_decode<1, skinny::kScaleAbsmax, true>(tmC, tmX, tmB, p, ctas, stream);
+    case 3: return run_decode<2, skinny::kScaleInt8, true>(tmC, tmX, tmB, p, ctas, stream);
+    case 4: return run_decode<2, skinny::kScaleFp8, true>(tmC, tmX, tmB, p, ctas, stream);
+    default: return run_decode<2, skinny::kScaleAbsmax, true>(tmC, tmX, tmB, p, ctas, stream);
+  }
 }
 
 int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
