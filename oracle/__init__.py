@@ -29,7 +29,7 @@ def lib() -> ctypes.CDLL:
     if _lib is None:
         path = _build.build()
         L = ctypes.CDLL(path)
-        i64, f64, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        i64, f64, vp, ci = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
         L.nf4o_levels.argtypes = [vp, vp]
         L.nf4o_levels.restype = None
         L.nf4o_bf16_rne.argtypes = [ctypes.c_float]
@@ -44,26 +44,33 @@ def lib() -> ctypes.CDLL:
         L.nf4o_block_absmax.restype = None
         L.nf4o_quantize.argtypes = [vp, i64, vp, vp, vp, vp, vp, ctypes.c_int]
         L.nf4o_quantize.restype = None
-        L.nf4o_dequantize.argtypes = [vp, vp, vp, ctypes.c_float, i64, vp, ctypes.c_int]
+        L.nf4o_dequantize.argtypes = [vp, vp, vp, ctypes.c_float, i64, vp, ctypes.c_int,
+                                      ctypes.c_int]
         L.nf4o_e4m3_decode.argtypes = [ctypes.c_uint8]
         L.nf4o_e4m3_decode.restype = f64
         L.nf4o_e4m3_encode.argtypes = [ctypes.c_float]
         L.nf4o_e4m3_encode.restype = ctypes.c_uint8
         L.nf4o_dequantize.restype = None
-        L.nf4o_lora_u_rows.argtypes = [vp, vp, i64, i64, vp, i64, vp]
+        L.nf4o_lora_u_rows.argtypes = [vp, vp, i64, i64, vp, i64, vp, ci]
         L.nf4o_lora_u_rows.restype = None
-        L.nf4o_lora_fwd_rows.argtypes = [vp, vp, vp, vp, i64, i64, i64, f64, vp, i64, vp, vp]
+        L.nf4o_lora_fwd_rows.argtypes = [vp, vp, vp, vp, i64, i64, i64, f64, vp, i64, vp, vp,
+                                         ci]
         L.nf4o_lora_fwd_rows.restype = None
-        L.nf4o_lora_v_rows.argtypes = [vp, vp, i64, i64, vp, i64, vp]
+        L.nf4o_lora_v_rows.argtypes = [vp, vp, i64, i64, vp, i64, vp, ci]
         L.nf4o_lora_v_rows.restype = None
-        L.nf4o_lora_dx_rows.argtypes = [vp, vp, vp, vp, i64, i64, i64, f64, vp, i64, vp, vp]
+        L.nf4o_lora_dx_rows.argtypes = [vp, vp, vp, vp, i64, i64, i64, f64, vp, i64, vp, vp,
+                                        ci]
         L.nf4o_lora_dx_rows.restype = None
-        L.nf4o_lora_dadb.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f64, vp, vp]
+        L.nf4o_lora_dadb.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f64, vp, vp, ci]
         L.nf4o_lora_dadb.restype = None
         L.nf4o_bf16_rne_double.argtypes = [f64]
         L.nf4o_bf16_rne_double.restype = ctypes.c_uint16
         L.nf4o_merge.argtypes = [vp, vp, vp, i64, i64, i64, f64, vp]
-        L.nf4o_dequantize_nodq.argtypes = [vp, vp, i64, vp]
+        L.nf4o_dequantize_nodq.argtypes = [vp, vp, i64, vp, ci]
+        L.nf4o_f16_to_double.argtypes = [ctypes.c_uint16]
+        L.nf4o_f16_to_double.restype = f64
+        L.nf4o_f16_rne_double.argtypes = [f64]
+        L.nf4o_f16_rne_double.restype = ctypes.c_uint16
         L.nf4o_dequantize_nodq.restype = None
         L.nf4o_merge.restype = None
         L.nf4o_int4_error.argtypes = [vp, i64, vp]
@@ -142,15 +149,16 @@ def quantize(W: np.ndarray, fp8: bool = False) -> dict:
             "absmax": absmax, "numel": n, "fp8": bool(fp8)}
 
 
-def dequantize(q: dict) -> np.ndarray:
-    """bf16 bits (uint16) of the dequantized weights, flat order (reading R7)."""
+def dequantize(q: dict, f16: bool = False) -> np.ndarray:
+    """bf16 bits (uint16) of the dequantized weights, flat order (reading R7); binary16
+    bits with f16 (reading R16)."""
     n = int(q["numel"])
     out = np.zeros(n, np.uint16)
     codes = np.ascontiguousarray(q["codes"], np.uint8)
     qscale = np.ascontiguousarray(q["qscale"], np.int8)
     steps = np.ascontiguousarray(q["steps"], np.float32)
     lib().nf4o_dequantize(_p(codes), _p(qscale), _p(steps), float(q["mean"]), n, _p(out),
-                          1 if q.get("fp8") else 0)
+                          1 if q.get("fp8") else 0, 1 if f16 else 0)
     return out
 
 
@@ -170,19 +178,20 @@ def _rows(rows, M):
     return np.ascontiguousarray(rows, np.int64)
 
 
-def lora_u(X, A, rows=None):
-    """U[i] = X[rows[i]] A^T in fp64.  X [M,K], A [r,K] bf16 bits."""
+def lora_u(X, A, rows=None, f16=False):
+    """U[i] = X[rows[i]] A^T in fp64.  X [M,K], A [r,K] bf16 bits (binary16 with f16)."""
     X, A = _u16(X), _u16(A)
     M, K = X.shape
     r = A.shape[0]
     rows = _rows(rows, M)
     U = np.zeros((rows.size, r), np.float64)
-    lib().nf4o_lora_u_rows(_p(X), _p(A), K, r, _p(rows), rows.size, _p(U))
+    lib().nf4o_lora_u_rows(_p(X), _p(A), K, r, _p(rows), rows.size, _p(U), int(f16))
     return U
 
 
-def lora_fwd(X, Wd, A, B, scale, rows=None):
-    """(Y, U) for the selected rows, fp64 (reading R8).  Wd [N,K] bf16 bits."""
+def lora_fwd(X, Wd, A, B, scale, rows=None, f16=False):
+    """(Y, U) for the selected rows, fp64 (reading R8).  Wd [N,K] bf16 bits; every 16-bit
+    input binary16 instead with f16 (reading R16)."""
     X, Wd, A, B = _u16(X), _u16(Wd), _u16(A), _u16(B)
     M, K = X.shape
     N = Wd.shape[0]
@@ -191,22 +200,22 @@ def lora_fwd(X, Wd, A, B, scale, rows=None):
     Y = np.zeros((rows.size, N), np.float64)
     U = np.zeros((rows.size, r), np.float64)
     lib().nf4o_lora_fwd_rows(_p(X), _p(Wd), _p(A), _p(B), N, K, r, float(scale),
-                             _p(rows), rows.size, _p(Y), _p(U))
+                             _p(rows), rows.size, _p(Y), _p(U), int(f16))
     return Y, U
 
 
-def lora_v(dY, B, rows=None):
+def lora_v(dY, B, rows=None, f16=False):
     dY, B = _u16(dY), _u16(B)
     M, N = dY.shape
     r = B.shape[1]
     rows = _rows(rows, M)
     V = np.zeros((rows.size, r), np.float64)
-    lib().nf4o_lora_v_rows(_p(dY), _p(B), N, r, _p(rows), rows.size, _p(V))
+    lib().nf4o_lora_v_rows(_p(dY), _p(B), N, r, _p(rows), rows.size, _p(V), int(f16))
     return V
 
 
-def lora_dx(dY, Wd, A, B, scale, rows=None):
-    """(dX, V) for the selected rows, fp64 (reading R8)."""
+def lora_dx(dY, Wd, A, B, scale, rows=None, f16=False):
+    """(dX, V) for the selected rows, fp64 (reading R8; binary16 inputs with f16)."""
     dY, Wd, A, B = _u16(dY), _u16(Wd), _u16(A), _u16(B)
     M, N = dY.shape
     K = Wd.shape[1]
@@ -215,12 +224,12 @@ def lora_dx(dY, Wd, A, B, scale, rows=None):
     dX = np.zeros((rows.size, K), np.float64)
     V = np.zeros((rows.size, r), np.float64)
     lib().nf4o_lora_dx_rows(_p(dY), _p(Wd), _p(A), _p(B), N, K, r, float(scale),
-                            _p(rows), rows.size, _p(dX), _p(V))
+                            _p(rows), rows.size, _p(dX), _p(V), int(f16))
     return dX, V
 
 
-def lora_dadb(dY, X, A, B, scale):
-    """(dA [r,K], dB [N,r]) over all rows, fp64 (reading R8)."""
+def lora_dadb(dY, X, A, B, scale, f16=False):
+    """(dA [r,K], dB [N,r]) over all rows, fp64 (reading R8; binary16 inputs with f16)."""
     dY, X, A, B = _u16(dY), _u16(X), _u16(A), _u16(B)
     M, N = dY.shape
     K = X.shape[1]
@@ -228,7 +237,7 @@ def lora_dadb(dY, X, A, B, scale):
     dA = np.zeros((r, K), np.float64)
     dB = np.zeros((N, r), np.float64)
     lib().nf4o_lora_dadb(_p(dY), _p(X), _p(A), _p(B), M, N, K, r, float(scale),
-                         _p(dA), _p(dB))
+                         _p(dA), _p(dB), int(f16))
     return dA, dB
 
 
@@ -239,14 +248,28 @@ def bf16_rne_double(x) -> np.ndarray:
     return np.array([f(float(v)) for v in x], np.uint16)
 
 
-def dequantize_nodq(q: dict) -> np.ndarray:
+def dequantize_nodq(q: dict, f16: bool = False) -> np.ndarray:
     """bf16 bits of the variant without double quantization: L[c] times the block's fp32
-    absmax, one rounding (reading R14).  q is an oracle quantize() dict."""
+    absmax, one rounding (reading R14); binary16 bits with f16.  q is an oracle quantize()
+    dict."""
     n = int(q["numel"])
     out = np.zeros(n, np.uint16)
     lib().nf4o_dequantize_nodq(_p(np.ascontiguousarray(q["codes"], np.uint8)),
-                               _p(np.ascontiguousarray(q["absmax"], np.float32)), n, _p(out))
+                               _p(np.ascontiguousarray(q["absmax"], np.float32)), n, _p(out),
+                               int(f16))
     return out
+
+
+def f16_to_double(h) -> np.ndarray:
+    """Values of binary16 bit patterns, element by element from the format's definition."""
+    f = lib().nf4o_f16_to_double
+    return np.array([f(int(v) & 0xFFFF) for v in np.ravel(h)], np.float64)
+
+
+def f16_rne_double(x) -> np.ndarray:
+    """fp64 -> binary16 bits, one rounding (ties to even), element by element (reading R16)."""
+    f = lib().nf4o_f16_rne_double
+    return np.array([f(float(v)) for v in np.ravel(x)], np.uint16)
 
 
 def merge(Wd, A, B, scale) -> np.ndarray:

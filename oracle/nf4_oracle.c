@@ -16,6 +16,8 @@
  *                  dequantization, double quantization of the per-block scales.
  *   [addaly]       addaly.com "QLoRA on one card", "What each setting is doing": weights
  *                  stored in 4 bits and dequantized to bfloat16 for each matrix multiply.
+ *   [digipro]      digipro.cn "QLoRA: Fine-Tuning a 7B Model on a 16GB GPU", "The QLoRA
+ *                  insight": the compute-dtype flag dequantizes to fp16 for the matmuls.
  *
  * Readings where the pages are silent (each is also listed in the design notes):
  *   R1 level values: the asymmetric normal-quantile construction of the QLoRA paper the
@@ -39,6 +41,10 @@
  *   R8 LoRA: Y = X W'^T + s (X A^T) B^T with s = alpha/r, no bias, no dropout;
  *      dX = dY W' + s (dY B) A,  dA = s (dY B)^T X,  dB = s dY^T (X A^T).
  *      All contractions here are fp64 sums in index order over bf16-valued inputs.
+ *   R16 fp16 compute type ([digipro] "The QLoRA insight": the compute-dtype flag set to
+ *      fp16): the same steps with every 16-bit value an IEEE binary16 instead of bf16 --
+ *      w' = f16_rne(L[c] * ahat) (binary16 subnormals kept), and X, A, B, dY decoded as
+ *      binary16.  Selected by the f16 argument of the functions below.
  *
  * Build: gcc -O2 -fopenmp -ffp-contract=off -fPIC -shared (see oracle/build.py).
  * The fp32 steps above rely on IEEE single arithmetic without contraction (x86-64 SSE).
@@ -120,6 +126,49 @@ static double bf16_to_double(uint16_t h) {
   float f;
   memcpy(&f, &u, 4);
   return (double)f;
+}
+
+/* ------------------------------------------------------------------ binary16 (R16) */
+
+/* IEEE binary16 bits -> value, from the format's definition: 1 sign bit, 5 exponent bits
+ * (bias 15), 10 fraction bits; exponent 0 holds zero and the subnormals f * 2^-24, exponent
+ * 31 the infinities and NaNs. */
+double nf4o_f16_to_double(uint16_t h) {
+  int sign = h >> 15, e = (h >> 10) & 0x1F, f = h & 0x3FF;
+  double v;
+  if (e == 0) v = ldexp((double)f, -24);
+  else if (e == 31) v = f ? NAN : INFINITY;
+  else v = ldexp((double)(1024 + f), e - 25);
+  return sign ? -v : v;
+}
+
+/* A double rounded once to the nearest binary16 (ties to even), from the definition: 11
+ * significant bits for |x| >= 2^-14, a fixed quantum of 2^-24 below that; a magnitude that
+ * rounds to 2^16 or more becomes infinity.  NaN inputs are not used on this path. */
+uint16_t nf4o_f16_rne_double(double x) {
+  uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  double a = fabs(x);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);                     /* a = m 2^e, m in [0.5, 1) */
+  int qexp = e - 11;
+  if (qexp < -24) qexp = -24;
+  double k = nearbyint(ldexp(a, -qexp));   /* round half to even */
+  double v = ldexp(k, qexp);               /* the rounded magnitude, exact */
+  if (v >= 65536.0) return (uint16_t)(sign | 0x7C00u);
+  if (v < ldexp(1.0, -14)) return (uint16_t)(sign | (uint16_t)ldexp(v, 24));  /* subnormal */
+  int ev;
+  double mv = frexp(v, &ev);               /* v = mv 2^ev, mv in [0.5, 1) */
+  uint16_t frac = (uint16_t)(ldexp(mv, 11) - 1024.0);
+  return (uint16_t)(sign | (uint16_t)((ev - 1 + 15) << 10) | frac);
+}
+
+/* One 16-bit input element: bf16, or binary16 when f16. */
+static double in16(uint16_t h, int f16) { return f16 ? nf4o_f16_to_double(h) : bf16_to_double(h); }
+
+/* One fp32 product rounded to the 16-bit output type. */
+static uint16_t out16(float p, int f16) {
+  return f16 ? nf4o_f16_rne_double((double)p) : nf4o_bf16_rne(p);
 }
 
 /* ------------------------------------------------------------------ quantize (R3-R6) */
@@ -247,9 +296,9 @@ float nf4o_block_scale(const int8_t* qscale, const float* steps, float mean, int
   return fmaf((float)qscale[b], steps[b / NF4O_GROUP], mean);
 }
 
-/* Dequantize to bf16 (raw bits), R7. */
+/* Dequantize to bf16 (raw bits), R7; binary16 when f16 (R16). */
 void nf4o_dequantize(const uint8_t* codes, const int8_t* qscale, const float* steps,
-                     float mean, int64_t numel, uint16_t* out, int fp8) {
+                     float mean, int64_t numel, uint16_t* out, int fp8, int f16) {
   float L[16], T[15];
   nf4o_levels(L, T);
   for (int64_t e = 0; e < numel; ++e) {
@@ -259,36 +308,37 @@ void nf4o_dequantize(const uint8_t* codes, const int8_t* qscale, const float* st
     uint8_t byte = codes[e / 2];
     int c = (e & 1) ? (byte & 0xF) : (byte >> 4);
     float p = L[c] * ahat;
-    out[e] = nf4o_bf16_rne(p);
+    out[e] = out16(p, f16);
   }
 }
 
 /* Dequantize the variant without double quantization (R14): the block scale is the stored
  * fp32 absmax itself. */
 void nf4o_dequantize_nodq(const uint8_t* codes, const float* absmax, int64_t numel,
-                          uint16_t* out) {
+                          uint16_t* out, int f16) {
   float L[16], T[15];
   nf4o_levels(L, T);
   for (int64_t e = 0; e < numel; ++e) {
     uint8_t byte = codes[e / 2];
     int c = (e & 1) ? (byte & 0xF) : (byte >> 4);
-    out[e] = nf4o_bf16_rne(L[c] * absmax[e / NF4O_BLOCK]);
+    out[e] = out16(L[c] * absmax[e / NF4O_BLOCK], f16);
   }
 }
 
 /* ------------------------------------------------------------------ LoRA linear (R8) */
-/* Shapes: X [M,K], Wd [N,K] (dequantized bf16), A [r,K], B [N,r], dY [M,N]; all bf16 bits.
+/* Shapes: X [M,K], Wd [N,K] (dequantized bf16), A [r,K], B [N,r], dY [M,N]; all bf16 bits,
+ * or all binary16 bits when f16 (R16).
  * Row subsets let the tests check sampled rows of full-size problems one by one. */
 
 /* U rows: U[i][j] = sum_k X[m_i][k] A[j][k]. */
 void nf4o_lora_u_rows(const uint16_t* X, const uint16_t* A, int64_t K, int64_t r,
-                      const int64_t* rows, int64_t nrows, double* U) {
+                      const int64_t* rows, int64_t nrows, double* U, int f16) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < nrows; ++i) {
     const uint16_t* x = X + rows[i] * K;
     for (int64_t j = 0; j < r; ++j) {
       double acc = 0.0;
-      for (int64_t k = 0; k < K; ++k) acc += bf16_to_double(x[k]) * bf16_to_double(A[j * K + k]);
+      for (int64_t k = 0; k < K; ++k) acc += in16(x[k], f16) * in16(A[j * K + k], f16);
       U[i * r + j] = acc;
     }
   }
@@ -297,16 +347,16 @@ void nf4o_lora_u_rows(const uint16_t* X, const uint16_t* A, int64_t K, int64_t r
 /* Forward rows: Y[i][n] = sum_k X[m_i][k] Wd[n][k] + s * sum_j U[i][j] B[n][j]. */
 void nf4o_lora_fwd_rows(const uint16_t* X, const uint16_t* Wd, const uint16_t* A,
                         const uint16_t* B, int64_t N, int64_t K, int64_t r, double s,
-                        const int64_t* rows, int64_t nrows, double* Y, double* U) {
-  nf4o_lora_u_rows(X, A, K, r, rows, nrows, U);
+                        const int64_t* rows, int64_t nrows, double* Y, double* U, int f16) {
+  nf4o_lora_u_rows(X, A, K, r, rows, nrows, U, f16);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < nrows; ++i) {
     const uint16_t* x = X + rows[i] * K;
     for (int64_t n = 0; n < N; ++n) {
       double base = 0.0;
-      for (int64_t k = 0; k < K; ++k) base += bf16_to_double(x[k]) * bf16_to_double(Wd[n * K + k]);
+      for (int64_t k = 0; k < K; ++k) base += in16(x[k], f16) * in16(Wd[n * K + k], f16);
       double lora = 0.0;
-      for (int64_t j = 0; j < r; ++j) lora += U[i * r + j] * bf16_to_double(B[n * r + j]);
+      for (int64_t j = 0; j < r; ++j) lora += U[i * r + j] * in16(B[n * r + j], f16);
       Y[i * N + n] = base + s * lora;
     }
   }
@@ -314,13 +364,13 @@ void nf4o_lora_fwd_rows(const uint16_t* X, const uint16_t* Wd, const uint16_t* A
 
 /* V rows: V[i][j] = sum_n dY[m_i][n] B[n][j]. */
 void nf4o_lora_v_rows(const uint16_t* dY, const uint16_t* B, int64_t N, int64_t r,
-                      const int64_t* rows, int64_t nrows, double* V) {
+                      const int64_t* rows, int64_t nrows, double* V, int f16) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < nrows; ++i) {
     const uint16_t* g = dY + rows[i] * N;
     for (int64_t j = 0; j < r; ++j) {
       double acc = 0.0;
-      for (int64_t n = 0; n < N; ++n) acc += bf16_to_double(g[n]) * bf16_to_double(B[n * r + j]);
+      for (int64_t n = 0; n < N; ++n) acc += in16(g[n], f16) * in16(B[n * r + j], f16);
       V[i * r + j] = acc;
     }
   }
@@ -330,21 +380,21 @@ void nf4o_lora_v_rows(const uint16_t* dY, const uint16_t* B, int64_t N, int64_t 
  * The loop over n is outside the loop over k; every dX entry is still a sum in n order. */
 void nf4o_lora_dx_rows(const uint16_t* dY, const uint16_t* Wd, const uint16_t* A,
                        const uint16_t* B, int64_t N, int64_t K, int64_t r, double s,
-                       const int64_t* rows, int64_t nrows, double* dX, double* V) {
-  nf4o_lora_v_rows(dY, B, N, r, rows, nrows, V);
+                       const int64_t* rows, int64_t nrows, double* dX, double* V, int f16) {
+  nf4o_lora_v_rows(dY, B, N, r, rows, nrows, V, f16);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < nrows; ++i) {
     const uint16_t* g = dY + rows[i] * N;
     double* out = dX + i * K;
     for (int64_t k = 0; k < K; ++k) out[k] = 0.0;
     for (int64_t n = 0; n < N; ++n) {
-      double gn = bf16_to_double(g[n]);
+      double gn = in16(g[n], f16);
       const uint16_t* w = Wd + n * K;
-      for (int64_t k = 0; k < K; ++k) out[k] += gn * bf16_to_double(w[k]);
+      for (int64_t k = 0; k < K; ++k) out[k] += gn * in16(w[k], f16);
     }
     for (int64_t k = 0; k < K; ++k) {
       double lora = 0.0;
-      for (int64_t j = 0; j < r; ++j) lora += V[i * r + j] * bf16_to_double(A[j * K + k]);
+      for (int64_t j = 0; j < r; ++j) lora += V[i * r + j] * in16(A[j * K + k], f16);
       out[k] += s * lora;
     }
   }
@@ -356,14 +406,14 @@ void nf4o_lora_dx_rows(const uint16_t* dY, const uint16_t* Wd, const uint16_t* A
  * outside the column loop for memory order; every entry is still a sum in m order. */
 void nf4o_lora_dadb(const uint16_t* dY, const uint16_t* X, const uint16_t* A,
                     const uint16_t* B, int64_t M, int64_t N, int64_t K, int64_t r, double s,
-                    double* dA, double* dB) {
+                    double* dA, double* dB, int f16) {
   const int64_t CH = 256;
   int64_t* all = (int64_t*)malloc((size_t)M * sizeof(int64_t));
   for (int64_t m = 0; m < M; ++m) all[m] = m;
   double* U = (double*)malloc((size_t)(M * r) * sizeof(double));
   double* V = (double*)malloc((size_t)(M * r) * sizeof(double));
-  nf4o_lora_u_rows(X, A, K, r, all, M, U);
-  nf4o_lora_v_rows(dY, B, N, r, all, M, V);
+  nf4o_lora_u_rows(X, A, K, r, all, M, U, f16);
+  nf4o_lora_v_rows(dY, B, N, r, all, M, V, f16);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t k0 = 0; k0 < K; k0 += CH) {
     int64_t k1 = k0 + CH < K ? k0 + CH : K;
@@ -371,7 +421,7 @@ void nf4o_lora_dadb(const uint16_t* dY, const uint16_t* X, const uint16_t* A,
     for (int64_t m = 0; m < M; ++m)
       for (int64_t j = 0; j < r; ++j) {
         double v = V[m * r + j];
-        for (int64_t k = k0; k < k1; ++k) acc[j * CH + (k - k0)] += v * bf16_to_double(X[m * K + k]);
+        for (int64_t k = k0; k < k1; ++k) acc[j * CH + (k - k0)] += v * in16(X[m * K + k], f16);
       }
     for (int64_t j = 0; j < r; ++j)
       for (int64_t k = k0; k < k1; ++k) dA[j * K + k] = s * acc[j * CH + (k - k0)];
@@ -384,7 +434,7 @@ void nf4o_lora_dadb(const uint16_t* dY, const uint16_t* X, const uint16_t* A,
     for (int64_t m = 0; m < M; ++m)
       for (int64_t j = 0; j < r; ++j) {
         double u = U[m * r + j];
-        for (int64_t n = n0; n < n1; ++n) acc[j * CH + (n - n0)] += bf16_to_double(dY[m * N + n]) * u;
+        for (int64_t n = n0; n < n1; ++n) acc[j * CH + (n - n0)] += in16(dY[m * N + n], f16) * u;
       }
     for (int64_t n = n0; n < n1; ++n)
       for (int64_t j = 0; j < r; ++j) dB[n * r + j] = s * acc[j * CH + (n - n0)];

@@ -542,3 +542,78 @@ def test_fp8_second_level_error_bound_and_extremes():
     for gidx in range(q["steps"].size):
         seg = slice(256 * gidx, min(256 * gidx + 256, a.size))
         assert np.max(np.abs(qv[seg])) == 448.0
+
+
+# ---------------------------------------------------------------- fp16 compute type (R16)
+# digipro.cn "QLoRA: Fine-Tuning a 7B Model on a 16GB GPU", "The QLoRA insight": the
+# compute-dtype flag dequantizes to fp16 for the matrix multiplies.
+
+def test_f16_decode_matches_numpy_on_every_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.f16_to_double(bits)
+    want = bits.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    fin = ~np.isnan(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert got[0x3C00] == 1.0 and got[0x0001] == 2.0 ** -24 and got[0x7BFF] == 65504.0
+
+
+def test_f16_rne_double_matches_numpy_and_ties():
+    """numpy converts fp64 to binary16 with one round-to-nearest-even; so must the oracle,
+    through normals, subnormals, exact ties and the overflow edge."""
+    g = wl.rng(71)
+    vals = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = (vals[:-1] + vals[1:]) / 2            # exact ties (representable in fp64)
+    x = np.concatenate([g.standard_normal(4000) * 10.0 ** g.integers(-9, 5, 4000),
+                        mids[::7], -mids[::11], mids[::13] * (1 + 2.0 ** -40),
+                        [0.0, -0.0, 65504.0, 65519.99, 65520.0, 1e6, -1e6, 2.0 ** -25,
+                         2.0 ** -25 * 1.0000001, 3 * 2.0 ** -26]])
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.f16_rne_double(x), want)
+
+
+def test_dequantize_f16_is_library_rounding_of_the_same_product():
+    """The fp16 dequantization rounds the same fp32 product L[c] * ahat as the bf16 one:
+    numpy's binary16 conversion of it (a library rounding) for double-quantized and for
+    absmax scales, with values small enough to reach binary16 subnormals."""
+    L, _ = oracle.levels()
+    W = wl.weight((3, 64 * 90 + 17), seed=72, sigma=0.02, outlier_frac=0.001).ravel()
+    W[: 64 * 3] *= 2.0 ** -14                    # blocks whose products are fp16 subnormals
+    q = oracle.quantize(W)
+    n = W.size
+    c = _unpack(q["codes"], n)
+    b = np.arange(n) // 64
+    ahat = np.array([np.float32(np.float64(qq) * np.float64(s) + np.float64(q["mean"]))
+                     for qq, s in zip(q["qscale"], np.repeat(q["steps"], 256)[:q["qscale"].size])],
+                    np.float32)
+    prod = (L[c] * ahat[b]).astype(np.float32)
+    assert np.array_equal(oracle.dequantize(q, f16=True), prod.astype(np.float16).view(np.uint16))
+    prod0 = (L[c] * np.repeat(q["absmax"], 64)[:n]).astype(np.float32)
+    assert np.array_equal(oracle.dequantize_nodq(q, f16=True),
+                          prod0.astype(np.float16).view(np.uint16))
+    sub = oracle.dequantize(q, f16=True)[: 64 * 3]
+    assert np.any((sub & 0x7C00) == 0) and np.any(sub & 0x3FF)
+
+
+def test_lora_f16_inputs_match_numpy_matmul():
+    """With f16 every 16-bit input is read as binary16: forward, dX, dA and dB equal the fp64
+    numpy products of the binary16 values."""
+    g = wl.rng(73)
+    M, N, K, r, s = 24, 64, 128, 8, 0.75
+    h = lambda *shape: (g.standard_normal(shape) * 0.5).astype(np.float16)
+    X, Wd, A, B, dY = h(M, K), h(N, K), h(r, K), h(N, r), h(M, N)
+    u = lambda a: a.view(np.uint16)
+    d = lambda a: a.astype(np.float64)
+    Y, U = oracle.lora_fwd(u(X), u(Wd), u(A), u(B), s, f16=True)
+    assert np.allclose(U, d(X) @ d(A).T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(Y, d(X) @ d(Wd).T + s * (d(X) @ d(A).T) @ d(B).T, rtol=1e-12, atol=1e-12)
+    dX, V = oracle.lora_dx(u(dY), u(Wd), u(A), u(B), s, f16=True)
+    assert np.allclose(V, d(dY) @ d(B), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dX, d(dY) @ d(Wd) + s * (d(dY) @ d(B)) @ d(A), rtol=1e-12, atol=1e-12)
+    dA, dB = oracle.lora_dadb(u(dY), u(X), u(A), u(B), s, f16=True)
+    assert np.allclose(dA, s * (d(dY) @ d(B)).T @ d(X), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dB, s * d(dY).T @ (d(X) @ d(A).T), rtol=1e-12, atol=1e-12)
+    # the same bits read as bf16 give a different answer: the flag is live
+    Yb, _ = oracle.lora_fwd(u(X), u(Wd), u(A), u(B), s)
+    assert not np.allclose(Yb, Y)
