@@ -419,6 +419,7 @@ def main():
                                                                l2_flush)
     if not args.no_secondary:
         secondary.update(measure_merge_and_error(qn, wl, p, q, A, B, dev, peaks, l2_flush))
+        secondary.update(measure_f16(qn, p, q, X, A, B, dY, peaks, l2_flush))
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -517,6 +518,23 @@ def measure_merge_and_error(qn, wl, p, q, A, B, dev, peaks, l2_flush):
     return out
 
 
+def measure_f16(qn, p, q, X, A, B, dY, peaks, l2_flush):
+    """The fp16 compute type on the same 4096^2 layer: forward + backward with X, A, B and dY
+    converted to fp16, against the bf16 burst peak (the tensor cores' dense fp16 and bf16
+    rates are equal)."""
+    import torch
+    Xh, Ah, Bh, dYh = (t.to(torch.float16) for t in (X, A, B, dY))
+
+    def step():
+        Y, U = qn.qlora_linear_fwd_f16(Xh, q, Ah, Bh, p.scale)
+        qn.qlora_linear_bwd_f16(dYh, Xh, q, Ah, Bh, p.scale, U)
+
+    ms = graph_timed_ms(step, l2_flush)
+    tf = p.fwd_bwd_flops() / ms / 1e9
+    return {"fwd_bwd_f16_4096x4096x4096_r16": {
+        "TFLOP/s": tf, "frac_tensor": tf / peaks["bf16_tflops"], "ms": ms}}
+
+
 def measure_secondary(qn, wl, dev, peaks, traffic, l2_flush, reps: int = 10):
     """HBM-bound paths on the decode-shaped 28672 x 8192 weight: dequantize, quantize and the
     M = 1 / 4 / 16 decode forward, each in GB/s of algorithmic bytes against the HBM peak."""
@@ -577,6 +595,12 @@ def measure_secondary(qn, wl, dev, peaks, traffic, l2_flush, reps: int = 10):
     out["dequantize_28672x8192"] = {"GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm,
                                     "ms": ms, "bytes": nbytes,
                                     "traffic": traffic.get(("nf4_dequant", "config4"))}
+    Wh = torch.empty(p4.N, p4.K, dtype=torch.float16, device=dev)
+    ms, _ = timed(lambda: qn.nf4_dequantize_f16(q, Wh), ["nf4_dequant"])
+    out["dequantize_f16_28672x8192"] = {"GB/s": nbytes / ms / 1e6,
+                                        "frac_hbm": nbytes / ms / 1e6 / hbm, "ms": ms,
+                                        "bytes": nbytes}
+    del Wh
     qq = qn.NF4Tensor.empty(p4.N, p4.K, dev)
     ms, prof = timed(lambda: qn.nf4_quantize(W, qq),
                      ["nf4_quant_blocks", "nf4_absmax_mean", "nf4_double_quant"])
@@ -602,6 +626,16 @@ def measure_secondary(qn, wl, dev, peaks, traffic, l2_flush, reps: int = 10):
             "gemv_kernel_frac_hbm": meta / ms_gemv / 1e6 / hbm,
             "gemv_traffic": traffic.get(("decode_gemv", "config4")) if M == 1 else None,
             "kernels_ms": {k: v[1] / reps for k, v in prof.items()}}
+    # the fp16 compute type at M = 1
+    p = wl.config4(1)
+    X, A, B = (bf16_dev(t, dev).to(torch.float16) for t in (p.X(), p.A(), p.B()))
+    Y = torch.empty(1, p.N, dtype=torch.float16, device=dev)
+    fn = lambda: qn.qlora_linear_fwd_f16(X, q, A, B, p.scale, save_u=False, out=Y)  # noqa: E731
+    ms_all, prof = timed(fn, ["decode_u", "decode_gemv"])
+    nbytes = meta + 2 * p.K + 2 * p.N + 2 * p.r * (p.K + p.N)
+    out["decode_fwd_f16_M1"] = {
+        "GB/s": nbytes / ms_all / 1e6, "frac_hbm": nbytes / ms_all / 1e6 / hbm, "ms": ms_all,
+        "bytes": nbytes, "kernels_ms": {k: v[1] / reps for k, v in prof.items()}}
     # per-token adapters: 16 tokens over 4 adapters (r = 64) on the same base
     p = wl.config4(16)
     nad = 4

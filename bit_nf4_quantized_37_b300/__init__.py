@@ -1,8 +1,9 @@
 """QLoRA NF4 + LoRA linear layer on B300 (sm_103a): thin Python binding of the C ABI.
 
 The entry points have the names of the C ABI in ``include/qlora_nf4.h``:
-``nf4_quantize``, ``nf4_dequantize``, ``qlora_linear_fwd``, ``qlora_linear_bwd`` (plus the
-size/utility calls).  This module only marshals torch tensors (device memory and the
+``nf4_quantize``, ``nf4_dequantize``, ``qlora_linear_fwd``, ``qlora_linear_bwd``, their fp16
+compute-type twins (``*_f16``), plus the merge, error-statistics, per-token-adapter and
+size/utility calls.  This module only marshals torch tensors (device memory and the
 current stream) into raw pointers; every step of the computation runs in the CUDA library
 ``libqlora_nf4.so``.  There is no CPU fallback: without the library or a compute-capability
 10.3 GPU the calls raise.
@@ -16,6 +17,7 @@ from ._binding import (  # noqa: F401
     level_table,
     lib,
     nf4_dequantize,
+    nf4_dequantize_f16,
     nf4_int4_error_stats,
     nf4_merge_lora,
     nf4_quantize,
@@ -25,7 +27,9 @@ from ._binding import (  # noqa: F401
     profile_start,
     profile_stop,
     qlora_linear_bwd,
+    qlora_linear_bwd_f16,
     qlora_linear_fwd,
+    qlora_linear_fwd_f16,
     qlora_linear_fwd_multi,
     qlora_workspace_bytes,
     status_str,
@@ -33,8 +37,9 @@ from ._binding import (  # noqa: F401
 
 __all__ = [
     "NF4Tensor", "QLoRAError", "device_status", "level_table", "lib", "nf4_dequantize",
-    "nf4_int4_error_stats", "nf4_merge_lora",
-    "nf4_quantize", "nf4_quantize_noalloc", "nf4_quantize_workspace_bytes", "nf4_storage_bytes", "profile_start",
-    "profile_stop", "qlora_linear_bwd",
-    "qlora_linear_fwd", "qlora_linear_fwd_multi", "qlora_workspace_bytes", "status_str",
+    "nf4_dequantize_f16", "nf4_int4_error_stats", "nf4_merge_lora", "nf4_quantize",
+    "nf4_quantize_noalloc", "nf4_quantize_workspace_bytes", "nf4_storage_bytes",
+    "profile_start", "profile_stop", "qlora_linear_bwd", "qlora_linear_bwd_f16",
+    "qlora_linear_fwd", "qlora_linear_fwd_f16", "qlora_linear_fwd_multi",
+    "qlora_workspace_bytes", "status_str",
 ]

@@ -25,7 +25,8 @@ EXPORTS = ["nf4_storage_bytes", "nf4_quantize_workspace_bytes", "nf4_quantize",
            "nf4_level_table", "qlora_device_status", "qlora_status_str", "qlora_version",
            "qlora_profile_start", "qlora_profile_stop", "nf4_quantize_noalloc",
            "nf4_merge_lora", "nf4_int4_error_workspace_bytes", "nf4_int4_error_stats",
-           "qlora_linear_fwd_multi"]
+           "qlora_linear_fwd_multi", "nf4_dequantize_f16", "qlora_linear_fwd_f16",
+           "qlora_linear_bwd_f16"]
 
 
 class QLoRAError(RuntimeError):
@@ -61,11 +62,16 @@ def lib() -> ctypes.CDLL:
             "nf4_quantize_workspace_bytes": [i64, u64p],
             "nf4_quantize": [vp, sp, vp, ctypes.c_uint64, vp],
             "nf4_dequantize": [sp, vp, vp],
+            "nf4_dequantize_f16": [sp, vp, vp],
             "qlora_workspace_bytes": [i64, i64, i64, i32, u64p],
             "qlora_linear_fwd": [vp, i64, sp, vp, vp, i32, ctypes.c_float, vp, vp, vp,
                                  ctypes.c_uint64, vp],
             "qlora_linear_bwd": [vp, vp, i64, sp, vp, vp, i32, ctypes.c_float, vp, vp, vp, vp,
                                  vp, ctypes.c_uint64, vp],
+            "qlora_linear_fwd_f16": [vp, i64, sp, vp, vp, i32, ctypes.c_float, vp, vp, vp,
+                                     ctypes.c_uint64, vp],
+            "qlora_linear_bwd_f16": [vp, vp, i64, sp, vp, vp, i32, ctypes.c_float, vp, vp, vp,
+                                     vp, vp, ctypes.c_uint64, vp],
             "nf4_level_table": [vp, vp],
             "qlora_device_status": [vp, vp],
             "qlora_status_str": [ctypes.c_int],
@@ -224,32 +230,53 @@ def nf4_quantize_noalloc(W: torch.Tensor, out: NF4Tensor) -> NF4Tensor:
     return out
 
 
+def _dequantize(call: str, dtype, q: NF4Tensor, out: torch.Tensor | None) -> torch.Tensor:
+    o = out if out is not None else torch.empty(q.rows, q.cols, dtype=dtype,
+                                                device=q.codes.device)
+    _req(o, dtype, "out")
+    s = q.c_struct()
+    _check(call, getattr(lib(), call)(ctypes.byref(s), _ptr(o), _stream()))
+    return o
+
+
 def nf4_dequantize(q: NF4Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
     """bf16 [rows, cols] dequantization of an NF4Tensor."""
-    o = out if out is not None else torch.empty(q.rows, q.cols, dtype=torch.bfloat16,
-                                                device=q.codes.device)
+    return _dequantize("nf4_dequantize", torch.bfloat16, q, out)
+
+
+def nf4_dequantize_f16(q: NF4Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """fp16 [rows, cols] dequantization of an NF4Tensor (the fp16 compute type)."""
+    return _dequantize("nf4_dequantize_f16", torch.float16, q, out)
+
+
+def _linear_fwd(call: str, dtype, X, q, A, B, scale, save_u, out):
+    for t, n in ((X, "X"), (A, "A"), (B, "B")):
+        _req(t, dtype, n)
+    M, K = X.shape
+    r = A.shape[0]
+    N = q.rows
+    Y = out if out is not None else torch.empty(M, N, dtype=dtype, device=X.device)
+    _req(Y, dtype, "out")
+    U = torch.empty(M, r, dtype=torch.float32, device=X.device) if save_u else None
+    nb = qlora_workspace_bytes(M, N, K, r)
+    ws = _workspace(nb, X.device)
     s = q.c_struct()
-    _check("nf4_dequantize", lib().nf4_dequantize(ctypes.byref(s), _ptr(o), _stream()))
-    return o
+    _check(call, getattr(lib(), call)(
+        _ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(Y), _ptr(U),
+        _ptr(ws), ws.numel(), _stream()))
+    return Y, U
 
 
 def qlora_linear_fwd(X: torch.Tensor, q: NF4Tensor, A: torch.Tensor, B: torch.Tensor,
                      scale: float, save_u: bool = True, out: torch.Tensor | None = None):
     """Y = X W'^T + scale (X A^T) B^T.  Returns (Y bf16 [M, N], U fp32 [M, r] or None)."""
-    for t, n in ((X, "X"), (A, "A"), (B, "B")):
-        _req(t, torch.bfloat16, n)
-    M, K = X.shape
-    r = A.shape[0]
-    N = q.rows
-    Y = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=X.device)
-    U = torch.empty(M, r, dtype=torch.float32, device=X.device) if save_u else None
-    nb = qlora_workspace_bytes(M, N, K, r)
-    ws = _workspace(nb, X.device)
-    s = q.c_struct()
-    _check("qlora_linear_fwd", lib().qlora_linear_fwd(
-        _ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(Y), _ptr(U),
-        _ptr(ws), ws.numel(), _stream()))
-    return Y, U
+    return _linear_fwd("qlora_linear_fwd", torch.bfloat16, X, q, A, B, scale, save_u, out)
+
+
+def qlora_linear_fwd_f16(X: torch.Tensor, q: NF4Tensor, A: torch.Tensor, B: torch.Tensor,
+                         scale: float, save_u: bool = True, out: torch.Tensor | None = None):
+    """qlora_linear_fwd in the fp16 compute type: X, A, B and Y are fp16."""
+    return _linear_fwd("qlora_linear_fwd_f16", torch.float16, X, q, A, B, scale, save_u, out)
 
 
 def qlora_linear_fwd_multi(X: torch.Tensor, q: NF4Tensor, A_all: torch.Tensor,
@@ -274,27 +301,38 @@ def qlora_linear_fwd_multi(X: torch.Tensor, q: NF4Tensor, A_all: torch.Tensor,
     return Y
 
 
-def qlora_linear_bwd(dY: torch.Tensor, X: torch.Tensor, q: NF4Tensor, A: torch.Tensor,
-                     B: torch.Tensor, scale: float, U: torch.Tensor | None = None,
-                     need_dx: bool = True):
-    """Returns (dX bf16 [M, K] or None, dA fp32 [r, K], dB fp32 [N, r]); the base is frozen."""
+def _linear_bwd(call: str, dtype, dY, X, q, A, B, scale, U, need_dx):
     for t, n in ((dY, "dY"), (X, "X"), (A, "A"), (B, "B")):
-        _req(t, torch.bfloat16, n)
+        _req(t, dtype, n)
     if U is not None:
         _req(U, torch.float32, "U")
     M, K = X.shape
     r = A.shape[0]
     N = q.rows
-    dX = torch.empty(M, K, dtype=torch.bfloat16, device=X.device) if need_dx else None
+    dX = torch.empty(M, K, dtype=dtype, device=X.device) if need_dx else None
     dA = torch.empty(r, K, dtype=torch.float32, device=X.device)
     dB = torch.empty(N, r, dtype=torch.float32, device=X.device)
     nb = qlora_workspace_bytes(M, N, K, r)
     ws = _workspace(nb, X.device)
     s = q.c_struct()
-    _check("qlora_linear_bwd", lib().qlora_linear_bwd(
+    _check(call, getattr(lib(), call)(
         _ptr(dY), _ptr(X), M, ctypes.byref(s), _ptr(A), _ptr(B), r, float(scale), _ptr(U),
         _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), ws.numel(), _stream()))
     return dX, dA, dB
+
+
+def qlora_linear_bwd(dY: torch.Tensor, X: torch.Tensor, q: NF4Tensor, A: torch.Tensor,
+                     B: torch.Tensor, scale: float, U: torch.Tensor | None = None,
+                     need_dx: bool = True):
+    """Returns (dX bf16 [M, K] or None, dA fp32 [r, K], dB fp32 [N, r]); the base is frozen."""
+    return _linear_bwd("qlora_linear_bwd", torch.bfloat16, dY, X, q, A, B, scale, U, need_dx)
+
+
+def qlora_linear_bwd_f16(dY: torch.Tensor, X: torch.Tensor, q: NF4Tensor, A: torch.Tensor,
+                         B: torch.Tensor, scale: float, U: torch.Tensor | None = None,
+                         need_dx: bool = True):
+    """qlora_linear_bwd in the fp16 compute type: dY, X, A, B and dX are fp16."""
+    return _linear_bwd("qlora_linear_bwd_f16", torch.float16, dY, X, q, A, B, scale, U, need_dx)
 
 
 def nf4_merge_lora(q: NF4Tensor, A: torch.Tensor, B: torch.Tensor, scale: float,

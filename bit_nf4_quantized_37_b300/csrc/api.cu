@@ -104,13 +104,24 @@ int nf4_quantize(const float* W, const nf4_tensor* out, void* workspace,
   return launch_quantize(W, numel, *out, workspace, static_cast<cudaStream_t>(stream));
 }
 
-int nf4_dequantize(const nf4_tensor* q, uint16_t* W_out, void* stream) {
+namespace {
+int dequantize_impl(const nf4_tensor* q, uint16_t* W_out, bool half, void* stream) {
   int st = check_tensor(q);
   if (st) return st;
   if (!W_out) return QLORA_ERR_INVALID_ARG;
   if (!aligned16(W_out)) return QLORA_ERR_MISALIGNED;
   if ((st = check_device())) return st;
-  return launch_dequantize(*q, q->rows * q->cols, W_out, static_cast<cudaStream_t>(stream));
+  return launch_dequantize(*q, q->rows * q->cols, W_out, half,
+                           static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+int nf4_dequantize(const nf4_tensor* q, uint16_t* W_out, void* stream) {
+  return dequantize_impl(q, W_out, false, stream);
+}
+
+int nf4_dequantize_f16(const nf4_tensor* q, uint16_t* W_out, void* stream) {
+  return dequantize_impl(q, W_out, true, stream);
 }
 
 int nf4_merge_lora(const nf4_tensor* Wq, const uint16_t* A, const uint16_t* B, int32_t r,
@@ -155,9 +166,10 @@ int qlora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r, uint64_t* 
   return QLORA_OK;
 }
 
-int qlora_linear_fwd(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const uint16_t* A,
-                     const uint16_t* B, int32_t r, float scale, uint16_t* Y, float* U_save,
-                     void* ws, uint64_t ws_bytes, void* stream) {
+namespace {
+int linear_fwd_impl(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const uint16_t* A,
+                    const uint16_t* B, int32_t r, float scale, uint16_t* Y, float* U_save,
+                    void* ws, uint64_t ws_bytes, bool half, void* stream) {
   int st = check_tensor(Wq);
   if (st) return st;
   if (!X || !A || !B || !Y || !ws || M < 1 || r < 1) return QLORA_ERR_INVALID_ARG;
@@ -173,8 +185,21 @@ int qlora_linear_fwd(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const u
   LinearArgs a{};
   a.M = M; a.N = N; a.K = K; a.r = r; a.scale = scale;
   a.X = X; a.A = A; a.B = B; a.Y = Y; a.U = U_save; a.q = *Wq;
-  a.ws = ws; a.ws_bytes = ws_bytes;
+  a.ws = ws; a.ws_bytes = ws_bytes; a.half = half;
   return linear_forward(a, static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+int qlora_linear_fwd(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const uint16_t* A,
+                     const uint16_t* B, int32_t r, float scale, uint16_t* Y, float* U_save,
+                     void* ws, uint64_t ws_bytes, void* stream) {
+  return linear_fwd_impl(X, M, Wq, A, B, r, scale, Y, U_save, ws, ws_bytes, false, stream);
+}
+
+int qlora_linear_fwd_f16(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const uint16_t* A,
+                         const uint16_t* B, int32_t r, float scale, uint16_t* Y, float* U_save,
+                         void* ws, uint64_t ws_bytes, void* stream) {
+  return linear_fwd_impl(X, M, Wq, A, B, r, scale, Y, U_save, ws, ws_bytes, true, stream);
 }
 
 int qlora_linear_fwd_multi(const uint16_t* X, int64_t M, const nf4_tensor* Wq,
@@ -203,10 +228,11 @@ int qlora_linear_fwd_multi(const uint16_t* X, int64_t M, const nf4_tensor* Wq,
   return linear_forward(a, static_cast<cudaStream_t>(stream));
 }
 
-int qlora_linear_bwd(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
-                     const uint16_t* A, const uint16_t* B, int32_t r, float scale,
-                     const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,
-                     uint64_t ws_bytes, void* stream) {
+namespace {
+int linear_bwd_impl(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                    const uint16_t* A, const uint16_t* B, int32_t r, float scale,
+                    const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,
+                    uint64_t ws_bytes, bool half, void* stream) {
   int st = check_tensor(Wq);
   if (st) return st;
   if (!dY || !X || !A || !B || !dA || !dB || !ws || M < 1 || r < 1) return QLORA_ERR_INVALID_ARG;
@@ -223,8 +249,25 @@ int qlora_linear_bwd(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4
   LinearArgs a{};
   a.M = M; a.N = N; a.K = K; a.r = r; a.scale = scale;
   a.X = X; a.A = A; a.B = B; a.dY = dY; a.dX = dX; a.dA = dA; a.dB = dB;
-  a.U_in = U_saved; a.q = *Wq; a.ws = ws; a.ws_bytes = ws_bytes;
+  a.U_in = U_saved; a.q = *Wq; a.ws = ws; a.ws_bytes = ws_bytes; a.half = half;
   return linear_backward(a, static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+int qlora_linear_bwd(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                     const uint16_t* A, const uint16_t* B, int32_t r, float scale,
+                     const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,
+                     uint64_t ws_bytes, void* stream) {
+  return linear_bwd_impl(dY, X, M, Wq, A, B, r, scale, U_saved, dX, dA, dB, ws, ws_bytes, false,
+                         stream);
+}
+
+int qlora_linear_bwd_f16(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                         const uint16_t* A, const uint16_t* B, int32_t r, float scale,
+                         const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,
+                         uint64_t ws_bytes, void* stream) {
+  return linear_bwd_impl(dY, X, M, Wq, A, B, r, scale, U_saved, dX, dA, dB, ws, ws_bytes, true,
+                         stream);
 }
 
 int qlora_device_status(int32_t* out, void* stream) {

@@ -330,10 +330,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // a_mn / b_mn: operand is MN-major (1) or K-major (0).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+// f16: A and B both fp16 (format 0) instead of both bf16 (format 1); kind::f16 takes the two
+// operands in one type.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn,
+                                                      bool f16 = false) {
   return (1u << 4)                                  // D format: f32
-         | (1u << 7)                                // A format: bf16
-         | (1u << 10)                               // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)                   // A format: bf16 (1) or f16 (0)
+         | ((f16 ? 0u : 1u) << 10)                  // B format: the same
          | (static_cast<uint32_t>(a_mn) << 15)      // A major
          | (static_cast<uint32_t>(b_mn) << 16)      // B major
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8

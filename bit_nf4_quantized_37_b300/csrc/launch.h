@@ -23,7 +23,9 @@ int read_and_clear_decode_error(int* out);
 uint64_t quantize_workspace_bytes(int64_t numel);
 int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws,
                     cudaStream_t stream);
-int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, cudaStream_t stream);
+// out: bf16, or fp16 when half
+int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, bool half,
+                      cudaStream_t stream);
 
 // Adapter merge and NF4-vs-INT4 error statistics (merge.cu).
 int launch_merge(const nf4_tensor& q, const uint16_t* A, const uint16_t* B, int r, float scale,

@@ -38,6 +38,9 @@ struct LinearArgs {
   const int32_t* adapter_idx;
   int n_adapters;
   const float* scales;
+  // fp16 compute type: X, A, B, dY, Y, dX, the staged sU / sV and the dequantized base in
+  // fp16 (else bf16)
+  bool half;
 };
 
 // Workspace regions (byte offsets, each 1024-aligned), for rank padded to rp = 64*ceil(r/64).

@@ -7,8 +7,9 @@
 // Each is tall and skinny: one big operand P read once from HBM, one rank-r operand Q that
 // fits in shared memory.  One kernel serves all four: P streams through a 4-stage TMA
 // ring of 128 x 64 tiles (two CTAs per SM) into the warp-level tensor cores (mma.sync m16n8k16, bf16 in, fp32
-// accumulate; ldmatrix.trans reads the column-wise P), Q is staged once per CTA for its whole
-// contraction range (converted to bf16 on the way, zero past the rank), and the contraction
+// accumulate; fp16 in the fp16 compute type; ldmatrix.trans reads the column-wise P), Q is
+// staged once per CTA for its whole contraction range (converted to the 16-bit type on the
+// way, zero past the rank), and the contraction
 // is split over blockIdx.y.  The CTA that finishes a row tile last (atomic ticket) adds the
 // split partial sums in split order and writes the outputs -- so results are
 // bit-reproducible and no separate reduction launch is needed.
@@ -17,6 +18,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "linear.h"
+#include "nf4_device.cuh"
 #include "profile.h"
 
 namespace qlora {
@@ -57,16 +59,25 @@ __device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t (&r)[2]) {
                : "=r"(r[0]), "=r"(r[1])
                : "r"(addr));
 }
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                               const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-      " {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+// bf16 operands, or fp16 when H; fp32 accumulate
+template <bool H>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
+                                          const uint32_t (&b)[2]) {
+  if constexpr (H)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Rank-r operand: Q(c, j) = src[c * ldc + j * ldj] (fp32 or bf16), zero for j >= r.
+// Rank-r operand: Q(c, j) = src[c * ldc + j * ldj] (fp32, or the 16-bit type), zero for j >= r.
 struct QSrc {
   const void* ptr;
   int64_t ldc, ldj;
@@ -75,7 +86,7 @@ struct QSrc {
 
 // Outputs of the last CTA of a row tile, for rows < R:
 //   out32[row * ld_row + j * ld_j] = scale32 * v                 (j < r)
-//   op[row * ld_op + j] = bf16(scale_op * v), zero for j >= r      (j < op_cols)
+//   op[row * ld_op + j] = 16-bit(scale_op * v), zero for j >= r    (j < op_cols)
 struct Epi {
   float* out32;
   int64_t ld_row, ld_j;
@@ -86,15 +97,16 @@ struct Epi {
   float scale_op;
 };
 
-__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
+// One fp32 value rounded to the 16-bit type (bf16, or fp16 when H).
+template <bool H>
+__device__ __forceinline__ uint16_t round16(float v) {
+  return static_cast<uint16_t>(pack_pair<H>(v, 0.0f) & 0xFFFFu);
 }
 
 // Stage Q(c, j), c in [c_begin, c_begin + clen), into sQ[c][j] (pitch NJ + 8).  Three vector
 // layouts of the source: bf16 contiguous along c (A[j][k]), bf16 contiguous along j (B[n][j],
 // sV[m][j]) and fp32 contiguous along j (U[m][j]); anything else element by element.
-template <int NJ>
+template <int NJ, bool H>
 __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int64_t C,
                                         int64_t c_begin, int clen, int tid) {
   constexpr int QP = NJ + 8;
@@ -148,7 +160,7 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
       }
     }
   } else if (qs.fp32 && qs.ldj == 1 && (qs.ldc % 4) == 0 && (r % 4) == 0) {
-    // fp32 src[c][j]: 4 j per load, converted to bf16
+    // fp32 src[c][j]: 4 j per load, converted to the 16-bit type
     constexpr int J4 = NJ / 4;
     const int n = clen * J4;
     for (int base = tid; base < n; base += BATCH * THREADS) {
@@ -167,7 +179,7 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
         if (idx >= n) break;
         const int c = idx / J4, j4 = idx % J4;
         *reinterpret_cast<uint2*>(sQ + c * QP + 4 * j4) =
-            make_uint2(pack2_bf16(v[u].x, v[u].y), pack2_bf16(v[u].z, v[u].w));
+            make_uint2(pack_pair<H>(v[u].x, v[u].y), pack_pair<H>(v[u].z, v[u].w));
       }
     }
   } else {
@@ -177,14 +189,14 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
       float v = 0.f;
       if (j < r && gc < C) {
         const int64_t off = gc * qs.ldc + (int64_t)j * qs.ldj;
-        v = qs.fp32 ? __ldg(f32 + off) : __bfloat162float(__ushort_as_bfloat16(__ldg(b16 + off)));
+        v = qs.fp32 ? __ldg(f32 + off) : widen16<H>(__ldg(b16 + off));
       }
-      sQ[c * QP + j] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      sQ[c * QP + j] = round16<H>(v);
     }
   }
 }
 
-template <bool kPCol, int NJ>
+template <bool kPCol, int NJ, bool H>
 __global__ void __launch_bounds__(THREADS, 2)
     side_gemm(const __grid_constant__ CUtensorMap tmP, int64_t R, int64_t C, QSrc qs, int r,
               float* __restrict__ part, int* __restrict__ tickets, int64_t chunk, int S, Epi epi) {
@@ -236,7 +248,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   // rank-r operand for the whole contraction range, as [c][j] bf16 (zero past the rank),
   // loaded with 16-byte vectors in batches of 8 per thread so the loads overlap
-  stage_q<NJ>(sQ, qs, r, C, c_begin, static_cast<int>(c_end - c_begin), tid);
+  stage_q<NJ, H>(sQ, qs, r, C, c_begin, static_cast<int>(c_end - c_begin), tid);
 
   float acc[NJ / 8][4];
 #pragma unroll
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       for (int t = 0; t < NJ / 8; ++t) {
         uint32_t b[2];
         ldsm_x2_t(smem_u32(sQ + qc * QP + t * 8), b);
-        mma_bf16_16816(acc[t], a, b);
+        mma_16816<H>(acc[t], a, b);
       }
     }
   }
@@ -362,7 +374,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         const float x = j < r ? vv[e] : 0.f;
         if (epi.out32 && j < r) epi.out32[row * epi.ld_row + j * epi.ld_j] = x * epi.scale32;
         if (epi.op && j < epi.op_cols)
-          epi.op[row * epi.ld_op + j] = __bfloat16_as_ushort(__float2bfloat16_rn(x * epi.scale_op));
+          epi.op[row * epi.ld_op + j] = round16<H>(x * epi.scale_op);
       }
     }
   }
@@ -418,8 +430,8 @@ Split pick_split(int64_t R, int64_t C, int NJ) {
   return sp;
 }
 
-template <bool kCol>
-int run_side(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t ldp, side::QSrc qs,
+template <bool kCol, bool H>
+int run_side_t(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t ldp, side::QSrc qs,
              int r, const side::Epi& epi, const LinearArgs& a, const WorkspaceLayout& L,
              cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
@@ -445,12 +457,12 @@ int run_side(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t 
     {                                                                                             \
       static bool attr = false; /* once per instantiation: the largest configuration */          \
       if (!attr)                                                                                  \
-        attr = cudaFuncSetAttribute(side::side_gemm<kCol, nj>,                                     \
+        attr = cudaFuncSetAttribute(side::side_gemm<kCol, nj, H>,                                  \
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,                  \
                                     side::STAGES * side::P_STAGE_BYTES + side::Q_SMEM_MAX + 1024) \
                == cudaSuccess;                                                                    \
     }                                                                                             \
-    side::side_gemm<kCol, nj><<<grid, side::THREADS, smem, stream>>>(tm, R, C, qs, r, part,         \
+    side::side_gemm<kCol, nj, H><<<grid, side::THREADS, smem, stream>>>(tm, R, C, qs, r, part,      \
                                                                      tickets, sp.chunk, sp.S, epi); \
     break;
     QLORA_SIDE_CASE(16)
@@ -461,6 +473,15 @@ int run_side(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t 
     default: return QLORA_ERR_UNSUPPORTED;
   }
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+}
+
+// The 16-bit type of P, Q and op follows the call (bf16, or fp16 in the fp16 compute type).
+template <bool kCol>
+int run_side(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t ldp, side::QSrc qs,
+             int r, const side::Epi& epi, const LinearArgs& a, const WorkspaceLayout& L,
+             cudaStream_t stream) {
+  return a.half ? run_side_t<kCol, true>(name, P, R, C, ldp, qs, r, epi, a, L, stream)
+                : run_side_t<kCol, false>(name, P, R, C, ldp, qs, r, epi, a, L, stream);
 }
 
 side::Epi no_epi() {
@@ -500,7 +521,7 @@ int launch_pad_b(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
-// U = X A^T -> sU = bf16(scale U) [M, rp], and U fp32 [M, r] into u32 (caller's U_save or
+// U = X A^T -> sU = 16-bit(scale U) [M, rp], and U fp32 [M, r] into u32 (caller's U_save or
 // the workspace copy the backward recomputes), when given.
 int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
@@ -516,7 +537,7 @@ int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cud
   return run_side<false>("side_u", a.X, a.M, a.K, a.K, qs, a.r, e, a, L, stream);
 }
 
-// V = dY B -> sV = bf16(scale V) [M, rp].
+// V = dY B -> sV = 16-bit(scale V) [M, rp].
 int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   side::QSrc qs{a.B, a.r, 1, 0};  // Q(c = n, j) = B[n][j]

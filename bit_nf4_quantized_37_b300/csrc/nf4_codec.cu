@@ -354,10 +354,11 @@ __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict_
 }
 
 // -------------------------------------------------------------------- dequantize
-// Grid-stride over 16-weight pieces: 8 code bytes in, 32 bytes of bf16 out per thread; the
-// four threads of a 64-block each build the block's byte table.  Without double
+// Grid-stride over 16-weight pieces: 8 code bytes in, 32 bytes of bf16 (fp16 when H) out per
+// thread; the four threads of a 64-block each build the block's byte table.  Without double
 // quantization (dq = 0) `steps` holds the fp32 absmax of every block, and the block scale is
 // fmaf(1, absmax, 0) = absmax through the same arithmetic.
+template <bool H>
 __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restrict__ codes,
                                                           const int8_t* __restrict__ scale_codes,
                                                           const float* __restrict__ steps,
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
         dq ? __fmaf_rn(nf4_second_level(static_cast<uint8_t>(__ldg(scale_codes + b)), fp8),
                        __ldg(steps + b / kGroup), mu)
            : __ldg(steps + b);
-    const Nf4ByteTable tab = nf4_make_table(scale);
+    const Nf4ByteTable tab = nf4_make_table<H>(scale);
     uint32_t q[2];
     if (e0 + 16 <= numel) {
       const uint2 raw = __ldg(reinterpret_cast<const uint2*>(codes + e0 / 2));
@@ -471,17 +472,18 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
-int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, cudaStream_t stream) {
+int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, bool half,
+                      cudaStream_t stream) {
   const int64_t npieces = (numel + 15) / 16;
   const int threads = 256;
   int64_t blocks = (npieces + threads - 1) / threads;
   const int64_t cap = (int64_t)num_sms() * 8;
   if (blocks > cap) blocks = cap;
   ProfileScope ps("nf4_dequant", stream);
-  nf4_dequant_kernel<<<(unsigned)blocks, threads, 0, stream>>>(q.codes, q.scale_codes,
-                                                               q.scale_steps, q.scale_mean,
-                                                               numel, q.dq_block != 0 ? 1 : 0,
-                                                               q.dq_type == NF4_DQ_FP8 ? 1 : 0, out);
+  (half ? nf4_dequant_kernel<true> : nf4_dequant_kernel<false>)<<<(unsigned)blocks, threads, 0,
+                                                                   stream>>>(
+      q.codes, q.scale_codes, q.scale_steps, q.scale_mean, numel, q.dq_block != 0 ? 1 : 0,
+      q.dq_type == NF4_DQ_FP8 ? 1 : 0, out);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 

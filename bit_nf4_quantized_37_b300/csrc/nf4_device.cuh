@@ -59,22 +59,46 @@ __device__ __forceinline__ uint32_t lop_select(uint32_t a, uint32_t b, uint32_t 
   return (a & ~m) | (b & m);  // per bit: m ? b : a  (one LOP3)
 }
 
-// One block's 16 dequantized values T[c] = bf16_rne(level[c] * scale), kept as byte tables
-// for prmt: lo[i] holds the low bytes of T[4i..4i+3], hi[i] their high bytes.
+// One block's 16 dequantized values T[c] = bf16_rne(level[c] * scale) (fp16 in the fp16
+// compute type), kept as byte tables for prmt: lo[i] holds the low bytes of T[4i..4i+3],
+// hi[i] their high bytes.
 struct Nf4ByteTable {
   uint32_t lo[4];
   uint32_t hi[4];
 };
 
+// Two fp32 values rounded to nearest even as one 32-bit pair (lo in the low half): bf16, or
+// fp16 when H (the fp16 compute type; fp16 subnormals kept).
+template <bool H>
+__device__ __forceinline__ uint32_t pack_pair(float lo, float hi) {
+  if constexpr (H) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+// Value of one 16-bit element (the low half of `bits`): bf16, or fp16 when H.
+template <bool H>
+__device__ __forceinline__ float widen16(uint32_t bits) {
+  if constexpr (H) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits & 0xFFFFu)));
+  } else {
+    return __uint_as_float(bits << 16);
+  }
+}
+
+template <bool H = false>
 __device__ __forceinline__ Nf4ByteTable nf4_make_table(float scale) {
   constexpr float L[16] = QLORA_NF4_LEVELS;
   uint32_t P[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    // one IEEE fp32 multiply per level, then round-to-nearest-even to bf16
-    __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(L[2 * j], scale),
-                                             __fmul_rn(L[2 * j + 1], scale));
-    P[j] = *reinterpret_cast<uint32_t*>(&h);  // low half = T[2j], high half = T[2j+1]
+    // one IEEE fp32 multiply per level, then round-to-nearest-even to the 16-bit type;
+    // low half = T[2j], high half = T[2j+1]
+    P[j] = pack_pair<H>(__fmul_rn(L[2 * j], scale), __fmul_rn(L[2 * j + 1], scale));
   }
   Nf4ByteTable t;
 #pragma unroll
@@ -86,7 +110,8 @@ __device__ __forceinline__ Nf4ByteTable nf4_make_table(float scale) {
 }
 
 // Eight packed codes (one little-endian u32 of the code stream: byte j holds elements 2j in
-// the high nibble and 2j+1 in the low nibble) -> eight bf16 in element order, as four u32
+// the high nibble and 2j+1 in the low nibble) -> eight 16-bit values in element order (the
+// table's type), as four u32
 // (element 2k in the low half of out[k]).
 __device__ __forceinline__ void nf4_dequant8(const Nf4ByteTable& t, uint32_t q, uint32_t (&out)[4]) {
   const uint32_t q4 = q * 16u;  // a multiply (IMAD, FMA pipe) keeps the shift off the ALU pipe
@@ -103,7 +128,7 @@ __device__ __forceinline__ void nf4_dequant8(const Nf4ByteTable& t, uint32_t q, 
     const uint32_t m = h ? m_hi : m_lo;
     const uint32_t lo = lop_select(prmt(t.lo[0], t.lo[1], s), prmt(t.lo[2], t.lo[3], s), m);
     const uint32_t hi = lop_select(prmt(t.hi[0], t.hi[1], s), prmt(t.hi[2], t.hi[3], s), m);
-    // lo/hi bytes are ordered [e1, e0, e3, e2]; interleave into bf16 pairs (e0,e1),(e2,e3)
+    // lo/hi bytes are ordered [e1, e0, e3, e2]; interleave into pairs (e0,e1),(e2,e3)
     out[2 * h + 0] = prmt(lo, hi, 0x4051u);
     out[2 * h + 1] = prmt(lo, hi, 0x6273u);
   }

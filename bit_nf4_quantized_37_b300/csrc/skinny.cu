@@ -96,25 +96,41 @@ static_assert(Cfg<1>::SMEM_END <= 228 * 1024 && Cfg<2>::SMEM_END <= 228 * 1024,
 __device__ __forceinline__ int perm8(int g) { return 2 * (g & 3) + (g >> 2); }
 __device__ __forceinline__ int inv_perm8(int p) { return (p >> 1) + 4 * (p & 1); }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
+// One fp32 value rounded to the 16-bit type (bf16, or fp16 when H).
+template <bool H>
+__device__ __forceinline__ uint16_t round16(float v) {
+  return static_cast<uint16_t>(pack_pair<H>(v, 0.0f) & 0xFFFFu);
 }
 
+// bf16 operands, or fp16 when H; fp32 accumulate
+template <bool H>
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-      " {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (H)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 // Same with a zero accumulator input.
+template <bool H>
 __device__ __forceinline__ void mma_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                             uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-      " {%8, %9}, {%10, %10, %10, %10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+  if constexpr (H)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -188,8 +204,9 @@ __device__ __forceinline__ uint32_t scale_slot_off(int sl, int e) {
 // format test: the int8 or E4M3 second level, or the fp32 block absmax (no double quant).
 enum ScaleFormat : int { kScaleInt8 = 0, kScaleFp8 = 1, kScaleAbsmax = 2 };
 
-// OWN_LORA: the LoRA term from sU and B on the tensor cores (else the fp32 term p.Z is added)
-template <int NT, int SCALE, bool OWN_LORA>
+// OWN_LORA: the LoRA term from sU and B on the tensor cores (else the fp32 term p.Z is added).
+// H: fp16 tokens, adapters, output and level table (the fp16 compute type), else bf16.
+template <int NT, int SCALE, bool OWN_LORA, bool H>
 __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     nf4_decode_gemv(const __grid_constant__ CUtensorMap tmCodes,
                     const __grid_constant__ CUtensorMap tmX,
@@ -271,7 +288,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   }
   for (int i = tid; i < 256 * 8; i += THREADS + PRODUCERS) {
     const int v = i >> 3;  // 8 threads per entry: 16 bytes (4 lane copies) each
-    const uint32_t e = pack_bf16x2(p.levels[v >> 4], p.levels[v & 15]);
+    const uint32_t e = pack_pair<H>(p.levels[v >> 4], p.levels[v & 15]);
     *reinterpret_cast<uint4*>(sTab + v * 256 + (i & 7) * 16) = make_uint4(e, e, e, e);
   }
   if (tid < 16 * (SU_PITCH / 8))
@@ -418,7 +435,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
               const uint16_t* ur = sUs + (g + 8 * o) * SU_PITCH + 16 * c + 2 * q;
               const uint32_t b0 = *reinterpret_cast<const uint32_t*>(ur);
               const uint32_t b1 = *reinterpret_cast<const uint32_t*>(ur + 8);
-              mma_16816(acc[j][o], a0, a1, a2, a3, b0, b1);
+              mma_16816<H>(acc[j][o], a0, a1, a2, a3, b0, b1);
             }
           }
         }
@@ -456,7 +473,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       if (whole) {
         if (n < p.N) {
           if constexpr (!OWN_LORA) v += __ldg(p.Z + t * p.N + n);
-          p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+          p.Y[t * p.N + n] = round16<H>(v);
         }
       } else {
         __stcg(mine + t * ROWS + R, v);
@@ -482,7 +499,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
           }
           if (n < p.N) {
             if constexpr (!OWN_LORA) v += __ldg(p.Z + t * p.N + n);
-            p.Y[t * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+            p.Y[t * p.N + n] = round16<H>(v);
           }
         }
         if (tid == 0) p.tickets[rb] = 0;  // ready for the next launch
@@ -569,9 +586,9 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
 #pragma unroll
           for (int o = 0; o < NT; ++o) {
             if (m == 0)
-              mma_16816_z(d[o], a0, a1, a2, a3, xf[o][0], xf[o][1]);
+              mma_16816_z<H>(d[o], a0, a1, a2, a3, xf[o][0], xf[o][1]);
             else
-              mma_16816(d[o], a0, a1, a2, a3, xf[o][2 * m], xf[o][2 * m + 1]);
+              mma_16816<H>(d[o], a0, a1, a2, a3, xf[o][2 * m], xf[o][2 * m + 1]);
           }
         }
 #pragma unroll
@@ -607,6 +624,7 @@ constexpr int U_PITCH = U_KC + 8;  // bf16 per staged row (+16 bytes: conflict-f
 
 inline int small_u_smem(int64_t rp) { return static_cast<int>((16 + rp) * U_PITCH * 2); }
 
+template <bool H>
 __global__ void __launch_bounds__(256) small_u(const uint16_t* __restrict__ X, int64_t M,
                                                int64_t K, const uint16_t* __restrict__ A, int r,
                                                int64_t rp, float scale, uint16_t* __restrict__ sU,
@@ -663,7 +681,7 @@ __global__ void __launch_bounds__(256) small_u(const uint16_t* __restrict__ X, i
         b0 = t0;
         b1 = t1;
       }
-      mma_16816(d, a0, a1, a2, a3, b0, b1);
+      mma_16816<H>(d, a0, a1, a2, a3, b0, b1);
     }
     // d: [0] token g / row 8 oc + 2q, [1] token g / + 1, [2] token g + 8 / 2q, [3] token g + 8
     *reinterpret_cast<float2*>(mine + g * rp + 8 * oc + 2 * q) = make_float2(d[0], d[1]);
@@ -690,7 +708,7 @@ __global__ void __launch_bounds__(256) small_u(const uint16_t* __restrict__ X, i
       for (int k = 0; k < 16; ++k) u += a[k];
     }
     for (; c < S; ++c) u += __ldcg(src + c * cs);
-    sU[t * rp + j] = j < r ? __bfloat16_as_ushort(__float2bfloat16_rn(u * scale)) : 0;
+    sU[t * rp + j] = j < r ? round16<H>(u * scale) : 0;
     if (U_out && j < r) U_out[t * r + j] = u;
   }
   if (tid == 0) *ticket = 0;  // ready for the next launch
@@ -709,7 +727,7 @@ int64_t skinny_ctas(int64_t N, int64_t K) {
   return T < num_sms() ? T : num_sms();
 }
 
-template <int NT, int SCALE, bool OWN_LORA>
+template <int NT, int SCALE, bool OWN_LORA, bool H = false>
 int run_decode(const CUtensorMap& tmC, const CUtensorMap& tmX, const CUtensorMap& tmB,
                const skinny::Params& p, unsigned ctas, cudaStream_t stream) {
   using C = skinny::Cfg<NT>;
@@ -722,19 +740,19 @@ int run_decode(const CUtensorMap& tmC, const CUtensorMap& tmX, const CUtensorMap
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA>) != cudaSuccess)
+        cudaFuncGetAttributes(&fa, skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA, H>) != cudaSuccess)
       return QLORA_ERR_CUDA;
     const int base = reserved + static_cast<int>(fa.sharedSizeBytes);
     const int size = optin - static_cast<int>(fa.sharedSizeBytes);
     if (base > static_cast<int>(skinny::kStageBase) ||
         base + size < static_cast<int>(C::SMEM_END))
       return QLORA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA, H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              size) != cudaSuccess)
       return QLORA_ERR_CUDA;
     dyn = size;
   }
-  skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA><<<ctas, skinny::THREADS + skinny::PRODUCERS, dyn, stream>>>(tmC, tmX, tmB, p);
+  skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA, H><<<ctas, skinny::THREADS + skinny::PRODUCERS, dyn, stream>>>(tmC, tmX, tmB, p);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
@@ -752,14 +770,17 @@ int launch_skinny_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t 
   uint16_t* sU = reinterpret_cast<uint16_t*>(ws + L.sU);
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(skinny::small_u, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(skinny::small_u<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             skinny::small_u_smem(2 * 64)) != cudaSuccess ||
+        cudaFuncSetAttribute(skinny::small_u<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              skinny::small_u_smem(2 * 64)) != cudaSuccess)
       return QLORA_ERR_CUDA;
     attr = true;
   }
   ProfileScope ps("decode_u", stream);
   const unsigned chunks = (unsigned)((a.K + skinny::U_KC - 1) / skinny::U_KC);
-  skinny::small_u<<<chunks, 256, skinny::small_u_smem(L.rp), stream>>>(
+  (a.half ? skinny::small_u<true> : skinny::small_u<false>)<<<chunks, 256,
+                                                             skinny::small_u_smem(L.rp), stream>>>(
       a.X, a.M, a.K, a.A, a.r, L.rp, a.scale, sU, a.U, reinterpret_cast<float*>(ws + L.part),
       reinterpret_cast<int*>(ws + L.tickets));
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
@@ -808,6 +829,15 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
   ProfileScope ps("decode_gemv", stream);
   const int fmt = a.q.dq_block == 0 ? skinny::kScaleAbsmax
                   : a.q.dq_type == NF4_DQ_FP8 ? skinny::kScaleFp8 : skinny::kScaleInt8;
+  if (a.half)  // the fp16 compute type (with the LoRA term on chip)
+    switch (fmt + 3 * (a.M > 8 ? 1 : 0)) {
+      case 0: return run_decode<1, skinny::kScaleInt8, true, true>(tmC, tmX, tmB, p, ctas, stream);
+      case 1: return run_decode<1, skinny::kScaleFp8, true, true>(tmC, tmX, tmB, p, ctas, stream);
+      case 2: return run_decode<1, skinny::kScaleAbsmax, true, true>(tmC, tmX, tmB, p, ctas, stream);
+      case 3: return run_decode<2, skinny::kScaleInt8, true, true>(tmC, tmX, tmB, p, ctas, stream);
+      case 4: return run_decode<2, skinny::kScaleFp8, true, true>(tmC, tmX, tmB, p, ctas, stream);
+      default: return run_decode<2, skinny::kScaleAbsmax, true, true>(tmC, tmX, tmB, p, ctas, stream);
+    }
   if (!own_lora)  // per-token adapters: the int8 / fp8 / absmax formats without the LoRA MMA
     switch (fmt + 3 * (a.M > 8 ? 1 : 0)) {
       case 0: return run_decode<1, skinny::kScaleInt8, false>(tmC, tmX, tmB, p, ctas, stream);

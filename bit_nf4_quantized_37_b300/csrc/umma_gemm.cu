@@ -116,12 +116,9 @@ __device__ __forceinline__ void bulk_wait_read1() {
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-template <int kMode, int kAcc>  // kMode 0: forward (W tile K-major), 1: input gradient (MN-major)
+// kMode 0: forward (W tile K-major), 1: input gradient (MN-major).  H: the fp16 compute type
+// (operands, dequantized tiles and output in fp16), else bf16.
+template <int kMode, int kAcc, bool H>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fused_nf4_lora_gemm(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA2,
@@ -199,7 +196,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
     if (elect_one_sync()) {
-      constexpr uint32_t idesc = idesc_bf16_f32(UM, BN, 0, kMode);
+      constexpr uint32_t idesc = idesc_bf16_f32(UM, BN, 0, kMode, H);
       bool ok = true;
       for (int s = 0; s < total && ok; ++s) {
         const int slot = s % STAGES, round = s / STAGES;
@@ -270,7 +267,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Slice cur = (kc & 1) ? pf1 : pf0;  // loaded two stages ago
         uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
         if (cur.valid) {
-          const Nf4ByteTable tab = nf4_make_table(__fmaf_rn(cur.q, cur.step, mu));
+          const Nf4ByteTable tab = nf4_make_table<H>(__fmaf_rn(cur.q, cur.step, mu));
           const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
                                      cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
 #pragma unroll
@@ -326,10 +323,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int j = 0; j < 4; ++j) {
           const uint32_t phys = j ^ ((lane >> 1) & 3);  // 64-byte swizzle
           *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) = make_uint4(
-              pack_bf16(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-              pack_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-              pack_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-              pack_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+              pack_pair<H>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+              pack_pair<H>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+              pack_pair<H>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+              pack_pair<H>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -382,7 +379,7 @@ constexpr int GROUP_WARPS = 4;
 constexpr int TMEM_COLS = 512;
 }  // namespace pairk
 
-template <int kMode>
+template <int kMode, bool H>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     fused_pair_gemm(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmA2,
@@ -469,7 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer (leader)
     if (rank == 0 && elect_one_sync()) {
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * UM, BN, 0, kMode);
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * UM, BN, 0, kMode, H);
       bool ok = true;
       for (int s = 0; s < total && ok; ++s) {
         const int slot = s % STAGES, round = s / STAGES;
@@ -544,7 +541,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint4 rv[8];
     auto dequant = [&](const Slice& cur) {
       if (cur.valid) {
-        const Nf4ByteTable tab = nf4_make_table(__fmaf_rn(cur.q, cur.step, mu));
+        const Nf4ByteTable tab = nf4_make_table<H>(__fmaf_rn(cur.q, cur.step, mu));
         const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
                                    cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
 #pragma unroll
@@ -617,10 +614,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int j = 0; j < 4; ++j) {
           const uint32_t phys = j ^ ((lane >> 1) & 3);  // 64-byte swizzle
           *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) = make_uint4(
-              pack_bf16(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-              pack_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-              pack_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-              pack_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+              pack_pair<H>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+              pack_pair<H>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+              pack_pair<H>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+              pack_pair<H>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -646,13 +643,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
 namespace {
 
+// A 2-D map of 16-bit elements.  The copy is bitwise and the out-of-range fill is all-zero
+// bits (+0 in bf16 and in fp16), so the same map serves the fp16 compute type.
 bool map_bf16(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t pitch_elems,
               uint32_t box_inner, uint32_t box_outer, MapSwizzle sw) {
   return make_tensor_map_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)inner,
                             (uint64_t)outer, (uint64_t)pitch_elems * 2, box_inner, box_outer, sw);
 }
 
-template <int kMode, int kAcc, bool kPair>
+template <int kMode, int kAcc, bool kPair, bool H>
 int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
   using namespace fused;
   constexpr int BM = kPair ? pairk::BM_CTA : Tile<kAcc>::BM;
@@ -661,9 +660,9 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   static bool attr_set = false;  // per process; the attribute is per function
   if (!attr_set) {
     const cudaError_t e =
-        kPair ? cudaFuncSetAttribute(fused_pair_gemm<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES)
-              : cudaFuncSetAttribute(fused_nf4_lora_gemm<kMode, kAcc>,
+        kPair ? cudaFuncSetAttribute(fused_pair_gemm<kMode, H>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)
+              : cudaFuncSetAttribute(fused_nf4_lora_gemm<kMode, kAcc, H>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return QLORA_ERR_CUDA;
     attr_set = true;
@@ -720,10 +719,10 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   cudaError_t e;
   if (kPair) {  // the CTA pair is the kernel's compile-time cluster shape
     cfg.gridDim = dim3((unsigned)(2 * ((a.M + 511) / 512)), (unsigned)((p.Nout + BN - 1) / BN));
-    e = cudaLaunchKernelEx(&cfg, fused_pair_gemm<kMode>, tA, tA2, tB2, tOut, p);
+    e = cudaLaunchKernelEx(&cfg, fused_pair_gemm<kMode, H>, tA, tA2, tB2, tOut, p);
   } else {
     cfg.gridDim = dim3((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM));
-    e = cudaLaunchKernelEx(&cfg, fused_nf4_lora_gemm<kMode, kAcc>, tA, tA2, tB2, tOut, p);
+    e = cudaLaunchKernelEx(&cfg, fused_nf4_lora_gemm<kMode, kAcc, H>, tA, tA2, tB2, tOut, p);
   }
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
@@ -739,20 +738,23 @@ static int tile_choice(int64_t M, int64_t Nout) {
   return tiles >= num_sms() ? 1 : 0;
 }
 
-int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  switch (tile_choice(a.M, a.N)) {
-    case 2: return launch_fused<0, 2, true>(a, L, stream);
-    case 1: return launch_fused<0, 2, false>(a, L, stream);
-    default: return launch_fused<0, 1, false>(a, L, stream);
+template <int kMode, bool H>
+static int launch_fused_mode(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+  switch (tile_choice(a.M, kMode == 0 ? a.N : a.K)) {
+    case 2: return launch_fused<kMode, 2, true, H>(a, L, stream);
+    case 1: return launch_fused<kMode, 2, false, H>(a, L, stream);
+    default: return launch_fused<kMode, 1, false, H>(a, L, stream);
   }
 }
 
+int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+  return a.half ? launch_fused_mode<0, true>(a, L, stream)
+                : launch_fused_mode<0, false>(a, L, stream);
+}
+
 int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  switch (tile_choice(a.M, a.K)) {
-    case 2: return launch_fused<1, 2, true>(a, L, stream);
-    case 1: return launch_fused<1, 2, false>(a, L, stream);
-    default: return launch_fused<1, 1, false>(a, L, stream);
-  }
+  return a.half ? launch_fused_mode<1, true>(a, L, stream)
+                : launch_fused_mode<1, false>(a, L, stream);
 }
 
 }  // namespace qlora

@@ -149,6 +149,15 @@ int nf4_quantize_noalloc(const float* W, const nf4_tensor* out, void* stream);
  */
 int nf4_dequantize(const nf4_tensor* q, uint16_t* W_out, void* stream);
 
+/*
+ * nf4_dequantize with fp16 output (the fp16 compute type: digipro.cn "QLoRA: Fine-Tuning a
+ * 7B Model on a 16GB GPU", "The QLoRA insight", where the compute-dtype flag dequantizes to
+ * fp16 for the matrix multiplies).  Each weight is the same fp32 product L[c] * absmax_hat
+ * rounded once to fp16 (nearest, ties to even; fp16 subnormals kept).  Arguments, alignment
+ * and errors as nf4_dequantize.
+ */
+int nf4_dequantize_f16(const nf4_tensor* q, uint16_t* W_out, void* stream);
+
 /* Device workspace (bytes) qlora_linear_fwd / qlora_linear_bwd need for these sizes. */
 int qlora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r, uint64_t* out);
 
@@ -166,6 +175,19 @@ int qlora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r, uint64_t* 
 int qlora_linear_fwd(const uint16_t* X, int64_t M, const nf4_tensor* Wq,
                      const uint16_t* A, const uint16_t* B, int32_t r, float scale,
                      uint16_t* Y, float* U_save, void* ws, uint64_t ws_bytes, void* stream);
+
+/*
+ * qlora_linear_fwd in the fp16 compute type (digipro.cn "QLoRA: Fine-Tuning a 7B Model on a
+ * 16GB GPU", "The QLoRA insight": the compute-dtype flag set to fp16).  X, A, B and Y are
+ * fp16; W' is the fp16 dequantization (as nf4_dequantize_f16); the LoRA term enters the fp32
+ * accumulator as fp16(scale*U) and Y is rounded once to fp16.  Everything else (shapes,
+ * decode path for M <= 16, U_save, ws, errors) as qlora_linear_fwd.  Values beyond the fp16
+ * range become infinities, as in any fp16 matrix multiply.
+ */
+int qlora_linear_fwd_f16(const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                         const uint16_t* A, const uint16_t* B, int32_t r, float scale,
+                         uint16_t* Y, float* U_save, void* ws, uint64_t ws_bytes,
+                         void* stream);
 
 /*
  * qlora_linear_fwd for M <= 16 tokens that each choose their own adapter over one shared NF4
@@ -200,6 +222,16 @@ int qlora_linear_bwd(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4
                      const uint16_t* A, const uint16_t* B, int32_t r, float scale,
                      const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,
                      uint64_t ws_bytes, void* stream);
+
+/*
+ * qlora_linear_bwd in the fp16 compute type: dY, X, A, B and dX are fp16, W' is the fp16
+ * dequantization, and the fp32 side products enter the tensor cores as fp16(scale*V) and
+ * fp16(U); dA and dB are fp32 as in qlora_linear_bwd.  Everything else as qlora_linear_bwd.
+ */
+int qlora_linear_bwd_f16(const uint16_t* dY, const uint16_t* X, int64_t M,
+                         const nf4_tensor* Wq, const uint16_t* A, const uint16_t* B, int32_t r,
+                         float scale, const float* U_saved, uint16_t* dX, float* dA, float* dB,
+                         void* ws, uint64_t ws_bytes, void* stream);
 
 /*
  * Fold a LoRA adapter into the NF4 base (junaidshaukat.com "QLoRA -- the democratization

@@ -15,6 +15,17 @@ def bf16_dev(bits: np.ndarray) -> torch.Tensor:
     return t.view(torch.bfloat16).cuda()
 
 
+def f16_dev(bits: np.ndarray) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.float16).cuda()
+
+
+def f16_from_bf16_bits(bits: np.ndarray) -> np.ndarray:
+    """binary16 bits of bf16-valued inputs (numpy's round to nearest even; exact for the
+    normal range, which the seeded inputs stay in apart from their smallest values)."""
+    return wl.bf16_bits_to_f32(bits).astype(np.float16).view(np.uint16)
+
+
 def bits_host(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
@@ -43,19 +54,25 @@ class Problem:
     """A LinearProblem with its oracle quantization and device copies."""
 
     def __init__(self, p: wl.LinearProblem, quantize_on_gpu: bool = True,
-                 double_quant: bool = True, fp8_second_level: bool = False):
+                 double_quant: bool = True, fp8_second_level: bool = False, half: bool = False):
         self.p = p
+        self.half = half
         W = p.W()
         self.qo = oracle.quantize(W, fp8=fp8_second_level)
         if double_quant:
-            self.Wd = oracle.dequantize(self.qo).reshape(p.N, p.K)
+            self.Wd = oracle.dequantize(self.qo, f16=half).reshape(p.N, p.K)
         else:
-            self.Wd = oracle.dequantize_nodq(self.qo).reshape(p.N, p.K)
+            self.Wd = oracle.dequantize_nodq(self.qo, f16=half).reshape(p.N, p.K)
         if quantize_on_gpu or not double_quant or fp8_second_level:
             self.qd = qn.nf4_quantize(torch.from_numpy(W).cuda(), double_quant=double_quant,
                                       fp8_second_level=fp8_second_level)
         else:
             self.qd = upload_oracle_tensor(self.qo, p.N, p.K)
         self.X, self.A, self.B, self.dY = p.X(), p.A(), p.B(), p.dY()
-        self.Xd, self.Ad, self.Bd, self.dYd = (bf16_dev(self.X), bf16_dev(self.A),
-                                               bf16_dev(self.B), bf16_dev(self.dY))
+        dev = bf16_dev
+        if half:
+            self.X, self.A, self.B, self.dY = (f16_from_bf16_bits(t)
+                                               for t in (self.X, self.A, self.B, self.dY))
+            dev = f16_dev
+        self.Xd, self.Ad, self.Bd, self.dYd = (dev(self.X), dev(self.A), dev(self.B),
+                                               dev(self.dY))

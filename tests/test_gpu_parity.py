@@ -110,8 +110,10 @@ def test_dequantize_decode_tensor_bit_exact():
 # ------------------------------------------------------------------ forward / backward
 def _check_fwd(pb: Problem, rows=None):
     p = pb.p
-    Y, U = qn.qlora_linear_fwd(pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale)
-    Yo, Uo = oracle.lora_fwd(pb.X, pb.Wd, pb.A, pb.B, p.scale, rows)
+    fwd = qn.qlora_linear_fwd_f16 if pb.half else qn.qlora_linear_fwd
+    Y, U = fwd(pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale)
+    assert Y.dtype == (torch.float16 if pb.half else torch.bfloat16)
+    Yo, Uo = oracle.lora_fwd(pb.X, pb.Wd, pb.A, pb.B, p.scale, rows, f16=pb.half)
     Yg = f32_host(Y)
     Ug = f32_host(U)
     if rows is not None:
@@ -124,9 +126,10 @@ def _check_fwd(pb: Problem, rows=None):
 
 def _check_bwd(pb: Problem, U, rows=None):
     p = pb.p
-    dX, dA, dB = qn.qlora_linear_bwd(pb.dYd, pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale, U)
-    dXo, _ = oracle.lora_dx(pb.dY, pb.Wd, pb.A, pb.B, p.scale, rows)
-    dAo, dBo = oracle.lora_dadb(pb.dY, pb.X, pb.A, pb.B, p.scale)
+    bwd = qn.qlora_linear_bwd_f16 if pb.half else qn.qlora_linear_bwd
+    dX, dA, dB = bwd(pb.dYd, pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale, U)
+    dXo, _ = oracle.lora_dx(pb.dY, pb.Wd, pb.A, pb.B, p.scale, rows, f16=pb.half)
+    dAo, dBo = oracle.lora_dadb(pb.dY, pb.X, pb.A, pb.B, p.scale, f16=pb.half)
     dXg = f32_host(dX)
     if rows is not None:
         dXg = dXg[rows]
@@ -474,3 +477,75 @@ def test_config2_fp8_second_level():
 def test_config4_decode_fp8_second_level(M):
     pb = Problem(wl.config4(M), fp8_second_level=True)
     _check_fwd(pb)
+
+
+# ------------------------------------------------------------------ fp16 compute type
+# digipro.cn "QLoRA: Fine-Tuning a 7B Model on a 16GB GPU", "The QLoRA insight": the
+# compute-dtype flag dequantizes to fp16 for the matrix multiplies.
+@pytest.mark.parametrize("rows,cols", [(1, 1), (1, 17), (3, 333), (256, 256), (4096, 4096)])
+def test_dequantize_f16_bit_exact(rows, cols):
+    W = wl.weight((rows, cols), seed=rows * 5 + cols, sigma=0.02, outlier_frac=0.001)
+    W.reshape(-1)[:128] *= 2.0 ** -14   # two blocks whose weights are binary16 subnormals
+    o = oracle.quantize(W)
+    got = bits_host(qn.nf4_dequantize_f16(upload_oracle_tensor(o, rows, cols))).reshape(-1)
+    assert np.array_equal(got, oracle.dequantize(o, f16=True))
+    for dq, fp8 in ((False, False), (True, True)):
+        q = qn.nf4_quantize(torch.from_numpy(W).cuda(), double_quant=dq, fp8_second_level=fp8)
+        o = oracle.quantize(W, fp8=fp8)
+        want = oracle.dequantize(o, f16=True) if dq else oracle.dequantize_nodq(o, f16=True)
+        out = qn.nf4_dequantize_f16(q)
+        assert out.dtype == torch.float16
+        assert np.array_equal(bits_host(out).reshape(-1), want)
+
+
+def test_dequantize_f16_decode_tensor_bit_exact():
+    W = wl.config4(1).W()
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda())
+    got = bits_host(qn.nf4_dequantize_f16(q)).reshape(-1)
+    assert np.array_equal(got, oracle.dequantize(oracle.quantize(W), f16=True))
+
+
+@pytest.mark.parametrize("name,M,N,K,r,alpha", [s for s in SMALL if s[0] in
+                                                ("cfg1", "ragged", "rank72", "rank128",
+                                                 "tokens17", "tokens1", "tokens5",
+                                                 "multi_tile", "rank12", "tokens9_rank13")])
+def test_fwd_bwd_f16(name, M, N, K, r, alpha):
+    p = wl.LinearProblem(name, M, N, K, r, alpha, 0.02, 0.001, config=90 + len(name))
+    pb = Problem(p, half=True)
+    Y, U = _check_fwd(pb)
+    _check_bwd(pb, U)
+    _check_bwd(pb, None)
+
+
+@pytest.mark.parametrize("variant", ["nodq", "fp8"])
+def test_fwd_bwd_f16_format_variants(variant):
+    p = wl.LinearProblem(f"f16-{variant}", 200, 320, 448, 16, 32.0, 0.02, 0.001, config=93)
+    pb = Problem(p, double_quant=variant != "nodq", fp8_second_level=variant == "fp8",
+                 half=True)
+    Y, U = _check_fwd(pb)
+    _check_bwd(pb, U)
+    p1 = wl.LinearProblem(f"f16-{variant}-decode", 4, 576, 320, 8, 16.0, 0.02, 0.001, config=94)
+    _check_fwd(Problem(p1, double_quant=variant != "nodq", fp8_second_level=variant == "fp8",
+                       half=True))
+
+
+def test_config2_f16():
+    pb = Problem(wl.config2(), half=True)
+    rows = _sample_rows(pb.p.M)
+    Y, U = _check_fwd(pb, rows)
+    _check_bwd(pb, U, rows)
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_config4_decode_f16(M):
+    pb = Problem(wl.config4(M), half=True)
+    _check_fwd(pb)
+
+
+def test_f16_and_bf16_entry_points_refuse_each_others_dtype():
+    pb = Problem(wl.config1(), half=True)
+    with pytest.raises(ValueError):
+        qn.qlora_linear_fwd(pb.Xd, pb.qd, pb.Ad, pb.Bd, pb.p.scale)
+    pbb = Problem(wl.config1())
+    with pytest.raises(ValueError):
+        qn.qlora_linear_fwd_f16(pbb.Xd, pbb.qd, pbb.Ad, pbb.Bd, pbb.p.scale)
