@@ -85,6 +85,47 @@ def test_host_validation_without_device(lib):
     assert lib.qlora_status_str(-4).decode() == "workspace too small"
 
 
+def test_f16_entry_points_validate_like_the_bf16_ones(lib):
+    """The fp16 compute-type entry points share the bf16 ones' host validation: the same
+    status for the same bad argument, before any device work."""
+    S = _binding._NF4Struct
+    good = S(16, 32, 48, 64, 256, 256, 64, 256)
+    for f in (lib.nf4_dequantize, lib.nf4_dequantize_f16):
+        assert f(ctypes.byref(S(16, 32, 48, 64, 256, 256, 32, 256)), 16, None) == -2
+        assert f(ctypes.byref(S(17, 32, 48, 64, 256, 256, 64, 256)), 16, None) == -3
+        assert f(ctypes.byref(good), 24, None) == -3
+        assert f(ctypes.byref(good), 16, None) in (-7, 0)
+    bad_shape = S(16, 32, 48, 64, 250, 256, 64, 256)
+    f32 = ctypes.c_float
+    for fwd in (lib.qlora_linear_fwd, lib.qlora_linear_fwd_f16):
+        assert fwd(16, 16, ctypes.byref(bad_shape), 16, 16, 8, f32(2.0), 16, None, 16, 1 << 30,
+                   None) == -2
+        assert fwd(16, 16, ctypes.byref(good), 16, 16, 129, f32(2.0), 16, None, 16, 1 << 30,
+                   None) == -2                                   # rank above 128
+        assert fwd(16, 16, ctypes.byref(good), 16, 16, 8, f32(float("nan")), 16, None, 16,
+                   1 << 30, None) == -1                          # NaN scale
+        assert fwd(24, 16, ctypes.byref(good), 16, 16, 8, f32(2.0), 16, None, 16, 1 << 30,
+                   None) == -3                                   # X not 16-byte aligned
+        assert fwd(16, 16, ctypes.byref(good), 16, 16, 8, f32(2.0), 16, None, 16, 1, None) == -4
+    for bwd in (lib.qlora_linear_bwd, lib.qlora_linear_bwd_f16):
+        assert bwd(16, 16, 16, ctypes.byref(bad_shape), 16, 16, 8, f32(2.0), None, 16, 16, 16,
+                   16, 1 << 30, None) == -2
+        assert bwd(16, 16, 16, ctypes.byref(good), 16, 16, 8, f32(2.0), None, 16, None, 16,
+                   16, 1 << 30, None) == -1                      # dA missing
+        assert bwd(16, 16, 16, ctypes.byref(good), 16, 16, 8, f32(2.0), None, 16, 16, 16,
+                   16, 1, None) == -4
+
+
+def test_f16_wrappers_refuse_host_tensors():
+    import torch
+    q = qn.NF4Tensor.__new__(qn.NF4Tensor)  # never reaches the library
+    x = torch.zeros(4, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        qn.qlora_linear_fwd_f16(x, q, x, x, 1.0)       # host tensors
+    with pytest.raises(ValueError):
+        qn.qlora_linear_bwd_f16(x, x, q, x, x, 1.0)
+
+
 def test_workspace_grows_with_problem(lib):
     a = qn.qlora_workspace_bytes(16, 256, 256, 8)
     b = qn.qlora_workspace_bytes(4096, 4096, 4096, 16)
