@@ -1,6 +1,6 @@
 // linear.cu -- orchestration of the LoRA-wrapped NF4 linear layer.
 //
-// forward   pad adapters -> U = X A^T (sU = bf16(s U)) -> fused GEMM (M > 16) or the decode
+// forward   pad adapters -> U = X A^T (sU = 16-bit(s U)) -> fused GEMM (M > 16) or the decode
 //           kernel (M <= 16)
 // backward  U (saved or recomputed) -> V = dY B (sV) -> fused input-gradient GEMM, with
 //           dB = s dY^T U and dA = (X^T sV)^T on a side stream meanwhile

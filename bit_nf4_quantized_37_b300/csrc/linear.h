@@ -43,13 +43,14 @@ struct LinearArgs {
   bool half;
 };
 
-// Workspace regions (byte offsets, each 1024-aligned), for rank padded to rp = 64*ceil(r/64).
+// Workspace regions (byte offsets, each 1024-aligned), for rank padded to rp = 64*ceil(r/64);
+// the 16-bit regions hold bf16, or fp16 in the fp16 compute type.
 struct WorkspaceLayout {
   int64_t rp;
-  uint64_t sU;       // bf16 [M, rp]  scale * U (columns past r: read as TMA zero fill)
-  uint64_t sV;       // bf16 [M, rp]  scale * V (the same)
+  uint64_t sU;       // 16-bit [M, rp]  scale * U (columns past r: read as TMA zero fill)
+  uint64_t sV;       // 16-bit [M, rp]  scale * V (the same)
   uint64_t U32;      // fp32 [M, r]   U recomputed by the backward when none is saved
-  uint64_t Bp;       // bf16 [N, rp]  B zero-padded (only for r not a multiple of 8)
+  uint64_t Bp;       // 16-bit [N, rp]  B zero-padded (only for r not a multiple of 8)
   uint64_t part;     // fp32 split-contraction partial sums (side products, decode path)
   uint64_t part_bytes;
   uint64_t tickets;  // int [ntickets] arrival counters of the split reductions
@@ -71,7 +72,7 @@ int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t
 int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 // Decode path (M <= 16): Y = X W'^T + sU Bp^T with the weights streamed once.
 int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
-// Its two parts: sU = bf16(scale X A^T) (small_u), and the GEMV, which forms the LoRA term
+// Its two parts: sU = 16-bit(scale X A^T) (small_u), and the GEMV, which forms the LoRA term
 // from sU and B on the tensor cores, or adds a precomputed fp32 term Z when Z is not null.
 int launch_skinny_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const float* Z,
