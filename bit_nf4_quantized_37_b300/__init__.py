@@ -33,6 +33,7 @@ from ._binding import (  # noqa: F401
     qlora_linear_fwd_multi,
     qlora_workspace_bytes,
     status_str,
+    wait_timeout_selftest,
 )
 
 __all__ = [
@@ -41,5 +42,5 @@ __all__ = [
     "nf4_quantize_noalloc", "nf4_quantize_workspace_bytes", "nf4_storage_bytes",
     "profile_start", "profile_stop", "qlora_linear_bwd", "qlora_linear_bwd_f16",
     "qlora_linear_fwd", "qlora_linear_fwd_f16", "qlora_linear_fwd_multi",
-    "qlora_workspace_bytes", "status_str",
+    "qlora_workspace_bytes", "status_str", "wait_timeout_selftest",
 ]

@@ -26,7 +26,7 @@ EXPORTS = ["nf4_storage_bytes", "nf4_quantize_workspace_bytes", "nf4_quantize",
            "qlora_profile_start", "qlora_profile_stop", "nf4_quantize_noalloc",
            "nf4_merge_lora", "nf4_int4_error_workspace_bytes", "nf4_int4_error_stats",
            "qlora_linear_fwd_multi", "nf4_dequantize_f16", "qlora_linear_fwd_f16",
-           "qlora_linear_bwd_f16"]
+           "qlora_linear_bwd_f16", "qlora_wait_timeout_selftest"]
 
 
 class QLoRAError(RuntimeError):
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
                                      vp, vp, ctypes.c_uint64, vp],
             "nf4_level_table": [vp, vp],
             "qlora_device_status": [vp, vp],
+            "qlora_wait_timeout_selftest": [vp],
             "qlora_status_str": [ctypes.c_int],
             "qlora_version": [],
             "qlora_profile_start": [],
@@ -384,6 +385,13 @@ def profile_stop() -> dict:
     _check("qlora_profile_stop", lib().qlora_profile_stop(buf, cap, ctypes.byref(n)))
     return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
             for i in range(min(n.value, cap))}
+
+
+def wait_timeout_selftest() -> None:
+    """Enqueue the bounded-wait self-test on the current stream: one wait that nothing
+    completes, which gives up after its limit (about 2 s) and sets wait code 8; read it with
+    device_status()."""
+    _check("qlora_wait_timeout_selftest", lib().qlora_wait_timeout_selftest(_stream()))
 
 
 def device_status() -> int:

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libqlora_nf4.so")
 SOURCES = ["api.cu", "linear.cu", "nf4_codec.cu", "umma_gemm.cu", "lora_side.cu", "skinny.cu",
            "tensormap.cu", "profile.cu",
-           "noalloc.cu", "merge.cu", "multi.cu"]
+           "noalloc.cu", "merge.cu", "multi.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

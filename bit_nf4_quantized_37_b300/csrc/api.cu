@@ -278,13 +278,21 @@ int qlora_device_status(int32_t* out, void* stream) {
   int v = 0;
   if (cudaStreamSynchronize(s) != cudaSuccess) return QLORA_ERR_CUDA;
   if ((st = read_and_clear_gemm_error(&v))) return st;
-  int w = 0, d = 0;
+  int w = 0, d = 0, t = 0;
   if ((st = read_and_clear_side_error(&w))) return st;
   if ((st = read_and_clear_decode_error(&d))) return st;
+  if ((st = read_and_clear_selftest_error(&t))) return st;
   if (!v) v = w;
   if (!v) v = d;
+  if (!v) v = t;
   *out = v;
   return v ? QLORA_ERR_DEVICE_TIMEOUT : QLORA_OK;
+}
+
+int qlora_wait_timeout_selftest(void* stream) {
+  const int st = check_device();
+  if (st) return st;
+  return launch_wait_selftest(static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

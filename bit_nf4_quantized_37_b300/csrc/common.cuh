@@ -24,6 +24,7 @@ enum WaitSite : int {
   kWaitLora = 5,
   kWaitPeer = 6,
   kWaitLayout = 7,  // not a wait: the shared window does not fit a kernel's fixed layout
+  kWaitSelftest = 8,  // the wait self-test (qlora_wait_timeout_selftest) ran out, as it must
 };
 
 // ~2 s of wall time, far beyond any legitimate wait in these kernels (< 10 ms each).

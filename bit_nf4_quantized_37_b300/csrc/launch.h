@@ -18,6 +18,10 @@ int read_and_clear_gemm_error(int* out);
 int read_and_clear_side_error(int* out);
 // Reads and clears the decode kernel's device error word (skinny.cu).
 int read_and_clear_decode_error(int* out);
+// Reads and clears the wait self-test's device error word, and launches that self-test: one
+// bounded wait on an mbarrier nothing arrives on (selftest.cu).
+int read_and_clear_selftest_error(int* out);
+int launch_wait_selftest(cudaStream_t stream);
 
 // Quantize / dequantize (nf4_codec.cu).
 uint64_t quantize_workspace_bytes(int64_t numel);

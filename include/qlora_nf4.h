@@ -273,11 +273,23 @@ int nf4_level_table(float levels[16], float thresholds[15]);
 /*
  * Reads and clears the device error word that kernels set when a bounded wait on an
  * mbarrier gives up (instead of hanging).  Synchronizes `stream`.  *out = 0 when clean,
- * else a nonzero code naming the wait (1..6), or 7 when the decode kernel found a shared
- * window that its fixed layout does not fit and returned without work.  Returns
- * QLORA_ERR_DEVICE_TIMEOUT if it was set.
+ * else a nonzero code naming the wait (1..6), 7 when the decode kernel found a shared
+ * window that its fixed layout does not fit and returned without work, or 8 after
+ * qlora_wait_timeout_selftest.  Returns QLORA_ERR_DEVICE_TIMEOUT if it was set.
  */
 int qlora_device_status(int32_t* out, void* stream);
+
+/*
+ * Self-test of the bounded waits (the pages have no counterpart; every kernel here waits on
+ * mbarriers for its TMA copies and stages, and a wait that never completes must end in a
+ * status, not a hang).  Enqueues on `stream` one CTA that waits, with the same bounded wait
+ * the kernels use, on an mbarrier that nothing ever arrives on.  After the wait limit (about
+ * 2 s) the wait gives up, records code 8 in the device error word and the kernel returns; the
+ * device and its context stay usable.  The next qlora_device_status returns
+ * QLORA_ERR_DEVICE_TIMEOUT with *out = 8 and clears the word.  Returns QLORA_OK once the
+ * kernel is enqueued, QLORA_ERR_NO_DEVICE without a compute-capability 10.3 device.
+ */
+int qlora_wait_timeout_selftest(void* stream);
 
 /*
  * Opt-in per-kernel device timing (host only; a measurement aid, not thread-safe).

@@ -83,6 +83,10 @@ def test_host_validation_without_device(lib):
     st = lib.nf4_dequantize(ctypes.byref(good), 16, None)
     assert st in (-7, 0)
     assert lib.qlora_status_str(-4).decode() == "workspace too small"
+    # the wait self-test needs a device; without one it answers at once
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.qlora_wait_timeout_selftest(None) == -7
 
 
 def test_f16_entry_points_validate_like_the_bf16_ones(lib):
