@@ -42,6 +42,64 @@ int check_tensor(const nf4_tensor* q) {
   return QLORA_OK;
 }
 
+// The bf16 and fp16 entry points share their validation and launch; `half` selects the
+// 16-bit type of the activations, adapters and outputs.
+int dequantize_impl(const nf4_tensor* q, uint16_t* W_out, bool half, void* stream) {
+  int st = check_tensor(q);
+  if (st) return st;
+  if (!W_out) return QLORA_ERR_INVALID_ARG;
+  if (!aligned16(W_out)) return QLORA_ERR_MISALIGNED;
+  if ((st = check_device())) return st;
+  return launch_dequantize(*q, q->rows * q->cols, W_out, half,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int linear_fwd_impl(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const uint16_t* A,
+                    const uint16_t* B, int32_t r, float scale, uint16_t* Y, float* U_save,
+                    void* ws, uint64_t ws_bytes, bool half, void* stream) {
+  int st = check_tensor(Wq);
+  if (st) return st;
+  if (!X || !A || !B || !Y || !ws || M < 1 || r < 1) return QLORA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return QLORA_ERR_INVALID_ARG;
+  if (r > kMaxRank) return QLORA_ERR_UNSUPPORTED;
+  const int64_t N = Wq->rows, K = Wq->cols;
+  if (N % 64 != 0 || K % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(Y) || !aligned16(ws) ||
+      (U_save && !aligned16(U_save)))
+    return QLORA_ERR_MISALIGNED;
+  if (ws_bytes < linear_workspace_bytes(M, N, K, r)) return QLORA_ERR_WORKSPACE;
+  if ((st = check_device())) return st;
+  LinearArgs a{};
+  a.M = M; a.N = N; a.K = K; a.r = r; a.scale = scale;
+  a.X = X; a.A = A; a.B = B; a.Y = Y; a.U = U_save; a.q = *Wq;
+  a.ws = ws; a.ws_bytes = ws_bytes; a.half = half;
+  return linear_forward(a, static_cast<cudaStream_t>(stream));
+}
+
+int linear_bwd_impl(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
+                    const uint16_t* A, const uint16_t* B, int32_t r, float scale,
+                    const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,
+                    uint64_t ws_bytes, bool half, void* stream) {
+  int st = check_tensor(Wq);
+  if (st) return st;
+  if (!dY || !X || !A || !B || !dA || !dB || !ws || M < 1 || r < 1) return QLORA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return QLORA_ERR_INVALID_ARG;
+  if (r > kMaxRank) return QLORA_ERR_UNSUPPORTED;
+  const int64_t N = Wq->rows, K = Wq->cols;
+  if (N % 64 != 0 || K % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (!aligned16(dY) || !aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(dA) ||
+      !aligned16(dB) || !aligned16(ws) || (dX && !aligned16(dX)) ||
+      (U_saved && !aligned16(U_saved)))
+    return QLORA_ERR_MISALIGNED;
+  if (ws_bytes < linear_workspace_bytes(M, N, K, r)) return QLORA_ERR_WORKSPACE;
+  if ((st = check_device())) return st;
+  LinearArgs a{};
+  a.M = M; a.N = N; a.K = K; a.r = r; a.scale = scale;
+  a.X = X; a.A = A; a.B = B; a.dY = dY; a.dX = dX; a.dA = dA; a.dB = dB;
+  a.U_in = U_saved; a.q = *Wq; a.ws = ws; a.ws_bytes = ws_bytes; a.half = half;
+  return linear_backward(a, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -104,18 +162,6 @@ int nf4_quantize(const float* W, const nf4_tensor* out, void* workspace,
   return launch_quantize(W, numel, *out, workspace, static_cast<cudaStream_t>(stream));
 }
 
-namespace {
-int dequantize_impl(const nf4_tensor* q, uint16_t* W_out, bool half, void* stream) {
-  int st = check_tensor(q);
-  if (st) return st;
-  if (!W_out) return QLORA_ERR_INVALID_ARG;
-  if (!aligned16(W_out)) return QLORA_ERR_MISALIGNED;
-  if ((st = check_device())) return st;
-  return launch_dequantize(*q, q->rows * q->cols, W_out, half,
-                           static_cast<cudaStream_t>(stream));
-}
-}  // namespace
-
 int nf4_dequantize(const nf4_tensor* q, uint16_t* W_out, void* stream) {
   return dequantize_impl(q, W_out, false, stream);
 }
@@ -166,30 +212,6 @@ int qlora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r, uint64_t* 
   return QLORA_OK;
 }
 
-namespace {
-int linear_fwd_impl(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const uint16_t* A,
-                    const uint16_t* B, int32_t r, float scale, uint16_t* Y, float* U_save,
-                    void* ws, uint64_t ws_bytes, bool half, void* stream) {
-  int st = check_tensor(Wq);
-  if (st) return st;
-  if (!X || !A || !B || !Y || !ws || M < 1 || r < 1) return QLORA_ERR_INVALID_ARG;
-  if (!(scale == scale)) return QLORA_ERR_INVALID_ARG;
-  if (r > kMaxRank) return QLORA_ERR_UNSUPPORTED;
-  const int64_t N = Wq->rows, K = Wq->cols;
-  if (N % 64 != 0 || K % 64 != 0) return QLORA_ERR_UNSUPPORTED;
-  if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(Y) || !aligned16(ws) ||
-      (U_save && !aligned16(U_save)))
-    return QLORA_ERR_MISALIGNED;
-  if (ws_bytes < linear_workspace_bytes(M, N, K, r)) return QLORA_ERR_WORKSPACE;
-  if ((st = check_device())) return st;
-  LinearArgs a{};
-  a.M = M; a.N = N; a.K = K; a.r = r; a.scale = scale;
-  a.X = X; a.A = A; a.B = B; a.Y = Y; a.U = U_save; a.q = *Wq;
-  a.ws = ws; a.ws_bytes = ws_bytes; a.half = half;
-  return linear_forward(a, static_cast<cudaStream_t>(stream));
-}
-}  // namespace
-
 int qlora_linear_fwd(const uint16_t* X, int64_t M, const nf4_tensor* Wq, const uint16_t* A,
                      const uint16_t* B, int32_t r, float scale, uint16_t* Y, float* U_save,
                      void* ws, uint64_t ws_bytes, void* stream) {
@@ -227,32 +249,6 @@ int qlora_linear_fwd_multi(const uint16_t* X, int64_t M, const nf4_tensor* Wq,
   a.adapter_idx = adapter_idx; a.n_adapters = n_adapters; a.scales = scales;
   return linear_forward(a, static_cast<cudaStream_t>(stream));
 }
-
-namespace {
-int linear_bwd_impl(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
-                    const uint16_t* A, const uint16_t* B, int32_t r, float scale,
-                    const float* U_saved, uint16_t* dX, float* dA, float* dB, void* ws,
-                    uint64_t ws_bytes, bool half, void* stream) {
-  int st = check_tensor(Wq);
-  if (st) return st;
-  if (!dY || !X || !A || !B || !dA || !dB || !ws || M < 1 || r < 1) return QLORA_ERR_INVALID_ARG;
-  if (!(scale == scale)) return QLORA_ERR_INVALID_ARG;
-  if (r > kMaxRank) return QLORA_ERR_UNSUPPORTED;
-  const int64_t N = Wq->rows, K = Wq->cols;
-  if (N % 64 != 0 || K % 64 != 0) return QLORA_ERR_UNSUPPORTED;
-  if (!aligned16(dY) || !aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(dA) ||
-      !aligned16(dB) || !aligned16(ws) || (dX && !aligned16(dX)) ||
-      (U_saved && !aligned16(U_saved)))
-    return QLORA_ERR_MISALIGNED;
-  if (ws_bytes < linear_workspace_bytes(M, N, K, r)) return QLORA_ERR_WORKSPACE;
-  if ((st = check_device())) return st;
-  LinearArgs a{};
-  a.M = M; a.N = N; a.K = K; a.r = r; a.scale = scale;
-  a.X = X; a.A = A; a.B = B; a.dY = dY; a.dX = dX; a.dA = dA; a.dB = dB;
-  a.U_in = U_saved; a.q = *Wq; a.ws = ws; a.ws_bytes = ws_bytes; a.half = half;
-  return linear_backward(a, static_cast<cudaStream_t>(stream));
-}
-}  // namespace
 
 int qlora_linear_bwd(const uint16_t* dY, const uint16_t* X, int64_t M, const nf4_tensor* Wq,
                      const uint16_t* A, const uint16_t* B, int32_t r, float scale,
