@@ -421,8 +421,13 @@ def main():
     secondary = {} if args.no_secondary else measure_secondary(qn, wl, dev, peaks, traffic,
                                                                l2_flush)
     if not args.no_secondary:
+        with_cpu = rank == 0 and not args.no_cpu
         secondary.update(measure_merge_and_error(qn, wl, p, q, A, B, dev, peaks, l2_flush))
         secondary.update(measure_f16(qn, p, q, X, A, B, dY, peaks, l2_flush))
+        secondary["config3_mlp_M2048"] = measure_config3(qn, wl, dev, peaks, l2_flush, with_cpu)
+        secondary["config5_llama7b_stack"] = measure_config5(qn, wl, dev, peaks, l2_flush, with_cpu)
+        if with_cpu:
+            add_cpu_secondary(secondary, wl)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -536,6 +541,181 @@ def measure_f16(qn, p, q, X, A, B, dY, peaks, l2_flush):
     tf = p.fwd_bwd_flops() / ms / 1e9
     return {"fwd_bwd_f16_4096x4096x4096_r16": {
         "TFLOP/s": tf, "frac_tensor": tf / peaks["bf16_tflops"], "ms": ms}}
+
+
+def profiled(qn, fn, l2_flush, reps: int = 10):
+    """Whole-call device time (graph_timed_ms) and the library's per-kernel mean device times
+    from a second graph of the same calls with the profiling events."""
+    import torch
+    ms = graph_timed_ms(fn, l2_flush, reps)
+    qn.profile_start()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        for _ in range(reps):
+            l2_flush()
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    prof = qn.profile_stop()
+    return ms, {k: v[1] / reps for k, v in prof.items()}
+
+
+def fused_fracs(p, kms, peaks):
+    """TFLOP/s and fraction of the bf16 burst peak of the two fused GEMMs of one fwd + bwd."""
+    out = {}
+    flops = {"fused_fwd_gemm": 2.0 * p.M * p.N * p.K + 2.0 * p.M * p.N * p.r,
+             "fused_dx_gemm": 2.0 * p.M * p.N * p.K + 2.0 * p.M * p.K * p.r}
+    for k, f in flops.items():
+        if k in kms and kms[k] > 0:
+            a = f / kms[k] / 1e9
+            out[k] = {"ms": kms[k], "TFLOP/s": a, "frac_bf16_burst": a / peaks["bf16_tflops"]}
+    return out
+
+
+def oracle_quantize_sample(W: np.ndarray, target_s: float = 3.0):
+    """The oracle's quantize on leading rows of W (about target_s of CPU time): GB/s of
+    algorithmic bytes (4 B read + 0.516 B written per weight) and the sample's text."""
+    import oracle
+    rows = max(1, min(W.shape[0], int(2e6 // W.shape[1])))
+    t0 = time.perf_counter()
+    oracle.quantize(W[:rows])
+    dt = time.perf_counter() - t0
+    rows = max(1, min(W.shape[0], int(rows * target_s / max(dt, 1e-6))))
+    t0 = time.perf_counter()
+    oracle.quantize(W[:rows])
+    dt = time.perf_counter() - t0
+    n = rows * W.shape[1]
+    return {"GB/s": n * 4.51587 / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"quantize of {rows} x {W.shape[1]} weights in {dt:.1f} s (one thread: the "
+                      "oracle's quantize has no parallel loop)"}
+
+
+def measure_config3(qn, wl, dev, peaks, l2_flush, with_cpu: bool):
+    """The 7B MLP projections (gate / up 11008 x 4096, down 4096 x 11008, 0.1% Student-t
+    outliers), M = 2048 tokens, r = 16: fwd + bwd of each, TFLOP/s against the bf16 burst."""
+    import torch
+    out = {}
+    tot_ms = tot_flops = 0.0
+    cpu_s = cpu_flops = 0.0
+    cpu_desc = []
+    cores = None
+    for p in wl.config3():
+        W = p.W()
+        q = qn.nf4_quantize(torch.from_numpy(W).to(dev))
+        Xh, Ah, Bh, dYh = p.X(), p.A(), p.B(), p.dY()
+        X, A, B, dY = (bf16_dev(t, dev) for t in (Xh, Ah, Bh, dYh))
+
+        def step():
+            Y, U = qn.qlora_linear_fwd(X, q, A, B, p.scale)
+            qn.qlora_linear_bwd(dY, X, q, A, B, p.scale, U)
+
+        ms, kms = profiled(qn, step, l2_flush)
+        f = p.fwd_bwd_flops()
+        tf = f / ms / 1e9
+        out[p.name] = {"ms": ms, "TFLOP/s": tf, "frac_bf16_burst": tf / peaks["bf16_tflops"],
+                       "gemms": fused_fracs(p, kms, peaks), "kernels_ms": kms}
+        tot_ms += ms
+        tot_flops += f
+        if with_cpu:
+            import oracle
+            Wd = oracle.dequantize(oracle.quantize(W)).reshape(p.N, p.K)
+            v, desc, cores, secs = oracle_sample(p, Xh, Wd, Ah, Bh, dYh, target_s=6.0)
+            cpu_s += secs
+            cpu_flops += v * 1e12 * secs
+            cpu_desc.append(desc)
+        del q, X, A, B, dY
+    tf = tot_flops / tot_ms / 1e9
+    out["total_3_projections"] = {"ms": tot_ms, "TFLOP/s": tf,
+                                  "frac_bf16_burst": tf / peaks["bf16_tflops"],
+                                  "target_ms_at_60pct": tot_flops / (0.6 * peaks["bf16_tflops"]) / 1e9}
+    if with_cpu:
+        out["cpu_oracle"] = {"value": cpu_flops / cpu_s / 1e12, "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": "; ".join(cpu_desc)}
+    return out
+
+
+def measure_config5(qn, wl, dev, peaks, l2_flush, with_cpu: bool):
+    """The 32-layer Llama-7B-shaped stack, all-linear LoRA r = 16: nf4_quantize of all 224
+    weight matrices (6.48 G weights, fp32 resident on the device), then forward + backward of
+    every projection of every layer at M = 512 tokens (the seeded inputs of layer 0's
+    projections, shared by the layers), each timed as one CUDA graph of the whole stack."""
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+    hbm = peaks["hbm_gbs"]
+    out = {}
+    Ws, qs = [], []
+    with ThreadPoolExecutor(8) as gen:
+        for layer in range(32):
+            projs = wl.config5(layer=layer)
+            for p, W in zip(projs, gen.map(lambda pp: pp.W(), projs)):
+                Ws.append(torch.from_numpy(W).to(dev))
+                qs.append(qn.NF4Tensor.empty(p.N, p.K, dev))
+    numel = sum(w.numel() for w in Ws)
+    nbytes = sum(4 * w.numel() + q.storage_bytes() for w, q in zip(Ws, qs))
+    ws = torch.empty(max(qn.nf4_quantize_workspace_bytes(w.numel()) for w in Ws),
+                     dtype=torch.uint8, device=dev)
+
+    def quantize_all():
+        for w, q in zip(Ws, qs):
+            qn.nf4_quantize(w, q, workspace=ws)
+
+    ms = graph_timed_ms(quantize_all, l2_flush, reps=3)
+    out["quantize_stack_224_matrices"] = {
+        "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm, "ms": ms,
+        "bytes": nbytes, "weights": numel}
+    if with_cpu:
+        out["quantize_stack_224_matrices"]["cpu_oracle"] = oracle_quantize_sample(
+            Ws[6].cpu().numpy(), target_s=3.0)
+    del Ws, ws
+    torch.cuda.empty_cache()
+
+    projs0 = wl.config5(layer=0)
+    ins = {}
+    for p in projs0:
+        ins[p.name.split("-")[-1]] = tuple(bf16_dev(t, dev) for t in (p.X(), p.A(), p.B(), p.dY()))
+    scale = projs0[0].scale
+
+    def layer_calls(layer):
+        for i, p in enumerate(projs0):
+            X, A, B, dY = ins[p.name.split("-")[-1]]
+            q = qs[7 * layer + i]
+            Y, U = qn.qlora_linear_fwd(X, q, A, B, scale)
+            qn.qlora_linear_bwd(dY, X, q, A, B, scale, U)
+
+    layer_flops = sum(p.fwd_bwd_flops() for p in projs0)
+    per_proj = {}
+    for i, p in enumerate(projs0):
+        X, A, B, dY = ins[p.name.split("-")[-1]]
+        q = qs[i]
+
+        def step(q=q, X=X, A=A, B=B, dY=dY):
+            Y, U = qn.qlora_linear_fwd(X, q, A, B, scale)
+            qn.qlora_linear_bwd(dY, X, q, A, B, scale, U)
+
+        pms, kms = profiled(qn, step, l2_flush)
+        tf = p.fwd_bwd_flops() / pms / 1e9
+        per_proj[p.name.split("-")[-1]] = {"ms": pms, "TFLOP/s": tf,
+                                           "frac_bf16_burst": tf / peaks["bf16_tflops"],
+                                           "gemms": fused_fracs(p, kms, peaks)}
+    out["layer_projections_M512"] = per_proj
+    sms = graph_timed_ms(lambda: [layer_calls(l) for l in range(32)], l2_flush, reps=2)
+    tf = 32 * layer_flops / sms / 1e9
+    out["stack_fwd_bwd_M512"] = {"ms": sms, "TFLOP/s": tf, "frac_bf16_burst": tf / peaks["bf16_tflops"],
+                                 "flops": 32 * layer_flops,
+                                 "note": "32 layers x 7 projections, forward then backward each, "
+                                         "one L2 flush per stack pass"}
+    if with_cpu:
+        import oracle
+        p = projs0[6]  # the down projection, the largest contraction
+        Xh, Ah, Bh, dYh = p.X(), p.A(), p.B(), p.dY()
+        Wd = oracle.dequantize(oracle.quantize(p.W())).reshape(p.N, p.K)
+        v, desc, cores, _ = oracle_sample(p, Xh, Wd, Ah, Bh, dYh, target_s=5.0)
+        out["stack_fwd_bwd_M512"]["cpu_oracle"] = {
+            "value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": "layer 0 down projection: " + desc}
+    del qs
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_secondary(qn, wl, dev, peaks, traffic, l2_flush, reps: int = 10):
@@ -657,6 +837,45 @@ def measure_secondary(qn, wl, dev, peaks, traffic, l2_flush, reps: int = 10):
         "GB/s": nbytes / ms_all / 1e6, "frac_hbm": nbytes / ms_all / 1e6 / hbm, "ms": ms_all,
         "bytes": nbytes, "kernels_ms": {k: v[1] / reps for k, v in prof.items()}}
     return out
+
+
+def add_cpu_secondary(secondary, wl):
+    """The oracle beside the HBM-bound lines on the 28672 x 8192 weight: quantize and
+    dequantize on leading rows, the decode forward (M = 1 / 4 / 16) in full."""
+    import oracle
+    p4 = wl.config4(1)
+    W = p4.W()
+    qline = secondary.get("quantize_28672x8192")
+    if qline is not None:
+        qline["cpu_oracle"] = oracle_quantize_sample(W, target_s=3.0)
+    rows = 2048
+    o = oracle.quantize(W[:rows])
+    t0 = time.perf_counter()
+    Wd_part = oracle.dequantize(o)
+    dt = time.perf_counter() - t0
+    n = rows * p4.K
+    for key in ("dequantize_28672x8192", "dequantize_f16_28672x8192"):
+        if key in secondary:
+            secondary[key]["cpu_oracle"] = {
+                "GB/s": n * 2.51587 / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"dequantize of {rows} x {p4.K} weights in {dt:.2f} s (one thread)"}
+    del Wd_part
+    Wd = oracle.dequantize(oracle.quantize(W)).reshape(p4.N, p4.K)
+    for M in (1, 4, 16):
+        key = f"decode_fwd_M{M}"
+        if key not in secondary:
+            continue
+        pm = wl.config4(M)
+        X, A, B = pm.X(), pm.A(), pm.B()
+        t0 = time.perf_counter()
+        oracle.lora_fwd(X, Wd, A, B, pm.scale)
+        dt = time.perf_counter() - t0
+        nbytes = secondary[key]["bytes"]
+        secondary[key]["cpu_oracle"] = {
+            "GB/s": nbytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"the whole forward (Y for all {M} tokens) over the dequantized weight in "
+                      f"{dt:.2f} s; the same algorithmic bytes as the device line"}
 
 
 if __name__ == "__main__":

@@ -194,6 +194,40 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
     return buf
 
 
+def _shape(t, want: tuple, name: str):
+    """Raise ValueError unless t has exactly the shape `want` (checked before any launch: a
+    mismatched buffer would make a kernel read or write past its allocation)."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(want):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(want)}")
+
+
+def _numel(t, want: int, name: str):
+    if t is not None and t.numel() != want:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {want}")
+
+
+def _check_nf4(q: "NF4Tensor"):
+    """The NF4 buffers hold at least the sizes rows x cols needs in its format."""
+    if q.rows < 1 or q.cols < 1:
+        raise ValueError(f"NF4Tensor has shape ({q.rows}, {q.cols})")
+    sizes, _ = nf4_storage_bytes(q.rows, q.cols, q.dq_block)
+    need = [("codes", q.codes, sizes[0], 1), ("scale_codes", q.scale_codes, sizes[1], 1),
+            ("scale_steps", q.scale_steps, sizes[2], 4), ("scale_mean", q.scale_mean, sizes[3], 4)]
+    for name, t, nbytes, esz in need:
+        have = 0 if t is None else t.numel() * t.element_size()
+        if have < nbytes:
+            raise ValueError(f"NF4Tensor.{name} holds {have} bytes, its {q.rows} x {q.cols} "
+                             f"tensor needs {nbytes}")
+
+
+def _rank2(t, name: str):
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    return t.shape
+
+
 def _req(t: torch.Tensor, dtype, name: str):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -209,8 +243,11 @@ def nf4_quantize(W: torch.Tensor, out: NF4Tensor | None = None,
     """Quantize fp32 weights [rows, cols] (CUDA) to NF4 with double-quantized scales (int8, or
     E4M3 with fp8_second_level), or with fp32 block absmax scales when double_quant is False
     (an `out` tensor brings its own variant)."""
-    _req(W, torch.float32, "W")
     rows, cols = (W.shape[0], W.shape[1]) if W.dim() == 2 else (1, W.numel())
+    if out is not None:
+        _numel(W, out.rows * out.cols, "W")
+        _check_nf4(out)
+    _req(W, torch.float32, "W")
     q = out if out is not None else NF4Tensor.empty(rows, cols, W.device, double_quant,
                                                     fp8_second_level)
     nb = nf4_quantize_workspace_bytes(rows * cols)
@@ -225,6 +262,8 @@ def nf4_quantize_noalloc(W: torch.Tensor, out: NF4Tensor) -> NF4Tensor:
     """nf4_quantize for callers that must not allocate device memory: the output buffers
     are the caller's and the scratch is the library's fixed device array (up to
     NF4_NOALLOC_MAX_NUMEL weights).  Calls overlapping on the GPU race on that array."""
+    _numel(W, out.rows * out.cols, "W")
+    _check_nf4(out)
     _req(W, torch.float32, "W")
     s = out.c_struct()
     _check("nf4_quantize_noalloc", lib().nf4_quantize_noalloc(_ptr(W), ctypes.byref(s), _stream()))
@@ -232,6 +271,8 @@ def nf4_quantize_noalloc(W: torch.Tensor, out: NF4Tensor) -> NF4Tensor:
 
 
 def _dequantize(call: str, dtype, q: NF4Tensor, out: torch.Tensor | None) -> torch.Tensor:
+    _check_nf4(q)
+    _numel(out, q.rows * q.cols, "out")
     o = out if out is not None else torch.empty(q.rows, q.cols, dtype=dtype,
                                                 device=q.codes.device)
     _req(o, dtype, "out")
@@ -250,12 +291,25 @@ def nf4_dequantize_f16(q: NF4Tensor, out: torch.Tensor | None = None) -> torch.T
     return _dequantize("nf4_dequantize_f16", torch.float16, q, out)
 
 
+def _linear_shapes(X, q, A, B):
+    """(M, N, K, r) of a LoRA-wrapped linear call; ValueError on any mismatch with the NF4
+    base [N, K]: X [M, K], A [r, K], B [N, r]."""
+    _check_nf4(q)
+    M, K = _rank2(X, "X")
+    N = q.rows
+    if K != q.cols:
+        raise ValueError(f"X has {K} columns, the NF4 base has {q.cols}")
+    r = _rank2(A, "A")[0]
+    _shape(A, (r, K), "A")
+    _shape(B, (N, r), "B")
+    return M, N, K, r
+
+
 def _linear_fwd(call: str, dtype, X, q, A, B, scale, save_u, out):
+    M, N, K, r = _linear_shapes(X, q, A, B)
+    _shape(out, (M, N), "out")
     for t, n in ((X, "X"), (A, "A"), (B, "B")):
         _req(t, dtype, n)
-    M, K = X.shape
-    r = A.shape[0]
-    N = q.rows
     Y = out if out is not None else torch.empty(M, N, dtype=dtype, device=X.device)
     _req(Y, dtype, "out")
     U = torch.empty(M, r, dtype=torch.float32, device=X.device) if save_u else None
@@ -285,13 +339,23 @@ def qlora_linear_fwd_multi(X: torch.Tensor, q: NF4Tensor, A_all: torch.Tensor,
                            out: torch.Tensor | None = None) -> torch.Tensor:
     """Y_t = X_t W'^T + s_a (X_t A_a^T) B_a^T with a = adapter_idx[t], for M <= 16 tokens.
     A_all [n, r, K], B_all [n, N, r] bf16; adapter_idx int32 [M]; scales fp32 [n]."""
+    _check_nf4(q)
+    M, K = _rank2(X, "X")
+    N = q.rows
+    if K != q.cols:
+        raise ValueError(f"X has {K} columns, the NF4 base has {q.cols}")
+    if A_all.dim() != 3:
+        raise ValueError(f"A_all must be 3-D [n, r, K], got shape {tuple(A_all.shape)}")
+    n_ad, r, _ = A_all.shape
+    _shape(A_all, (n_ad, r, K), "A_all")
+    _shape(B_all, (n_ad, N, r), "B_all")
+    _shape(adapter_idx, (M,), "adapter_idx")
+    _shape(scales, (n_ad,), "scales")
+    _shape(out, (M, N), "out")
     for t, n in ((X, "X"), (A_all, "A_all"), (B_all, "B_all")):
         _req(t, torch.bfloat16, n)
     _req(adapter_idx, torch.int32, "adapter_idx")
     _req(scales, torch.float32, "scales")
-    M, K = X.shape
-    n_ad, r, _ = A_all.shape
-    N = q.rows
     Y = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=X.device)
     nb = qlora_workspace_bytes(M, N, K, r)
     ws = _workspace(nb, X.device)
@@ -303,13 +367,13 @@ def qlora_linear_fwd_multi(X: torch.Tensor, q: NF4Tensor, A_all: torch.Tensor,
 
 
 def _linear_bwd(call: str, dtype, dY, X, q, A, B, scale, U, need_dx):
+    M, N, K, r = _linear_shapes(X, q, A, B)
+    _shape(dY, (M, N), "dY")
+    _shape(U, (M, r), "U")
     for t, n in ((dY, "dY"), (X, "X"), (A, "A"), (B, "B")):
         _req(t, dtype, n)
     if U is not None:
         _req(U, torch.float32, "U")
-    M, K = X.shape
-    r = A.shape[0]
-    N = q.rows
     dX = torch.empty(M, K, dtype=dtype, device=X.device) if need_dx else None
     dA = torch.empty(r, K, dtype=torch.float32, device=X.device)
     dB = torch.empty(N, r, dtype=torch.float32, device=X.device)
@@ -341,14 +405,23 @@ def nf4_merge_lora(q: NF4Tensor, A: torch.Tensor, B: torch.Tensor, scale: float,
                    out: torch.Tensor | None = None, out_f32: torch.Tensor | None = None):
     """W_merged = bf16(W' + scale B A) for the NF4 base q, A [r, K], B [N, r] bf16.
     Returns (bf16 [N, K] or None, the same values as fp32 [N, K] or None)."""
+    _check_nf4(q)
+    r = _rank2(A, "A")[0]
+    _shape(A, (r, q.cols), "A")
+    _shape(B, (q.rows, r), "B")
+    _shape(out, (q.rows, q.cols), "out")
+    _shape(out_f32, (q.rows, q.cols), "out_f32")
     for t, n in ((A, "A"), (B, "B")):
         _req(t, torch.bfloat16, n)
-    r = A.shape[0]
     dev = q.codes.device
     o16 = out if out is not None else (
         torch.empty(q.rows, q.cols, dtype=torch.bfloat16, device=dev) if bf16 else None)
     o32 = out_f32 if out_f32 is not None else (
         torch.empty(q.rows, q.cols, dtype=torch.float32, device=dev) if f32 else None)
+    if o16 is not None:
+        _req(o16, torch.bfloat16, "out")
+    if o32 is not None:
+        _req(o32, torch.float32, "out_f32")
     s = q.c_struct()
     _check("nf4_merge_lora", lib().nf4_merge_lora(ctypes.byref(s), _ptr(A), _ptr(B), r,
                                                   float(scale), _ptr(o16), _ptr(o32), _stream()))

@@ -65,16 +65,22 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     objdir = os.path.join(HERE, "_build")
     os.makedirs(objdir, exist_ok=True)
+    def compile_one(src):
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
+        cmd = [nvcc(), *ARCH, *FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        return src, obj, r.returncode, f"$ {' '.join(cmd)}\n{r.stdout}{r.stderr}"
+
+    # the translation units are independent: compile them side by side
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max(1, min(len(SOURCES), os.cpu_count() or 1))) as ex:
+        results = list(ex.map(compile_one, SOURCES))
     objs = []
     logs = []
-    for src in SOURCES:
-        obj = os.path.join(objdir, src.replace(".cu", ".o"))
-        cmd = [nvcc(), *ARCH, *FLAGS, "-I", INCLUDE, "-dc" if False else "-c",
-               os.path.join(CSRC, src), "-o", obj]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        logs.append(f"$ {' '.join(cmd)}\n{r.stdout}{r.stderr}")
-        if r.returncode != 0:
-            sys.stderr.write(logs[-1])
+    for src, obj, rc, log in results:
+        logs.append(log)
+        if rc != 0:
+            sys.stderr.write(log)
             raise RuntimeError(f"nvcc failed on {src}")
         objs.append(obj)
     tmp = LIB + f".tmp{os.getpid()}"

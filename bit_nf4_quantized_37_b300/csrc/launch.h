@@ -6,11 +6,34 @@
 #include <stdint.h>
 
 #include "../../include/qlora_nf4.h"
+#include "device_cache.h"
 
 namespace qlora {
 
+// Device ordinal and id of its current context (the key of the per-device set-up caches).
+DeviceKey device_context_key();
+
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
+
+// Sets `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per
+// device and context; `cache` is the call site's own (one per kernel).
+template <typename Kernel>
+int ensure_dynamic_smem(DeviceCache<int>& cache, Kernel kernel, int bytes) {
+  int have = 0;
+  const int st = cache.get(device_context_key, &have, [&](int* v) -> int {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return QLORA_ERR_CUDA;
+    }
+    *v = bytes;
+    return QLORA_OK;
+  });
+  if (st == -1) return QLORA_ERR_NO_DEVICE;
+  if (st) return st;
+  return have >= bytes ? QLORA_OK : QLORA_ERR_CUDA;
+}
 
 // Reads and clears the fused GEMMs' device error word (umma_gemm.cu).
 int read_and_clear_gemm_error(int* out);

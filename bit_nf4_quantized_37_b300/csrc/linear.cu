@@ -65,9 +65,11 @@ int linear_forward(const LinearArgs& a, cudaStream_t stream) {
 
 namespace {
 
-// Side stream and fork / join events of the calling host thread on the current device.
+// Side stream and fork / join events of the calling host thread on the current device
+// (and its context: after a context is created again they are created again).
 struct SideContext {
   int device = -1;
+  uint64_t context = 0;
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   int prio_hi = 0;
@@ -79,11 +81,17 @@ struct SideContext {
 };
 
 SideContext* side_context() {
-  thread_local SideContext ctx[8];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8) return nullptr;
+  thread_local SideContext ctx[kMaxCachedDevices];
+  const DeviceKey k = device_context_key();
+  const int dev = k.device;
+  if (dev < 0 || dev >= kMaxCachedDevices) return nullptr;
   SideContext& c = ctx[dev];
-  if (c.device == dev) return &c;
+  if (c.device == dev && k.context != 0 && c.context == k.context) return &c;
+  if (c.device == dev) {  // handles of a context that no longer exists: drop, do not destroy
+    c.side = nullptr;
+    c.fork = c.join = nullptr;
+    c.device = -1;
+  }
   int least = 0, greatest = 0;
   if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
       cudaStreamCreateWithPriority(&c.side, cudaStreamNonBlocking, least) != cudaSuccess ||
@@ -94,6 +102,7 @@ SideContext* side_context() {
   }
   c.prio_hi = greatest;
   c.device = dev;
+  c.context = device_context_key().context;  // the calls above created it if it was missing
   return &c;
 }
 

@@ -455,12 +455,10 @@ int run_side_t(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_
 #define QLORA_SIDE_CASE(nj)                                                                       \
   case nj:                                                                                        \
     {                                                                                             \
-      static bool attr = false; /* once per instantiation: the largest configuration */          \
-      if (!attr)                                                                                  \
-        attr = cudaFuncSetAttribute(side::side_gemm<kCol, nj, H>,                                  \
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,                  \
-                                    side::STAGES * side::P_STAGE_BYTES + side::Q_SMEM_MAX + 1024) \
-               == cudaSuccess;                                                                    \
+      static DeviceCache<int> attr; /* per instantiation and device: the largest configuration */ \
+      const int st = ensure_dynamic_smem(attr, side::side_gemm<kCol, nj, H>,                      \
+                                         side::STAGES * side::P_STAGE_BYTES + side::Q_SMEM_MAX + 1024); \
+      if (st) return st;                                                                          \
     }                                                                                             \
     side::side_gemm<kCol, nj, H><<<grid, side::THREADS, smem, stream>>>(tm, R, C, qs, r, part,      \
                                                                      tickets, sp.chunk, sp.S, epi); \

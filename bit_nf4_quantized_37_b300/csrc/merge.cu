@@ -22,6 +22,7 @@
 // fp64 across threads and CTAs).
 #include "common.cuh"
 #include "launch.h"
+#include "linear.h"
 #include "nf4_device.cuh"
 #include "profile.h"
 
@@ -213,12 +214,10 @@ __global__ void nf4_int4_error_sum(const double* __restrict__ part, int nparts,
 int launch_merge(const nf4_tensor& q, const uint16_t* A, const uint16_t* B, int r, float scale,
                  uint16_t* out16, float* out32, cudaStream_t stream) {
   const int smem = merge::smem_bytes(r);
-  static int attr = 0;
-  if (smem > 48 * 1024 && attr < smem) {
-    if (cudaFuncSetAttribute(merge::nf4_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return QLORA_ERR_CUDA;
-    attr = smem;
+  static DeviceCache<int> attr;  // set once per device to the largest rank's need
+  if (smem > 48 * 1024) {
+    const int st = ensure_dynamic_smem(attr, merge::nf4_merge_kernel, merge::smem_bytes(kMaxRank));
+    if (st) return st;
   }
   const dim3 grid((unsigned)((q.cols + merge::COLS - 1) / merge::COLS),
                   (unsigned)((q.rows + merge::ROWS - 1) / merge::ROWS));

@@ -425,14 +425,20 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   {
     ProfileScope ps("nf4_quant_blocks", stream);
     // persistent: as many CTAs as are resident at once, or fewer groups
-    static int per_sm = 0;
-    if (per_sm <= 0 &&
-        (cudaFuncSetAttribute(nf4_quant_blocks, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kCellBytes) != cudaSuccess ||
-         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nf4_quant_blocks, kQuantThreads,
-                                                       kCellBytes) != cudaSuccess))
-      return QLORA_ERR_CUDA;
-    if (per_sm < 1) per_sm = 1;
+    static DeviceCache<int> occupancy;  // resident CTAs per SM, per device
+    int per_sm = 0;
+    const int st = occupancy.get(device_context_key, &per_sm, [](int* v) -> int {
+      if (cudaFuncSetAttribute(nf4_quant_blocks, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kCellBytes) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, nf4_quant_blocks, kQuantThreads,
+                                                        kCellBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return QLORA_ERR_CUDA;
+      }
+      if (*v < 1) *v = 1;
+      return QLORA_OK;
+    });
+    if (st) return st == -1 ? QLORA_ERR_NO_DEVICE : st;
     const int64_t resident = (int64_t)per_sm * num_sms();
     const int64_t ctas = ng < resident ? ng : resident;
     nf4_quant_blocks<<<(unsigned)ctas, kQuantThreads, kCellBytes, stream>>>(W, numel, q.codes, absmax, gsum);

@@ -11,12 +11,12 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the library holds
 // it (about 4.2 MB) until the process exits.  Host code cannot hand the symbol itself to a
 // kernel (on the host it is only a stand-in), so the first call on each device looks up
-// its device address with cudaGetSymbolAddress while that device is current and caches it.
+// its device address with cudaGetSymbolAddress while that device is current and caches it
+// for that device's context; make that first call before any stream capture.  The stream
+// passed must belong to the current device (checked; QLORA_ERR_INVALID_ARG otherwise).
 // Every call shares the array and it keeps the last call's contents; the quantizer writes
 // every scratch entry it later reads, so nothing needs clearing between calls.  Calls that
 // overlap on the GPU (for instance on two streams) race on the array.
-#include <mutex>
-
 #include "common.cuh"
 #include "launch.h"
 
@@ -31,24 +31,34 @@ constexpr uint64_t kNoallocScratchBytes =
 
 __device__ __align__(256) unsigned char g_noalloc_quant_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array on the current device: looked up with that device
+// current, once per device and context (a context created again after cudaDeviceReset
+// looks it up again).
 int scratch_for_current_device(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return QLORA_ERR_NO_DEVICE;
-  if (dev < 0 || dev >= kMaxDevices) return QLORA_ERR_NO_DEVICE;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  static DeviceCache<void*> scratch;
+  const int st = scratch.get(device_context_key, out, [](void** v) -> int {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_quant_scratch) != cudaSuccess || !p)
+    if (cudaGetSymbolAddress(&p, g_noalloc_quant_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
       return QLORA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    }
+    *v = p;
+    return QLORA_OK;
+  });
+  return st == -1 ? QLORA_ERR_NO_DEVICE : st;
+}
+
+// The stream must belong to the current device: the scratch address is that device's.
+// The legacy and per-thread default streams (handles 0, 1, 2) always do.
+int check_stream_device(cudaStream_t stream, int dev) {
+  const uintptr_t h = reinterpret_cast<uintptr_t>(stream);
+  if (h <= 2) return QLORA_OK;
+  int sdev = -1;
+  if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) {
+    cudaGetLastError();
+    return QLORA_ERR_INVALID_ARG;
   }
-  *out = g_scratch_ptr[dev];
-  return QLORA_OK;
+  return sdev == dev ? QLORA_OK : QLORA_ERR_INVALID_ARG;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -80,8 +90,9 @@ extern "C" int nf4_quantize_noalloc(const float* W, const nf4_tensor* out, void*
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
       major != 10 || minor != 3)
     return QLORA_ERR_NO_DEVICE;
-  void* scratch = nullptr;
-  const int st = scratch_for_current_device(&scratch);
+  int st = check_stream_device(static_cast<cudaStream_t>(stream), dev);
   if (st) return st;
+  void* scratch = nullptr;
+  if ((st = scratch_for_current_device(&scratch))) return st;
   return launch_quantize(W, numel, *out, scratch, static_cast<cudaStream_t>(stream));
 }

@@ -733,25 +733,32 @@ int run_decode(const CUtensorMap& tmC, const CUtensorMap& tmX, const CUtensorMap
   using C = skinny::Cfg<NT>;
   // The kernel places its regions at fixed window offsets; it takes the whole opt-in
   // dynamic window, which starts after the reserved and static shared memory.
-  static int dyn = 0;
-  if (!dyn) {
+  static DeviceCache<int> window;  // this instantiation's dynamic window, per device
+  int dyn = 0;
+  const int st = window.get(device_context_key, &dyn, [](int* v) -> int {
     int dev = 0, optin = 0, reserved = 0;
     cudaFuncAttributes fa{};
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA, H>) != cudaSuccess)
+        cudaFuncGetAttributes(&fa, skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA, H>) != cudaSuccess) {
+      cudaGetLastError();
       return QLORA_ERR_CUDA;
+    }
     const int base = reserved + static_cast<int>(fa.sharedSizeBytes);
     const int size = optin - static_cast<int>(fa.sharedSizeBytes);
     if (base > static_cast<int>(skinny::kStageBase) ||
         base + size < static_cast<int>(C::SMEM_END))
       return QLORA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA, H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             size) != cudaSuccess)
+    if (cudaFuncSetAttribute(skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA, H>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, size) != cudaSuccess) {
+      cudaGetLastError();
       return QLORA_ERR_CUDA;
-    dyn = size;
-  }
+    }
+    *v = size;
+    return QLORA_OK;
+  });
+  if (st) return st == -1 ? QLORA_ERR_NO_DEVICE : st;
   skinny::nf4_decode_gemv<NT, SCALE, OWN_LORA, H><<<ctas, skinny::THREADS + skinny::PRODUCERS, dyn, stream>>>(tmC, tmX, tmB, p);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
@@ -768,14 +775,11 @@ uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K, int r) {
 int launch_skinny_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   uint16_t* sU = reinterpret_cast<uint16_t*>(ws + L.sU);
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(skinny::small_u<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             skinny::small_u_smem(2 * 64)) != cudaSuccess ||
-        cudaFuncSetAttribute(skinny::small_u<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             skinny::small_u_smem(2 * 64)) != cudaSuccess)
-      return QLORA_ERR_CUDA;
-    attr = true;
+  static DeviceCache<int> attr_bf16, attr_f16;
+  {
+    const int st = a.half ? ensure_dynamic_smem(attr_f16, skinny::small_u<true>, skinny::small_u_smem(2 * 64))
+                          : ensure_dynamic_smem(attr_bf16, skinny::small_u<false>, skinny::small_u_smem(2 * 64));
+    if (st) return st;
   }
   ProfileScope ps("decode_u", stream);
   const unsigned chunks = (unsigned)((a.K + skinny::U_KC - 1) / skinny::U_KC);

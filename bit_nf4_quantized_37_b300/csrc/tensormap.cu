@@ -1,7 +1,6 @@
 // tensormap.cu -- TMA tensor-map construction through the driver entry point (no link-time
 // dependency on libcuda), and the cached SM count.
 #include <mutex>
-#include <unordered_map>
 
 #include "launch.h"
 
@@ -50,18 +49,57 @@ bool make_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType 
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(p);
+  return nullptr;
+}
+
+}  // namespace
+
+DeviceKey device_context_key() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 12000);
+    get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  });
+  DeviceKey k{-1, 0};
+  if (cudaGetDevice(&k.device) != cudaSuccess) {
+    cudaGetLastError();
+    k.device = -1;
+    return k;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx &&
+      get_id(ctx, &id) == CUDA_SUCCESS)
+    k.context = id;
+  return k;
+}
+
 int num_sms() {
-  static std::mutex mu;
-  static std::unordered_map<int, int> cache;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  std::lock_guard<std::mutex> lk(mu);
-  auto it = cache.find(dev);
-  if (it != cache.end()) return it->second;
+  static DeviceCache<int> cache;
   int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 148;
-  cache[dev] = n;
+  if (cache.get(device_context_key, &n, [](int* v) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            *v <= 0)
+          return -1;
+        return 0;
+      }) != 0)
+    return 148;
   return n;
 }
 

@@ -657,15 +657,11 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   constexpr int BM = kPair ? pairk::BM_CTA : Tile<kAcc>::BM;
   constexpr int SMEM_BYTES = kPair ? pairk::SMEM_BYTES : Tile<kAcc>::SMEM_BYTES;
   constexpr int BNB = kPair ? pairk::BN_CTA : BN;  // W-tile box of one CTA (forward)
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    const cudaError_t e =
-        kPair ? cudaFuncSetAttribute(fused_pair_gemm<kMode, H>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)
-              : cudaFuncSetAttribute(fused_nf4_lora_gemm<kMode, kAcc, H>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return QLORA_ERR_CUDA;
-    attr_set = true;
+  static DeviceCache<int> smem_attr;  // this instantiation's kernel, per device
+  {
+    const int st = kPair ? ensure_dynamic_smem(smem_attr, fused_pair_gemm<kMode, H>, SMEM_BYTES)
+                         : ensure_dynamic_smem(smem_attr, fused_nf4_lora_gemm<kMode, kAcc, H>, SMEM_BYTES);
+    if (st) return st;
   }
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   const int64_t rp = L.rp;

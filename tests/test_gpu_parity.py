@@ -3,6 +3,9 @@
 Bit-exact: packed codes, second-level scale codes, steps, mean, dequantized bf16 weights.
 Relative Frobenius error <= 5e-3 against the fp64 oracle: Y, U, dX, dA, dB.
 """
+import os
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -53,6 +56,15 @@ def test_quantize_special_blocks():
     W[12, :] = -W[12, :]
     W[200:456] = W[200]             # a whole group of identical blocks
     _quant_parity(W.reshape(1, -1))
+
+
+def test_quantize_second_level_ties():
+    """A group whose second-level quotients are exact half-integers (tests/dq_ties.py): the
+    int8 codes follow rounding half to even, bit for bit with the oracle."""
+    from dq_ties import tie_tensor
+    W, expect = tie_tensor()
+    q, o = _quant_parity(W)
+    assert np.array_equal(q.scale_codes.cpu().numpy(), expect)
 
 
 def test_quantize_near_thresholds():
@@ -171,14 +183,18 @@ def test_fwd_bwd_small(name, M, N, K, r, alpha):
     _check_bwd(pb, None)  # U recomputed in the backward
 
 
-@pytest.mark.parametrize("M,N,K,r", [(2000, 4800, 320, 24),    # forward takes 256-row tiles
-                                     (2000, 320, 4800, 40)])   # input gradient takes them
-def test_two_accumulator_tiles_ragged(M, N, K, r):
-    p = wl.LinearProblem(f"twoacc-{M}-{N}-{K}", M, N, K, r, 2.0 * r, 0.02, 0.001, config=60 + r)
+@pytest.mark.parametrize("M,N,K,r", [(2000, 4800, 320, 24),    # forward on CTA pairs
+                                     (2000, 320, 4800, 40),    # input gradient on CTA pairs
+                                     (2100, 4864, 256, 16),    # forward pairs, 5th pair row partial
+                                     (2100, 256, 4864, 16)])   # input gradient, the same
+def test_pair_tiles_every_output(M, N, K, r):
+    """The CTA-pair GEMMs (512 x 256 tiles) against the oracle on every output element: all
+    16 row classes of a pair tile (2 CTAs x 2 accumulators x 4 TMEM lane groups), partial
+    last tiles in M and in the output columns."""
+    p = wl.LinearProblem(f"pairs-{M}-{N}-{K}", M, N, K, r, 2.0 * r, 0.02, 0.001, config=60 + r)
     pb = Problem(p)
-    rows = _sample_rows(M, 20, r)
-    Y, U = _check_fwd(pb, rows)
-    _check_bwd(pb, U, rows)
+    Y, U = _check_fwd(pb)
+    _check_bwd(pb, U)
 
 
 def test_zero_b_equals_base_matmul():
@@ -216,23 +232,25 @@ def test_base_is_frozen_and_results_reproducible():
 
 
 # ------------------------------------------------------------------ full-size workloads
-def _sample_rows(M, n=24, seed=0):
-    r = np.random.default_rng(seed)
+def _sample_rows(M, n, key: str):
+    """Sampled token rows for the oracle: the first and last row plus n rows drawn with a
+    seed of their own for every test (key), so tests on one shape check different rows."""
+    r = np.random.default_rng(zlib.crc32(key.encode()))
     rows = np.unique(np.concatenate([[0, M - 1], r.choice(M, size=min(n, M), replace=False)]))
     return rows.astype(np.int64)
 
 
 def test_config2_attention_projection():
+    """The headline shape on the CTA-pair kernels, every output element of Y and dX."""
     pb = Problem(wl.config2())
-    rows = _sample_rows(pb.p.M)
-    Y, U = _check_fwd(pb, rows)
-    _check_bwd(pb, U, rows)
+    Y, U = _check_fwd(pb)
+    _check_bwd(pb, U)
 
 
-@pytest.mark.parametrize("which", [0, 2])
+@pytest.mark.parametrize("which", [0, 1, 2])
 def test_config3_mlp_projection(which):
     pb = Problem(wl.config3()[which])
-    rows = _sample_rows(pb.p.M, 16, which)
+    rows = _sample_rows(pb.p.M, 64, f"config3-{which}")
     Y, U = _check_fwd(pb, rows)
     _check_bwd(pb, U, rows)
 
@@ -243,12 +261,38 @@ def test_config4_decode(M):
     _check_fwd(pb)
 
 
-def test_config5_layer_sampled():
-    for p in wl.config5(layer=0)[::3]:
+@pytest.mark.parametrize("layer", [0, 15, 31])
+def test_config5_layer_gemms(layer):
+    """Every projection of three layers of the 32-layer stack at M = 512 (all-linear LoRA):
+    Y and dX on sampled rows, U, dA and dB in full."""
+    for p in wl.config5(layer=layer):
         pb = Problem(p)
-        rows = _sample_rows(p.M, 12, 5)
+        rows = _sample_rows(p.M, 24, p.name)
         Y, U = _check_fwd(pb, rows)
         _check_bwd(pb, U, rows)
+
+
+def test_config5_quantize_every_layer_bit_exact():
+    """nf4_quantize on all 224 weight matrices of the 32-layer stack (6.48 G weights), each
+    bit-exact with the oracle.  The oracle runs in spawned worker processes (no GPU state)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+
+    import oracle_pool
+    workers = max(1, min(8, (os.cpu_count() or 2) // 2))
+    with cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn")) as ex, \
+            cf.ThreadPoolExecutor(7) as gen:
+        for layer, ref in enumerate(ex.map(oracle_pool.quantize_stack_layer, range(32))):
+            projs = wl.config5(layer=layer)
+            weights = list(gen.map(lambda p: p.W(), projs))  # the seeded draws, in threads
+            for p, W, (name, codes, qs, steps, mean) in zip(projs, weights, ref):
+                assert p.name == name
+                q = qn.nf4_quantize(torch.from_numpy(W).cuda())
+                assert np.array_equal(q.codes.cpu().numpy(), codes), name
+                assert np.array_equal(q.scale_codes.cpu().numpy(), qs), name
+                assert np.array_equal(q.scale_steps.cpu().numpy().view(np.uint32),
+                                      steps.view(np.uint32)), name
+                assert q.scale_mean.cpu().numpy()[0].view(np.uint32) == mean.view(np.uint32), name
 
 
 # ------------------------------------------------------------------ error paths
@@ -411,7 +455,7 @@ def test_fwd_bwd_nodq(name, M, N, K, r, alpha):
 
 def test_config2_nodq():
     pb = Problem(wl.config2(), double_quant=False)
-    rows = _sample_rows(pb.p.M)
+    rows = _sample_rows(pb.p.M, 48, "config2-nodq")
     Y, U = _check_fwd(pb, rows)
     _check_bwd(pb, U, rows)
 
@@ -468,7 +512,7 @@ def test_fwd_bwd_fp8_second_level(name, M, N, K, r, alpha):
 
 def test_config2_fp8_second_level():
     pb = Problem(wl.config2(), fp8_second_level=True)
-    rows = _sample_rows(pb.p.M)
+    rows = _sample_rows(pb.p.M, 48, "config2-fp8")
     Y, U = _check_fwd(pb, rows)
     _check_bwd(pb, U, rows)
 
@@ -531,7 +575,7 @@ def test_fwd_bwd_f16_format_variants(variant):
 
 def test_config2_f16():
     pb = Problem(wl.config2(), half=True)
-    rows = _sample_rows(pb.p.M)
+    rows = _sample_rows(pb.p.M, 48, "config2-f16")
     Y, U = _check_fwd(pb, rows)
     _check_bwd(pb, U, rows)
 

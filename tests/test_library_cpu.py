@@ -120,14 +120,16 @@ def test_f16_entry_points_validate_like_the_bf16_ones(lib):
                    16, 1, None) == -4
 
 
-def test_f16_wrappers_refuse_host_tensors():
+def test_f16_wrappers_refuse_host_tensors(lib):
     import torch
-    q = qn.NF4Tensor.__new__(qn.NF4Tensor)  # never reaches the library
+    q = _cpu_nf4(64, 64)  # never reaches a kernel
     x = torch.zeros(4, 64, dtype=torch.float16)
-    with pytest.raises(ValueError):
-        qn.qlora_linear_fwd_f16(x, q, x, x, 1.0)       # host tensors
-    with pytest.raises(ValueError):
-        qn.qlora_linear_bwd_f16(x, x, q, x, x, 1.0)
+    a = torch.zeros(4, 64, dtype=torch.float16)
+    b = torch.zeros(64, 4, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        qn.qlora_linear_fwd_f16(x, q, a, b, 1.0)       # host tensors
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        qn.qlora_linear_bwd_f16(x, x, q, a, b, 1.0)
 
 
 def test_workspace_grows_with_problem(lib):
@@ -136,3 +138,114 @@ def test_workspace_grows_with_problem(lib):
     c = qn.qlora_workspace_bytes(4096, 4096, 4096, 128)
     assert 0 < a < b < c
     assert qn.nf4_quantize_workspace_bytes(28672 * 8192) >= 28672 * 8192 // 64 * 4
+
+
+# ------------------------------------------------------------------ binding shape checks
+# A buffer whose shape does not match the NF4 base would make a kernel read or write past
+# its allocation; the binding refuses it with ValueError before anything is launched.  The
+# checks run before the device checks, so CPU tensors of the wrong shape exercise them here.
+def _cpu_nf4(rows, cols, dq=True):
+    import torch
+    sizes, _ = qn.nf4_storage_bytes(rows, cols, 256 if dq else 0)
+    return qn.NF4Tensor(torch.zeros(sizes[0], dtype=torch.uint8),
+                        torch.zeros(sizes[1], dtype=torch.int8),
+                        torch.zeros(sizes[2] // 4, dtype=torch.float32),
+                        torch.zeros(sizes[3] // 4, dtype=torch.float32), rows, cols,
+                        256 if dq else 0)
+
+
+def _bf(*shape):
+    import torch
+    return torch.zeros(*shape, dtype=torch.bfloat16)
+
+
+SHAPE_WORDS = r"shape|columns|elements|holds"
+
+
+def test_linear_fwd_refuses_mismatched_shapes(lib):
+    q = _cpu_nf4(256, 128)
+    cases = [
+        (_bf(16, 64), _bf(8, 64), _bf(256, 8), None),     # X has K = 64, base has 128
+        (_bf(16, 128), _bf(8, 64), _bf(256, 8), None),    # A [r, 64]
+        (_bf(16, 128), _bf(8, 128), _bf(128, 8), None),   # B rows != N
+        (_bf(16, 128), _bf(8, 128), _bf(256, 4), None),   # B columns != r
+        (_bf(16, 128), _bf(8, 128), _bf(256, 8), _bf(16, 128)),  # out [M, K] instead of [M, N]
+        (_bf(2, 8, 128), _bf(8, 128), _bf(256, 8), None),  # X not 2-D
+    ]
+    for X, A, B, out in cases:
+        for fn in (qn.qlora_linear_fwd, qn.qlora_linear_fwd_f16):
+            with pytest.raises(ValueError, match=SHAPE_WORDS + "|2-D"):
+                fn(X, q, A, B, 2.0, out=out)
+
+
+def test_linear_bwd_refuses_mismatched_shapes(lib):
+    import torch
+    q = _cpu_nf4(256, 128)
+    X, A, B = _bf(16, 128), _bf(8, 128), _bf(256, 8)
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.qlora_linear_bwd(_bf(16, 128), X, q, A, B, 2.0)           # dY [M, K]
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.qlora_linear_bwd(_bf(8, 256), X, q, A, B, 2.0)            # dY with other M
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.qlora_linear_bwd(_bf(16, 256), X, q, A, B, 2.0,
+                            U=torch.zeros(16, 4, dtype=torch.float32))  # U [M, r'] r' != r
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.qlora_linear_bwd_f16(_bf(16, 256), _bf(16, 64), q, A, B, 2.0)  # X columns
+
+
+def test_quantize_and_dequantize_refuse_mismatched_sizes(lib):
+    import torch
+    q = _cpu_nf4(64, 64)
+    W = torch.zeros(64, 65, dtype=torch.float32)
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.nf4_quantize(W, out=q)
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.nf4_quantize_noalloc(W, q)
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.nf4_dequantize(q, out=_bf(64, 63))
+    short = qn.NF4Tensor(q.codes[:100], q.scale_codes, q.scale_steps, q.scale_mean, 64, 64)
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.nf4_dequantize(short)
+    nodq_short = _cpu_nf4(64, 64, dq=False)
+    nodq_short.scale_steps = nodq_short.scale_steps[:10]  # 64 blocks need 64 fp32 absmax
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.nf4_dequantize(nodq_short)
+
+
+def test_multi_and_merge_refuse_mismatched_shapes(lib):
+    import torch
+    q = _cpu_nf4(256, 128)
+    X = _bf(4, 128)
+    A_all, B_all = _bf(3, 8, 128), _bf(3, 256, 8)
+    idx = torch.zeros(4, dtype=torch.int32)
+    sc = torch.ones(3, dtype=torch.float32)
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.qlora_linear_fwd_multi(X, q, A_all, _bf(2, 256, 8), idx, sc)
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.qlora_linear_fwd_multi(X, q, A_all, B_all, torch.zeros(5, dtype=torch.int32), sc)
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.qlora_linear_fwd_multi(X, q, A_all, B_all, idx, torch.ones(2, dtype=torch.float32))
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.nf4_merge_lora(q, _bf(8, 64), _bf(256, 8), 2.0)
+    with pytest.raises(ValueError, match=SHAPE_WORDS):
+        qn.nf4_merge_lora(q, _bf(8, 128), _bf(256, 8), 2.0, out=_bf(128, 256))
+
+
+def test_matching_cpu_tensors_reach_the_device_check(lib):
+    """With every shape right, the first refusal is the device check (CPU tensors)."""
+    q = _cpu_nf4(256, 128)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        qn.qlora_linear_fwd(_bf(16, 128), q, _bf(8, 128), _bf(256, 8), 2.0)
+
+
+def test_per_device_setup_cache_keying(tmp_path):
+    """The per-device set-up cache (csrc/device_cache.h): one entry per device ordinal, a
+    new set-up when that device's context changes (cudaDeviceReset), nothing stored when the
+    set-up fails or no context id exists.  Built with g++ against a fake key; no GPU."""
+    import subprocess
+    src = os.path.join(ROOT, "tests", "device_cache_test.cpp")
+    exe = str(tmp_path / "device_cache_test")
+    subprocess.run(["g++", "-std=c++17", "-O1", "-Wall", "-Werror", "-pthread", src, "-o", exe],
+                   check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "OK", r.stdout + r.stderr

@@ -235,6 +235,32 @@ def test_double_quant_two_value_group():
     assert np.all(q["qscale"][:128] == -127) and np.all(q["qscale"][128:] == 127)
 
 
+def test_double_quant_ties_round_half_to_even():
+    """Reading R5 rounds the second-level quotient half to even.  dq_ties builds one group
+    whose quotients (a - mu) / step are exact half-integers (mu = 1, step = 2^-7, both exact),
+    so each code is fixed by the tie rule alone: 0.5 -> 0, 2.5 -> 2, 126.5 -> 126 (even k, where
+    rounding half away from zero would give k + 1), 1.5 -> 2, 3.5 -> 4 (odd k), and the same
+    with the signs flipped."""
+    from dq_ties import tie_tensor, tie_offsets
+    W, expect = tie_tensor()
+    q = oracle.quantize(W)
+    assert q["mean"] == np.float32(1.0)
+    assert q["steps"][0] == np.float32(2.0 ** -7)
+    assert np.array_equal(q["qscale"], expect)
+    u = tie_offsets()
+    got = dict(zip(u.tolist(), q["qscale"][:128].tolist()))
+    assert got[0.5] == 0 and got[2.5] == 2 and got[10.5] == 10 and got[62.5] == 62
+    assert got[126.5] == 126
+    assert got[1.5] == 2 and got[3.5] == 4 and got[11.5] == 12 and got[63.5] == 64
+    assert got[127.0] == 127 and got[64.0] == 64 and got[0.0] == 0
+    neg = dict(zip((-u).tolist(), q["qscale"][128:].tolist()))
+    assert neg[-0.5] == 0 and neg[-2.5] == -2 and neg[-126.5] == -126 and neg[-1.5] == -2
+    # half away from zero would differ on every even k: the pin separates the two rules
+    away = np.sign(u) * np.floor(np.abs(u) + 0.5)
+    even_k = np.isin(u, [0.5, 2.5, 10.5, 62.5, 126.5])
+    assert np.all(q["qscale"][:128][even_k] != away[even_k])
+
+
 def test_double_quant_error_bound_and_range():
     """|ahat - a| <= step/2 (plus fp32 rounding); codes in [-127, 127]; the block with the
     largest |a - mu| in each group gets |q| = 127."""
