@@ -34,8 +34,13 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r) {
   L.part_bytes = std::max(side_partial_bytes(M, N, K, r), skinny_partial_bytes(M, N, K, r));
   L.part = take(L.part_bytes);
   // the split reductions' counters; at least one per token for the per-token adapter path
-  L.ntickets = std::max<uint64_t>(side_ticket_count(M, N, K), (uint64_t)kSkinnyMaxM);
-  L.tickets = take(L.ntickets * 4);
+  L.ntickets = std::max<uint64_t>(std::max(side_ticket_count(M, N, K), skinny_ticket_count(M, N)),
+                                  (uint64_t)kSkinnyMaxM);
+  const uint64_t gpart_bytes = M > kSkinnyMaxM ? fused_partial_bytes(M, N, K, &L.ngtickets) : 0;
+  if (M <= kSkinnyMaxM) L.ngtickets = 0;
+  L.tickets = take((L.ntickets + L.ngtickets) * 4);
+  L.gtickets = L.tickets + L.ntickets * 4;
+  L.gpart = take(gpart_bytes);
   L.Z = take(M <= kSkinnyMaxM ? (uint64_t)M * N * 4 : 0);
   L.total = off;
   return L;
@@ -46,7 +51,8 @@ uint64_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int r) {
 }
 
 static int clear_tickets(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  return cudaMemsetAsync(static_cast<uint8_t*>(a.ws) + L.tickets, 0, L.ntickets * 4, stream) ==
+  return cudaMemsetAsync(static_cast<uint8_t*>(a.ws) + L.tickets, 0,
+                         (L.ntickets + L.ngtickets) * 4, stream) ==
                  cudaSuccess
              ? QLORA_OK
              : QLORA_ERR_CUDA;

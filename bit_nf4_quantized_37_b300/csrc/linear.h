@@ -55,12 +55,29 @@ struct WorkspaceLayout {
   uint64_t part_bytes;
   uint64_t tickets;  // int [ntickets] arrival counters of the split reductions
   uint64_t ntickets;
+  uint64_t gpart;    // fp32 [nsplit][M][Nout] split-contraction tiles of the fused GEMM
+  uint64_t gtickets; // int [ngtickets] its per-tile arrivals (right after the tickets above)
+  uint64_t ngtickets;
   uint64_t Z;        // fp32 [M, N] per-token LoRA term (decode path, per-token adapters)
   uint64_t total;
 };
 
 WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r);
 uint64_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int r);
+
+// Tile plan of a fused GEMM with Nout output columns and contraction Kc: kind 2 = CTA pairs
+// (512 x 256 tiles), 1 = single CTAs with 256 x 256 tiles, 0 = 128 x 256 tiles; the
+// contraction is cut into nsplit runs of split_stages 64-wide stages (tiles: the output tiles).
+struct FusedPlan {
+  int kind;
+  int nsplit;
+  int split_stages;
+  int64_t tiles;
+};
+FusedPlan fused_plan(int64_t M, int64_t Nout, int64_t Kc);
+// Workspace of the split contraction (the larger of the forward and the input gradient) and,
+// in *tickets, its arrival counters.
+uint64_t fused_partial_bytes(int64_t M, int64_t N, int64_t K, uint64_t* tickets);
 
 int linear_forward(const LinearArgs& a, cudaStream_t stream);
 int linear_backward(const LinearArgs& a, cudaStream_t stream);
@@ -72,9 +89,8 @@ int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t
 int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 // Decode path (M <= 16): Y = X W'^T + sU Bp^T with the weights streamed once.
 int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
-// Its two parts: sU = 16-bit(scale X A^T) (small_u), and the GEMV, which forms the LoRA term
-// from sU and B on the tensor cores, or adds a precomputed fp32 term Z when Z is not null.
-int launch_skinny_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+// The GEMV: forms U = X A^T inside the launch and the LoRA term from sU and B on the tensor
+// cores, or adds a precomputed fp32 term Z when Z is not null.
 int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const float* Z,
                        cudaStream_t stream);
 // Decode path with per-token adapters (multi.cu): U_t = X_t A_{a(t)}^T, then
@@ -91,5 +107,6 @@ int launch_pad_b(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
 uint64_t side_partial_bytes(int64_t M, int64_t N, int64_t K, int r);
 uint64_t side_ticket_count(int64_t M, int64_t N, int64_t K);
 uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K, int r);
+uint64_t skinny_ticket_count(int64_t M, int64_t N);
 
 }  // namespace qlora

@@ -6,9 +6,9 @@
 // Three launches quantize a tensor, no host synchronization:
 //   nf4_quant_blocks   reads W once: per-64 absmax, the nearest level of w/absmax (exactly as
 //                      with an IEEE division, see below), 4-bit packing; writes the codes, the
-//                      absmax values and, per group of 256 blocks, the fp64 pairwise sum of
+//                      absmax values and, per unit of 64 blocks, the fp64 pairwise sum of
 //                      its absmax.
-//   nf4_absmax_mean    up to 32 CTAs: aligned subtrees of the pairwise sum over the group
+//   nf4_absmax_mean    up to 32 CTAs: aligned subtrees of the pairwise sum over the unit
 //                      sums.
 //   nf4_double_quant   a warp per group: mean (fp32) from the subtree sums, then
 //                      step = max|a - mean| / 127, int8 codes.
@@ -25,12 +25,16 @@ constexpr int kBlock = NF4_BLOCKSIZE;               // 64 weights per block
 constexpr int kGroup = NF4_DQ_BLOCK;                // 256 blocks per group
 constexpr int64_t kGroupElems = (int64_t)kBlock * kGroup;  // 16384 weights
 constexpr int kQuantThreads = 256;
+constexpr int kUnit = 64;                               // blocks per pass-1 work unit
+constexpr int64_t kUnitElems = (int64_t)kBlock * kUnit;  // 4096 weights
 
 // -------------------------------------------------------------------- pass 1
-// Persistent CTAs, each taking groups of 256 blocks (16384 weights) in a grid-stride loop.
+// Persistent CTAs, each taking units of 64 blocks (4096 weights) in a grid-stride loop: units
+// a quarter of a scale group keep the CTAs' shares even on tensors of a few thousand groups
+// (1024 groups on 592 resident CTAs left every CTA one or two).
 //
-// Full groups: four lanes per 64-block, 16 weights per lane (four float4 loads, the next
-// group's first loads in flight across the group boundary), so a block's absmax is 15 max
+// Full units: four lanes per 64-block, 16 weights per lane (four float4 loads, the next
+// unit's loads in flight across the unit boundary), so a block's absmax is 15 max
 // operations and two shuffles.  The exact quotient x = RN(w / a) is never needed away from a
 // threshold: y = RN(w * RN(1/a)) is within 3 * 2^-24 * |x| of x, so whenever y is more than
 // 2^-20 from every threshold, y and x fall between the same two thresholds and the level
@@ -42,7 +46,7 @@ constexpr int kQuantThreads = 256;
 // finite reciprocal, which leaves every y of the fast path finite and inside the table.  The
 // table is built once per CTA, one interleaved copy per lane (entry i of copy l at word pair
 // 32 i + l), so the 8-byte lookups of a half-warp never collide on a bank.
-// The last, partial group takes the element-by-element path with the exact division.
+// The last, partial unit takes the element-by-element path with the exact division.
 constexpr int kCells = 82;                  // per sign: [0, 2^-5), then 5 binades x 16, [1, 1.0625)
 constexpr int kCopies = 32;                 // one table copy per lane
 constexpr uint32_t kCellBase = 0x3D000000u;  // bits of 2^-5
@@ -102,85 +106,81 @@ __device__ __forceinline__ uint32_t code_fast(float y, uint32_t tab_b, float& dm
 
 __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
     const float* __restrict__ W, int64_t numel, uint8_t* __restrict__ codes,
-    float* __restrict__ absmax, double* __restrict__ group_sum) {
-  __shared__ float s_abs[2][kGroup];  // per group, double-buffered across groups
+    float* __restrict__ absmax, double* __restrict__ unit_sum) {
+  __shared__ float s_abs[2][kUnit];  // per unit, double-buffered across units
   extern __shared__ float2 s_cells[];  // 2 * kCells * kCopies entries
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nblocks = (numel + kBlock - 1) / kBlock;
-  const int64_t ngroups = (nblocks + kGroup - 1) / kGroup;
-  const int64_t nfull = numel / kGroupElems;  // groups with all 16384 weights present
+  const int64_t nunits = (nblocks + kUnit - 1) / kUnit;
+  const int64_t nfull = numel / kUnitElems;  // units with all 4096 weights present
   launch_dependents();  // pass 2 may be scheduled meanwhile (it waits for this grid)
   build_cells(s_cells);
   __syncthreads();
   const uint32_t tab_b = smem_u32(s_cells) + static_cast<uint32_t>(lane) * 8u - kCellBias * kEntryBytes;
   const int ql = lane & 3, bw = lane >> 2;  // quarter of the block, block within the warp
-  auto load16 = [&](int64_t g, int it, float4 (&f)[4]) {
-    const int64_t b = g * kGroup + warp * 32 + it * 8 + bw;
+  auto load16 = [&](int64_t u, float4 (&f)[4]) {
+    const int64_t b = u * kUnit + warp * 8 + bw;
     const float4* src = reinterpret_cast<const float4*>(W + b * kBlock + ql * 16);
 #pragma unroll
     for (int v = 0; v < 4; ++v) f[v] = __ldg(src + v);
   };
   float4 nxt[4];
-  if (blockIdx.x < nfull) load16(blockIdx.x, 0, nxt);
+  if (blockIdx.x < nfull) load16(blockIdx.x, nxt);
 
   int buf = 0;
 #pragma unroll 1
-  for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x, buf ^= 1) {
+  for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x, buf ^= 1) {
     float* sab = s_abs[buf];
-    if (g < nfull) {
-#pragma unroll 1
-      for (int it = 0; it < 4; ++it) {
-        const int local_block = warp * 32 + it * 8 + bw;
-        const int64_t b = g * kGroup + local_block;
-        float w[16];
+    if (u < nfull) {
+      const int local_block = warp * 8 + bw;
+      const int64_t b = u * kUnit + local_block;
+      float w[16];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          w[4 * v + 0] = nxt[v].x; w[4 * v + 1] = nxt[v].y; w[4 * v + 2] = nxt[v].z; w[4 * v + 3] = nxt[v].w;
-        }
-        // the next block's loads in flight during this one (across the group boundary too)
-        if (it + 1 < 4) load16(g, it + 1, nxt);
-        else if (g + gridDim.x < nfull) load16(g + gridDim.x, 0, nxt);
-        float m = fabsf(w[0]);
-#pragma unroll
-        for (int i = 1; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        if (ql == 0) {
-          sab[local_block] = m;
-          absmax[b] = m;
-        }
-        uint32_t c[16];
-        // a tiny, infinite or NaN absmax has no usable reciprocal: exact division
-        bool near = !(m >= 0x1p-100f && m <= 0x1.fffffep127f);
-        if (!near) {
-          const float rcp = __frcp_rn(m);
-          float dmin = __int_as_float(0x7f800000);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) c[i] = code_fast(__fmul_rn(w[i], rcp), tab_b, dmin);
-          near = !(dmin >= kGuard);
-        }
-        if (near) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) c[i] = code_exact(w[i], m);
-        }
-        // byte j = (c[2j] << 4) | c[2j+1], little endian: the nibbles from the top are
-        // c6 c7 c4 c5 c2 c3 c0 c1, accumulated as a multiply-add chain (multiply-add pipe)
-        uint32_t lo = c[6], hi = c[14];
-#pragma unroll
-        for (int t = 1; t < 8; ++t) {
-          const int e = 6 - 2 * (t >> 1) + (t & 1);  // 7, 4, 5, 2, 3, 0, 1
-          lo = lo * 16u + c[e];
-          hi = hi * 16u + c[8 + e];
-        }
-        *reinterpret_cast<uint2*>(codes + b * (kBlock / 2) + ql * 8) = make_uint2(lo, hi);
+      for (int v = 0; v < 4; ++v) {
+        w[4 * v + 0] = nxt[v].x; w[4 * v + 1] = nxt[v].y; w[4 * v + 2] = nxt[v].z; w[4 * v + 3] = nxt[v].w;
       }
+      // the next unit's loads in flight during this one
+      if (u + gridDim.x < nfull) load16(u + gridDim.x, nxt);
+      float m = fabsf(w[0]);
+#pragma unroll
+      for (int i = 1; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      if (ql == 0) {
+        sab[local_block] = m;
+        absmax[b] = m;
+      }
+      uint32_t c[16];
+      // a tiny, infinite or NaN absmax has no usable reciprocal: exact division
+      bool near = !(m >= 0x1p-100f && m <= 0x1.fffffep127f);
+      if (!near) {
+        const float rcp = __frcp_rn(m);
+        float dmin = __int_as_float(0x7f800000);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) c[i] = code_fast(__fmul_rn(w[i], rcp), tab_b, dmin);
+        near = !(dmin >= kGuard);
+      }
+      if (near) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) c[i] = code_exact(w[i], m);
+      }
+      // byte j = (c[2j] << 4) | c[2j+1], little endian: the nibbles from the top are
+      // c6 c7 c4 c5 c2 c3 c0 c1, accumulated as a multiply-add chain (multiply-add pipe)
+      uint32_t lo = c[6], hi = c[14];
+#pragma unroll
+      for (int t = 1; t < 8; ++t) {
+        const int e = 6 - 2 * (t >> 1) + (t & 1);  // 7, 4, 5, 2, 3, 0, 1
+        lo = lo * 16u + c[e];
+        hi = hi * 16u + c[8 + e];
+      }
+      *reinterpret_cast<uint2*>(codes + b * (kBlock / 2) + ql * 8) = make_uint2(lo, hi);
     } else {
-      // partial last group: half a warp per block, one float4 per lane, exact division
+      // partial last unit: half a warp per block, one float4 per lane, exact division
       const int half = lane >> 4, hl = lane & 15;
 #pragma unroll 1
-      for (int it = 0; it < 16; ++it) {
-        const int local_block = warp * 32 + it * 2 + half;
-        const int64_t b = g * kGroup + local_block;
+      for (int it = 0; it < kUnit / 16; ++it) {
+        const int local_block = it * 16 + warp * 2 + half;
+        const int64_t b = u * kUnit + local_block;
         const int64_t e = b * kBlock + hl * 4;
         float v[4];
 #pragma unroll
@@ -198,23 +198,22 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
         if (e + 2 < numel) codes[e / 2 + 1] = static_cast<uint8_t>(e + 3 < numel ? ((c2 << 4) | c3) : (c2 << 4));
       }
     }
-    __syncthreads();  // the group's absmax values are all in sab
+    __syncthreads();  // the unit's absmax values are all in sab
     if (warp == 0) {
-      // Perfect binary tree over the 256 absmax values in block order: each lane sums 8
-      // neighbours pairwise, then the xor butterfly combines lanes (x+y == y+x in IEEE).
-      // The other warps go on with the next group, which writes the other buffer.
-      const float* a = sab + lane * 8;
-      double sum = (((double)a[0] + (double)a[1]) + ((double)a[2] + (double)a[3])) +
-                   (((double)a[4] + (double)a[5]) + ((double)a[6] + (double)a[7]));
+      // Perfect binary tree over the 64 absmax values in block order: each lane adds its two
+      // neighbours, then the xor butterfly combines lanes (x+y == y+x in IEEE).  The other
+      // warps go on with the next unit, which writes the other buffer.
+      const float* a = sab + lane * 2;
+      double sum = (double)a[0] + (double)a[1];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (lane == 0) group_sum[g] = sum;
+      if (lane == 0) unit_sum[u] = sum;
     }
   }
 }
 
 // -------------------------------------------------------------------- pass 2
-// The pairwise tree over the group sums, zero-padded to a power of two P, is cut into
+// The pairwise tree over the unit sums, zero-padded to a power of two P, is cut into
 // nparts <= 32 aligned subtrees of P / nparts leaves, one CTA of 1024 threads each; pass 3
 // combines the subtree sums (the top levels of the same tree) and forms
 // mean = (float)(total / nblocks).  Each thread folds a run of kRun consecutive leaves (a
@@ -232,26 +231,26 @@ __device__ __forceinline__ double fold_run(const double* __restrict__ leaf, int6
   return v[0];
 }
 
-__global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict__ group_sum,
-                                                        int64_t ngroups, int64_t run,
+__global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict__ unit_sum,
+                                                        int64_t nunits, int64_t run,
                                                         double* __restrict__ part) {
   __shared__ double s_warp[32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   launch_dependents();     // pass 3 may be scheduled meanwhile (it waits for this grid)
-  grid_dependency_wait();  // the group sums of pass 1
+  grid_dependency_wait();  // the unit sums of pass 1
   const int64_t lo = ((int64_t)blockIdx.x * 1024 + t) * run;
   double s;
   switch (run) {
-    case 1: s = fold_run<1>(group_sum, lo, ngroups); break;
-    case 2: s = fold_run<2>(group_sum, lo, ngroups); break;
-    case 4: s = fold_run<4>(group_sum, lo, ngroups); break;
-    case 8: s = fold_run<8>(group_sum, lo, ngroups); break;
-    case 16: s = fold_run<16>(group_sum, lo, ngroups); break;
+    case 1: s = fold_run<1>(unit_sum, lo, nunits); break;
+    case 2: s = fold_run<2>(unit_sum, lo, nunits); break;
+    case 4: s = fold_run<4>(unit_sum, lo, nunits); break;
+    case 8: s = fold_run<8>(unit_sum, lo, nunits); break;
+    case 16: s = fold_run<16>(unit_sum, lo, nunits); break;
     default: {  // very large tensors: binary-counter fold of the run, still the pairwise tree
       double stack[48];
       int depth = 0;
       for (int64_t i = 0; i < run; ++i) {
-        double v = (lo + i < ngroups) ? group_sum[lo + i] : 0.0;
+        double v = (lo + i < nunits) ? unit_sum[lo + i] : 0.0;
         int64_t k = i + 1;
         while ((k & 1) == 0) {
           v = stack[--depth] + v;
@@ -409,9 +408,9 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
 uint64_t quantize_workspace_bytes(int64_t numel) {
   const int64_t nb = (numel + kBlock - 1) / kBlock;
   const int64_t ng = (nb + kGroup - 1) / kGroup;
-  // absmax fp32 [ngroups * 256] (padded to whole groups), group sums fp64 [ngroups], then the
-  // mean's subtree sums fp64 [<= 32] in the 256-byte tail
-  return (uint64_t)ng * kGroup * 4 + (uint64_t)ng * 8 + 256;
+  // absmax fp32 [ngroups * 256] (padded to whole groups), unit sums fp64 [<= 4 ngroups], then
+  // the mean's subtree sums fp64 [<= 32] in the 256-byte tail
+  return (uint64_t)ng * kGroup * 4 + (uint64_t)ng * (kGroup / kUnit) * 8 + 256;
 }
 
 int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws,
@@ -421,10 +420,11 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   const bool dq = q.dq_block != 0;
   // without double quantization pass 1 writes the block absmax straight into the tensor
   float* absmax = dq ? reinterpret_cast<float*>(ws) : q.scale_steps;
-  double* gsum = reinterpret_cast<double*>(reinterpret_cast<char*>(ws) + ng * kGroup * 4);
+  const int64_t nu = (nb + kUnit - 1) / kUnit;
+  double* usum = reinterpret_cast<double*>(reinterpret_cast<char*>(ws) + ng * kGroup * 4);
   {
     ProfileScope ps("nf4_quant_blocks", stream);
-    // persistent: as many CTAs as are resident at once, or fewer groups
+    // persistent: as many CTAs as are resident at once, or fewer units
     static DeviceCache<int> occupancy;  // resident CTAs per SM, per device
     int per_sm = 0;
     const int st = occupancy.get(device_context_key, &per_sm, [](int* v) -> int {
@@ -440,13 +440,13 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     });
     if (st) return st == -1 ? QLORA_ERR_NO_DEVICE : st;
     const int64_t resident = (int64_t)per_sm * num_sms();
-    const int64_t ctas = ng < resident ? ng : resident;
-    nf4_quant_blocks<<<(unsigned)ctas, kQuantThreads, kCellBytes, stream>>>(W, numel, q.codes, absmax, gsum);
+    const int64_t ctas = nu < resident ? nu : resident;
+    nf4_quant_blocks<<<(unsigned)ctas, kQuantThreads, kCellBytes, stream>>>(W, numel, q.codes, absmax, usum);
   }
   if (!dq) return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
-  double* part = gsum + ng;
+  double* part = usum + ng * (kGroup / kUnit);
   int64_t p2 = 1;
-  while (p2 < ng) p2 *= 2;
+  while (p2 < nu) p2 *= 2;
   const int nparts = p2 > 1024 ? static_cast<int>(p2 / 1024 < 32 ? p2 / 1024 : 32) : 1;
   const int64_t run = p2 > 1024 * nparts ? p2 / (1024 * nparts) : 1;
   // passes 2 and 3 are programmatic dependents: launched while the pass before finishes,
@@ -462,7 +462,7 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     ProfileScope ps("nf4_absmax_mean", stream);
     cfg.gridDim = dim3(nparts);
     cfg.blockDim = dim3(1024);
-    if (cudaLaunchKernelEx(&cfg, nf4_absmax_mean, static_cast<const double*>(gsum), ng, run,
+    if (cudaLaunchKernelEx(&cfg, nf4_absmax_mean, static_cast<const double*>(usum), nu, run,
                            part) != cudaSuccess)
       return QLORA_ERR_CUDA;
   }

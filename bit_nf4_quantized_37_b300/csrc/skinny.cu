@@ -18,16 +18,25 @@
 // add for the address and one shared load, instead of the ~10 integer-pipe operations of a
 // per-block byte-permute table.
 //
-// Work split.  The packed codes are walked as stages of [128 rows x 256 k] (16 KB, one TMA
-// box, 128-byte swizzle) together with the tokens' [M x 256] slice (four 64-wide boxes).
-// The stages of all row blocks, k-fastest, are cut into one contiguous run per CTA (one CTA
-// per SM, a deep TMA ring): every SM streams the same number of bytes.  A row block whose
-// stages fall to several CTAs ("pieces") is summed, in CTA order, by the CTA whose piece
-// completes it (atomic stage count); the piece that starts a row block adds the LoRA term
-// s U B^T (B rows by TMA, U from the small-M U kernel) on the tensor cores as well.
-// Inside a stage, warp w dequantizes 64-block (w & 3) of four 16-row groups; the 16
+// Work split.  The packed codes are walked as stages of [128 rows x KSTEP k] (KSTEP = 512 for
+// up to 8 tokens, 256 for up to 16; 128-byte TMA boxes with 128-byte swizzle) together with
+// the tokens' [M x KSTEP] slice (64-wide boxes).  A stage reads 256 contiguous bytes of each
+// weight row when KSTEP is 512: on B300 a TMA stream of 128-row x 128-byte boxes reached
+// 3.9 TB/s, one of 128 x 256 bytes 4.8 TB/s.  The stages of all row blocks, k-fastest, are
+// cut into one contiguous run per CTA (one CTA per SM): every SM streams the same number of
+// bytes.  A row block whose stages fall to several CTAs ("pieces") is summed, in CTA order,
+// by the CTA whose piece completes it (atomic stage count); the piece that starts a row block
+// adds the LoRA term s U B^T (B rows by TMA) on the tensor cores as well.
+// U = X A^T is formed inside the same launch: the producer warps of the first CTAs each take
+// a 256-wide chunk of the contraction once the ring's first stages are on their way, and the
+// last of them to finish sums the chunks in chunk order, publishes sU and raises a flag that
+// the first LoRA flush of every CTA waits for (bounded).  No LoRA flush comes before a CTA has
+// streamed a whole row block or its whole run, long after U is done.
+// Inside a stage, warp w dequantizes 64-block (w % BPS) of GPW 16-row groups; the 16
 // contraction slots of an MMA map to k = 16 q + 4 i + {0..3} of the block for lane class q
 // and MMA i (the contraction order is free as long as the token operand uses the same map).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 #include "linear.h"
@@ -53,8 +62,6 @@ namespace skinny {
 constexpr int THREADS = 512;                     // 16 consumer warps
 constexpr int PRODUCERS = 128;                   // one producer warpgroup (one thread per row)
 constexpr int ROWS = 128;                        // weight rows per stage (8 groups of 16)
-constexpr int KSTEP = 256;                       // k per stage (4 blocks of 64)
-constexpr int CODE_BYTES = ROWS * KSTEP / 2;     // 16 KB
 // Byte table: entry v at v * 256 bytes, lane l's copy of it at + 4 l (the upper half of each
 // entry row is unused), so one byte_perm forms the address from the code word and 4 l.
 constexpr int TABLE_BYTES = 256 * 256;
@@ -63,6 +70,7 @@ constexpr int LORA_BYTES = 2 * LORA_BOX_BYTES;   // rank up to 128
 constexpr int SU_PITCH = 128 + 8;                // bf16 per token row of the staged sU
 constexpr int SU_BYTES = 16 * SU_PITCH * 2;
 constexpr int SCALE_AHEAD = 4;                   // stages between a scale load and its use
+constexpr int U_KC = 256;                        // contraction chunk of one U-computing CTA
 // Fixed shared-window layout.  The byte table sits at a 64 KB boundary, so the window
 // address of entry v, lane l's copy, is (0x02 << 16) | (v << 8) | 4 l: one byte_perm of the
 // code word and a per-lane constant forms it, with no add.  The TMA ring and the staged sU
@@ -74,10 +82,15 @@ constexpr uint32_t kLoraBase = kTableBase + TABLE_BYTES;
 // NT token octets (M <= 8 NT).
 template <int NT>
 struct Cfg {
+  static constexpr int KSTEP = NT == 1 ? 512 : 256;       // k per stage
+  static constexpr int BPS = KSTEP / 64;                  // 64-blocks per stage
+  static constexpr int GPW = BPS / 2;                     // 16-row groups per consumer warp
+  static constexpr int CODE_BYTES = ROWS * KSTEP / 2;     // 32 or 16 KB (128-byte boxes)
   static constexpr int XSLOT = NT * 8 * 128;              // [8 NT tokens x 64 k] bf16
-  static constexpr int STAGE_BYTES = CODE_BYTES + 4 * XSLOT;
-  static constexpr int STAGES = NT == 1 ? 6 : 5;
-  static constexpr int ACC = 2 * NT * 4;                  // accumulators per lane
+  static constexpr int STAGE_BYTES = CODE_BYTES + BPS * XSLOT;
+  static constexpr int STAGES = NT == 1 ? 3 : 5;
+  static constexpr int TAB_ROWS = ROWS * BPS / 32;        // byte-table rows of a stage's scales
+  static constexpr int ACC = GPW * NT * 4;                // accumulators per lane
   static constexpr int RED_BYTES = (THREADS / 32) * 32 * ACC * 4;
   // the B-row tile of the LoRA term and the cross-warp reduction share one region: the
   // tile is consumed before the reduction writes it
@@ -89,6 +102,8 @@ static_assert(Cfg<1>::SU_BASE + SU_BYTES <= kTableBase, "decode ring below the b
 static_assert(Cfg<2>::SU_BASE + SU_BYTES <= kTableBase, "decode ring below the byte table");
 static_assert(Cfg<1>::SMEM_END <= 228 * 1024 && Cfg<2>::SMEM_END <= 228 * 1024,
               "decode kernel shared window");
+static_assert(Cfg<1>::STAGES * Cfg<1>::TAB_ROWS <= 256 && Cfg<2>::STAGES * Cfg<2>::TAB_ROWS <= 256,
+              "stage scale tables fit the byte-table holes");
 
 // Row order inside a 16-row group: MMA row g (and g + 8) is weight row perm8(g) (and + 8),
 // so the four rows a half-warp reads from one swizzled code tile hit eight distinct 16-byte
@@ -150,13 +165,23 @@ struct Params {
   int qs_words;        // scale codes of a row's stage are one aligned 32-bit word
   float* part;         // [CTAs][2][16][128] fp32 pieces of split row blocks
   int* tickets;        // [row blocks] stages summed so far
-  const uint16_t* sU;  // [M][rp] bf16, scale * U
   int64_t rp;
   int r;
   uint16_t* Y;
   // [M][N] fp32 LoRA term computed outside (per-token adapters); when set, the kernel adds it
   // before the final rounding instead of forming s U B^T on the tensor cores
   const float* Z;
+  // U = X A^T inside the launch (with the on-chip LoRA term): CTAs [0, nU) each take U chunks
+  // c = blockIdx.x + k G of U_KC contraction columns
+  int nU;
+  const uint16_t* X;   // [M][K]
+  const uint16_t* A;   // [r][K]
+  float scale;
+  float* U_out;        // [M][r] fp32, or null
+  float* part_u;       // [chunks][16][rp] fp32 partial U
+  int* u_ticket;       // arrivals of the U CTAs (zero at launch)
+  int* u_ready;        // 1 once sU (in the workspace) is complete (zero at launch)
+  uint16_t* sU_out;    // [M][rp] 16-bit scale * U, written by the last U CTA
   float levels[16];  // the NF4 levels (parameter space: no cold constant-cache miss)
 };
 
@@ -194,10 +219,32 @@ __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
 }
 
-// Shared byte offset of stage-scale entry e (0..511) of ring slot sl: the scale tables live
-// in the unused upper halves of the byte-table rows (128 bytes = 32 entries per row).
+// Shared byte offset of stage-scale entry e (0 .. 128 BPS - 1) of ring slot sl: the scale
+// tables live in the unused upper halves of the byte-table rows (128 bytes = 32 entries per
+// row), TAB_ROWS rows per slot.
+template <int TAB_ROWS>
 __device__ __forceinline__ uint32_t scale_slot_off(int sl, int e) {
-  return static_cast<uint32_t>(((sl * 16 + (e >> 5)) * 256) + 128 + (e & 31) * 4);
+  return static_cast<uint32_t>(((sl * TAB_ROWS + (e >> 5)) * 256) + 128 + (e & 31) * 4);
+}
+
+// Bounded wait for a flag in global memory written by another CTA of the same launch.
+// Returns false (and records kWaitLora) after the limit.
+__device__ __forceinline__ bool wait_flag(const int* flag, volatile int* abort_flag, int* err) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicCAS(err, 0, kWaitLora);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+    __nanosleep(200);
+  }
 }
 
 // Scale formats, a compile-time parameter so the producers' per-stage scale writes carry no
@@ -213,6 +260,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
                     const __grid_constant__ CUtensorMap tmB, const Params p) {
   using C = Cfg<NT>;
   constexpr int STAGES = C::STAGES;
+  constexpr int KSTEP = C::KSTEP, BPS = C::BPS, GPW = C::GPW, CODE_BYTES = C::CODE_BYTES;
   constexpr bool kDq = SCALE != kScaleAbsmax;
   constexpr int kFp8 = SCALE == kScaleFp8 ? 1 : 0;
   static_assert(STAGES * 16 <= 256, "scale tables fit the byte-table holes");
@@ -247,14 +295,16 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   float* sRed = reinterpret_cast<float*>(sLora);  // shares the region (see Cfg)
   uint16_t* sUs = reinterpret_cast<uint16_t*>(sWin + C::SU_BASE);
   uint8_t* sTab = sWin + kTableBase;
-  const uint32_t x_bytes = 4u * 128u * static_cast<uint32_t>(p.M);
+  const uint32_t x_bytes = static_cast<uint32_t>(BPS) * 128u * static_cast<uint32_t>(p.M);
   auto issue_stage = [&](int slot, int64_t rb, int64_t ks) {
     uint8_t* d = sStage + slot * C::STAGE_BYTES;
     mbar_arrive_expect_tx(&full_bar[slot], CODE_BYTES + x_bytes);
-    tma_load_2d(d, &tmCodes, &full_bar[slot], static_cast<int32_t>(ks * (KSTEP / 2)),
-                static_cast<int32_t>(rb * ROWS));
 #pragma unroll
-    for (int x = 0; x < 4; ++x)
+    for (int h = 0; h < BPS / 4; ++h)  // 128-byte boxes of the rows' codes, k ascending
+      tma_load_2d(d + h * (ROWS * 128), &tmCodes, &full_bar[slot],
+                  static_cast<int32_t>(ks * (KSTEP / 2) + 128 * h), static_cast<int32_t>(rb * ROWS));
+#pragma unroll
+    for (int x = 0; x < BPS; ++x)
       tma_load_2d(d + CODE_BYTES + x * C::XSLOT, &tmX, &full_bar[slot],
                   static_cast<int32_t>(ks * KSTEP + 64 * x), 0);
   };
@@ -277,67 +327,70 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       if (++ks == p.KST) ks = 0, ++rb;
     }
   }
-  // the scaled U rows (zero past M and past the rank padding): loads first, so they are in
-  // flight while the byte table (lower half of each row) is built
-  static_assert(16 * (SU_PITCH / 8) <= THREADS + PRODUCERS, "one sU piece per thread");
-  uint4 su_v = make_uint4(0, 0, 0, 0);
-  {
-    const int t = tid / (SU_PITCH / 8), c8 = tid % (SU_PITCH / 8);
-    if (p.sU && t < p.M && 8 * c8 < p.rp)
-      su_v = __ldg(reinterpret_cast<const uint4*>(p.sU + t * p.rp + 8 * c8));
-  }
+  static_assert(16 * (SU_PITCH / 8) <= THREADS, "one sU piece per consumer thread");
   for (int i = tid; i < 256 * 8; i += THREADS + PRODUCERS) {
     const int v = i >> 3;  // 8 threads per entry: 16 bytes (4 lane copies) each
     const uint32_t e = pack_pair<H>(p.levels[v >> 4], p.levels[v & 15]);
     *reinterpret_cast<uint4*>(sTab + v * 256 + (i & 7) * 16) = make_uint4(e, e, e, e);
   }
-  if (tid < 16 * (SU_PITCH / 8))
-    *reinterpret_cast<uint4*>(sUs + (tid / (SU_PITCH / 8)) * SU_PITCH + 8 * (tid % (SU_PITCH / 8))) = su_v;
   __syncthreads();
 
   if (warp >= THREADS / 32) {
     // ============================================================ producer warpgroup
     // Per stage, lane 0 of the first producer warp issues the TMA of codes and token slice
     // (one arrival with the transaction bytes) as soon as the slot is free, and thread R of
-    // the four producer warps writes the four block scales of weight row R into the stage's
+    // the four producer warps writes the BPS block scales of weight row R into the stage's
     // slot table (one arrival per warp): the full barrier counts 1 + 4 arrivals.
-    // A row's four scale codes of a stage are one aligned 32-bit word when the 64-blocks
-    // per row are a multiple of 4: that word and its dq step are loaded SCALE_AHEAD stages
-    // early into rotating register sets; otherwise each code is read when needed.
+    // A row's BPS scale codes of a stage are BPS / 4 aligned 32-bit words when the 64-blocks
+    // per row are a multiple of BPS: those words and the dq step are loaded SCALE_AHEAD
+    // stages early into rotating register sets; otherwise each code is read when needed.
+    // In the first CTAs the warps form U = X A^T (see u_work) once the ring's first stages
+    // have their scale tables.
+    constexpr int SW = BPS / 4;
+    struct ScaleSet {
+      uint32_t w[SW];
+      float st;
+    };
     const int R = tid - THREADS;
     const int pw_idx = warp - THREADS / 32;
     const float mu = kDq ? __ldg(p.mean) : 0.0f;
     const bool word_path = p.qs_words != 0;
     const int e0 = 16 * (R >> 4) + 2 * inv_perm8(R & 7) + ((R >> 3) & 1);
-    uint32_t pw[SCALE_AHEAD];
-    float pst[SCALE_AHEAD];
+    ScaleSet ps0, ps1, ps2, ps3;
     int64_t f_n = rb_first * ROWS + R, f_ks = s_begin % p.KST;  // next stage to fetch
-    auto fetch = [&](uint32_t& w, float& st) {
-      w = 0u;
-      st = 0.f;
+    auto fetch = [&](ScaleSet& z) {
+#pragma unroll
+      for (int i = 0; i < SW; ++i) z.w[i] = 0u;
+      z.st = 0.f;
       if (f_n < p.N) {
-        const int64_t idx = f_n * p.KB + f_ks * 4;
-        w = __ldg(reinterpret_cast<const uint32_t*>(p.qs + idx));
-        st = __ldg(p.steps + (idx >> 8));
+        const int64_t idx = f_n * p.KB + f_ks * BPS;
+        if constexpr (SW == 2) {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(p.qs + idx));
+          z.w[0] = v.x;
+          z.w[SW - 1] = v.y;
+        } else {
+          z.w[0] = __ldg(reinterpret_cast<const uint32_t*>(p.qs + idx));
+        }
+        z.st = __ldg(p.steps + (idx >> 8));
       }
       if (++f_ks == p.KST) f_ks = 0, f_n += ROWS;
     };
     auto fetch_set = [&](int set) {
       switch (set) {
-        case 0: fetch(pw[0], pst[0]); break;
-        case 1: fetch(pw[1], pst[1]); break;
-        case 2: fetch(pw[2], pst[2]); break;
-        default: fetch(pw[3], pst[3]); break;
+        case 0: fetch(ps0); break;
+        case 1: fetch(ps1); break;
+        case 2: fetch(ps2); break;
+        default: fetch(ps3); break;
       }
     };
-    auto write_set = [&](int slot, int64_t n, int64_t ks, uint32_t w, float st) {
+    auto write_set = [&](int slot, int64_t n, int64_t ks, const ScaleSet& z) {
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int64_t kb = ks * 4 + b;
+      for (int b = 0; b < BPS; ++b) {
+        const int64_t kb = ks * BPS + b;
         float v = 0.f;
         if (n < p.N && kb < p.KB) {
           if (word_path) {
-            v = __fmaf_rn(nf4_second_level(w >> (8 * b), kFp8), st, mu);
+            v = __fmaf_rn(nf4_second_level(z.w[b >> 2] >> (8 * (b & 3)), kFp8), z.st, mu);
           } else {
             const int64_t idx = n * p.KB + kb;
             v = kDq ? __fmaf_rn(nf4_second_level(static_cast<uint8_t>(__ldg(p.qs + idx)), kFp8),
@@ -345,15 +398,107 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
                     : __ldg(p.steps + idx);
           }
         }
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(kTableBase + scale_slot_off(slot, b * 128 + e0)), "f"(v));
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(kTableBase + scale_slot_off<C::TAB_ROWS>(slot, b * 128 + e0)),
+                     "f"(v));
       }
+    };
+    // U = X A^T for the contraction chunks of this CTA (chunks c = blockIdx.x + k G of U_KC
+    // columns): warp pw_idx takes the 8-row adapter tiles pw_idx, pw_idx + 4, ...; a lane
+    // holds 16 consecutive k of its token rows and adapter row per 64-wide step (the same
+    // contraction-slot map on both operands).  The partial sums go to part_u; the last CTA to
+    // arrive sums the chunks in chunk order, writes sU (and U), and raises u_ready.
+    auto u_work = [&]() {
+      if (p.nU <= 0 || blockIdx.x >= p.nU) return;
+      const int g = lane >> 2, q = lane & 3;
+      const int ntiles = static_cast<int>(p.rp / 8);
+      const int64_t nchunks = (p.K + U_KC - 1) / U_KC;
+      auto ld16 = [&](const uint16_t* base, int64_t row, int64_t nrows, int64_t k) -> uint4 {
+        return (row < nrows && k < p.K) ? __ldg(reinterpret_cast<const uint4*>(base + row * p.K + k))
+                                        : make_uint4(0, 0, 0, 0);
+      };
+      for (int64_t c = blockIdx.x; c < nchunks; c += G) {
+        float d[4][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
+#pragma unroll 1
+        for (int kk = 0; kk < U_KC; kk += 64) {
+          const int64_t k = c * U_KC + kk + 16 * q;
+          uint4 xa[2], xb[2], av[4][2];
+          xa[0] = ld16(p.X, g, p.M, k);
+          xa[1] = ld16(p.X, g, p.M, k + 8);
+          xb[0] = NT > 1 ? ld16(p.X, g + 8, p.M, k) : make_uint4(0, 0, 0, 0);
+          xb[1] = NT > 1 ? ld16(p.X, g + 8, p.M, k + 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int j = pw_idx + 4 * t;
+            av[t][0] = j < ntiles ? ld16(p.A, 8 * j + g, p.r, k) : make_uint4(0, 0, 0, 0);
+            av[t][1] = j < ntiles ? ld16(p.A, 8 * j + g, p.r, k + 8) : make_uint4(0, 0, 0, 0);
+          }
+          const uint32_t xw[8] = {xa[0].x, xa[0].y, xa[0].z, xa[0].w, xa[1].x, xa[1].y, xa[1].z, xa[1].w};
+          const uint32_t yw[8] = {xb[0].x, xb[0].y, xb[0].z, xb[0].w, xb[1].x, xb[1].y, xb[1].z, xb[1].w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            if (pw_idx + 4 * t >= ntiles) continue;
+            const uint32_t aw[8] = {av[t][0].x, av[t][0].y, av[t][0].z, av[t][0].w,
+                                    av[t][1].x, av[t][1].y, av[t][1].z, av[t][1].w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              mma_16816<H>(d[t], xw[2 * m], yw[2 * m], xw[2 * m + 1], yw[2 * m + 1], aw[2 * m],
+                           aw[2 * m + 1]);
+          }
+        }
+        // d[t]: [0] token g / adapter row 8j + 2q, [1] + 1, [2] token g + 8 / 8j + 2q, [3] + 1
+        float* mine = p.part_u + c * 16 * p.rp;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int j = pw_idx + 4 * t;
+          if (j >= ntiles) continue;
+          if (g < p.M)
+            __stcg(reinterpret_cast<float2*>(mine + g * p.rp + 8 * j + 2 * q), make_float2(d[t][0], d[t][1]));
+          if (g + 8 < p.M)
+            __stcg(reinterpret_cast<float2*>(mine + (g + 8) * p.rp + 8 * j + 2 * q),
+                   make_float2(d[t][2], d[t][3]));
+        }
+      }
+      __threadfence();
+      asm volatile("bar.sync 2, %0;" ::"n"(PRODUCERS) : "memory");
+      if (R == 0) s_last = atomicAdd(p.u_ticket, 1) == p.nU - 1;
+      asm volatile("bar.sync 2, %0;" ::"n"(PRODUCERS) : "memory");
+      if (!s_last) return;
+      __threadfence();
+      const int rpi = static_cast<int>(p.rp);
+      for (int i = R; i < static_cast<int>(p.M) * rpi; i += PRODUCERS) {
+        const int t = i / rpi, j = i % rpi;
+        const float* src = p.part_u + t * rpi + j;
+        const int64_t cs = 16 * p.rp;  // stride between chunks
+        float u = 0.f;
+        int64_t c = 0;
+        for (; c + 8 <= nchunks; c += 8) {  // 8 loads in flight, summed in chunk order
+          float a[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) a[k] = __ldcg(src + (c + k) * cs);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) u += a[k];
+        }
+        for (; c < nchunks; ++c) u += __ldcg(src + c * cs);
+        p.sU_out[t * p.rp + j] = j < p.r ? round16<H>(u * p.scale) : 0;
+        if (p.U_out && j < p.r) p.U_out[t * p.r + j] = u;
+      }
+      __threadfence();
+      asm volatile("bar.sync 2, %0;" ::"n"(PRODUCERS) : "memory");
+      if (R == 0) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.u_ready), "r"(1) : "memory");
     };
     if (word_path)
       for (int d = 0; d < SCALE_AHEAD && d < nst; ++d) fetch_set(d);
     int64_t rb = rb_first, ks = s_begin % p.KST;
     int slot = 0, issued = 0;
     uint32_t phase = 0;
+    bool u_done = false;
     for (int i = 0; i < nst; ++i) {
+      if (i == pre && !u_done) {  // the prefilled stages have their tables
+        u_work();
+        u_done = true;
+      }
       if (i >= STAGES &&
           !mbar_wait<false, true>(&empty_bar[slot], phase ^ 1u, kWaitEmpty, abort_p, &g_decode_error))
         break;
@@ -361,10 +506,10 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       const int set = i & (SCALE_AHEAD - 1);
       const int64_t n = rb * ROWS + R;
       switch (set) {
-        case 0: write_set(slot, n, ks, pw[0], pst[0]); break;
-        case 1: write_set(slot, n, ks, pw[1], pst[1]); break;
-        case 2: write_set(slot, n, ks, pw[2], pst[2]); break;
-        default: write_set(slot, n, ks, pw[3], pst[3]); break;
+        case 0: write_set(slot, n, ks, ps0); break;
+        case 1: write_set(slot, n, ks, ps1); break;
+        case 2: write_set(slot, n, ks, ps2); break;
+        default: write_set(slot, n, ks, ps3); break;
       }
       if (word_path && i + SCALE_AHEAD < nst) fetch_set(set);
       __syncwarp();
@@ -373,6 +518,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       if (++ks == p.KST) ks = 0, ++rb;
       if (++slot == STAGES) slot = 0, phase ^= 1u;
     }
+    if (!u_done) u_work();
     __syncthreads();  // with the consumers: everything issued has been consumed or aborted
     if (pw_idx == 0 && lane == 0 && *abort_p) {
       // never release shared memory with a copy still landing in it: only the last STAGES
@@ -385,8 +531,8 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
 
   // ============================================================ consumer warps
   const int g = lane >> 2, q = lane & 3;
-  const int blk = warp & 3;         // the 64-block of each stage this warp dequantizes
-  const int gi0 = (warp >> 2) * 2;  // its first 16-row group (two per warp)
+  const int blk = warp % BPS;             // the 64-block of each stage this warp dequantizes
+  const int gi0 = (warp / BPS) * GPW;     // its first 16-row group (GPW per warp)
   const int lora_boxes = static_cast<int>(p.rp / 64);
   auto issue_lora = [&](int64_t rb) {
     mbar_arrive_expect_tx(&lora_bar, static_cast<uint32_t>(lora_boxes * LORA_BOX_BYTES));
@@ -404,23 +550,39 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     return ld_s32(__byte_perm(word, lane_addr, 0x7604u | (j << 4)));
   };
 
-  float acc[2][NT][4];
+  float acc[GPW][NT][4];
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
+  for (int j = 0; j < GPW; ++j)
 #pragma unroll
     for (int o = 0; o < NT; ++o) acc[j][o][0] = acc[j][o][1] = acc[j][o][2] = acc[j][o][3] = 0.f;
 
   // ---------------------------------------------------------------- piece flush
-  // Adds the LoRA term if the piece starts its row block, sums the four block-warps of each
+  // Adds the LoRA term if the piece starts its row block, sums the BPS block-warps of each
   // row in a fixed order, and writes Y -- or the piece's partial sums, the last of which
-  // sums all pieces of the row block in CTA order.
+  // sums all pieces of the row block in CTA order.  The first LoRA flush stages sU, once the
+  // U flag of this launch is up.
   uint32_t lora_phase = 0;
+  bool su_staged = false;
   const int nchunks = (p.r + 15) / 16;
   auto flush = [&](int64_t rb, int64_t ks_first, int64_t ks_last) -> bool {
     if (ks_first == 0 && own_lora) {
+      if (!su_staged) {
+        if (tid == 0) wait_flag(p.u_ready, abort_p, &g_decode_error);
+        consumers_sync();
+        if (*abort_p) return false;  // uniform after the barrier
+        if (tid < 16 * (SU_PITCH / 8)) {
+          const int t = tid / (SU_PITCH / 8), c8 = tid % (SU_PITCH / 8);
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (t < p.M && 8 * c8 < p.rp)
+            v = __ldcg(reinterpret_cast<const uint4*>(p.sU_out + t * p.rp + 8 * c8));
+          *reinterpret_cast<uint4*>(sUs + t * SU_PITCH + 8 * c8) = v;
+        }
+        consumers_sync();
+        su_staged = true;
+      }
       if (blk == 0 && mbar_wait(&lora_bar, lora_phase, kWaitLora, abort_p, &g_decode_error)) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < GPW; ++j) {
           const int gi = gi0 + j;
           const int mat = lane >> 3, rr = lane & 7;
           const int R = 16 * gi + perm8(rr) + 8 * (mat & 1);
@@ -444,7 +606,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     }
     // every warp's accumulators to shared memory, lane-contiguous
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+    for (int j = 0; j < GPW; ++j)
 #pragma unroll
       for (int o = 0; o < NT; ++o)
 #pragma unroll
@@ -460,16 +622,15 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     const int R = tid & (ROWS - 1);
     const int64_t n = rb * ROWS + R;
     const int gi = R >> 4, h = (R >> 3) & 1, gg = inv_perm8(R & 7);
-    const int wb = 4 * (gi >> 1), jj = gi & 1;
+    const int wb = BPS * (gi / GPW), jj = gi % GPW;
     const int64_t slot = rb == rb_first ? 0 : 1;
     float* mine = p.part + (static_cast<int64_t>(blockIdx.x) * 2 + slot) * 16 * ROWS;
     for (int t = tid >> 7; t < p.M; t += THREADS / ROWS) {
       const int o = t >> 3, qq = (t & 7) >> 1, d = 2 * h + (t & 1);
       const int idx = ((jj * NT + o) * 4 + d) * 32 + 4 * gg + qq;
-      float v = sRed[(wb + 0) * C::ACC * 32 + idx];
-      v += sRed[(wb + 1) * C::ACC * 32 + idx];
-      v += sRed[(wb + 2) * C::ACC * 32 + idx];
-      v += sRed[(wb + 3) * C::ACC * 32 + idx];
+      float v = sRed[wb * C::ACC * 32 + idx];
+#pragma unroll
+      for (int b = 1; b < BPS; ++b) v += sRed[(wb + b) * C::ACC * 32 + idx];
       if (whole) {
         if (n < p.N) {
           if constexpr (!OWN_LORA) v += __ldg(p.Z + t * p.N + n);
@@ -507,23 +668,24 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     }
     consumers_sync();  // the shared region is free again
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+    for (int j = 0; j < GPW; ++j)
 #pragma unroll
       for (int o = 0; o < NT; ++o) acc[j][o][0] = acc[j][o][1] = acc[j][o][2] = acc[j][o][3] = 0.f;
     return true;
   };
 
   // ---------------------------------------------------------------- main loop
-  // per-lane constant shared-memory offsets: code words of rows R0, R0 + 8 of both groups,
-  // the token fragments, and the scale pairs
-  uint32_t code_off[2], scale_e[2];
+  // per-lane constant shared-memory offsets: code words of rows R0, R0 + 8 of the warp's
+  // groups (block blk lies in the stage's 128-byte box blk / 4), the token fragments, and
+  // the scale pairs
+  uint32_t code_off[GPW], scale_e[GPW];
   {
-    const int chunk = 2 * blk + (q >> 1);
+    const int chunk = 2 * (blk & 3) + (q >> 1);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < GPW; ++j) {
       const int gi = gi0 + j;
       const int R0 = 16 * gi + perm8(g);  // MMA rows g, g + 8 -> weight rows R0, R0 + 8
-      code_off[j] = R0 * 128 + ((chunk ^ (R0 & 7)) << 4) + (q & 1) * 8;
+      code_off[j] = (blk >> 2) * (ROWS * 128) + R0 * 128 + ((chunk ^ (R0 & 7)) << 4) + (q & 1) * 8;
       scale_e[j] = ((blk * 8 + gi) * 8 + g) * 2;
     }
   }
@@ -572,10 +734,10 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
         xf[o][4] = hi.x; xf[o][5] = hi.y; xf[o][6] = hi.z; xf[o][7] = hi.w;
       }
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+      for (int j = 0; j < GPW; ++j) {
         const uint2 c0 = ld_s64(cs + code_off[j]);
         const uint2 c1 = ld_s64(cs + code_off[j] + 8 * 128);
-        const float2 sc = ld_sf2(kTableBase + scale_slot_off(slot, scale_e[j]));
+        const float2 sc = ld_sf2(kTableBase + scale_slot_off<C::TAB_ROWS>(slot, scale_e[j]));
         float d[NT][4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -614,117 +776,26 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
   if (tid == 0 && lora_pending && *abort_p) mbar_drain(&lora_bar, lora_phase);
 }
 
-// U = X A^T for M <= 16 tokens.  The contraction over K is cut into 256-wide chunks, one
-// CTA each: the chunk of X (tokens padded to 16) and of A (rows padded to rp) is staged in
-// shared memory with 16-byte loads, warp w forms the [16 x 8] tile of adapter rows
-// 8 w (+ 64) on the tensor cores, and the CTA that finishes last sums the chunks in chunk
-// order and writes sU = bf16(scale U) (zero past the rank) and, when asked, U in fp32.
-constexpr int U_KC = 256;
-constexpr int U_PITCH = U_KC + 8;  // bf16 per staged row (+16 bytes: conflict-free ldmatrix)
-
-inline int small_u_smem(int64_t rp) { return static_cast<int>((16 + rp) * U_PITCH * 2); }
-
-template <bool H>
-__global__ void __launch_bounds__(256) small_u(const uint16_t* __restrict__ X, int64_t M,
-                                               int64_t K, const uint16_t* __restrict__ A, int r,
-                                               int64_t rp, float scale, uint16_t* __restrict__ sU,
-                                               float* __restrict__ U_out, float* __restrict__ part,
-                                               int* __restrict__ ticket) {
-  extern __shared__ __align__(16) uint16_t su_smem[];
-  uint16_t* sX = su_smem;               // [16][U_PITCH]
-  uint16_t* sA = su_smem + 16 * U_PITCH;  // [rp][U_PITCH]
-  __shared__ int s_last;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t k0 = static_cast<int64_t>(blockIdx.x) * U_KC;
-  const int S = gridDim.x;
-  constexpr int C8 = U_KC / 8;  // 16-byte pieces per staged row
-  // stage X (rows >= M zero) and A (rows >= r zero); columns past K zero
-  {
-    const int n = (16 + static_cast<int>(rp)) * C8;
-    for (int base = tid; base < n; base += 4 * 256) {
-      uint4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = base + u * 256;
-        const int row = i / C8, c8 = i % C8;
-        const int64_t k = k0 + 8 * c8;
-        v[u] = make_uint4(0, 0, 0, 0);
-        if (i < n && k < K) {
-          if (row < 16) {
-            if (row < M) v[u] = __ldg(reinterpret_cast<const uint4*>(X + row * K + k));
-          } else if (row - 16 < r) {
-            v[u] = __ldg(reinterpret_cast<const uint4*>(A + (row - 16) * K + k));
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = base + u * 256;
-        if (i < n) *reinterpret_cast<uint4*>(su_smem + (i / C8) * U_PITCH + 8 * (i % C8)) = v[u];
-      }
-    }
-  }
-  __syncthreads();
-  const int g = lane >> 2, q = lane & 3;
-  float* mine = part + static_cast<int64_t>(blockIdx.x) * 16 * rp;
-  for (int oc = warp; oc < rp / 8; oc += 8) {
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int kk = 0; kk < U_KC / 16; ++kk) {
-      uint32_t a0, a1, a2, a3, b0, b1;
-      // A operand: tokens x k (rows lane & 15, k half lane >> 4); B operand: k x adapter rows
-      ldsm_x4(smem_u32(sX + (lane & 15) * U_PITCH + 16 * kk + 8 * (lane >> 4)), a0, a1, a2, a3);
-      {
-        const int rr = lane & 7, half = (lane >> 3) & 1;
-        uint32_t t0, t1, t2, t3;
-        ldsm_x4(smem_u32(sA + (8 * oc + rr) * U_PITCH + 16 * kk + 8 * half), t0, t1, t2, t3);
-        b0 = t0;
-        b1 = t1;
-      }
-      mma_16816<H>(d, a0, a1, a2, a3, b0, b1);
-    }
-    // d: [0] token g / row 8 oc + 2q, [1] token g / + 1, [2] token g + 8 / 2q, [3] token g + 8
-    *reinterpret_cast<float2*>(mine + g * rp + 8 * oc + 2 * q) = make_float2(d[0], d[1]);
-    *reinterpret_cast<float2*>(mine + (g + 8) * rp + 8 * oc + 2 * q) = make_float2(d[2], d[3]);
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(ticket, 1) == S - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int rpi = static_cast<int>(rp);
-  for (int i = tid; i < static_cast<int>(M) * rpi; i += 256) {
-    const int t = i / rpi, j = i % rpi;
-    const float* src = part + t * rpi + j;
-    const int cs = 16 * rpi;  // stride between chunks
-    float u = 0.f;
-    int c = 0;
-    for (; c + 16 <= S; c += 16) {  // 16 loads in flight, summed in chunk order
-      float a[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) a[k] = __ldcg(src + (c + k) * cs);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) u += a[k];
-    }
-    for (; c < S; ++c) u += __ldcg(src + c * cs);
-    sU[t * rp + j] = j < r ? round16<H>(u * scale) : 0;
-    if (U_out && j < r) U_out[t * r + j] = u;
-  }
-  if (tid == 0) *ticket = 0;  // ready for the next launch
-}
-
 }  // namespace skinny
 
 namespace {
 
+template <int NT>
 int64_t skinny_stages(int64_t N, int64_t K) {
-  return ((N + skinny::ROWS - 1) / skinny::ROWS) * ((K + skinny::KSTEP - 1) / skinny::KSTEP);
+  return ((N + skinny::ROWS - 1) / skinny::ROWS) *
+         ((K + skinny::Cfg<NT>::KSTEP - 1) / skinny::Cfg<NT>::KSTEP);
 }
 
+template <int NT>
 int64_t skinny_ctas(int64_t N, int64_t K) {
-  const int64_t T = skinny_stages(N, K);
+  const int64_t T = skinny_stages<NT>(N, K);
   return T < num_sms() ? T : num_sms();
+}
+
+// The GEMV's split-row partial sums (two slots per CTA), then the U chunks' partials.
+uint64_t gemv_partial_bytes(int64_t N, int64_t K) {
+  const int64_t c = std::max(skinny_ctas<1>(N, K), skinny_ctas<2>(N, K));
+  return (uint64_t)round_up(c * 2 * 16 * skinny::ROWS * 4, 256);
 }
 
 template <int NT, int SCALE, bool OWN_LORA, bool H = false>
@@ -767,27 +838,13 @@ int run_decode(const CUtensorMap& tmC, const CUtensorMap& tmX, const CUtensorMap
 
 uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K, int r) {
   if (M > kSkinnyMaxM) return 0;
-  const uint64_t gemv = (uint64_t)skinny_ctas(N, K) * 2 * 16 * skinny::ROWS * 4;
   const uint64_t u = (uint64_t)((K + skinny::U_KC - 1) / skinny::U_KC) * 16 * round_up(r, 64) * 4;
-  return gemv > u ? gemv : u;
+  return gemv_partial_bytes(N, K) + u;
 }
 
-int launch_skinny_u(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  uint8_t* ws = static_cast<uint8_t*>(a.ws);
-  uint16_t* sU = reinterpret_cast<uint16_t*>(ws + L.sU);
-  static DeviceCache<int> attr_bf16, attr_f16;
-  {
-    const int st = a.half ? ensure_dynamic_smem(attr_f16, skinny::small_u<true>, skinny::small_u_smem(2 * 64))
-                          : ensure_dynamic_smem(attr_bf16, skinny::small_u<false>, skinny::small_u_smem(2 * 64));
-    if (st) return st;
-  }
-  ProfileScope ps("decode_u", stream);
-  const unsigned chunks = (unsigned)((a.K + skinny::U_KC - 1) / skinny::U_KC);
-  (a.half ? skinny::small_u<true> : skinny::small_u<false>)<<<chunks, 256,
-                                                             skinny::small_u_smem(L.rp), stream>>>(
-      a.X, a.M, a.K, a.A, a.r, L.rp, a.scale, sU, a.U, reinterpret_cast<float*>(ws + L.part),
-      reinterpret_cast<int*>(ws + L.tickets));
-  return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+uint64_t skinny_ticket_count(int64_t M, int64_t N) {
+  // a stage count per row block, then the U arrivals and the U flag
+  return M > kSkinnyMaxM ? 0 : (uint64_t)((N + skinny::ROWS - 1) / skinny::ROWS) + 2;
 }
 
 int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const float* Z,
@@ -808,19 +865,23 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
                                 MapSwizzle::B128));
   if (!mapped) return QLORA_ERR_CUDA;
   skinny::Params p{};
+  const bool wide = a.M <= 8;  // one token octet: 512-wide stages
+  const int kstep = wide ? skinny::Cfg<1>::KSTEP : skinny::Cfg<2>::KSTEP;
+  const int bps = kstep / 64;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
   p.KB = a.K / 64;
-  p.KST = (a.K + skinny::KSTEP - 1) / skinny::KSTEP;
-  p.T = skinny_stages(a.N, a.K);
+  p.KST = (a.K + kstep - 1) / kstep;
+  p.T = wide ? skinny_stages<1>(a.N, a.K) : skinny_stages<2>(a.N, a.K);
   p.qs = a.q.scale_codes;
   p.steps = a.q.scale_steps;
   p.mean = a.q.scale_mean;
-  p.qs_words = (a.q.dq_block != 0 && p.KB % 4 == 0 && reinterpret_cast<uintptr_t>(a.q.scale_codes) % 4 == 0) ? 1 : 0;
+  // a stage's scale codes of a row are whole aligned words when the blocks per row are a
+  // multiple of the stage's blocks (the pointer is 16-byte aligned)
+  p.qs_words = (a.q.dq_block != 0 && p.KB % bps == 0) ? 1 : 0;
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.tickets = reinterpret_cast<int*>(ws + L.tickets);
-  p.sU = own_lora ? reinterpret_cast<const uint16_t*>(ws + L.sU) : nullptr;
   p.rp = L.rp;
   p.r = a.r;
   p.Y = a.Y;
@@ -829,7 +890,20 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
     constexpr float Lv[16] = QLORA_NF4_LEVELS;
     for (int i = 0; i < 16; ++i) p.levels[i] = Lv[i];
   }
-  const unsigned ctas = (unsigned)skinny_ctas(a.N, a.K);
+  const unsigned ctas = (unsigned)(wide ? skinny_ctas<1>(a.N, a.K) : skinny_ctas<2>(a.N, a.K));
+  if (own_lora) {  // U inside the launch: the first CTAs take its contraction chunks
+    const int64_t nrb = (a.N + skinny::ROWS - 1) / skinny::ROWS;
+    const int64_t nchunks = (a.K + skinny::U_KC - 1) / skinny::U_KC;
+    p.nU = static_cast<int>(nchunks < (int64_t)ctas ? nchunks : (int64_t)ctas);
+    p.X = a.X;
+    p.A = a.A;
+    p.scale = a.scale;
+    p.U_out = a.U;
+    p.part_u = reinterpret_cast<float*>(ws + L.part + gemv_partial_bytes(a.N, a.K));
+    p.u_ticket = p.tickets + nrb;
+    p.u_ready = p.tickets + nrb + 1;
+    p.sU_out = reinterpret_cast<uint16_t*>(ws + L.sU);
+  }
   ProfileScope ps("decode_gemv", stream);
   const int fmt = a.q.dq_block == 0 ? skinny::kScaleAbsmax
                   : a.q.dq_type == NF4_DQ_FP8 ? skinny::kScaleFp8 : skinny::kScaleInt8;
@@ -862,8 +936,7 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
 }
 
 int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  int st = launch_skinny_u(a, L, stream);
-  if (st) return st;
+  int st;
   if (a.r % 8 && (st = launch_pad_b(a, L, stream))) return st;
   return launch_decode_gemv(a, L, nullptr, stream);
 }

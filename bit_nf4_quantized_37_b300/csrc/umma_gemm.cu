@@ -75,6 +75,14 @@ struct Params {
   const float* mean;
   int dq;         // 1: double-quantized scales; 0: steps holds the fp32 absmax per block
   int fp8;        // second-level codes are E4M3 (else int8)
+  // split contraction (single-CTA kernel): blockIdx.z takes NF4 stages
+  // [z * split_stages, (z + 1) * split_stages); the last split also runs the LoRA stages.
+  // With nsplit > 1 every CTA writes its fp32 tile to part[z] and the CTA that completes a
+  // tile (arrival ticket) sums the splits in split order and stores the 16-bit output.
+  int nsplit;
+  int split_stages;
+  float* part;    // [nsplit][M][Nout] fp32
+  int* tickets;   // [output tiles] arrivals, zero at launch, zeroed again by the last CTA
 };
 
 // One thread's share of an NF4 stage: 64 codes (32 bytes) and the block's scale code/step.
@@ -135,13 +143,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
+  __shared__ int s_last;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t n0 = (int64_t)blockIdx.x * BN;  // output-column tile
   const int64_t m0 = (int64_t)blockIdx.y * BM;  // token tile
-  const int n_main = static_cast<int>(p.Kc / BK);
-  const int total = p.n_lora + n_main;
+  const int split = static_cast<int>(blockIdx.z);
+  const int n_all = static_cast<int>(p.Kc / BK);
+  const int kc0 = split * p.split_stages;  // first NF4 stage (global k-slice) of this split
+  const int n_main = min(n_all, kc0 + p.split_stages) - kc0;
+  const bool last_split = split == p.nsplit - 1;
+  const int total = (last_split ? p.n_lora : 0) + n_main;
   volatile int* abort_p = &abort_flag;
 
   if (threadIdx.x == 0) {
@@ -185,7 +198,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         } else {
           mbar_arrive_expect_tx(&full_bar[slot], A_BYTES);
-          tma_load_2d(a_dst, &tmA, &full_bar[slot], s * BK, (int32_t)m0);
+          tma_load_2d(a_dst, &tmA, &full_bar[slot], (kc0 + s) * BK, (int32_t)m0);
         }
       }
       // never leave with a load in flight: the last issued stages must have landed
@@ -245,57 +258,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       dst_off = blk * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
       swz = nl & 7;
     }
-    auto slice_coords = [&](int kc, int64_t& row, int64_t& col) {
-      if (kMode == 0) { row = row_base; col = (int64_t)kc * BK; }
-      else { row = (int64_t)kc * BK + row_base; col = kcol; }
+    auto slice_at = [&](int s, Slice& sl) {  // local NF4 stage s of this split
+      sl.valid = false;
+      if (s >= n_main) return;
+      const int kc = kc0 + s;
+      if (kMode == 0) load_slice(sl, p, row_base, (int64_t)kc * BK);
+      else load_slice(sl, p, (int64_t)kc * BK + row_base, kcol);
     };
-    Slice pf0, pf1;  // slices two stages ahead (even / odd NF4 stage)
-    {
-      int64_t row, col;
-      if (n_main > 0) { slice_coords(0, row, col); load_slice(pf0, p, row, col); }
-      if (n_main > 1) { slice_coords(1, row, col); load_slice(pf1, p, row, col); }
-    }
-    bool ok = true;
-    for (int s = 0; s < n_main; ++s) {  // the NF4 stages (the LoRA stages after them need nothing)
+    // Slices four stages ahead in four register sets (set s & 3 holds stage s): a set is
+    // refilled right after its stage was dequantized and signalled.
+    auto body = [&](int s, Slice& cur) -> bool {
       const int slot = s % STAGES, round = s / STAGES;
-      {
-        if (round > 0 && !mbar_wait(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) {
-          ok = false;
-          break;
-        }
-        const int kc = s;
-        const Slice cur = (kc & 1) ? pf1 : pf0;  // loaded two stages ago
-        uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
-        if (cur.valid) {
-          const Nf4ByteTable tab = nf4_make_table<H>(__fmaf_rn(cur.q, cur.step, mu));
-          const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
-                                     cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
+      if (round > 0 && !mbar_wait(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
+        return false;
+      uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
+      if (cur.valid) {
+        const Nf4ByteTable tab = nf4_make_table<H>(__fmaf_rn(cur.q, cur.step, mu));
+        const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
+                                   cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t o[4];
-            nf4_dequant8(tab, words[c], o);
-            *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[4];
+          nf4_dequant8(tab, words[c], o);
+          *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        fence_proxy_async_smem();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(0, 0, 0, 0);
       }
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bready_bar[slot]);
-      // the slice two stages ahead goes into the register set just consumed; its loads are
-      // issued after the (release) arrive above, which therefore never waits for them
-      {
-        const int kc = s;
-        if (kc + 2 < n_main) {
-          int64_t row, col;
-          slice_coords(kc + 2, row, col);
-          if (kc & 1) load_slice(pf1, p, row, col);
-          else load_slice(pf0, p, row, col);
-        }
-      }
+      // the set just consumed takes the stage four ahead; its loads are issued after the
+      // (release) arrive above, which therefore never waits for them
+      slice_at(s + 4, cur);
+      return true;
+    };
+    Slice pf0, pf1, pf2, pf3;
+    slice_at(0, pf0);
+    slice_at(1, pf1);
+    slice_at(2, pf2);
+    slice_at(3, pf3);
+    bool ok = true;
+    for (int s = 0; s < n_main && ok; s += 4) {  // the NF4 stages (the LoRA stages need nothing)
+      ok = body(s, pf0);
+      if (!ok || s + 1 >= n_main) break;
+      ok = body(s + 1, pf1);
+      if (!ok || s + 2 >= n_main) break;
+      ok = body(s + 2, pf2);
+      if (!ok || s + 3 >= n_main) break;
+      ok = body(s + 3, pf3);
     }
 
     // ------------------------------------------------------------ epilogue
@@ -307,13 +320,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int col0 = kAcc == 1 ? half * 128 : 0;
       const uint32_t tbase = tmem + (kAcc == 1 ? 0u : static_cast<uint32_t>(half * 256));
       const int64_t row0 = m0 + (kAcc == 1 ? 0 : half * UM) + lg * 32;
+      const int64_t my_row = row0 + lane;
       uint8_t* buf0 = smem + (warp - DEQ_WARP0) * 4096;
+      bool store = true;
+      if (p.nsplit > 1) {
+        // this split's fp32 tile (one row per thread, 32 columns per chunk) for whichever CTA
+        // completes the tile; columns past Nout (a multiple of 64) are skipped by whole float4
+        const size_t MN = static_cast<size_t>(p.M) * p.Nout;
+        float* mine = p.part + split * MN;
 #pragma unroll 1
-      for (int c = 0; c < NCHUNK; ++c) {
+        for (int c = 0; c < NCHUNK; ++c) {
+          const int64_t col = n0 + col0 + c * 32;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + (static_cast<uint32_t>(lg * 32) << 16) + (col0 + c * 32), v);
+          tmem_ld_wait();
+          if (my_row < p.M) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (col + 4 * j < p.Nout)
+                __stcg(reinterpret_cast<float4*>(mine + my_row * p.Nout + col + 4 * j),
+                       make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+          }
+        }
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"n"(NUM_DEQ_WARPS * 32) : "memory");
+        const int tile = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
+        if (warp == DEQ_WARP0 && lane == 0)
+          s_last = atomicAdd(&p.tickets[tile], 1) == p.nsplit - 1;
+        asm volatile("bar.sync 1, %0;" ::"n"(NUM_DEQ_WARPS * 32) : "memory");
+        store = s_last != 0;
+        if (store) {
+          __threadfence();
+          if (warp == DEQ_WARP0 && lane == 0) p.tickets[tile] = 0;  // ready for the next launch
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < NCHUNK && store; ++c) {
         const int col = col0 + c * 32;
         uint32_t v[32];
         tmem_ld_32x32b_x32(tbase + (static_cast<uint32_t>(lg * 32) << 16) + col, v);
         tmem_ld_wait();
+        if (p.nsplit > 1) {
+          // the sum over the splits in split order (this CTA's own values from TMEM)
+          const size_t MN = static_cast<size_t>(p.M) * p.Nout;
+          const int64_t gcol = n0 + col;
+          const bool live = my_row < p.M;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (!live || gcol + 4 * j >= p.Nout) continue;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int z = 0; z < p.nsplit; ++z) {
+              const float4 t = z == split
+                                   ? make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]))
+                                   : __ldcg(reinterpret_cast<const float4*>(p.part + z * MN + my_row * p.Nout +
+                                                                            gcol + 4 * j));
+              if (z == 0) acc = t;
+              else acc.x += t.x, acc.y += t.y, acc.z += t.z, acc.w += t.w;
+            }
+            v[4 * j] = __float_as_uint(acc.x);
+            v[4 * j + 1] = __float_as_uint(acc.y);
+            v[4 * j + 2] = __float_as_uint(acc.z);
+            v[4 * j + 3] = __float_as_uint(acc.w);
+          }
+        }
         uint8_t* buf = buf0 + (c & 1) * 2048;
         if (c >= 2) {
           if (lane == 0) bulk_wait_read1();
@@ -652,7 +723,8 @@ bool map_bf16(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
 }
 
 template <int kMode, int kAcc, bool kPair, bool H>
-int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, const FusedPlan& plan,
+                 cudaStream_t stream) {
   using namespace fused;
   constexpr int BM = kPair ? pairk::BM_CTA : Tile<kAcc>::BM;
   constexpr int SMEM_BYTES = kPair ? pairk::SMEM_BYTES : Tile<kAcc>::SMEM_BYTES;
@@ -679,6 +751,10 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   p.fp8 = a.q.dq_type == NF4_DQ_FP8 ? 1 : 0;
   p.n_lora = static_cast<int>(rp / 64);
   p.lora_last_k16 = static_cast<int>((a.r - 64 * (p.n_lora - 1) + 15) / 16);
+  p.nsplit = plan.nsplit;
+  p.split_stages = plan.split_stages;
+  p.part = plan.nsplit > 1 ? reinterpret_cast<float*>(ws + L.gpart) : nullptr;
+  p.tickets = plan.nsplit > 1 ? reinterpret_cast<int*>(ws + L.gtickets) : nullptr;
   if (kMode == 0) {
     p.Nout = a.N;
     p.Kc = a.K;
@@ -717,7 +793,8 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
     cfg.gridDim = dim3((unsigned)(2 * ((a.M + 511) / 512)), (unsigned)((p.Nout + BN - 1) / BN));
     e = cudaLaunchKernelEx(&cfg, fused_pair_gemm<kMode, H>, tA, tA2, tB2, tOut, p);
   } else {
-    cfg.gridDim = dim3((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM));
+    cfg.gridDim = dim3((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM),
+                       (unsigned)plan.nsplit);
     e = cudaLaunchKernelEx(&cfg, fused_nf4_lora_gemm<kMode, kAcc, H>, tA, tA2, tB2, tOut, p);
   }
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
@@ -725,21 +802,57 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
 
 }  // namespace
 
-// Tile choice: CTA pairs with 512 x 256 tiles when at least half the SMs get a pair tile,
-// single CTAs with 256 x 256 tiles when those fill the SMs, else 128 x 256 tiles.
-static int tile_choice(int64_t M, int64_t Nout) {
+// Tile plan: CTA pairs with 512 x 256 tiles when at least half the pair slots get a tile;
+// single CTAs with 256 x 256 tiles when those fill the SMs; else 128 x 256 tiles, with the
+// contraction split so that tiles x splits fill the SMs once (at most 4 splits, each at least
+// 8 stages of 64) -- a few large-K tiles (M = 512 and 4096 output columns: 64 tiles on 148
+// SMs) would otherwise leave most SMs idle.
+FusedPlan fused_plan(int64_t M, int64_t Nout, int64_t Kc) {
+  FusedPlan pl{};
+  const int64_t sms = num_sms();
+  const int64_t n_all = Kc / fused::BK;
+  pl.nsplit = 1;
+  pl.split_stages = static_cast<int>(n_all);
   const int64_t pair_tiles = ((M + 511) / 512) * ((Nout + 255) / 256);
-  if (pair_tiles * 4 >= num_sms()) return 2;
-  const int64_t tiles = ((M + 255) / 256) * ((Nout + 255) / 256);
-  return tiles >= num_sms() ? 1 : 0;
+  if (pair_tiles * 4 >= sms) {
+    pl.kind = 2;
+    return pl;
+  }
+  const int64_t tiles2 = ((M + 255) / 256) * ((Nout + 255) / 256);
+  if (tiles2 >= sms) {
+    pl.kind = 1;
+    return pl;
+  }
+  pl.kind = 0;
+  const int64_t tiles1 = ((M + 127) / 128) * ((Nout + 255) / 256);
+  int64_t want = sms / tiles1;
+  if (want > 4) want = 4;
+  if (want > n_all / 8) want = n_all / 8;
+  if (want > 1) {
+    const int64_t per = (n_all + want - 1) / want;
+    pl.split_stages = static_cast<int>(per);
+    pl.nsplit = static_cast<int>((n_all + per - 1) / per);  // every split has a stage
+  }
+  pl.tiles = tiles1;
+  return pl;
+}
+
+uint64_t fused_partial_bytes(int64_t M, int64_t N, int64_t K, uint64_t* tickets) {
+  const FusedPlan f = fused_plan(M, N, K), d = fused_plan(M, K, N);
+  const uint64_t bf = f.nsplit > 1 ? (uint64_t)f.nsplit * M * N * 4 : 0;
+  const uint64_t bd = d.nsplit > 1 ? (uint64_t)d.nsplit * M * K * 4 : 0;
+  const uint64_t tf = f.nsplit > 1 ? (uint64_t)f.tiles : 0, td = d.nsplit > 1 ? (uint64_t)d.tiles : 0;
+  if (tickets) *tickets = tf > td ? tf : td;
+  return bf > bd ? bf : bd;
 }
 
 template <int kMode, bool H>
 static int launch_fused_mode(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  switch (tile_choice(a.M, kMode == 0 ? a.N : a.K)) {
-    case 2: return launch_fused<kMode, 2, true, H>(a, L, stream);
-    case 1: return launch_fused<kMode, 2, false, H>(a, L, stream);
-    default: return launch_fused<kMode, 1, false, H>(a, L, stream);
+  const FusedPlan plan = kMode == 0 ? fused_plan(a.M, a.N, a.K) : fused_plan(a.M, a.K, a.N);
+  switch (plan.kind) {
+    case 2: return launch_fused<kMode, 2, true, H>(a, L, plan, stream);
+    case 1: return launch_fused<kMode, 2, false, H>(a, L, plan, stream);
+    default: return launch_fused<kMode, 1, false, H>(a, L, plan, stream);
   }
 }
 

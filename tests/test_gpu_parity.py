@@ -300,9 +300,13 @@ def test_bad_arguments_raise():
     pb = Problem(wl.config1())
     with pytest.raises(ValueError):
         qn.qlora_linear_fwd(pb.Xd.float(), pb.qd, pb.Ad, pb.Bd, 2.0)
+    # N = 250 is not a multiple of 64: the library refuses the shape (the binding's own shape
+    # checks pass: B has N rows)
     bad = qn.NF4Tensor(pb.qd.codes, pb.qd.scale_codes, pb.qd.scale_steps, pb.qd.scale_mean, 250, 256)
     with pytest.raises(qn.QLoRAError):
-        qn.qlora_linear_fwd(pb.Xd[:, :256], bad, pb.Ad, pb.Bd, 2.0)
+        qn.qlora_linear_fwd(pb.Xd[:, :256], bad, pb.Ad, pb.Bd[:250].contiguous(), 2.0)
+    with pytest.raises(ValueError):  # B rows do not match the base's N
+        qn.qlora_linear_fwd(pb.Xd, pb.qd, pb.Ad, pb.Bd[:128].contiguous(), 2.0)
 
 
 # ------------------------------------------------------------------ merge / requantize
