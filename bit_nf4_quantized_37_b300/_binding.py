@@ -8,7 +8,9 @@ from dataclasses import dataclass
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libqlora_nf4.so")
+# QLORA_NF4_LIB may name another build of the same library (the bounds-checked variant,
+# libqlora_nf4_checked.so, built by `python -m bit_nf4_quantized_37_b300.build --checked`)
+LIB_PATH = os.environ.get("QLORA_NF4_LIB") or os.path.join(_HERE, "libqlora_nf4.so")
 
 NF4_BLOCKSIZE = 64
 NF4_DQ_BLOCK = 256

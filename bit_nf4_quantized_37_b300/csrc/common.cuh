@@ -30,6 +30,30 @@ enum WaitSite : int {
 // ~2 s of wall time, far beyond any legitimate wait in these kernels (< 10 ms each).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// ------------------------------------------------------------------ bounds-checked build
+// Built with QLORA_CHECK_BOUNDS=1 (build.py's checked library, libqlora_nf4_checked.so),
+// QLORA_CHECK tests the kernels' own index arithmetic where it is not evident from the
+// launch shape: the decode kernel's fixed shared-window offsets, the split-reduction partial
+// buffers and the arrival tickets.  A failed check records its site in the kernel family's
+// device error word (read by qlora_device_status) and the access is skipped; nothing traps.
+// In the normal build every check is the constant true and costs nothing.
+enum BoundsSite : int {
+  kBoundsWindow = 9,    // a decode-kernel shared-window offset outside its region
+  kBoundsPartial = 10,  // a split-reduction partial index outside its buffer
+  kBoundsTicket = 11,   // a ticket index outside its array, or an arrival count past its total
+};
+
+__device__ __forceinline__ bool bounds_check(bool ok, int* err, int site) {
+  if (!ok) atomicCAS(err, 0, site);
+  return ok;
+}
+
+#if defined(QLORA_CHECK_BOUNDS) && QLORA_CHECK_BOUNDS
+#define QLORA_CHECK(cond, err, site) ::qlora::bounds_check(static_cast<bool>(cond), (err), (site))
+#else
+#define QLORA_CHECK(cond, err, site) true
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -36,11 +36,13 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r) {
   // the split reductions' counters; at least one per token for the per-token adapter path
   L.ntickets = std::max<uint64_t>(std::max(side_ticket_count(M, N, K), skinny_ticket_count(M, N)),
                                   (uint64_t)kSkinnyMaxM);
-  const uint64_t gpart_bytes = M > kSkinnyMaxM ? fused_partial_bytes(M, N, K, &L.ngtickets) : 0;
-  if (M <= kSkinnyMaxM) L.ngtickets = 0;
+  // the fused GEMMs' split contraction: the forward takes them above kSkinnyMaxM tokens, the
+  // input gradient at every M
+  const uint64_t gpart_bytes = fused_partial_bytes(M, N, K, &L.ngtickets);
   L.tickets = take((L.ntickets + L.ngtickets) * 4);
   L.gtickets = L.tickets + L.ntickets * 4;
   L.gpart = take(gpart_bytes);
+  L.gpart_bytes = gpart_bytes;
   L.Z = take(M <= kSkinnyMaxM ? (uint64_t)M * N * 4 : 0);
   L.total = off;
   return L;

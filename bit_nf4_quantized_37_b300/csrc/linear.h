@@ -56,6 +56,7 @@ struct WorkspaceLayout {
   uint64_t tickets;  // int [ntickets] arrival counters of the split reductions
   uint64_t ntickets;
   uint64_t gpart;    // fp32 [nsplit][M][Nout] split-contraction tiles of the fused GEMM
+  uint64_t gpart_bytes;
   uint64_t gtickets; // int [ngtickets] its per-tile arrivals (right after the tickets above)
   uint64_t ngtickets;
   uint64_t Z;        // fp32 [M, N] per-token LoRA term (decode path, per-token adapters)

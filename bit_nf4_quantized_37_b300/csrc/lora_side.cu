@@ -106,11 +106,14 @@ __device__ __forceinline__ uint16_t round16(float v) {
 // Stage Q(c, j), c in [c_begin, c_begin + clen), into sQ[c][j] (pitch NJ + 8).  Three vector
 // layouts of the source: bf16 contiguous along c (A[j][k]), bf16 contiguous along j (B[n][j],
 // sV[m][j]) and fp32 contiguous along j (U[m][j]); anything else element by element.
-template <int NJ, bool H>
+// kick() runs once, right after the first batch of loads is issued: the caller starts the
+// big operand's TMA stream there, so the rank-r loads are not queued behind it.
+template <int NJ, bool H, typename Kick>
 __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int64_t C,
-                                        int64_t c_begin, int clen, int tid) {
+                                        int64_t c_begin, int clen, int tid, Kick&& kick) {
   constexpr int QP = NJ + 8;
   constexpr int BATCH = 8;
+  bool kicked = false;
   const uint16_t* b16 = static_cast<const uint16_t*>(qs.ptr);
   const float* f32 = static_cast<const float*>(qs.ptr);
   if (!qs.fp32 && qs.ldc == 1 && (qs.ldj % 8) == 0 && (c_begin % 8) == 0) {
@@ -125,6 +128,10 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
         v[u] = make_uint4(0, 0, 0, 0);
         if (idx < n && j < r && c_begin + 8 * c8 < C)
           v[u] = __ldg(reinterpret_cast<const uint4*>(b16 + (int64_t)j * qs.ldj + c_begin + 8 * c8));
+      }
+      if (!kicked) {
+        kick();
+        kicked = true;
       }
 #pragma unroll
       for (int u = 0; u < BATCH; ++u) {
@@ -151,6 +158,10 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
         if (idx < n && 8 * j8 < r && c_begin + c < C)
           v[u] = __ldg(reinterpret_cast<const uint4*>(b16 + (c_begin + c) * qs.ldc + 8 * j8));
       }
+      if (!kicked) {
+        kick();
+        kicked = true;
+      }
 #pragma unroll
       for (int u = 0; u < BATCH; ++u) {
         const int idx = base + u * THREADS;
@@ -173,6 +184,10 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
         if (idx < n && 4 * j4 < r && c_begin + c < C)
           v[u] = __ldg(reinterpret_cast<const float4*>(f32 + (c_begin + c) * qs.ldc + 4 * j4));
       }
+      if (!kicked) {
+        kick();
+        kicked = true;
+      }
 #pragma unroll
       for (int u = 0; u < BATCH; ++u) {
         const int idx = base + u * THREADS;
@@ -183,6 +198,8 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
       }
     }
   } else {
+    kick();
+    kicked = true;
     for (int i = tid; i < clen * NJ; i += THREADS) {
       const int c = i / NJ, j = i % NJ;
       const int64_t gc = c_begin + c;
@@ -194,12 +211,27 @@ __device__ __forceinline__ void stage_q(uint16_t* sQ, const QSrc& qs, int r, int
       sQ[c * QP + j] = round16<H>(v);
     }
   }
+  if (!kicked) kick();
+}
+
+// The outputs of one float4 piece (row, columns j0 .. j0 + 3) of the summed tile.
+template <bool H>
+__device__ __forceinline__ void epi_store(const Epi& epi, int r, int64_t row, int j0, float4 v) {
+  const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int j = j0 + e;
+    const float x = j < r ? vv[e] : 0.f;
+    if (epi.out32 && j < r) epi.out32[row * epi.ld_row + j * epi.ld_j] = x * epi.scale32;
+    if (epi.op && j < epi.op_cols) epi.op[row * epi.ld_op + j] = round16<H>(x * epi.scale_op);
+  }
 }
 
 template <bool kPCol, int NJ, bool H>
 __global__ void __launch_bounds__(THREADS, 2)
     side_gemm(const __grid_constant__ CUtensorMap tmP, int64_t R, int64_t C, QSrc qs, int r,
-              float* __restrict__ part, int* __restrict__ tickets, int64_t chunk, int S, Epi epi) {
+              float* __restrict__ part, int* __restrict__ tickets, int64_t chunk, int S, Epi epi,
+              int64_t part_cap, int64_t ticket_cap) {
   constexpr int QP = NJ + 8;  // Q row pitch in elements (+16 bytes: conflict-free ldmatrix)
   extern __shared__ uint8_t smem_raw[];
   // TMA writes 128-byte-swizzled tiles: stage buffers start on 1024-byte boundaries
@@ -242,13 +274,14 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
   };
   int issued = 0;
-  if (tid == 0) {
-    tma_prefetch_desc(&tmP);
-    for (; issued < STAGES - 1 && issued < nst; ++issued) issue(issued);
-  }
+  if (tid == 0) tma_prefetch_desc(&tmP);
   // rank-r operand for the whole contraction range, as [c][j] bf16 (zero past the rank),
-  // loaded with 16-byte vectors in batches of 8 per thread so the loads overlap
-  stage_q<NJ, H>(sQ, qs, r, C, c_begin, static_cast<int>(c_end - c_begin), tid);
+  // loaded with 16-byte vectors in batches of 8 per thread so the loads overlap; its first
+  // loads go out before the big operand's stream starts
+  stage_q<NJ, H>(sQ, qs, r, C, c_begin, static_cast<int>(c_end - c_begin), tid, [&]() {
+    if (tid == 0)
+      for (; issued < STAGES - 1 && issued < nst; ++issued) issue(issued);
+  });
 
   float acc[NJ / 8][4];
 #pragma unroll
@@ -300,13 +333,14 @@ __global__ void __launch_bounds__(THREADS, 2)
     return;
   }
 
-  // this CTA's partial sums
   const int g = lane >> 2, q = lane & 3;
+  // this CTA's partial sums
   float* mine = part + (int64_t)blockIdx.y * R * NJ;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int64_t row = r0 + warp * 16 + g + 8 * h;
-    if (row < R) {
+    if (row < R && QLORA_CHECK((int64_t)blockIdx.y * R * NJ + row * NJ + NJ <= part_cap, &g_side_error,
+                               kBoundsPartial)) {
 #pragma unroll
       for (int t = 0; t < NJ / 8; ++t)
         __stcg(reinterpret_cast<float2*>(mine + row * NJ + t * 8 + 2 * q),
@@ -315,7 +349,14 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&tickets[blockIdx.x], 1) == S - 1);
+  if (tid == 0) {
+    s_last = 0;
+    if (QLORA_CHECK(blockIdx.x < ticket_cap, &g_side_error, kBoundsTicket)) {
+      const int before = atomicAdd(&tickets[blockIdx.x], 1);
+      (void)QLORA_CHECK(before < S, &g_side_error, kBoundsTicket);
+      s_last = before == S - 1;
+    }
+  }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -327,6 +368,10 @@ __global__ void __launch_bounds__(THREADS, 2)
   constexpr int PB = PER < 2 ? PER : 2;  // pieces per pass
   constexpr int SB = 16 / PB;            // splits per batch
   const int64_t sstride = R * NJ / 4;    // float4 stride between splits
+  // the last split's rows of this tile lie inside the partial buffer
+  if (!QLORA_CHECK((int64_t)(S - 1) * R * NJ + min(R, r0 + TR) * NJ <= part_cap, &g_side_error,
+                   kBoundsPartial))
+    return;
 #pragma unroll 1
   for (int p0 = 0; p0 < PER; p0 += PB) {
     const float4* src[PB];
@@ -365,17 +410,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     for (int b = 0; b < PB; ++b) {
       if (!live[b]) continue;
       const int i = tid + (p0 + b) * THREADS;
-      const int64_t row = r0 + i / V4;
-      const int j0 = (i % V4) * 4;
-      const float vv[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = j0 + e;
-        const float x = j < r ? vv[e] : 0.f;
-        if (epi.out32 && j < r) epi.out32[row * epi.ld_row + j * epi.ld_j] = x * epi.scale32;
-        if (epi.op && j < epi.op_cols)
-          epi.op[row * epi.ld_op + j] = round16<H>(x * epi.scale_op);
-      }
+      epi_store<H>(epi, r, r0 + i / V4, (i % V4) * 4, v[b]);
     }
   }
   if (epi.op && epi.op_cols > NJ) {  // zero columns of the operand copy past NJ
@@ -439,6 +474,8 @@ int run_side_t(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_
   const Split sp = pick_split(R, C, NJ);
   float* part = reinterpret_cast<float*>(ws + L.part);
   int* tickets = reinterpret_cast<int*>(ws + L.tickets);
+  const int64_t part_cap = static_cast<int64_t>(L.part_bytes / 4);
+  const int64_t ticket_cap = static_cast<int64_t>(L.ntickets);
   CUtensorMap tm;
   // K-major: P is [R rows][C] and a box is 64 c x 128 rows; column-wise: P is [C][R] and a
   // box is 64 rows x 64 c
@@ -460,8 +497,8 @@ int run_side_t(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_
                                          side::STAGES * side::P_STAGE_BYTES + side::Q_SMEM_MAX + 1024); \
       if (st) return st;                                                                          \
     }                                                                                             \
-    side::side_gemm<kCol, nj, H><<<grid, side::THREADS, smem, stream>>>(tm, R, C, qs, r, part,      \
-                                                                     tickets, sp.chunk, sp.S, epi); \
+    side::side_gemm<kCol, nj, H><<<grid, side::THREADS, smem, stream>>>(                          \
+        tm, R, C, qs, r, part, tickets, sp.chunk, sp.S, epi, part_cap, ticket_cap);               \
     break;
     QLORA_SIDE_CASE(16)
     QLORA_SIDE_CASE(32)

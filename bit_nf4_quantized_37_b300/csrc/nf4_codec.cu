@@ -6,10 +6,10 @@
 // Three launches quantize a tensor, no host synchronization:
 //   nf4_quant_blocks   reads W once: per-64 absmax, the nearest level of w/absmax (exactly as
 //                      with an IEEE division, see below), 4-bit packing; writes the codes, the
-//                      absmax values and, per unit of 64 blocks, the fp64 pairwise sum of
-//                      its absmax.
-//   nf4_absmax_mean    up to 32 CTAs: aligned subtrees of the pairwise sum over the unit
-//                      sums.
+//                      absmax values and, per run of 8 blocks, the fp64 pairwise sum of their
+//                      absmax (a warp's perfect 8-leaf subtree, by shuffles).
+//   nf4_absmax_mean    up to 32 CTAs: aligned subtrees of the pairwise sum over those
+//                      8-block sums.
 //   nf4_double_quant   a warp per group: mean (fp32) from the subtree sums, then
 //                      step = max|a - mean| / 127, int8 codes.
 // Dequantization is one launch (nf4_dequant_kernel) built on the byte-permute table
@@ -35,7 +35,8 @@ constexpr int64_t kUnitElems = (int64_t)kBlock * kUnit;  // 4096 weights
 //
 // Full units: four lanes per 64-block, 16 weights per lane (four float4 loads, the next
 // unit's loads in flight across the unit boundary), so a block's absmax is 15 max
-// operations and two shuffles.  The exact quotient x = RN(w / a) is never needed away from a
+// operations and two shuffles; a warp's eight blocks are a perfect subtree of the mean's
+// pairwise tree, summed by three more shuffles, so full units need no CTA barrier.  The exact quotient x = RN(w / a) is never needed away from a
 // threshold: y = RN(w * RN(1/a)) is within 3 * 2^-24 * |x| of x, so whenever y is more than
 // 2^-20 from every threshold, y and x fall between the same two thresholds and the level
 // follows from y.  The level comes from a shared-memory table over cells of y (sign; cell 0
@@ -106,8 +107,8 @@ __device__ __forceinline__ uint32_t code_fast(float y, uint32_t tab_b, float& dm
 
 __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
     const float* __restrict__ W, int64_t numel, uint8_t* __restrict__ codes,
-    float* __restrict__ absmax, double* __restrict__ unit_sum) {
-  __shared__ float s_abs[2][kUnit];  // per unit, double-buffered across units
+    float* __restrict__ absmax, double* __restrict__ sum8) {
+  __shared__ float s_abs[kUnit];  // the partial last unit's absmax values
   extern __shared__ float2 s_cells[];  // 2 * kCells * kCopies entries
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nblocks = (numel + kBlock - 1) / kBlock;
@@ -127,10 +128,8 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
   float4 nxt[4];
   if (blockIdx.x < nfull) load16(blockIdx.x, nxt);
 
-  int buf = 0;
 #pragma unroll 1
-  for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x, buf ^= 1) {
-    float* sab = s_abs[buf];
+  for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
     if (u < nfull) {
       const int local_block = warp * 8 + bw;
       const int64_t b = u * kUnit + local_block;
@@ -146,9 +145,15 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
       for (int i = 1; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      if (ql == 0) {
-        sab[local_block] = m;
-        absmax[b] = m;
+      if (ql == 0) absmax[b] = m;
+      {
+        // blocks warp*8 .. warp*8+7 sit at lanes 4 bw: pair sums over bw bits 0, 1, 2 build
+        // the perfect binary tree of the eight (x + y == y + x in IEEE)
+        double t = static_cast<double>(m);
+        t += __shfl_xor_sync(0xffffffffu, t, 4);
+        t += __shfl_xor_sync(0xffffffffu, t, 8);
+        t += __shfl_xor_sync(0xffffffffu, t, 16);
+        if (lane == 0) sum8[u * 8 + warp] = t;
       }
       uint32_t c[16];
       // a tiny, infinite or NaN absmax has no usable reciprocal: exact division
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (hl == 0) {
-          sab[local_block] = m;  // blocks past the end hold 0 (all their inputs read as 0)
+          s_abs[local_block] = m;  // blocks past the end hold 0 (all their inputs read as 0)
           if (b < nblocks) absmax[b] = m;
         }
         const uint32_t c0 = code_exact(v[0], m), c1 = code_exact(v[1], m);
@@ -197,23 +202,18 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
         if (e < numel) codes[e / 2] = static_cast<uint8_t>(e + 1 < numel ? ((c0 << 4) | c1) : (c0 << 4));
         if (e + 2 < numel) codes[e / 2 + 1] = static_cast<uint8_t>(e + 3 < numel ? ((c2 << 4) | c3) : (c2 << 4));
       }
-    }
-    __syncthreads();  // the unit's absmax values are all in sab
-    if (warp == 0) {
-      // Perfect binary tree over the 64 absmax values in block order: each lane adds its two
-      // neighbours, then the xor butterfly combines lanes (x+y == y+x in IEEE).  The other
-      // warps go on with the next unit, which writes the other buffer.
-      const float* a = sab + lane * 2;
-      double sum = (double)a[0] + (double)a[1];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (lane == 0) unit_sum[u] = sum;
+      __syncthreads();  // the partial unit's absmax values are all in s_abs
+      if (warp == 0 && lane < 8) {  // its eight 8-block subtrees
+        const float* a = s_abs + lane * 8;
+        sum8[u * 8 + lane] = (((double)a[0] + (double)a[1]) + ((double)a[2] + (double)a[3])) +
+                             (((double)a[4] + (double)a[5]) + ((double)a[6] + (double)a[7]));
+      }
     }
   }
 }
 
 // -------------------------------------------------------------------- pass 2
-// The pairwise tree over the unit sums, zero-padded to a power of two P, is cut into
+// The pairwise tree over the 8-block sums, zero-padded to a power of two P, is cut into
 // nparts <= 32 aligned subtrees of P / nparts leaves, one CTA of 1024 threads each; pass 3
 // combines the subtree sums (the top levels of the same tree) and forms
 // mean = (float)(total / nblocks).  Each thread folds a run of kRun consecutive leaves (a
@@ -231,26 +231,26 @@ __device__ __forceinline__ double fold_run(const double* __restrict__ leaf, int6
   return v[0];
 }
 
-__global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict__ unit_sum,
-                                                        int64_t nunits, int64_t run,
+__global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict__ leaf_sum,
+                                                        int64_t nleaves, int64_t run,
                                                         double* __restrict__ part) {
   __shared__ double s_warp[32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   launch_dependents();     // pass 3 may be scheduled meanwhile (it waits for this grid)
-  grid_dependency_wait();  // the unit sums of pass 1
+  grid_dependency_wait();  // the 8-block sums of pass 1
   const int64_t lo = ((int64_t)blockIdx.x * 1024 + t) * run;
   double s;
   switch (run) {
-    case 1: s = fold_run<1>(unit_sum, lo, nunits); break;
-    case 2: s = fold_run<2>(unit_sum, lo, nunits); break;
-    case 4: s = fold_run<4>(unit_sum, lo, nunits); break;
-    case 8: s = fold_run<8>(unit_sum, lo, nunits); break;
-    case 16: s = fold_run<16>(unit_sum, lo, nunits); break;
+    case 1: s = fold_run<1>(leaf_sum, lo, nleaves); break;
+    case 2: s = fold_run<2>(leaf_sum, lo, nleaves); break;
+    case 4: s = fold_run<4>(leaf_sum, lo, nleaves); break;
+    case 8: s = fold_run<8>(leaf_sum, lo, nleaves); break;
+    case 16: s = fold_run<16>(leaf_sum, lo, nleaves); break;
     default: {  // very large tensors: binary-counter fold of the run, still the pairwise tree
       double stack[48];
       int depth = 0;
       for (int64_t i = 0; i < run; ++i) {
-        double v = (lo + i < nunits) ? unit_sum[lo + i] : 0.0;
+        double v = (lo + i < nleaves) ? leaf_sum[lo + i] : 0.0;
         int64_t k = i + 1;
         while ((k & 1) == 0) {
           v = stack[--depth] + v;
@@ -408,9 +408,9 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
 uint64_t quantize_workspace_bytes(int64_t numel) {
   const int64_t nb = (numel + kBlock - 1) / kBlock;
   const int64_t ng = (nb + kGroup - 1) / kGroup;
-  // absmax fp32 [ngroups * 256] (padded to whole groups), unit sums fp64 [<= 4 ngroups], then
-  // the mean's subtree sums fp64 [<= 32] in the 256-byte tail
-  return (uint64_t)ng * kGroup * 4 + (uint64_t)ng * (kGroup / kUnit) * 8 + 256;
+  // absmax fp32 [ngroups * 256] (padded to whole groups), 8-block sums fp64 [<= 32 ngroups],
+  // then the mean's subtree sums fp64 [<= 32] in the 256-byte tail
+  return (uint64_t)ng * kGroup * 4 + (uint64_t)ng * (kGroup / 8) * 8 + 256;
 }
 
 int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws,
@@ -421,6 +421,7 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   // without double quantization pass 1 writes the block absmax straight into the tensor
   float* absmax = dq ? reinterpret_cast<float*>(ws) : q.scale_steps;
   const int64_t nu = (nb + kUnit - 1) / kUnit;
+  const int64_t nleaves = nu * (kUnit / 8);  // 8-block sums
   double* usum = reinterpret_cast<double*>(reinterpret_cast<char*>(ws) + ng * kGroup * 4);
   {
     ProfileScope ps("nf4_quant_blocks", stream);
@@ -444,9 +445,9 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     nf4_quant_blocks<<<(unsigned)ctas, kQuantThreads, kCellBytes, stream>>>(W, numel, q.codes, absmax, usum);
   }
   if (!dq) return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
-  double* part = usum + ng * (kGroup / kUnit);
+  double* part = usum + ng * (kGroup / 8);
   int64_t p2 = 1;
-  while (p2 < nu) p2 *= 2;
+  while (p2 < nleaves) p2 *= 2;
   const int nparts = p2 > 1024 ? static_cast<int>(p2 / 1024 < 32 ? p2 / 1024 : 32) : 1;
   const int64_t run = p2 > 1024 * nparts ? p2 / (1024 * nparts) : 1;
   // passes 2 and 3 are programmatic dependents: launched while the pass before finishes,
@@ -462,7 +463,7 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     ProfileScope ps("nf4_absmax_mean", stream);
     cfg.gridDim = dim3(nparts);
     cfg.blockDim = dim3(1024);
-    if (cudaLaunchKernelEx(&cfg, nf4_absmax_mean, static_cast<const double*>(usum), nu, run,
+    if (cudaLaunchKernelEx(&cfg, nf4_absmax_mean, static_cast<const double*>(usum), nleaves, run,
                            part) != cudaSuccess)
       return QLORA_ERR_CUDA;
   }

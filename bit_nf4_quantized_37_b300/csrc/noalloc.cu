@@ -9,7 +9,7 @@
 // quantizer needs between its passes live in g_noalloc_quant_scratch below.
 //
 // The array is a file-scope __device__ variable, so every GPU that loads the library holds
-// it (about 4.3 MB) until the process exits.  Host code cannot hand the symbol itself to a
+// it (about 5.2 MB) until the process exits.  Host code cannot hand the symbol itself to a
 // kernel (on the host it is only a stand-in), so the first call on each device looks up
 // its device address with cudaGetSymbolAddress while that device is current and caches it
 // for that device's context; make that first call before any stream capture.  The stream
@@ -24,10 +24,10 @@ namespace qlora {
 namespace {
 
 constexpr int64_t kNoallocMaxNumel = NF4_NOALLOC_MAX_NUMEL;
-// absmax fp32 for whole groups of 256 blocks, one fp64 sum per unit of 64 blocks, 256 bytes
-// of slack: the same layout the workspace of nf4_quantize uses
+// absmax fp32 for whole groups of 256 blocks, one fp64 sum per 8 blocks, 256 bytes of
+// slack: the same layout the workspace of nf4_quantize uses
 constexpr uint64_t kNoallocScratchBytes =
-    ((kNoallocMaxNumel + 64 * 256 - 1) / (64 * 256)) * (256 * 4 + 4 * 8) + 256;
+    ((kNoallocMaxNumel + 64 * 256 - 1) / (64 * 256)) * (256 * 4 + 32 * 8) + 256;
 
 __device__ __align__(256) unsigned char g_noalloc_quant_scratch[kNoallocScratchBytes];
 

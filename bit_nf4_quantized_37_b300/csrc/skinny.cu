@@ -82,13 +82,13 @@ constexpr uint32_t kLoraBase = kTableBase + TABLE_BYTES;
 // NT token octets (M <= 8 NT).
 template <int NT>
 struct Cfg {
-  static constexpr int KSTEP = NT == 1 ? 512 : 256;       // k per stage
+  static constexpr int KSTEP = 256;                       // k per stage
   static constexpr int BPS = KSTEP / 64;                  // 64-blocks per stage
   static constexpr int GPW = BPS / 2;                     // 16-row groups per consumer warp
   static constexpr int CODE_BYTES = ROWS * KSTEP / 2;     // 32 or 16 KB (128-byte boxes)
   static constexpr int XSLOT = NT * 8 * 128;              // [8 NT tokens x 64 k] bf16
   static constexpr int STAGE_BYTES = CODE_BYTES + BPS * XSLOT;
-  static constexpr int STAGES = NT == 1 ? 3 : 5;
+  static constexpr int STAGES = NT == 1 ? 6 : 5;
   static constexpr int TAB_ROWS = ROWS * BPS / 32;        // byte-table rows of a stage's scales
   static constexpr int ACC = GPW * NT * 4;                // accumulators per lane
   static constexpr int RED_BYTES = (THREADS / 32) * 32 * ACC * 4;
@@ -165,6 +165,9 @@ struct Params {
   int qs_words;        // scale codes of a row's stage are one aligned 32-bit word
   float* part;         // [CTAs][2][16][128] fp32 pieces of split row blocks
   int* tickets;        // [row blocks] stages summed so far
+  int64_t part_cap;    // floats in part, ints in tickets, floats in part_u (bounds checks)
+  int64_t ticket_cap;
+  int64_t part_u_cap;
   int64_t rp;
   int r;
   uint16_t* Y;
@@ -423,24 +426,17 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
 #pragma unroll 1
         for (int kk = 0; kk < U_KC; kk += 64) {
           const int64_t k = c * U_KC + kk + 16 * q;
-          uint4 xa[2], xb[2], av[4][2];
-          xa[0] = ld16(p.X, g, p.M, k);
-          xa[1] = ld16(p.X, g, p.M, k + 8);
-          xb[0] = NT > 1 ? ld16(p.X, g + 8, p.M, k) : make_uint4(0, 0, 0, 0);
-          xb[1] = NT > 1 ? ld16(p.X, g + 8, p.M, k + 8) : make_uint4(0, 0, 0, 0);
+          const uint4 xa0 = ld16(p.X, g, p.M, k), xa1 = ld16(p.X, g, p.M, k + 8);
+          const uint4 xb0 = NT > 1 ? ld16(p.X, g + 8, p.M, k) : make_uint4(0, 0, 0, 0);
+          const uint4 xb1 = NT > 1 ? ld16(p.X, g + 8, p.M, k + 8) : make_uint4(0, 0, 0, 0);
+          const uint32_t xw[8] = {xa0.x, xa0.y, xa0.z, xa0.w, xa1.x, xa1.y, xa1.z, xa1.w};
+          const uint32_t yw[8] = {xb0.x, xb0.y, xb0.z, xb0.w, xb1.x, xb1.y, xb1.z, xb1.w};
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const int j = pw_idx + 4 * t;
-            av[t][0] = j < ntiles ? ld16(p.A, 8 * j + g, p.r, k) : make_uint4(0, 0, 0, 0);
-            av[t][1] = j < ntiles ? ld16(p.A, 8 * j + g, p.r, k + 8) : make_uint4(0, 0, 0, 0);
-          }
-          const uint32_t xw[8] = {xa[0].x, xa[0].y, xa[0].z, xa[0].w, xa[1].x, xa[1].y, xa[1].z, xa[1].w};
-          const uint32_t yw[8] = {xb[0].x, xb[0].y, xb[0].z, xb[0].w, xb[1].x, xb[1].y, xb[1].z, xb[1].w};
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            if (pw_idx + 4 * t >= ntiles) continue;
-            const uint32_t aw[8] = {av[t][0].x, av[t][0].y, av[t][0].z, av[t][0].w,
-                                    av[t][1].x, av[t][1].y, av[t][1].z, av[t][1].w};
+            if (j >= ntiles) continue;
+            const uint4 a0 = ld16(p.A, 8 * j + g, p.r, k), a1 = ld16(p.A, 8 * j + g, p.r, k + 8);
+            const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
             for (int m = 0; m < 4; ++m)
               mma_16816<H>(d[t], xw[2 * m], yw[2 * m], xw[2 * m + 1], yw[2 * m + 1], aw[2 * m],
@@ -448,21 +444,25 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
           }
         }
         // d[t]: [0] token g / adapter row 8j + 2q, [1] + 1, [2] token g + 8 / 8j + 2q, [3] + 1
-        float* mine = p.part_u + c * 16 * p.rp;
+        const int64_t base = c * 16 * p.rp;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const int j = pw_idx + 4 * t;
           if (j >= ntiles) continue;
-          if (g < p.M)
-            __stcg(reinterpret_cast<float2*>(mine + g * p.rp + 8 * j + 2 * q), make_float2(d[t][0], d[t][1]));
-          if (g + 8 < p.M)
-            __stcg(reinterpret_cast<float2*>(mine + (g + 8) * p.rp + 8 * j + 2 * q),
-                   make_float2(d[t][2], d[t][3]));
+          const int64_t i0 = base + g * p.rp + 8 * j + 2 * q, i1 = i0 + 8 * p.rp;
+          if (g < p.M && QLORA_CHECK(i0 + 2 <= p.part_u_cap, &g_decode_error, kBoundsPartial))
+            __stcg(reinterpret_cast<float2*>(p.part_u + i0), make_float2(d[t][0], d[t][1]));
+          if (g + 8 < p.M && QLORA_CHECK(i1 + 2 <= p.part_u_cap, &g_decode_error, kBoundsPartial))
+            __stcg(reinterpret_cast<float2*>(p.part_u + i1), make_float2(d[t][2], d[t][3]));
         }
       }
       __threadfence();
       asm volatile("bar.sync 2, %0;" ::"n"(PRODUCERS) : "memory");
-      if (R == 0) s_last = atomicAdd(p.u_ticket, 1) == p.nU - 1;
+      if (R == 0) {
+        const int before = atomicAdd(p.u_ticket, 1);
+        (void)QLORA_CHECK(before < p.nU, &g_decode_error, kBoundsTicket);
+        s_last = before == p.nU - 1;
+      }
       asm volatile("bar.sync 2, %0;" ::"n"(PRODUCERS) : "memory");
       if (!s_last) return;
       __threadfence();
@@ -473,6 +473,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
         const int64_t cs = 16 * p.rp;  // stride between chunks
         float u = 0.f;
         int64_t c = 0;
+        (void)QLORA_CHECK((nchunks - 1) * cs + t * rpi + j < p.part_u_cap, &g_decode_error, kBoundsPartial);
         for (; c + 8 <= nchunks; c += 8) {  // 8 loads in flight, summed in chunk order
           float a[8];
 #pragma unroll
@@ -624,7 +625,8 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     const int gi = R >> 4, h = (R >> 3) & 1, gg = inv_perm8(R & 7);
     const int wb = BPS * (gi / GPW), jj = gi % GPW;
     const int64_t slot = rb == rb_first ? 0 : 1;
-    float* mine = p.part + (static_cast<int64_t>(blockIdx.x) * 2 + slot) * 16 * ROWS;
+    const int64_t mine_at = (static_cast<int64_t>(blockIdx.x) * 2 + slot) * 16 * ROWS;
+    float* mine = p.part + mine_at;
     for (int t = tid >> 7; t < p.M; t += THREADS / ROWS) {
       const int o = t >> 3, qq = (t & 7) >> 1, d = 2 * h + (t & 1);
       const int idx = ((jj * NT + o) * 4 + d) * 32 + 4 * gg + qq;
@@ -636,7 +638,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
           if constexpr (!OWN_LORA) v += __ldg(p.Z + t * p.N + n);
           p.Y[t * p.N + n] = round16<H>(v);
         }
-      } else {
+      } else if (QLORA_CHECK(mine_at + t * ROWS + R < p.part_cap, &g_decode_error, kBoundsPartial)) {
         __stcg(mine + t * ROWS + R, v);
       }
     }
@@ -645,7 +647,13 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
       consumers_sync();
       if (tid == 0) {
         const int add = static_cast<int>(ks_last - ks_first + 1);
-        s_last = atomicAdd(&p.tickets[rb], add) + add == p.KST;
+        if (QLORA_CHECK(rb < p.ticket_cap, &g_decode_error, kBoundsTicket)) {
+          const int after = atomicAdd(&p.tickets[rb], add) + add;
+          (void)QLORA_CHECK(after <= p.KST, &g_decode_error, kBoundsTicket);
+          s_last = after == p.KST;
+        } else {
+          s_last = 0;
+        }
       }
       consumers_sync();
       if (s_last) {
@@ -656,7 +664,8 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
           float v = 0.f;
           for (int64_t c = c_lo; c <= c_hi; ++c) {
             const int64_t sl = rb == stage_begin(p.T, G, c) / p.KST ? 0 : 1;
-            v += __ldcg(p.part + (c * 2 + sl) * 16 * ROWS + t * ROWS + R);
+            const int64_t at = (c * 2 + sl) * 16 * ROWS + t * ROWS + R;
+            if (QLORA_CHECK(at < p.part_cap, &g_decode_error, kBoundsPartial)) v += __ldcg(p.part + at);
           }
           if (n < p.N) {
             if constexpr (!OWN_LORA) v += __ldg(p.Z + t * p.N + n);
@@ -699,6 +708,24 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     x_off[o][1] = CODE_BYTES + blk * C::XSLOT + t * 128 + (((2 * q + 1) ^ g) << 4);
   }
   const uint32_t stage_s = kStageBase;
+  // the lane's fixed window offsets stay inside their regions: code words inside the stage's
+  // code tile, token fragments inside the stage, scale pairs inside the upper halves of the
+  // byte-table rows of their slot (a failed check skips the shared reads)
+  bool window_ok = true;
+#pragma unroll
+  for (int j = 0; j < GPW; ++j) {
+    window_ok &= QLORA_CHECK(code_off[j] + 8 * 128 + 8 <= static_cast<uint32_t>(CODE_BYTES),
+                             &g_decode_error, kBoundsWindow);
+    window_ok &= QLORA_CHECK(scale_e[j] + 1 < static_cast<uint32_t>(ROWS * BPS) &&
+                                 (scale_slot_off<C::TAB_ROWS>(STAGES - 1, scale_e[j]) & 255u) >= 128u &&
+                                 scale_slot_off<C::TAB_ROWS>(STAGES - 1, scale_e[j]) + 8 <= TABLE_BYTES,
+                             &g_decode_error, kBoundsWindow);
+  }
+#pragma unroll
+  for (int o = 0; o < NT; ++o)
+    window_ok &= QLORA_CHECK(!x_live[o] || x_off[o][1] + 16 <= static_cast<uint32_t>(C::STAGE_BYTES),
+                             &g_decode_error, kBoundsWindow);
+  window_ok &= QLORA_CHECK(stage_s + STAGES * C::STAGE_BYTES <= C::SU_BASE, &g_decode_error, kBoundsWindow);
 
   bool ok = true;
   // 32-bit bookkeeping in the loop: stage counts per CTA and per row block are small
@@ -720,7 +747,7 @@ __global__ void __launch_bounds__(THREADS + PRODUCERS, 1)
     }
     const bool got =
         mbar_wait<false, true>(&full_bar[slot], phase, kWaitTmaFull, abort_p, &g_decode_error);
-    if (got) {
+    if (got && window_ok) {
       const uint32_t cs = stage_s + slot * C::STAGE_BYTES;
       uint32_t xf[NT][8];
 #pragma unroll
@@ -882,6 +909,8 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
   p.qs_words = (a.q.dq_block != 0 && p.KB % bps == 0) ? 1 : 0;
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.tickets = reinterpret_cast<int*>(ws + L.tickets);
+  p.part_cap = static_cast<int64_t>(gemv_partial_bytes(a.N, a.K) / 4);
+  p.ticket_cap = static_cast<int64_t>((a.N + skinny::ROWS - 1) / skinny::ROWS);
   p.rp = L.rp;
   p.r = a.r;
   p.Y = a.Y;
@@ -900,6 +929,7 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
     p.scale = a.scale;
     p.U_out = a.U;
     p.part_u = reinterpret_cast<float*>(ws + L.part + gemv_partial_bytes(a.N, a.K));
+    p.part_u_cap = static_cast<int64_t>((L.part_bytes - gemv_partial_bytes(a.N, a.K)) / 4);
     p.u_ticket = p.tickets + nrb;
     p.u_ready = p.tickets + nrb + 1;
     p.sU_out = reinterpret_cast<uint16_t*>(ws + L.sU);

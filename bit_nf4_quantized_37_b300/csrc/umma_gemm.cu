@@ -83,6 +83,7 @@ struct Params {
   int split_stages;
   float* part;    // [nsplit][M][Nout] fp32
   int* tickets;   // [output tiles] arrivals, zero at launch, zeroed again by the last CTA
+  int64_t part_cap, ticket_cap;  // floats in part, ints in tickets (bounds checks)
 };
 
 // One thread's share of an NF4 stage: 64 codes (32 bytes) and the block's scale code/step.
@@ -123,6 +124,91 @@ __device__ __forceinline__ void bulk_wait_read1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ------------------------------------------------------------ split contraction epilogue
+// With nsplit > 1 every CTA first writes its fp32 tile: one output row per thread (my_row),
+// nchunk 32-column chunks read from TMEM at taddr + tcol0 + 32 c, for output columns
+// gcol0 + 32 c (columns past Nout, a multiple of 64, skipped by whole float4).  Then the
+// 256 epilogue threads (named barrier 1) take the tile's arrival ticket; the CTA completing
+// the tile returns true and sums the splits chunk by chunk with split_sum.  Without a split
+// it returns true at once.
+__device__ __forceinline__ bool split_epilogue_partial(const Params& p, int split, uint32_t taddr,
+                                                       int64_t my_row, int64_t gcol0, int nchunk,
+                                                       int tcol0, bool ticket_thread, int tile,
+                                                       int& s_last) {
+  if (p.nsplit <= 1) return true;
+  const size_t MN = static_cast<size_t>(p.M) * p.Nout;
+  float* mine = p.part + split * MN;
+  const bool in_part = QLORA_CHECK(static_cast<int64_t>(p.nsplit * MN) <= p.part_cap, &g_gemm_error,
+                                   kBoundsPartial);
+#pragma unroll 1
+  for (int c = 0; c < nchunk; ++c) {
+    const int64_t col = gcol0 + c * 32;
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(taddr + tcol0 + c * 32, v);
+    tmem_ld_wait();
+    if (my_row < p.M && in_part) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (col + 4 * j < p.Nout)
+          __stcg(reinterpret_cast<float4*>(mine + my_row * p.Nout + col + 4 * j),
+                 make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+    }
+  }
+  __threadfence();
+  asm volatile("bar.sync 1, %0;" ::"n"(NUM_DEQ_WARPS * 32) : "memory");
+  if (ticket_thread) {
+    s_last = 0;
+    if (QLORA_CHECK(tile < p.ticket_cap, &g_gemm_error, kBoundsTicket)) {
+      const int before = atomicAdd(&p.tickets[tile], 1);
+      (void)QLORA_CHECK(before < p.nsplit, &g_gemm_error, kBoundsTicket);
+      s_last = before == p.nsplit - 1;
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(NUM_DEQ_WARPS * 32) : "memory");
+  const bool last = s_last != 0;
+  if (last) {
+    __threadfence();
+    if (ticket_thread) p.tickets[tile] = 0;  // ready for the next launch
+  }
+  return last;
+}
+
+// v: this CTA's 32 values of row my_row at output columns gcol .. gcol + 31 (from TMEM);
+// becomes the sum over the splits in split order (the other splits' values from part).
+__device__ __forceinline__ void split_sum(const Params& p, int split, int64_t my_row, int64_t gcol,
+                                          uint32_t (&v)[32]) {
+  if (p.nsplit <= 1 || my_row >= p.M) return;
+  const size_t MN = static_cast<size_t>(p.M) * p.Nout;
+  if (!QLORA_CHECK(static_cast<int64_t>(p.nsplit * MN) <= p.part_cap, &g_gemm_error, kBoundsPartial))
+    return;
+  // all loads of the chunk first (up to 4 splits x 8 float4 in flight), then the sums in
+  // split order
+  constexpr int kMaxSplit = 4;
+  float4 t[kMaxSplit][8];
+#pragma unroll
+  for (int z = 0; z < kMaxSplit; ++z)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (z < p.nsplit && z != split && gcol + 4 * j < p.Nout)
+        t[z][j] = __ldcg(reinterpret_cast<const float4*>(p.part + z * MN + my_row * p.Nout + gcol + 4 * j));
+      else
+        t[z][j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                              __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+    }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float4 acc = t[0][j];
+#pragma unroll
+    for (int z = 1; z < kMaxSplit; ++z)
+      if (z < p.nsplit) acc.x += t[z][j].x, acc.y += t[z][j].y, acc.z += t[z][j].z, acc.w += t[z][j].w;
+    v[4 * j] = __float_as_uint(acc.x);
+    v[4 * j + 1] = __float_as_uint(acc.y);
+    v[4 * j + 2] = __float_as_uint(acc.z);
+    v[4 * j + 3] = __float_as_uint(acc.w);
+  }
+}
 
 // kMode 0: forward (W tile K-major), 1: input gradient (MN-major).  H: the fp16 compute type
 // (operands, dequantized tiles and output in fp16), else bf16.
@@ -322,69 +408,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t row0 = m0 + (kAcc == 1 ? 0 : half * UM) + lg * 32;
       const int64_t my_row = row0 + lane;
       uint8_t* buf0 = smem + (warp - DEQ_WARP0) * 4096;
-      bool store = true;
-      if (p.nsplit > 1) {
-        // this split's fp32 tile (one row per thread, 32 columns per chunk) for whichever CTA
-        // completes the tile; columns past Nout (a multiple of 64) are skipped by whole float4
-        const size_t MN = static_cast<size_t>(p.M) * p.Nout;
-        float* mine = p.part + split * MN;
-#pragma unroll 1
-        for (int c = 0; c < NCHUNK; ++c) {
-          const int64_t col = n0 + col0 + c * 32;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + (static_cast<uint32_t>(lg * 32) << 16) + (col0 + c * 32), v);
-          tmem_ld_wait();
-          if (my_row < p.M) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (col + 4 * j < p.Nout)
-                __stcg(reinterpret_cast<float4*>(mine + my_row * p.Nout + col + 4 * j),
-                       make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
-          }
-        }
-        __threadfence();
-        asm volatile("bar.sync 1, %0;" ::"n"(NUM_DEQ_WARPS * 32) : "memory");
-        const int tile = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
-        if (warp == DEQ_WARP0 && lane == 0)
-          s_last = atomicAdd(&p.tickets[tile], 1) == p.nsplit - 1;
-        asm volatile("bar.sync 1, %0;" ::"n"(NUM_DEQ_WARPS * 32) : "memory");
-        store = s_last != 0;
-        if (store) {
-          __threadfence();
-          if (warp == DEQ_WARP0 && lane == 0) p.tickets[tile] = 0;  // ready for the next launch
-        }
-      }
+      const bool store = split_epilogue_partial(p, split, tbase + (static_cast<uint32_t>(lg * 32) << 16),
+                                                my_row, n0 + col0, NCHUNK, col0,
+                                                warp == DEQ_WARP0 && lane == 0,
+                                                static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), s_last);
 #pragma unroll 1
       for (int c = 0; c < NCHUNK && store; ++c) {
         const int col = col0 + c * 32;
         uint32_t v[32];
         tmem_ld_32x32b_x32(tbase + (static_cast<uint32_t>(lg * 32) << 16) + col, v);
         tmem_ld_wait();
-        if (p.nsplit > 1) {
-          // the sum over the splits in split order (this CTA's own values from TMEM)
-          const size_t MN = static_cast<size_t>(p.M) * p.Nout;
-          const int64_t gcol = n0 + col;
-          const bool live = my_row < p.M;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (!live || gcol + 4 * j >= p.Nout) continue;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int z = 0; z < p.nsplit; ++z) {
-              const float4 t = z == split
-                                   ? make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]))
-                                   : __ldcg(reinterpret_cast<const float4*>(p.part + z * MN + my_row * p.Nout +
-                                                                            gcol + 4 * j));
-              if (z == 0) acc = t;
-              else acc.x += t.x, acc.y += t.y, acc.z += t.z, acc.w += t.w;
-            }
-            v[4 * j] = __float_as_uint(acc.x);
-            v[4 * j + 1] = __float_as_uint(acc.y);
-            v[4 * j + 2] = __float_as_uint(acc.z);
-            v[4 * j + 3] = __float_as_uint(acc.w);
-          }
-        }
+        split_sum(p, split, my_row, n0 + col, v);
         uint8_t* buf = buf0 + (c & 1) * 2048;
         if (c >= 2) {
           if (lane == 0) bulk_wait_read1();
@@ -468,6 +502,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
+  __shared__ int s_last;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -475,8 +510,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int64_t m0 = (int64_t)(blockIdx.x >> 1) * 512 + rank * BM_CTA;  // this CTA's A rows
   const int64_t n0 = (int64_t)blockIdx.y * BN;                          // pair's columns
   const int64_t nb0 = n0 + rank * BN_CTA;                               // this CTA's W half
-  const int n_main = static_cast<int>(p.Kc / BK);
-  const int total = p.n_lora + n_main;
+  const int split = static_cast<int>(blockIdx.z);
+  const int n_all = static_cast<int>(p.Kc / BK);
+  const int kc0 = split * p.split_stages;  // first NF4 stage (global k-slice) of this split
+  const int n_main = min(n_all, kc0 + p.split_stages) - kc0;
+  const int total = (split == p.nsplit - 1 ? p.n_lora : 0) + n_main;
   volatile int* abort_p = &abort_flag;
 
   if (threadIdx.x == 0) {
@@ -525,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           }
         } else {
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[slot], 2 * A_BYTES);
-          tma_load_2d_pair(a_dst, &tmA, full_lead, s * BK, (int32_t)m0);
+          tma_load_2d_pair(a_dst, &tmA, full_lead, (kc0 + s) * BK, (int32_t)m0);
         }
       }
       // the leader's full barriers count both CTAs' copies: the leader drains them
@@ -600,8 +638,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       dst_off = blk * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
       swz = nl & 7;
     }
-    auto slice_at = [&](int s, Slice& sl) {
-      const int kc = s;
+    auto slice_at = [&](int s, Slice& sl) {  // local NF4 stage s of this split
+      const int kc = kc0 + s;
       if (kMode == 0) load_slice(sl, p, row_base, (int64_t)kc * BK);
       else load_slice(sl, p, (int64_t)kc * BK + row_base, kcol);
     };
@@ -669,13 +707,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int acc = (warp - DEQ_WARP0) >> 2;           // accumulator (128-row slab)
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * 256);
       const int64_t row0 = m0 + acc * UM + lg * 32;
+      const int64_t my_row = row0 + lane;
       uint8_t* buf0 = smem + (warp - DEQ_WARP0) * 4096;
+      const bool store = split_epilogue_partial(p, split, tbase + (static_cast<uint32_t>(lg * 32) << 16),
+                                                my_row, n0, 8, 0, warp == DEQ_WARP0 && lane == 0,
+                                                static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x),
+                                                s_last);
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 8 && store; ++c) {
         const int col = c * 32;
         uint32_t v[32];
         tmem_ld_32x32b_x32(tbase + (static_cast<uint32_t>(lg * 32) << 16) + col, v);
         tmem_ld_wait();
+        split_sum(p, split, my_row, n0 + col, v);
         uint8_t* buf = buf0 + (c & 1) * 2048;
         if (c >= 2) {
           if (lane == 0) bulk_wait_read1();
@@ -753,8 +797,13 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, const FusedPlan&
   p.lora_last_k16 = static_cast<int>((a.r - 64 * (p.n_lora - 1) + 15) / 16);
   p.nsplit = plan.nsplit;
   p.split_stages = plan.split_stages;
+  if (plan.nsplit > 1 &&  // the workspace layout must have made room for the split tiles
+      (L.gpart_bytes < (uint64_t)plan.nsplit * a.M * p.Nout * 4 || L.ngtickets < (uint64_t)plan.tiles))
+    return QLORA_ERR_WORKSPACE;
   p.part = plan.nsplit > 1 ? reinterpret_cast<float*>(ws + L.gpart) : nullptr;
   p.tickets = plan.nsplit > 1 ? reinterpret_cast<int*>(ws + L.gtickets) : nullptr;
+  p.part_cap = static_cast<int64_t>(L.gpart_bytes / 4);
+  p.ticket_cap = static_cast<int64_t>(L.ngtickets);
   if (kMode == 0) {
     p.Nout = a.N;
     p.Kc = a.K;
@@ -790,7 +839,8 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, const FusedPlan&
   cfg.numAttrs = a.gemm_priority ? 2 : 1;
   cudaError_t e;
   if (kPair) {  // the CTA pair is the kernel's compile-time cluster shape
-    cfg.gridDim = dim3((unsigned)(2 * ((a.M + 511) / 512)), (unsigned)((p.Nout + BN - 1) / BN));
+    cfg.gridDim = dim3((unsigned)(2 * ((a.M + 511) / 512)), (unsigned)((p.Nout + BN - 1) / BN),
+                       (unsigned)plan.nsplit);
     e = cudaLaunchKernelEx(&cfg, fused_pair_gemm<kMode, H>, tA, tA2, tB2, tOut, p);
   } else {
     cfg.gridDim = dim3((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM),
@@ -802,37 +852,50 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, const FusedPlan&
 
 }  // namespace
 
-// Tile plan: CTA pairs with 512 x 256 tiles when at least half the pair slots get a tile;
-// single CTAs with 256 x 256 tiles when those fill the SMs; else 128 x 256 tiles, with the
-// contraction split so that tiles x splits fill the SMs once (at most 4 splits, each at least
-// 8 stages of 64) -- a few large-K tiles (M = 512 and 4096 output columns: 64 tiles on 148
-// SMs) would otherwise leave most SMs idle.
-FusedPlan fused_plan(int64_t M, int64_t Nout, int64_t Kc) {
-  FusedPlan pl{};
-  const int64_t sms = num_sms();
-  const int64_t n_all = Kc / fused::BK;
-  pl.nsplit = 1;
-  pl.split_stages = static_cast<int>(n_all);
-  const int64_t pair_tiles = ((M + 511) / 512) * ((Nout + 255) / 256);
-  if (pair_tiles * 4 >= sms) {
-    pl.kind = 2;
-    return pl;
-  }
-  const int64_t tiles2 = ((M + 255) / 256) * ((Nout + 255) / 256);
-  if (tiles2 >= sms) {
-    pl.kind = 1;
-    return pl;
-  }
-  pl.kind = 0;
-  const int64_t tiles1 = ((M + 127) / 128) * ((Nout + 255) / 256);
-  int64_t want = sms / tiles1;
+// Tile plan.  CTA pairs with 512 x 256 tiles when the tiles give at least half the pair
+// slots work; single CTAs with 256 x 256 tiles when those fill the SMs; else 128 x 256
+// tiles, with the contraction split (up to 4 splits of at least 8 stages of 64) so that
+// tiles x splits fill the SMs once.  The pair kernel takes a split contraction too (blockIdx.z),
+// which no plan selects at present.
+namespace {
+void split_into(FusedPlan& pl, int64_t n_all, int64_t want) {
   if (want > 4) want = 4;
   if (want > n_all / 8) want = n_all / 8;
+  pl.nsplit = 1;
+  pl.split_stages = static_cast<int>(n_all);
   if (want > 1) {
     const int64_t per = (n_all + want - 1) / want;
     pl.split_stages = static_cast<int>(per);
     pl.nsplit = static_cast<int>((n_all + per - 1) / per);  // every split has a stage
   }
+}
+}  // namespace
+
+FusedPlan fused_plan(int64_t M, int64_t Nout, int64_t Kc) {
+  FusedPlan pl{};
+  const int64_t sms = num_sms();
+  const int64_t pair_slots = sms / 2;
+  const int64_t n_all = Kc / fused::BK;
+  const int64_t pair_tiles = ((M + 511) / 512) * ((Nout + 255) / 256);
+  // measured at M = 512 with 4096 output columns: 16 pair tiles x 4 splits ran at 255
+  // TFLOP/s, 64 single-CTA tiles x 2 splits at 294 -- a pair's 256 KB fp32 tile per split
+  // makes the sum of the splits long; pairs stay unsplit
+  split_into(pl, n_all, 1);
+  if (pair_tiles * 2 >= pair_slots) {
+    pl.kind = 2;
+    pl.tiles = 2 * pair_tiles;  // CTA tiles (each CTA of a pair takes its own ticket)
+    return pl;
+  }
+  split_into(pl, n_all, 1);
+  const int64_t tiles2 = ((M + 255) / 256) * ((Nout + 255) / 256);
+  if (tiles2 >= sms) {
+    pl.kind = 1;
+    pl.tiles = tiles2;
+    return pl;
+  }
+  pl.kind = 0;
+  const int64_t tiles1 = ((M + 127) / 128) * ((Nout + 255) / 256);
+  split_into(pl, n_all, sms / tiles1);
   pl.tiles = tiles1;
   return pl;
 }

@@ -132,7 +132,7 @@ int nf4_quantize(const float* W, const nf4_tensor* out, void* workspace,
  * its implicit synchronization) off the request path.  The QLoRA pages have no counterpart
  * to this call; it computes exactly what nf4_quantize computes (bit-identical outputs).
  * Its scratch is a file-scope device array of the library sized for NF4_NOALLOC_MAX_NUMEL
- * weights (about 4.3 MB, held by every GPU that loads the library until exit); the call
+ * weights (about 5.2 MB, held by every GPU that loads the library until exit); the call
  * itself allocates nothing.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current (again after the device's context is
  * created anew, e.g. after cudaDeviceReset), so make that first call before any stream

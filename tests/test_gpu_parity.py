@@ -171,6 +171,10 @@ SMALL = [
     ("rank12", 150, 256, 320, 12, 24.0),     # rank not a multiple of 8: padded B path
     ("rank3", 40, 192, 128, 3, 6.0),
     ("tokens9_rank13", 9, 320, 256, 13, 26.0),
+    # few tokens, long contractions: the input gradient on 128-row tiles with a split
+    # contraction (its workspace is needed below the decode path's token limit too)
+    ("tokens1_split", 1, 2048, 4096, 64, 16.0),
+    ("tokens5_split", 5, 1088, 2560, 24, 48.0),
 ]
 
 
@@ -186,11 +190,15 @@ def test_fwd_bwd_small(name, M, N, K, r, alpha):
 @pytest.mark.parametrize("M,N,K,r", [(2000, 4800, 320, 24),    # forward on CTA pairs
                                      (2000, 320, 4800, 40),    # input gradient on CTA pairs
                                      (2100, 4864, 256, 16),    # forward pairs, 5th pair row partial
-                                     (2100, 256, 4864, 16)])   # input gradient, the same
+                                     (2100, 256, 4864, 16),    # input gradient, the same
+                                     (512, 3072, 3072, 16),    # 128-row tiles, 3-way split contraction
+                                     (400, 3072, 2560, 24)])   # the same, rows past M in the tile
 def test_pair_tiles_every_output(M, N, K, r):
-    """The CTA-pair GEMMs (512 x 256 tiles) against the oracle on every output element: all
-    16 row classes of a pair tile (2 CTAs x 2 accumulators x 4 TMEM lane groups), partial
-    last tiles in M and in the output columns."""
+    """The fused GEMMs against the oracle on every output element: the CTA pairs (512 x 256
+    tiles: all 16 row classes of a pair tile -- 2 CTAs x 2 accumulators x 4 TMEM lane groups
+    -- and partial last tiles in M and in the output columns), and single-CTA tiles with the
+    contraction split (fp32 tiles summed in split order by the CTA completing the tile) in
+    both directions."""
     p = wl.LinearProblem(f"pairs-{M}-{N}-{K}", M, N, K, r, 2.0 * r, 0.02, 0.001, config=60 + r)
     pb = Problem(p)
     Y, U = _check_fwd(pb)

@@ -249,3 +249,12 @@ def test_per_device_setup_cache_keying(tmp_path):
                    check=True)
     r = subprocess.run([exe], capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.strip() == "OK", r.stdout + r.stderr
+
+
+def test_checked_variant_builds_and_exports_every_symbol():
+    """The bounds-checked build (QLORA_CHECK_BOUNDS=1) compiles for sm_103a and exports the
+    same C ABI (its GPU test runs the small parity cases through it)."""
+    from bit_nf4_quantized_37_b300 import build
+    lib = ctypes.CDLL(build.build(checked=True))
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
