@@ -51,14 +51,19 @@ constexpr int NUM_DEQ_WARPS = 8;
 // is (128 kAcc) x 256, so each dequantized weight feeds 256 kAcc FLOPs.  The byte-permute
 // dequantizer runs on the integer (ALU) pipe, which a 128-row tile saturates before the
 // tensor pipe; two accumulators halve the ALU work per FLOP.
+// The A tiles (X / dY, by TMA) and the B tiles (the dequantized W tile) sit in rings of their
+// own, the B ring the deeper one: the MMA thread waited for B tiles, never for A tiles (each
+// stage is now dequantized into registers before its B slot is free, so a freed slot only
+// takes the stores).  The LoRA stages take an A and a B slot, by TMA.
 template <int kAcc>
 struct Tile {
   static constexpr int BM = UM * kAcc;
-  static constexpr int STAGES = kAcc == 1 ? 4 : 3;
+  static constexpr int SA = 3;                  // A ring
+  static constexpr int SB = kAcc == 1 ? 5 : 4;  // B ring
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int B_BASE = SA * A_BYTES;
   static constexpr int TMEM_COLS = 256 * kAcc;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  static constexpr int SMEM_BYTES = SA * A_BYTES + SB * B_BYTES + 1024;
 };
 
 struct Params {
@@ -219,12 +224,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmB2,
                         const __grid_constant__ CUtensorMap tmOut, const Params p) {
   using T = Tile<kAcc>;
-  constexpr int BM = T::BM, STAGES = T::STAGES, A_BYTES = T::A_BYTES;
-  constexpr int STAGE_BYTES = T::STAGE_BYTES, TMEM_COLS = T::TMEM_COLS;
+  constexpr int BM = T::BM, SA = T::SA, SB = T::SB, A_BYTES = T::A_BYTES, B_BASE = T::B_BASE;
+  constexpr int TMEM_COLS = T::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[STAGES];
-  __shared__ __align__(8) uint64_t bready_bar[STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t a_full[SA];
+  __shared__ __align__(8) uint64_t a_empty[SA];
+  __shared__ __align__(8) uint64_t bready_bar[SB];
+  __shared__ __align__(8) uint64_t b_empty[SB];
   __shared__ __align__(8) uint64_t acc_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -244,10 +250,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_p = &abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < SA; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < SB; ++i) {
       mbar_init(&bready_bar[i], NUM_DEQ_WARPS);
-      mbar_init(&empty_bar[i], 1);
+      mbar_init(&b_empty[i], 1);
     }
     mbar_init(&acc_bar, 1);
     abort_flag = 0;
@@ -266,30 +275,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB2);
       for (int s = 0; s < total; ++s) {
-        const int slot = s % STAGES, round = s / STAGES;
-        if (round > 0 && !mbar_wait(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) break;
-        uint8_t* a_dst = smem + slot * STAGE_BYTES;
-        uint8_t* b_dst = a_dst + A_BYTES;
+        const int as = s % SA, ar = s / SA;
+        if (ar > 0 && !mbar_wait(&a_empty[as], (ar - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) break;
+        uint8_t* a_dst = smem + as * A_BYTES;
         if (s >= n_main) {
+          // a LoRA stage: its B tile comes by TMA into the B slot, once that slot is free
+          const int bs = s % SB, br = s / SB;
+          if (br > 0 && !mbar_wait(&b_empty[bs], (br - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) break;
+          uint8_t* b_dst = smem + B_BASE + bs * B_BYTES;
           const int li = s - n_main;
           if (li == 0) grid_dependency_wait();  // sU / sV (and Bp) come from the kernel before
-          mbar_arrive_expect_tx(&full_bar[slot], A_BYTES + B_BYTES);
-          tma_load_2d(a_dst, &tmA2, &full_bar[slot], li * BK, (int32_t)m0);
+          mbar_arrive_expect_tx(&a_full[as], A_BYTES + B_BYTES);
+          tma_load_2d(a_dst, &tmA2, &a_full[as], li * BK, (int32_t)m0);
           if (kMode == 0) {
-            tma_load_2d(b_dst, &tmB2, &full_bar[slot], li * BK, (int32_t)n0);
+            tma_load_2d(b_dst, &tmB2, &a_full[as], li * BK, (int32_t)n0);
           } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              tma_load_2d(b_dst + i * 8192, &tmB2, &full_bar[slot], (int32_t)(n0 + 64 * i), li * BK);
+              tma_load_2d(b_dst + i * 8192, &tmB2, &a_full[as], (int32_t)(n0 + 64 * i), li * BK);
           }
         } else {
-          mbar_arrive_expect_tx(&full_bar[slot], A_BYTES);
-          tma_load_2d(a_dst, &tmA, &full_bar[slot], (kc0 + s) * BK, (int32_t)m0);
+          mbar_arrive_expect_tx(&a_full[as], A_BYTES);
+          tma_load_2d(a_dst, &tmA, &a_full[as], (kc0 + s) * BK, (int32_t)m0);
         }
       }
       // never leave with a load in flight: the last issued stages must have landed
-      for (int s = total - STAGES < 0 ? 0 : total - STAGES; s < total; ++s)
-        mbar_wait(&full_bar[s % STAGES], (s / STAGES) & 1, kWaitTmaFull, abort_p, &g_gemm_error);
+      for (int s = total - SA < 0 ? 0 : total - SA; s < total; ++s)
+        mbar_wait(&a_full[s % SA], (s / SA) & 1, kWaitTmaFull, abort_p, &g_gemm_error);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -298,15 +310,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(UM, BN, 0, kMode, H);
       bool ok = true;
       for (int s = 0; s < total && ok; ++s) {
-        const int slot = s % STAGES, round = s / STAGES;
+        const int as = s % SA, ar = s / SA, bs = s % SB, br = s / SB;
         // the LoRA stages (the last ones) come entirely by TMA: no dequantized tile to wait for
-        ok = mbar_wait(&full_bar[slot], round & 1, kWaitTmaFull, abort_p, &g_gemm_error) &&
+        ok = mbar_wait(&a_full[as], ar & 1, kWaitTmaFull, abort_p, &g_gemm_error) &&
              (s >= n_main ||
-              mbar_wait(&bready_bar[slot], round & 1, kWaitBReady, abort_p, &g_gemm_error));
+              mbar_wait(&bready_bar[bs], br & 1, kWaitBReady, abort_p, &g_gemm_error));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(smem + slot * STAGE_BYTES);
-        const uint32_t b_addr = a_addr + A_BYTES;
+        const uint32_t a_addr = smem_u32(smem + as * A_BYTES);
+        const uint32_t b_addr = smem_u32(smem + B_BASE + bs * B_BYTES);
         const int ksteps = (s >= n_main && s == total - 1) ? p.lora_last_k16 : 4;
         for (int kk = 0; kk < ksteps; ++kk) {
           const uint64_t bdesc = (kMode == 0)
@@ -320,7 +332,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             umma_bf16_ss<1>(tmem + acc * 256, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        umma_commit(&empty_bar[slot]);
+        umma_commit(&a_empty[as]);
+        umma_commit(&b_empty[bs]);
       }
       if (ok) umma_commit(&acc_bar);
     }
@@ -352,12 +365,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       else load_slice(sl, p, (int64_t)kc * BK + row_base, kcol);
     };
     // Slices four stages ahead in four register sets (set s & 3 holds stage s): a set is
-    // refilled right after its stage was dequantized and signalled.
+    // refilled right after its stage was stored and signalled.  Each stage is dequantized into
+    // registers before its B slot is free, so a freed slot only takes the stores.
     auto body = [&](int s, Slice& cur) -> bool {
-      const int slot = s % STAGES, round = s / STAGES;
-      if (round > 0 && !mbar_wait(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
-        return false;
-      uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
+      const int slot = s % SB, round = s / SB;
+      uint4 rv[8];
       if (cur.valid) {
         const Nf4ByteTable tab = nf4_make_table<H>(__fmaf_rn(cur.q, cur.step, mu));
         const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
@@ -366,13 +378,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < 8; ++c) {
           uint32_t o[4];
           nf4_dequant8(tab, words[c], o);
-          *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          rv[c] = make_uint4(o[0], o[1], o[2], o[3]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 8; ++c) rv[c] = make_uint4(0, 0, 0, 0);
       }
+      if (round > 0 && !mbar_wait(&b_empty[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
+        return false;
+      uint8_t* dst = smem + B_BASE + slot * B_BYTES + dst_off;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = rv[c];
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bready_bar[slot]);
@@ -461,25 +477,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // TMEM accumulators per CTA.  Each SM now dequantizes 8192 weights per stage for 4 x 128 x 256
 // x 64 multiply-adds: twice the tensor work per integer-pipe instruction of the single-CTA
 // 256 x 256 tile, and a quarter of its W tile in shared memory.
-//   full_bar   (leader) TMA bytes of both CTAs            waited by the leader's UMMA thread
+//   a_full     (leader) TMA bytes of both CTAs            waited by the leader's UMMA thread
+//   a_empty    (each)   multicast tcgen05.commit          waited by each CTA's TMA thread
 //   bready_bar (leader) the leader's 4 dequant warps + one peer relay lane, waited by the
 //                       leader's UMMA thread
 //   pready_bar (peer)   the peer's 4 dequant warps        waited by the peer's relay lane
-// The dequant warps signal at CTA scope only; one lane of the peer per ring slot forwards
+// The dequant warps signal at CTA scope only; one lane of the peer per B slot forwards
 // each stage to the leader with a single cluster-scope release (measured: a cluster-scope
 // release costs ~0.6 us, more than the dequantization of a stage; one per warp and stage
 // made the dequant warps the bottleneck, one thread for all stages made it the relay).
-//   empty_bar  (each)   multicast tcgen05.commit          waited by each CTA's producers
+//   b_empty    (each)   multicast tcgen05.commit          waited by each CTA's dequant warps
+//                                                         (and TMA thread, LoRA stages)
 //   acc_bar    (each)   multicast tcgen05.commit          waited by each CTA's epilogue
 // Two dequant groups of 4 warps take alternate stages (one 64-weight block per thread each).
+// The A tiles (X / dY, by TMA) and the B tiles (dequantized W halves) sit in two rings of
+// their own.  The B ring is the deeper one (six stages against four): a B slot goes round a
+// longer loop -- the MMA's commit reaches both CTAs, the dequant warps store the stage they
+// hold in registers, fence and signal, and the peer's relay forwards its half with a
+// cluster-scope release -- measured at ~2 us on the 4096^2 step, so with one ring of four the
+// MMA thread waited ~0.3 us for every stage's B tile while the A tiles were always there.  The
+// LoRA stages take an A slot and a B slot, both by TMA.
 namespace pairk {
 constexpr int BM_CTA = 256;
 constexpr int BN_CTA = 128;
-constexpr int STAGES = 4;
+constexpr int SA = 4;                      // A ring
+constexpr int SB = 6;                      // B ring
 constexpr int A_BYTES = BM_CTA * BK * 2;   // 32 KB
 constexpr int B_BYTES = BN_CTA * BK * 2;   // 16 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr int B_BASE = SA * A_BYTES;
+constexpr int SMEM_BYTES = SA * A_BYTES + SB * B_BYTES + 1024;
 constexpr int GROUP_WARPS = 4;
 constexpr int TMEM_COLS = 512;
 }  // namespace pairk
@@ -490,14 +516,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB2,
                     const __grid_constant__ CUtensorMap tmOut, const Params p) {
-  using pairk::BM_CTA; using pairk::BN_CTA; using pairk::STAGES; using pairk::A_BYTES;
-  using pairk::STAGE_BYTES; using pairk::GROUP_WARPS; using pairk::TMEM_COLS;
+  using pairk::BM_CTA; using pairk::BN_CTA; using pairk::SA; using pairk::SB; using pairk::A_BYTES;
+  using pairk::B_BASE; using pairk::GROUP_WARPS; using pairk::TMEM_COLS;
   constexpr int B_BYTES = pairk::B_BYTES;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[STAGES];
-  __shared__ __align__(8) uint64_t bready_bar[STAGES];
-  __shared__ __align__(8) uint64_t pready_bar[STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t a_full[SA];    // (leader) TMA bytes of both CTAs
+  __shared__ __align__(8) uint64_t a_empty[SA];   // (each) multicast commit of the stage's MMAs
+  __shared__ __align__(8) uint64_t bready_bar[SB];
+  __shared__ __align__(8) uint64_t pready_bar[SB];
+  __shared__ __align__(8) uint64_t b_empty[SB];   // (each) multicast commit
   __shared__ __align__(8) uint64_t acc_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -518,11 +545,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_p = &abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < SA; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < SB; ++i) {
       mbar_init(&bready_bar[i], GROUP_WARPS + 1);
       mbar_init(&pready_bar[i], GROUP_WARPS);
-      mbar_init(&empty_bar[i], 1);
+      mbar_init(&b_empty[i], 1);
     }
     mbar_init(&acc_bar, 1);
     abort_flag = 0;
@@ -542,17 +572,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB2);
       for (int s = 0; s < total; ++s) {
-        const int slot = s % STAGES, round = s / STAGES;
-        if (round > 0 &&
-            !mbar_wait<true>(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
+        const int as = s % SA, ar = s / SA;
+        if (ar > 0 &&
+            !mbar_wait<true>(&a_empty[as], (ar - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
           break;
-        const uint32_t full_lead = mapa_shared(smem_u32(&full_bar[slot]), 0);
-        uint8_t* a_dst = smem + slot * STAGE_BYTES;
-        uint8_t* b_dst = a_dst + A_BYTES;
+        const uint32_t full_lead = mapa_shared(smem_u32(&a_full[as]), 0);
+        uint8_t* a_dst = smem + as * A_BYTES;
         if (s >= n_main) {
+          // a LoRA stage: its B tile comes by TMA into the B slot, once that slot is free
+          const int bs = s % SB, br = s / SB;
+          if (br > 0 &&
+              !mbar_wait<true>(&b_empty[bs], (br - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
+            break;
+          uint8_t* b_dst = smem + B_BASE + bs * B_BYTES;
           const int li = s - n_main;
           if (li == 0) grid_dependency_wait();  // sU / sV (and Bp) come from the kernel before
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[slot], 2 * (A_BYTES + B_BYTES));
+          if (rank == 0) mbar_arrive_expect_tx(&a_full[as], 2 * (A_BYTES + B_BYTES));
           tma_load_2d_pair(a_dst, &tmA2, full_lead, li * BK, (int32_t)m0);
           if (kMode == 0) {
             tma_load_2d_pair(b_dst, &tmB2, full_lead, li * BK, (int32_t)nb0);
@@ -562,14 +597,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
               tma_load_2d_pair(b_dst + i * 8192, &tmB2, full_lead, (int32_t)(nb0 + 64 * i), li * BK);
           }
         } else {
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[slot], 2 * A_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&a_full[as], 2 * A_BYTES);
           tma_load_2d_pair(a_dst, &tmA, full_lead, (kc0 + s) * BK, (int32_t)m0);
         }
       }
       // the leader's full barriers count both CTAs' copies: the leader drains them
       if (rank == 0)
-        for (int s = total - STAGES < 0 ? 0 : total - STAGES; s < total; ++s)
-          mbar_drain(&full_bar[s % STAGES], (s / STAGES) & 1);
+        for (int s = total - SA < 0 ? 0 : total - SA; s < total; ++s)
+          mbar_drain(&a_full[s % SA], (s / SA) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -578,15 +613,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(2 * UM, BN, 0, kMode, H);
       bool ok = true;
       for (int s = 0; s < total && ok; ++s) {
-        const int slot = s % STAGES, round = s / STAGES;
+        const int as = s % SA, ar = s / SA, bs = s % SB, br = s / SB;
         // the LoRA stages (the last ones) come entirely by TMA: no dequantized tile to wait for
-        ok = mbar_wait<true>(&full_bar[slot], round & 1, kWaitTmaFull, abort_p, &g_gemm_error) &&
+        ok = mbar_wait<true>(&a_full[as], ar & 1, kWaitTmaFull, abort_p, &g_gemm_error) &&
              (s >= n_main ||
-              mbar_wait<true>(&bready_bar[slot], round & 1, kWaitBReady, abort_p, &g_gemm_error));
+              mbar_wait<true>(&bready_bar[bs], br & 1, kWaitBReady, abort_p, &g_gemm_error));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(smem + slot * STAGE_BYTES);
-        const uint32_t b_addr = a_addr + A_BYTES;
+        const uint32_t a_addr = smem_u32(smem + as * A_BYTES);
+        const uint32_t b_addr = smem_u32(smem + B_BASE + bs * B_BYTES);
         const int ksteps = (s >= n_main && s == total - 1) ? p.lora_last_k16 : 4;
         for (int kk = 0; kk < ksteps; ++kk) {
           const uint64_t bdesc = (kMode == 0)
@@ -599,7 +634,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             umma_bf16_ss<2>(tmem + acc * 256, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        umma_commit_pair(&empty_bar[slot], 0x3);
+        umma_commit_pair(&a_empty[as], 0x3);
+        umma_commit_pair(&b_empty[bs], 0x3);
       }
       if (ok) umma_commit_pair(&acc_bar, 0x3);
     }
@@ -607,12 +643,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ relay (peer)
     // each stage's dequantized half of the peer, forwarded to the leader's bready barrier;
-    // one lane per ring slot, so the (slow) cluster-scope releases of consecutive stages
-    // are in flight together
-    if (rank == 1 && lane < STAGES) {
+    // one lane per B slot, so the (slow) cluster-scope releases of consecutive stages are in
+    // flight together
+    if (rank == 1 && lane < SB) {
       const uint32_t bready_lead = mapa_shared(smem_u32(&bready_bar[lane]), 0);
-      for (int s = lane; s < n_main; s += STAGES) {
-        if (!mbar_wait(&pready_bar[lane], (s / STAGES) & 1, kWaitBReady, abort_p, &g_gemm_error))
+      for (int s = lane; s < n_main; s += SB) {
+        if (!mbar_wait(&pready_bar[lane], (s / SB) & 1, kWaitBReady, abort_p, &g_gemm_error))
           break;
         mbar_arrive_cluster(bready_lead);
       }
@@ -665,12 +701,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
     };
     auto put = [&](int s) -> bool {  // NF4 stages only
-      const int slot = s % STAGES, round = s / STAGES;
+      const int slot = s % SB, round = s / SB;
       {
         if (round > 0 &&
-            !mbar_wait<true>(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
+            !mbar_wait<true>(&b_empty[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
           return false;
-        uint8_t* dst = smem + slot * STAGE_BYTES + A_BYTES + dst_off;
+        uint8_t* dst = smem + B_BASE + slot * B_BYTES + dst_off;
 #pragma unroll
         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = rv[c];
         // this CTA's generic-proxy writes, ordered before the tensor core's (async-proxy)
