@@ -50,9 +50,11 @@ int launch_wait_selftest(cudaStream_t stream);
 uint64_t quantize_workspace_bytes(int64_t numel);
 int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws,
                     cudaStream_t stream);
-// out: bf16, or fp16 when half
+// out: bf16, or fp16 when half.  dependent: launched as a programmatic dependent of the
+// kernel before it in the stream (it reads nothing that kernel writes, and its CTAs wait for
+// that kernel before they exit, so its completion implies the other's).
 int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, bool half,
-                      cudaStream_t stream);
+                      cudaStream_t stream, bool dependent = false);
 
 // Adapter merge and NF4-vs-INT4 error statistics (merge.cu).
 int launch_merge(const nf4_tensor& q, const uint16_t* A, const uint16_t* B, int r, float scale,

@@ -1,7 +1,7 @@
 // linear.cu -- orchestration of the LoRA-wrapped NF4 linear layer.
 //
-// forward   pad adapters -> U = X A^T (sU = 16-bit(s U)) -> fused GEMM (M > 16) or the decode
-//           kernel (M <= 16)
+// forward   pad adapters -> U = X A^T (sU = 16-bit(s U)) -> [W' dequantized once, for GEMM
+//           plans with a staged base] -> fused GEMM (M > 16) or the decode kernel (M <= 16)
 // backward  U (saved or recomputed) -> V = dY B (sV) -> fused input-gradient GEMM, with
 //           dB = s dY^T U and dA = (X^T sV)^T on a side stream meanwhile
 // The NF4 buffers are only read (junaidshaukat.com recipe item 3: the base never moves).
@@ -30,6 +30,8 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r) {
   L.sU = take((uint64_t)M * L.rp * 2);
   L.sV = take((uint64_t)M * L.rp * 2);
   L.U32 = take((uint64_t)M * r * 4);
+  L.dbpart_bytes = fused_db(M, N, K, r) ? (uint64_t)((M + 127) / 128) * N * 64 : 0;
+  L.dbpart = take(L.dbpart_bytes);
   L.Bp = take(r % 8 ? (uint64_t)N * L.rp * 2 : 0);
   L.part_bytes = std::max(side_partial_bytes(M, N, K, r), skinny_partial_bytes(M, N, K, r));
   L.part = take(L.part_bytes);
@@ -44,6 +46,8 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r) {
   L.gpart = take(gpart_bytes);
   L.gpart_bytes = gpart_bytes;
   L.Z = take(M <= kSkinnyMaxM ? (uint64_t)M * N * 4 : 0);
+  L.Wd_bytes = (fused_plan(M, N, K).wstage || fused_plan(M, K, N).wstage) ? (uint64_t)N * K * 2 : 0;
+  L.Wd = take(L.Wd_bytes);
   L.total = off;
   return L;
 }
@@ -62,13 +66,24 @@ static int clear_tickets(const LinearArgs& a, const WorkspaceLayout& L, cudaStre
 
 int linear_forward(const LinearArgs& a, cudaStream_t stream) {
   const WorkspaceLayout L = workspace_layout(a.M, a.N, a.K, a.r);
-  int st = clear_tickets(a, L, stream);
-  if (st) return st;
+  const bool small = a.adapter_idx || a.M <= kSkinnyMaxM;
+  int st = QLORA_OK;
+  // the narrow U zeroes the arrival tickets itself
+  if ((small || !side_narrow_u(a)) && (st = clear_tickets(a, L, stream))) return st;
   if (a.adapter_idx) return launch_multi_fwd(a, L, stream);  // M <= 16, checked by the caller
   if (a.M <= kSkinnyMaxM) return launch_skinny_fwd(a, L, stream);
   if ((st = launch_lora_u(a, L, a.U, stream))) return st;
   if (a.r % 8 && (st = launch_pad_b(a, L, stream))) return st;
+  if (fused_plan(a.M, a.N, a.K).wstage && (st = launch_stage_base(a, L, stream))) return st;
   return launch_fused_fwd(a, L, stream);
+}
+
+int launch_stage_base(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+  if (L.Wd_bytes < (uint64_t)a.N * a.K * 2) return QLORA_ERR_WORKSPACE;
+  // a programmatic dependent of the rank-r product before it: the two run side by side
+  return launch_dequantize(a.q, a.N * a.K,
+                           reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.ws) + L.Wd), a.half,
+                           stream, /*dependent=*/true);
 }
 
 namespace {
@@ -118,18 +133,21 @@ SideContext* side_context() {
 
 int linear_backward(const LinearArgs& a, cudaStream_t stream) {
   const WorkspaceLayout L = workspace_layout(a.M, a.N, a.K, a.r);
-  int st = clear_tickets(a, L, stream);
-  if (st) return st;
+  int st = QLORA_OK;
+  // the narrow V zeroes the arrival tickets itself, unless a recomputed U before it uses them
+  if ((!a.U_in || !side_narrow_v(a)) && (st = clear_tickets(a, L, stream))) return st;
   const float* u32 = a.U_in;
   if (!u32) {
     float* w = reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + L.U32);
-    if ((st = launch_lora_u(a, L, w, stream))) return st;
+    if ((st = launch_lora_u(a, L, w, stream, /*narrow_ok=*/false))) return st;
     u32 = w;
   }
-  if ((st = launch_lora_v(a, L, stream))) return st;
+  if ((st = launch_lora_v(a, L, u32, stream))) return st;
   SideContext* sc = a.dX ? side_context() : nullptr;
+  const bool wstage = a.dX && fused_plan(a.M, a.K, a.N).wstage;
   if (!sc) {
     if ((st = launch_lora_db(a, L, u32, stream))) return st;
+    if (wstage && (st = launch_stage_base(a, L, stream))) return st;
     if (a.dX && (st = launch_fused_dx(a, L, stream))) return st;
     return launch_lora_da(a, L, stream);
   }
@@ -138,6 +156,7 @@ int linear_backward(const LinearArgs& a, cudaStream_t stream) {
   if (cudaEventRecord(sc->fork, stream) != cudaSuccess) return QLORA_ERR_CUDA;
   LinearArgs hi = a;
   hi.gemm_priority = sc->prio_hi;
+  if (wstage && (st = launch_stage_base(a, L, stream))) return st;
   if ((st = launch_fused_dx(hi, L, stream))) return st;
   if (cudaStreamWaitEvent(sc->side, sc->fork, 0) != cudaSuccess) return QLORA_ERR_CUDA;
   if ((st = launch_lora_db(a, L, u32, sc->side))) return st;

@@ -50,6 +50,8 @@ struct WorkspaceLayout {
   uint64_t sU;       // 16-bit [M, rp]  scale * U (columns past r: read as TMA zero fill)
   uint64_t sV;       // 16-bit [M, rp]  scale * V (the same)
   uint64_t U32;      // fp32 [M, r]   U recomputed by the backward when none is saved
+  uint64_t dbpart;   // fp32 [ceil(M/128)][N][16] dB partials of the narrow V (rank <= 16)
+  uint64_t dbpart_bytes;
   uint64_t Bp;       // 16-bit [N, rp]  B zero-padded (only for r not a multiple of 8)
   uint64_t part;     // fp32 split-contraction partial sums (side products, decode path)
   uint64_t part_bytes;
@@ -60,6 +62,8 @@ struct WorkspaceLayout {
   uint64_t gtickets; // int [ngtickets] its per-tile arrivals (right after the tickets above)
   uint64_t ngtickets;
   uint64_t Z;        // fp32 [M, N] per-token LoRA term (decode path, per-token adapters)
+  uint64_t Wd;       // 16-bit [N, K] W' dequantized once, for GEMM plans with a staged base
+  uint64_t Wd_bytes;
   uint64_t total;
 };
 
@@ -69,11 +73,15 @@ uint64_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int r);
 // Tile plan of a fused GEMM with Nout output columns and contraction Kc: kind 2 = CTA pairs
 // (512 x 256 tiles), 1 = single CTAs with 256 x 256 tiles, 0 = 128 x 256 tiles; the
 // contraction is cut into nsplit runs of split_stages 64-wide stages (tiles: the output tiles).
+// wstage: W' is dequantized once into the workspace beforehand and every stage's W tile
+// comes by TMA (128-row tiles past one row tile, where each weight would otherwise be
+// dequantized once per row tile).
 struct FusedPlan {
   int kind;
   int nsplit;
   int split_stages;
   int64_t tiles;
+  int wstage;
 };
 FusedPlan fused_plan(int64_t M, int64_t Nout, int64_t Kc);
 // Workspace of the split contraction (the larger of the forward and the input gradient) and,
@@ -85,9 +93,12 @@ int linear_backward(const LinearArgs& a, cudaStream_t stream);
 
 // ---- kernels behind the orchestration (umma_gemm.cu, lora_side.cu, skinny.cu)
 // Fused tcgen05 GEMMs.  Forward: Y = [X | sU] [W' | Bp]^T.  Input gradient:
-// dX = [dY | sV] [W' ; Ap].  W' is dequantized inside the kernel.
+// dX = [dY | sV] [W' ; Ap].  W' is dequantized inside the kernel, or read by TMA from the
+// workspace for plans with a staged base.
 int launch_fused_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 int launch_fused_dx(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+// W' = dequantize(q) into the workspace region Wd, for plans with a staged base.
+int launch_stage_base(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 // Decode path (M <= 16): Y = X W'^T + sU Bp^T with the weights streamed once.
 int launch_skinny_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 // The GEMV: forms U = X A^T inside the launch and the LoRA term from sU and B on the tensor
@@ -99,13 +110,21 @@ int launch_decode_gemv(const LinearArgs& a, const WorkspaceLayout& L, const floa
 int launch_multi_fwd(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 // Rank-r side products on the tensor cores (mma.sync), split over the contraction, with the
 // split reduction done by the last CTA of each row tile (lora_side.cu).
-int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cudaStream_t stream);
-int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
+int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cudaStream_t stream,
+                  bool narrow_ok = true);
+// Whether U / V take the narrow form (one CTA per 128-row tile beside a pair GEMM); that form
+// also zeroes the call's arrival tickets, so the call needs no memset.
+bool side_narrow_u(const LinearArgs& a);
+bool side_narrow_v(const LinearArgs& a);
+int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, const float* u32,
+                  cudaStream_t stream);
 int launch_lora_db(const LinearArgs& a, const WorkspaceLayout& L, const float* u32,
                    cudaStream_t stream);
 int launch_lora_da(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 int launch_pad_b(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream);
 uint64_t side_partial_bytes(int64_t M, int64_t N, int64_t K, int r);
+// Whether the backward's V forms the dB partials (and launch_lora_db only sums them).
+bool fused_db(int64_t M, int64_t N, int64_t K, int r);
 uint64_t side_ticket_count(int64_t M, int64_t N, int64_t K);
 uint64_t skinny_partial_bytes(int64_t M, int64_t N, int64_t K, int r);
 uint64_t skinny_ticket_count(int64_t M, int64_t N);

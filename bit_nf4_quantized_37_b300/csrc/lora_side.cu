@@ -95,6 +95,15 @@ struct Epi {
   int64_t ld_op;
   int op_cols;
   float scale_op;
+  // narrow V only (rank <= 16): with db_part set, also the partial products of
+  // dB = dY^T U16 over this CTA's 128 rows, U16 = 16-bit(u_src) (fp32 [R][r]):
+  // db_part[row tile][c][16] fp32 for every contraction index c of P
+  const float* u_src;
+  float* db_part;
+  // narrow form only: CTA 0 zeroes zero_tickets[0, nzero) first (the arrival counters of the
+  // split reductions later in the call), in place of a memset launch
+  int* zero_tickets;
+  int64_t nzero;
 };
 
 // One fp32 value rounded to the 16-bit type (bf16, or fp16 when H).
@@ -423,6 +432,214 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (tid == 0) tickets[blockIdx.x] = 0;  // ready for the next launch
 }
 
+// Narrow form of the row-wise products U = X A^T and V = dY B, for launches whose row tiles
+// alone leave most SMs free: one CTA per 128-row tile takes the whole contraction, so there
+// are no split partials and no ticket, and the rank-r operand streams beside P in the same
+// TMA ring instead of being staged up front.  A fused GEMM launched behind it as a
+// programmatic dependent then finds most SMs free for its first wave and only needs this
+// output at its LoRA stage, after its NF4 stages.
+// P is row-major: one [64 c x 128 rows] box per stage, 128-byte swizzled.
+//   kQRows: Q is [r rows][C] with c contiguous (A of U): one [64 c x NJ rows] box per stage,
+//           128-byte swizzled, read with plain ldmatrix (rows j, 8 consecutive c);
+//   else    Q is [C rows][rq] with j contiguous (B of V): one [NJ j x 64 c] box per stage,
+//           read with ldmatrix.trans.
+// Rows past r (or past rq) arrive as zeros.
+// kDB (V with rank <= 16): the dY tile of each stage also feeds the partial products of
+// dB = dY^T U over the CTA's 128 rows.  Warp w takes 16 columns of the stage (w & 3) and 8 of
+// the rank (w >> 2): an m16n8k16 with A = the tile read transposed (ldmatrix.trans) and B = the
+// rows' U in the 16-bit type, held in registers for the whole launch.  A fixed-order sum of
+// the row tiles' partials (db_reduce) finishes dB.
+template <int NJ>
+struct Narrow {
+  static constexpr int Q_STAGE_BYTES = NJ * TC * 2;
+  static constexpr int STAGE_BYTES = P_STAGE_BYTES + Q_STAGE_BYTES;
+  static constexpr int STAGES = (160 * 1024) / STAGE_BYTES < 8 ? (160 * 1024) / STAGE_BYTES : 8;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+};
+
+template <bool kQRows, int NJ, bool H, bool kDB>
+__global__ void __launch_bounds__(THREADS, 1)
+    side_rows(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
+              int64_t R, int64_t C, int r, Epi epi) {
+  using G = Narrow<NJ>;
+  constexpr int S = G::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sP = smem;                          // S x [128 rows x 64 c], 128-byte swizzled
+  uint8_t* sQ = smem + S * P_STAGE_BYTES;      // S x Q tile (1 KB multiples: swizzle atoms)
+  __shared__ __align__(8) uint64_t full_bar[S];
+  __shared__ int abort_flag;
+  volatile int* abort_p = &abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t r0 = (int64_t)blockIdx.x * TR;
+  const int nst = static_cast<int>((C + TC - 1) / TC);
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) mbar_init(&full_bar[i], 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  launch_dependents();
+  if (blockIdx.x == 0 && epi.zero_tickets)
+    for (int64_t i = tid; i < epi.nzero; i += THREADS) epi.zero_tickets[i] = 0;
+  __syncthreads();
+
+  auto issue = [&](int st) {
+    const int slot = st % S;
+    const int32_t c0 = static_cast<int32_t>((int64_t)st * TC);
+    mbar_arrive_expect_tx(&full_bar[slot], G::STAGE_BYTES);
+    tma_load_2d(sP + slot * P_STAGE_BYTES, &tmP, &full_bar[slot], c0, static_cast<int32_t>(r0));
+    if (kQRows)
+      tma_load_2d(sQ + slot * G::Q_STAGE_BYTES, &tmQ, &full_bar[slot], c0, 0);
+    else
+      tma_load_2d(sQ + slot * G::Q_STAGE_BYTES, &tmQ, &full_bar[slot], 0, c0);
+  };
+  int issued = 0;
+  if (tid == 0) {
+    tma_prefetch_desc(&tmP);
+    tma_prefetch_desc(&tmQ);
+    for (; issued < S - 1 && issued < nst; ++issued) issue(issued);
+  }
+
+  float acc[NJ / 8][4];
+#pragma unroll
+  for (int t = 0; t < NJ / 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+
+  // kDB: B fragments of U (rows r0 + 16 kc + 2 q (+1, +8, +9), rank 8 (warp >> 2) + g)
+  uint32_t ub[kDB ? 8 : 1][2];
+  if constexpr (kDB) {
+    const int g = lane >> 2, q = lane & 3, j = 8 * (warp >> 2) + g;
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t m = r0 + 16 * kc + 2 * q + 8 * h;
+        const float lo = (j < r && m < R) ? __ldg(epi.u_src + m * r + j) : 0.f;
+        const float hi = (j < r && m + 1 < R) ? __ldg(epi.u_src + (m + 1) * r + j) : 0.f;
+        ub[kc][h] = pack_pair<H>(lo, hi);
+      }
+  }
+
+  bool ok = true;
+  for (int st = 0; st < nst; ++st) {
+    ok = mbar_wait(&full_bar[st % S], (st / S) & 1, kWaitTmaFull, abort_p, &g_side_error);
+    __syncthreads();  // every warp is past stage st - 1: its buffers can be refilled
+    if (!ok || *abort_p) {
+      ok = false;
+      break;
+    }
+    if (tid == 0 && st + S - 1 < nst) {
+      fence_proxy_async_smem();  // the generic-proxy reads of those buffers precede the refill
+      issue(st + S - 1);
+      ++issued;
+    }
+    const uint32_t tP = smem_u32(sP + (st % S) * P_STAGE_BYTES);
+    const uint32_t tQ = smem_u32(sQ + (st % S) * G::Q_STAGE_BYTES);
+#pragma unroll
+    for (int kk = 0; kk < TC / 16; ++kk) {
+      uint32_t a[4];
+      {
+        const int row = warp * 16 + (lane & 15);
+        ldsm_x4(tP + row * 128 + ((((kk * 2 + (lane >> 4)) ^ (row & 7))) << 4), a);
+      }
+#pragma unroll
+      for (int t = 0; t < NJ / 8; t += 2) {
+        // lanes 0-15: n-tile t, lanes 16-31: n-tile t + 1; within each, c halves 0-7 / 8-15
+        uint32_t b[4];
+        if (kQRows) {
+          const int j = 8 * (t + (lane >> 4)) + (lane & 7);
+          const int chunk = kk * 2 + ((lane >> 3) & 1);
+          ldsm_x4(tQ + j * 128 + ((chunk ^ (j & 7)) << 4), b);
+        } else {
+          const int c = kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+          ldsm_x4_t(tQ + c * (NJ * 2) + (t + (lane >> 4)) * 16, b);
+        }
+        const uint32_t b0[2] = {b[0], b[1]}, b1[2] = {b[2], b[3]};
+        mma_16816<H>(acc[t], a, b0);
+        mma_16816<H>(acc[t + 1], a, b1);
+      }
+    }
+    if constexpr (kDB) {
+      // columns c = 64 st + 16 (warp & 3) .. + 15 of this stage against the tile's 128 rows
+      const int nt = warp & 3, i = lane & 7, mat = lane >> 3;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        uint32_t a[4];  // A = tile^T: rows c (16 nt + 8 (mat & 1) + ..), columns m (16 kc + ..)
+        const int m = 16 * kc + i + 8 * (mat >> 1);
+        const int chunk = 2 * nt + (mat & 1);
+        ldsm_x4_t(tP + m * 128 + ((chunk ^ (m & 7)) << 4), a);
+        mma_16816<H>(d, a, ub[kc]);
+      }
+      const int g = lane >> 2, q = lane & 3;
+      float* dst = epi.db_part + (int64_t)blockIdx.x * C * 16 + 8 * (warp >> 2) + 2 * q;
+      const int64_t c = (int64_t)st * TC + 16 * nt + g;
+      if (c < C) __stcg(reinterpret_cast<float2*>(dst + c * 16), make_float2(d[0], d[1]));
+      if (c + 8 < C) __stcg(reinterpret_cast<float2*>(dst + (c + 8) * 16), make_float2(d[2], d[3]));
+    }
+  }
+  if (!ok) {
+    if (tid == 0)
+      for (int st = issued - (S - 1) < 0 ? 0 : issued - (S - 1); st < issued; ++st)
+        mbar_drain(&full_bar[st % S], (st / S) & 1);
+    __syncthreads();
+    return;
+  }
+
+  // outputs straight from the accumulators: lane (g, q) holds rows g and g + 8 of the warp's
+  // 16, columns 8t + 2q and 8t + 2q + 1
+  const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int64_t row = r0 + warp * 16 + g + 8 * h;
+    if (row >= R) continue;
+#pragma unroll
+    for (int t = 0; t < NJ / 8; ++t)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = 8 * t + 2 * q + e;
+        const float x = j < r ? acc[t][2 * h + e] : 0.f;
+        if (epi.out32 && j < r) epi.out32[row * epi.ld_row + j * epi.ld_j] = x * epi.scale32;
+        if (epi.op && j < epi.op_cols) epi.op[row * epi.ld_op + j] = round16<H>(x * epi.scale_op);
+      }
+    if (epi.op)
+      for (int j = NJ + q; j < epi.op_cols; j += 4) epi.op[row * epi.ld_op + j] = 0;
+  }
+}
+
+// dB[n][j] = scale * sum over the row tiles t (ascending) of part[t][n][j], j < r <= 16.
+__global__ void __launch_bounds__(256) db_reduce(const float* __restrict__ part, int ntiles,
+                                                 int64_t N, int r, float scale,
+                                                 float* __restrict__ dB) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (n, 4-column group)
+  if (i >= N * 4) return;
+  const int64_t n = i >> 2;
+  const int j0 = 4 * static_cast<int>(i & 3);
+  if (j0 >= r) return;
+  const float4* src = reinterpret_cast<const float4*>(part + n * 16 + j0);
+  const int64_t stride = N * 4;  // float4 per tile
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int t = 0;
+  for (; t + 8 <= ntiles; t += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (t + u) * stride);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
+    }
+  }
+  for (; t < ntiles; ++t) {
+    const float4 v = __ldcg(src + t * stride);
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (j0 + e < r) dB[n * r + j0 + e] = scale * vv[e];
+}
+
 // Zero-padded copy Bp [N, rp] of B [N, r], for ranks whose rows are not 16-byte multiples.
 __global__ void pad_b(const uint16_t* __restrict__ B, int64_t N, int r, int64_t rp,
                       uint16_t* __restrict__ Bp) {
@@ -519,6 +736,69 @@ int run_side(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t 
                 : run_side_t<kCol, false>(name, P, R, C, ldp, qs, r, epi, a, L, stream);
 }
 
+// The narrow form serves U and V when their row tiles fill at most a quarter of the SMs, in
+// front of a GEMM on CTA pairs: the GEMM has work for the other SMs from its first stage on and
+// reads U / V only in its LoRA stage.  (A GEMM with a staged base waits for the kernels before
+// it instead, and one-CTA tiles come at sizes where the split form is short.)  A narrow CTA
+// streams at about 40 GB/s, so the narrow form is no use where its rows must finish quickly
+// on few SMs: dB and dA keep the split form.
+bool use_narrow(int64_t M, int64_t Nout, int64_t Kc) {
+  return (M + side::TR - 1) / side::TR <= num_sms() / 4 && fused_plan(M, Nout, Kc).kind == 2;
+}
+
+template <bool kQRows, int NJ, bool H, bool kDB>
+int launch_rows(const CUtensorMap& tmP, const CUtensorMap& tmQ, int64_t R, int64_t C, int r,
+                const side::Epi& epi, cudaStream_t stream) {
+  constexpr int smem = side::Narrow<NJ>::SMEM_BYTES;
+  static DeviceCache<int> attr;  // per instantiation and device
+  const int st = ensure_dynamic_smem(attr, side::side_rows<kQRows, NJ, H, kDB>, smem);
+  if (st) return st;
+  const dim3 grid((unsigned)((R + side::TR - 1) / side::TR));
+  side::side_rows<kQRows, NJ, H, kDB><<<grid, side::THREADS, smem, stream>>>(tmP, tmQ, R, C, r, epi);
+  return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+}
+
+// P: [R rows][C] (ldp).  Q: kQRows -> [q_outer rows = r][q_inner = C] (A); else
+// [q_outer = C][q_inner] (B).  kDB: the V form with the dB partials (rank <= 16).
+template <bool kQRows, bool H, bool kDB>
+int run_rows_t(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t ldp,
+               const uint16_t* Q, int64_t q_outer, int64_t q_inner, int64_t q_pitch, int r,
+               const side::Epi& epi, cudaStream_t stream) {
+  const int NJ = pick_nj(r);
+  CUtensorMap tmP, tmQ;
+  if (!make_tensor_map_2d(&tmP, P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)C, (uint64_t)R,
+                          (uint64_t)ldp * 2, 64, side::TR, MapSwizzle::B128))
+    return QLORA_ERR_CUDA;
+  const bool qmap =
+      kQRows ? make_tensor_map_2d(&tmQ, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)q_inner,
+                                  (uint64_t)q_outer, (uint64_t)q_pitch * 2, 64, (uint32_t)NJ,
+                                  MapSwizzle::B128)
+             : make_tensor_map_2d(&tmQ, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)q_inner,
+                                  (uint64_t)q_outer, (uint64_t)q_pitch * 2, (uint32_t)NJ, 64,
+                                  MapSwizzle::None);
+  if (!qmap) return QLORA_ERR_CUDA;
+  ProfileScope ps(name, stream);
+  if (kDB) return NJ == 16 ? launch_rows<kQRows, 16, H, kDB>(tmP, tmQ, R, C, r, epi, stream)
+                           : QLORA_ERR_UNSUPPORTED;
+  switch (NJ) {
+    case 16: return launch_rows<kQRows, 16, H, false>(tmP, tmQ, R, C, r, epi, stream);
+    case 32: return launch_rows<kQRows, 32, H, false>(tmP, tmQ, R, C, r, epi, stream);
+    case 64: return launch_rows<kQRows, 64, H, false>(tmP, tmQ, R, C, r, epi, stream);
+    case 128: return launch_rows<kQRows, 128, H, false>(tmP, tmQ, R, C, r, epi, stream);
+    default: return QLORA_ERR_UNSUPPORTED;
+  }
+}
+
+template <bool kQRows, bool kDB = false>
+int run_rows(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t ldp,
+             const uint16_t* Q, int64_t q_outer, int64_t q_inner, int64_t q_pitch, int r,
+             const side::Epi& epi, const LinearArgs& a, cudaStream_t stream) {
+  return a.half ? run_rows_t<kQRows, true, kDB>(name, P, R, C, ldp, Q, q_outer, q_inner, q_pitch,
+                                                r, epi, stream)
+                : run_rows_t<kQRows, false, kDB>(name, P, R, C, ldp, Q, q_outer, q_inner, q_pitch,
+                                                 r, epi, stream);
+}
+
 side::Epi no_epi() {
   side::Epi e{};
   e.scale32 = 1.f;
@@ -556,9 +836,15 @@ int launch_pad_b(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t str
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
+bool side_narrow_u(const LinearArgs& a) { return use_narrow(a.M, a.N, a.K) && a.K % 8 == 0; }
+bool side_narrow_v(const LinearArgs& a) { return use_narrow(a.M, a.K, a.N) && a.r % 8 == 0; }
+
 // U = X A^T -> sU = 16-bit(scale U) [M, rp], and U fp32 [M, r] into u32 (caller's U_save or
-// the workspace copy the backward recomputes), when given.
-int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cudaStream_t stream) {
+// the workspace copy the backward recomputes), when given.  narrow_ok: the narrow form may be
+// used (it zeroes the call's arrival tickets); the backward's recomputation, on the critical
+// path, takes the split form.
+int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cudaStream_t stream,
+                  bool narrow_ok) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   side::QSrc qs{a.A, 1, a.K, 0};  // Q(c = k, j) = A[j][k]
   side::Epi e = no_epi();
@@ -569,11 +855,25 @@ int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cud
   e.ld_op = L.rp;
   e.op_cols = a.r;  // readers see the columns past r as zeros (TMA fill)
   e.scale_op = a.scale;
+  if (narrow_ok && side_narrow_u(a)) {
+    e.zero_tickets = reinterpret_cast<int*>(ws + L.tickets);
+    e.nzero = static_cast<int64_t>(L.ntickets + L.ngtickets);
+    return run_rows<true>("side_u", a.X, a.M, a.K, a.K, a.A, a.r, a.K, a.K, a.r, e, a, stream);
+  }
   return run_side<false>("side_u", a.X, a.M, a.K, a.K, qs, a.r, e, a, L, stream);
 }
 
-// V = dY B -> sV = 16-bit(scale V) [M, rp].
-int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
+// The narrow V also forms the dB partials (rank <= 16); launch_lora_db then only sums them.
+bool fused_db(int64_t M, int64_t N, int64_t K, int r) {
+  return use_narrow(M, K, N) && r % 8 == 0 && pick_nj(r) == 16;
+}
+static bool fused_db(const LinearArgs& a) { return fused_db(a.M, a.N, a.K, a.r); }
+
+// V = dY B -> sV = 16-bit(scale V) [M, rp]; with fused_db also the partial products of dB over
+// each 128-row tile of dY (U from u32), into the workspace.  The narrow form zeroes the call's
+// arrival tickets.
+int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, const float* u32,
+                  cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   side::QSrc qs{a.B, a.r, 1, 0};  // Q(c = n, j) = B[n][j]
   side::Epi e = no_epi();
@@ -581,6 +881,20 @@ int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t st
   e.ld_op = L.rp;
   e.op_cols = a.r;  // readers see the columns past r as zeros (TMA fill)
   e.scale_op = a.scale;
+  if (side_narrow_v(a)) {
+    e.zero_tickets = reinterpret_cast<int*>(ws + L.tickets);
+    e.nzero = static_cast<int64_t>(L.ntickets + L.ngtickets);
+  }
+  if (fused_db(a)) {
+    if (L.dbpart_bytes < (uint64_t)((a.M + side::TR - 1) / side::TR) * a.N * 64)
+      return QLORA_ERR_WORKSPACE;
+    e.u_src = u32;
+    e.db_part = reinterpret_cast<float*>(ws + L.dbpart);
+    return run_rows<false, true>("side_v", a.dY, a.M, a.N, a.N, a.B, a.N, a.r, a.r, a.r, e, a,
+                                 stream);
+  }
+  if (side_narrow_v(a))
+    return run_rows<false>("side_v", a.dY, a.M, a.N, a.N, a.B, a.N, a.r, a.r, a.r, e, a, stream);
   return run_side<false>("side_v", a.dY, a.M, a.N, a.N, qs, a.r, e, a, L, stream);
 }
 
@@ -593,6 +907,15 @@ int launch_lora_db(const LinearArgs& a, const WorkspaceLayout& L, const float* u
   e.ld_row = a.r;
   e.ld_j = 1;
   e.scale32 = a.scale;
+  if (fused_db(a)) {  // the partials come from the narrow V
+    const int ntiles = static_cast<int>((a.M + side::TR - 1) / side::TR);
+    const unsigned blocks = (unsigned)((a.N * 4 + 255) / 256);
+    ProfileScope ps("side_db", stream);
+    side::db_reduce<<<blocks, 256, 0, stream>>>(
+        reinterpret_cast<const float*>(static_cast<uint8_t*>(a.ws) + L.dbpart), ntiles, a.N, a.r,
+        a.scale, a.dB);
+    return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+  }
   return run_side<true>("side_db", a.dY, a.N, a.M, a.N, qs, a.r, e, a, L, stream);
 }
 

@@ -5,12 +5,12 @@
 // bf16 adapter merged into a 4-bit base and saved loses precision twice; addaly.com "QLoRA on
 // one card", "Merging a QLoRA adapter, and the subtlety"):
 //     W_merged = bf16( W' + s * B A )          W' = the bf16 dequantization of the NF4 base
-// One pass over the packed codes: each CTA stages its [r x 128] slice of A (16-byte slots
-// swizzled against bank conflicts) and [32 x r] slice of B in shared memory as fp32, a thread
-// forms the rank-r product of eight consecutive columns of one row with fp32 multiply-adds
-// (each bf16 x bf16 product is exact in fp32), dequantizes the same eight codes exactly as
-// nf4_dequantize does, adds RN(s * delta) in fp32 and rounds once to bf16.  The fp32 copy
-// (the same values) feeds nf4_quantize for the requantized artifact.
+// One pass over the packed codes: each CTA stages its [r x 128] slice of A and [64 x r] slice
+// of B in shared memory, forms the rank-r product of its 64 x 128 tile on the tensor cores
+// (mma.sync, bf16 x bf16 products exact, fp32 accumulation), and a thread then dequantizes
+// eight consecutive base weights of a row exactly as nf4_dequantize does, adds RN(s * delta)
+// in fp32 and rounds once to bf16.  The fp32 copy (the same values) feeds nf4_quantize for
+// the requantized artifact.
 //
 // Error statistics (aicurriculum.codextroop.com "QLoRA -- Module 12.4", "Design Details That
 // Matter": NF4 places levels at normal quantiles and is often better than naive INT4;
@@ -34,95 +34,150 @@ constexpr int COLS = 128;     // output columns per CTA
 constexpr int THREADS = 256;  // 16 threads per row (8 columns each); a thread takes 4 rows
 constexpr int RPT = ROWS / (THREADS / 16);  // rows per thread, sharing each A load
 
-inline int smem_bytes(int r) { return (r * COLS + ROWS * (r + 1)) * 4; }
-
-// 16-byte slot of columns 8 c8 + 4 h .. + 3 within a staged row of A: the low slot bit is
-// flipped for c8 & 4, so the eight lanes of a 128-bit shared load hit eight distinct bank
-// quads (unswizzled, lanes c8 and c8 + 4 collide)
-__device__ __forceinline__ int a_slot(int c8, int h) { return (2 * c8 + h) ^ ((c8 >> 2) & 1); }
+// Rank padded to the MMA contraction (16) and the shared-memory pitches (in bf16 / fp32
+// elements; the +8 / +4 pads make the ldmatrix rows and the fp32 tile's float2 stores
+// conflict-free).
+__host__ __device__ inline int rank16(int r) { return (r + 15) / 16 * 16; }
+constexpr int A_PITCH = COLS + 8;   // sA [r16][COLS] bf16
+constexpr int D_PITCH = COLS + 4;   // sD [ROWS][COLS] fp32
+inline int b_pitch(int r) { return rank16(r) + 8; }  // sB [ROWS][r16] bf16
+inline int smem_bytes(int r) {
+  return rank16(r) * A_PITCH * 2 + ROWS * b_pitch(r) * 2 + ROWS * D_PITCH * 4;
+}
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&v)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&v)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(addr));
+}
+
+// One CTA: output rows n0 .. n0 + 63, columns k0 .. k0 + 127.  delta = B A for the tile on the
+// tensor cores (mma.sync m16n8k16, bf16 x bf16 products exact, fp32 accumulation): warp w
+// takes rows 16 (w & 3) .. + 15 and columns 64 (w >> 2) .. + 63; the fp32 tile goes through
+// shared memory to the element-wise pass, where a thread dequantizes eight consecutive base
+// weights of four rows exactly as nf4_dequantize does, adds RN(s * delta) in fp32 and rounds
+// once to bf16.
 __global__ void __launch_bounds__(THREADS) nf4_merge_kernel(
     const uint8_t* __restrict__ codes, const int8_t* __restrict__ qs,
     const float* __restrict__ steps, const float* __restrict__ mean,
     int dq, int fp8, const uint16_t* __restrict__ A, const uint16_t* __restrict__ B, int64_t N,
     int64_t K, int r, float scale, uint16_t* __restrict__ out16, float* __restrict__ out32) {
-  extern __shared__ float msm[];
-  float* sA = msm;               // [r][COLS]
-  float* sB = msm + r * COLS;    // [ROWS][r + 1]
-  const int tid = threadIdx.x;
+  extern __shared__ __align__(16) uint8_t msm[];
+  const int r16 = rank16(r), bp = r16 + 8;
+  uint16_t* sA = reinterpret_cast<uint16_t*>(msm);              // [r16][A_PITCH]
+  uint16_t* sB = sA + r16 * A_PITCH;                            // [ROWS][bp]
+  float* sD = reinterpret_cast<float*>(sB + ROWS * bp);         // [ROWS][D_PITCH]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t k0 = static_cast<int64_t>(blockIdx.x) * COLS;
   const int64_t n0 = static_cast<int64_t>(blockIdx.y) * ROWS;
-  for (int i = tid; i < r * (COLS / 8); i += THREADS) {
-    const int j = i / (COLS / 8), c8 = i % (COLS / 8);
-    const int64_t k = k0 + 8 * c8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (k < K) v = __ldg(reinterpret_cast<const uint4*>(A + j * K + k));
-    float* row = sA + j * COLS;
-    *reinterpret_cast<float4*>(row + 4 * a_slot(c8, 0)) =
-        make_float4(bf16_bits_to_f32(v.x & 0xFFFFu), bf16_bits_to_f32(v.x >> 16),
-                    bf16_bits_to_f32(v.y & 0xFFFFu), bf16_bits_to_f32(v.y >> 16));
-    *reinterpret_cast<float4*>(row + 4 * a_slot(c8, 1)) =
-        make_float4(bf16_bits_to_f32(v.z & 0xFFFFu), bf16_bits_to_f32(v.z >> 16),
-                    bf16_bits_to_f32(v.w & 0xFFFFu), bf16_bits_to_f32(v.w >> 16));
-  }
-  for (int i = tid; i < ROWS * r; i += THREADS) {
-    const int rr = i / r, j = i % r;
-    const int64_t n = n0 + rr;
-    sB[rr * (r + 1) + j] = n < N ? bf16_bits_to_f32(__ldg(B + n * r + j)) : 0.0f;
-  }
-  __syncthreads();
-  const float mu = dq ? __ldg(mean) : 0.0f;
   const int c8 = tid & 15;
   const int64_t kk = k0 + 8 * c8;
-  if (kk >= K) return;
-  // rows (tid >> 4) + 16 p, p < RPT: each A value read from shared memory feeds RPT rows
-  float d[RPT][8];
-#pragma unroll
-  for (int p = 0; p < RPT; ++p)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d[p][i] = 0.f;
   const int rr0 = tid >> 4;
-  const float* acol0 = sA + 4 * a_slot(c8, 0);
-  const float* acol1 = sA + 4 * a_slot(c8, 1);
-#pragma unroll 2
-  for (int j = 0; j < r; ++j) {  // ascending j: a fixed fp32 summation order
-    const float4 a0 = *reinterpret_cast<const float4*>(acol0 + j * COLS);
-    const float4 a1 = *reinterpret_cast<const float4*>(acol1 + j * COLS);
-#pragma unroll
-    for (int p = 0; p < RPT; ++p) {
-      const float b = sB[(rr0 + 16 * p) * (r + 1) + j];
-      d[p][0] = __fmaf_rn(b, a0.x, d[p][0]);
-      d[p][1] = __fmaf_rn(b, a0.y, d[p][1]);
-      d[p][2] = __fmaf_rn(b, a0.z, d[p][2]);
-      d[p][3] = __fmaf_rn(b, a0.w, d[p][3]);
-      d[p][4] = __fmaf_rn(b, a1.x, d[p][4]);
-      d[p][5] = __fmaf_rn(b, a1.y, d[p][5]);
-      d[p][6] = __fmaf_rn(b, a1.z, d[p][6]);
-      d[p][7] = __fmaf_rn(b, a1.w, d[p][7]);
-    }
-  }
+  // this thread's base weights (rows rr0 + 16 p, columns kk .. kk + 7: one code word and one
+  // block scale each), loaded first so they arrive while the adapters are staged and multiplied
+  uint32_t word[RPT];
+  uint8_t scode[RPT];
+  float sstep[RPT];
 #pragma unroll
   for (int p = 0; p < RPT; ++p) {
     const int64_t n = n0 + rr0 + 16 * p;
+    word[p] = 0;
+    scode[p] = 0;
+    sstep[p] = 0.f;
+    if (n < N && kk < K) {
+      const int64_t e = n * K + kk;
+      const int64_t blk = e / 64;
+      word[p] = __ldg(reinterpret_cast<const uint32_t*>(codes + e / 2));
+      if (dq) {
+        scode[p] = static_cast<uint8_t>(__ldg(qs + blk));
+        sstep[p] = __ldg(steps + (blk >> 8));
+      } else {
+        sstep[p] = __ldg(steps + blk);
+      }
+    }
+  }
+  // A [r][K] -> sA[j][0, COLS) (16-byte pieces; zero past r and past K)
+  for (int i = tid; i < r16 * (COLS / 8); i += THREADS) {
+    const int j = i / (COLS / 8), c = i % (COLS / 8);
+    const int64_t k = k0 + 8 * c;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (j < r && k < K) v = __ldg(reinterpret_cast<const uint4*>(A + j * K + k));
+    *reinterpret_cast<uint4*>(sA + j * A_PITCH + 8 * c) = v;
+  }
+  // B [N][r] -> sB[row][0, r16) (element by element: r need not be a multiple of 8)
+  for (int i = tid; i < ROWS * r16; i += THREADS) {
+    const int rr = i / r16, j = i % r16;
+    const int64_t n = n0 + rr;
+    sB[rr * bp + j] = (n < N && j < r) ? __ldg(B + n * r + j) : static_cast<uint16_t>(0);
+  }
+  __syncthreads();
+
+  {
+    const int mt = warp & 3, nh = warp >> 2;
+    float acc[8][4];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
+    for (int j0 = 0; j0 < r16; j0 += 16) {
+      uint32_t a[4];  // rows 16 mt + (lane & 15), rank j0 + 8 (lane >> 4) .. + 7
+      ldsm_x4(sB0 + ((16 * mt + (lane & 15)) * bp + j0 + 8 * (lane >> 4)) * 2, a);
+#pragma unroll
+      for (int t = 0; t < 8; t += 2) {
+        // n-tiles t, t + 1 of this warp's 64 columns; rank halves j0 .. + 7, j0 + 8 .. + 15
+        uint32_t b[4];
+        const int jr = j0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int col = 64 * nh + 8 * (t + (lane >> 4));
+        ldsm_x4_t(sA0 + (jr * A_PITCH + col) * 2, b);
+        const uint32_t b0[2] = {b[0], b[1]}, b1[2] = {b[2], b[3]};
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+            " {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(acc[t][0]), "+f"(acc[t][1]), "+f"(acc[t][2]), "+f"(acc[t][3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0[0]), "r"(b0[1]));
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+            " {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(acc[t + 1][0]), "+f"(acc[t + 1][1]), "+f"(acc[t + 1][2]), "+f"(acc[t + 1][3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b1[0]), "r"(b1[1]));
+      }
+    }
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int col = 64 * nh + 8 * t + 2 * q;
+      *reinterpret_cast<float2*>(sD + (16 * mt + g) * D_PITCH + col) = make_float2(acc[t][0], acc[t][1]);
+      *reinterpret_cast<float2*>(sD + (16 * mt + g + 8) * D_PITCH + col) = make_float2(acc[t][2], acc[t][3]);
+    }
+  }
+  __syncthreads();
+
+  const float mu = dq ? __ldg(mean) : 0.0f;
+  if (kk >= K) return;
+#pragma unroll
+  for (int p = 0; p < RPT; ++p) {
+    const int rr = rr0 + 16 * p;
+    const int64_t n = n0 + rr;
     if (n >= N) break;
-    // the eight base weights (n, kk .. kk + 7): one code word, one block scale
     const int64_t e = n * K + kk;
-    const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(codes + e / 2));
-    const int64_t blk = e / 64;
-    const float a_hat =
-        dq ? __fmaf_rn(nf4_second_level(static_cast<uint8_t>(__ldg(qs + blk)), fp8),
-                       __ldg(steps + (blk >> 8)), mu)
-           : __ldg(steps + blk);
+    const float4 d0 = *reinterpret_cast<const float4*>(sD + rr * D_PITCH + 8 * c8);
+    const float4 d1 = *reinterpret_cast<const float4*>(sD + rr * D_PITCH + 8 * c8 + 4);
+    const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+    const float a_hat = dq ? __fmaf_rn(nf4_second_level(scode[p], fp8), sstep[p], mu) : sstep[p];
     uint32_t wd[4];
-    nf4_dequant8(nf4_make_table(a_hat), word, wd);
+    nf4_dequant8(nf4_make_table(a_hat), word[p], wd);
     uint32_t o16[4];
     float o32[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float v0 = __fadd_rn(bf16_bits_to_f32(wd[i] & 0xFFFFu), __fmul_rn(scale, d[p][2 * i]));
-      const float v1 = __fadd_rn(bf16_bits_to_f32(wd[i] >> 16), __fmul_rn(scale, d[p][2 * i + 1]));
+      const float v0 = __fadd_rn(bf16_bits_to_f32(wd[i] & 0xFFFFu), __fmul_rn(scale, d[2 * i]));
+      const float v1 = __fadd_rn(bf16_bits_to_f32(wd[i] >> 16), __fmul_rn(scale, d[2 * i + 1]));
       const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
       o16[i] = *reinterpret_cast<const uint32_t*>(&h);
       o32[2 * i] = bf16_bits_to_f32(o16[i] & 0xFFFFu);

@@ -364,6 +364,7 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
                                                           const float* __restrict__ mean,
                                                           int64_t numel, int dq, int fp8,
                                                           uint16_t* __restrict__ out) {
+  launch_dependents();  // a GEMM that streams the output waits for this grid before reading it
   const float mu = dq ? __ldg(mean) : 0.0f;
   const int64_t npieces = (numel + 15) / 16;
   for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < npieces;
@@ -402,6 +403,9 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
       }
     }
   }
+  // launched as a programmatic dependent (the staged base of a GEMM): the kernel before it
+  // (the rank-r product the GEMM reads) must be complete when this grid is
+  grid_dependency_wait();
 }
 
 // -------------------------------------------------------------------- launchers
@@ -480,18 +484,30 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
 }
 
 int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, bool half,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool dependent) {
   const int64_t npieces = (numel + 15) / 16;
   const int threads = 256;
   int64_t blocks = (npieces + threads - 1) / threads;
-  const int64_t cap = (int64_t)num_sms() * 8;
+  // as a dependent: at most four CTAs per SM, so the kernel before it keeps room to finish
+  const int64_t cap = (int64_t)num_sms() * (dependent ? 4 : 8);
   if (blocks > cap) blocks = cap;
   ProfileScope ps("nf4_dequant", stream);
-  (half ? nf4_dequant_kernel<true> : nf4_dequant_kernel<false>)<<<(unsigned)blocks, threads, 0,
-                                                                   stream>>>(
-      q.codes, q.scale_codes, q.scale_steps, q.scale_mean, numel, q.dq_block != 0 ? 1 : 0,
-      q.dq_type == NF4_DQ_FP8 ? 1 : 0, out);
-  return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  const int dq = q.dq_block != 0 ? 1 : 0, fp8 = q.dq_type == NF4_DQ_FP8 ? 1 : 0;
+  const cudaError_t e =
+      half ? cudaLaunchKernelEx(&cfg, nf4_dequant_kernel<true>, q.codes, q.scale_codes, q.scale_steps,
+                                q.scale_mean, numel, dq, fp8, out)
+           : cudaLaunchKernelEx(&cfg, nf4_dequant_kernel<false>, q.codes, q.scale_codes,
+                                q.scale_steps, q.scale_mean, numel, dq, fp8, out);
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
 }  // namespace qlora

@@ -91,6 +91,9 @@ struct Params {
   float* part;    // [nsplit][M][Nout] fp32
   int* tickets;   // [output tiles] arrivals, zero at launch, zeroed again by the last CTA
   int64_t part_cap, ticket_cap;  // floats in part, ints in tickets (bounds checks)
+  // staged base (single-CTA kernel): W' was dequantized into the workspace by the kernel
+  // before this one; every NF4 stage takes its W tile by TMA (map tmW) like a LoRA stage
+  int wstage;
 };
 
 // One thread's share of an NF4 stage: 64 codes (32 bytes) and the block's scale code/step.
@@ -217,6 +220,44 @@ __device__ __forceinline__ void split_sum(const Params& p, int split, int64_t my
   }
 }
 
+// The 16-bit output of this warp's 32 TMEM lanes (row0 .. row0 + 31; my_row = row0 + lane):
+// nchunk 32-column chunks, chunk c from TMEM columns tcol0 + 32 c to output columns
+// gcol0 + 32 c.  Each chunk goes through a 2 KB buffer of its own (64-byte swizzle; the ring's
+// shared memory is idle once the accumulator is complete) and one TMA store, so no store
+// waits for an earlier one to release its buffer.
+template <bool H>
+__device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMap* tmOut,
+                                               uint32_t taddr, int tcol0, int64_t gcol0,
+                                               int64_t row0, int64_t my_row, int split,
+                                               int nchunk, uint8_t* buf0, int lane) {
+#pragma unroll 1
+  for (int c = 0; c < nchunk; ++c) {
+    const int64_t col = gcol0 + c * 32;
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(taddr + tcol0 + c * 32, v);
+    tmem_ld_wait();
+    split_sum(p, split, my_row, col, v);
+    uint8_t* buf = buf0 + c * 2048;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t phys = j ^ ((lane >> 1) & 3);  // 64-byte swizzle
+      *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) = make_uint4(
+          pack_pair<H>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+          pack_pair<H>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+          pack_pair<H>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+          pack_pair<H>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (col < p.Nout && row0 < p.M) tma_store_2d(tmOut, buf, (int32_t)col, (int32_t)row0);
+      bulk_commit();
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
+}
+
 // kMode 0: forward (W tile K-major), 1: input gradient (MN-major).  H: the fp16 compute type
 // (operands, dequantized tiles and output in fp16), else bf16.
 template <int kMode, int kAcc, bool H>
@@ -224,7 +265,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fused_nf4_lora_gemm(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB2,
-                        const __grid_constant__ CUtensorMap tmOut, const Params p) {
+                        const __grid_constant__ CUtensorMap tmOut,
+                        const __grid_constant__ CUtensorMap tmW, const Params p) {
   using T = Tile<kAcc>;
   constexpr int BM = T::BM, SA = T::SA, SB = T::SB, A_BYTES = T::A_BYTES, B_BASE = T::B_BASE;
   constexpr int TMEM_COLS = T::TMEM_COLS;
@@ -276,11 +318,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB2);
+      if (p.wstage) tma_prefetch_desc(&tmW);
       for (int s = 0; s < total; ++s) {
         const int as = s % SA, ar = s / SA;
         if (ar > 0 && !mbar_wait(&a_empty[as], (ar - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) break;
         uint8_t* a_dst = smem + as * A_BYTES;
-        if (s >= n_main) {
+        if (s < n_main && p.wstage) {
+          // staged base: the W tile by TMA into the B slot, once that slot is free
+          const int bs = s % SB, br = s / SB;
+          if (br > 0 && !mbar_wait(&b_empty[bs], (br - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) break;
+          uint8_t* b_dst = smem + B_BASE + bs * B_BYTES;
+          if (s == 0) grid_dependency_wait();  // W' comes from the kernel before
+          const int32_t k0 = (kc0 + s) * BK;
+          mbar_arrive_expect_tx(&a_full[as], A_BYTES + B_BYTES);
+          tma_load_2d(a_dst, &tmA, &a_full[as], k0, (int32_t)m0);
+          if (kMode == 0) {
+            tma_load_2d(b_dst, &tmW, &a_full[as], k0, (int32_t)n0);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              tma_load_2d(b_dst + i * 8192, &tmW, &a_full[as], (int32_t)(n0 + 64 * i), k0);
+          }
+        } else if (s >= n_main) {
           // a LoRA stage: its B tile comes by TMA into the B slot, once that slot is free
           const int bs = s % SB, br = s / SB;
           if (br > 0 && !mbar_wait(&b_empty[bs], (br - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) break;
@@ -313,9 +372,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int s = 0; s < total && ok; ++s) {
         const int as = s % SA, ar = s / SA, bs = s % SB, br = s / SB;
-        // the LoRA stages (the last ones) come entirely by TMA: no dequantized tile to wait for
+        // the LoRA stages (the last ones), and every stage of a staged base, come entirely by
+        // TMA: no dequantized tile to wait for
         ok = mbar_wait(&a_full[as], ar & 1, kWaitTmaFull, abort_p, &g_gemm_error) &&
-             (s >= n_main ||
+             (s >= n_main || p.wstage ||
               mbar_wait(&bready_bar[bs], br & 1, kWaitBReady, abort_p, &g_gemm_error));
         if (!ok) break;
         tc_fence_after();
@@ -399,20 +459,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       slice_at(s + 4, cur);
       return true;
     };
-    Slice pf0, pf1, pf2, pf3;
-    slice_at(0, pf0);
-    slice_at(1, pf1);
-    slice_at(2, pf2);
-    slice_at(3, pf3);
     bool ok = true;
-    for (int s = 0; s < n_main && ok; s += 4) {  // the NF4 stages (the LoRA stages need nothing)
-      ok = body(s, pf0);
-      if (!ok || s + 1 >= n_main) break;
-      ok = body(s + 1, pf1);
-      if (!ok || s + 2 >= n_main) break;
-      ok = body(s + 2, pf2);
-      if (!ok || s + 3 >= n_main) break;
-      ok = body(s + 3, pf3);
+    if (!p.wstage) {  // (a staged base needs no dequantization here)
+      Slice pf0, pf1, pf2, pf3;
+      slice_at(0, pf0);
+      slice_at(1, pf1);
+      slice_at(2, pf2);
+      slice_at(3, pf3);
+      for (int s = 0; s < n_main && ok; s += 4) {  // the NF4 stages (the LoRA stages need nothing)
+        ok = body(s, pf0);
+        if (!ok || s + 1 >= n_main) break;
+        ok = body(s + 1, pf1);
+        if (!ok || s + 2 >= n_main) break;
+        ok = body(s + 2, pf2);
+        if (!ok || s + 3 >= n_main) break;
+        ok = body(s + 3, pf3);
+      }
     }
 
     // ------------------------------------------------------------ epilogue
@@ -425,41 +487,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tbase = tmem + (kAcc == 1 ? 0u : static_cast<uint32_t>(half * 256));
       const int64_t row0 = m0 + (kAcc == 1 ? 0 : half * UM) + lg * 32;
       const int64_t my_row = row0 + lane;
-      uint8_t* buf0 = smem + (warp - DEQ_WARP0) * 4096;
-      const bool store = split_epilogue_partial(p, split, tbase + (static_cast<uint32_t>(lg * 32) << 16),
-                                                my_row, n0 + col0, NCHUNK, col0,
+      uint8_t* buf0 = smem + (warp - DEQ_WARP0) * (NCHUNK * 2048);
+      const uint32_t taddr = tbase + (static_cast<uint32_t>(lg * 32) << 16);
+      const bool store = split_epilogue_partial(p, split, taddr, my_row, n0 + col0, NCHUNK, col0,
                                                 warp == DEQ_WARP0 && lane == 0,
                                                 static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), s_last);
-#pragma unroll 1
-      for (int c = 0; c < NCHUNK && store; ++c) {
-        const int col = col0 + c * 32;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tbase + (static_cast<uint32_t>(lg * 32) << 16) + col, v);
-        tmem_ld_wait();
-        split_sum(p, split, my_row, n0 + col, v);
-        uint8_t* buf = buf0 + (c & 1) * 2048;
-        if (c >= 2) {
-          if (lane == 0) bulk_wait_read1();
-          __syncwarp();
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t phys = j ^ ((lane >> 1) & 3);  // 64-byte swizzle
-          *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) = make_uint4(
-              pack_pair<H>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-              pack_pair<H>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-              pack_pair<H>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-              pack_pair<H>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && n0 + col < p.Nout && row0 < p.M) {
-          tma_store_2d(&tmOut, buf, (int32_t)(n0 + col), (int32_t)row0);
-        }
-        if (lane == 0) bulk_commit();
-      }
-      if (lane == 0) bulk_wait_all();
-      __syncwarp();
+      if (store)
+        epilogue_store<H>(p, &tmOut, taddr, col0, n0 + col0, row0, my_row, split, NCHUNK, buf0, lane);
     }
   }
 
@@ -746,40 +780,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * 256);
       const int64_t row0 = m0 + acc * UM + lg * 32;
       const int64_t my_row = row0 + lane;
-      uint8_t* buf0 = smem + (warp - DEQ_WARP0) * 4096;
-      const bool store = split_epilogue_partial(p, split, tbase + (static_cast<uint32_t>(lg * 32) << 16),
-                                                my_row, n0, 8, 0, warp == DEQ_WARP0 && lane == 0,
+      uint8_t* buf0 = smem + (warp - DEQ_WARP0) * (8 * 2048);
+      const uint32_t taddr = tbase + (static_cast<uint32_t>(lg * 32) << 16);
+      const bool store = split_epilogue_partial(p, split, taddr, my_row, n0, 8, 0,
+                                                warp == DEQ_WARP0 && lane == 0,
                                                 static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x),
                                                 s_last);
-#pragma unroll 1
-      for (int c = 0; c < 8 && store; ++c) {
-        const int col = c * 32;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tbase + (static_cast<uint32_t>(lg * 32) << 16) + col, v);
-        tmem_ld_wait();
-        split_sum(p, split, my_row, n0 + col, v);
-        uint8_t* buf = buf0 + (c & 1) * 2048;
-        if (c >= 2) {
-          if (lane == 0) bulk_wait_read1();
-          __syncwarp();
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t phys = j ^ ((lane >> 1) & 3);  // 64-byte swizzle
-          *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) = make_uint4(
-              pack_pair<H>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-              pack_pair<H>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-              pack_pair<H>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-              pack_pair<H>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && n0 + col < p.Nout && row0 < p.M)
-          tma_store_2d(&tmOut, buf, (int32_t)(n0 + col), (int32_t)row0);
-        if (lane == 0) bulk_commit();
-      }
-      if (lane == 0) bulk_wait_all();
-      __syncwarp();
+      if (store) epilogue_store<H>(p, &tmOut, taddr, 0, n0, row0, my_row, split, 8, buf0, lane);
     }
   }
 
@@ -860,6 +867,15 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, const FusedPlan&
          map_bf16(&tOut, a.dX, a.K, a.M, a.K, 32, 32, MapSwizzle::B64);
   }
   if (!ok) return QLORA_ERR_CUDA;
+  CUtensorMap tW = tB2;  // (not read without a staged base)
+  p.wstage = plan.wstage && !kPair && kAcc == 1 ? 1 : 0;
+  if (p.wstage) {
+    if (L.Wd_bytes < (uint64_t)a.N * a.K * 2) return QLORA_ERR_WORKSPACE;
+    // W' [N rows][K]: forward tiles are [64 k x 256 rows], input-gradient tiles four
+    // [64 k x 64 rows] boxes (MN-major), as for the adapters of the LoRA stages
+    if (!map_bf16(&tW, ws + L.Wd, a.K, a.N, a.K, 64, kMode == 0 ? BN : 64, MapSwizzle::B128))
+      return QLORA_ERR_CUDA;
+  }
   ProfileScope ps(kMode == 0 ? "fused_fwd_gemm" : "fused_dx_gemm", stream);
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS);
@@ -883,7 +899,7 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, const FusedPlan&
   } else {
     cfg.gridDim = dim3((unsigned)((p.Nout + BN - 1) / BN), (unsigned)((a.M + BM - 1) / BM),
                        (unsigned)plan.nsplit);
-    e = cudaLaunchKernelEx(&cfg, fused_nf4_lora_gemm<kMode, kAcc, H>, tA, tA2, tB2, tOut, p);
+    e = cudaLaunchKernelEx(&cfg, fused_nf4_lora_gemm<kMode, kAcc, H>, tA, tA2, tB2, tOut, tW, p);
   }
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
@@ -908,6 +924,9 @@ void split_into(FusedPlan& pl, int64_t n_all, int64_t want) {
   }
 }
 }  // namespace
+
+// Largest base that plans stage in the workspace: 128 MiB of bf16, about the L2.
+constexpr int64_t kStagedBaseMaxWeights = 64LL << 20;
 
 FusedPlan fused_plan(int64_t M, int64_t Nout, int64_t Kc) {
   FusedPlan pl{};
@@ -935,6 +954,10 @@ FusedPlan fused_plan(int64_t M, int64_t Nout, int64_t Kc) {
   const int64_t tiles1 = ((M + 127) / 128) * ((Nout + 255) / 256);
   split_into(pl, n_all, sms / tiles1);
   pl.tiles = tiles1;
+  // Past one row tile each weight would be dequantized once per row tile by the dequant
+  // warps, which then set the stage time; dequantizing W' once into the workspace (it stays
+  // in L2 at these sizes) and streaming it by TMA is faster.
+  pl.wstage = M > 128 && Nout * Kc <= kStagedBaseMaxWeights ? 1 : 0;
   return pl;
 }
 

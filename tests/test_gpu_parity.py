@@ -175,6 +175,9 @@ SMALL = [
     # contraction (its workspace is needed below the decode path's token limit too)
     ("tokens1_split", 1, 2048, 4096, 64, 16.0),
     ("tokens5_split", 5, 1088, 2560, 24, 48.0),
+    # more row tiles than a quarter of the SMs: U and V with the split contraction and the
+    # last-CTA sum (below that they take one CTA per row tile and the whole contraction)
+    ("tall_split_side", 4800, 256, 320, 16, 32.0),
 ]
 
 
@@ -203,6 +206,50 @@ def test_pair_tiles_every_output(M, N, K, r):
     pb = Problem(p)
     Y, U = _check_fwd(pb)
     _check_bwd(pb, U)
+    if M == 2100:
+        _check_bwd(pb, None)  # U recomputed (split form) before the narrow V
+
+
+def test_base_past_staging_limit():
+    """One-CTA tiles over two row tiles with a base too large to stage in the workspace
+    (8192 x 8256 > 64 Mi weights): W' is dequantized inside both GEMMs, once per row tile,
+    with a two-way split contraction.  (Smaller bases at more than 128 tokens on one-CTA
+    tiles are dequantized once into the workspace and streamed by TMA: the ragged, rank and
+    multi-tile cases above and the 7B-stack layers.)  Sampled rows of Y and dX, U / dA / dB
+    in full."""
+    p = wl.LinearProblem("unstaged-160-8192-8256", 160, 8192, 8256, 16, 32.0, 0.02, 0.001,
+                         config=77)
+    pb = Problem(p)
+    rows = _sample_rows(p.M, 24, p.name)
+    Y, U = _check_fwd(pb, rows)
+    _check_bwd(pb, U, rows)
+
+
+def test_arrival_tickets_zeroed_without_memset():
+    """A call whose U / V take the narrow form (one CTA per 128-row tile beside a pair GEMM)
+    launches no ticket memset: the narrow kernel zeroes the arrival counters that split-form
+    kernels later in the call use (dA here).  The cached workspace is filled with 0xFF bytes
+    before each call, so a counter left unzeroed would lose dA's split sums.  The backward
+    also recomputes U (split form, with the memset) once."""
+    from bit_nf4_quantized_37_b300 import _binding as bnd
+    p = wl.LinearProblem("tickets-1024-4864-4864", 1024, 4864, 4864, 16, 32.0, 0.02, 0.001,
+                         config=78)
+    pb = Problem(p)
+    rows = _sample_rows(p.M, 16, p.name)
+
+    def dirty():
+        torch.cuda.synchronize()
+        for buf in bnd._ws_cache.values():
+            buf.fill_(0xFF)
+        torch.cuda.synchronize()
+
+    qn.qlora_linear_fwd(pb.Xd, pb.qd, pb.Ad, pb.Bd, p.scale)  # sizes the cached workspace
+    dirty()
+    Y, U = _check_fwd(pb, rows)
+    dirty()
+    _check_bwd(pb, U, rows)
+    dirty()
+    _check_bwd(pb, None, rows)
 
 
 def test_zero_b_equals_base_matmul():
@@ -329,10 +376,12 @@ def _ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
 @pytest.mark.parametrize("cfg", ["config1", "config2"])
 def test_merge_matches_oracle(cfg):
     """bf16(W' + s B A): the device's fp32 bracket against the oracle's fp64 one, each rounded
-    once to bf16.  Bound from the fp32 arithmetic: r sequential multiply-adds, one multiply and
-    one add leave at most (r + 2) 2^-24 (|W'| + s sum_j |B A|) before the final rounding, so the
-    two results differ by at most that plus one bf16 step of the result; more than one step
-    only where W' and s B A nearly cancel.  Differences of any size are rare (~2^-16)."""
+    once to bf16.  Bound from the fp32 arithmetic: the r exact bf16 x bf16 products summed on
+    the tensor cores (r additions; their fp32 accumulation is not specified as
+    round-to-nearest, so a unit of 2^-23 each), one multiply and one add leave at most
+    (2 r + 2) 2^-24 (|W'| + s sum_j |B A|) before the final rounding, so the two results differ
+    by at most that plus one bf16 step of the result; more than one step only where W' and
+    s B A nearly cancel.  Differences of any size are rare (~2^-16)."""
     p = getattr(wl, cfg)()
     W = p.W()
     qo = oracle.quantize(W)
@@ -349,7 +398,7 @@ def test_merge_matches_oracle(cfg):
     mag = np.abs(wd) + p.scale * (np.abs(wl.bf16_bits_to_f32(B).astype(np.float64)) @
                                   np.abs(wl.bf16_bits_to_f32(A).astype(np.float64)))
     step = np.exp2(np.floor(np.log2(np.maximum(np.abs(wv), 2.0 ** -126))) - 7)
-    bound = (p.r + 2) * 2.0 ** -24 * mag + step
+    bound = (2 * p.r + 2) * 2.0 ** -24 * mag + step
     assert np.all(np.abs(gv - wv) <= bound)
     assert np.array_equal(m32.cpu().numpy(), wl.bf16_bits_to_f32(got))
 
