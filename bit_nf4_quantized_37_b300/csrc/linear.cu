@@ -41,8 +41,10 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int r) {
   // the fused GEMMs' split contraction: the forward takes them above kSkinnyMaxM tokens, the
   // input gradient at every M
   const uint64_t gpart_bytes = fused_partial_bytes(M, N, K, &L.ngtickets);
-  L.tickets = take((L.ntickets + L.ngtickets) * 4);
+  L.nticket_words = L.ntickets + L.ngtickets + 1;
+  L.tickets = take(L.nticket_words * 4);
   L.gtickets = L.tickets + L.ntickets * 4;
+  L.pers_ctr = L.gtickets + L.ngtickets * 4;
   L.gpart = take(gpart_bytes);
   L.gpart_bytes = gpart_bytes;
   L.Z = take(M <= kSkinnyMaxM ? (uint64_t)M * N * 4 : 0);
@@ -57,8 +59,8 @@ uint64_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int r) {
 }
 
 static int clear_tickets(const LinearArgs& a, const WorkspaceLayout& L, cudaStream_t stream) {
-  return cudaMemsetAsync(static_cast<uint8_t*>(a.ws) + L.tickets, 0,
-                         (L.ntickets + L.ngtickets) * 4, stream) ==
+  return cudaMemsetAsync(static_cast<uint8_t*>(a.ws) + L.tickets, 0, L.nticket_words * 4,
+                         stream) ==
                  cudaSuccess
              ? QLORA_OK
              : QLORA_ERR_CUDA;

@@ -61,6 +61,8 @@ struct WorkspaceLayout {
   uint64_t gpart_bytes;
   uint64_t gtickets; // int [ngtickets] its per-tile arrivals (right after the tickets above)
   uint64_t ngtickets;
+  uint64_t pers_ctr; // int: the persistent pair GEMM's cluster tickets (right after those)
+  uint64_t nticket_words;  // ints from `tickets` on, all zeroed at the start of a call
   uint64_t Z;        // fp32 [M, N] per-token LoRA term (decode path, per-token adapters)
   uint64_t Wd;       // 16-bit [N, K] W' dequantized once, for GEMM plans with a staged base
   uint64_t Wd_bytes;

@@ -453,14 +453,14 @@ template <int NJ>
 struct Narrow {
   static constexpr int Q_STAGE_BYTES = NJ * TC * 2;
   static constexpr int STAGE_BYTES = P_STAGE_BYTES + Q_STAGE_BYTES;
-  static constexpr int STAGES = (160 * 1024) / STAGE_BYTES < 8 ? (160 * 1024) / STAGE_BYTES : 8;
+  static constexpr int STAGES = (216 * 1024) / STAGE_BYTES < 12 ? (216 * 1024) / STAGE_BYTES : 12;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 };
 
 template <bool kQRows, int NJ, bool H, bool kDB>
 __global__ void __launch_bounds__(THREADS, 1)
     side_rows(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-              int64_t R, int64_t C, int r, Epi epi) {
+              int64_t R, int64_t C, int r, Epi epi, const uint16_t* __restrict__ q_rows) {
   using G = Narrow<NJ>;
   constexpr int S = G::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -480,10 +480,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     abort_flag = 0;
     fence_barrier_init();
   }
-  launch_dependents();
-  if (blockIdx.x == 0 && epi.zero_tickets)
+  // the tickets are zero (and visible device-wide) before the kernel behind this one, which
+  // draws from them before it waits for this grid, may start
+  if (blockIdx.x == 0 && epi.zero_tickets) {
     for (int64_t i = tid; i < epi.nzero; i += THREADS) epi.zero_tickets[i] = 0;
+    __threadfence();
+  }
   __syncthreads();
+  launch_dependents();
 
   auto issue = [&](int st) {
     const int slot = st % S;
@@ -492,6 +496,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_load_2d(sP + slot * P_STAGE_BYTES, &tmP, &full_bar[slot], c0, static_cast<int32_t>(r0));
     if (kQRows)
       tma_load_2d(sQ + slot * G::Q_STAGE_BYTES, &tmQ, &full_bar[slot], c0, 0);
+    else if (q_rows && c0 + TC <= C)  // whole stage of Q rows of exactly NJ: one contiguous piece
+      bulk_load_1d(sQ + slot * G::Q_STAGE_BYTES, q_rows + (int64_t)c0 * NJ, G::Q_STAGE_BYTES,
+                   &full_bar[slot]);
     else
       tma_load_2d(sQ + slot * G::Q_STAGE_BYTES, &tmQ, &full_bar[slot], 0, c0);
   };
@@ -563,15 +570,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     if constexpr (kDB) {
       // columns c = 64 st + 16 (warp & 3) .. + 15 of this stage against the tile's 128 rows
       const int nt = warp & 3, i = lane & 7, mat = lane >> 3;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};  // two MMA chains
 #pragma unroll
       for (int kc = 0; kc < 8; ++kc) {
         uint32_t a[4];  // A = tile^T: rows c (16 nt + 8 (mat & 1) + ..), columns m (16 kc + ..)
         const int m = 16 * kc + i + 8 * (mat >> 1);
         const int chunk = 2 * nt + (mat & 1);
         ldsm_x4_t(tP + m * 128 + ((chunk ^ (m & 7)) << 4), a);
-        mma_16816<H>(d, a, ub[kc]);
+        mma_16816<H>((kc & 1) ? d2 : d, a, ub[kc]);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[e] += d2[e];
       const int g = lane >> 2, q = lane & 3;
       float* dst = epi.db_part + (int64_t)blockIdx.x * C * 16 + 8 * (warp >> 2) + 2 * q;
       const int64_t c = (int64_t)st * TC + 16 * nt + g;
@@ -748,13 +757,14 @@ bool use_narrow(int64_t M, int64_t Nout, int64_t Kc) {
 
 template <bool kQRows, int NJ, bool H, bool kDB>
 int launch_rows(const CUtensorMap& tmP, const CUtensorMap& tmQ, int64_t R, int64_t C, int r,
-                const side::Epi& epi, cudaStream_t stream) {
+                const side::Epi& epi, const uint16_t* q_rows, cudaStream_t stream) {
   constexpr int smem = side::Narrow<NJ>::SMEM_BYTES;
   static DeviceCache<int> attr;  // per instantiation and device
   const int st = ensure_dynamic_smem(attr, side::side_rows<kQRows, NJ, H, kDB>, smem);
   if (st) return st;
   const dim3 grid((unsigned)((R + side::TR - 1) / side::TR));
-  side::side_rows<kQRows, NJ, H, kDB><<<grid, side::THREADS, smem, stream>>>(tmP, tmQ, R, C, r, epi);
+  side::side_rows<kQRows, NJ, H, kDB><<<grid, side::THREADS, smem, stream>>>(tmP, tmQ, R, C, r, epi,
+                                                                            q_rows);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
@@ -777,14 +787,20 @@ int run_rows_t(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_
                                   (uint64_t)q_outer, (uint64_t)q_pitch * 2, (uint32_t)NJ, 64,
                                   MapSwizzle::None);
   if (!qmap) return QLORA_ERR_CUDA;
+  // rows of Q exactly NJ wide (and 16-byte aligned): a stage's Q is one contiguous piece,
+  // loaded as one bulk copy instead of a box of narrow rows
+  const uint16_t* q_rows = (!kQRows && q_pitch == NJ && q_inner == NJ &&
+                            (reinterpret_cast<uintptr_t>(Q) & 15) == 0)
+                               ? Q
+                               : nullptr;
   ProfileScope ps(name, stream);
-  if (kDB) return NJ == 16 ? launch_rows<kQRows, 16, H, kDB>(tmP, tmQ, R, C, r, epi, stream)
+  if (kDB) return NJ == 16 ? launch_rows<kQRows, 16, H, kDB>(tmP, tmQ, R, C, r, epi, q_rows, stream)
                            : QLORA_ERR_UNSUPPORTED;
   switch (NJ) {
-    case 16: return launch_rows<kQRows, 16, H, false>(tmP, tmQ, R, C, r, epi, stream);
-    case 32: return launch_rows<kQRows, 32, H, false>(tmP, tmQ, R, C, r, epi, stream);
-    case 64: return launch_rows<kQRows, 64, H, false>(tmP, tmQ, R, C, r, epi, stream);
-    case 128: return launch_rows<kQRows, 128, H, false>(tmP, tmQ, R, C, r, epi, stream);
+    case 16: return launch_rows<kQRows, 16, H, false>(tmP, tmQ, R, C, r, epi, q_rows, stream);
+    case 32: return launch_rows<kQRows, 32, H, false>(tmP, tmQ, R, C, r, epi, q_rows, stream);
+    case 64: return launch_rows<kQRows, 64, H, false>(tmP, tmQ, R, C, r, epi, q_rows, stream);
+    case 128: return launch_rows<kQRows, 128, H, false>(tmP, tmQ, R, C, r, epi, q_rows, stream);
     default: return QLORA_ERR_UNSUPPORTED;
   }
 }
@@ -857,7 +873,7 @@ int launch_lora_u(const LinearArgs& a, const WorkspaceLayout& L, float* u32, cud
   e.scale_op = a.scale;
   if (narrow_ok && side_narrow_u(a)) {
     e.zero_tickets = reinterpret_cast<int*>(ws + L.tickets);
-    e.nzero = static_cast<int64_t>(L.ntickets + L.ngtickets);
+    e.nzero = static_cast<int64_t>(L.nticket_words);
     return run_rows<true>("side_u", a.X, a.M, a.K, a.K, a.A, a.r, a.K, a.K, a.r, e, a, stream);
   }
   return run_side<false>("side_u", a.X, a.M, a.K, a.K, qs, a.r, e, a, L, stream);
@@ -883,7 +899,7 @@ int launch_lora_v(const LinearArgs& a, const WorkspaceLayout& L, const float* u3
   e.scale_op = a.scale;
   if (side_narrow_v(a)) {
     e.zero_tickets = reinterpret_cast<int*>(ws + L.tickets);
-    e.nzero = static_cast<int64_t>(L.ntickets + L.ngtickets);
+    e.nzero = static_cast<int64_t>(L.nticket_words);
   }
   if (fused_db(a)) {
     if (L.dbpart_bytes < (uint64_t)((a.M + side::TR - 1) / side::TR) * a.N * 64)

@@ -111,11 +111,23 @@ __global__ void __launch_bounds__(THREADS) nf4_merge_kernel(
     if (j < r && k < K) v = __ldg(reinterpret_cast<const uint4*>(A + j * K + k));
     *reinterpret_cast<uint4*>(sA + j * A_PITCH + 8 * c) = v;
   }
-  // B [N][r] -> sB[row][0, r16) (element by element: r need not be a multiple of 8)
-  for (int i = tid; i < ROWS * r16; i += THREADS) {
-    const int rr = i / r16, j = i % r16;
-    const int64_t n = n0 + rr;
-    sB[rr * bp + j] = (n < N && j < r) ? __ldg(B + n * r + j) : static_cast<uint16_t>(0);
+  // B [N][r] -> sB[row][0, r16): 16-byte pieces when the rows are 16-byte multiples, else
+  // element by element
+  if (r % 8 == 0) {
+    const int per = r16 / 8;  // pieces per staged row
+    for (int i = tid; i < ROWS * per; i += THREADS) {
+      const int rr = i / per, j8 = i % per;
+      const int64_t n = n0 + rr;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (n < N && 8 * j8 < r) v = __ldg(reinterpret_cast<const uint4*>(B + n * r + 8 * j8));
+      *reinterpret_cast<uint4*>(sB + rr * bp + 8 * j8) = v;
+    }
+  } else {
+    for (int i = tid; i < ROWS * r16; i += THREADS) {
+      const int rr = i / r16, j = i % r16;
+      const int64_t n = n0 + rr;
+      sB[rr * bp + j] = (n < N && j < r) ? __ldg(B + n * r + j) : static_cast<uint16_t>(0);
+    }
   }
   __syncthreads();
 

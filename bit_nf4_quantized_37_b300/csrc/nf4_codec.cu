@@ -14,6 +14,8 @@
 //                      step = max|a - mean| / 127, int8 codes.
 // Dequantization is one launch (nf4_dequant_kernel) built on the byte-permute table
 // dequantizer shared with the GEMM producers.
+#include <algorithm>
+
 #include "common.cuh"
 #include "nf4_device.cuh"
 #include "launch.h"
@@ -357,14 +359,14 @@ __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict_
 // thread; the four threads of a 64-block each build the block's byte table.  Without double
 // quantization (dq = 0) `steps` holds the fp32 absmax of every block, and the block scale is
 // fmaf(1, absmax, 0) = absmax through the same arithmetic.
-template <bool H>
+template <bool H, bool kDependent>
 __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restrict__ codes,
                                                           const int8_t* __restrict__ scale_codes,
                                                           const float* __restrict__ steps,
                                                           const float* __restrict__ mean,
                                                           int64_t numel, int dq, int fp8,
                                                           uint16_t* __restrict__ out) {
-  launch_dependents();  // a GEMM that streams the output waits for this grid before reading it
+  if (kDependent) launch_dependents();  // the GEMM streaming the output waits for this grid
   const float mu = dq ? __ldg(mean) : 0.0f;
   const int64_t npieces = (numel + 15) / 16;
   for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < npieces;
@@ -404,8 +406,11 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
     }
   }
   // launched as a programmatic dependent (the staged base of a GEMM): the kernel before it
-  // (the rank-r product the GEMM reads) must be complete when this grid is
-  grid_dependency_wait();
+  // (the rank-r product the GEMM reads) must be complete when this grid is; one thread per
+  // CTA waits, so its CTA completes no earlier.  A separate instantiation: the wait raised
+  // the kernel from 30 to 40 registers, 6 instead of 8 resident CTAs per SM (the standalone
+  // 28672 x 8192 dequantization took 137 instead of 104 us).
+  if (kDependent && threadIdx.x == 0) grid_dependency_wait();
 }
 
 // -------------------------------------------------------------------- launchers
@@ -483,13 +488,37 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
+// Resident CTAs per SM of the dequantize kernel (per device and context).
+template <bool H, bool kDependent>
+static int dequant_resident(int* per_sm) {
+  static DeviceCache<int> occupancy;
+  const int st = occupancy.get(device_context_key, per_sm, [](int* v) -> int {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, nf4_dequant_kernel<H, kDependent>, 256,
+                                                      0) != cudaSuccess) {
+      cudaGetLastError();
+      return QLORA_ERR_CUDA;
+    }
+    if (*v < 1) *v = 1;
+    return QLORA_OK;
+  });
+  return st == -1 ? QLORA_ERR_NO_DEVICE : st;
+}
+
 int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, bool half,
                       cudaStream_t stream, bool dependent) {
   const int64_t npieces = (numel + 15) / 16;
   const int threads = 256;
   int64_t blocks = (npieces + threads - 1) / threads;
-  // as a dependent: at most four CTAs per SM, so the kernel before it keeps room to finish
-  const int64_t cap = (int64_t)num_sms() * (dependent ? 4 : 8);
+  // one wave of the grid-stride loop: as many CTAs as are resident (at most 8 per SM; as a
+  // programmatic dependent it launches once every CTA of the kernel before it is running, so
+  // its CTAs only take what is left)
+  int per_sm = 0;
+  const int ost = dependent ? (half ? dequant_resident<true, true>(&per_sm)
+                                    : dequant_resident<false, true>(&per_sm))
+                            : (half ? dequant_resident<true, false>(&per_sm)
+                                    : dequant_resident<false, false>(&per_sm));
+  if (ost) return ost;
+  const int64_t cap = (int64_t)num_sms() * std::min(per_sm, 8);
   if (blocks > cap) blocks = cap;
   ProfileScope ps("nf4_dequant", stream);
   cudaLaunchConfig_t cfg = {};
@@ -502,11 +531,10 @@ int launch_dequantize(const nf4_tensor& q, int64_t numel, uint16_t* out, bool ha
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
   const int dq = q.dq_block != 0 ? 1 : 0, fp8 = q.dq_type == NF4_DQ_FP8 ? 1 : 0;
-  const cudaError_t e =
-      half ? cudaLaunchKernelEx(&cfg, nf4_dequant_kernel<true>, q.codes, q.scale_codes, q.scale_steps,
-                                q.scale_mean, numel, dq, fp8, out)
-           : cudaLaunchKernelEx(&cfg, nf4_dequant_kernel<false>, q.codes, q.scale_codes,
-                                q.scale_steps, q.scale_mean, numel, dq, fp8, out);
+  const auto kernel = dependent ? (half ? nf4_dequant_kernel<true, true> : nf4_dequant_kernel<false, true>)
+                                : (half ? nf4_dequant_kernel<true, false> : nf4_dequant_kernel<false, false>);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, q.codes, q.scale_codes, q.scale_steps,
+                                           q.scale_mean, numel, dq, fp8, out);
   return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 

@@ -17,6 +17,8 @@
 //               scale from global memory two stages ahead, byte-permute dequantization into
 //               the swizzled operand layout), then the epilogue (TMEM -> bf16 -> TMA store)
 // Every wait is bounded; on a time-out the CTA records the site and unwinds.
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 #include "linear.h"
@@ -94,6 +96,13 @@ struct Params {
   // staged base (single-CTA kernel): W' was dequantized into the workspace by the kernel
   // before this one; every NF4 stage takes its W tile by TMA (map tmW) like a LoRA stage
   int wstage;
+  // persistent CTA pairs: pers_clusters clusters share the 512 x 256 tiles; the cluster whose
+  // leader draws ticket k from *pers_ctr (zero at launch) takes tiles k, k + G, k + 2G, ...;
+  // its 16-bit output goes straight from registers to out (row pitch ld_out elements)
+  int* pers_ctr;
+  int pers_clusters;
+  uint16_t* out;
+  int64_t ld_out;
 };
 
 // One thread's share of an NF4 stage: 64 codes (32 bytes) and the block's scale code/step.
@@ -134,6 +143,9 @@ __device__ __forceinline__ void bulk_wait_read1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // ------------------------------------------------------------ split contraction epilogue
 // With nsplit > 1 every CTA first writes its fp32 tile: one output row per thread (my_row),
@@ -799,6 +811,409 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+
+// ============================================================================ persistent pairs
+// The pair GEMM with the tiles shared out among resident CTA pairs (one wave of clusters).
+// Each cluster's leader draws an arrival ticket k and the cluster takes tiles k, k + G, ...
+// (G clusters): the pairs that start first (the others may wait for SMs still held by the
+// rank-r kernel before this one) take the second tiles.  The rings and their barrier phases
+// run on across the tiles (global stage counter); between tiles the dequant warps first fill
+// the B ring with the next tile's first stages, then drain the accumulators (tcgen05.ld ->
+// 16-bit -> global stores straight from registers: the ring's shared memory is in use) and
+// release TMEM to the MMA issuer (tmem_empty, all 16 epilogue warps of the pair), so the next
+// tile starts on a full ring instead of a cold prologue.
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+template <int kMode, bool H>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    fused_pair_persistent(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmA2,
+                          const __grid_constant__ CUtensorMap tmB2,
+                          const __grid_constant__ CUtensorMap tmOut, const Params p) {
+  using pairk::BM_CTA; using pairk::BN_CTA; using pairk::SA; using pairk::SB; using pairk::A_BYTES;
+  using pairk::B_BASE; using pairk::GROUP_WARPS; using pairk::TMEM_COLS;
+  constexpr int B_BYTES = pairk::B_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t a_full[SA];    // (leader) TMA bytes of both CTAs
+  __shared__ __align__(8) uint64_t a_empty[SA];   // (each) multicast commit of the stage's MMAs
+  __shared__ __align__(8) uint64_t bready_bar[SB];
+  __shared__ __align__(8) uint64_t pready_bar[SB];
+  __shared__ __align__(8) uint64_t b_empty[SB];   // (each) multicast commit
+  __shared__ __align__(8) uint64_t acc_bar;       // (each) multicast commit after a tile's MMAs
+  __shared__ __align__(8) uint64_t tmem_empty;    // (leader) the pair's 16 epilogue warps
+  __shared__ __align__(8) uint64_t staging_free;  // (each) its 8 epilogue warps' stores read
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ int s_ticket;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: leader, 1: peer
+  const int n_main = static_cast<int>(p.Kc / BK);
+  const int total = p.n_lora + n_main;
+  const int64_t row_blocks = (p.M + 511) / 512;
+  const int64_t ntiles_all = row_blocks * ((p.Nout + BN - 1) / BN);
+  volatile int* abort_p = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SA; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(&bready_bar[i], GROUP_WARPS + 1);
+      mbar_init(&pready_bar[i], GROUP_WARPS);
+      mbar_init(&b_empty[i], 1);
+    }
+    mbar_init(&acc_bar, 1);
+    mbar_init(&tmem_empty, 2 * NUM_DEQ_WARPS);
+    mbar_init(&staging_free, NUM_DEQ_WARPS);
+    abort_flag = 0;
+    if (rank == 0) s_ticket = atomicAdd(p.pers_ctr, 1);  // this cluster's place in arrival order
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc<2>(&tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the leader's barriers and ticket exist before the peer uses them
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int ticket = rank == 0 ? s_ticket
+                               : static_cast<int>(ld_shared_cluster_u32(mapa_shared(smem_u32(&s_ticket), 0)));
+  const int G = p.pers_clusters;
+  const int ntiles = ticket < ntiles_all ? static_cast<int>((ntiles_all - ticket + G - 1) / G) : 0;
+  // tile i of this cluster: this CTA's A rows and W half
+  const int rb = static_cast<int>(row_blocks);
+  auto tile_m0 = [&](int i) -> int64_t {
+    const int t = ticket + i * G;
+    return (int64_t)(t % rb) * 512 + rank * BM_CTA;
+  };
+  auto tile_n0 = [&](int i) -> int64_t {
+    const int t = ticket + i * G;
+    return (int64_t)(t / rb) * BN;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (elect_one_sync()) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+      int g = 0;  // global stage
+      bool ok = true;
+      for (int i = 0; i < ntiles && ok; ++i) {
+        const int64_t m0 = tile_m0(i), nb0 = tile_n0(i) + rank * BN_CTA;
+        for (int s = 0; s < total; ++s, ++g) {
+          const int as = g % SA, ar = g / SA;
+          if (ar > 0 &&
+              !mbar_wait<true>(&a_empty[as], (ar - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_lead = mapa_shared(smem_u32(&a_full[as]), 0);
+          uint8_t* a_dst = smem + as * A_BYTES;
+          if (s >= n_main) {
+            const int bs = g % SB, br = g / SB;
+            if (br > 0 &&
+                !mbar_wait<true>(&b_empty[bs], (br - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error)) {
+              ok = false;
+              break;
+            }
+            uint8_t* b_dst = smem + B_BASE + bs * B_BYTES;
+            const int li = s - n_main;
+            if (i == 0 && li == 0) grid_dependency_wait();  // sU / sV (and Bp): the kernel before
+            if (rank == 0) mbar_arrive_expect_tx(&a_full[as], 2 * (A_BYTES + B_BYTES));
+            tma_load_2d_pair(a_dst, &tmA2, full_lead, li * BK, (int32_t)m0);
+            if (kMode == 0) {
+              tma_load_2d_pair(b_dst, &tmB2, full_lead, li * BK, (int32_t)nb0);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_2d_pair(b_dst + h * 8192, &tmB2, full_lead, (int32_t)(nb0 + 64 * h), li * BK);
+            }
+          } else {
+            if (rank == 0) mbar_arrive_expect_tx(&a_full[as], 2 * A_BYTES);
+            tma_load_2d_pair(a_dst, &tmA, full_lead, s * BK, (int32_t)m0);
+          }
+        }
+      }
+      // the leader's full barriers count both CTAs' copies: the leader drains them
+      if (rank == 0)
+        for (int q = g - SA < 0 ? 0 : g - SA; q < g; ++q) mbar_drain(&a_full[q % SA], (q / SA) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer (leader)
+    if (rank == 0 && elect_one_sync()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * UM, BN, 0, kMode, H);
+      bool ok = true;
+      int g = 0;
+      uint32_t nf4_parity = 0;  // bit j: parity of the NF4 stages through B slot j so far
+      for (int i = 0; i < ntiles && ok; ++i) {
+        if (i > 0) {  // the previous tile's accumulators drained by both CTAs' epilogues
+          if (!(ok = mbar_wait<true>(&tmem_empty, (i - 1) & 1, kWaitAccFull, abort_p, &g_gemm_error)))
+            break;
+          tc_fence_after();
+        }
+        for (int s = 0; s < total; ++s, ++g) {
+          const int as = g % SA, ar = g / SA, bs = g % SB;
+          ok = mbar_wait<true>(&a_full[as], ar & 1, kWaitTmaFull, abort_p, &g_gemm_error);
+          if (ok && s < n_main) {
+            ok = mbar_wait<true>(&bready_bar[bs], (nf4_parity >> bs) & 1, kWaitBReady, abort_p,
+                                 &g_gemm_error);
+            nf4_parity ^= 1u << bs;
+          }
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + as * A_BYTES);
+          const uint32_t b_addr = smem_u32(smem + B_BASE + bs * B_BYTES);
+          const int ksteps = (s >= n_main && s == total - 1) ? p.lora_last_k16 : 4;
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t bdesc = (kMode == 0)
+                                       ? smem_desc(b_addr + kk * 32, 16, 1024, Swizzle::B128)
+                                       : smem_desc(b_addr + kk * 2048, 8192, 1024, Swizzle::B128);
+#pragma unroll
+            for (int acc = 0; acc < 2; ++acc) {
+              const uint64_t adesc =
+                  smem_desc(a_addr + acc * (UM * BK * 2) + kk * 32, 16, 1024, Swizzle::B128);
+              umma_bf16_ss<2>(tmem + acc * 256, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit_pair(&a_empty[as], 0x3);
+          umma_commit_pair(&b_empty[bs], 0x3);
+        }
+        if (ok) umma_commit_pair(&acc_bar, 0x3);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ relay (peer)
+    // each NF4 stage's dequantized half of the peer, forwarded to the leader's bready barrier;
+    // lane j serves B slot j (the stages g with g % SB == j), so the cluster-scope releases of
+    // consecutive stages are in flight together
+    if (rank == 1 && lane < SB) {
+      // each lane walks only its own stages (a loop over all stages would reconverge the warp
+      // at every stage and serialise the lanes' waits)
+      const uint32_t bready_lead = mapa_shared(smem_u32(&bready_bar[lane]), 0);
+      uint32_t parity = 0;
+      int s = lane;  // stage within the tile of global stage g
+      for (int g = lane; g < ntiles * total; g += SB, s += SB) {
+        while (s >= total) s -= total;
+        if (s >= n_main) continue;  // a LoRA stage: by TMA, nothing to forward
+        if (!mbar_wait(&pready_bar[lane], parity, kWaitBReady, abort_p, &g_gemm_error)) break;
+        parity ^= 1;
+        mbar_arrive_cluster(bready_lead);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= DEQ_WARP0) {
+    // ------------------------------------------------------------ NF4 producers + epilogue
+    const int group = (warp - DEQ_WARP0) / GROUP_WARPS;           // stages s % 2 == group
+    const int t = ((warp - DEQ_WARP0) % GROUP_WARPS) * 32 + lane;  // 0..127
+    const float mu = p.dq ? __ldg(p.mean) : 0.0f;
+    uint32_t dst_off, swz;
+    int nl = 0, blk = 0;
+    if (kMode == 0) {
+      dst_off = t * 128;
+      swz = t & 7;
+    } else {
+      nl = (t & 7) + 8 * ((t >> 3) & 7);  // W row within the stage's 64
+      blk = t >> 6;                        // which 64 of this CTA's 128 columns
+      dst_off = blk * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
+      swz = nl & 7;
+    }
+    // this group's items: (tile i, NF4 stage s = group + 2 j), tile-major, walked by two
+    // cursors (the next item to store, and the item whose slice is loaded next) so that no
+    // division runs per stage
+    const int per = n_main > group ? (n_main - group + 1) / 2 : 0;
+    const int nitems = ntiles * per;
+    // A slice of NF4 stage s of a tile is 32 code bytes at cbase + s * cstride and the block
+    // scale of block bbase + s * bstride (tile-constant bases, so no 64-bit index math per stage)
+    struct Cursor {
+      int i, j;              // tile of this cluster, item within the tile
+      const uint8_t* cbase;  // this thread's code bytes in stage 0 of tile i
+      int64_t bbase;         // its 64-block in stage 0
+      bool valid;            // its W row / column lies inside W
+    };
+    const int64_t cstride = kMode == 0 ? BK / 2 : (int64_t)BK * (p.Kw / 2);
+    const int64_t bstride = kMode == 0 ? 1 : (int64_t)BK * (p.Kw / 64);
+    auto cursor_tile = [&](Cursor& c) {
+      const int64_t nb0 = tile_n0(c.i) + rank * BN_CTA;
+      const int64_t row = kMode == 0 ? nb0 + t : nl;         // W row in stage 0
+      const int64_t kcol = kMode == 0 ? 0 : nb0 + blk * 64;  // W column in stage 0
+      c.valid = row < p.Nw && kcol < p.Kw;
+      c.cbase = p.codes + row * (p.Kw / 2) + kcol / 2;
+      c.bbase = row * (p.Kw / 64) + kcol / 64;
+    };
+    auto advance = [&](Cursor& c) {
+      if (++c.j == per) {
+        c.j = 0;
+        if (++c.i < ntiles) cursor_tile(c);
+      }
+    };
+    Cursor ld{0, 0, nullptr, 0, false}, st{0, 0, nullptr, 0, false};
+    if (ntiles > 0) {
+      cursor_tile(ld);
+      cursor_tile(st);
+    }
+    auto next_slice = [&](Slice& sl) {  // the slice of item `ld`, then advance it
+      sl.valid = false;
+      if (ld.i >= ntiles || per == 0) return;
+      const int s = group + 2 * ld.j;
+      if (ld.valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(ld.cbase + s * cstride);
+        sl.c0 = __ldg(src);
+        sl.c1 = __ldg(src + 1);
+        const int64_t b = ld.bbase + s * bstride;
+        if (p.dq) {
+          sl.q = nf4_second_level(static_cast<uint8_t>(__ldg(p.qs + b)), p.fp8);
+          sl.step = __ldg(p.steps + (b >> 8));
+        } else {
+          sl.q = 1.0f;
+          sl.step = __ldg(p.steps + b);
+        }
+        sl.valid = true;
+      }
+      advance(ld);
+    };
+    uint4 rv[8];
+    auto dequant = [&](const Slice& cur) {
+      if (cur.valid) {
+        const Nf4ByteTable tab = nf4_make_table<H>(__fmaf_rn(cur.q, cur.step, mu));
+        const uint32_t words[8] = {cur.c0.x, cur.c0.y, cur.c0.z, cur.c0.w,
+                                   cur.c1.x, cur.c1.y, cur.c1.z, cur.c1.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[4];
+          nf4_dequant8(tab, words[c], o);
+          rv[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) rv[c] = make_uint4(0, 0, 0, 0);
+      }
+    };
+    auto put = [&]() -> bool {  // item `st`, then advance it
+      const int g = st.i * total + group + 2 * st.j;
+      advance(st);
+      const int slot = g % SB, round = g / SB;
+      if (round > 0 &&
+          !mbar_wait<true>(&b_empty[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_gemm_error))
+        return false;
+      uint8_t* dst = smem + B_BASE + slot * B_BYTES + dst_off;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + ((c ^ swz) << 4)) = rv[c];
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rank == 0 ? &bready_bar[slot] : &pready_bar[slot]);
+      return true;
+    };
+    // Epilogue of tile i: this warp's 32 TMEM lanes of its slab, 8 chunks of 32 columns (TMEM
+    // -> 16-bit -> 64-byte-swizzled staging -> TMA store, two 2 KB buffers per warp).  The
+    // staging lies in the two B slots that the next tile's stages 4 and 5 will take: the groups
+    // fill only its first 4 stages before the epilogue, and every previous use of those two
+    // slots was consumed before the accumulators were complete.  Then TMEM is released.
+    const int lg = warp & 3;                  // TMEM lanes 32 lg .. 32 lg + 31
+    const int acc = (warp - DEQ_WARP0) >> 2;  // accumulator (128-row slab)
+    const uint32_t taddr = tmem + static_cast<uint32_t>(acc * 256) + (static_cast<uint32_t>(lg * 32) << 16);
+    const uint32_t tmem_empty_lead = mapa_shared(smem_u32(&tmem_empty), 0);
+    auto epilogue = [&](int i) -> bool {
+      if (!mbar_wait<true>(&acc_bar, i & 1, kWaitAccFull, abort_p, &g_gemm_error)) return false;
+      tc_fence_after();
+      const int g0 = (i + 1) * total;  // the next tile's first stage (or one past the last)
+      const int slot = (g0 + 4 + (warp - DEQ_WARP0) / 4) % SB;
+      uint8_t* buf0 = smem + B_BASE + slot * B_BYTES + ((warp - DEQ_WARP0) % 4) * 4096;
+      const int64_t row0 = tile_m0(i) + acc * UM + lg * 32;
+      const int64_t n0 = tile_n0(i);
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, v);
+        tmem_ld_wait();
+        uint8_t* buf = buf0 + (c & 1) * 2048;
+        if (c >= 2) {
+          if (lane == 0) bulk_wait_read1();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t phys = j ^ ((lane >> 1) & 3);  // 64-byte swizzle
+          *reinterpret_cast<uint4*>(buf + lane * 64 + phys * 16) = make_uint4(
+              pack_pair<H>(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+              pack_pair<H>(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+              pack_pair<H>(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+              pack_pair<H>(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (n0 + c * 32 < p.Nout && row0 < p.M)
+            tma_store_2d(&tmOut, buf, (int32_t)(n0 + c * 32), (int32_t)row0);
+          bulk_commit();
+        }
+      }
+      if (lane == 0) bulk_wait_read0();  // the staging is read: the slots may be refilled
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(&tmem_empty);
+        else mbar_arrive_cluster(tmem_empty_lead);
+      }
+      // every dequant warp's stores have left the staging before either slot is refilled
+      // (a bounded wait: a warp that gave up never hangs the others)
+      if (lane == 0) mbar_arrive(&staging_free);
+      return mbar_wait(&staging_free, i & 1, kWaitAccFull, abort_p, &g_gemm_error);
+    };
+    // The item stream: `sa` / `sb` hold the slices of the next two items (by item parity);
+    // step() stores the next item, starts the load of the one two ahead into the set it frees
+    // and dequantizes the following one into registers.
+    constexpr int kPre = 2;  // the next tile's stages per group filled before an epilogue
+    const int pre = per < kPre ? per : kPre;
+    // Two items per iteration with the two register sets in fixed roles, as in the one-tile
+    // kernel: `sa` holds the next item (already dequantized into rv), `sb` the one after.
+    Slice sa, sb;
+    next_slice(sa);
+    next_slice(sb);
+    if (nitems > 0) dequant(sa);
+    bool ok = true;
+    int produced = 0;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      const int target = min((i + 1) * per + (i + 1 < ntiles ? pre : 0), nitems);
+      while (ok && produced + 2 <= target) {
+        if (!(ok = put())) break;
+        next_slice(sa);
+        dequant(sb);
+        if (!(ok = put())) break;
+        next_slice(sb);
+        dequant(sa);
+        produced += 2;
+      }
+      if (ok && produced < target) {  // an odd item: store it and let the sets trade roles
+        if ((ok = put())) {
+          next_slice(sa);
+          dequant(sb);
+          const Slice tmp = sa;
+          sa = sb;
+          sb = tmp;
+          ++produced;
+        }
+      }
+      if (ok) ok = epilogue(i);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its pair may still touch its barriers or smem
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<2>(tmem, TMEM_COLS);
+  }
+}
 }  // namespace fused
 
 namespace {
@@ -892,7 +1307,23 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, const FusedPlan&
   cfg.attrs = attr;
   cfg.numAttrs = a.gemm_priority ? 2 : 1;
   cudaError_t e;
-  if (kPair) {  // the CTA pair is the kernel's compile-time cluster shape
+  // (the persistent kernel stages each epilogue in the B slots of the next tile's NF4 stages
+  // 4 and 5, so it needs at least 6 NF4 stages)
+  if (kPair && plan.nsplit == 1 && p.Kc / BK >= 6) {
+    // persistent pairs: one wave of clusters sharing the tiles (the CTA pair is the kernel's
+    // compile-time cluster shape)
+    static DeviceCache<int> smem_attr_p;
+    const int st = ensure_dynamic_smem(smem_attr_p, fused_pair_persistent<kMode, H>, SMEM_BYTES);
+    if (st) return st;
+    const int64_t tiles = ((a.M + 511) / 512) * ((p.Nout + BN - 1) / BN);
+    const int clusters = static_cast<int>(std::min<int64_t>(tiles, num_sms() / 2));
+    p.pers_ctr = reinterpret_cast<int*>(ws + L.pers_ctr);
+    p.pers_clusters = clusters;
+    p.out = kMode == 0 ? a.Y : a.dX;
+    p.ld_out = p.Nout;
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    e = cudaLaunchKernelEx(&cfg, fused_pair_persistent<kMode, H>, tA, tA2, tB2, tOut, p);
+  } else if (kPair) {  // the CTA pair is the kernel's compile-time cluster shape
     cfg.gridDim = dim3((unsigned)(2 * ((a.M + 511) / 512)), (unsigned)((p.Nout + BN - 1) / BN),
                        (unsigned)plan.nsplit);
     e = cudaLaunchKernelEx(&cfg, fused_pair_gemm<kMode, H>, tA, tA2, tB2, tOut, p);
