@@ -445,10 +445,11 @@ __global__ void __launch_bounds__(THREADS, 2)
 //           read with ldmatrix.trans.
 // Rows past r (or past rq) arrive as zeros.
 // kDB (V with rank <= 16): the dY tile of each stage also feeds the partial products of
-// dB = dY^T U over the CTA's 128 rows.  Warp w takes 16 columns of the stage (w & 3) and 8 of
-// the rank (w >> 2): an m16n8k16 with A = the tile read transposed (ldmatrix.trans) and B = the
-// rows' U in the 16-bit type, held in registers for the whole launch.  A fixed-order sum of
-// the row tiles' partials (db_reduce) finishes dB.
+// dB = dY^T U over the CTA's 128 rows, on 8 more warps beside the 8 of V (measured: 39 us per
+// launch with both on the same 8 warps).  dB warp w takes 16 columns of the stage (w & 3) and 8
+// of the rank (w >> 2): an m16n8k16 with A = the tile read transposed (ldmatrix.trans) and
+// B = the rows' U in the 16-bit type, held in registers for the whole launch.  A fixed-order
+// sum of the row tiles' partials (db_reduce) finishes dB.
 template <int NJ>
 struct Narrow {
   static constexpr int Q_STAGE_BYTES = NJ * TC * 2;
@@ -457,66 +458,92 @@ struct Narrow {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 };
 
+// The consumer warps (8 for U / V: 16 rows each; 16 with kDB: 8 more form the dB partials)
+// and one producer warp.  Each stage's slot is released by an empty barrier that every
+// consumer warp arrives on after its last read, so the warps drift freely across the ring
+// (measured: a CTA-wide barrier per stage made the launch wait on its slowest warp every
+// stage).
+template <bool kDB>
+struct NarrowWarps {
+  static constexpr int kConsumers = kDB ? 2 * (THREADS / 32) : THREADS / 32;
+  static constexpr int kThreads = (kConsumers + 1) * 32;
+};
+
 template <bool kQRows, int NJ, bool H, bool kDB>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(NarrowWarps<kDB>::kThreads, 1)
     side_rows(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-              int64_t R, int64_t C, int r, Epi epi, const uint16_t* __restrict__ q_rows) {
+              int64_t R, int64_t C, int r, Epi epi) {
   using G = Narrow<NJ>;
   constexpr int S = G::STAGES;
+  constexpr int NWC = NarrowWarps<kDB>::kConsumers;
+  constexpr int kThreads = NarrowWarps<kDB>::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sP = smem;                          // S x [128 rows x 64 c], 128-byte swizzled
   uint8_t* sQ = smem + S * P_STAGE_BYTES;      // S x Q tile (1 KB multiples: swizzle atoms)
   __shared__ __align__(8) uint64_t full_bar[S];
+  __shared__ __align__(8) uint64_t empty_bar[S];
   __shared__ int abort_flag;
   volatile int* abort_p = &abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool v_warp = warp < THREADS / 32;       // forms U / V (rows 16 warp ..)
+  const int dw = warp - THREADS / 32;            // kDB: dB warp index (0..7)
   const int64_t r0 = (int64_t)blockIdx.x * TR;
   const int nst = static_cast<int>((C + TC - 1) / TC);
 
   if (tid == 0) {
-    for (int i = 0; i < S; ++i) mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], NWC);
+    }
     abort_flag = 0;
     fence_barrier_init();
   }
   // the tickets are zero (and visible device-wide) before the kernel behind this one, which
   // draws from them before it waits for this grid, may start
   if (blockIdx.x == 0 && epi.zero_tickets) {
-    for (int64_t i = tid; i < epi.nzero; i += THREADS) epi.zero_tickets[i] = 0;
+    for (int64_t i = tid; i < epi.nzero; i += kThreads) epi.zero_tickets[i] = 0;
     __threadfence();
   }
   __syncthreads();
   launch_dependents();
 
-  auto issue = [&](int st) {
-    const int slot = st % S;
-    const int32_t c0 = static_cast<int32_t>((int64_t)st * TC);
-    mbar_arrive_expect_tx(&full_bar[slot], G::STAGE_BYTES);
-    tma_load_2d(sP + slot * P_STAGE_BYTES, &tmP, &full_bar[slot], c0, static_cast<int32_t>(r0));
-    if (kQRows)
-      tma_load_2d(sQ + slot * G::Q_STAGE_BYTES, &tmQ, &full_bar[slot], c0, 0);
-    else if (q_rows && c0 + TC <= C)  // whole stage of Q rows of exactly NJ: one contiguous piece
-      bulk_load_1d(sQ + slot * G::Q_STAGE_BYTES, q_rows + (int64_t)c0 * NJ, G::Q_STAGE_BYTES,
-                   &full_bar[slot]);
-    else
-      tma_load_2d(sQ + slot * G::Q_STAGE_BYTES, &tmQ, &full_bar[slot], 0, c0);
-  };
-  int issued = 0;
-  if (tid == 0) {
-    tma_prefetch_desc(&tmP);
-    tma_prefetch_desc(&tmQ);
-    for (; issued < S - 1 && issued < nst; ++issued) issue(issued);
+  if (warp == NWC) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmP);
+      tma_prefetch_desc(&tmQ);
+      int issued = 0;
+      for (; issued < nst; ++issued) {
+        const int slot = issued % S, round = issued / S;
+        if (round > 0 &&
+            !mbar_wait(&empty_bar[slot], (round - 1) & 1, kWaitEmpty, abort_p, &g_side_error))
+          break;
+        fence_proxy_async_smem();  // the consumers' reads of the slot precede the refill
+        const int32_t c0 = static_cast<int32_t>((int64_t)issued * TC);
+        mbar_arrive_expect_tx(&full_bar[slot], G::STAGE_BYTES);
+        tma_load_2d(sP + slot * P_STAGE_BYTES, &tmP, &full_bar[slot], c0, static_cast<int32_t>(r0));
+        if (kQRows)
+          tma_load_2d(sQ + slot * G::Q_STAGE_BYTES, &tmQ, &full_bar[slot], c0, 0);
+        else
+          tma_load_2d(sQ + slot * G::Q_STAGE_BYTES, &tmQ, &full_bar[slot], 0, c0);
+      }
+      // never leave with a copy in flight into this CTA's shared memory
+      for (int st = issued - S < 0 ? 0 : issued - S; st < issued; ++st)
+        mbar_drain(&full_bar[st % S], (st / S) & 1);
+    }
+    return;
   }
 
   float acc[NJ / 8][4];
 #pragma unroll
   for (int t = 0; t < NJ / 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 
-  // kDB: B fragments of U (rows r0 + 16 kc + 2 q (+1, +8, +9), rank 8 (warp >> 2) + g)
+  // kDB: B fragments of U (rows r0 + 16 kc + 2 q (+1, +8, +9), rank 8 (dw >> 2) + g)
   uint32_t ub[kDB ? 8 : 1][2];
-  if constexpr (kDB) {
-    const int g = lane >> 2, q = lane & 3, j = 8 * (warp >> 2) + g;
+  if (kDB && !v_warp) {
+    const int g = lane >> 2, q = lane & 3, j = 8 * (dw >> 2) + g;
 #pragma unroll
     for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
@@ -527,49 +554,46 @@ __global__ void __launch_bounds__(THREADS, 1)
         ub[kc][h] = pack_pair<H>(lo, hi);
       }
   }
+  // Q rows of NJ j (2 NJ bytes) with the swizzle of that span (32 / 64 / 128 bytes; none for
+  // wider rows): 16-byte chunk h of row c sits at chunk h ^ ((c * 2 NJ / 128) & (2 NJ / 16 - 1))
+  constexpr int QSPAN = 2 * NJ;
+  constexpr int QXOR = QSPAN <= 128 ? QSPAN / 16 - 1 : 0;
 
-  bool ok = true;
   for (int st = 0; st < nst; ++st) {
-    ok = mbar_wait(&full_bar[st % S], (st / S) & 1, kWaitTmaFull, abort_p, &g_side_error);
-    __syncthreads();  // every warp is past stage st - 1: its buffers can be refilled
-    if (!ok || *abort_p) {
-      ok = false;
-      break;
-    }
-    if (tid == 0 && st + S - 1 < nst) {
-      fence_proxy_async_smem();  // the generic-proxy reads of those buffers precede the refill
-      issue(st + S - 1);
-      ++issued;
-    }
-    const uint32_t tP = smem_u32(sP + (st % S) * P_STAGE_BYTES);
-    const uint32_t tQ = smem_u32(sQ + (st % S) * G::Q_STAGE_BYTES);
+    const int slot = st % S;
+    if (!mbar_wait(&full_bar[slot], (st / S) & 1, kWaitTmaFull, abort_p, &g_side_error)) return;
+    const uint32_t tP = smem_u32(sP + slot * P_STAGE_BYTES);
+    const uint32_t tQ = smem_u32(sQ + slot * G::Q_STAGE_BYTES);
+    if (v_warp) {
 #pragma unroll
-    for (int kk = 0; kk < TC / 16; ++kk) {
-      uint32_t a[4];
-      {
-        const int row = warp * 16 + (lane & 15);
-        ldsm_x4(tP + row * 128 + ((((kk * 2 + (lane >> 4)) ^ (row & 7))) << 4), a);
-      }
-#pragma unroll
-      for (int t = 0; t < NJ / 8; t += 2) {
-        // lanes 0-15: n-tile t, lanes 16-31: n-tile t + 1; within each, c halves 0-7 / 8-15
-        uint32_t b[4];
-        if (kQRows) {
-          const int j = 8 * (t + (lane >> 4)) + (lane & 7);
-          const int chunk = kk * 2 + ((lane >> 3) & 1);
-          ldsm_x4(tQ + j * 128 + ((chunk ^ (j & 7)) << 4), b);
-        } else {
-          const int c = kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-          ldsm_x4_t(tQ + c * (NJ * 2) + (t + (lane >> 4)) * 16, b);
+      for (int kk = 0; kk < TC / 16; ++kk) {
+        uint32_t a[4];
+        {
+          const int row = warp * 16 + (lane & 15);
+          ldsm_x4(tP + row * 128 + ((((kk * 2 + (lane >> 4)) ^ (row & 7))) << 4), a);
         }
-        const uint32_t b0[2] = {b[0], b[1]}, b1[2] = {b[2], b[3]};
-        mma_16816<H>(acc[t], a, b0);
-        mma_16816<H>(acc[t + 1], a, b1);
+#pragma unroll
+        for (int t = 0; t < NJ / 8; t += 2) {
+          // lanes 0-15: n-tile t, lanes 16-31: n-tile t + 1; within each, c halves 0-7 / 8-15
+          uint32_t b[4];
+          if (kQRows) {
+            const int j = 8 * (t + (lane >> 4)) + (lane & 7);
+            const int chunk = kk * 2 + ((lane >> 3) & 1);
+            ldsm_x4(tQ + j * 128 + ((chunk ^ (j & 7)) << 4), b);
+          } else {
+            const int c = kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+            const int h = t + (lane >> 4);
+            ldsm_x4_t(tQ + c * QSPAN + ((h ^ ((c * QSPAN / 128) & QXOR)) << 4), b);
+          }
+          const uint32_t b0[2] = {b[0], b[1]}, b1[2] = {b[2], b[3]};
+          mma_16816<H>(acc[t], a, b0);
+          mma_16816<H>(acc[t + 1], a, b1);
+        }
       }
     }
-    if constexpr (kDB) {
-      // columns c = 64 st + 16 (warp & 3) .. + 15 of this stage against the tile's 128 rows
-      const int nt = warp & 3, i = lane & 7, mat = lane >> 3;
+    if (kDB && !v_warp) {
+      // columns c = 64 st + 16 (dw & 3) .. + 15 of this stage against the tile's 128 rows
+      const int nt = dw & 3, i = lane & 7, mat = lane >> 3;
       float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};  // two MMA chains
 #pragma unroll
       for (int kc = 0; kc < 8; ++kc) {
@@ -581,23 +605,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) d[e] += d2[e];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);  // this warp's reads of the slot are done
       const int g = lane >> 2, q = lane & 3;
-      float* dst = epi.db_part + (int64_t)blockIdx.x * C * 16 + 8 * (warp >> 2) + 2 * q;
+      float* dst = epi.db_part + (int64_t)blockIdx.x * C * 16 + 8 * (dw >> 2) + 2 * q;
       const int64_t c = (int64_t)st * TC + 16 * nt + g;
       if (c < C) __stcg(reinterpret_cast<float2*>(dst + c * 16), make_float2(d[0], d[1]));
       if (c + 8 < C) __stcg(reinterpret_cast<float2*>(dst + (c + 8) * 16), make_float2(d[2], d[3]));
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);  // this warp's reads of the slot are done
     }
-  }
-  if (!ok) {
-    if (tid == 0)
-      for (int st = issued - (S - 1) < 0 ? 0 : issued - (S - 1); st < issued; ++st)
-        mbar_drain(&full_bar[st % S], (st / S) & 1);
-    __syncthreads();
-    return;
   }
 
   // outputs straight from the accumulators: lane (g, q) holds rows g and g + 8 of the warp's
   // 16, columns 8t + 2q and 8t + 2q + 1
+  if (!v_warp) return;
   const int g = lane >> 2, q = lane & 3;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -757,19 +780,21 @@ bool use_narrow(int64_t M, int64_t Nout, int64_t Kc) {
 
 template <bool kQRows, int NJ, bool H, bool kDB>
 int launch_rows(const CUtensorMap& tmP, const CUtensorMap& tmQ, int64_t R, int64_t C, int r,
-                const side::Epi& epi, const uint16_t* q_rows, cudaStream_t stream) {
+                const side::Epi& epi, cudaStream_t stream) {
   constexpr int smem = side::Narrow<NJ>::SMEM_BYTES;
   static DeviceCache<int> attr;  // per instantiation and device
   const int st = ensure_dynamic_smem(attr, side::side_rows<kQRows, NJ, H, kDB>, smem);
   if (st) return st;
   const dim3 grid((unsigned)((R + side::TR - 1) / side::TR));
-  side::side_rows<kQRows, NJ, H, kDB><<<grid, side::THREADS, smem, stream>>>(tmP, tmQ, R, C, r, epi,
-                                                                            q_rows);
+  side::side_rows<kQRows, NJ, H, kDB><<<grid, side::NarrowWarps<kDB>::kThreads, smem, stream>>>(
+      tmP, tmQ, R, C, r, epi);
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
-// P: [R rows][C] (ldp).  Q: kQRows -> [q_outer rows = r][q_inner = C] (A); else
-// [q_outer = C][q_inner] (B).  kDB: the V form with the dB partials (rank <= 16).
+// P: [R rows][C] (ldp).  Q: kQRows -> [q_outer rows = r][q_inner = C] (A), 128-byte swizzled
+// boxes of [64 c x NJ rows]; else [q_outer = C][q_inner] (B) in boxes of [NJ j x 64 c], with
+// the swizzle of their 2 NJ-byte rows (none past 128 bytes).  kDB: the V form with the dB
+// partials (rank <= 16).
 template <bool kQRows, bool H, bool kDB>
 int run_rows_t(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_t ldp,
                const uint16_t* Q, int64_t q_outer, int64_t q_inner, int64_t q_pitch, int r,
@@ -779,28 +804,25 @@ int run_rows_t(const char* name, const uint16_t* P, int64_t R, int64_t C, int64_
   if (!make_tensor_map_2d(&tmP, P, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)C, (uint64_t)R,
                           (uint64_t)ldp * 2, 64, side::TR, MapSwizzle::B128))
     return QLORA_ERR_CUDA;
+  const MapSwizzle qsw = NJ == 16 ? MapSwizzle::B32
+                       : NJ == 32 ? MapSwizzle::B64
+                       : NJ == 64 ? MapSwizzle::B128
+                                  : MapSwizzle::None;
   const bool qmap =
       kQRows ? make_tensor_map_2d(&tmQ, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)q_inner,
                                   (uint64_t)q_outer, (uint64_t)q_pitch * 2, 64, (uint32_t)NJ,
                                   MapSwizzle::B128)
              : make_tensor_map_2d(&tmQ, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)q_inner,
-                                  (uint64_t)q_outer, (uint64_t)q_pitch * 2, (uint32_t)NJ, 64,
-                                  MapSwizzle::None);
+                                  (uint64_t)q_outer, (uint64_t)q_pitch * 2, (uint32_t)NJ, 64, qsw);
   if (!qmap) return QLORA_ERR_CUDA;
-  // rows of Q exactly NJ wide (and 16-byte aligned): a stage's Q is one contiguous piece,
-  // loaded as one bulk copy instead of a box of narrow rows
-  const uint16_t* q_rows = (!kQRows && q_pitch == NJ && q_inner == NJ &&
-                            (reinterpret_cast<uintptr_t>(Q) & 15) == 0)
-                               ? Q
-                               : nullptr;
   ProfileScope ps(name, stream);
-  if (kDB) return NJ == 16 ? launch_rows<kQRows, 16, H, kDB>(tmP, tmQ, R, C, r, epi, q_rows, stream)
+  if (kDB) return NJ == 16 ? launch_rows<kQRows, 16, H, kDB>(tmP, tmQ, R, C, r, epi, stream)
                            : QLORA_ERR_UNSUPPORTED;
   switch (NJ) {
-    case 16: return launch_rows<kQRows, 16, H, false>(tmP, tmQ, R, C, r, epi, q_rows, stream);
-    case 32: return launch_rows<kQRows, 32, H, false>(tmP, tmQ, R, C, r, epi, q_rows, stream);
-    case 64: return launch_rows<kQRows, 64, H, false>(tmP, tmQ, R, C, r, epi, q_rows, stream);
-    case 128: return launch_rows<kQRows, 128, H, false>(tmP, tmQ, R, C, r, epi, q_rows, stream);
+    case 16: return launch_rows<kQRows, 16, H, false>(tmP, tmQ, R, C, r, epi, stream);
+    case 32: return launch_rows<kQRows, 32, H, false>(tmP, tmQ, R, C, r, epi, stream);
+    case 64: return launch_rows<kQRows, 64, H, false>(tmP, tmQ, R, C, r, epi, stream);
+    case 128: return launch_rows<kQRows, 128, H, false>(tmP, tmQ, R, C, r, epi, stream);
     default: return QLORA_ERR_UNSUPPORTED;
   }
 }

@@ -195,7 +195,9 @@ def test_fwd_bwd_small(name, M, N, K, r, alpha):
                                      (2100, 4864, 256, 16),    # forward pairs, 5th pair row partial
                                      (2100, 256, 4864, 16),    # input gradient, the same
                                      (512, 3072, 3072, 16),    # 128-row tiles, 3-way split contraction
-                                     (400, 3072, 2560, 24)])   # the same, rows past M in the tile
+                                     (400, 3072, 2560, 24),    # the same, rows past M in the tile
+                                     (1024, 4864, 512, 128),   # narrow U at rank 128 (unswizzled rows)
+                                     (1024, 512, 4864, 128)])  # narrow V at rank 128
 def test_pair_tiles_every_output(M, N, K, r):
     """The fused GEMMs against the oracle on every output element: the CTA pairs (512 x 256
     tiles: all 16 row classes of a pair tile -- 2 CTAs x 2 accumulators x 4 TMEM lane groups
