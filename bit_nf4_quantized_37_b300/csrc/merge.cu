@@ -178,8 +178,13 @@ __global__ void __launch_bounds__(THREADS) nf4_merge_kernel(
     const int64_t n = n0 + rr;
     if (n >= N) break;
     const int64_t e = n * K + kk;
-    const float4 d0 = *reinterpret_cast<const float4*>(sD + rr * D_PITCH + 8 * c8);
-    const float4 d1 = *reinterpret_cast<const float4*>(sD + rr * D_PITCH + 8 * c8 + 4);
+    // the thread's two 16-byte pieces, in an order that alternates by groups of 4 lanes, so
+    // the 16 lanes of a row cover all 8 bank groups in each load (in column order, only the
+    // even pieces in the first load: 4-way conflicts)
+    const int sw = (c8 >> 2) & 1;
+    const float4 e0 = *reinterpret_cast<const float4*>(sD + rr * D_PITCH + 8 * c8 + 4 * sw);
+    const float4 e1 = *reinterpret_cast<const float4*>(sD + rr * D_PITCH + 8 * c8 + 4 * (1 - sw));
+    const float4 d0 = sw ? e1 : e0, d1 = sw ? e0 : e1;
     const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
     const float a_hat = dq ? __fmaf_rn(nf4_second_level(scode[p], fp8), sstep[p], mu) : sstep[p];
     uint32_t wd[4];
