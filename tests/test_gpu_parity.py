@@ -375,8 +375,7 @@ def _ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
     return np.abs(key(a) - key(b))
 
 
-@pytest.mark.parametrize("cfg", ["config1", "config2"])
-def test_merge_matches_oracle(cfg):
+def _check_merge(p):
     """bf16(W' + s B A): the device's fp32 bracket against the oracle's fp64 one, each rounded
     once to bf16.  Bound from the fp32 arithmetic: the r exact bf16 x bf16 products summed on
     the tensor cores (r additions; their fp32 accumulation is not specified as
@@ -384,7 +383,6 @@ def test_merge_matches_oracle(cfg):
     (2 r + 2) 2^-24 (|W'| + s sum_j |B A|) before the final rounding, so the two results differ
     by at most that plus one bf16 step of the result; more than one step only where W' and
     s B A nearly cancel.  Differences of any size are rare (~2^-16)."""
-    p = getattr(wl, cfg)()
     W = p.W()
     qo = oracle.quantize(W)
     qd = qn.nf4_quantize(torch.from_numpy(W).cuda())
@@ -403,6 +401,22 @@ def test_merge_matches_oracle(cfg):
     bound = (2 * p.r + 2) * 2.0 ** -24 * mag + step
     assert np.all(np.abs(gv - wv) <= bound)
     assert np.array_equal(m32.cpu().numpy(), wl.bf16_bits_to_f32(got))
+
+
+@pytest.mark.parametrize("cfg", ["config1", "config2"])
+def test_merge_matches_oracle(cfg):
+    """The merge on the config shapes (ranks 8 and 16: the persistent form)."""
+    _check_merge(getattr(wl, cfg)())
+
+
+@pytest.mark.parametrize("N,K,r", [(200, 320, 24),    # persistent form, rank 24 (32-wide slices)
+                                   (200, 320, 12),    # one-tile form: rank not a multiple of 8
+                                   (130, 448, 40),    # one-tile form: rank past 32
+                                   (64, 8192, 128)])  # one-tile form at the largest rank
+def test_merge_ranks_and_ragged(N, K, r):
+    """The merge's two forms on ragged tiles (rows past N, columns past K in the last tiles)."""
+    p = wl.LinearProblem(f"merge-{N}-{K}-{r}", 16, N, K, r, 2.0 * r, 0.02, 0.001, config=79)
+    _check_merge(p)
 
 
 def test_merge_zero_adapter_is_dequantize():
