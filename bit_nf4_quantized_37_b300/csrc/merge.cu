@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(THREADS, 3) nf4_merge_persistent(
     const float* __restrict__ steps, const float* __restrict__ mean,
     int dq, int fp8, const uint16_t* __restrict__ A, const uint16_t* __restrict__ B, int64_t N,
     int64_t K, int r, float scale, uint16_t* __restrict__ out16, float* __restrict__ out32,
-    int64_t ntiles, int64_t kblocks) {
+    int ntr, int kbl) {
   constexpr int BP = R16 + 8;
   constexpr int APT = R16 * (COLS / 8) / THREADS;  // A pieces per thread (1 or 2)
   constexpr int BPR = R16 / 8;                     // B pieces per staged row
@@ -339,53 +339,62 @@ __global__ void __launch_bounds__(THREADS, 3) nf4_merge_persistent(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rr = tid >> 2, b = (tid >> 1) & 1, h = tid & 1;
   const float mu = dq ? __ldg(mean) : 0.0f;
+  // per-thread pieces of the A / B slices: A row j = tid / 16 + 16 u, columns 8 (tid % 16) ..;
+  // B row tid / BPR, ranks 8 (tid % BPR) ..
+  const int a_j = tid / (COLS / 8), a_c = tid % (COLS / 8);
+  const int b_r = tid / BPR, b_j = tid % BPR;
+  const bool b_on = tid < ROWS * BPR && 8 * b_j < r;
   uint4 av[APT], bv;
   RowCodes rc;
-  auto load = [&](int64_t t, uint4 (&a)[APT], uint4& bb, RowCodes& c) {
-    const int64_t n0 = (t / kblocks) * ROWS, k0 = (t % kblocks) * COLS;
+  // tile (tr, tc): rows 64 tr .., columns 128 tc ..
+  auto load = [&](int tr, int tc, uint4 (&a)[APT], uint4& bb, RowCodes& c) {
+    const int64_t n0 = static_cast<int64_t>(tr) * ROWS, k0 = static_cast<int64_t>(tc) * COLS;
+    const int64_t k = k0 + 8 * a_c;
 #pragma unroll
     for (int u = 0; u < APT; ++u) {
-      const int i = tid + u * THREADS, j = i / (COLS / 8), ch = i % (COLS / 8);
-      const int64_t k = k0 + 8 * ch;
+      const int j = a_j + u * (THREADS / (COLS / 8));
       a[u] = make_uint4(0, 0, 0, 0);
       if (j < r && k < K) a[u] = __ldg(reinterpret_cast<const uint4*>(A + j * K + k));
     }
     bb = make_uint4(0, 0, 0, 0);
-    if (tid < ROWS * BPR) {
-      const int sr = tid / BPR, j8 = tid % BPR;
-      const int64_t n = n0 + sr;
-      if (n < N && 8 * j8 < r) bb = __ldg(reinterpret_cast<const uint4*>(B + n * r + 8 * j8));
-    }
+    if (b_on && n0 + b_r < N)
+      bb = __ldg(reinterpret_cast<const uint4*>(B + (n0 + b_r) * r + 8 * b_j));
     merge_row_load(c, codes, qs, steps, dq, N, K, n0 + rr, k0 + 64 * b, h);
   };
   auto stage = [&](const uint4 (&a)[APT], const uint4& bb) {
 #pragma unroll
-    for (int u = 0; u < APT; ++u) {
-      const int i = tid + u * THREADS, j = i / (COLS / 8), ch = i % (COLS / 8);
-      *reinterpret_cast<uint4*>(sA + j * A_PITCH + 8 * ch) = a[u];
-    }
-    if (tid < ROWS * BPR)
-      *reinterpret_cast<uint4*>(sB + (tid / BPR) * BP + 8 * (tid % BPR)) = bb;
+    for (int u = 0; u < APT; ++u)
+      *reinterpret_cast<uint4*>(sA + (a_j + u * (THREADS / (COLS / 8))) * A_PITCH + 8 * a_c) = a[u];
+    if (tid < ROWS * BPR) *reinterpret_cast<uint4*>(sB + b_r * BP + 8 * b_j) = bb;
   };
-  int64_t t = blockIdx.x;
-  if (t >= ntiles) return;
-  load(t, av, bv, rc);
+  // the CTA's tiles t, t + grid, ... (of ntr x kbl) as (row tile, column tile), advanced
+  // without division
+  const int step_r = static_cast<int>(gridDim.x) / kbl, step_c = static_cast<int>(gridDim.x) % kbl;
+  int tr = static_cast<int>(blockIdx.x) / kbl, tc = static_cast<int>(blockIdx.x) % kbl;
+  if (tr >= ntr) return;
+  load(tr, tc, av, bv, rc);
   stage(av, bv);
   __syncthreads();
-  for (; t < ntiles; t += gridDim.x) {
-    const int64_t tn = t + gridDim.x;
+  while (true) {
+    int nr = tr + step_r, nc = tc + step_c;
+    if (nc >= kbl) {
+      nc -= kbl;
+      ++nr;
+    }
+    const bool more = nr < ntr;
     RowCodes nrc;
-    if (tn < ntiles) load(tn, av, bv, nrc);  // in flight during this tile's work
+    if (more) load(nr, nc, av, bv, nrc);  // in flight during this tile's work
     merge_tile_mma<true>(sA, sB, sD, R16, BP, warp, lane);
     __syncthreads();
-    const int64_t n0 = (t / kblocks) * ROWS, k0 = (t % kblocks) * COLS;
+    const int64_t n0 = static_cast<int64_t>(tr) * ROWS, k0 = static_cast<int64_t>(tc) * COLS;
     merge_row_epilogue(rc, sD, mu, dq, fp8, scale, N, K, n0 + rr, k0 + 64 * b, rr, b, h, out16,
                        out32);
+    if (!more) break;
     __syncthreads();  // every read of sA / sB / sD is done
-    if (tn < ntiles) {
-      stage(av, bv);
-      rc = nrc;
-    }
+    stage(av, bv);
+    rc = nrc;
+    tr = nr;
+    tc = nc;
     __syncthreads();
   }
 }
@@ -491,14 +500,16 @@ static int launch_merge_persistent(const nf4_tensor& q, const uint16_t* A, const
   const int st = merge_resident<R16>(&per_sm);
   if (st) return st;
   const int64_t kblocks = (q.cols + merge::COLS - 1) / merge::COLS;
-  const int64_t ntiles = kblocks * ((q.rows + merge::ROWS - 1) / merge::ROWS);
+  const int64_t rblocks = (q.rows + merge::ROWS - 1) / merge::ROWS;
+  const int64_t ntiles = kblocks * rblocks;
+  if (ntiles > INT32_MAX) return QLORA_ERR_UNSUPPORTED;
   const int64_t grid = std::min<int64_t>(ntiles, (int64_t)per_sm * num_sms());
   const int smem = merge::ROWS * merge::COLS * 4;  // the fp32 tile (32 KB)
   ProfileScope ps("nf4_merge", stream);
   merge::nf4_merge_persistent<R16><<<(unsigned)grid, merge::THREADS, smem, stream>>>(
       q.codes, q.scale_codes, q.scale_steps, q.scale_mean, q.dq_block != 0 ? 1 : 0,
-      q.dq_type == NF4_DQ_FP8 ? 1 : 0, A, B, q.rows, q.cols, r, scale, out16, out32, ntiles,
-      kblocks);
+      q.dq_type == NF4_DQ_FP8 ? 1 : 0, A, B, q.rows, q.cols, r, scale, out16, out32,
+      static_cast<int>(rblocks), static_cast<int>(kblocks));
   return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
 }
 
