@@ -242,6 +242,14 @@ __device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* src, ui
       : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16); no
+// completion to wait for.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // 2-D tiled load whose completion is signalled on an mbarrier given as a shared::cluster
 // address (the leader CTA's barrier in a CTA pair).
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap,

@@ -8,7 +8,7 @@
 //                      with an IEEE division, see below), 4-bit packing; writes the codes, the
 //                      absmax values and, per run of 8 blocks, the fp64 pairwise sum of their
 //                      absmax (a warp's perfect 8-leaf subtree, by shuffles).
-//   nf4_absmax_mean    up to 32 CTAs: aligned subtrees of the pairwise sum over those
+//   nf4_absmax_mean    up to 128 CTAs: aligned subtrees of the pairwise sum over those
 //                      8-block sums.
 //   nf4_double_quant   a warp per group: mean (fp32) from the subtree sums, then
 //                      step = max|a - mean| / 127, int8 codes.
@@ -109,7 +109,7 @@ __device__ __forceinline__ uint32_t code_fast(float y, uint32_t tab_b, float& dm
 
 __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
     const float* __restrict__ W, int64_t numel, uint8_t* __restrict__ codes,
-    float* __restrict__ absmax, double* __restrict__ sum8) {
+    float* __restrict__ absmax, double* __restrict__ sum8, int* ticket) {
   __shared__ float s_abs[kUnit];  // the partial last unit's absmax values
   extern __shared__ float2 s_cells[];  // 2 * kCells * kCopies entries
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
   const int64_t nunits = (nblocks + kUnit - 1) / kUnit;
   const int64_t nfull = numel / kUnitElems;  // units with all 4096 weights present
   launch_dependents();  // pass 2 may be scheduled meanwhile (it waits for this grid)
+  if (ticket && blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;  // pass 2's arrival count
   build_cells(s_cells);
   __syncthreads();
   const uint32_t tab_b = smem_u32(s_cells) + static_cast<uint32_t>(lane) * 8u - kCellBias * kEntryBytes;
@@ -129,6 +130,9 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
   };
   float4 nxt[4];
   if (blockIdx.x < nfull) load16(blockIdx.x, nxt);
+  // the unit after is pulled into L2 ahead of its register loads (one bulk prefetch per unit)
+  if (threadIdx.x == 0 && blockIdx.x + gridDim.x < nfull)
+    prefetch_l2_bulk(W + (blockIdx.x + gridDim.x) * kUnitElems, kUnitElems * 4);
 
 #pragma unroll 1
   for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
@@ -140,8 +144,10 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
       for (int v = 0; v < 4; ++v) {
         w[4 * v + 0] = nxt[v].x; w[4 * v + 1] = nxt[v].y; w[4 * v + 2] = nxt[v].z; w[4 * v + 3] = nxt[v].w;
       }
-      // the next unit's loads in flight during this one
+      // the next unit's loads in flight during this one, the one after that on its way to L2
       if (u + gridDim.x < nfull) load16(u + gridDim.x, nxt);
+      if (threadIdx.x == 0 && u + 2 * gridDim.x < nfull)
+        prefetch_l2_bulk(W + (u + 2 * gridDim.x) * kUnitElems, kUnitElems * 4);
       float m = fabsf(w[0]);
 #pragma unroll
       for (int i = 1; i < 16; ++i) m = fmaxf(m, fabsf(w[i]));
@@ -216,7 +222,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4) nf4_quant_blocks(
 
 // -------------------------------------------------------------------- pass 2
 // The pairwise tree over the 8-block sums, zero-padded to a power of two P, is cut into
-// nparts <= 32 aligned subtrees of P / nparts leaves, one CTA of 1024 threads each; pass 3
+// nparts <= 128 aligned subtrees of P / nparts leaves, one CTA of 1024 threads each; pass 3
 // combines the subtree sums (the top levels of the same tree) and forms
 // mean = (float)(total / nblocks).  Each thread folds a run of kRun consecutive leaves (a
 // power of two) with a register tree -- exactly the pairwise tree of the run -- and the runs
@@ -235,8 +241,10 @@ __device__ __forceinline__ double fold_run(const double* __restrict__ leaf, int6
 
 __global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict__ leaf_sum,
                                                         int64_t nleaves, int64_t run,
-                                                        double* __restrict__ part) {
+                                                        double* __restrict__ part, int* ticket,
+                                                        int64_t nblocks, float* __restrict__ mean) {
   __shared__ double s_warp[32];
+  __shared__ int s_last;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   launch_dependents();     // pass 3 may be scheduled meanwhile (it waits for this grid)
   grid_dependency_wait();  // the 8-block sums of pass 1
@@ -271,25 +279,47 @@ __global__ void __launch_bounds__(1024) nf4_absmax_mean(const double* __restrict
     double w = s_warp[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-    if (lane == 0) part[blockIdx.x] = w;
+    if (lane == 0) {
+      part[blockIdx.x] = w;
+      __threadfence();
+      s_last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1;
+    }
+  }
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  // the last CTA: the top levels of the tree over the nparts subtree sums -- a lane folds
+  // nparts / 32 consecutive sums (past 32 parts), then a butterfly over the lanes holding
+  // one -- and mean = (float)(total / nblocks); the ticket is left at zero for the next call
+  __threadfence();
+  const int nparts = static_cast<int>(gridDim.x);
+  double v = 0.0;
+  if (nparts <= 32) {
+    if (lane < nparts) v = __ldcg(part + lane);
+  } else if (nparts == 64) {
+    v = __ldcg(part + 2 * lane) + __ldcg(part + 2 * lane + 1);
+  } else {  // 128
+    v = (__ldcg(part + 4 * lane) + __ldcg(part + 4 * lane + 1)) +
+        (__ldcg(part + 4 * lane + 2) + __ldcg(part + 4 * lane + 3));
+  }
+  const int lanes = nparts < 32 ? nparts : 32;
+  for (int o = 1; o < lanes; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) {
+    mean[0] = (float)(v / (double)nblocks);
+    *ticket = 0;
   }
 }
 
 // -------------------------------------------------------------------- pass 3
-// A warp per group of 256 blocks (8 per lane), 8 groups per CTA.  Every CTA first combines
-// the nparts subtree sums of pass 2 (a butterfly over lanes < nparts: the top levels of the
-// pairwise tree) into the mean; CTA 0 stores it.
+// A warp per group of 256 blocks (8 per lane), 8 groups per CTA, with the mean that pass 2
+// stored.
 __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict__ absmax,
                                                         int64_t nblocks, int64_t ngroups,
-                                                        const double* __restrict__ part,
-                                                        int nparts, float* __restrict__ mean,
-                                                        int fp8, int8_t* __restrict__ scale_codes,
+                                                        const float* mean, int fp8,
+                                                        int8_t* __restrict__ scale_codes,
                                                         float* __restrict__ steps) {
-  __shared__ float s_mu;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t g = (int64_t)blockIdx.x * 8 + warp;
-  grid_dependency_wait();  // the subtree sums of pass 2 (and with them the absmax of pass 1)
-  // the group's absmax values first, so their loads overlap the mean's fp64 arithmetic
+  grid_dependency_wait();  // the mean of pass 2 (and with it the absmax of pass 1)
   const int64_t b0 = g * kGroup + lane * 8;
   const bool whole = b0 + 8 <= nblocks;
   float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -305,18 +335,8 @@ __global__ void __launch_bounds__(256) nf4_double_quant(const float* __restrict_
         if (b0 + i < nblocks) a[i] = absmax[b0 + i];
     }
   }
-  if (warp == 0) {
-    double v = lane < nparts ? part[lane] : 0.0;
-    for (int o = 1; o < nparts; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) {
-      const float mu = (float)(v / (double)nblocks);
-      s_mu = mu;
-      if (blockIdx.x == 0) mean[0] = mu;
-    }
-  }
-  __syncthreads();
   if (g >= ngroups) return;
-  const float mu = s_mu;
+  const float mu = __ldcg(mean);
   float d[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) d[i] = (whole || b0 + i < nblocks) ? __fsub_rn(a[i], mu) : 0.0f;
@@ -414,12 +434,14 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
 }
 
 // -------------------------------------------------------------------- launchers
+constexpr int kMeanParts = 128;  // most CTAs of pass 2 (a power of two)
+
 uint64_t quantize_workspace_bytes(int64_t numel) {
   const int64_t nb = (numel + kBlock - 1) / kBlock;
   const int64_t ng = (nb + kGroup - 1) / kGroup;
   // absmax fp32 [ngroups * 256] (padded to whole groups), 8-block sums fp64 [<= 32 ngroups],
-  // then the mean's subtree sums fp64 [<= 32] in the 256-byte tail
-  return (uint64_t)ng * kGroup * 4 + (uint64_t)ng * (kGroup / 8) * 8 + 256;
+  // then the mean's subtree sums fp64 [<= kMeanParts] and the arrival ticket of pass 2
+  return (uint64_t)ng * kGroup * 4 + (uint64_t)ng * (kGroup / 8) * 8 + kMeanParts * 8 + 16;
 }
 
 int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws,
@@ -432,6 +454,8 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
   const int64_t nu = (nb + kUnit - 1) / kUnit;
   const int64_t nleaves = nu * (kUnit / 8);  // 8-block sums
   double* usum = reinterpret_cast<double*>(reinterpret_cast<char*>(ws) + ng * kGroup * 4);
+  double* part = usum + ng * (kGroup / 8);
+  int* ticket = reinterpret_cast<int*>(part + kMeanParts);  // zeroed by pass 1
   {
     ProfileScope ps("nf4_quant_blocks", stream);
     // persistent: as many CTAs as are resident at once, or fewer units
@@ -451,13 +475,14 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     if (st) return st == -1 ? QLORA_ERR_NO_DEVICE : st;
     const int64_t resident = (int64_t)per_sm * num_sms();
     const int64_t ctas = nu < resident ? nu : resident;
-    nf4_quant_blocks<<<(unsigned)ctas, kQuantThreads, kCellBytes, stream>>>(W, numel, q.codes, absmax, usum);
+    nf4_quant_blocks<<<(unsigned)ctas, kQuantThreads, kCellBytes, stream>>>(
+        W, numel, q.codes, absmax, usum, dq ? ticket : nullptr);
   }
   if (!dq) return cudaGetLastError() == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA;
-  double* part = usum + ng * (kGroup / 8);
   int64_t p2 = 1;
   while (p2 < nleaves) p2 *= 2;
-  const int nparts = p2 > 1024 ? static_cast<int>(p2 / 1024 < 32 ? p2 / 1024 : 32) : 1;
+  const int nparts =
+      p2 > 1024 ? static_cast<int>(p2 / 1024 < kMeanParts ? p2 / 1024 : kMeanParts) : 1;
   const int64_t run = p2 > 1024 * nparts ? p2 / (1024 * nparts) : 1;
   // passes 2 and 3 are programmatic dependents: launched while the pass before finishes,
   // they wait for it (griddepcontrol.wait) before reading its output
@@ -473,7 +498,7 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     cfg.gridDim = dim3(nparts);
     cfg.blockDim = dim3(1024);
     if (cudaLaunchKernelEx(&cfg, nf4_absmax_mean, static_cast<const double*>(usum), nleaves, run,
-                           part) != cudaSuccess)
+                           part, ticket, nb, q.scale_mean) != cudaSuccess)
       return QLORA_ERR_CUDA;
   }
   {
@@ -481,7 +506,7 @@ int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws
     cfg.gridDim = dim3((unsigned)((ng + 7) / 8));
     cfg.blockDim = dim3(256);
     if (cudaLaunchKernelEx(&cfg, nf4_double_quant, static_cast<const float*>(absmax), nb, ng,
-                           static_cast<const double*>(part), nparts, q.scale_mean,
+                           static_cast<const float*>(q.scale_mean),
                            q.dq_type == NF4_DQ_FP8 ? 1 : 0, q.scale_codes, q.scale_steps) != cudaSuccess)
       return QLORA_ERR_CUDA;
   }

@@ -94,6 +94,13 @@ def test_quantize_decode_tensor_bit_exact():
     _quant_parity(wl.config4(1).W())
 
 
+@pytest.mark.parametrize("rows", [2048, 5000, 9000])
+def test_quantize_mean_partitions(rows):
+    """The mean's pairwise tree cut into 16, 64 and 128 subtree sums (8.4 M, 20.5 M and
+    36.9 M weights), the last of which the final CTA of that pass combines."""
+    _quant_parity(wl.weight((rows, 4096), seed=rows, sigma=0.02, outlier_frac=0.001))
+
+
 @pytest.mark.parametrize("rows,cols", [(1, 1), (1, 17), (3, 333), (256, 256), (64, 64 * 256 + 64),
                                        (4096, 4096)])
 def test_dequantize_bit_exact(rows, cols):
