@@ -203,6 +203,8 @@ def test_fwd_bwd_small(name, M, N, K, r, alpha):
                                      (2100, 256, 4864, 16),    # input gradient, the same
                                      (512, 3072, 3072, 16),    # 128-row tiles, 3-way split contraction
                                      (400, 3072, 2560, 24),    # the same, rows past M in the tile
+                                     (700, 768, 640, 16),      # staged base, six row tiles, ragged
+                                     (384, 640, 576, 24),      # staged base, three row tiles
                                      (1024, 4864, 512, 128),   # narrow U at rank 128 (unswizzled rows)
                                      (1024, 512, 4864, 128)])  # narrow V at rank 128
 def test_pair_tiles_every_output(M, N, K, r):
