@@ -384,6 +384,17 @@ __global__ void __launch_bounds__(THREADS, 3) nf4_merge_persistent(
     const bool more = nr < ntr;
     RowCodes nrc;
     if (more) load(nr, nc, av, bv, nrc);  // in flight during this tile's work
+    {
+      // the codes of the tile after that on their way to L2, so its register loads hit there
+      int pr = nr + step_r, pc = nc + step_c;
+      if (pc >= kbl) {
+        pc -= kbl;
+        ++pr;
+      }
+      const int64_t pn = static_cast<int64_t>(pr) * ROWS + rr, pk = static_cast<int64_t>(pc) * COLS + 64 * b;
+      if (h == 0 && pr < ntr && pn < N && pk < K)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(codes + ((pn * K + pk) >> 1)));
+    }
     merge_tile_mma<true>(sA, sB, sD, R16, BP, warp, lane);
     __syncthreads();
     const int64_t n0 = static_cast<int64_t>(tr) * ROWS, k0 = static_cast<int64_t>(tc) * COLS;
