@@ -390,28 +390,55 @@ def main():
     dXp = torch.empty(p.M, p.K, dtype=torch.bfloat16).pin_memory()
     dAp = torch.empty(p.r, p.K, dtype=torch.float32).pin_memory()
     dBp = torch.empty(p.N, p.r, dtype=torch.float32).pin_memory()
-    Xd = torch.empty_like(X)
-    dYd = torch.empty_like(dY)
+    # Steps are pipelined the way a caller streaming batches would run them: step i + 1's
+    # inputs go up on one copy stream and step i's results come down on another while step i
+    # computes on the current stream (the two directions of the host link run at once). The
+    # device inputs are double-buffered; events order every reuse of a buffer.
+    Xd = [torch.empty_like(X) for _ in range(2)]
+    dYd = [torch.empty_like(dY) for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        Xd.copy_(Xp, non_blocking=True)
-        dYd.copy_(dYp, non_blocking=True)
-        Y, U = qn.qlora_linear_fwd(Xd, q, A, B, s)
-        dX, dA, dB = qn.qlora_linear_bwd(dYd, Xd, q, A, B, s, U)
-        Yp.copy_(Y, non_blocking=True)
-        dXp.copy_(dX, non_blocking=True)
-        dAp.copy_(dA, non_blocking=True)
-        dBp.copy_(dB, non_blocking=True)
+    def upload(i):
+        b = i & 1
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(in_free[b])  # step i - 2 has finished with this buffer
+            Xd[b].copy_(Xp, non_blocking=True)
+            dYd[b].copy_(dYp, non_blocking=True)
+            in_ready[b].record(up)
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_steps(n, start):
+        up.wait_event(start)
+        upload(0)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                upload(i + 1)
+            comp.wait_event(in_ready[b])
+            Y, U = qn.qlora_linear_fwd(Xd[b], q, A, B, s)
+            dX, dA, dB = qn.qlora_linear_bwd(dYd[b], Xd[b], q, A, B, s, U)
+            in_free[b].record(comp)
+            done[b].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(done[b])
+                for host, dev_t in ((Yp, Y), (dXp, dX), (dAp, dA), (dBp, dB)):
+                    host.copy_(dev_t, non_blocking=True)
+                    dev_t.record_stream(down)  # not reused before its copy has run
+        comp.wait_stream(down)
+
+    w0 = torch.cuda.Event()
+    w0.record(comp)
+    e2e_steps(3, w0)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record()
+    e0.record(comp)
+    e2e_steps(args.steps, e0)
+    e1.record(comp)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_val = flops_step * args.steps * world / (e2e_ms / 1e3) / 1e12
