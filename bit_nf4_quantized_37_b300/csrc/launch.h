@@ -47,6 +47,11 @@ int read_and_clear_selftest_error(int* out);
 int launch_wait_selftest(cudaStream_t stream);
 
 // Quantize / dequantize (nf4_codec.cu).
+// The quantize workspace: absmax fp32 for whole groups of 256 blocks, one fp64 sum per 8
+// blocks, then a tail of kQuantizeMeanParts fp64 subtree sums of the mean and the arrival
+// ticket of the pass that combines them.
+constexpr int kQuantizeMeanParts = 128;  // a power of two
+constexpr uint64_t kQuantizeTailBytes = kQuantizeMeanParts * 8 + 16;
 uint64_t quantize_workspace_bytes(int64_t numel);
 int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws,
                     cudaStream_t stream);

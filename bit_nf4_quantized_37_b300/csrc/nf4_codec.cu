@@ -434,14 +434,14 @@ __global__ void __launch_bounds__(256) nf4_dequant_kernel(const uint8_t* __restr
 }
 
 // -------------------------------------------------------------------- launchers
-constexpr int kMeanParts = 128;  // most CTAs of pass 2 (a power of two)
+constexpr int kMeanParts = kQuantizeMeanParts;  // most CTAs of pass 2
 
 uint64_t quantize_workspace_bytes(int64_t numel) {
   const int64_t nb = (numel + kBlock - 1) / kBlock;
   const int64_t ng = (nb + kGroup - 1) / kGroup;
   // absmax fp32 [ngroups * 256] (padded to whole groups), 8-block sums fp64 [<= 32 ngroups],
   // then the mean's subtree sums fp64 [<= kMeanParts] and the arrival ticket of pass 2
-  return (uint64_t)ng * kGroup * 4 + (uint64_t)ng * (kGroup / 8) * 8 + kMeanParts * 8 + 16;
+  return (uint64_t)ng * kGroup * 4 + (uint64_t)ng * (kGroup / 8) * 8 + kQuantizeTailBytes;
 }
 
 int launch_quantize(const float* W, int64_t numel, const nf4_tensor& q, void* ws,

@@ -24,10 +24,10 @@ namespace qlora {
 namespace {
 
 constexpr int64_t kNoallocMaxNumel = NF4_NOALLOC_MAX_NUMEL;
-// absmax fp32 for whole groups of 256 blocks, one fp64 sum per 8 blocks, 256 bytes of
-// slack: the same layout the workspace of nf4_quantize uses
+// absmax fp32 for whole groups of 256 blocks, one fp64 sum per 8 blocks, then the mean's
+// tail: the layout of nf4_quantize's workspace, for the largest tensor
 constexpr uint64_t kNoallocScratchBytes =
-    ((kNoallocMaxNumel + 64 * 256 - 1) / (64 * 256)) * (256 * 4 + 32 * 8) + 256;
+    ((kNoallocMaxNumel + 64 * 256 - 1) / (64 * 256)) * (256 * 4 + 32 * 8) + kQuantizeTailBytes;
 
 __device__ __align__(256) unsigned char g_noalloc_quant_scratch[kNoallocScratchBytes];
 

@@ -59,6 +59,23 @@ def test_noalloc_matches_workspace_quantize_on_two_calls_in_a_row():
         _same(got, want)
 
 
+def test_noalloc_at_its_largest_size():
+    """Exactly NF4_NOALLOC_MAX_NUMEL weights (8192 x 8192): the whole scratch, the mean's
+    tail included, is in use; bit-exact with the oracle."""
+    import oracle
+    rows, cols = 8192, 8192
+    assert rows * cols == _binding.NF4_NOALLOC_MAX_NUMEL
+    Wh = wl.weight((rows, cols), seed=917, sigma=0.02, outlier_frac=0.001)
+    W = torch.from_numpy(Wh).cuda()
+    got = _via_c_abi(W, rows, cols)
+    torch.cuda.synchronize()
+    o = oracle.quantize(Wh)
+    assert np.array_equal(got.codes.cpu().numpy(), o["codes"])
+    assert np.array_equal(got.scale_codes.cpu().numpy(), o["qscale"])
+    assert np.array_equal(got.scale_steps.cpu().numpy().view(np.uint32), o["steps"].view(np.uint32))
+    assert got.scale_mean.cpu().numpy()[0].view(np.uint32) == np.float32(o["mean"]).view(np.uint32)
+
+
 def test_noalloc_rejects_tensors_beyond_its_scratch():
     rows, cols = 8193, 8192  # one row past NF4_NOALLOC_MAX_NUMEL
     assert rows * cols > _binding.NF4_NOALLOC_MAX_NUMEL
