@@ -14,6 +14,7 @@
 // split partial sums in split order and writes the outputs -- so results are
 // bit-reproducible and no separate reduction launch is needed.
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "launch.h"
@@ -703,6 +704,13 @@ Split pick_split(int64_t R, int64_t C, int NJ) {
   sp.row_tiles = (unsigned)((R + side::TR - 1) / side::TR);
   const int64_t c_tiles = (C + side::TC - 1) / side::TC;
   int64_t want = 2LL * num_sms() / (int64_t)sp.row_tiles;  // two CTAs per SM
+  // With few row tiles that would cut the contraction into many short chunks, and the last
+  // CTA of a row tile reads every split's TR x NJ fp32 partial tile alone.  A CTA reads
+  // TR * 2 bytes per contraction column and the final sum TR * NJ * 4 per split: the two
+  // balance at S = sqrt(C / (2 NJ)), the most splits taken (at M = 512 on the 4096^2 layer:
+  // 11 instead of 64 for U; twice the balance point measured 3 us slower per step).
+  const int64_t bal = static_cast<int64_t>(std::sqrt(static_cast<double>(C) / (2.0 * NJ)));
+  if (want > bal) want = bal;
   if (want < 1) want = 1;
   if (want > c_tiles) want = c_tiles;
   int64_t per = (c_tiles + want - 1) / want;
