@@ -96,6 +96,9 @@ struct Params {
   // staged base (single-CTA kernel): W' was dequantized into the workspace by the kernel
   // before this one; every NF4 stage takes its W tile by TMA (map tmW) like a LoRA stage
   int wstage;
+  // single-CTA kernel, two splits: the splits of a tile form a cluster and exchange halves
+  // of their accumulators in shared memory instead of going through part / tickets
+  int csplit;
   // persistent CTA pairs: pers_clusters clusters share the 512 x 256 tiles; the cluster whose
   // leader draws ticket k from *pers_ctr (zero at launch) takes tiles k, k + G, k + 2G, ...;
   // its 16-bit output goes straight from registers to out (row pitch ld_out elements)
@@ -237,18 +240,35 @@ __device__ __forceinline__ void split_sum(const Params& p, int split, int64_t my
 // gcol0 + 32 c.  Each chunk goes through a 2 KB buffer of its own (64-byte swizzle; the ring's
 // shared memory is idle once the accumulator is complete) and one TMA store, so no store
 // waits for an earlier one to release its buffer.
+// recv (split clusters): the other split's values of this CTA's 128 columns, [128 rows] x
+// [32 16-byte pieces] fp32, piece q of row rr at q ^ (rr & 7); the sum is split 0's value plus
+// split 1's, as split_sum forms it.
 template <bool H>
 __device__ __forceinline__ void epilogue_store(const Params& p, const CUtensorMap* tmOut,
                                                uint32_t taddr, int tcol0, int64_t gcol0,
                                                int64_t row0, int64_t my_row, int split,
-                                               int nchunk, uint8_t* buf0, int lane) {
+                                               int nchunk, uint8_t* buf0, int lane,
+                                               const uint8_t* recv = nullptr, int rr = 0) {
 #pragma unroll 1
   for (int c = 0; c < nchunk; ++c) {
     const int64_t col = gcol0 + c * 32;
     uint32_t v[32];
     tmem_ld_32x32b_x32(taddr + tcol0 + c * 32, v);
     tmem_ld_wait();
-    split_sum(p, split, my_row, col, v);
+    if (recv) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 o = *reinterpret_cast<const float4*>(recv + rr * 512 + (((c * 8 + j) ^ (rr & 7)) << 4));
+        const float ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float mine = __uint_as_float(v[4 * j + e]);
+          v[4 * j + e] = __float_as_uint(split == 0 ? mine + ov[e] : ov[e] + mine);
+        }
+      }
+    } else {
+      split_sum(p, split, my_row, col, v);
+    }
     uint8_t* buf = buf0 + c * 2048;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -288,6 +308,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ __align__(8) uint64_t bready_bar[SB];
   __shared__ __align__(8) uint64_t b_empty[SB];
   __shared__ __align__(8) uint64_t acc_bar;
+  __shared__ __align__(8) uint64_t peer_free, peer_data;  // split clusters (see csplit)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -304,6 +325,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const bool last_split = split == p.nsplit - 1;
   const int total = (last_split ? p.n_lora : 0) + n_main;
   volatile int* abort_p = &abort_flag;
+  // the two splits of a tile as a cluster (rank = split): each finishes 128 of the 256 columns
+  const bool cx = kAcc == 1 && p.csplit != 0 && p.nsplit == 2;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SA; ++i) {
@@ -315,12 +338,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&b_empty[i], 1);
     }
     mbar_init(&acc_bar, 1);
+    mbar_init(&peer_free, 1);  // the peer: its B ring may take this CTA's half
+    mbar_init(&peer_data, 4);  // the peer's four sending warps: their half has arrived
     abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc<1>(&tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
+  if (cx) cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
@@ -501,16 +527,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t my_row = row0 + lane;
       uint8_t* buf0 = smem + (warp - DEQ_WARP0) * (NCHUNK * 2048);
       const uint32_t taddr = tbase + (static_cast<uint32_t>(lg * 32) << 16);
-      const bool store = split_epilogue_partial(p, split, taddr, my_row, n0 + col0, NCHUNK, col0,
-                                                warp == DEQ_WARP0 && lane == 0,
-                                                static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), s_last);
-      if (store)
-        epilogue_store<H>(p, &tmOut, taddr, col0, n0 + col0, row0, my_row, split, NCHUNK, buf0, lane);
+      if (cx) {
+        // This CTA's B ring is idle now (every stage consumed): the peer may write its half
+        // there.  The warps of the column half the peer owns send their values to the peer's
+        // ring (fp32, piece q of row rr at q ^ (rr & 7)); the others wait for the peer's half
+        // and store the sums of their 128 columns.
+        const uint32_t peer = static_cast<uint32_t>(split ^ 1);
+        uint8_t* recv = smem + B_BASE;
+        const int rr = lg * 32 + lane;
+        if (warp == DEQ_WARP0 && lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&peer_free), peer));
+        if (half != split) {
+          if (mbar_wait<true>(&peer_free, 0, kWaitPeer, abort_p, &g_gemm_error)) {
+            const uint32_t rbase = mapa_shared(smem_u32(recv), peer) + static_cast<uint32_t>(rr * 512);
+#pragma unroll 1
+            for (int c = 0; c < NCHUNK; ++c) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(taddr + col0 + c * 32, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 rbase + static_cast<uint32_t>(((c * 8 + j) ^ (rr & 7)) << 4)),
+                             "r"(v[4 * j]), "r"(v[4 * j + 1]), "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
+                             : "memory");
+            }
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");  // this lane's stores, cluster-wide
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&peer_data), peer));
+          }
+        } else if (mbar_wait<true>(&peer_data, 0, kWaitPeer, abort_p, &g_gemm_error)) {
+          epilogue_store<H>(p, &tmOut, taddr, col0, n0 + col0, row0, my_row, split, NCHUNK, buf0,
+                            lane, recv, rr);
+        }
+      } else {
+        const bool store = split_epilogue_partial(p, split, taddr, my_row, n0 + col0, NCHUNK, col0,
+                                                  warp == DEQ_WARP0 && lane == 0,
+                                                  static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x), s_last);
+        if (store)
+          epilogue_store<H>(p, &tmOut, taddr, col0, n0 + col0, row0, my_row, split, NCHUNK, buf0, lane);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a split cluster leaves while the other may still write into it
+  if (cx) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<1>(tmem, TMEM_COLS);
@@ -1257,6 +1319,8 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, const FusedPlan&
   p.lora_last_k16 = static_cast<int>((a.r - 64 * (p.n_lora - 1) + 15) / 16);
   p.nsplit = plan.nsplit;
   p.split_stages = plan.split_stages;
+  // single-CTA tiles with two splits: the splits of a tile are a cluster (grid z)
+  p.csplit = !kPair && kAcc == 1 && plan.nsplit == 2 ? 1 : 0;
   if (plan.nsplit > 1 &&  // the workspace layout must have made room for the split tiles
       (L.gpart_bytes < (uint64_t)plan.nsplit * a.M * p.Nout * 4 || L.ngtickets < (uint64_t)plan.tiles))
     return QLORA_ERR_WORKSPACE;
@@ -1299,13 +1363,20 @@ int launch_fused(const LinearArgs& a, const WorkspaceLayout& L, const FusedPlan&
   // programmatic dependent launch: the GEMM may start while the kernel before it (the
   // rank-r product it reads in its last stages) finishes; its TMA thread waits for that
   // kernel before the first LoRA-stage load
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributePriority;
   attr[1].val.priority = a.gemm_priority;
   cfg.attrs = attr;
   cfg.numAttrs = a.gemm_priority ? 2 : 1;
+  if (p.csplit) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = 1;
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 2;
+    ++cfg.numAttrs;
+  }
   cudaError_t e;
   // (the persistent kernel stages each epilogue in the B slots of the next tile's NF4 stages
   // 4 and 5, so it needs at least 6 NF4 stages)

@@ -205,6 +205,8 @@ def test_fwd_bwd_small(name, M, N, K, r, alpha):
                                      (400, 3072, 2560, 24),    # the same, rows past M in the tile
                                      (700, 768, 640, 16),      # staged base, six row tiles, ragged
                                      (384, 640, 576, 24),      # staged base, three row tiles
+                                     (512, 4096, 4096, 16),    # two splits as a cluster, both ways
+                                     (300, 2048, 1024, 16),    # the same with a ragged row tile
                                      (1024, 4864, 512, 128),   # narrow U at rank 128 (unswizzled rows)
                                      (1024, 512, 4864, 128)])  # narrow V at rank 128
 def test_pair_tiles_every_output(M, N, K, r):
