@@ -395,26 +395,23 @@ __global__ void __launch_bounds__(THREADS, 2)
       src[b] = reinterpret_cast<const float4*>(part + (live[b] ? row : r0) * NJ + (i % V4) * 4);
       v[b] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    int s = 0;
-    for (; s + SB <= S; s += SB) {
+    // batches of SB splits, the last one partial (its loads and adds predicated): one L2
+    // round trip per batch
+    for (int s = 0; s < S; s += SB) {
+      const int n = S - s < SB ? S - s : SB;
       float4 a[PB][SB];
 #pragma unroll
       for (int b = 0; b < PB; ++b)
 #pragma unroll
-        for (int u = 0; u < SB; ++u) a[b][u] = __ldcg(src[b] + (s + u) * sstride);
+        for (int u = 0; u < SB; ++u)
+          if (u < n) a[b][u] = __ldcg(src[b] + (s + u) * sstride);
 #pragma unroll
       for (int b = 0; b < PB; ++b)
 #pragma unroll
-        for (int u = 0; u < SB; ++u) {
-          v[b].x += a[b][u].x; v[b].y += a[b][u].y; v[b].z += a[b][u].z; v[b].w += a[b][u].w;
-        }
-    }
-    for (; s < S; ++s) {
-#pragma unroll
-      for (int b = 0; b < PB; ++b) {
-        const float4 a = __ldcg(src[b] + s * sstride);
-        v[b].x += a.x; v[b].y += a.y; v[b].z += a.z; v[b].w += a.w;
-      }
+        for (int u = 0; u < SB; ++u)
+          if (u < n) {
+            v[b].x += a[b][u].x; v[b].y += a[b][u].y; v[b].z += a[b][u].z; v[b].w += a[b][u].w;
+          }
     }
 #pragma unroll
     for (int b = 0; b < PB; ++b) {
