@@ -567,6 +567,30 @@ def test_merge_and_noalloc_nodq():
     assert torch.equal(q2.codes, q.codes) and torch.equal(q2.scale_steps, q.scale_steps)
 
 
+@pytest.mark.parametrize("variant", ["nodq", "fp8"])
+def test_merge_format_variants(variant):
+    """The merge's scale decoding in both format variants (fp32 absmax per block, E4M3 second
+    level), on the persistent form at rank 24 with a ragged row tile."""
+    N, K, r = 200, 1024, 24
+    W = wl.weight((N, K), seed=61, sigma=0.02, outlier_frac=0.001)
+    A = wl.bf16_normal((r, K), seed=62, sigma=0.01)
+    B = wl.bf16_normal((N, r), seed=63, sigma=0.01)
+    scale = 2.0
+    if variant == "nodq":
+        o = oracle.quantize(W)
+        q = qn.nf4_quantize(torch.from_numpy(W).cuda(), double_quant=False)
+        wd = oracle.dequantize_nodq(o)
+    else:
+        o = oracle.quantize(W, fp8=True)
+        q = qn.nf4_quantize(torch.from_numpy(W).cuda(), fp8_second_level=True)
+        wd = oracle.dequantize(o)
+    m16, m32 = qn.nf4_merge_lora(q, bf16_dev(A), bf16_dev(B), scale, f32=True)
+    got = bits_host(m16)
+    want = oracle.merge(wd.reshape(N, K), A, B, scale)
+    assert (_ulp_diff(got, want) > 0).mean() <= 1e-3
+    assert np.array_equal(m32.cpu().numpy(), wl.bf16_bits_to_f32(got))
+
+
 # ------------------------------------------------------------------ fp8 second level
 @pytest.mark.parametrize("n", [1, 65, 1001, 64 * 256 + 1, 64 * 300 + 37, 1 << 20])
 def test_quantize_fp8_second_level_bit_exact(n):
