@@ -416,7 +416,14 @@ constexpr int ES_THREADS = 256;
 __global__ void __launch_bounds__(ES_THREADS) nf4_int4_error_kernel(
     const float* __restrict__ W, int64_t numel, double* __restrict__ part) {
   __shared__ double s_red[ES_THREADS / 32][3];
-  constexpr float L[16] = QLORA_NF4_LEVELS;
+  // the levels in shared memory: a lane's level is one conflict-free load (16 words in 16
+  // banks), where a per-lane index into a constant array is not
+  __shared__ float s_L[16];
+  {
+    constexpr float L[16] = QLORA_NF4_LEVELS;
+    if (threadIdx.x < 16) s_L[threadIdx.x] = L[threadIdx.x];
+    __syncthreads();
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ql = lane & 3;  // quarter of a 64-block: 16 weights
   const int64_t nblocks = (numel + 63) / 64;
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(ES_THREADS) nf4_int4_error_kernel(
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float x = a > 0.0f ? __fdiv_rn(w[i], a) : 0.0f;
-      const float en = __fsub_rn(w[i], __fmul_rn(L[nf4_code(x)], a));
+      const float en = __fsub_rn(w[i], __fmul_rn(s_L[nf4_code(x)], a));
       const float q = fminf(fmaxf(rintf(__fmul_rn(7.0f, x)), -7.0f), 7.0f);
       const float ei = __fsub_rn(w[i], __fmul_rn(q, a7));
       s_w = __fmaf_rn(w[i], w[i], s_w);
