@@ -232,16 +232,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
       : "memory");
 }
 
-// 1-D bulk load of `bytes` (a multiple of 16; both addresses 16-byte aligned); completion is
-// signalled on `bar` (same CTA) as transaction bytes.
-__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* src, uint32_t bytes,
-                                             uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16); no
 // completion to wait for.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
